@@ -1,0 +1,277 @@
+"""Plain, slow, fp64 CPU oracle for Laplacian-kernel Nystrom attention.
+
+TEST INFRASTRUCTURE.  Only the tests, the smoke check and the benchmark's CPU
+baseline may import this module.  It shares no code with the CUDA library and
+imports nothing from it: it takes numpy arrays and returns numpy arrays.
+
+Sources (page title, then section / equation):
+  [LF-nl]  "LaplacianFormer: Rethinking Linear Attention with Laplacian Kernel",
+           Dutch summary, Methodology 1 (Laplacian kernel and injectivity) and
+           Methodology 2 (efficient computation: Nystrom and Newton-Schulz).
+  [LF-ar]  the same paper, Arabic summary, section 2a (the Laplacian kernel
+           equation), 2b (injective feature map), 2c (Nystrom, Newton-Schulz,
+           diagonal perturbation).
+  [SOFT]   "[Paper review] SOFT: Softmax-free Transformer with Linear
+           Complexity", Proposed method: S-hat = P^T A^+ P, A_0 = alpha A,
+           A_{k+1} = 2 A_k - A_k A A_k, bottleneck tokens by average pooling,
+           kernel used "without further normalisation".
+
+Every step follows those passages in their order; where they are silent the
+reading taken is stated next to the step.  The method is an approximation with a
+truncated iteration, so this oracle runs the same T Newton-Schulz steps as the
+GPU path (it does not substitute an exact inverse).  Everything is float64.
+
+Per (b, h) slice, with Q, K, V in R^{N x d}, m landmarks and T iterations:
+  L      = average-pool of K over non-overlapping windows of the token grid
+  A      = k(L, L) + eps I                       k(x, y) = exp(-|x - y|_1 / lam)
+  alpha  = 1 / (|A|_1 |A|_inf)
+  X_0    = alpha A;  X_{t+1} = 2 X_t - X_t A X_t;  A^+ := X_T
+  C      = k(L, K)  (m x N);  W = C V;  W-hat = A^+ W
+  P      = k(Q, L)  (N x m);  Z = P, or Z = (P - mu) / sqrt(sigma^2 + eta)
+  O      = Z W-hat
+The backward pass is reverse-mode differentiation of exactly these steps.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+ETA = 1e-5  # variance floor inside the whitening square root (reading: not on the pages)
+
+
+# --------------------------------------------------------------------------
+# kernel  [LF-nl Methodology 1; LF-ar 2a: k(x, y) = exp(-||x - y||_1 / lambda)]
+# --------------------------------------------------------------------------
+def l1_distances(X: np.ndarray, Y: np.ndarray) -> np.ndarray:
+    """D[i, j] = sum_c |X[i, c] - Y[j, c]|, by direct broadcasting (chunked)."""
+    X = np.asarray(X, dtype=np.float64)
+    Y = np.asarray(Y, dtype=np.float64)
+    out = np.empty((X.shape[0], Y.shape[0]))
+    rows = max(1, (1 << 22) // max(1, Y.shape[0] * X.shape[1]))
+    for s in range(0, X.shape[0], rows):
+        out[s:s + rows] = np.abs(X[s:s + rows, None, :] - Y[None, :, :]).sum(axis=-1)
+    return out
+
+
+def laplacian_kernel(X: np.ndarray, Y: np.ndarray, lam: float) -> np.ndarray:
+    return np.exp(-l1_distances(X, Y) / lam)
+
+
+# --------------------------------------------------------------------------
+# landmarks  [LF-ar 2c.1: landmark keys chosen by average pooling;
+#             SOFT Proposed method: average pooling preferred]
+# Reading: non-overlapping sqrt(m) x sqrt(m) windows that tile the grid exactly;
+# landmark a = i * mw + j for window row i, column j (row-major).
+# --------------------------------------------------------------------------
+def pool_index(grid_h: int, grid_w: int, m: int) -> np.ndarray:
+    """token n = y * grid_w + x  ->  landmark of the window containing (y, x)."""
+    mh = math.isqrt(m)
+    if mh * mh != m or grid_h % mh or grid_w % mh:
+        raise ValueError("m must be a square whose root divides both grid sides")
+    mw = mh
+    sh, sw = grid_h // mh, grid_w // mw
+    idx = np.empty(grid_h * grid_w, dtype=np.int64)
+    for y in range(grid_h):
+        for x in range(grid_w):
+            idx[y * grid_w + x] = (y // sh) * mw + (x // sw)
+    return idx
+
+
+def pool_landmarks(K: np.ndarray, idx: np.ndarray, m: int) -> np.ndarray:
+    K = np.asarray(K, dtype=np.float64)
+    L = np.zeros((m, K.shape[1]))
+    np.add.at(L, idx, K)
+    return L / np.bincount(idx, minlength=m)[:, None]
+
+
+# --------------------------------------------------------------------------
+# landmark matrix and Newton-Schulz inverse
+#  [LF-nl Methodology 2, LF-ar 2c.2: small diagonal perturbation eps I;
+#   SOFT Proposed method: A_0 = alpha A, A_{k+1} = 2 A_k - A_k A A_k]
+# Readings: eps only on A's diagonal; alpha = 1 / (|A|_1 |A|_inf) on A including
+# eps I; "iters" = T updates after X_0, returning X_T.
+# --------------------------------------------------------------------------
+def landmark_matrix(L: np.ndarray, lam: float, eps: float) -> np.ndarray:
+    return laplacian_kernel(L, L, lam) + eps * np.eye(L.shape[0])
+
+
+def ns_scale(A: np.ndarray):
+    """alpha and the two norms with their maximising column / row (lowest index on ties)."""
+    colsum = A.sum(axis=0)
+    rowsum = A.sum(axis=1)
+    jstar = int(np.argmax(colsum))
+    istar = int(np.argmax(rowsum))
+    n1, ninf = colsum[jstar], rowsum[istar]
+    return 1.0 / (n1 * ninf), n1, ninf, jstar, istar
+
+
+def newton_schulz(A: np.ndarray, iters: int):
+    """Return ([X_0 .. X_T], [Y_0 .. Y_{T-1}]) with Y_t = A X_t."""
+    alpha = ns_scale(A)[0]
+    X = [alpha * A]
+    Y = []
+    for _ in range(iters):
+        Yt = A @ X[-1]
+        Y.append(Yt)
+        X.append(2.0 * X[-1] - X[-1] @ Yt)
+    return X, Y
+
+
+# --------------------------------------------------------------------------
+# query-side feature map  [LF-nl Methodology 1: normalised injective feature
+#  map; LF-ar 2b: centre and whiten each query's similarity vector with a
+#  diagonal (per-feature) variance estimate instead of a full inverse square root]
+# Readings: statistics per (b, h) and per landmark column over the slice's N
+# queries; biased variance; eta inside the square root; gradients flow
+# through mean and variance; applied to P only, never to C.
+# --------------------------------------------------------------------------
+def feature_map(P: np.ndarray, norm: bool):
+    if not norm:
+        return P, None
+    mu = P.mean(axis=0)
+    var = ((P - mu) ** 2).mean(axis=0)
+    s = np.sqrt(var + ETA)
+    return (P - mu) / s, (mu, var, s)
+
+
+# --------------------------------------------------------------------------
+# forward  [SOFT Proposed method: S-hat = P^T A^+ P, read for separate Q and K as
+#  O = k(Q, L) A^+ (k(L, K) V), no row normalisation]
+# --------------------------------------------------------------------------
+def forward_slice(q, k, v, grid_h, grid_w, m, lam, eps, iters, norm=False):
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    idx = pool_index(grid_h, grid_w, m)
+    L = pool_landmarks(k, idx, m)
+    A = landmark_matrix(L, lam, eps)
+    X, Y = newton_schulz(A, iters)
+    C = laplacian_kernel(L, k, lam)
+    W = C @ v
+    What = X[-1] @ W
+    P = laplacian_kernel(q, L, lam)
+    Z, stats = feature_map(P, norm)
+    O = Z @ What
+    saved = dict(q=q, k=k, v=v, idx=idx, L=L, A=A, X=X, Y=Y, C=C, W=W, What=What,
+                 P=P, Z=Z, stats=stats, lam=lam, eps=eps, m=m, norm=norm)
+    return O, saved
+
+
+# --------------------------------------------------------------------------
+# backward: reverse mode of forward_slice, step by step.
+#  The Laplacian kernel's gradient is -(k/lam) sgn(x - y) per coordinate
+#  [LF-nl Methodology 1 and LF-ar 2a: the L1 norm keeps a non-vanishing
+#  gradient]; reading: sgn(0) = 0.
+# --------------------------------------------------------------------------
+def _sgn(x):
+    return np.sign(x)
+
+
+def _kernel_grad_x(G, X, Y, lam):
+    """For K = k(X, Y) and upstream G_ij = dLoss/dK_ij * K_ij, return dLoss/dX.
+
+    dK_ij/dX_ic = -(K_ij / lam) sgn(X_ic - Y_jc).
+    """
+    dX = np.zeros_like(X)
+    for c in range(X.shape[1]):
+        S = _sgn(X[:, c][:, None] - Y[:, c][None, :])
+        dX[:, c] = -(G * S).sum(axis=1) / lam
+    return dX
+
+
+def _kernel_grad_y(G, X, Y, lam):
+    """Same as _kernel_grad_x but with respect to the second argument Y."""
+    dY = np.zeros_like(Y)
+    for c in range(Y.shape[1]):
+        S = _sgn(X[:, c][:, None] - Y[:, c][None, :])
+        dY[:, c] = (G * S).sum(axis=0) / lam
+    return dY
+
+
+def backward_slice(saved, dO, tied=False):
+    """Return (dq, dk, dv); with tied=True, dq holds the whole gradient of the shared tensor."""
+    dO = np.asarray(dO, dtype=np.float64)
+    lam = saved["lam"]
+    L, A, X, Y, C, W, What = (saved[n] for n in ("L", "A", "X", "Y", "C", "W", "What"))
+    P, Z, q, k, v = saved["P"], saved["Z"], saved["q"], saved["k"], saved["v"]
+    m = saved["m"]
+
+    # O = Z W-hat
+    dWhat = Z.T @ dO
+    dZ = dO @ What.T
+    # feature map (batch-norm style reverse of centring and diagonal whitening)
+    if saved["norm"]:
+        _, _, s = saved["stats"]
+        dP = (dZ - dZ.mean(axis=0) - Z * (dZ * Z).mean(axis=0)) / s
+    else:
+        dP = dZ
+    # P = k(q, L)
+    dq = _kernel_grad_x(dP * P, q, L, lam)
+    dL = _kernel_grad_y(dP * P, q, L, lam)
+
+    # W-hat = X_T W
+    T = len(Y)
+    G = dWhat @ W.T
+    dW = X[T].T @ dWhat
+    # unrolled Newton-Schulz: X_{t+1} = 2 X_t - X_t A X_t
+    dA = np.zeros_like(A)
+    for t in range(T - 1, -1, -1):
+        XtG = X[t].T @ G
+        dA -= XtG @ X[t].T
+        G = 2.0 * G - G @ Y[t].T - A.T @ XtG
+    # X_0 = alpha A, alpha = 1 / (n1 ninf)
+    alpha, n1, ninf, jstar, istar = ns_scale(A)
+    dA += alpha * G
+    dalpha = float((G * A).sum())
+    dA[:, jstar] += dalpha * (-alpha / n1)
+    dA[istar, :] += dalpha * (-alpha / ninf)
+    # A = k(L, L) + eps I: both arguments are L; the eps I term has no gradient
+    Akern = A - saved["eps"] * np.eye(m)
+    GA = dA * Akern
+    dL += _kernel_grad_x(GA, L, L, lam) + _kernel_grad_y(GA, L, L, lam)
+
+    # W = C V, C = k(L, k)
+    dv = C.T @ dW
+    dC = dW @ v.T
+    GC = dC * C
+    dL += _kernel_grad_x(GC, L, k, lam)
+    dk = _kernel_grad_y(GC, L, k, lam)
+
+    # L = window mean of k
+    idx = saved["idx"]
+    counts = np.bincount(idx, minlength=m)
+    dk += dL[idx] / counts[idx][:, None]
+
+    if tied:
+        return dq + dk, None, dv
+    return dq, dk, dv
+
+
+# --------------------------------------------------------------------------
+# batched drivers over [B, H, N, d]
+# --------------------------------------------------------------------------
+def forward(q, k, v, grid_h, grid_w, m, lam, eps, iters, norm=False, slices=None):
+    """O [B, H, N, d] and the per-slice saved state (list)."""
+    B, H, N, d = q.shape
+    O = np.zeros((B, H, N, d))
+    saved = {}
+    for b in range(B):
+        for h in range(H):
+            if slices is not None and (b, h) not in slices:
+                continue
+            O[b, h], saved[(b, h)] = forward_slice(q[b, h], k[b, h], v[b, h], grid_h, grid_w,
+                                                   m, lam, eps, iters, norm)
+    return O, saved
+
+
+def backward(saved, dO, tied=False):
+    """Gradients for every slice in `saved`; returns dicts keyed by (b, h)."""
+    out = {}
+    for key, s in saved.items():
+        out[key] = backward_slice(s, dO[key[0], key[1]], tied)
+    return out
+
+
+def attention(q, k, v, grid_h, grid_w, m, lam, eps, iters, norm=False):
+    return forward(q, k, v, grid_h, grid_w, m, lam, eps, iters, norm)[0]

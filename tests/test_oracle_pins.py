@@ -1,0 +1,207 @@
+"""Pins for the CPU oracle: checks against facts the pages and mathematics fix,
+not against the oracle's own formulas.
+
+- Laplacian kernel values by pure-Python loops; range (0, 1], k(x, x) = 1,
+  symmetry  (LaplacianFormer, Methodology 1 / Arabic summary 2a; SOFT review,
+  Proposed method: the kernel is symmetric with values in [0, 1]).
+- Average-pooling windows enumerated by coordinates (LaplacianFormer Arabic
+  summary 2c.1; SOFT review, Proposed method: average pooling).
+- eps I makes A strictly positive definite (LaplacianFormer Methodology 2).
+- Truncated Newton-Schulz against its closed form through a library eigensolver;
+  the residual |I - A X_t| falls monotonically (SOFT review, Proposed method).
+- With one landmark per token, eps = 0 and a converged iteration, Nystrom gives
+  exact full-kernel attention S V, brute-forced.
+- lambda -> infinity closed form; centring/whitening invariants.
+- Backward against central finite differences of the forward.
+"""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import lapnys_oracle as orc
+
+
+def _loop_kernel(X, Y, lam):
+    out = [[0.0] * len(Y) for _ in range(len(X))]
+    for i, x in enumerate(X):
+        for j, y in enumerate(Y):
+            s = 0.0
+            for c in range(len(x)):
+                s += abs(float(x[c]) - float(y[c]))
+            out[i][j] = math.exp(-s / lam)
+    return np.array(out)
+
+
+def test_kernel_matches_loops_and_range():
+    rng = np.random.default_rng(0)
+    X = rng.standard_normal((7, 5))
+    Y = rng.standard_normal((6, 5)) * 3.0
+    lam = 2.5
+    Kx = orc.laplacian_kernel(X, Y, lam)
+    np.testing.assert_allclose(Kx, _loop_kernel(X, Y, lam), rtol=1e-14, atol=0)
+    assert np.all(Kx > 0) and np.all(Kx <= 1)
+    Kxx = orc.laplacian_kernel(X, X, lam)
+    np.testing.assert_array_equal(np.diag(Kxx), 1.0)
+    np.testing.assert_array_equal(Kxx, Kxx.T)
+    # heavy-tailed values still land in (0, 1]
+    Xt = rng.standard_t(3, size=(9, 64)) * 50
+    Kt = orc.laplacian_kernel(Xt, Xt[::-1], 64.0)
+    assert np.all(Kt >= 0) and np.all(Kt <= 1)
+
+
+@pytest.mark.parametrize("gh,gw,m", [(14, 14, 49), (8, 12, 4), (6, 6, 36), (28, 28, 49), (4, 4, 1)])
+def test_pool_windows_by_enumeration(gh, gw, m):
+    idx = orc.pool_index(gh, gw, m)
+    r = math.isqrt(m)
+    sh, sw = gh // r, gw // r
+    expect = -np.ones(gh * gw, dtype=np.int64)
+    for i in range(r):
+        for j in range(r):
+            for y in range(i * sh, (i + 1) * sh):
+                for x in range(j * sw, (j + 1) * sw):
+                    expect[y * gw + x] = i * r + j
+    np.testing.assert_array_equal(idx, expect)
+    # landmark values by a reshape-mean over (window row, in-window row, window col, in-window col)
+    rng = np.random.default_rng(1)
+    K = rng.standard_normal((gh * gw, 3))
+    L = orc.pool_landmarks(K, idx, m)
+    L2 = K.reshape(r, sh, r, sw, 3).mean(axis=(1, 3)).reshape(m, 3)
+    np.testing.assert_allclose(L, L2, rtol=1e-13, atol=1e-15)
+
+
+def test_pool_rejects_bad_geometry():
+    for args in [(14, 14, 48), (14, 14, 16), (10, 12, 9)]:
+        with pytest.raises(ValueError):
+            orc.pool_index(*args)
+
+
+def test_one_landmark_per_token_is_identity():
+    rng = np.random.default_rng(2)
+    K = rng.standard_normal((16, 4))
+    idx = orc.pool_index(4, 4, 16)
+    np.testing.assert_array_equal(orc.pool_landmarks(K, idx, 16), K)
+
+
+def test_landmark_matrix_is_spd_with_eps_diagonal():
+    rng = np.random.default_rng(3)
+    L = rng.standard_normal((49, 32))
+    A = orc.landmark_matrix(L, 32.0, 1e-3)
+    np.testing.assert_allclose(np.diag(A), 1.0 + 1e-3, rtol=0, atol=1e-15)
+    np.testing.assert_array_equal(A, A.T)
+    assert np.linalg.eigvalsh(A).min() > 0
+
+
+@pytest.mark.parametrize("m,d,T", [(49, 32, 20), (64, 64, 20), (16, 4, 3), (36, 8, 0)])
+def test_newton_schulz_closed_form(m, d, T):
+    rng = np.random.default_rng(4 + m)
+    L = rng.standard_normal((m, d))
+    A = orc.landmark_matrix(L, float(d), 1e-3)
+    X, Y = orc.newton_schulz(A, T)
+    assert len(X) == T + 1 and len(Y) == T
+    sig, U = np.linalg.eigh(A)
+    alpha = 1.0 / (np.abs(A).sum(axis=0).max() * np.abs(A).sum(axis=1).max())
+    assert alpha * sig.max() ** 2 <= 1.0 + 1e-12
+    # X_t has eigenvalues (1 - (1 - alpha s^2)^(2^t)) / s for eigenvalue s of A
+    prev = np.inf
+    for t in range(T + 1):
+        e = (1.0 - alpha * sig ** 2) ** (2.0 ** t)
+        Xt = (U * ((1.0 - e) / sig)) @ U.T
+        np.testing.assert_allclose(X[t], Xt, rtol=0, atol=1e-10 * np.abs(Xt).max())
+        res = np.linalg.norm(np.eye(m) - A @ X[t])
+        np.testing.assert_allclose(res, np.sqrt((e ** 2).sum()), rtol=1e-6, atol=1e-12)
+        assert res <= prev + 1e-12
+        prev = res
+
+
+def _brute_full_attention(q, k, v, lam):
+    S = _loop_kernel(q, k, lam)
+    return S @ v, S
+
+
+def test_one_landmark_per_token_equals_full_kernel_attention():
+    rng = np.random.default_rng(5)
+    N, d = 16, 4
+    q, k, v = (rng.standard_normal((N, d)) for _ in range(3))
+    lam = float(d)
+    O, _ = orc.forward_slice(q, k, v, 4, 4, N, lam, 0.0, 40)
+    Oref, S = _brute_full_attention(q, k, v, lam)
+    np.testing.assert_allclose(O, Oref, rtol=1e-9, atol=1e-9)
+    # eps > 0 with a converged iteration gives S (G + eps I)^-1 G V, G = k(K, K)
+    eps = 1e-3
+    O2, _ = orc.forward_slice(q, k, v, 4, 4, N, lam, eps, 40)
+    G = _loop_kernel(k, k, lam)
+    O2ref = S @ np.linalg.solve(G + eps * np.eye(N), G @ v)
+    np.testing.assert_allclose(O2, O2ref, rtol=1e-9, atol=1e-9)
+
+
+def test_large_lambda_closed_form():
+    # kernel == 1 everywhere: A = J + eps I, X_T 1 = 1 / (m + eps), O_i = m / (m + eps) sum_j V_j
+    rng = np.random.default_rng(6)
+    N, d, m, eps = 36, 8, 9, 1e-3
+    q, k, v = (rng.standard_normal((N, d)) for _ in range(3))
+    O, _ = orc.forward_slice(q, k, v, 6, 6, m, 1e300, eps, 5)
+    expect = np.broadcast_to(m / (m + eps) * v.sum(axis=0), (N, d))
+    np.testing.assert_allclose(O, expect, rtol=1e-10, atol=1e-10)
+
+
+def test_feature_map_invariants():
+    rng = np.random.default_rng(7)
+    N, d, m = 64, 8, 16
+    q, k, v = (rng.standard_normal((N, d)) for _ in range(3))
+    _, s = orc.forward_slice(q, k, v, 8, 8, m, float(d), 1e-3, 5, norm=True)
+    Z, P = s["Z"], s["P"]
+    np.testing.assert_allclose(Z.mean(axis=0), 0.0, atol=1e-12)
+    var = P.var(axis=0)
+    np.testing.assert_allclose(Z.var(axis=0), var / (var + orc.ETA), rtol=1e-10)
+
+
+def _fd_check(tied, norm, seed):
+    rng = np.random.default_rng(seed)
+    gh = gw = 4
+    N, d, m, T, lam, eps = 16, 4, 4, 3, 4.0, 1e-3
+    q = rng.standard_normal((N, d))
+    k = q.copy() if tied else rng.standard_normal((N, d))
+    v = rng.standard_normal((N, d))
+    R = rng.standard_normal((N, d))
+
+    def loss(q_, k_, v_):
+        O, _ = orc.forward_slice(q_, q_ if tied else k_, v_, gh, gw, m, lam, eps, T, norm)
+        return float((O * R).sum())
+
+    _, saved = orc.forward_slice(q, k, v, gh, gw, m, lam, eps, T, norm)
+    dq, dk, dv = orc.backward_slice(saved, R, tied=tied)
+    h = 1e-6
+    names = ("q", "v") if tied else ("q", "k", "v")
+    grads = {"q": dq, "k": dk, "v": dv}
+    for name in names:
+        base = {"q": q, "k": k, "v": v}
+        fd = np.zeros((N, d))
+        for i in range(N):
+            for c in range(d):
+                plus = {n: a.copy() for n, a in base.items()}
+                minus = {n: a.copy() for n, a in base.items()}
+                plus[name][i, c] += h
+                minus[name][i, c] -= h
+                fd[i, c] = (loss(plus["q"], plus["k"], plus["v"])
+                            - loss(minus["q"], minus["k"], minus["v"])) / (2 * h)
+        g = grads[name]
+        err = np.linalg.norm(g - fd) / np.linalg.norm(fd)
+        assert err < 1e-6, (name, err)
+
+
+@pytest.mark.parametrize("tied,norm", [(False, False), (False, True), (True, False), (True, True)])
+def test_backward_matches_finite_differences(tied, norm):
+    _fd_check(tied, norm, seed=10 + 2 * tied + norm)
+
+
+def test_dv_is_linear_map_transpose():
+    # O = M V with M = Z A^+ C, so dV = M^T dO
+    rng = np.random.default_rng(11)
+    N, d, m = 36, 4, 9
+    q, k, v, dO = (rng.standard_normal((N, d)) for _ in range(4))
+    O, s = orc.forward_slice(q, k, v, 6, 6, m, float(d), 1e-3, 6, norm=True)
+    M = s["Z"] @ s["X"][-1] @ s["C"]
+    np.testing.assert_allclose(O, M @ v, rtol=1e-12, atol=1e-12)
+    _, _, dv = orc.backward_slice(s, dO)
+    np.testing.assert_allclose(dv, M.T @ dO, rtol=1e-12, atol=1e-12)
