@@ -1,0 +1,362 @@
+#!/usr/bin/env python
+"""Benchmark: tokens/s of Laplacian-kernel Nystrom attention, forward + backward.
+
+One step = one pass of the whole path (landmark pooling, landmark matrix,
+Newton-Schulz, key pass, W-hat, query pass, and the full backward) over one
+batch of the high-resolution workload: B=8, H=8, 128x128 token grid
+(N=16384), d=64, m=256 landmarks (8x8 pooling windows), bf16 inputs with fp32
+accumulation, lambda=d, eps=1e-3, 24 Newton-Schulz iterations, 1% heavy-tailed
+tokens in Q and K.  Inputs are synthetic and seeded; Q, K, V and dO are 134 MB
+each, so every step streams inputs larger than the 129 MB L2.
+
+Under torchrun each rank runs its own copy of the workload on its own GPU
+(independent (b, h) slices: weak scaling, no collective on the data path).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "tokens/sec Laplacian-Nyström attn fwd & fwd+bwd; % of ALU/HBM roofline"
+UNIT = "tokens/s"
+WORKLOAD = "hires16k"
+
+# FP32 lane-op peak of the part: 152 SMs x 128 FP32 lanes x 2070 MHz (max SM clock);
+# one lane-op = one FADD / FMUL / FFMA / select result.
+ALU_PEAK_TOPS = 152 * 128 * 2070e6 / 1e12
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--oracle-worker", action="store_true", help=argparse.SUPPRESS)
+    return ap.parse_args()
+
+
+def algorithmic_ops(w):
+    """FP32 lane-ops per step, from the method's arithmetic."""
+    BH, N, m, d, T = w.B * w.H, w.N, w.m, w.d, w.iters
+    nmd = BH * N * m * d
+    per = {
+        # distance (sub + abs-add) + contraction FMA
+        "key_fwd": 3 * nmd,
+        "query_fwd": 3 * nmd,
+        "qstats": 2 * nmd if w.norm else 0,
+        # distance 2 + dot 1 + contraction 1 + sign term (sub, select, two adds) 4
+        "bwd_query": 8 * nmd,
+        "bwd_key": 8 * nmd,
+        "bwd_qstats": 4 * nmd if w.norm else 0,
+        # Newton-Schulz: two m^3 products per forward step, four per backward step
+        "ns_fwd": 2 * T * BH * m ** 3,
+        "ns_bwd": 4 * T * BH * m ** 3,
+    }
+    return per
+
+
+def clock_sampler(gpu_index: int):
+    f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+    q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    try:
+        p = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                              "-i", str(gpu_index), "-lms", "200"], stdout=f,
+                             stderr=subprocess.DEVNULL)
+    except OSError:
+        p = None
+    return p, f.name
+
+
+def clock_summary(proc, path):
+    if proc is not None:
+        proc.terminate()
+        try:
+            proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            proc.kill()
+    sm, mx, reasons = [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    try:
+        for line in open(path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(path)
+    except OSError:
+        pass
+    return {"sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(mx) if mx else None, "samples": len(sm),
+            "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm): one (b, h) slice, forward + backward
+# ---------------------------------------------------------------------------
+def _oracle_slice(wname: str):
+    import dataclasses
+
+    from laplacian_nystr_linear_gb300.inputs import WORKLOADS, make_inputs
+    from oracle import lapnys_oracle as orc
+    w = dataclasses.replace(WORKLOADS[wname], B=1, H=1)
+    inp = make_inputs(w, with_grad=True)
+    t0 = time.perf_counter()
+    _, saved = orc.forward(inp["q"], inp["k"], inp["v"], w.grid_h, w.grid_w, w.m, w.lam, w.eps,
+                           w.iters, w.norm)
+    orc.backward(saved, inp["dout"], tied=w.tied)
+    return time.perf_counter() - t0, w.N
+
+
+def _single_thread_env():
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[k] = "1"
+    return env
+
+
+def cpu_baseline(wname: str):
+    """The oracle as it stands, one process, one thread, on one (b, h) slice."""
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-worker",
+                        "--workload", wname], capture_output=True, text=True,
+                       env=_single_thread_env(), timeout=1800)
+    if r.returncode != 0:
+        return {"error": r.stderr.strip().splitlines()[-1:]}
+    sec, tokens = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": tokens / sec, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"one (b,h) slice of {wname} (N={tokens} tokens), fwd+bwd, fp64, "
+                      f"{sec:.1f} s single-threaded"}
+
+
+def _pool_task(wname):
+    os.environ.update({k: "1" for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS",
+                                         "MKL_NUM_THREADS")})
+    return _oracle_slice(wname)
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the fp64 oracle, each step one slice fwd+bwd, steps spread over host cores."""
+    if rank != 0:
+        return
+    import multiprocessing as mp
+    cores = max(1, min(os.cpu_count() or 1, max(args.steps, args.warmup)))
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(cores) as pool:
+        pool.map(_pool_task, [args.workload] * max(args.warmup, 1))
+        t0 = time.perf_counter()
+        res = pool.map(_pool_task, [args.workload] * args.steps)
+        wall = time.perf_counter() - t0
+    tokens = sum(t for _, t in res)
+    value = tokens / wall
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": args.workload, "sample": "one (b,h) slice per step"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} steps x one (b,h) slice of {args.workload}, "
+                                   f"fwd+bwd, fp64, {cores} processes x 1 thread"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from laplacian_nystr_linear_gb300 import api
+    from laplacian_nystr_linear_gb300.inputs import WORKLOADS, make_inputs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    w = WORKLOADS[args.workload]
+    p = api.Params(w.B, w.H, w.grid_h, w.grid_w, w.d, w.m, w.lam, w.eps, w.iters, w.tied, w.norm)
+    tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    inp = make_inputs(w, with_grad=True)
+    host = {n: torch.from_numpy(np.ascontiguousarray(inp[n])).to(tdt) for n in ("q", "k", "v", "dout")}
+    q, k, v, dout = (host[n].to(dev) for n in ("q", "k", "v", "dout"))
+    if w.tied:
+        k = q
+    out = torch.empty_like(q)
+    dq, dv = torch.empty_like(q), torch.empty_like(q)
+    dk = None if w.tied else torch.empty_like(q)
+    ctx = api.alloc_ctx(p, dev)
+    ws = api.alloc_workspace(p, dev)
+
+    def step():
+        api.fwd(q, k, v, p, out=out, ctx=ctx, ws=ws)
+        api.bwd(q, k, v, dout, ctx, p, dq=dq, dk=dk, dv=dv, ws=ws)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x: float) -> float:
+        if world == 1:
+            return x
+        t = torch.tensor([x], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    sampler, cpath = clock_sampler(local_rank)
+    time.sleep(0.3)
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = api.launch_count()
+    api.profile_enable(True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    barrier()
+    clocks = clock_summary(sampler, cpath)
+    prof = api.profile_read()
+    api.profile_enable(False)
+    launches = api.launch_count() - launches0
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+    value = world * w.tokens / (ms / 1e3)
+
+    # forward alone (same buffers)
+    for _ in range(2):
+        api.fwd(q, k, v, p, out=out, ctx=ctx, ws=ws)
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        api.fwd(q, k, v, p, out=out, ctx=ctx, ws=ws)
+    e1.record(stream)
+    barrier()
+    ms_fwd = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+
+    # roofline of the dominant kernel (FP32 lane-ops; the path is ALU-bound)
+    ops = algorithmic_ops(w)
+    per_launch_ops = {"bwd_key": ops["bwd_key"], "bwd_query": ops["bwd_query"],
+                      "key_fwd": ops["key_fwd"], "query_fwd": ops["query_fwd"]}
+    kernel_ms = {n: (c, t / c) for n, (c, t) in prof.items() if c}
+    step_ms_sum = sum(t for _, t in prof.values()) / args.steps
+    dom = max(per_launch_ops, key=lambda n: prof.get(n, (0, 0.0))[1])
+    dom_ms = kernel_ms[dom][1]
+    achieved = per_launch_ops[dom] / (dom_ms / 1e3) / 1e12
+    total_ops = sum(ops.values())
+    roofline = {
+        "bound": "alu", "kernel": dom, "achieved": achieved, "peak": ALU_PEAK_TOPS,
+        "unit": "Tlaneop/s", "frac": achieved / ALU_PEAK_TOPS,
+        "traffic": None,
+        "peak_source": "152 SMs x 128 FP32 lanes x 2070 MHz",
+        "step_frac": total_ops / (ms / 1e3) / 1e12 / ALU_PEAK_TOPS,
+    }
+
+    # end to end through the public API: pinned host inputs in, results back to host
+    e2e = None
+    if not args.no_e2e:
+        pin = {n: host[n].pin_memory() for n in host}
+        back = {n: torch.empty(q.shape, dtype=tdt).pin_memory() for n in ("out", "dq", "dk", "dv")}
+        ne = max(3, min(args.steps, 10))
+
+        def step_e2e():
+            qd = pin["q"].to(dev, non_blocking=True)
+            kd = qd if w.tied else pin["k"].to(dev, non_blocking=True)
+            vd = pin["v"].to(dev, non_blocking=True)
+            dd = pin["dout"].to(dev, non_blocking=True)
+            o, c = api.fwd(qd, kd, vd, p, out=out, ctx=ctx, ws=ws)
+            gq, gk, gv = api.bwd(qd, kd, vd, dd, c, p, dq=dq, dk=dk, dv=dv, ws=ws)
+            back["out"].copy_(o, non_blocking=True)
+            back["dq"].copy_(gq, non_blocking=True)
+            if gk is not None:
+                back["dk"].copy_(gk, non_blocking=True)
+            back["dv"].copy_(gv, non_blocking=True)
+
+        step_e2e()
+        barrier()
+        e0.record(stream)
+        for _ in range(ne):
+            step_e2e()
+        e1.record(stream)
+        barrier()
+        ms_e2e = max_over_ranks(e0.elapsed_time(e1) / ne)
+        nbytes = q.numel() * q.element_size()
+        n_in = 3 if w.tied else 4
+        n_out = 3 if w.tied else 4
+        e2e = {"value": world * w.tokens / (ms_e2e / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": n_in * nbytes, "d2h_bytes_per_step": n_out * nbytes,
+               "ms_per_step": ms_e2e}
+
+    if rank != 0:
+        return
+    base = None
+    if world == 1 and not args.no_cpu_baseline:
+        base = cpu_baseline(args.workload)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded N(0,1) plus 1% Student-t tokens in Q and K)",
+        "config": {"workload": args.workload, "B": w.B, "H": w.H, "N": w.N, "grid": [w.grid_h, w.grid_w],
+                   "d": w.d, "m": w.m, "iters": w.iters, "lambda": w.lam, "eps": w.eps,
+                   "norm": w.norm, "tied": w.tied, "pass": "fwd+bwd",
+                   "l2": "inputs larger than L2 (Q, K, V, dO 134 MB each, 129 MB L2); no flush",
+                   "parallelism": f"replicas x{world}"},
+        "fwd_tokens_per_s": world * w.tokens / (ms_fwd / 1e3), "ms_fwd": ms_fwd,
+        "roofline": roofline,
+        "kernels_ms_per_step": {n: t / args.steps for n, (c, t) in sorted(prof.items(), key=lambda x: -x[1][1])},
+        "kernel_sum_ms_per_step": step_ms_sum,
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": base,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.oracle_worker:
+        sec, tokens = _oracle_slice(args.workload)
+        print(json.dumps([sec, tokens]))
+        return
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.gpus == 1 else 1)))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,148 @@
+/*
+ * lapnys.h - C ABI of the GB300 (sm_103a) library for Laplacian-kernel Nystrom
+ * attention: forward and backward of
+ *
+ *     O = Z . A^+ . (C . V),   C = k(L, K),  P = k(Q, L),  A = k(L, L) + eps I,
+ *     k(x, y) = exp(-||x - y||_1 / lambda),  Z = P  or  (P - mu) / sqrt(var + eta),
+ *
+ * with landmarks L average-pooled from K and A^+ the Newton-Schulz iterate
+ * X_T (X_0 = alpha A, X_{t+1} = 2 X_t - X_t A X_t, alpha = 1/(|A|_1 |A|_inf)).
+ *
+ * Defining passages (page title, section):
+ *  - kernel: "LaplacianFormer: Rethinking Linear Attention with Laplacian
+ *    Kernel" (Dutch summary), Methodology 1; Arabic summary, section 2a.
+ *  - Nystrom landmarks by average pooling, Newton-Schulz inverse, eps I:
+ *    the same pages, Methodology 2 / section 2c; "[Paper review] SOFT:
+ *    Softmax-free Transformer with Linear Complexity", Proposed method
+ *    (S-hat = P^T A^+ P, A_0 = alpha A, A_{k+1} = 2 A_k - A_k A A_k, pooling).
+ *  - normalised query feature map (centring + diagonal variance): Dutch
+ *    summary Methodology 1, Arabic summary section 2b.
+ *  - gradient through sgn(x - y) of the L1 distance: Dutch summary
+ *    Methodology 1 (non-vanishing gradient), Arabic summary section 2a.
+ *
+ * Conventions for every entry point
+ *  - Tensors q, k, v, out, dout, dq, dk, dv are DEVICE pointers to contiguous
+ *    [B][H][N][d] arrays (d innermost), token n = y * grid_w + x on the
+ *    grid_h x grid_w grid, 16-byte aligned, all of one element type `dtype`
+ *    (LAPNYS_F32 = float, LAPNYS_BF16 = bfloat16).  Arithmetic is float32.
+ *  - Landmarks: m = r * r, r divides grid_h and grid_w; landmark a = i * r + j
+ *    is the mean of the (grid_h / r) x (grid_w / r) window in window-row i,
+ *    window-column j.
+ *  - The caller owns and allocates everything: out, gradients, `ctx` (state
+ *    saved by the forward for the backward) and `ws` (scratch).  The library
+ *    allocates no device memory, does not synchronise, and enqueues all work
+ *    on `stream` (0 = legacy default stream).  Sizes come from
+ *    lapnys_ctx_bytes / lapnys_workspace_bytes.
+ *  - Return value: LAPNYS_OK, or an error code.  Argument errors (EINVAL,
+ *    ENOSPC, ENOTSUP) are detected on the host before anything is enqueued, so
+ *    nothing has been written.  ECUDA reports a failed launch (the CUDA error
+ *    is left for cudaGetLastError-style inspection by the caller).
+ *  - Not thread-safe only with respect to lapnys_profile_*; the compute entry
+ *    points keep no state between calls.
+ */
+#ifndef LAPNYS_H
+#define LAPNYS_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LAPNYS_OK = 0,
+  LAPNYS_EINVAL = 1,   /* bad dimension, pointer, alignment or parameter */
+  LAPNYS_ECUDA = 2,    /* a kernel launch failed */
+  LAPNYS_ETIMEOUT = 3, /* reserved: a bounded device wait expired (no current kernel waits) */
+  LAPNYS_ENOSPC = 4,   /* ctx or workspace smaller than the *_bytes functions require */
+  LAPNYS_ENOTSUP = 5   /* valid request outside what this build supports (e.g. d) */
+} lapnys_status;
+
+enum { LAPNYS_F32 = 0, LAPNYS_BF16 = 1 };
+
+/* flags: centre each landmark column of P over the slice's N queries and divide
+ * by sqrt(biased variance + 1e-5) (the "injective" normalised feature map). */
+enum { LAPNYS_NORM = 1u << 0 };
+
+/* Limits of this build: d in {16, 32, 64, 128}; 1 <= m <= N; m a perfect
+ * square dividing the grid as above; 0 <= iters <= 64; lambda > 0; eps >= 0;
+ * B * H * N * d < 2^31. */
+
+/* Bytes of the caller-owned context written by lapnys_fwd and read by
+ * lapnys_bwd (landmarks, A, alpha, all Newton-Schulz iterates, W, W-hat,
+ * feature-map statistics).  Returns 0 for invalid dimensions. */
+size_t lapnys_ctx_bytes(int B, int H, int N, int d, int m, int iters, unsigned flags);
+
+/* Bytes of scratch memory needed by lapnys_fwd (with or without ctx) and by
+ * lapnys_bwd for these dimensions.  Returns 0 for invalid dimensions. */
+size_t lapnys_workspace_bytes(int B, int H, int N, int d, int m, int iters, unsigned flags);
+
+/* Forward.  Writes out = Z . X_T . (C . V) for every (b, h) slice.
+ *  tied_qk: 1 = queries and keys are one tensor (k may be NULL or equal q).
+ *  ctx: NULL for inference only; otherwise ctx_bytes >= lapnys_ctx_bytes(...)
+ *       and lapnys_bwd can be called with it afterwards.
+ *  ws/ws_bytes: scratch, ws_bytes >= lapnys_workspace_bytes(...). */
+int lapnys_fwd(const void* q, const void* k, const void* v, void* out,
+               int B, int H, int N, int d, int grid_h, int grid_w, int m,
+               float lambda, float eps, int iters, int tied_qk, cudaStream_t stream,
+               int dtype, unsigned flags, void* ctx, size_t ctx_bytes,
+               void* ws, size_t ws_bytes);
+
+/* Backward of lapnys_fwd for the upstream gradient dout.  Needs the ctx written
+ * by the forward with the same q, k, v and parameters.  Writes dq, dk, dv
+ * (overwritten, not accumulated).  With tied_qk = 1, dk must be NULL and dq
+ * receives the whole gradient of the shared query/key tensor (query path, key
+ * path and the landmark-pooling path). */
+int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout,
+               const void* ctx, void* dq, void* dk, void* dv,
+               int B, int H, int N, int d, int grid_h, int grid_w, int m,
+               float lambda, float eps, int iters, int tied_qk, cudaStream_t stream,
+               int dtype, unsigned flags, void* ws, size_t ws_bytes);
+
+/* Byte offsets of the intermediates inside ctx, for inspection and tests.
+ * All float32 unless noted:
+ *   L     [B*H][m][d]             landmarks
+ *   A     [B*H][m][m]             k(L, L) + eps I
+ *   alpha [B*H][4]                alpha, |A|_1, |A|_inf, and the int32 argmax
+ *                                 column of |A|_1 stored bitwise in slot 3
+ *   X     [B*H][iters+1][m][m]    Newton-Schulz iterates X_0 .. X_T
+ *   Y     [B*H][iters][m][m]      products A X_t
+ *   W     [B*H][m][d]             C . V
+ *   What  [B*H][m][d]             X_T . W
+ *   stats [B*H][3][m]             mu, var, 1/sqrt(var + 1e-5) (LAPNYS_NORM only)
+ *   idx   int32 [N]               landmark of each token (same for all slices) */
+typedef struct {
+  size_t L, A, alpha, X, Y, W, What, stats, idx, total;
+} lapnys_ctx_layout;
+
+int lapnys_ctx_offsets(int B, int H, int N, int d, int m, int iters, unsigned flags,
+                       lapnys_ctx_layout* out);
+
+/* Landmark pooling alone: L [B*H][m][d] float32 from k, and idx int32 [N]
+ * (idx may be NULL).  Same rules as lapnys_fwd. */
+int lapnys_pool(const void* k, float* L, int32_t* idx, int B, int H, int N, int d,
+                int grid_h, int grid_w, int m, int dtype, cudaStream_t stream);
+
+/* Human-readable text for a status code (static storage). */
+const char* lapnys_strerror(int status);
+
+/* Instrumentation (host side, process-wide, not thread-safe):
+ *  lapnys_launch_count: kernels this library has enqueued since load.
+ *  lapnys_profile_enable(1): from then on record a CUDA event pair around
+ *    every launch (on the launch's stream); lapnys_profile_read, called after
+ *    the caller synchronised, adds up elapsed times per kernel name and
+ *    clears them.  Up to 4096 launches are recorded between reads; later ones
+ *    are counted but not timed.
+ *  lapnys_profile_read fills at most max_kernels entries (name pointer with
+ *    static storage, launches, total milliseconds) and returns how many kernel
+ *    names it found, or -1 if an event query failed. */
+uint64_t lapnys_launch_count(void);
+int lapnys_profile_enable(int on);
+int lapnys_profile_read(const char** names, int* launches, double* total_ms, int max_kernels);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LAPNYS_H */

@@ -1,0 +1,211 @@
+"""PyTorch-facing wrappers over the C ABI (marshalling only: PyTorch supplies
+device memory and the current stream; every step runs in liblapnys kernels)."""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+
+import torch
+
+from . import _lib
+from ._lib import check, load
+
+_DT = {torch.float32: _lib.LAPNYS_F32, torch.bfloat16: _lib.LAPNYS_BF16}
+
+
+@dataclasses.dataclass(frozen=True)
+class Params:
+    """Shape and method parameters of one call ([B, H, N, d] tensors on a grid)."""
+    B: int
+    H: int
+    grid_h: int
+    grid_w: int
+    d: int
+    m: int
+    lam: float
+    eps: float = 1e-3
+    iters: int = 20
+    tied: bool = False
+    norm: bool = False
+
+    @property
+    def N(self) -> int:
+        return self.grid_h * self.grid_w
+
+    @property
+    def flags(self) -> int:
+        return _lib.LAPNYS_NORM if self.norm else 0
+
+    def dims(self):
+        return (self.B, self.H, self.N, self.d, self.grid_h, self.grid_w, self.m)
+
+    @staticmethod
+    def of(q: torch.Tensor, grid, m: int, lam=None, eps=1e-3, iters=20, tied=False, norm=False):
+        B, H, N, d = q.shape
+        gh, gw = grid
+        return Params(B, H, gh, gw, d, m, float(d if lam is None else lam), float(eps), int(iters),
+                      bool(tied), bool(norm))
+
+
+def ctx_bytes(p: Params) -> int:
+    return load().lapnys_ctx_bytes(p.B, p.H, p.N, p.d, p.m, p.iters, p.flags)
+
+
+def workspace_bytes(p: Params) -> int:
+    return load().lapnys_workspace_bytes(p.B, p.H, p.N, p.d, p.m, p.iters, p.flags)
+
+
+def ctx_offsets(p: Params) -> dict:
+    lay = _lib.CtxLayout()
+    check(load().lapnys_ctx_offsets(p.B, p.H, p.N, p.d, p.m, p.iters, p.flags, ctypes.byref(lay)),
+          "lapnys_ctx_offsets")
+    return {n: getattr(lay, n) for n, _ in _lib.CtxLayout._fields_}
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype not in _DT:
+        raise TypeError(f"unsupported dtype {t.dtype}; use float32 or bfloat16")
+    return _DT[t.dtype]
+
+
+def _check_tensor(t: torch.Tensor, name: str, like: torch.Tensor) -> None:
+    if not t.is_cuda or not t.is_contiguous() or t.dtype != like.dtype or t.shape != like.shape:
+        raise ValueError(f"{name} must be a contiguous CUDA tensor like q ({like.shape}, {like.dtype})")
+
+
+def alloc_ctx(p: Params, device) -> torch.Tensor:
+    return torch.empty(ctx_bytes(p), dtype=torch.uint8, device=device)
+
+
+def alloc_workspace(p: Params, device) -> torch.Tensor:
+    return torch.empty(workspace_bytes(p), dtype=torch.uint8, device=device)
+
+
+def fwd(q, k, v, p: Params, out=None, ctx=None, ws=None, need_ctx=True):
+    """lapnys_fwd: returns (out, ctx); ctx is None when need_ctx is False."""
+    _check_tensor(q, "q", q)
+    _check_tensor(v, "v", q)
+    if not p.tied:
+        _check_tensor(k, "k", q)
+    dev = q.device
+    out = torch.empty_like(q) if out is None else out
+    if need_ctx and ctx is None:
+        ctx = alloc_ctx(p, dev)
+    ws = alloc_workspace(p, dev) if ws is None else ws
+    rc = load().lapnys_fwd(
+        _ptr(q), None if p.tied else _ptr(k), _ptr(v), _ptr(out), *p.dims(), p.lam, p.eps,
+        p.iters, int(p.tied), _stream(dev), _dtype(q), p.flags,
+        _ptr(ctx) if need_ctx else None, ctx.numel() if need_ctx else 0, _ptr(ws), ws.numel())
+    check(rc, "lapnys_fwd")
+    return out, (ctx if need_ctx else None)
+
+
+def bwd(q, k, v, dout, ctx, p: Params, dq=None, dk=None, dv=None, ws=None):
+    """lapnys_bwd: returns (dq, dk, dv); dk is None in tied mode (dq holds it all)."""
+    _check_tensor(dout, "dout", q)
+    dev = q.device
+    dq = torch.empty_like(q) if dq is None else dq
+    dv = torch.empty_like(q) if dv is None else dv
+    if not p.tied and dk is None:
+        dk = torch.empty_like(q)
+    ws = alloc_workspace(p, dev) if ws is None else ws
+    rc = load().lapnys_bwd(
+        _ptr(q), None if p.tied else _ptr(k), _ptr(v), _ptr(dout), _ptr(ctx), _ptr(dq),
+        None if p.tied else _ptr(dk), _ptr(dv), *p.dims(), p.lam, p.eps, p.iters, int(p.tied),
+        _stream(dev), _dtype(q), p.flags, _ptr(ws), ws.numel())
+    check(rc, "lapnys_bwd")
+    return dq, (None if p.tied else dk), dv
+
+
+def pool(k, grid, m):
+    """lapnys_pool: landmarks [B, H, m, d] float32 and the token -> landmark index [N] int32."""
+    B, H, N, d = k.shape
+    L = torch.empty((B, H, m, d), dtype=torch.float32, device=k.device)
+    idx = torch.empty((N,), dtype=torch.int32, device=k.device)
+    rc = load().lapnys_pool(_ptr(k), _ptr(L), _ptr(idx), B, H, N, d, grid[0], grid[1], m,
+                            _dtype(k), _stream(k.device))
+    check(rc, "lapnys_pool")
+    return L, idx
+
+
+def ctx_views(ctx: torch.Tensor, p: Params) -> dict:
+    """Float32 / int32 views of the intermediates saved in ctx (see lapnys_ctx_layout)."""
+    off = ctx_offsets(p)
+    BH, m, d, T = p.B * p.H, p.m, p.d, p.iters
+
+    def f32(name, shape):
+        n = 1
+        for s in shape:
+            n *= s
+        return ctx[off[name]:off[name] + 4 * n].view(torch.float32).view(shape)
+
+    views = {
+        "L": f32("L", (p.B, p.H, m, d)),
+        "A": f32("A", (p.B, p.H, m, m)),
+        "alpha": f32("alpha", (p.B, p.H, 4)),
+        "X": f32("X", (p.B, p.H, T + 1, m, m)),
+        "W": f32("W", (p.B, p.H, m, d)),
+        "What": f32("What", (p.B, p.H, m, d)),
+        "stats": f32("stats", (p.B, p.H, 3, m)),
+        "idx": ctx[off["idx"]:off["idx"] + 4 * p.N].view(torch.int32),
+    }
+    if T > 0:
+        views["Y"] = f32("Y", (p.B, p.H, T, m, m))
+    return views
+
+
+def launch_count() -> int:
+    return int(load().lapnys_launch_count())
+
+
+def profile_enable(on: bool) -> None:
+    load().lapnys_profile_enable(1 if on else 0)
+
+
+def profile_read(max_kernels: int = 64) -> dict:
+    """{kernel name: (launches, total ms)} since the last read; call after a synchronize."""
+    names = (ctypes.c_char_p * max_kernels)()
+    launches = (ctypes.c_int * max_kernels)()
+    total = (ctypes.c_double * max_kernels)()
+    n = load().lapnys_profile_read(names, launches, total, max_kernels)
+    if n < 0:
+        raise RuntimeError("lapnys_profile_read: an event query failed")
+    return {names[i].decode(): (launches[i], total[i]) for i in range(n)}
+
+
+class _Attention(torch.autograd.Function):
+    @staticmethod
+    def forward(fctx, q, k, v, p: Params):
+        out, ctx = fwd(q, k, v, p, need_ctx=True)
+        fctx.p = p
+        fctx.save_for_backward(q, k if not p.tied else q, v, ctx)
+        return out
+
+    @staticmethod
+    def backward(fctx, dout):
+        q, k, v, ctx = fctx.saved_tensors
+        p = fctx.p
+        dq, dk, dv = bwd(q, k, v, dout.contiguous(), ctx, p)
+        if p.tied:
+            return dq, None, dv, None
+        return dq, dk, dv, None
+
+
+def attention(q, k, v, grid, m, lam=None, eps=1e-3, iters=20, tied=False, norm=False):
+    """Laplacian-kernel Nystrom attention O = Z . X_T . (k(L, K) . V) with autograd.
+
+    q, k, v: [B, H, N, d] CUDA tensors (float32 or bfloat16), N = grid[0] * grid[1].
+    In tied mode pass k=None (or k=q); the gradient of the shared tensor goes to q.
+    """
+    p = Params.of(q, grid, m, lam, eps, iters, tied, norm)
+    if tied:
+        k = q
+    return _Attention.apply(q, k, v, p)

@@ -1,0 +1,94 @@
+// Device helpers shared by the lapnys kernels (sm_103a).
+//
+// Tiles: 64 tokens x 64 landmarks per CTA step, 256 threads arranged as a
+// 16 x 16 grid (ty = tid / 16, tx = tid % 16).  Row tiles of a [rows][D]
+// matrix live in shared memory as float [64][D + 4]; the +4 pad keeps 16-byte
+// alignment and spreads rows over the 32 banks.
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace lapnys {
+
+constexpr int kTile = 64;      // tokens per token block == landmarks per landmark tile
+constexpr int kThreads = 256;  // threads per CTA for the tile kernels
+constexpr int kPad = 4;        // row padding (floats) of shared-memory tiles
+
+__host__ __device__ constexpr int row_stride(int D) { return D + kPad; }
+__host__ __device__ constexpr int tile_floats(int D) { return kTile * (D + kPad); }
+
+// ---- element loads/stores (4 consecutive elements) ------------------------
+__device__ __forceinline__ float4 ld4(const float* p) {
+  return __ldg(reinterpret_cast<const float4*>(p));
+}
+__device__ __forceinline__ float4 ld4(const __nv_bfloat16* p) {
+  uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+  // bf16 -> fp32 is exact: the bf16 bits are the high half of the fp32 bits
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+}
+__device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ void st4(__nv_bfloat16* p, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+  __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&a);
+  u.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+__device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float comp(const float4& v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+// Load rows [row0, row0 + 64) of a row-major [nrows][D] matrix into a padded
+// shared tile; rows at or beyond nrows are zero-filled.
+template <int D, typename T>
+__device__ __forceinline__ void load_tile(float* s, const T* g, int row0, int nrows) {
+  constexpr int C4 = D / 4;
+  for (int id = threadIdx.x; id < kTile * C4; id += kThreads) {
+    const int r = id / C4, c = (id % C4) * 4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row0 + r < nrows) v = ld4(g + (size_t)(row0 + r) * D + c);
+    st4(s + r * row_stride(D) + c, v);
+  }
+}
+
+// Register-blocked L1 distances between 4 token rows (j = 4*ty + r) and 4
+// landmark rows (a = tx + 16*s) of two shared tiles:
+//   dist[r][s] = sum_c |X[j][c] - L[a][c]|   (c ascending)
+template <int D>
+__device__ __forceinline__ void dist_tile(const float* __restrict__ Xs, const float* __restrict__ Ls,
+                                          float dist[4][4]) {
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int s = 0; s < 4; ++s) dist[r][s] = 0.f;
+#pragma unroll 4
+  for (int c = 0; c < D; c += 4) {
+    float4 x[4], l[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) x[r] = lds4(Xs + (4 * ty + r) * row_stride(D) + c);
+#pragma unroll
+    for (int s = 0; s < 4; ++s) l[s] = lds4(Ls + (tx + 16 * s) * row_stride(D) + c);
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        dist[r][s] += fabsf(x[r].x - l[s].x);
+        dist[r][s] += fabsf(x[r].y - l[s].y);
+        dist[r][s] += fabsf(x[r].z - l[s].z);
+        dist[r][s] += fabsf(x[r].w - l[s].w);
+      }
+  }
+}
+
+// sgn(t) * g with sgn(0) = 0
+__device__ __forceinline__ float sgn_times(float t, float g) {
+  return t > 0.f ? g : (t < 0.f ? -g : 0.f);
+}
+
+}  // namespace lapnys

@@ -1,0 +1,108 @@
+// Host-side internals of liblapnys: problem description, launch wrapper with
+// launch counting and optional per-launch CUDA-event timing, and the launch
+// functions each translation unit provides.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace lapnys {
+
+struct Prob {
+  int B, H, BH, N, d, gh, gw, m, r, sh, sw, iters, tied, dtype;
+  unsigned flags;
+  float lam, eps;
+  float ns;       // -log2(e) / lambda: k = exp2(ns * distance)
+  float inv_lam;  // 1 / lambda
+  int nt;         // landmark tiles of 64
+  int mp;         // nt * 64
+  int nblk;       // token blocks of 64
+  int Sk, Sq, Sb; // token splits of the key pass, statistics pass, backward passes
+  bool norm() const { return flags & 1u; }
+};
+
+// ---- instrumentation -------------------------------------------------------
+int prof_begin(const char* name, cudaStream_t s);
+void prof_end(int slot, cudaStream_t s);
+void count_launch();
+
+template <typename Kern, typename... Args>
+inline cudaError_t launch(const char* name, Kern kern, dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t st, Args... args) {
+  const int slot = prof_begin(name, st);
+  kern<<<grid, block, smem, st>>>(args...);
+  cudaError_t e = cudaGetLastError();
+  prof_end(slot, st);
+  count_launch();
+  return e;
+}
+
+// opt a kernel into more than 48 KB of dynamic shared memory (once per kernel)
+template <typename Kern>
+inline cudaError_t allow_smem(Kern kern, size_t bytes) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+// ---- launchers (return the first CUDA error, cudaSuccess otherwise) -------
+// landmarks: L [BH][m][d] f32, idx [N] int32 (may be null)
+cudaError_t run_pool(const Prob& p, const void* k, float* L, int32_t* idx, cudaStream_t st);
+
+// gram + alpha + Newton-Schulz, m <= 64: one CTA per slice, everything on chip.
+// X has nx slots per slice, Y ny slots; slot of iterate t is t % nx (t % ny).
+cudaError_t run_ns_small(const Prob& p, const float* L, float* A, float* alpha, float* X,
+                         float* Y, int nx, int ny, cudaStream_t st);
+// gram tiles for any m: A = k(L, L) + eps I
+cudaError_t run_gram(const Prob& p, const float* L, float* A, cudaStream_t st);
+// alpha = 1 / (|A|_1 |A|_inf) and X_0 = alpha A
+cudaError_t run_alpha(const Prob& p, const float* A, float* alpha, float* X0, long x_bstride,
+                      cudaStream_t st);
+
+// batched C[b] = alpha op(A[b]) op(B[b]) + beta E[b] (fp32, row-major)
+cudaError_t run_bgemm(bool ta, bool tb, int batch, int M, int N, int K, const float* A, int lda,
+                      long sA, const float* B, int ldb, long sB, float* C, int ldc, long sC,
+                      const float* E, int lde, long sE, float alpha, float beta, cudaStream_t st);
+
+// forward passes
+cudaError_t run_key_fwd(const Prob& p, const void* k, const void* v, const float* L, float* part,
+                        cudaStream_t st);
+cudaError_t run_reduce_parts(int BH, int S, int m, int mp, int d, const float* part, float* out,
+                             cudaStream_t st);
+cudaError_t run_qstats(const Prob& p, const void* q, const float* L, float* spart, cudaStream_t st);
+cudaError_t run_stats_final(const Prob& p, const float* spart, float* stats, cudaStream_t st);
+cudaError_t run_query_fwd(const Prob& p, const void* q, const float* L, const float* What,
+                          const float* stats, void* out, cudaStream_t st);
+
+// backward
+// mode 0: query side statistics pass (LAPNYS_NORM only): dWhat and sum dZ, sum dZ*Z partials
+// mode 1: query side gradients: dQ partials per landmark tile, dL partials, (no norm) dWhat partials
+// mode 2: key side gradients: dK, dV partials per landmark tile, dL partials
+struct BwdArgs {
+  const void* X;      // q (modes 0, 1) or k (mode 2)
+  const void* U;      // dout (modes 0, 1) or v (mode 2)
+  const float* L;     // landmarks
+  const float* R;     // What (modes 0, 1) or dW (mode 2)
+  const float* stats; // mu, var, rs [BH][3][m] (norm)
+  const float* mdz;   // [BH][2][mp] mean dZ, mean dZ*Z (norm, mode 1)
+  float* tok_part;    // [nt][BH][N][d]: dQ (mode 1) or dK (mode 2)
+  float* tok_part2;   // [nt][BH][N][d]: dV (mode 2)
+  float* lm_part;     // [BH][S][mp][d]: dL
+  float* lm_part2;    // [BH][S][mp][d]: dWhat (modes 0, 1)
+  float* ns_part;     // [BH][S][2][mp]: sum dZ, sum dZ*Z (mode 0)
+};
+cudaError_t run_bwd_tile(const Prob& p, int mode, const BwdArgs& a, cudaStream_t st);
+cudaError_t run_mdz(const Prob& p, const float* ns_part, float* mdz, cudaStream_t st);
+cudaError_t run_gram_bwd(const Prob& p, const float* L, const float* A, const float* dA, float* dLA,
+                         cudaStream_t st);
+// Newton-Schulz backward for m <= 64 (full ctx: iters + 1 iterates, iters products);
+// GT = dLoss/dX_T; writes dA including the alpha term
+cudaError_t run_ns_bwd_small(const Prob& p, const float* A, const float* alpha, const float* X,
+                             const float* Y, const float* GT, float* dA, cudaStream_t st);
+cudaError_t run_alpha_bwd(const Prob& p, const float* A, const float* alpha, const float* G,
+                          float* dA, cudaStream_t st);
+cudaError_t run_reduce_dl(const Prob& p, const float* dLq, const float* dLc, const float* dLA,
+                          float* dL, cudaStream_t st);
+cudaError_t run_zero(float* x, size_t n, cudaStream_t st);
+cudaError_t run_finalize(const Prob& p, const float* dQp, const float* dKp, const float* dVp,
+                         const float* dL, void* dq, void* dk, void* dv, cudaStream_t st);
+
+}  // namespace lapnys

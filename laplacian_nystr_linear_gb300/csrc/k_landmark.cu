@@ -1,0 +1,527 @@
+// Landmark-side kernels: average-pool landmarks, the landmark matrix
+// A = k(L, L) + eps I, the Newton-Schulz scale alpha, the on-chip Newton-Schulz
+// solver for m <= 64, and their backward counterparts.
+//
+// Passages: landmarks are keys chosen by average pooling ("LaplacianFormer",
+// Arabic summary 2c.1; "SOFT" review, Proposed method); the landmark matrix is
+// inverted by Newton-Schulz, A_0 = alpha A, A_{k+1} = 2 A_k - A_k A A_k
+// ("SOFT" review, Proposed method; "LaplacianFormer" Dutch summary,
+// Methodology 2), after adding a small eps I (same passages).
+#include "common.cuh"
+#include "internal.h"
+
+namespace lapnys {
+
+// ---------------------------------------------------------------------------
+// pooling: one CTA per (landmark, slice); threads = (token group, 4-wide chunk)
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kThreads) k_pool(const T* __restrict__ K, float* __restrict__ L,
+                                                   int32_t* __restrict__ idx, int N, int d, int gw,
+                                                   int r, int sh, int sw, int m) {
+  __shared__ float4 red[kThreads];
+  const int a = blockIdx.x, bh = blockIdx.y;
+  const int wi = a / r, wj = a % r;
+  const int C4 = d / 4, groups = kThreads / C4;
+  const int chunk = threadIdx.x % C4, g = threadIdx.x / C4;
+  const int wsz = sh * sw;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const T* Kb = K + (size_t)bh * N * d;
+  for (int t = g; t < wsz; t += groups) {
+    const int n = (wi * sh + t / sw) * gw + wj * sw + t % sw;
+    const float4 v = ld4(Kb + (size_t)n * d + chunk * 4);
+    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+  }
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  if (threadIdx.x < C4) {
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < groups; ++q) {
+      const float4 v = red[q * C4 + threadIdx.x];
+      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    }
+    const float inv = 1.0f / (float)wsz;
+    st4(L + ((size_t)bh * m + a) * d + threadIdx.x * 4,
+        make_float4(s.x * inv, s.y * inv, s.z * inv, s.w * inv));
+  }
+  if (idx != nullptr && bh == 0)
+    for (int t = threadIdx.x; t < wsz; t += kThreads)
+      idx[(wi * sh + t / sw) * gw + wj * sw + t % sw] = a;
+}
+
+cudaError_t run_pool(const Prob& p, const void* k, float* L, int32_t* idx, cudaStream_t st) {
+  dim3 grid(p.m, p.BH);
+  if (p.dtype == 1)
+    return launch("pool", k_pool<__nv_bfloat16>, grid, dim3(kThreads), 0, st,
+                  (const __nv_bfloat16*)k, L, idx, p.N, p.d, p.gw, p.r, p.sh, p.sw, p.m);
+  return launch("pool", k_pool<float>, grid, dim3(kThreads), 0, st, (const float*)k, L, idx, p.N,
+                p.d, p.gw, p.r, p.sh, p.sw, p.m);
+}
+
+// ---------------------------------------------------------------------------
+// 64 x 64 shared-memory matrix products for the on-chip solver.
+// Thread (ty, tx) owns rows i = 4 ty + r and columns j = col(s):
+//   TB == false: j = 4 tx + s   (B read as [k][j])
+//   TB == true : j = tx + 16 s  (B read as [j][k], interleaved to avoid bank conflicts)
+// op(A) is A[i][k] (TA == false) or A[k][i] (TA == true).  Stride 68 floats.
+// ---------------------------------------------------------------------------
+constexpr int kMS = 68;
+
+template <bool TB>
+__device__ __forceinline__ int mcol(int s) {
+  const int tx = threadIdx.x & 15;
+  return TB ? tx + 16 * s : 4 * tx + s;
+}
+
+template <bool TA, bool TB>
+__device__ __forceinline__ void mm64(const float* __restrict__ A, const float* __restrict__ B, int K,
+                                     float acc[4][4]) {
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int s = 0; s < 4; ++s) acc[r][s] = 0.f;
+  for (int k = 0; k < K; k += 4) {
+    float a[4][4], b[4][4];  // a[r][kk], b[kk][s]
+    if (!TA) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float4 v = lds4(A + (4 * ty + r) * kMS + k);
+        a[r][0] = v.x; a[r][1] = v.y; a[r][2] = v.z; a[r][3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const float4 v = lds4(A + (k + kk) * kMS + 4 * ty);
+        a[0][kk] = v.x; a[1][kk] = v.y; a[2][kk] = v.z; a[3][kk] = v.w;
+      }
+    }
+    if (!TB) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const float4 v = lds4(B + (k + kk) * kMS + 4 * tx);
+        b[kk][0] = v.x; b[kk][1] = v.y; b[kk][2] = v.z; b[kk][3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const float4 v = lds4(B + (tx + 16 * s) * kMS + k);
+        b[0][s] = v.x; b[1][s] = v.y; b[2][s] = v.z; b[3][s] = v.w;
+      }
+    }
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int s = 0; s < 4; ++s) acc[r][s] = fmaf(a[r][kk], b[kk][s], acc[r][s]);
+  }
+}
+
+// load an m x m row-major global matrix into a zero-padded 64 x 68 tile
+__device__ __forceinline__ void load_mat(float* s, const float* g, int m) {
+  for (int e = threadIdx.x; e < 64 * 64; e += kThreads) {
+    const int i = e >> 6, j = e & 63;
+    s[i * kMS + j] = (i < m && j < m) ? g[i * m + j] : 0.f;
+  }
+}
+__device__ __forceinline__ void store_mat(float* g, const float* s, int m) {
+  for (int e = threadIdx.x; e < m * m; e += kThreads) g[e] = s[(e / m) * kMS + e % m];
+}
+
+// alpha = 1 / (|A|_1 |A|_inf) of the m x m tile in shared memory; writes the
+// info record {alpha, |A|_1, |A|_inf, argmax column (int bits)}.
+__device__ void alpha_of_tile(const float* As, int m, float* info_g, float* alpha_s) {
+  __shared__ float csum[64], rsum[64];
+  if (threadIdx.x < 64) {
+    float cs = 0.f, rs = 0.f;
+    if (threadIdx.x < m)
+      for (int i = 0; i < m; ++i) {
+        cs += As[i * kMS + threadIdx.x];
+        rs += As[threadIdx.x * kMS + i];
+      }
+    csum[threadIdx.x] = cs;
+    rsum[threadIdx.x] = rs;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int jc = 0, ir = 0;
+    for (int i = 1; i < m; ++i) {
+      if (csum[i] > csum[jc]) jc = i;
+      if (rsum[i] > rsum[ir]) ir = i;
+    }
+    const float n1 = csum[jc], ninf = rsum[ir];
+    const float al = 1.0f / (n1 * ninf);
+    *alpha_s = al;
+    info_g[0] = al;
+    info_g[1] = n1;
+    info_g[2] = ninf;
+    info_g[3] = __int_as_float(jc | (ir << 16));
+  }
+  __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// gram + alpha + Newton-Schulz for m <= 64: one CTA per slice
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(kThreads) k_ns_small(const float* __restrict__ L, float* __restrict__ A,
+                                                       float* __restrict__ alpha, float* __restrict__ X,
+                                                       float* __restrict__ Y, int m, int iters, int nx,
+                                                       int ny, float ns, float eps) {
+  extern __shared__ float4 sm4[];
+  float* Ls = reinterpret_cast<float*>(sm4);
+  float* As = Ls + tile_floats(D);
+  float* Xa = As + 64 * kMS;
+  float* Xb = Xa + 64 * kMS;
+  float* Ys = Xb + 64 * kMS;
+  __shared__ float al_s;
+  const int bh = blockIdx.x;
+  const int ty = threadIdx.x >> 4;
+  const size_t mm = (size_t)m * m;
+
+  load_tile<D>(Ls, L + (size_t)bh * m * D, 0, m);
+  __syncthreads();
+  {
+    float dist[4][4];
+    dist_tile<D>(Ls, Ls, dist);
+    const int tx = threadIdx.x & 15;
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const int i = 4 * ty + r, j = tx + 16 * s;
+        float v = 0.f;
+        if (i < m && j < m) v = exp2f(dist[r][s] * ns) + (i == j ? eps : 0.f);
+        As[i * kMS + j] = v;
+      }
+  }
+  __syncthreads();
+  store_mat(A + bh * mm, As, m);
+  alpha_of_tile(As, m, alpha + (size_t)bh * 4, &al_s);
+  const float al = al_s;
+  for (int e = threadIdx.x; e < 64 * 64; e += kThreads) {
+    const int i = e >> 6, j = e & 63;
+    Xa[i * kMS + j] = al * As[i * kMS + j];
+  }
+  __syncthreads();
+  store_mat(X + (size_t)bh * nx * mm, Xa, m);
+  const int K = (m + 3) & ~3;
+  for (int t = 0; t < iters; ++t) {
+    float acc[4][4];
+    mm64<false, false>(As, Xa, K, acc);  // Y_t = A X_t
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int s = 0; s < 4; ++s) Ys[(4 * ty + r) * kMS + mcol<false>(s)] = acc[r][s];
+    __syncthreads();
+    store_mat(Y + ((size_t)bh * ny + t % ny) * mm, Ys, m);
+    mm64<false, false>(Xa, Ys, K, acc);  // X_{t+1} = 2 X_t - X_t Y_t
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const int o = (4 * ty + r) * kMS + mcol<false>(s);
+        Xb[o] = 2.f * Xa[o] - acc[r][s];
+      }
+    __syncthreads();
+    store_mat(X + ((size_t)bh * nx + (t + 1) % nx) * mm, Xb, m);
+    float* tmp = Xa; Xa = Xb; Xb = tmp;
+  }
+}
+
+cudaError_t run_ns_small(const Prob& p, const float* L, float* A, float* alpha, float* X, float* Y,
+                         int nx, int ny, cudaStream_t st) {
+#define NS_SMALL_CASE(DD)                                                                   \
+  case DD: {                                                                                \
+    const size_t smem = (size_t)(tile_floats(DD) + 4 * 64 * kMS) * sizeof(float);           \
+    static bool once = (allow_smem(k_ns_small<DD>, smem), true);                            \
+    (void)once;                                                                             \
+    return launch("ns_small", k_ns_small<DD>, dim3(p.BH), dim3(kThreads), smem, st, L, A,   \
+                  alpha, X, Y, p.m, p.iters, nx, ny, p.ns, p.eps);                          \
+  }
+  switch (p.d) {
+    NS_SMALL_CASE(16)
+    NS_SMALL_CASE(32)
+    NS_SMALL_CASE(64)
+    NS_SMALL_CASE(128)
+  }
+#undef NS_SMALL_CASE
+  return cudaErrorInvalidValue;
+}
+
+
+// ---------------------------------------------------------------------------
+// gram tiles for any m: grid (column tile, row tile, slice)
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(kThreads) k_gram(const float* __restrict__ L, float* __restrict__ A,
+                                                   int m, float ns, float eps) {
+  extern __shared__ float4 sm4[];
+  float* Xs = reinterpret_cast<float*>(sm4);
+  float* Ls = Xs + tile_floats(D);
+  const int it = blockIdx.y, jt = blockIdx.x, bh = blockIdx.z;
+  const float* Lb = L + (size_t)bh * m * D;
+  load_tile<D>(Xs, Lb, it * 64, m);
+  load_tile<D>(Ls, Lb, jt * 64, m);
+  __syncthreads();
+  float dist[4][4];
+  dist_tile<D>(Xs, Ls, dist);
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const int i = it * 64 + 4 * ty + r, j = jt * 64 + tx + 16 * s;
+      if (i < m && j < m)
+        A[((size_t)bh * m + i) * m + j] = exp2f(dist[r][s] * ns) + (i == j ? eps : 0.f);
+    }
+}
+
+cudaError_t run_gram(const Prob& p, const float* L, float* A, cudaStream_t st) {
+  dim3 grid(p.nt, p.nt, p.BH);
+#define GRAM_CASE(DD)                                                                        \
+  case DD: {                                                                                 \
+    const size_t smem = 2 * (size_t)tile_floats(DD) * sizeof(float);                         \
+    static bool once = (allow_smem(k_gram<DD>, smem), true);                                 \
+    (void)once;                                                                              \
+    return launch("gram", k_gram<DD>, grid, dim3(kThreads), smem, st, L, A, p.m, p.ns, p.eps); \
+  }
+  switch (p.d) {
+    GRAM_CASE(16)
+    GRAM_CASE(32)
+    GRAM_CASE(64)
+    GRAM_CASE(128)
+  }
+#undef GRAM_CASE
+  return cudaErrorInvalidValue;
+}
+
+// ---------------------------------------------------------------------------
+// alpha for any m (m <= 1024): one CTA per slice; also X_0 = alpha A
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) k_alpha(const float* __restrict__ A, float* __restrict__ info,
+                                                    float* __restrict__ X0, long x_bstride, int m) {
+  __shared__ float csum[1024], rsum[1024];
+  __shared__ float al_s;
+  const int bh = blockIdx.x;
+  const float* Ab = A + (size_t)bh * m * m;
+  for (int j = threadIdx.x; j < m; j += kThreads) {
+    float cs = 0.f, rs = 0.f;
+    for (int i = 0; i < m; ++i) {
+      cs += Ab[(size_t)i * m + j];
+      rs += Ab[(size_t)j * m + i];
+    }
+    csum[j] = cs;
+    rsum[j] = rs;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int jc = 0, ir = 0;
+    for (int i = 1; i < m; ++i) {
+      if (csum[i] > csum[jc]) jc = i;
+      if (rsum[i] > rsum[ir]) ir = i;
+    }
+    const float n1 = csum[jc], ninf = rsum[ir];
+    const float al = 1.0f / (n1 * ninf);
+    al_s = al;
+    float* o = info + (size_t)bh * 4;
+    o[0] = al;
+    o[1] = n1;
+    o[2] = ninf;
+    o[3] = __int_as_float(jc | (ir << 16));
+  }
+  __syncthreads();
+  const float al = al_s;
+  float* Xb = X0 + (size_t)bh * x_bstride;
+  for (int e = threadIdx.x; e < m * m; e += kThreads) Xb[e] = al * Ab[e];
+}
+
+cudaError_t run_alpha(const Prob& p, const float* A, float* alpha, float* X0, long x_bstride,
+                      cudaStream_t st) {
+  return launch("alpha", k_alpha, dim3(p.BH), dim3(kThreads), 0, st, A, alpha, X0, x_bstride, p.m);
+}
+
+// ---------------------------------------------------------------------------
+// backward of A = k(L, L) + eps I:
+//   dL_A[a][c] = -(1/lambda) sum_{b != a} (dA_ab + dA_ba) A_ab sgn(L_ac - L_bc)
+// block = (D columns) x (256 / D landmarks); grid (landmark groups, slice)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) k_gram_bwd(const float* __restrict__ L, const float* __restrict__ A,
+                                                       const float* __restrict__ dA, float* __restrict__ dLA,
+                                                       int m, int d, float inv_lam) {
+  const int lpb = kThreads / d;
+  const int c = threadIdx.x % d;
+  const int a = blockIdx.x * lpb + threadIdx.x / d;
+  const int bh = blockIdx.y;
+  if (a >= m) return;
+  const float* Lb = L + (size_t)bh * m * d;
+  const float* Ab = A + (size_t)bh * m * m;
+  const float* dAb = dA + (size_t)bh * m * m;
+  const float la = Lb[(size_t)a * d + c];
+  float s = 0.f;
+  for (int b = 0; b < m; ++b) {
+    if (b == a) continue;
+    const float w = (dAb[(size_t)a * m + b] + dAb[(size_t)b * m + a]) * Ab[(size_t)a * m + b];
+    s += sgn_times(la - Lb[(size_t)b * d + c], w);
+  }
+  dLA[((size_t)bh * m + a) * d + c] = -inv_lam * s;
+}
+
+cudaError_t run_gram_bwd(const Prob& p, const float* L, const float* A, const float* dA, float* dLA,
+                         cudaStream_t st) {
+  const int lpb = kThreads / p.d;
+  dim3 grid((p.m + lpb - 1) / lpb, p.BH);
+  return launch("gram_bwd", k_gram_bwd, grid, dim3(kThreads), 0, st, L, A, dA, dLA, p.m, p.d,
+                p.inv_lam);
+}
+
+// ---------------------------------------------------------------------------
+// Newton-Schulz backward for m <= 64, one CTA per slice, all on chip.
+// Reverse of X_{t+1} = 2 X_t - X_t A X_t with upstream G = dLoss/dX_{t+1}:
+//   dA  -= X_t^T G X_t^T
+//   G    = 2 G - G Y_t^T - A^T (X_t^T G)          (Y_t = A X_t)
+// then X_0 = alpha A contributes alpha G and, through alpha = 1/(n1 ninf),
+// dalpha = <G, A> spread over the maximising column (n1) and row (ninf).
+// GT holds dLoss/dX_T on entry.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) k_ns_bwd_small(const float* __restrict__ A,
+                                                           const float* __restrict__ info,
+                                                           const float* __restrict__ X,
+                                                           const float* __restrict__ Y,
+                                                           const float* __restrict__ GT,
+                                                           float* __restrict__ dA, int m, int iters,
+                                                           int nx, int ny) {
+  extern __shared__ float4 sm4[];
+  float* As = reinterpret_cast<float*>(sm4);
+  float* Xt = As + 64 * kMS;
+  float* Yt = Xt + 64 * kMS;
+  float* G = Yt + 64 * kMS;
+  float* XG = G + 64 * kMS;
+  float* dAs = XG + 64 * kMS;
+  float* Tm = dAs + 64 * kMS;
+  __shared__ float red[kThreads];
+  const int bh = blockIdx.x;
+  const int ty = threadIdx.x >> 4;
+  const size_t mm = (size_t)m * m;
+  const int K = (m + 3) & ~3;
+
+  load_mat(As, A + bh * mm, m);
+  load_mat(G, GT + bh * mm, m);
+  for (int e = threadIdx.x; e < 64 * kMS; e += kThreads) dAs[e] = 0.f;
+  float acc[4][4];
+  for (int t = iters - 1; t >= 0; --t) {
+    load_mat(Xt, X + ((size_t)bh * nx + t % nx) * mm, m);
+    load_mat(Yt, Y + ((size_t)bh * ny + t % ny) * mm, m);
+    __syncthreads();
+    mm64<true, false>(Xt, G, K, acc);  // XG = X_t^T G
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int s = 0; s < 4; ++s) XG[(4 * ty + r) * kMS + mcol<false>(s)] = acc[r][s];
+    __syncthreads();
+    mm64<false, true>(XG, Xt, K, acc);  // dA -= XG X_t^T
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int s = 0; s < 4; ++s) dAs[(4 * ty + r) * kMS + mcol<true>(s)] -= acc[r][s];
+    mm64<false, true>(G, Yt, K, acc);  // Tm = 2 G - G Y_t^T
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const int o = (4 * ty + r) * kMS + mcol<true>(s);
+        Tm[o] = 2.f * G[o] - acc[r][s];
+      }
+    __syncthreads();
+    mm64<true, false>(As, XG, K, acc);  // G = Tm - A^T XG
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const int o = (4 * ty + r) * kMS + mcol<false>(s);
+        G[o] = Tm[o] - acc[r][s];
+      }
+    __syncthreads();
+  }
+  // X_0 = alpha A
+  const float* in = info + (size_t)bh * 4;
+  const float al = in[0], n1 = in[1], ninf = in[2];
+  const int code = __float_as_int(in[3]);
+  const int jc = code & 0xffff, ir = code >> 16;
+  float part = 0.f;
+  for (int e = threadIdx.x; e < 64 * 64; e += kThreads) {
+    const int o = (e >> 6) * kMS + (e & 63);
+    part += G[o] * As[o];
+  }
+  red[threadIdx.x] = part;
+  __syncthreads();
+  for (int w = kThreads / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  const float dal = red[0];
+  for (int e = threadIdx.x; e < 64 * 64; e += kThreads) {
+    const int i = e >> 6, j = e & 63;
+    const int o = i * kMS + j;
+    float v = dAs[o] + al * G[o];
+    if (j == jc) v += dal * (-al / n1);
+    if (i == ir) v += dal * (-al / ninf);
+    dAs[o] = v;
+  }
+  __syncthreads();
+  store_mat(dA + bh * mm, dAs, m);
+}
+
+cudaError_t run_ns_bwd_small(const Prob& p, const float* A, const float* alpha, const float* X,
+                             const float* Y, const float* GT, float* dA, cudaStream_t st) {
+  const size_t smem = 7 * 64 * kMS * sizeof(float);
+  static bool once = (allow_smem(k_ns_bwd_small, smem), true);
+  (void)once;
+  return launch("ns_bwd_small", k_ns_bwd_small, dim3(p.BH), dim3(kThreads), smem, st, A, alpha, X,
+                Y, GT, dA, p.m, p.iters, p.iters + 1, p.iters);
+}
+
+// ---------------------------------------------------------------------------
+// alpha part of the Newton-Schulz backward for any m: one CTA per slice.
+//   dA += alpha G;  dalpha = <G, A>;  dA[:, j*] += dalpha (-alpha / n1);
+//   dA[i*, :] += dalpha (-alpha / ninf)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) k_alpha_bwd(const float* __restrict__ A,
+                                                        const float* __restrict__ info,
+                                                        const float* __restrict__ G,
+                                                        float* __restrict__ dA, int m) {
+  __shared__ float red[kThreads];
+  const int bh = blockIdx.x;
+  const size_t mm = (size_t)m * m;
+  const float* Ab = A + bh * mm;
+  const float* Gb = G + bh * mm;
+  float* dAb = dA + bh * mm;
+  float part = 0.f;
+  for (size_t e = threadIdx.x; e < mm; e += kThreads) part += Gb[e] * Ab[e];
+  red[threadIdx.x] = part;
+  __syncthreads();
+  for (int w = kThreads / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  const float dal = red[0];
+  const float* in = info + (size_t)bh * 4;
+  const float al = in[0], n1 = in[1], ninf = in[2];
+  const int code = __float_as_int(in[3]);
+  const int jc = code & 0xffff, ir = code >> 16;
+  for (size_t e = threadIdx.x; e < mm; e += kThreads) {
+    const int i = (int)(e / m), j = (int)(e % m);
+    float v = dAb[e] + al * Gb[e];
+    if (j == jc) v += dal * (-al / n1);
+    if (i == ir) v += dal * (-al / ninf);
+    dAb[e] = v;
+  }
+}
+
+cudaError_t run_alpha_bwd(const Prob& p, const float* A, const float* alpha, const float* G,
+                          float* dA, cudaStream_t st) {
+  return launch("alpha_bwd", k_alpha_bwd, dim3(p.BH), dim3(kThreads), 0, st, A, alpha, G, dA, p.m);
+}
+
+}  // namespace lapnys

@@ -1,0 +1,763 @@
+// Token-side passes of Laplacian-kernel Nystrom attention: the fused
+// L1-distance + exp tiles that never write the N x m kernel matrices to HBM.
+//
+//   key pass      W   = C V,     C_aj = k(L_a, K_j)                (forward)
+//   stats pass    mu, var of P_ia = k(Q_i, L_a) per landmark column (forward, norm)
+//   query pass    O   = Z W-hat, Z = P or (P - mu) / sqrt(var + eta)   (forward)
+//   tile backward dQ, dK, dV, dL, dW-hat through sgn(x - l)          (backward)
+//
+// Passages: the Laplacian kernel k(x, y) = exp(-|x - y|_1 / lambda) and its
+// non-vanishing L1 gradient ("LaplacianFormer", Dutch summary Methodology 1;
+// Arabic summary 2a); the Nystrom product S-hat = P^T A^+ P ("SOFT" review,
+// Proposed method) read as O = k(Q, L) A^+ (k(L, K) V); the normalised query
+// feature map with a diagonal variance estimate (Arabic summary 2b).
+//
+// The distance is not a dot product, so it runs on the FP32 pipe: each thread
+// holds a 4 x 4 (token x landmark) block of distances and streams the feature
+// dimension through shared memory in float4 steps (32 ALU ops per 2 LDS.128).
+#include "common.cuh"
+#include "internal.h"
+
+namespace lapnys {
+
+// ---- CPT-wide (D / 16 columns per thread) shared loads and global stores --
+template <int CPT>
+__device__ __forceinline__ void lds_cpt(const float* p, float (&v)[CPT]) {
+  if constexpr (CPT % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < CPT; i += 4) {
+      const float4 t = lds4(p + i);
+      v[i] = t.x; v[i + 1] = t.y; v[i + 2] = t.z; v[i + 3] = t.w;
+    }
+  } else if constexpr (CPT == 2) {
+    const float2 t = *reinterpret_cast<const float2*>(p);
+    v[0] = t.x; v[1] = t.y;
+  } else {
+    v[0] = p[0];
+  }
+}
+
+template <int CPT>
+__device__ __forceinline__ void st_cpt(float* p, const float (&v)[CPT]) {
+#pragma unroll
+  for (int i = 0; i < CPT; ++i) p[i] = v[i];
+}
+template <int CPT>
+__device__ __forceinline__ void st_cpt(__nv_bfloat16* p, const float (&v)[CPT]) {
+#pragma unroll
+  for (int i = 0; i < CPT; ++i) p[i] = __float2bfloat16_rn(v[i]);
+}
+
+__device__ __forceinline__ void split_range(int nblk, int S, int s, int& b0, int& b1) {
+  b0 = (int)((long long)nblk * s / S);
+  b1 = (int)((long long)nblk * (s + 1) / S);
+}
+
+template <typename T>
+struct TypeOf;
+template <>
+struct TypeOf<float> { static constexpr int id = 0; };
+template <>
+struct TypeOf<__nv_bfloat16> { static constexpr int id = 1; };
+
+// ===========================================================================
+// key pass: grid (landmark tile, split, slice).  Each CTA keeps its 64
+// landmarks in shared memory, streams its share of the key/value tokens in
+// blocks of 64 and accumulates W[a][c] = sum_j C_aj V_jc in registers.
+// ===========================================================================
+template <int D, typename T>
+__global__ void __launch_bounds__(kThreads, 2)
+    k_key_fwd(const T* __restrict__ K, const T* __restrict__ V, const float* __restrict__ L,
+              float* __restrict__ part, int N, int m, int mp, int S, int nblk, float ns) {
+  constexpr int CPT = D / 16;
+  extern __shared__ float4 sm4[];
+  float* Ls = reinterpret_cast<float*>(sm4);
+  float* Xs = Ls + tile_floats(D);
+  float* Vs = Xs + tile_floats(D);
+  float* Cs = Vs + tile_floats(D);  // [64 tokens][68]
+  const int lt = blockIdx.x, sp = blockIdx.y, bh = blockIdx.z;
+  const int a0 = lt * kTile;
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+  const T* Kb = K + (size_t)bh * N * D;
+  const T* Vb = V + (size_t)bh * N * D;
+  load_tile<D>(Ls, L + (size_t)bh * m * D, a0, m);
+  float w[4][CPT];
+#pragma unroll
+  for (int s = 0; s < 4; ++s)
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) w[s][c] = 0.f;
+  int b0, b1;
+  split_range(nblk, S, sp, b0, b1);
+  for (int b = b0; b < b1; ++b) {
+    __syncthreads();
+    load_tile<D>(Xs, Kb, b * kTile, N);
+    load_tile<D>(Vs, Vb, b * kTile, N);
+    __syncthreads();
+    float dist[4][4];
+    dist_tile<D>(Xs, Ls, dist);
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const int j = b * kTile + 4 * ty + r, a = a0 + tx + 16 * s;
+        Cs[(4 * ty + r) * 68 + tx + 16 * s] = (j < N && a < m) ? exp2f(dist[r][s] * ns) : 0.f;
+      }
+    __syncthreads();
+#pragma unroll 4
+    for (int j = 0; j < kTile; ++j) {
+      const float4 c4 = lds4(Cs + j * 68 + 4 * ty);
+      float v[CPT];
+      lds_cpt<CPT>(Vs + j * row_stride(D) + tx * CPT, v);
+#pragma unroll
+      for (int c = 0; c < CPT; ++c) {
+        w[0][c] = fmaf(c4.x, v[c], w[0][c]);
+        w[1][c] = fmaf(c4.y, v[c], w[1][c]);
+        w[2][c] = fmaf(c4.z, v[c], w[2][c]);
+        w[3][c] = fmaf(c4.w, v[c], w[3][c]);
+      }
+    }
+  }
+  float* P = part + (((size_t)bh * S + sp) * mp + a0 + 4 * ty) * D + tx * CPT;
+#pragma unroll
+  for (int s = 0; s < 4; ++s) st_cpt<CPT>(P + s * D, w[s]);
+}
+
+template <int D, typename T>
+static cudaError_t key_fwd_t(const Prob& p, const void* k, const void* v, const float* L, float* part,
+                             cudaStream_t st) {
+  const size_t smem = (3 * (size_t)tile_floats(D) + 64 * 68) * sizeof(float);
+  static bool once = (allow_smem(k_key_fwd<D, T>, smem), true);
+  (void)once;
+  return launch("key_fwd", k_key_fwd<D, T>, dim3(p.nt, p.Sk, p.BH), dim3(kThreads), smem, st,
+                (const T*)k, (const T*)v, L, part, p.N, p.m, p.mp, p.Sk, p.nblk, p.ns);
+}
+
+#define DISPATCH_DT(FN, ...)                                                        \
+  do {                                                                              \
+    if (p.dtype == 1) {                                                             \
+      switch (p.d) {                                                                \
+        case 16: return FN<16, __nv_bfloat16>(__VA_ARGS__);                         \
+        case 32: return FN<32, __nv_bfloat16>(__VA_ARGS__);                         \
+        case 64: return FN<64, __nv_bfloat16>(__VA_ARGS__);                         \
+        case 128: return FN<128, __nv_bfloat16>(__VA_ARGS__);                       \
+      }                                                                             \
+    } else {                                                                        \
+      switch (p.d) {                                                                \
+        case 16: return FN<16, float>(__VA_ARGS__);                                 \
+        case 32: return FN<32, float>(__VA_ARGS__);                                 \
+        case 64: return FN<64, float>(__VA_ARGS__);                                 \
+        case 128: return FN<128, float>(__VA_ARGS__);                               \
+      }                                                                             \
+    }                                                                               \
+    return cudaErrorInvalidValue;                                                   \
+  } while (0)
+
+cudaError_t run_key_fwd(const Prob& p, const void* k, const void* v, const float* L, float* part,
+                        cudaStream_t st) {
+  DISPATCH_DT(key_fwd_t, p, k, v, L, part, st);
+}
+
+// ===========================================================================
+// out[bh][a][c] = sum_s part[bh][s][a][c]  (a < m; fixed order over s)
+// ===========================================================================
+__global__ void k_reduce_parts(const float* __restrict__ part, float* __restrict__ out, int BH, int S,
+                               int m, int mp, int d) {
+  const size_t total = (size_t)BH * m * d;
+  for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < total;
+       e += (size_t)gridDim.x * blockDim.x) {
+    const size_t bh = e / ((size_t)m * d);
+    const size_t ac = e % ((size_t)m * d);
+    const float* p = part + bh * S * mp * d + ac;
+    float s = 0.f;
+    for (int q = 0; q < S; ++q) s += p[(size_t)q * mp * d];
+    out[e] = s;
+  }
+}
+
+static int grid_for(size_t n) {
+  size_t g = (n + kThreads - 1) / kThreads;
+  return (int)(g < 4096 ? (g < 1 ? 1 : g) : 4096);
+}
+
+cudaError_t run_reduce_parts(int BH, int S, int m, int mp, int d, const float* part, float* out,
+                             cudaStream_t st) {
+  const size_t n = (size_t)BH * m * d;
+  return launch("reduce_parts", k_reduce_parts, dim3(grid_for(n)), dim3(kThreads), 0, st, part, out,
+                BH, S, m, mp, d);
+}
+
+// ===========================================================================
+// statistics pass (normalised feature map): per landmark column, the mean and
+// centred second moment of P_ia over the slice's queries.  Each 64-token block
+// gives an exact two-pass (count, mean, M2) that is merged into the running
+// triple with the pairwise update of Chan, Golub and LeVeque.
+// grid (landmark tile, split, slice); spart [BH][S][3][mp]
+// ===========================================================================
+__device__ __forceinline__ void chan_merge(float& n, float& mean, float& M2, float nb, float meanb,
+                                           float M2b) {
+  if (nb == 0.f) return;
+  const float nn = n + nb;
+  const float delta = meanb - mean;
+  mean += delta * (nb / nn);
+  M2 += M2b + delta * delta * (n * nb / nn);
+  n = nn;
+}
+
+template <int D, typename T>
+__global__ void __launch_bounds__(kThreads, 2)
+    k_qstats(const T* __restrict__ Q, const float* __restrict__ L, float* __restrict__ spart, int N,
+             int m, int mp, int S, int nblk, float ns) {
+  extern __shared__ float4 sm4[];
+  float* Ls = reinterpret_cast<float*>(sm4);
+  float* Xs = Ls + tile_floats(D);
+  float* Ps = Xs + tile_floats(D);  // [64 tokens][68]
+  const int lt = blockIdx.x, sp = blockIdx.y, bh = blockIdx.z;
+  const int a0 = lt * kTile;
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+  const T* Qb = Q + (size_t)bh * N * D;
+  load_tile<D>(Ls, L + (size_t)bh * m * D, a0, m);
+  float n = 0.f, mean = 0.f, M2 = 0.f;  // meaningful for threads 0..63 (landmark a0 + tid)
+  int b0, b1;
+  split_range(nblk, S, sp, b0, b1);
+  for (int b = b0; b < b1; ++b) {
+    __syncthreads();
+    load_tile<D>(Xs, Qb, b * kTile, N);
+    __syncthreads();
+    float dist[4][4];
+    dist_tile<D>(Xs, Ls, dist);
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int s = 0; s < 4; ++s) Ps[(4 * ty + r) * 68 + tx + 16 * s] = exp2f(dist[r][s] * ns);
+    __syncthreads();
+    if (threadIdx.x < kTile) {
+      const int nb = min(kTile, N - b * kTile);
+      float sum = 0.f;
+      for (int j = 0; j < nb; ++j) sum += Ps[j * 68 + threadIdx.x];
+      const float mb = sum / (float)nb;
+      float m2b = 0.f;
+      for (int j = 0; j < nb; ++j) {
+        const float dv = Ps[j * 68 + threadIdx.x] - mb;
+        m2b = fmaf(dv, dv, m2b);
+      }
+      chan_merge(n, mean, M2, (float)nb, mb, m2b);
+    }
+  }
+  if (threadIdx.x < kTile) {
+    float* o = spart + ((size_t)bh * S + sp) * 3 * mp + a0 + threadIdx.x;
+    o[0] = n;
+    o[mp] = mean;
+    o[2 * mp] = M2;
+  }
+}
+
+template <int D, typename T>
+static cudaError_t qstats_t(const Prob& p, const void* q, const float* L, float* spart,
+                            cudaStream_t st) {
+  const size_t smem = (2 * (size_t)tile_floats(D) + 64 * 68) * sizeof(float);
+  static bool once = (allow_smem(k_qstats<D, T>, smem), true);
+  (void)once;
+  return launch("qstats", k_qstats<D, T>, dim3(p.nt, p.Sq, p.BH), dim3(kThreads), smem, st,
+                (const T*)q, L, spart, p.N, p.m, p.mp, p.Sq, p.nblk, p.ns);
+}
+
+cudaError_t run_qstats(const Prob& p, const void* q, const float* L, float* spart, cudaStream_t st) {
+  DISPATCH_DT(qstats_t, p, q, L, spart, st);
+}
+
+// stats [BH][3][m]: mu, var (biased), 1 / sqrt(var + 1e-5)
+__global__ void k_stats_final(const float* __restrict__ spart, float* __restrict__ stats, int BH,
+                              int S, int m, int mp, int N) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= BH * m) return;
+  const int bh = e / m, a = e % m;
+  float n = 0.f, mean = 0.f, M2 = 0.f;
+  for (int s = 0; s < S; ++s) {
+    const float* o = spart + ((size_t)bh * S + s) * 3 * mp + a;
+    chan_merge(n, mean, M2, o[0], o[mp], o[2 * mp]);
+  }
+  const float var = M2 / (float)N;
+  float* st = stats + (size_t)bh * 3 * m;
+  st[a] = mean;
+  st[m + a] = var;
+  st[2 * m + a] = 1.0f / sqrtf(var + 1e-5f);
+}
+
+cudaError_t run_stats_final(const Prob& p, const float* spart, float* stats, cudaStream_t st) {
+  const int n = p.BH * p.m;
+  return launch("stats_final", k_stats_final, dim3((n + 255) / 256), dim3(256), 0, st, spart, stats,
+                p.BH, p.Sq, p.m, p.mp, p.N);
+}
+
+// ===========================================================================
+// query pass: grid (token block, slice).  Each CTA keeps 64 queries in shared
+// memory and walks the landmark tiles: P tile on the fly (never stored to
+// HBM), optional centring/whitening, then O += Z_tile W-hat_tile.
+// ===========================================================================
+template <int D, typename T, bool NORM>
+__global__ void __launch_bounds__(kThreads, 2)
+    k_query_fwd(const T* __restrict__ Q, const float* __restrict__ L, const float* __restrict__ What,
+                const float* __restrict__ stats, T* __restrict__ O, int N, int m, int nt, float ns) {
+  constexpr int CPT = D / 16;
+  extern __shared__ float4 sm4[];
+  float* Xs = reinterpret_cast<float*>(sm4);
+  float* Ls = Xs + tile_floats(D);
+  float* Ws = Ls + tile_floats(D);
+  float* Pt = Ws + tile_floats(D);  // [64 landmarks][68 tokens]
+  __shared__ float mu_s[kTile], rs_s[kTile];
+  const int b = blockIdx.x, bh = blockIdx.y;
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+  const T* Qb = Q + (size_t)bh * N * D;
+  load_tile<D>(Xs, Qb, b * kTile, N);
+  float o[4][CPT];
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) o[r][c] = 0.f;
+  for (int lt = 0; lt < nt; ++lt) {
+    const int a0 = lt * kTile;
+    __syncthreads();
+    load_tile<D>(Ls, L + (size_t)bh * m * D, a0, m);
+    load_tile<D>(Ws, What + (size_t)bh * m * D, a0, m);
+    if (NORM && threadIdx.x < kTile) {
+      const int a = a0 + threadIdx.x;
+      mu_s[threadIdx.x] = a < m ? stats[(size_t)bh * 3 * m + a] : 0.f;
+      rs_s[threadIdx.x] = a < m ? stats[(size_t)bh * 3 * m + 2 * m + a] : 0.f;
+    }
+    __syncthreads();
+    float dist[4][4];
+    dist_tile<D>(Xs, Ls, dist);
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const int a = tx + 16 * s;
+        float pv = 0.f;
+        if (a0 + a < m) {
+          pv = exp2f(dist[r][s] * ns);
+          if (NORM) pv = (pv - mu_s[a]) * rs_s[a];
+        }
+        Pt[a * 68 + 4 * ty + r] = pv;
+      }
+    __syncthreads();
+#pragma unroll 4
+    for (int a = 0; a < kTile; ++a) {
+      const float4 p4 = lds4(Pt + a * 68 + 4 * ty);
+      float wv[CPT];
+      lds_cpt<CPT>(Ws + a * row_stride(D) + tx * CPT, wv);
+#pragma unroll
+      for (int c = 0; c < CPT; ++c) {
+        o[0][c] = fmaf(p4.x, wv[c], o[0][c]);
+        o[1][c] = fmaf(p4.y, wv[c], o[1][c]);
+        o[2][c] = fmaf(p4.z, wv[c], o[2][c]);
+        o[3][c] = fmaf(p4.w, wv[c], o[3][c]);
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int j = b * kTile + 4 * ty + r;
+    if (j < N) st_cpt<CPT>(O + ((size_t)bh * N + j) * D + tx * CPT, o[r]);
+  }
+}
+
+template <int D, typename T>
+static cudaError_t query_fwd_t(const Prob& p, const void* q, const float* L, const float* What,
+                               const float* stats, void* out, cudaStream_t st) {
+  const size_t smem = (3 * (size_t)tile_floats(D) + 64 * 68) * sizeof(float);
+  dim3 grid(p.nblk, p.BH);
+  if (p.norm()) {
+    static bool once = (allow_smem(k_query_fwd<D, T, true>, smem), true);
+    (void)once;
+    return launch("query_fwd", k_query_fwd<D, T, true>, grid, dim3(kThreads), smem, st,
+                  (const T*)q, L, What, stats, (T*)out, p.N, p.m, p.nt, p.ns);
+  }
+  static bool once2 = (allow_smem(k_query_fwd<D, T, false>, smem), true);
+  (void)once2;
+  return launch("query_fwd", k_query_fwd<D, T, false>, grid, dim3(kThreads), smem, st, (const T*)q,
+                L, What, stats, (T*)out, p.N, p.m, p.nt, p.ns);
+}
+
+cudaError_t run_query_fwd(const Prob& p, const void* q, const float* L, const float* What,
+                          const float* stats, void* out, cudaStream_t st) {
+  DISPATCH_DT(query_fwd_t, p, q, L, What, stats, out, st);
+}
+
+// ===========================================================================
+// backward tile kernel, grid (landmark tile, split, slice).
+//
+// For a token block X (queries or keys, 64 rows) against the CTA's 64
+// landmarks, with kv_ja = k(X_j, L_a) recomputed on the fly and
+// dot_ja = U_j . R_a (U = dO, R = W-hat on the query side; U = V, R = dW on
+// the key side), the upstream weight g_ja is
+//   query side: g = dP * P / lambda, dP = dZ (no norm) or the centring/whitening
+//               reverse (dZ - mean dZ - Z mean(dZ Z)) / sqrt(var + eta), dZ = dot
+//   key side:   g = dC * C / lambda, dC = dot
+// and, since dk(x, l)/dx_c = -(k / lambda) sgn(x_c - l_c),
+//   token side    dX_jc = -sum_a g_ja sgn(X_jc - L_ac)   (per landmark tile)
+//   landmark side dL_ac += sum_j g_ja sgn(X_jc - L_ac)   (accumulated over the split)
+// plus dW-hat_a = sum_j Z_ja dO_j (query side) and dV_j = sum_a C_ja dW_a
+// (key side, per landmark tile).  MODE 0 is the query-side statistics pass of
+// the normalised map (sum dZ, sum dZ Z and dW-hat only).
+// ===========================================================================
+template <int D, typename T, int MODE, bool NORM>
+__global__ void __launch_bounds__(kThreads, 2)
+    k_bwd_tile(const T* __restrict__ X, const T* __restrict__ U, const float* __restrict__ L,
+               const float* __restrict__ R, const float* __restrict__ stats,
+               const float* __restrict__ mdz, float* __restrict__ tok_part,
+               float* __restrict__ tok_part2, float* __restrict__ lm_part,
+               float* __restrict__ lm_part2, float* __restrict__ ns_part, int N, int m, int mp,
+               int S, int nblk, int BH, float ns, float inv_lam) {
+  constexpr int CPT = D / 16;
+  constexpr bool kTokenSide = MODE != 0;
+  constexpr bool kDWhat = (MODE == 0) || (MODE == 1 && !NORM);
+  extern __shared__ float4 sm4[];
+  float* Ls = reinterpret_cast<float*>(sm4);
+  float* Rs = Ls + tile_floats(D);
+  float* Xs = Rs + tile_floats(D);
+  float* Us = Xs + tile_floats(D);
+  float* Gs = Us + tile_floats(D);  // [64 tokens][68]: g
+  float* Zs = Gs + 64 * 68;         // [64 tokens][68]: Z (query side) or C (key side)
+  __shared__ float mu_s[kTile], rs_s[kTile], m0_s[kTile], m1_s[kTile];
+
+  const int lt = blockIdx.x, sp = blockIdx.y, bh = blockIdx.z;
+  const int a0 = lt * kTile;
+  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+  const T* Xb = X + (size_t)bh * N * D;
+  const T* Ub = U + (size_t)bh * N * D;
+  load_tile<D>(Ls, L + (size_t)bh * m * D, a0, m);
+  load_tile<D>(Rs, R + (size_t)bh * m * D, a0, m);
+  if (NORM && threadIdx.x < kTile) {
+    const int a = a0 + threadIdx.x;
+    const float* stb = stats + (size_t)bh * 3 * m;
+    mu_s[threadIdx.x] = a < m ? stb[a] : 0.f;
+    rs_s[threadIdx.x] = a < m ? stb[2 * m + a] : 0.f;
+    if (MODE == 1) {
+      m0_s[threadIdx.x] = mdz[(size_t)bh * 2 * mp + a0 + threadIdx.x];
+      m1_s[threadIdx.x] = mdz[(size_t)bh * 2 * mp + mp + a0 + threadIdx.x];
+    }
+  }
+  __syncthreads();
+
+  // landmark-side registers: thread owns landmarks 4 ty + s, columns tx * CPT + c
+  float lreg[4][CPT], dl[4][CPT], dw[4][CPT];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    lds_cpt<CPT>(Ls + (4 * ty + s) * row_stride(D) + tx * CPT, lreg[s]);
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) dl[s][c] = dw[s][c] = 0.f;
+  }
+  float sdz[4] = {0.f, 0.f, 0.f, 0.f}, sdzz[4] = {0.f, 0.f, 0.f, 0.f};
+
+  int b0, b1;
+  split_range(nblk, S, sp, b0, b1);
+  for (int b = b0; b < b1; ++b) {
+    __syncthreads();
+    load_tile<D>(Xs, Xb, b * kTile, N);
+    load_tile<D>(Us, Ub, b * kTile, N);
+    __syncthreads();
+
+    // ---- phase 1: distances and dots, thread = 4 tokens x 4 landmarks ----
+    float dist[4][4], dot[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int s = 0; s < 4; ++s) dist[r][s] = dot[r][s] = 0.f;
+#pragma unroll 2
+    for (int c = 0; c < D; c += 4) {
+      float4 x[4], l[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) x[r] = lds4(Xs + (4 * ty + r) * row_stride(D) + c);
+#pragma unroll
+      for (int s = 0; s < 4; ++s) l[s] = lds4(Ls + (tx + 16 * s) * row_stride(D) + c);
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          dist[r][s] += fabsf(x[r].x - l[s].x);
+          dist[r][s] += fabsf(x[r].y - l[s].y);
+          dist[r][s] += fabsf(x[r].z - l[s].z);
+          dist[r][s] += fabsf(x[r].w - l[s].w);
+        }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) x[r] = lds4(Us + (4 * ty + r) * row_stride(D) + c);
+#pragma unroll
+      for (int s = 0; s < 4; ++s) l[s] = lds4(Rs + (tx + 16 * s) * row_stride(D) + c);
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          dot[r][s] = fmaf(x[r].x, l[s].x, dot[r][s]);
+          dot[r][s] = fmaf(x[r].y, l[s].y, dot[r][s]);
+          dot[r][s] = fmaf(x[r].z, l[s].z, dot[r][s]);
+          dot[r][s] = fmaf(x[r].w, l[s].w, dot[r][s]);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const int jl = 4 * ty + r, al = tx + 16 * s;
+        const bool valid = (b * kTile + jl < N) && (a0 + al < m);
+        const float kv = exp2f(dist[r][s] * ns);
+        float g = 0.f, zc = 0.f;
+        if (MODE == 2) {
+          g = dot[r][s] * kv * inv_lam;
+          zc = kv;
+        } else {
+          const float z = NORM ? (kv - mu_s[al]) * rs_s[al] : kv;
+          zc = z;
+          if (MODE == 0) {
+            if (valid) {
+              sdz[s] += dot[r][s];
+              sdzz[s] = fmaf(dot[r][s], z, sdzz[s]);
+            }
+          } else {
+            const float dp = NORM ? (dot[r][s] - m0_s[al] - z * m1_s[al]) * rs_s[al] : dot[r][s];
+            g = dp * kv * inv_lam;
+          }
+        }
+        Gs[jl * 68 + al] = valid ? g : 0.f;
+        Zs[jl * 68 + al] = valid ? zc : 0.f;
+      }
+    __syncthreads();
+
+    // ---- phase A: token side, thread = 4 tokens x CPT columns ----
+    if (kTokenSide) {
+      float xr[4][CPT], tq[4][CPT], tv[4][CPT];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        lds_cpt<CPT>(Xs + (4 * ty + r) * row_stride(D) + tx * CPT, xr[r]);
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) tq[r][c] = tv[r][c] = 0.f;
+      }
+#pragma unroll 2
+      for (int a = 0; a < kTile; ++a) {
+        float lv[CPT], gr[4];
+        lds_cpt<CPT>(Ls + a * row_stride(D) + tx * CPT, lv);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) gr[r] = Gs[(4 * ty + r) * 68 + a];
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int c = 0; c < CPT; ++c) tq[r][c] += sgn_times(xr[r][c] - lv[c], gr[r]);
+        if (MODE == 2) {
+          float rv[CPT], cr[4];
+          lds_cpt<CPT>(Rs + a * row_stride(D) + tx * CPT, rv);
+#pragma unroll
+          for (int r = 0; r < 4; ++r) cr[r] = Zs[(4 * ty + r) * 68 + a];
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c = 0; c < CPT; ++c) tv[r][c] = fmaf(cr[r], rv[c], tv[r][c]);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int j = b * kTile + 4 * ty + r;
+        if (j < N) {
+          const size_t off = (((size_t)lt * BH + bh) * N + j) * D + tx * CPT;
+#pragma unroll
+          for (int c = 0; c < CPT; ++c) tq[r][c] = -tq[r][c];
+          st_cpt<CPT>(tok_part + off, tq[r]);
+          if (MODE == 2) st_cpt<CPT>(tok_part2 + off, tv[r]);
+        }
+      }
+    }
+
+    // ---- phase B: landmark side, thread = 4 landmarks x CPT columns ----
+#pragma unroll 2
+    for (int j = 0; j < kTile; ++j) {
+      if (kTokenSide) {
+        float xv[CPT];
+        lds_cpt<CPT>(Xs + j * row_stride(D) + tx * CPT, xv);
+        const float4 g4 = lds4(Gs + j * 68 + 4 * ty);
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) {
+          dl[0][c] += sgn_times(xv[c] - lreg[0][c], g4.x);
+          dl[1][c] += sgn_times(xv[c] - lreg[1][c], g4.y);
+          dl[2][c] += sgn_times(xv[c] - lreg[2][c], g4.z);
+          dl[3][c] += sgn_times(xv[c] - lreg[3][c], g4.w);
+        }
+      }
+      if (kDWhat) {
+        float uv[CPT];
+        lds_cpt<CPT>(Us + j * row_stride(D) + tx * CPT, uv);
+        const float4 z4 = lds4(Zs + j * 68 + 4 * ty);
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) {
+          dw[0][c] = fmaf(z4.x, uv[c], dw[0][c]);
+          dw[1][c] = fmaf(z4.y, uv[c], dw[1][c]);
+          dw[2][c] = fmaf(z4.z, uv[c], dw[2][c]);
+          dw[3][c] = fmaf(z4.w, uv[c], dw[3][c]);
+        }
+      }
+    }
+  }
+
+  const size_t lo = (((size_t)bh * S + sp) * mp + a0 + 4 * ty) * D + tx * CPT;
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    if (kTokenSide) st_cpt<CPT>(lm_part + lo + (size_t)s * D, dl[s]);
+    if (kDWhat) st_cpt<CPT>(lm_part2 + lo + (size_t)s * D, dw[s]);
+  }
+  if (MODE == 0) {
+    // per-landmark sums over the 16 token rows of threads, through the g / Z tiles
+    float* red0 = Gs;  // [16][64]
+    float* red1 = Zs;  // [16][64]
+    __syncthreads();
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      red0[ty * kTile + tx + 16 * s] = sdz[s];
+      red1[ty * kTile + tx + 16 * s] = sdzz[s];
+    }
+    __syncthreads();
+    if (threadIdx.x < kTile) {
+      float s0 = 0.f, s1 = 0.f;
+      for (int q = 0; q < 16; ++q) {
+        s0 += red0[q * kTile + threadIdx.x];
+        s1 += red1[q * kTile + threadIdx.x];
+      }
+      float* o = ns_part + ((size_t)bh * S + sp) * 2 * mp + a0 + threadIdx.x;
+      o[0] = s0;
+      o[mp] = s1;
+    }
+  }
+}
+
+template <int D, typename T, int MODE, bool NORM>
+static cudaError_t bwd_tile_t2(const Prob& p, const BwdArgs& a, cudaStream_t st) {
+  const size_t smem = (4 * (size_t)tile_floats(D) + 2 * 64 * 68) * sizeof(float);
+  static bool once = (allow_smem(k_bwd_tile<D, T, MODE, NORM>, smem), true);
+  (void)once;
+  static const char* names[3] = {"bwd_qstats", "bwd_query", "bwd_key"};
+  return launch(names[MODE], k_bwd_tile<D, T, MODE, NORM>, dim3(p.nt, p.Sb, p.BH), dim3(kThreads),
+                smem, st, (const T*)a.X, (const T*)a.U, a.L, a.R, a.stats, a.mdz, a.tok_part,
+                a.tok_part2, a.lm_part, a.lm_part2, a.ns_part, p.N, p.m, p.mp, p.Sb, p.nblk, p.BH,
+                p.ns, p.inv_lam);
+}
+
+template <int D, typename T>
+static cudaError_t bwd_tile_t(const Prob& p, int mode, const BwdArgs& a, cudaStream_t st) {
+  if (mode == 0) return bwd_tile_t2<D, T, 0, true>(p, a, st);
+  if (mode == 1) {
+    if (p.norm()) return bwd_tile_t2<D, T, 1, true>(p, a, st);
+    return bwd_tile_t2<D, T, 1, false>(p, a, st);
+  }
+  return bwd_tile_t2<D, T, 2, false>(p, a, st);
+}
+
+cudaError_t run_bwd_tile(const Prob& p, int mode, const BwdArgs& a, cudaStream_t st) {
+  DISPATCH_DT(bwd_tile_t, p, mode, a, st);
+}
+
+// mdz [BH][2][mp]: (1/N) sum dZ and (1/N) sum dZ Z per landmark, fixed order over splits
+__global__ void k_mdz(const float* __restrict__ ns_part, float* __restrict__ mdz, int BH, int S, int mp,
+                      int N) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= BH * mp) return;
+  const int bh = e / mp, a = e % mp;
+  float s0 = 0.f, s1 = 0.f;
+  for (int s = 0; s < S; ++s) {
+    const float* o = ns_part + ((size_t)bh * S + s) * 2 * mp + a;
+    s0 += o[0];
+    s1 += o[mp];
+  }
+  mdz[(size_t)bh * 2 * mp + a] = s0 / (float)N;
+  mdz[(size_t)bh * 2 * mp + mp + a] = s1 / (float)N;
+}
+
+cudaError_t run_mdz(const Prob& p, const float* ns_part, float* mdz, cudaStream_t st) {
+  const int n = p.BH * p.mp;
+  return launch("mdz", k_mdz, dim3((n + 255) / 256), dim3(256), 0, st, ns_part, mdz, p.BH, p.Sb, p.mp,
+                p.N);
+}
+
+// dL[bh][a][c] = sum_s dLq + sum_s dLc + dLA (fixed order)
+__global__ void k_reduce_dl(const float* __restrict__ dLq, const float* __restrict__ dLc,
+                            const float* __restrict__ dLA, float* __restrict__ dL, int BH, int S,
+                            int m, int mp, int d) {
+  const size_t total = (size_t)BH * m * d;
+  for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < total;
+       e += (size_t)gridDim.x * blockDim.x) {
+    const size_t bh = e / ((size_t)m * d), ac = e % ((size_t)m * d);
+    const size_t base = bh * S * mp * d + ac;
+    float s = 0.f;
+    for (int q = 0; q < S; ++q) s += dLq[base + (size_t)q * mp * d];
+    for (int q = 0; q < S; ++q) s += dLc[base + (size_t)q * mp * d];
+    dL[e] = s + dLA[e];
+  }
+}
+
+cudaError_t run_reduce_dl(const Prob& p, const float* dLq, const float* dLc, const float* dLA,
+                          float* dL, cudaStream_t st) {
+  const size_t n = (size_t)p.BH * p.m * p.d;
+  return launch("reduce_dl", k_reduce_dl, dim3(grid_for(n)), dim3(kThreads), 0, st, dLq, dLc, dLA, dL,
+                p.BH, p.Sb, p.m, p.mp, p.d);
+}
+
+// token gradients: sum the per-landmark-tile partials in tile order, add the
+// pooling path dL[a(n)] / window size to dK, convert to the tensor type.
+template <typename T>
+__global__ void k_finalize(const float* __restrict__ dQp, const float* __restrict__ dKp,
+                           const float* __restrict__ dVp, const float* __restrict__ dL,
+                           T* __restrict__ dq, T* __restrict__ dk, T* __restrict__ dv, int BH, int N,
+                           int d, int nt, int m, int gw, int r, int sh, int sw, int tied) {
+  const size_t total4 = (size_t)BH * N * d / 4;
+  const size_t plane = (size_t)BH * N * d;
+  const float inv = 1.0f / (float)(sh * sw);
+  for (size_t e4 = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e4 < total4;
+       e4 += (size_t)gridDim.x * blockDim.x) {
+    const size_t e = e4 * 4;
+    const size_t row = e / d;
+    const int c = (int)(e % d);
+    const int n = (int)(row % N);
+    const size_t bh = row / N;
+    float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f), k4 = q4, v4 = q4;
+    for (int t = 0; t < nt; ++t) {
+      const float4 a = *reinterpret_cast<const float4*>(dQp + t * plane + e);
+      const float4 b = *reinterpret_cast<const float4*>(dKp + t * plane + e);
+      const float4 v = *reinterpret_cast<const float4*>(dVp + t * plane + e);
+      q4.x += a.x; q4.y += a.y; q4.z += a.z; q4.w += a.w;
+      k4.x += b.x; k4.y += b.y; k4.z += b.z; k4.w += b.w;
+      v4.x += v.x; v4.y += v.y; v4.z += v.z; v4.w += v.w;
+    }
+    const int y = n / gw, x = n % gw;
+    const int a = (y / sh) * r + x / sw;
+    const float4 l4 = *reinterpret_cast<const float4*>(dL + (bh * m + a) * d + c);
+    k4.x += l4.x * inv; k4.y += l4.y * inv; k4.z += l4.z * inv; k4.w += l4.w * inv;
+    if (tied) {
+      q4.x += k4.x; q4.y += k4.y; q4.z += k4.z; q4.w += k4.w;
+      st4(dq + e, q4);
+    } else {
+      st4(dq + e, q4);
+      st4(dk + e, k4);
+    }
+    st4(dv + e, v4);
+  }
+}
+
+cudaError_t run_finalize(const Prob& p, const float* dQp, const float* dKp, const float* dVp,
+                         const float* dL, void* dq, void* dk, void* dv, cudaStream_t st) {
+  const size_t n4 = (size_t)p.BH * p.N * p.d / 4;
+  if (p.dtype == 1)
+    return launch("finalize", k_finalize<__nv_bfloat16>, dim3(grid_for(n4)), dim3(kThreads), 0, st,
+                  dQp, dKp, dVp, dL, (__nv_bfloat16*)dq, (__nv_bfloat16*)dk, (__nv_bfloat16*)dv,
+                  p.BH, p.N, p.d, p.nt, p.m, p.gw, p.r, p.sh, p.sw, p.tied);
+  return launch("finalize", k_finalize<float>, dim3(grid_for(n4)), dim3(kThreads), 0, st, dQp, dKp,
+                dVp, dL, (float*)dq, (float*)dk, (float*)dv, p.BH, p.N, p.d, p.nt, p.m, p.gw, p.r,
+                p.sh, p.sw, p.tied);
+}
+
+// zero-fill (used when the Newton-Schulz backward has no step to initialise dA)
+__global__ void k_zero(float* __restrict__ x, size_t n) {
+  for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < n;
+       e += (size_t)gridDim.x * blockDim.x)
+    x[e] = 0.f;
+}
+
+cudaError_t run_zero(float* x, size_t n, cudaStream_t st) {
+  return launch("zero", k_zero, dim3(grid_for(n)), dim3(kThreads), 0, st, x, n);
+}
+
+}  // namespace lapnys

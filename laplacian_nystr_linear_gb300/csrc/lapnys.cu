@@ -1,0 +1,462 @@
+// C ABI of liblapnys: argument checks, ctx / workspace layout, and the launch
+// sequences of the forward and backward passes of Laplacian-kernel Nystrom
+// attention (see include/lapnys.h for the contract).
+#include <math.h>
+#include <string.h>
+
+#include <vector>
+
+#include "../../include/lapnys.h"
+#include "common.cuh"
+#include "internal.h"
+
+namespace lapnys {
+
+// ---------------------------------------------------------------------------
+// instrumentation
+// ---------------------------------------------------------------------------
+namespace {
+constexpr int kMaxRec = 4096;
+struct Rec {
+  const char* name;
+  cudaEvent_t a, b;
+};
+bool g_prof = false;
+std::vector<Rec> g_rec;
+int g_used = 0;
+uint64_t g_launches = 0;
+}  // namespace
+
+int prof_begin(const char* name, cudaStream_t s) {
+  if (!g_prof || g_used >= kMaxRec) return -1;
+  if ((int)g_rec.size() <= g_used) {
+    Rec r{name, nullptr, nullptr};
+    if (cudaEventCreate(&r.a) != cudaSuccess || cudaEventCreate(&r.b) != cudaSuccess) return -1;
+    g_rec.push_back(r);
+  }
+  Rec& r = g_rec[g_used];
+  r.name = name;
+  if (cudaEventRecord(r.a, s) != cudaSuccess) return -1;
+  return g_used++;
+}
+
+void prof_end(int slot, cudaStream_t s) {
+  if (slot >= 0) cudaEventRecord(g_rec[slot].b, s);
+}
+
+void count_launch() { ++g_launches; }
+
+// ---------------------------------------------------------------------------
+// problem description and memory layout
+// ---------------------------------------------------------------------------
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+static int isqrt_exact(int m) {
+  int r = (int)lrint(sqrt((double)m));
+  while (r * r > m) --r;
+  while ((r + 1) * (r + 1) <= m) ++r;
+  return r * r == m ? r : -1;
+}
+
+static int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// token splits so that each pass has roughly 8 CTAs per SM of a 152-SM part;
+// depends on the dimensions only, so results do not depend on the device.
+static int splits_for(int nblk, int nt, int BH) {
+  const int target = 1216;
+  int s = ceil_div(target, nt * BH);
+  if (s > nblk) s = nblk;
+  if (s < 1) s = 1;
+  return s;
+}
+
+static bool dims_ok(int B, int H, int N, int d, int m, int iters) {
+  if (B <= 0 || H <= 0 || N <= 0 || m <= 0 || m > N || iters < 0 || iters > 64) return false;
+  if (d <= 0) return false;
+  if (m > 1024) return false;
+  if (isqrt_exact(m) < 0) return false;
+  if ((long long)B * H * N * d >= (1LL << 31)) return false;
+  return true;
+}
+
+static bool d_supported(int d) { return d == 16 || d == 32 || d == 64 || d == 128; }
+
+static Prob make_prob(int B, int H, int N, int d, int gh, int gw, int m, float lam, float eps,
+                      int iters, int tied, int dtype, unsigned flags) {
+  Prob p;
+  memset(&p, 0, sizeof(p));
+  p.B = B; p.H = H; p.BH = B * H; p.N = N; p.d = d; p.gh = gh; p.gw = gw; p.m = m;
+  p.r = isqrt_exact(m);
+  p.sh = p.r > 0 ? gh / p.r : 0;
+  p.sw = p.r > 0 ? gw / p.r : 0;
+  p.iters = iters; p.tied = tied; p.dtype = dtype; p.flags = flags;
+  p.lam = lam; p.eps = eps;
+  p.ns = (float)(-1.4426950408889634 / (double)lam);
+  p.inv_lam = (float)(1.0 / (double)lam);
+  p.nt = ceil_div(m, kTile);
+  p.mp = p.nt * kTile;
+  p.nblk = ceil_div(N, kTile);
+  p.Sk = splits_for(p.nblk, p.nt, p.BH);
+  p.Sq = p.Sk;
+  p.Sb = p.Sk;
+  return p;
+}
+
+struct CtxLayout {
+  size_t L, A, alpha, X, Y, W, What, stats, idx, total;
+  int nx, ny;
+};
+
+static CtxLayout ctx_layout(int BH, int N, int d, int m, int iters, bool full) {
+  CtxLayout c;
+  c.nx = full ? iters + 1 : 2;
+  c.ny = full ? (iters > 0 ? iters : 1) : 1;
+  const size_t f = sizeof(float);
+  size_t o = 0;
+  c.L = o; o = align256(o + (size_t)BH * m * d * f);
+  c.A = o; o = align256(o + (size_t)BH * m * m * f);
+  c.alpha = o; o = align256(o + (size_t)BH * 4 * f);
+  c.X = o; o = align256(o + (size_t)BH * c.nx * m * m * f);
+  c.Y = o; o = align256(o + (size_t)BH * c.ny * m * m * f);
+  c.W = o; o = align256(o + (size_t)BH * m * d * f);
+  c.What = o; o = align256(o + (size_t)BH * m * d * f);
+  c.stats = o; o = align256(o + (size_t)BH * 3 * m * f);
+  c.idx = o; o = align256(o + (size_t)N * sizeof(int32_t));
+  c.total = o;
+  return c;
+}
+
+struct WsLayout {
+  size_t lite;                                 // ctx stand-in when the forward gets no ctx
+  size_t kpart, spart;                         // forward partials
+  size_t dWhp, dLqp, dLcp, nsp, mdz;           // backward landmark-side partials
+  size_t dQp, dKp, dVp;                        // backward token-side partials
+  size_t dWh, dW, dLA, dL, G, XG, Tm, dA;      // backward landmark-side results
+  size_t total;
+};
+
+static WsLayout ws_layout(const Prob& p) {
+  WsLayout w;
+  const size_t f = sizeof(float);
+  const size_t BH = p.BH, m = p.m, d = p.d, mp = p.mp;
+  size_t o = 0;
+  w.lite = o; o = align256(o + ctx_layout(p.BH, p.N, p.d, p.m, p.iters, false).total);
+  w.kpart = o; o = align256(o + BH * p.Sk * mp * d * f);
+  w.spart = o; o = align256(o + BH * p.Sq * 3 * mp * f);
+  w.dWhp = o; o = align256(o + BH * p.Sb * mp * d * f);
+  w.dLqp = o; o = align256(o + BH * p.Sb * mp * d * f);
+  w.dLcp = o; o = align256(o + BH * p.Sb * mp * d * f);
+  w.nsp = o; o = align256(o + BH * p.Sb * 2 * mp * f);
+  w.mdz = o; o = align256(o + BH * 2 * mp * f);
+  const size_t tok = (size_t)p.nt * BH * p.N * d * f;
+  w.dQp = o; o = align256(o + tok);
+  w.dKp = o; o = align256(o + tok);
+  w.dVp = o; o = align256(o + tok);
+  w.dWh = o; o = align256(o + BH * m * d * f);
+  w.dW = o; o = align256(o + BH * m * d * f);
+  w.dLA = o; o = align256(o + BH * m * d * f);
+  w.dL = o; o = align256(o + BH * m * d * f);
+  w.G = o; o = align256(o + BH * m * m * f);
+  w.XG = o; o = align256(o + BH * m * m * f);
+  w.Tm = o; o = align256(o + BH * m * m * f);
+  w.dA = o; o = align256(o + BH * m * m * f);
+  w.total = o;
+  return w;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+static int check_common(int B, int H, int N, int d, int gh, int gw, int m, float lam, float eps,
+                        int iters, int dtype, unsigned flags) {
+  if (!dims_ok(B, H, N, d, m, iters)) return LAPNYS_EINVAL;
+  if (gh <= 0 || gw <= 0 || (long long)gh * gw != N) return LAPNYS_EINVAL;
+  const int r = isqrt_exact(m);
+  if (gh % r != 0 || gw % r != 0) return LAPNYS_EINVAL;
+  if (!(lam > 0.f) || !isfinite(lam)) return LAPNYS_EINVAL;
+  if (!(eps >= 0.f) || !isfinite(eps)) return LAPNYS_EINVAL;
+  if (dtype != LAPNYS_F32 && dtype != LAPNYS_BF16) return LAPNYS_EINVAL;
+  if ((flags & ~(unsigned)LAPNYS_NORM) != 0) return LAPNYS_EINVAL;
+  if (!d_supported(d)) return LAPNYS_ENOTSUP;
+  return LAPNYS_OK;
+}
+
+#define CK(x)                                  \
+  do {                                         \
+    if ((x) != cudaSuccess) return LAPNYS_ECUDA; \
+  } while (0)
+
+// ---------------------------------------------------------------------------
+// Newton-Schulz for m > 64 via batched products (X slots: nx, Y slots: ny)
+// ---------------------------------------------------------------------------
+static int ns_forward_large(const Prob& p, const float* A, float* X, float* Y, int nx, int ny,
+                            cudaStream_t st) {
+  const int m = p.m;
+  const long mm = (long)m * m;
+  for (int t = 0; t < p.iters; ++t) {
+    float* Xt = X + (long)(t % nx) * mm;
+    float* Xn = X + (long)((t + 1) % nx) * mm;
+    float* Yt = Y + (long)(t % ny) * mm;
+    // Y_t = A X_t
+    CK(run_bgemm(false, false, p.BH, m, m, m, A, m, mm, Xt, m, nx * mm, Yt, m, ny * mm, nullptr, m,
+                 0, 1.f, 0.f, st));
+    // X_{t+1} = 2 X_t - X_t Y_t
+    CK(run_bgemm(false, false, p.BH, m, m, m, Xt, m, nx * mm, Yt, m, ny * mm, Xn, m, nx * mm, Xt, m,
+                 nx * mm, -1.f, 2.f, st));
+  }
+  return LAPNYS_OK;
+}
+
+}  // namespace lapnys
+
+using namespace lapnys;
+
+extern "C" {
+
+const char* lapnys_strerror(int status) {
+  switch (status) {
+    case LAPNYS_OK: return "ok";
+    case LAPNYS_EINVAL: return "invalid argument (dimension, pointer, alignment or parameter)";
+    case LAPNYS_ECUDA: return "CUDA launch failed";
+    case LAPNYS_ETIMEOUT: return "bounded device wait expired";
+    case LAPNYS_ENOSPC: return "ctx or workspace buffer too small";
+    case LAPNYS_ENOTSUP: return "unsupported configuration (d must be 16, 32, 64 or 128)";
+  }
+  return "unknown status";
+}
+
+size_t lapnys_ctx_bytes(int B, int H, int N, int d, int m, int iters, unsigned flags) {
+  (void)flags;
+  if (!dims_ok(B, H, N, d, m, iters)) return 0;
+  return ctx_layout(B * H, N, d, m, iters, true).total;
+}
+
+size_t lapnys_workspace_bytes(int B, int H, int N, int d, int m, int iters, unsigned flags) {
+  if (!dims_ok(B, H, N, d, m, iters)) return 0;
+  const int r = isqrt_exact(m);
+  Prob p = make_prob(B, H, N, d, r, N / r, m, 1.f, 0.f, iters, 0, 0, flags);
+  return ws_layout(p).total;
+}
+
+int lapnys_ctx_offsets(int B, int H, int N, int d, int m, int iters, unsigned flags,
+                       lapnys_ctx_layout* out) {
+  (void)flags;
+  if (out == nullptr || !dims_ok(B, H, N, d, m, iters)) return LAPNYS_EINVAL;
+  const CtxLayout c = ctx_layout(B * H, N, d, m, iters, true);
+  out->L = c.L; out->A = c.A; out->alpha = c.alpha; out->X = c.X; out->Y = c.Y;
+  out->W = c.W; out->What = c.What; out->stats = c.stats; out->idx = c.idx; out->total = c.total;
+  return LAPNYS_OK;
+}
+
+int lapnys_pool(const void* k, float* L, int32_t* idx, int B, int H, int N, int d, int grid_h,
+                int grid_w, int m, int dtype, cudaStream_t stream) {
+  int rc = check_common(B, H, N, d, grid_h, grid_w, m, 1.f, 0.f, 0, dtype, 0);
+  if (rc != LAPNYS_OK) return rc;
+  if (k == nullptr || L == nullptr || !aligned16(k) || !aligned16(L)) return LAPNYS_EINVAL;
+  Prob p = make_prob(B, H, N, d, grid_h, grid_w, m, 1.f, 0.f, 0, 0, dtype, 0);
+  CK(run_pool(p, k, L, idx, stream));
+  return LAPNYS_OK;
+}
+
+int lapnys_fwd(const void* q, const void* k, const void* v, void* out, int B, int H, int N, int d,
+               int grid_h, int grid_w, int m, float lambda, float eps, int iters, int tied_qk,
+               cudaStream_t stream, int dtype, unsigned flags, void* ctx, size_t ctx_bytes,
+               void* ws, size_t ws_bytes) {
+  int rc = check_common(B, H, N, d, grid_h, grid_w, m, lambda, eps, iters, dtype, flags);
+  if (rc != LAPNYS_OK) return rc;
+  if (tied_qk != 0 && tied_qk != 1) return LAPNYS_EINVAL;
+  if (tied_qk) {
+    if (k != nullptr && k != q) return LAPNYS_EINVAL;
+    k = q;
+  }
+  if (!q || !k || !v || !out || !ws) return LAPNYS_EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(ws))
+    return LAPNYS_EINVAL;
+  if (ctx != nullptr && !aligned16(ctx)) return LAPNYS_EINVAL;
+  Prob p = make_prob(B, H, N, d, grid_h, grid_w, m, lambda, eps, iters, tied_qk, dtype, flags);
+  const WsLayout w = ws_layout(p);
+  if (ws_bytes < w.total) return LAPNYS_ENOSPC;
+  const bool full = ctx != nullptr;
+  const CtxLayout c = ctx_layout(p.BH, N, d, m, iters, full);
+  if (full && ctx_bytes < c.total) return LAPNYS_ENOSPC;
+
+  char* cb = full ? (char*)ctx : (char*)ws + w.lite;
+  char* wb = (char*)ws;
+  float* L = (float*)(cb + c.L);
+  float* A = (float*)(cb + c.A);
+  float* alpha = (float*)(cb + c.alpha);
+  float* X = (float*)(cb + c.X);
+  float* Y = (float*)(cb + c.Y);
+  float* W = (float*)(cb + c.W);
+  float* What = (float*)(cb + c.What);
+  float* stats = (float*)(cb + c.stats);
+  int32_t* idx = (int32_t*)(cb + c.idx);
+  const long mm = (long)m * m;
+
+  CK(run_pool(p, k, L, idx, stream));
+  if (m <= kTile) {
+    CK(run_ns_small(p, L, A, alpha, X, Y, c.nx, c.ny, stream));
+  } else {
+    CK(run_gram(p, L, A, stream));
+    CK(run_alpha(p, A, alpha, X, c.nx * mm, stream));
+    rc = ns_forward_large(p, A, X, Y, c.nx, c.ny, stream);
+    if (rc != LAPNYS_OK) return rc;
+  }
+  float* kpart = (float*)(wb + w.kpart);
+  CK(run_key_fwd(p, k, v, L, kpart, stream));
+  CK(run_reduce_parts(p.BH, p.Sk, m, p.mp, d, kpart, W, stream));
+  const float* XT = X + (long)(iters % c.nx) * mm;
+  // W-hat = X_T W
+  CK(run_bgemm(false, false, p.BH, m, d, m, XT, m, c.nx * mm, W, d, (long)m * d, What, d,
+               (long)m * d, nullptr, d, 0, 1.f, 0.f, stream));
+  if (p.norm()) {
+    float* spart = (float*)(wb + w.spart);
+    CK(run_qstats(p, q, L, spart, stream));
+    CK(run_stats_final(p, spart, stats, stream));
+  }
+  CK(run_query_fwd(p, q, L, What, stats, out, stream));
+  return LAPNYS_OK;
+}
+
+int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, const void* ctx,
+               void* dq, void* dk, void* dv, int B, int H, int N, int d, int grid_h, int grid_w,
+               int m, float lambda, float eps, int iters, int tied_qk, cudaStream_t stream,
+               int dtype, unsigned flags, void* ws, size_t ws_bytes) {
+  int rc = check_common(B, H, N, d, grid_h, grid_w, m, lambda, eps, iters, dtype, flags);
+  if (rc != LAPNYS_OK) return rc;
+  if (tied_qk != 0 && tied_qk != 1) return LAPNYS_EINVAL;
+  if (tied_qk) {
+    if (k != nullptr && k != q) return LAPNYS_EINVAL;
+    if (dk != nullptr) return LAPNYS_EINVAL;
+    k = q;
+  } else if (dk == nullptr || !aligned16(dk)) {
+    return LAPNYS_EINVAL;
+  }
+  if (!q || !k || !v || !dout || !ctx || !dq || !dv || !ws) return LAPNYS_EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(ctx) ||
+      !aligned16(dq) || !aligned16(dv) || !aligned16(ws))
+    return LAPNYS_EINVAL;
+  Prob p = make_prob(B, H, N, d, grid_h, grid_w, m, lambda, eps, iters, tied_qk, dtype, flags);
+  const WsLayout w = ws_layout(p);
+  if (ws_bytes < w.total) return LAPNYS_ENOSPC;
+  const CtxLayout c = ctx_layout(p.BH, N, d, m, iters, true);
+
+  const char* cb = (const char*)ctx;
+  char* wb = (char*)ws;
+  const float* L = (const float*)(cb + c.L);
+  const float* A = (const float*)(cb + c.A);
+  const float* alpha = (const float*)(cb + c.alpha);
+  const float* X = (const float*)(cb + c.X);
+  const float* Y = (const float*)(cb + c.Y);
+  const float* W = (const float*)(cb + c.W);
+  const float* What = (const float*)(cb + c.What);
+  const float* stats = (const float*)(cb + c.stats);
+  float* dWhp = (float*)(wb + w.dWhp);
+  float* dLqp = (float*)(wb + w.dLqp);
+  float* dLcp = (float*)(wb + w.dLcp);
+  float* nsp = (float*)(wb + w.nsp);
+  float* mdz = (float*)(wb + w.mdz);
+  float* dQp = (float*)(wb + w.dQp);
+  float* dKp = (float*)(wb + w.dKp);
+  float* dVp = (float*)(wb + w.dVp);
+  float* dWh = (float*)(wb + w.dWh);
+  float* dW = (float*)(wb + w.dW);
+  float* dLA = (float*)(wb + w.dLA);
+  float* dL = (float*)(wb + w.dL);
+  float* G = (float*)(wb + w.G);
+  float* XG = (float*)(wb + w.XG);
+  float* Tm = (float*)(wb + w.Tm);
+  float* dA = (float*)(wb + w.dA);
+  const long mm = (long)m * m;
+  const long md = (long)m * d;
+
+  // ---- query side ----
+  BwdArgs qa;
+  memset(&qa, 0, sizeof(qa));
+  qa.X = q; qa.U = dout; qa.L = L; qa.R = What; qa.stats = stats; qa.mdz = mdz;
+  qa.tok_part = dQp; qa.lm_part = dLqp; qa.lm_part2 = dWhp; qa.ns_part = nsp;
+  if (p.norm()) {
+    CK(run_bwd_tile(p, 0, qa, stream));
+    CK(run_mdz(p, nsp, mdz, stream));
+    CK(run_reduce_parts(p.BH, p.Sb, m, p.mp, d, dWhp, dWh, stream));
+  }
+  CK(run_bwd_tile(p, 1, qa, stream));
+  if (!p.norm()) CK(run_reduce_parts(p.BH, p.Sb, m, p.mp, d, dWhp, dWh, stream));
+
+  // ---- W-hat = X_T W and the Newton-Schulz iteration ----
+  const float* XT = X + (long)iters * mm;
+  const long xs = (long)(iters + 1) * mm;
+  const long ys = (long)c.ny * mm;
+  // G = dLoss/dX_T = dW-hat W^T ;  dW = X_T^T dW-hat
+  CK(run_bgemm(false, true, p.BH, m, m, d, dWh, d, md, W, d, md, G, m, mm, nullptr, m, 0, 1.f, 0.f,
+               stream));
+  CK(run_bgemm(true, false, p.BH, m, d, m, XT, m, xs, dWh, d, md, dW, d, md, nullptr, d, 0, 1.f,
+               0.f, stream));
+  if (m <= kTile) {
+    CK(run_ns_bwd_small(p, A, alpha, X, Y, G, dA, stream));
+  } else {
+    if (iters == 0) CK(run_zero(dA, (size_t)p.BH * mm, stream));
+    for (int t = iters - 1; t >= 0; --t) {
+      const float* Xt = X + (long)t * mm;
+      const float* Yt = Y + (long)t * mm;
+      // XG = X_t^T G
+      CK(run_bgemm(true, false, p.BH, m, m, m, Xt, m, xs, G, m, mm, XG, m, mm, nullptr, m, 0, 1.f,
+                   0.f, stream));
+      // dA = dA - XG X_t^T   (first step initialises dA)
+      CK(run_bgemm(false, true, p.BH, m, m, m, XG, m, mm, Xt, m, xs, dA, m, mm, dA, m, mm, -1.f,
+                   t == iters - 1 ? 0.f : 1.f, stream));
+      // Tm = 2 G - G Y_t^T
+      CK(run_bgemm(false, true, p.BH, m, m, m, G, m, mm, Yt, m, ys, Tm, m, mm, G, m, mm, -1.f, 2.f,
+                   stream));
+      // G = Tm - A^T XG
+      CK(run_bgemm(true, false, p.BH, m, m, m, A, m, mm, XG, m, mm, G, m, mm, Tm, m, mm, -1.f, 1.f,
+                   stream));
+    }
+    CK(run_alpha_bwd(p, A, alpha, G, dA, stream));
+  }
+  CK(run_gram_bwd(p, L, A, dA, dLA, stream));
+
+  // ---- key side ----
+  BwdArgs ka;
+  memset(&ka, 0, sizeof(ka));
+  ka.X = k; ka.U = v; ka.L = L; ka.R = dW;
+  ka.tok_part = dKp; ka.tok_part2 = dVp; ka.lm_part = dLcp;
+  CK(run_bwd_tile(p, 2, ka, stream));
+  CK(run_reduce_dl(p, dLqp, dLcp, dLA, dL, stream));
+  CK(run_finalize(p, dQp, dKp, dVp, dL, dq, dk, dv, stream));
+  return LAPNYS_OK;
+}
+
+uint64_t lapnys_launch_count(void) { return g_launches; }
+
+int lapnys_profile_enable(int on) {
+  g_prof = on != 0;
+  g_used = 0;
+  return LAPNYS_OK;
+}
+
+int lapnys_profile_read(const char** names, int* launches, double* total_ms, int max_kernels) {
+  int n = 0;
+  int bad = 0;
+  for (int i = 0; i < g_used; ++i) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, g_rec[i].a, g_rec[i].b) != cudaSuccess) {
+      bad = 1;
+      continue;
+    }
+    int j = 0;
+    while (j < n && strcmp(names[j], g_rec[i].name) != 0) ++j;
+    if (j == n) {
+      if (n >= max_kernels) continue;
+      names[n] = g_rec[i].name;
+      launches[n] = 0;
+      total_ms[n] = 0.0;
+      ++n;
+    }
+    launches[j] += 1;
+    total_ms[j] += ms;
+  }
+  g_used = 0;
+  return bad ? -1 : n;
+}
+
+}  // extern "C"

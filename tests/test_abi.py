@@ -1,0 +1,117 @@
+"""C ABI checks that need no GPU: the library builds and loads, exports every
+symbol the header declares, sizes buffers, and rejects bad arguments on the
+host before anything is enqueued."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from laplacian_nystr_linear_gb300 import build as b
+    from laplacian_nystr_linear_gb300 import _lib
+    b.build()
+    return _lib.load()
+
+
+def _header_functions():
+    text = open(os.path.join(ROOT, "include", "lapnys.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lapnys_[a-z_]+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    from laplacian_nystr_linear_gb300 import _lib
+    assert _header_functions() == sorted(_lib.EXPORTS)
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in _header_functions():
+        assert hasattr(lib, name), name
+
+
+def test_sizes(lib):
+    # hires workload: 8 x 8 slices, N = 16384, d = 64, m = 256, 24 iterations
+    c = lib.lapnys_ctx_bytes(8, 8, 16384, 64, 256, 24, 0)
+    # iterates dominate: 64 slices x (25 X + 24 Y) x 256^2 floats
+    assert c >= 64 * 49 * 256 * 256 * 4
+    assert lib.lapnys_workspace_bytes(8, 8, 16384, 64, 256, 24, 0) > 0
+    # invalid dimensions give 0
+    assert lib.lapnys_ctx_bytes(1, 1, 196, 32, 48, 20, 0) == 0      # m not square
+    assert lib.lapnys_ctx_bytes(1, 1, 16, 32, 25, 20, 0) == 0       # m > N
+    assert lib.lapnys_ctx_bytes(1, 1, 196, 32, 49, -1, 0) == 0      # iters < 0
+    assert lib.lapnys_workspace_bytes(0, 1, 196, 32, 49, 20, 0) == 0
+
+
+def test_ctx_offsets_are_ordered_and_aligned(lib):
+    from laplacian_nystr_linear_gb300 import _lib
+    lay = _lib.CtxLayout()
+    assert lib.lapnys_ctx_offsets(2, 3, 784, 64, 49, 20, 1, ctypes.byref(lay)) == 0
+    offs = [getattr(lay, n) for n, _ in _lib.CtxLayout._fields_]
+    assert offs == sorted(offs)
+    assert all(o % 256 == 0 for o in offs)
+    assert lay.total == lib.lapnys_ctx_bytes(2, 3, 784, 64, 49, 20, 1)
+
+
+def test_strerror(lib):
+    for code in range(6):
+        assert lib.lapnys_strerror(code)
+    assert b"unknown" in lib.lapnys_strerror(99)
+
+
+FAKE = ctypes.c_void_p(1 << 20)  # aligned, never dereferenced: every call below fails validation
+
+
+def _fwd(lib, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, B=1, H=1, N=196, d=32, gh=14, gw=14, m=49,
+             lam=32.0, eps=1e-3, iters=20, tied=0, stream=None, dtype=0, flags=0, ctx=None,
+             ctx_bytes=0, ws=FAKE, ws_bytes=0)
+    a.update(kw)
+    return lib.lapnys_fwd(a["q"], a["k"], a["v"], a["out"], a["B"], a["H"], a["N"], a["d"], a["gh"],
+                          a["gw"], a["m"], a["lam"], a["eps"], a["iters"], a["tied"], a["stream"],
+                          a["dtype"], a["flags"], a["ctx"], a["ctx_bytes"], a["ws"], a["ws_bytes"])
+
+
+def test_fwd_rejects_bad_arguments(lib):
+    from laplacian_nystr_linear_gb300._lib import LAPNYS_EINVAL, LAPNYS_ENOSPC, LAPNYS_ENOTSUP
+    assert _fwd(lib, N=195) == LAPNYS_EINVAL                       # N != grid_h * grid_w
+    assert _fwd(lib, m=48) == LAPNYS_EINVAL                        # m not square
+    assert _fwd(lib, m=36) == LAPNYS_EINVAL                        # 6 does not divide 14
+    assert _fwd(lib, lam=0.0) == LAPNYS_EINVAL
+    assert _fwd(lib, lam=float("nan")) == LAPNYS_EINVAL
+    assert _fwd(lib, eps=-1.0) == LAPNYS_EINVAL
+    assert _fwd(lib, iters=-1) == LAPNYS_EINVAL
+    assert _fwd(lib, dtype=7) == LAPNYS_EINVAL
+    assert _fwd(lib, flags=2) == LAPNYS_EINVAL
+    assert _fwd(lib, q=None) == LAPNYS_EINVAL
+    assert _fwd(lib, out=ctypes.c_void_p((1 << 20) + 4)) == LAPNYS_EINVAL   # misaligned
+    assert _fwd(lib, tied=1, k=ctypes.c_void_p(2 << 20)) == LAPNYS_EINVAL  # tied but k != q
+    assert _fwd(lib, d=24) == LAPNYS_ENOTSUP
+    assert _fwd(lib, ws_bytes=16) == LAPNYS_ENOSPC
+    need = lib.lapnys_workspace_bytes(1, 1, 196, 32, 49, 20, 0)
+    assert _fwd(lib, ws_bytes=need, ctx=FAKE, ctx_bytes=16) == LAPNYS_ENOSPC
+
+
+def test_bwd_rejects_bad_arguments(lib):
+    from laplacian_nystr_linear_gb300._lib import LAPNYS_EINVAL, LAPNYS_ENOSPC
+
+    def bwd(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, dout=FAKE, ctx=FAKE, dq=FAKE, dk=FAKE, dv=FAKE, tied=0,
+                 ws_bytes=0)
+        a.update(kw)
+        return lib.lapnys_bwd(a["q"], a["k"], a["v"], a["dout"], a["ctx"], a["dq"], a["dk"],
+                              a["dv"], 1, 1, 196, 32, 14, 14, 49, 32.0, 1e-3, 20, a["tied"], None,
+                              0, 0, FAKE, a["ws_bytes"])
+
+    assert bwd(ctx=None) == LAPNYS_EINVAL
+    assert bwd(dk=None) == LAPNYS_EINVAL                  # untied needs dk
+    assert bwd(tied=1, k=None) == LAPNYS_EINVAL           # tied forbids dk
+    assert bwd() == LAPNYS_ENOSPC
+
+
+def test_launch_counter_starts_at_zero_without_gpu(lib):
+    assert lib.lapnys_launch_count() == 0

@@ -1,0 +1,215 @@
+"""CUDA path against the fp64 oracle on seeded inputs (needs a GPU).
+
+Tolerance: per (b, h) slice, |gpu - oracle|_F / |oracle|_F <= 1e-4 for float32
+tensors and <= 2e-2 for bf16 tensors (fp32 accumulation); landmark indices
+bit-exact.  Full-size workloads are checked on sampled slices, computed by the
+oracle one slice at a time, in the same launch configuration the benchmark
+times (the same library call on the whole batch).
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from laplacian_nystr_linear_gb300 import api
+from laplacian_nystr_linear_gb300.inputs import WORKLOADS, Workload, make_inputs, random_inputs
+from oracle import lapnys_oracle as orc
+
+from tests._parity import compare, gpu_run, oracle_run, params_of, rel, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.init()
+
+
+def _small(name, **kw):
+    base = dict(cfg=9, B=1, H=1, grid_h=8, grid_w=8, d=32, m=16, dtype="f32", iters=8)
+    base.update(kw)
+    return Workload(name=name, **base)
+
+
+# ---------------------------------------------------------------------------
+# landmarks
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("gh,gw,m,d,dtype", [(14, 14, 49, 32, "f32"), (56, 56, 49, 64, "bf16"),
+                                             (128, 128, 256, 64, "bf16"), (10, 12, 4, 16, "f32"),
+                                             (8, 8, 64, 128, "f32"), (6, 6, 1, 64, "bf16")])
+def test_pool_indices_exact_and_values(gh, gw, m, d, dtype):
+    inp = random_inputs(100 + m, 2, 3, gh * gw, d, dtype)
+    k = to_dev(inp["k"], dtype)
+    L, idx = api.pool(k, (gh, gw), m)
+    torch.cuda.synchronize()
+    ref_idx = orc.pool_index(gh, gw, m)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+    Lg = L.cpu().numpy()
+    for b in range(2):
+        for h in range(3):
+            Lr = orc.pool_landmarks(inp["k"][b, h], ref_idx, m)
+            assert rel(Lg[b, h], Lr) < 1e-6
+
+
+# ---------------------------------------------------------------------------
+# forward intermediates (landmark matrix, alpha, every Newton-Schulz iterate, W, W-hat)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("wname", ["tiny", "tiny_mN"])
+def test_forward_intermediates(wname):
+    w = WORKLOADS[wname]
+    inp = make_inputs(w)
+    g = gpu_run(w, inp)
+    o = oracle_run(w, inp)
+    s = o["saved"][(0, 0)]
+    c = g["ctx"]
+    assert rel(c["L"][0, 0], s["L"]) < 1e-6
+    assert rel(c["A"][0, 0], s["A"]) < 1e-6
+    alpha, n1, ninf, jc, ic = orc.ns_scale(s["A"])
+    np.testing.assert_allclose(c["alpha"][0, 0, :3], [alpha, n1, ninf], rtol=1e-5)
+    code = int(c["alpha"][0, 0, 3:4].view(np.int32)[0])
+    assert (code & 0xFFFF, code >> 16) == (jc, ic)
+    for t in range(w.iters + 1):
+        assert rel(c["X"][0, 0, t], s["X"][t]) < 1e-4, t
+    assert rel(c["W"][0, 0], s["W"]) < 1e-5
+    assert rel(c["What"][0, 0], s["What"]) < 1e-4
+    np.testing.assert_array_equal(c["idx"], s["idx"])
+
+
+def test_norm_statistics():
+    w = WORKLOADS["pvt3"]
+    inp = make_inputs(w)
+    g = gpu_run(w, inp)
+    o = oracle_run(w, inp, slices={(0, 0), (31, 4)})
+    for (b, h), s in o["saved"].items():
+        mu, var, sd = s["stats"]
+        st = g["ctx"]["stats"][b, h]
+        assert rel(st[0], mu) < 1e-5
+        assert rel(st[1], var) < 1e-4
+        assert rel(st[2], 1.0 / sd) < 1e-4
+
+
+# ---------------------------------------------------------------------------
+# forward outputs at the workload shapes
+# ---------------------------------------------------------------------------
+FWD_SLICES = {
+    "tiny": None, "tiny_mN": None, "pvt1": None, "pvt2": None, "pvt3": None,
+    "hires16k": {(0, 0), (7, 7)}, "tied64k": {(0, 0), (0, 15)},
+}
+
+
+@pytest.mark.parametrize("wname", list(FWD_SLICES))
+def test_forward_workloads(wname):
+    w = WORKLOADS[wname]
+    inp = make_inputs(w, with_grad=False)
+    g = gpu_run(w, inp)
+    o = oracle_run(w, inp, slices=FWD_SLICES[wname])
+    compare(w, g, o, backward=False)
+
+
+def test_one_landmark_per_token_reaches_exact_attention():
+    # m = N, eps = 0, converged iteration: Nystrom equals k(Q, K) V
+    w = dataclasses.replace(WORKLOADS["tiny_mN"], eps=0.0, iters=30)
+    inp = make_inputs(w)
+    g = gpu_run(w, inp)
+    q, k, v = (inp[n][0, 0].astype(np.float64) for n in ("q", "k", "v"))
+    S = orc.laplacian_kernel(q, k, w.lam)
+    assert rel(g["out"][0, 0], S @ v) < 1e-3
+
+
+# ---------------------------------------------------------------------------
+# backward
+# ---------------------------------------------------------------------------
+BWD_SLICES = {"pvt2": {(0, 0), (17, 1), (31, 1)}, "pvt3": {(0, 0), (31, 4)},
+              "hires16k": {(3, 5)}}
+
+
+@pytest.mark.parametrize("wname", list(BWD_SLICES))
+def test_backward_workloads(wname):
+    w = WORKLOADS[wname]
+    inp = make_inputs(w)
+    g = gpu_run(w, inp, backward=True)
+    o = oracle_run(w, inp, slices=BWD_SLICES[wname], backward=True)
+    compare(w, g, o, backward=True)
+
+
+SMALL = [
+    _small("f32"),
+    _small("f32_norm", norm=True),
+    _small("f32_tied", tied=True),
+    _small("f32_tied_norm", tied=True, norm=True),
+    _small("bf16", dtype="bf16", d=64),
+    _small("ragged", grid_h=10, grid_w=12, m=4, d=16, iters=6),
+    _small("ragged_large_m", grid_h=12, grid_w=12, m=144, d=16, iters=10),
+    _small("m1", m=1, iters=3),
+    _small("iters0", iters=0),
+    _small("d128", d=128, m=64, iters=6),
+    _small("tiny_grid", grid_h=2, grid_w=2, m=4, d=16, iters=5),
+    _small("m81", grid_h=18, grid_w=18, m=81, d=32, iters=12, norm=True),
+    _small("batch", B=3, H=2, grid_h=16, grid_w=16, m=16, d=64, iters=10),
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_backward_small_cases(w):
+    inp = random_inputs(7 + w.m + w.d, w.B, w.H, w.N, w.d, w.dtype, tied=w.tied)
+    g = gpu_run(w, inp, backward=True)
+    o = oracle_run(w, inp, backward=True)
+    compare(w, g, o, backward=True)
+
+
+def test_constant_inputs_use_zero_sign():
+    # every token equal: all L1 distances between tokens and landmarks are 0,
+    # so sgn(0) = 0 decides the kernel gradient
+    w = _small("const", grid_h=4, grid_w=4, m=4, d=16, iters=4)
+    inp = random_inputs(3, 1, 1, w.N, w.d, "f32")
+    inp["q"] = np.full_like(inp["q"], 0.25)
+    inp["k"] = np.full_like(inp["k"], 0.25)
+    g = gpu_run(w, inp, backward=True)
+    o = oracle_run(w, inp, backward=True)
+    compare(w, g, o, backward=True)
+
+
+def test_deterministic():
+    w = WORKLOADS["pvt2"]
+    inp = make_inputs(w)
+    a = gpu_run(w, inp, backward=True)
+    b = gpu_run(w, inp, backward=True)
+    for n in ("out", "dq", "dk", "dv"):
+        np.testing.assert_array_equal(a[n], b[n])
+
+
+def test_autograd_wrapper_matches_raw_calls():
+    w = _small("autograd", d=64, m=16, iters=6, norm=True)
+    inp = random_inputs(5, 2, 2, w.N, w.d, "f32")
+    q = to_dev(inp["q"], "f32").requires_grad_(True)
+    k = to_dev(inp["k"], "f32").requires_grad_(True)
+    v = to_dev(inp["v"], "f32").requires_grad_(True)
+    from laplacian_nystr_linear_gb300 import attention
+    out = attention(q, k, v, (w.grid_h, w.grid_w), w.m, iters=w.iters, norm=True)
+    dout = to_dev(inp["dout"], "f32")
+    out.backward(dout)
+    w2 = dataclasses.replace(w, B=2, H=2)
+    g = gpu_run(w2, inp, backward=True)
+    np.testing.assert_array_equal(out.detach().cpu().numpy(), g["out"].astype(np.float32))
+    np.testing.assert_array_equal(q.grad.cpu().numpy(), g["dq"].astype(np.float32))
+    np.testing.assert_array_equal(k.grad.cpu().numpy(), g["dk"].astype(np.float32))
+    np.testing.assert_array_equal(v.grad.cpu().numpy(), g["dv"].astype(np.float32))
+
+
+def test_launch_count_and_profile():
+    w = WORKLOADS["tiny"]
+    inp = make_inputs(w)
+    p = params_of(w)
+    q, k, v = (to_dev(inp[n], "f32") for n in ("q", "k", "v"))
+    before = api.launch_count()
+    api.profile_enable(True)
+    api.fwd(q, k, v, p)
+    torch.cuda.synchronize()
+    prof = api.profile_read()
+    api.profile_enable(False)
+    launched = api.launch_count() - before
+    assert launched == sum(n for n, _ in prof.values()) and launched >= 5
+    assert all(ms >= 0 for _, ms in prof.values())
