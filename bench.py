@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=None, help="override B (smaller profiling cases)")
+    ap.add_argument("--heads", type=int, default=None, help="override H (smaller profiling cases)")
     ap.add_argument("--oracle-worker", action="store_true", help=argparse.SUPPRESS)
     return ap.parse_args()
 
@@ -201,6 +203,9 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
     w = WORKLOADS[args.workload]
+    if args.batch or args.heads:
+        import dataclasses
+        w = dataclasses.replace(w, B=args.batch or w.B, H=args.heads or w.H)
     p = api.Params(w.B, w.H, w.grid_h, w.grid_w, w.d, w.m, w.lam, w.eps, w.iters, w.tied, w.norm)
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     inp = make_inputs(w, with_grad=True)
