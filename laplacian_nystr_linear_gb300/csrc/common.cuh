@@ -56,6 +56,58 @@ __device__ __forceinline__ void load_tile(float* s, const T* g, int row0, int nr
   }
 }
 
+// Load rows [row0, row0 + ROWS) of a row-major [nrows][D] matrix into a
+// padded shared tile of ROWS rows (zero-filled past nrows).
+template <int D, int ROWS, typename T>
+__device__ __forceinline__ void load_rows(float* s, const T* g, int row0, int nrows) {
+  constexpr int C4 = D / 4;
+  for (int id = threadIdx.x; id < ROWS * C4; id += kThreads) {
+    const int r = id / C4, c = (id % C4) * 4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row0 + r < nrows) v = ld4(g + (size_t)(row0 + r) * D + c);
+    st4(s + r * row_stride(D) + c, v);
+  }
+}
+
+// CPT consecutive floats from shared memory (CPT = 1, 2 or a multiple of 4)
+template <int CPT>
+__device__ __forceinline__ void lds_cpt(const float* p, float (&v)[CPT]) {
+  if constexpr (CPT % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < CPT; i += 4) {
+      const float4 t = lds4(p + i);
+      v[i] = t.x; v[i + 1] = t.y; v[i + 2] = t.z; v[i + 3] = t.w;
+    }
+  } else if constexpr (CPT == 2) {
+    const float2 t = *reinterpret_cast<const float2*>(p);
+    v[0] = t.x; v[1] = t.y;
+  } else {
+    v[0] = p[0];
+  }
+}
+
+// CPT consecutive values to global memory
+template <int CPT>
+__device__ __forceinline__ void st_cpt(float* p, const float (&v)[CPT]) {
+  if constexpr (CPT % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < CPT; i += 4) st4(p + i, make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+  } else {
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) p[i] = v[i];
+  }
+}
+template <int CPT>
+__device__ __forceinline__ void st_cpt(__nv_bfloat16* p, const float (&v)[CPT]) {
+  if constexpr (CPT % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < CPT; i += 4) st4(p + i, make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+  } else {
+#pragma unroll
+    for (int i = 0; i < CPT; ++i) p[i] = __float2bfloat16_rn(v[i]);
+  }
+}
+
 // Register-blocked L1 distances between 4 token rows (j = 4*ty + r) and 4
 // landmark rows (a = tx + 16*s) of two shared tiles:
 //   dist[r][s] = sum_c |X[j][c] - L[a][c]|   (c ascending)

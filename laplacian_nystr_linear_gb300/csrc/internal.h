@@ -62,6 +62,14 @@ cudaError_t run_bgemm(bool ta, bool tb, int batch, int M, int N, int K, const fl
                       long sA, const float* B, int ldb, long sB, float* C, int ldc, long sC,
                       const float* E, int lde, long sE, float alpha, float beta, cudaStream_t st);
 
+// batched C[b] = alpha (op(A1) op(B1) + op(A2) op(B2)) + beta E; sym: C symmetric,
+// only tiles on/above the diagonal are computed and mirrored (K2 may be 0)
+cudaError_t run_gemm2(bool ta, bool tb, bool sym, int batch, int M, int N, const float* A1, int lda1,
+                      long sA1, const float* B1, int ldb1, long sB1, int K1, const float* A2,
+                      int lda2, long sA2, const float* B2, int ldb2, long sB2, int K2, float* C,
+                      int ldc, long sC, const float* E, int lde, long sE, float alpha, float beta,
+                      cudaStream_t st);
+
 // forward passes
 cudaError_t run_key_fwd(const Prob& p, const void* k, const void* v, const float* L, float* part,
                         cudaStream_t st);
@@ -90,6 +98,8 @@ struct BwdArgs {
   float* ns_part;     // [BH][S][2][mp]: sum dZ, sum dZ*Z (mode 0)
 };
 cudaError_t run_bwd_tile(const Prob& p, int mode, const BwdArgs& a, cudaStream_t st);
+// modes 1 and 2 with the FMA-pipe sign term (32-token blocks)
+cudaError_t run_bwd_pair(const Prob& p, int mode, const BwdArgs& a, cudaStream_t st);
 cudaError_t run_mdz(const Prob& p, const float* ns_part, float* mdz, cudaStream_t st);
 cudaError_t run_gram_bwd(const Prob& p, const float* L, const float* A, const float* dA, float* dLA,
                          cudaStream_t st);

@@ -1,0 +1,527 @@
+// Backward tile kernels of Laplacian-kernel Nystrom attention, query side
+// (MODE 1) and key side (MODE 2).
+//
+// The Laplacian kernel k(x, l) = exp(-|x - l|_1 / lambda) has the
+// non-vanishing L1 gradient dk/dx_c = -(k / lambda) sgn(x_c - l_c)
+// ("LaplacianFormer", Dutch summary Methodology 1; Arabic summary 2a).  With
+// an upstream weight g_ja per (token, landmark) pair,
+//     dX_jc  = -sum_a g_ja sgn(x_jc - l_ac)      (token side, per landmark tile)
+//     dL_ac +=  sum_j g_ja sgn(x_jc - l_ac)      (landmark side, over the split)
+// Writing sgn(t) = 2 [t > 0] - 1 for t != 0, the sums become
+//     dX_jc  = G_j  - sum_a 2 g_ja [x_jc > l_ac],   G_j = sum_a g_ja
+//     dL_ac +=        sum_j 2 g_ja [x_jc > l_ac] - G'_a,  G'_a = sum_j g_ja
+// and [x > l] is one saturated FMA, sat(fma(x, 2^64, -2^64 l)), which is exactly
+// 0 or 1 whenever x != l and both lie in {0} u [2^-40, 2^60] (the difference is
+// then at least 2^-64).  So the sign term costs three FMA-pipe operations per
+// (token, landmark, feature) instead of compare/select work on the half-rate
+// ALU pipe.  Ties and out-of-range values are found before the main loop by a
+// binary search over the sorted landmark columns; a token block that has one
+// takes an exact path with sgn(0) = 0.
+//
+// Work split per CTA: one 64-landmark tile and a contiguous range of 32-token
+// blocks; per block
+//   phase 1  (thread = 4 tokens x 2 landmarks)  distance, dot, kernel value, g
+//   phase S  (warp = D/8 features, lane = 8 tokens x 8 landmarks) sign term
+//   phase C  contraction: dW-hat_a += sum_j Z_ja dO_j (query side) or
+//            dV_j = sum_a C_ja dW_a (key side)
+#include "common.cuh"
+#include "internal.h"
+
+namespace lapnys {
+
+namespace {
+constexpr int TJ = 32;            // tokens per block
+constexpr int TA = 64;            // landmarks per tile
+constexpr int AS = TA + 4;        // row stride of [*][TA] tiles
+constexpr int JS = TJ + 4;        // row stride of the transposed token tile
+constexpr float kBig = 18446744073709551616.0f;   // 2^64
+constexpr float kInvBig = 5.42101086242752217e-20f;  // 2^-64
+constexpr float kLo = 9.094947017729282e-13f;        // 2^-40
+constexpr float kHi = 1.152921504606846976e18f;      // 2^60
+constexpr int kMaxFlagBlocks = 4096;                  // per-CTA block flags (bits)
+
+__device__ __forceinline__ float fma_sat(float a, float b, float c) {
+  float d;
+  asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+__device__ __forceinline__ bool out_of_range(float v) {
+  const float a = fabsf(v);
+  return !(a <= kHi) || (a != 0.f && a < kLo);
+}
+
+__device__ __forceinline__ float ldx(const float* p) { return __ldg(p); }
+__device__ __forceinline__ float ldx(const __nv_bfloat16* p) {
+  return __uint_as_float(((uint32_t)__ldg(reinterpret_cast<const unsigned short*>(p))) << 16);
+}
+
+template <int D>
+struct Smem {
+  static constexpr int kScrWarp = 32 * 8 + 3 * 8;  // 8 floats per lane, 8 pad per 8 lanes
+  static constexpr int LBt = 0;                    // [D][AS]   -scale * l, transposed
+  static constexpr int Rs = LBt + D * AS;          // [TA][D+4] R rows
+  static constexpr int Xt = Rs + TA * (D + 4);     // [D][JS]   tokens, transposed
+  static constexpr int Us = Xt + D * JS;           // [TJ][D+4] U rows
+  static constexpr int Gs = Us + TJ * (D + 4);     // [TJ][AS]  2g
+  static constexpr int Zs = Gs + TJ * AS;          // [TJ][AS]  Z (query side) or C (key side)
+  static constexpr int Scr = Zs + TJ * AS;         // per-warp exchange areas
+  static constexpr int dLs = Scr + 8 * kScrWarp;   // [D][TA]   landmark-side accumulator
+  static constexpr int total = dLs + D * TA;
+  static constexpr int Ss = Xt;                    // sorted landmark columns [TA][D], pre-pass only
+  static constexpr int Stage = Gs;                 // dX staging [TJ][D+4] over Gs and Zs
+  static_assert(TA * D <= dLs - Xt, "sorted columns must fit before the accumulator");
+  static_assert(TJ * (D + 4) <= 2 * TJ * AS, "staging must fit in the g and Z tiles");
+};
+}  // namespace
+
+// Sign term for the warp's feature columns [cbase, cbase + D/8): lane (jg, ag)
+// holds 2g for tokens j0..j0+7 x landmarks al..al+7; partial sums are exchanged
+// through the warp's scratch area; the token-side result goes to Stage and the
+// landmark-side sum into dLs.
+template <int D, bool EXACT>
+__device__ __forceinline__ void sign_cols(int cbase, int j0, int al, int jg, int ag,
+                                          const float (&g2)[8][8], const float* Xt,
+                                          const float* LBt, float* mine, const float* qsrc,
+                                          const float* lsrc, float rowg, float inv_scale,
+                                          float* Stage, float* dLs) {
+  constexpr int CW = D / 8;
+#pragma unroll 1
+  for (int ci = 0; ci < CW; ++ci) {
+    const int c = cbase + ci;
+    float x[8], lb[8];
+    {
+      const float4 u = lds4(Xt + c * JS + j0);
+      const float4 v = lds4(Xt + c * JS + j0 + 4);
+      x[0] = u.x; x[1] = u.y; x[2] = u.z; x[3] = u.w;
+      x[4] = v.x; x[5] = v.y; x[6] = v.z; x[7] = v.w;
+    }
+    {
+      const float4 u = lds4(LBt + c * AS + al);
+      const float4 v = lds4(LBt + c * AS + al + 4);
+      lb[0] = u.x; lb[1] = u.y; lb[2] = u.z; lb[3] = u.w;
+      lb[4] = v.x; lb[5] = v.y; lb[6] = v.z; lb[7] = v.w;
+    }
+    float pq[8], pl[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) pq[t] = pl[t] = 0.f;
+    if (!EXACT) {
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const float p = fma_sat(x[r], kBig, lb[t]);
+          pq[r] = fmaf(g2[r][t], p, pq[r]);
+          pl[t] = fmaf(g2[r][t], p, pl[t]);
+        }
+    } else {
+      // exact sgn with sgn(0) = 0; l = -lb / scale (a power of two: exact)
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const float v = sgn_times(x[r] + lb[t] * inv_scale, 0.5f * g2[r][t]);
+          pq[r] += v;
+          pl[t] += v;
+        }
+    }
+    st4(mine, make_float4(pq[0], pq[1], pq[2], pq[3]));
+    st4(mine + 4, make_float4(pq[4], pq[5], pq[6], pq[7]));
+    __syncwarp();
+    float qs = 0.f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) qs += qsrc[8 * q];
+    __syncwarp();
+    st4(mine, make_float4(pl[0], pl[1], pl[2], pl[3]));
+    st4(mine + 4, make_float4(pl[4], pl[5], pl[6], pl[7]));
+    __syncwarp();
+    float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 v = *reinterpret_cast<const float2*>(lsrc + 72 * q);
+      ls0 += v.x;
+      ls1 += v.y;
+    }
+    __syncwarp();
+    // fast path: dX = G_j - sum_a 2 g [x > l];  exact path: dX = -sum_a g sgn
+    Stage[(j0 + ag) * (D + 4) + c] = EXACT ? -qs : rowg - qs;
+    float2* dl = reinterpret_cast<float2*>(dLs + c * TA + al + 2 * jg);
+    float2 o = *dl;
+    o.x += ls0;
+    o.y += ls1;
+    *dl = o;
+  }
+}
+
+template <int D, typename T, int MODE, bool NORM>
+__global__ void __launch_bounds__(kThreads, 2)
+    k_bwd_pair(const T* __restrict__ X, const T* __restrict__ U, const float* __restrict__ L,
+               const float* __restrict__ R, const float* __restrict__ stats,
+               const float* __restrict__ mdz, float* __restrict__ tok_part,
+               float* __restrict__ tok_part2, float* __restrict__ lm_part,
+               float* __restrict__ lm_part2, int N, int m, int mp, int S, int nblk, int BH,
+               float ns, float inv_lam) {
+  constexpr int CW = D / 8;     // features per warp in phase S
+  constexpr int CPT = D / 16;   // features per thread in phase C
+  constexpr bool kDWhat = (MODE == 1) && !NORM;
+  using SM = Smem<D>;
+  extern __shared__ float4 sm4[];
+  float* sm = reinterpret_cast<float*>(sm4);
+  float* LBt = sm + SM::LBt;
+  float* Rs = sm + SM::Rs;
+  float* Xt = sm + SM::Xt;
+  float* Us = sm + SM::Us;
+  float* Gs = sm + SM::Gs;
+  float* Zs = sm + SM::Zs;
+  float* Scr = sm + SM::Scr;
+  float* dLs = sm + SM::dLs;
+  float* Ss = sm + SM::Ss;
+  float* Stage = sm + SM::Stage;
+  __shared__ float mu_s[TA], rs_s[TA], m0_s[TA], m1_s[TA];
+  __shared__ unsigned flag_bits[kMaxFlagBlocks / 32];
+
+  const int lt = blockIdx.x, sp = blockIdx.y, bh = blockIdx.z;
+  const int a0 = lt * TA;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nv = min(TA, m - a0);  // valid landmarks in this tile
+  const T* Xb = X + (size_t)bh * N * D;
+  const T* Ub = U + (size_t)bh * N * D;
+  const float* Lb = L + ((size_t)bh * m + a0) * D;
+
+  // ---- landmark range check, R tile, statistics ----
+  bool bad_l = false;
+  for (int e = tid; e < nv * D; e += kThreads)
+    if (out_of_range(__ldg(Lb + e))) bad_l = true;
+  load_tile<D>(Rs, R + (size_t)bh * m * D, a0, m);
+  if (NORM && tid < TA) {
+    const int a = a0 + tid;
+    const float* stb = stats + (size_t)bh * 3 * m;
+    mu_s[tid] = a < m ? stb[a] : 0.f;
+    rs_s[tid] = a < m ? stb[2 * m + a] : 0.f;
+    m0_s[tid] = mdz[(size_t)bh * 2 * mp + a0 + tid];
+    m1_s[tid] = mdz[(size_t)bh * 2 * mp + mp + a0 + tid];
+  }
+  for (int e = tid; e < kMaxFlagBlocks / 32; e += kThreads) flag_bits[e] = 0u;
+  for (int e = tid; e < D * TA; e += kThreads) dLs[e] = 0.f;
+  // landmarks outside {0} u [2^-40, 2^60] force the exact path for the whole CTA;
+  // then distances use scale 1 instead of 2^64
+  const bool cta_exact = __syncthreads_or(bad_l) != 0;
+  const float scale = cta_exact ? 1.f : kBig;
+  const float inv_scale = cta_exact ? 1.f : kInvBig;
+  const float ns_s = ns * inv_scale;  // exp2 argument per unit of scaled distance
+  for (int e = tid; e < TA * D; e += kThreads) {
+    const int c = e / TA, a = e % TA;
+    LBt[c * AS + a] = a < nv ? -scale * __ldg(Lb + (size_t)a * D + c) : 0.f;
+  }
+  __syncthreads();
+
+  int b0, b1;
+  b0 = (int)((long long)nblk * sp / S);
+  b1 = (int)((long long)nblk * (sp + 1) / S);
+
+  // ---- tie / range pre-pass over this CTA's token blocks ----
+  if (!cta_exact) {
+    // sorted landmark columns (invalid landmarks sort last as +inf): a value's
+    // rank is the number of smaller values, ties broken by index
+    const float inf = __int_as_float(0x7f800000);
+    for (int e = tid; e < TA * D; e += kThreads) {
+      const int i = e / D, c = e % D;
+      const float v = i < nv ? LBt[c * AS + i] * -kInvBig : inf;
+      int rank = 0;
+      for (int k = 0; k < TA; ++k) {
+        const float w = k < nv ? LBt[c * AS + k] * -kInvBig : inf;
+        rank += (w < v) || (w == v && k < i);
+      }
+      Ss[rank * D + c] = v;
+    }
+    __syncthreads();
+    for (int b = b0; b < b1; ++b) {
+      bool tie = false;
+      for (int e = tid; e < TJ * D; e += kThreads) {
+        const int j = e / D, c = e % D;
+        const int n = b * TJ + j;
+        if (n >= N) break;
+        const float x = ldx(Xb + (size_t)n * D + c);
+        if (out_of_range(x)) {
+          tie = true;
+        } else {
+          int lo = 0;
+#pragma unroll
+          for (int step = TA / 2; step > 0; step >>= 1)
+            if (Ss[(lo + step - 1) * D + c] < x) lo += step;
+          if (lo < TA && Ss[lo * D + c] == x) tie = true;
+        }
+      }
+      const int any = __syncthreads_or(tie);
+      const int k = b - b0;
+      if (tid == 0 && any && k < kMaxFlagBlocks) flag_bits[k >> 5] |= 1u << (k & 31);
+    }
+  }
+  __syncthreads();
+
+  // phase S ownership: warp -> features [warp*CW, +CW); lane (jg, ag) -> tokens
+  // 8 jg .. 8 jg + 7 and landmarks 8 ag .. 8 ag + 7
+  const int jg = lane >> 3, ag = lane & 7;
+  float colg_acc0 = 0.f, colg_acc1 = 0.f;
+  // phase C ownership (query side dW-hat): landmarks 4 (tid >> 4) + s, features (tid & 15) CPT ..
+  float dw[4][CPT];
+#pragma unroll
+  for (int s = 0; s < 4; ++s)
+#pragma unroll
+    for (int c = 0; c < CPT; ++c) dw[s][c] = 0.f;
+
+  for (int b = b0; b < b1; ++b) {
+    const int n0 = b * TJ;
+    const int k = b - b0;
+    const bool exact =
+        cta_exact || k >= kMaxFlagBlocks || ((flag_bits[k >> 5] >> (k & 31)) & 1u);
+    __syncthreads();
+    // tokens transposed (Xt[c][j]) and U rows
+    for (int id = tid; id < TJ * (D / 4); id += kThreads) {
+      const int c4 = id / TJ, j = id % TJ;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (n0 + j < N) v = ld4(Xb + (size_t)(n0 + j) * D + c4 * 4);
+      Xt[(c4 * 4 + 0) * JS + j] = v.x;
+      Xt[(c4 * 4 + 1) * JS + j] = v.y;
+      Xt[(c4 * 4 + 2) * JS + j] = v.z;
+      Xt[(c4 * 4 + 3) * JS + j] = v.w;
+    }
+    load_rows<D, TJ>(Us, Ub, n0, N);
+    __syncthreads();
+
+    // ---- phase 1: thread = tokens 4 warp .. +3, landmarks lane and lane + 32 ----
+    {
+      const int jb = 4 * warp;
+      float dist[4][2], dot[4][2];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) dist[r][0] = dist[r][1] = dot[r][0] = dot[r][1] = 0.f;
+#pragma unroll 2
+      for (int c = 0; c < D; c += 4) {
+        const float4 r0 = lds4(Rs + lane * (D + 4) + c);
+        const float4 r1 = lds4(Rs + (lane + 32) * (D + 4) + c);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 x4 = lds4(Xt + (c + q) * JS + jb);
+          const float lb0 = LBt[(c + q) * AS + lane], lb1 = LBt[(c + q) * AS + lane + 32];
+          dist[0][0] += fabsf(fmaf(x4.x, scale, lb0)); dist[0][1] += fabsf(fmaf(x4.x, scale, lb1));
+          dist[1][0] += fabsf(fmaf(x4.y, scale, lb0)); dist[1][1] += fabsf(fmaf(x4.y, scale, lb1));
+          dist[2][0] += fabsf(fmaf(x4.z, scale, lb0)); dist[2][1] += fabsf(fmaf(x4.z, scale, lb1));
+          dist[3][0] += fabsf(fmaf(x4.w, scale, lb0)); dist[3][1] += fabsf(fmaf(x4.w, scale, lb1));
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const float4 u4 = lds4(Us + (jb + r) * (D + 4) + c);
+          dot[r][0] = fmaf(u4.x, r0.x, dot[r][0]);
+          dot[r][0] = fmaf(u4.y, r0.y, dot[r][0]);
+          dot[r][0] = fmaf(u4.z, r0.z, dot[r][0]);
+          dot[r][0] = fmaf(u4.w, r0.w, dot[r][0]);
+          dot[r][1] = fmaf(u4.x, r1.x, dot[r][1]);
+          dot[r][1] = fmaf(u4.y, r1.y, dot[r][1]);
+          dot[r][1] = fmaf(u4.z, r1.z, dot[r][1]);
+          dot[r][1] = fmaf(u4.w, r1.w, dot[r][1]);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int j = jb + r, a = lane + 32 * h;
+          const bool valid = (n0 + j < N) && (a < nv);
+          const float kv = exp2f(dist[r][h] * ns_s);
+          float g, zc;
+          if (MODE == 2) {
+            g = dot[r][h] * kv * inv_lam;
+            zc = kv;
+          } else {
+            const float z = NORM ? (kv - mu_s[a]) * rs_s[a] : kv;
+            const float dp = NORM ? (dot[r][h] - m0_s[a] - z * m1_s[a]) * rs_s[a] : dot[r][h];
+            g = dp * kv * inv_lam;
+            zc = z;
+          }
+          Gs[j * AS + a] = valid ? 2.f * g : 0.f;
+          Zs[j * AS + a] = valid ? zc : 0.f;
+        }
+    }
+    __syncthreads();
+
+    // ---- phase C: contractions ----
+    if (kDWhat) {
+      const int ty = tid >> 4, tx = tid & 15;
+#pragma unroll 4
+      for (int j = 0; j < TJ; ++j) {
+        const float4 z4 = lds4(Zs + j * AS + 4 * ty);
+        float uv[CPT];
+        lds_cpt<CPT>(Us + j * (D + 4) + tx * CPT, uv);
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) {
+          dw[0][c] = fmaf(z4.x, uv[c], dw[0][c]);
+          dw[1][c] = fmaf(z4.y, uv[c], dw[1][c]);
+          dw[2][c] = fmaf(z4.z, uv[c], dw[2][c]);
+          dw[3][c] = fmaf(z4.w, uv[c], dw[3][c]);
+        }
+      }
+    }
+    if (MODE == 2) {
+      // dV_j = sum_a C_ja dW_a: thread = tokens {ty, ty + 16}, features tx CPT ..
+      const int ty = tid >> 4, tx = tid & 15;
+      float v0[CPT], v1[CPT];
+#pragma unroll
+      for (int c = 0; c < CPT; ++c) v0[c] = v1[c] = 0.f;
+#pragma unroll 2
+      for (int a = 0; a < TA; a += 4) {
+        const float4 c0 = lds4(Zs + ty * AS + a);
+        const float4 c1 = lds4(Zs + (ty + 16) * AS + a);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float rv[CPT];
+          lds_cpt<CPT>(Rs + (a + q) * (D + 4) + tx * CPT, rv);
+          const float ck0 = comp(c0, q), ck1 = comp(c1, q);
+#pragma unroll
+          for (int c = 0; c < CPT; ++c) {
+            v0[c] = fmaf(ck0, rv[c], v0[c]);
+            v1[c] = fmaf(ck1, rv[c], v1[c]);
+          }
+        }
+      }
+      if (n0 + ty < N)
+        st_cpt<CPT>(tok_part2 + (((size_t)lt * BH + bh) * N + n0 + ty) * D + tx * CPT, v0);
+      if (n0 + ty + 16 < N)
+        st_cpt<CPT>(tok_part2 + (((size_t)lt * BH + bh) * N + n0 + ty + 16) * D + tx * CPT, v1);
+    }
+
+    // ---- phase S: sign term ----
+    {
+      const int j0 = 8 * jg, al = 8 * ag;
+      float g2[8][8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const float4 u = lds4(Gs + (j0 + r) * AS + al);
+        const float4 v = lds4(Gs + (j0 + r) * AS + al + 4);
+        g2[r][0] = u.x; g2[r][1] = u.y; g2[r][2] = u.z; g2[r][3] = u.w;
+        g2[r][4] = v.x; g2[r][5] = v.y; g2[r][6] = v.z; g2[r][7] = v.w;
+      }
+      // per-warp exchange area: lane l's 8 values at 8 l + 8 (l >> 3)
+      float* scr = Scr + warp * SM::kScrWarp;
+      float* mine = scr + 8 * lane + 8 * jg;
+      // token side gathers element ag of lanes 8 jg + q; landmark side gathers
+      // elements 2 jg, 2 jg + 1 of lanes 8 q + ag
+      const float* qsrc = scr + 72 * jg + ag;
+      const float* lsrc = scr + 8 * ag + 2 * jg;
+      float rowg, colg0, colg1;
+      {
+        float t8[8];
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          t8[r] = 0.f;
+#pragma unroll
+          for (int t = 0; t < 8; ++t) t8[r] += g2[r][t];
+        }
+        st4(mine, make_float4(t8[0], t8[1], t8[2], t8[3]));
+        st4(mine + 4, make_float4(t8[4], t8[5], t8[6], t8[7]));
+        __syncwarp();
+        rowg = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) rowg += qsrc[8 * q];
+        __syncwarp();
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          t8[t] = 0.f;
+#pragma unroll
+          for (int r = 0; r < 8; ++r) t8[t] += g2[r][t];
+        }
+        st4(mine, make_float4(t8[0], t8[1], t8[2], t8[3]));
+        st4(mine + 4, make_float4(t8[4], t8[5], t8[6], t8[7]));
+        __syncwarp();
+        colg0 = colg1 = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 v = *reinterpret_cast<const float2*>(lsrc + 72 * q);
+          colg0 += v.x;
+          colg1 += v.y;
+        }
+        __syncwarp();
+      }
+      if (!exact) {
+        colg_acc0 += 0.5f * colg0;
+        colg_acc1 += 0.5f * colg1;
+      }
+      rowg *= 0.5f;  // the identities use sums of g, the tile holds 2g
+      __syncthreads();  // g and Z tiles are free from here on (staging)
+
+      if (exact)
+        sign_cols<D, true>(warp * CW, j0, al, jg, ag, g2, Xt, LBt, mine, qsrc, lsrc, rowg,
+                           inv_scale, Stage, dLs);
+      else
+        sign_cols<D, false>(warp * CW, j0, al, jg, ag, g2, Xt, LBt, mine, qsrc, lsrc, rowg,
+                            inv_scale, Stage, dLs);
+    }
+    __syncthreads();
+    // staged token-side results -> per-tile partial rows
+    for (int id = tid; id < TJ * (D / 4); id += kThreads) {
+      const int j = id / (D / 4), c = (id % (D / 4)) * 4;
+      if (n0 + j < N)
+        st4(tok_part + (((size_t)lt * BH + bh) * N + n0 + j) * D + c, lds4(Stage + j * (D + 4) + c));
+    }
+  }
+
+  // ---- landmark-side outputs: dL = accumulated sum - sum of g per landmark ----
+  {
+    const int al = 8 * ag + 2 * jg;
+    float* o = lm_part + ((size_t)bh * S + sp) * mp * D;
+#pragma unroll
+    for (int ci = 0; ci < CW; ++ci) {
+      const int c = warp * CW + ci;
+      o[(size_t)(a0 + al) * D + c] = dLs[c * TA + al] - colg_acc0;
+      o[(size_t)(a0 + al + 1) * D + c] = dLs[c * TA + al + 1] - colg_acc1;
+    }
+  }
+  if (kDWhat) {
+    const int ty = tid >> 4, tx = tid & 15;
+    float* o = lm_part2 + (((size_t)bh * S + sp) * mp + a0 + 4 * ty) * D + tx * CPT;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) st_cpt<CPT>(o + (size_t)s * D, dw[s]);
+  }
+}
+
+template <int D, typename T, int MODE, bool NORM>
+static cudaError_t bwd_pair_t2(const Prob& p, const BwdArgs& a, cudaStream_t st) {
+  const size_t smem = (size_t)Smem<D>::total * sizeof(float);
+  static bool once = (allow_smem(k_bwd_pair<D, T, MODE, NORM>, smem), true);
+  (void)once;
+  static const char* names[3] = {"", "bwd_query", "bwd_key"};
+  const int nblk = (p.N + TJ - 1) / TJ;
+  return launch(names[MODE], k_bwd_pair<D, T, MODE, NORM>, dim3(p.nt, p.Sb, p.BH), dim3(kThreads),
+                smem, st, (const T*)a.X, (const T*)a.U, a.L, a.R, a.stats, a.mdz, a.tok_part,
+                a.tok_part2, a.lm_part, a.lm_part2, p.N, p.m, p.mp, p.Sb, nblk, p.BH, p.ns,
+                p.inv_lam);
+}
+
+template <int D, typename T>
+static cudaError_t bwd_pair_t(const Prob& p, int mode, const BwdArgs& a, cudaStream_t st) {
+  if (mode == 1) {
+    if (p.norm()) return bwd_pair_t2<D, T, 1, true>(p, a, st);
+    return bwd_pair_t2<D, T, 1, false>(p, a, st);
+  }
+  return bwd_pair_t2<D, T, 2, false>(p, a, st);
+}
+
+cudaError_t run_bwd_pair(const Prob& p, int mode, const BwdArgs& a, cudaStream_t st) {
+  if (p.dtype == 1) {
+    switch (p.d) {
+      case 16: return bwd_pair_t<16, __nv_bfloat16>(p, mode, a, st);
+      case 32: return bwd_pair_t<32, __nv_bfloat16>(p, mode, a, st);
+      case 64: return bwd_pair_t<64, __nv_bfloat16>(p, mode, a, st);
+      case 128: return bwd_pair_t<128, __nv_bfloat16>(p, mode, a, st);
+    }
+  } else {
+    switch (p.d) {
+      case 16: return bwd_pair_t<16, float>(p, mode, a, st);
+      case 32: return bwd_pair_t<32, float>(p, mode, a, st);
+      case 64: return bwd_pair_t<64, float>(p, mode, a, st);
+      case 128: return bwd_pair_t<128, float>(p, mode, a, st);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace lapnys

@@ -20,34 +20,6 @@
 
 namespace lapnys {
 
-// ---- CPT-wide (D / 16 columns per thread) shared loads and global stores --
-template <int CPT>
-__device__ __forceinline__ void lds_cpt(const float* p, float (&v)[CPT]) {
-  if constexpr (CPT % 4 == 0) {
-#pragma unroll
-    for (int i = 0; i < CPT; i += 4) {
-      const float4 t = lds4(p + i);
-      v[i] = t.x; v[i + 1] = t.y; v[i + 2] = t.z; v[i + 3] = t.w;
-    }
-  } else if constexpr (CPT == 2) {
-    const float2 t = *reinterpret_cast<const float2*>(p);
-    v[0] = t.x; v[1] = t.y;
-  } else {
-    v[0] = p[0];
-  }
-}
-
-template <int CPT>
-__device__ __forceinline__ void st_cpt(float* p, const float (&v)[CPT]) {
-#pragma unroll
-  for (int i = 0; i < CPT; ++i) p[i] = v[i];
-}
-template <int CPT>
-__device__ __forceinline__ void st_cpt(__nv_bfloat16* p, const float (&v)[CPT]) {
-#pragma unroll
-  for (int i = 0; i < CPT; ++i) p[i] = __float2bfloat16_rn(v[i]);
-}
-
 __device__ __forceinline__ void split_range(int nblk, int S, int s, int& b0, int& b1) {
   b0 = (int)((long long)nblk * s / S);
   b1 = (int)((long long)nblk * (s + 1) / S);

@@ -196,12 +196,14 @@ static int ns_forward_large(const Prob& p, const float* A, float* X, float* Y, i
     float* Xt = X + (long)(t % nx) * mm;
     float* Xn = X + (long)((t + 1) % nx) * mm;
     float* Yt = Y + (long)(t % ny) * mm;
-    // Y_t = A X_t
-    CK(run_bgemm(false, false, p.BH, m, m, m, A, m, mm, Xt, m, nx * mm, Yt, m, ny * mm, nullptr, m,
-                 0, 1.f, 0.f, st));
-    // X_{t+1} = 2 X_t - X_t Y_t
-    CK(run_bgemm(false, false, p.BH, m, m, m, Xt, m, nx * mm, Yt, m, ny * mm, Xn, m, nx * mm, Xt, m,
-                 nx * mm, -1.f, 2.f, st));
+    // Y_t = A X_t, computed in full: forcing this product to be exactly
+    // symmetric makes the fp32 iteration diverge in its unconverged directions
+    CK(run_gemm2(false, false, false, p.BH, m, m, A, m, mm, Xt, m, nx * mm, m, nullptr, 0, 0,
+                 nullptr, 0, 0, 0, Yt, m, ny * mm, nullptr, m, 0, 1.f, 0.f, st));
+    // X_{t+1} = 2 X_t - X_t Y_t, written symmetric (stable: the residual
+    // I - A X_{t+1} = (I - A X_t)^2 keeps contracting)
+    CK(run_gemm2(false, false, true, p.BH, m, m, Xt, m, nx * mm, Yt, m, ny * mm, m, nullptr, 0, 0,
+                 nullptr, 0, 0, 0, Xn, m, nx * mm, Xt, m, nx * mm, -1.f, 2.f, st));
   }
   return LAPNYS_OK;
 }
@@ -306,8 +308,8 @@ int lapnys_fwd(const void* q, const void* k, const void* v, void* out, int B, in
   CK(run_reduce_parts(p.BH, p.Sk, m, p.mp, d, kpart, W, stream));
   const float* XT = X + (long)(iters % c.nx) * mm;
   // W-hat = X_T W
-  CK(run_bgemm(false, false, p.BH, m, d, m, XT, m, c.nx * mm, W, d, (long)m * d, What, d,
-               (long)m * d, nullptr, d, 0, 1.f, 0.f, stream));
+  CK(run_gemm2(false, false, false, p.BH, m, d, XT, m, c.nx * mm, W, d, (long)m * d, m, nullptr, 0,
+               0, nullptr, 0, 0, 0, What, d, (long)m * d, nullptr, d, 0, 1.f, 0.f, stream));
   if (p.norm()) {
     float* spart = (float*)(wb + w.spart);
     CK(run_qstats(p, q, L, spart, stream));
@@ -379,39 +381,48 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
     CK(run_mdz(p, nsp, mdz, stream));
     CK(run_reduce_parts(p.BH, p.Sb, m, p.mp, d, dWhp, dWh, stream));
   }
-  CK(run_bwd_tile(p, 1, qa, stream));
+  CK(run_bwd_pair(p, 1, qa, stream));
   if (!p.norm()) CK(run_reduce_parts(p.BH, p.Sb, m, p.mp, d, dWhp, dWh, stream));
 
   // ---- W-hat = X_T W and the Newton-Schulz iteration ----
   const float* XT = X + (long)iters * mm;
   const long xs = (long)(iters + 1) * mm;
   const long ys = (long)c.ny * mm;
-  // G = dLoss/dX_T = dW-hat W^T ;  dW = X_T^T dW-hat
-  CK(run_bgemm(false, true, p.BH, m, m, d, dWh, d, md, W, d, md, G, m, mm, nullptr, m, 0, 1.f, 0.f,
-               stream));
-  CK(run_bgemm(true, false, p.BH, m, d, m, XT, m, xs, dWh, d, md, dW, d, md, nullptr, d, 0, 1.f,
-               0.f, stream));
   if (m <= kTile) {
+    // G = dLoss/dX_T = dW-hat W^T ;  dW = X_T^T dW-hat
+    CK(run_bgemm(false, true, p.BH, m, m, d, dWh, d, md, W, d, md, G, m, mm, nullptr, m, 0, 1.f,
+                 0.f, stream));
+    CK(run_bgemm(true, false, p.BH, m, d, m, XT, m, xs, dWh, d, md, dW, d, md, nullptr, d, 0, 1.f,
+                 0.f, stream));
     CK(run_ns_bwd_small(p, A, alpha, X, Y, G, dA, stream));
   } else {
+    // Exact reverse of the forward's own products (Y_t = A X_t, then X_t Y_t).
+    // The unconverged directions grow by about 2 per step in this recursion, so
+    // it must not lean on X_t commuting with A: in fp32 that shortcut diverges.
+    // G = dLoss/dX_T = dW-hat W^T ;  dW = X_T^T dW-hat
+    CK(run_gemm2(false, true, false, p.BH, m, m, dWh, d, md, W, d, md, d, nullptr, 0, 0, nullptr, 0,
+                 0, 0, G, m, mm, nullptr, m, 0, 1.f, 0.f, stream));
+    CK(run_gemm2(true, false, false, p.BH, m, d, XT, m, xs, dWh, d, md, m, nullptr, 0, 0, nullptr,
+                 0, 0, 0, dW, d, md, nullptr, d, 0, 1.f, 0.f, stream));
     if (iters == 0) CK(run_zero(dA, (size_t)p.BH * mm, stream));
+    float* Sc = G;
     for (int t = iters - 1; t >= 0; --t) {
       const float* Xt = X + (long)t * mm;
       const float* Yt = Y + (long)t * mm;
       // XG = X_t^T G
-      CK(run_bgemm(true, false, p.BH, m, m, m, Xt, m, xs, G, m, mm, XG, m, mm, nullptr, m, 0, 1.f,
-                   0.f, stream));
-      // dA = dA - XG X_t^T   (first step initialises dA)
-      CK(run_bgemm(false, true, p.BH, m, m, m, XG, m, mm, Xt, m, xs, dA, m, mm, dA, m, mm, -1.f,
-                   t == iters - 1 ? 0.f : 1.f, stream));
+      CK(run_gemm2(true, false, false, p.BH, m, m, Xt, m, xs, Sc, m, mm, m, nullptr, 0, 0, nullptr,
+                   0, 0, 0, XG, m, mm, nullptr, m, 0, 1.f, 0.f, stream));
+      // dA = dA - XG X_t^T   (the first step initialises dA)
+      CK(run_gemm2(false, true, false, p.BH, m, m, XG, m, mm, Xt, m, xs, m, nullptr, 0, 0, nullptr,
+                   0, 0, 0, dA, m, mm, dA, m, mm, -1.f, t == iters - 1 ? 0.f : 1.f, stream));
       // Tm = 2 G - G Y_t^T
-      CK(run_bgemm(false, true, p.BH, m, m, m, G, m, mm, Yt, m, ys, Tm, m, mm, G, m, mm, -1.f, 2.f,
-                   stream));
+      CK(run_gemm2(false, true, false, p.BH, m, m, Sc, m, mm, Yt, m, ys, m, nullptr, 0, 0, nullptr,
+                   0, 0, 0, Tm, m, mm, Sc, m, mm, -1.f, 2.f, stream));
       // G = Tm - A^T XG
-      CK(run_bgemm(true, false, p.BH, m, m, m, A, m, mm, XG, m, mm, G, m, mm, Tm, m, mm, -1.f, 1.f,
-                   stream));
+      CK(run_gemm2(true, false, false, p.BH, m, m, A, m, mm, XG, m, mm, m, nullptr, 0, 0, nullptr, 0,
+                   0, 0, Sc, m, mm, Tm, m, mm, -1.f, 1.f, stream));
     }
-    CK(run_alpha_bwd(p, A, alpha, G, dA, stream));
+    CK(run_alpha_bwd(p, A, alpha, Sc, dA, stream));
   }
   CK(run_gram_bwd(p, L, A, dA, dLA, stream));
 
@@ -420,7 +431,7 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
   memset(&ka, 0, sizeof(ka));
   ka.X = k; ka.U = v; ka.L = L; ka.R = dW;
   ka.tok_part = dKp; ka.tok_part2 = dVp; ka.lm_part = dLcp;
-  CK(run_bwd_tile(p, 2, ka, stream));
+  CK(run_bwd_pair(p, 2, ka, stream));
   CK(run_reduce_dl(p, dLqp, dLcp, dLA, dL, stream));
   CK(run_finalize(p, dQp, dKp, dVp, dL, dq, dk, dv, stream));
   return LAPNYS_OK;

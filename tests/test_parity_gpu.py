@@ -132,7 +132,7 @@ def test_backward_workloads(wname):
     inp = make_inputs(w)
     g = gpu_run(w, inp, backward=True)
     o = oracle_run(w, inp, slices=BWD_SLICES[wname], backward=True)
-    compare(w, g, o, backward=True)
+    print(w.name, compare(w, g, o, backward=True))
 
 
 SMALL = [
@@ -157,7 +157,7 @@ def test_backward_small_cases(w):
     inp = random_inputs(7 + w.m + w.d, w.B, w.H, w.N, w.d, w.dtype, tied=w.tied)
     g = gpu_run(w, inp, backward=True)
     o = oracle_run(w, inp, backward=True)
-    compare(w, g, o, backward=True)
+    print(w.name, compare(w, g, o, backward=True))
 
 
 def test_constant_inputs_use_zero_sign():
@@ -169,7 +169,7 @@ def test_constant_inputs_use_zero_sign():
     inp["k"] = np.full_like(inp["k"], 0.25)
     g = gpu_run(w, inp, backward=True)
     o = oracle_run(w, inp, backward=True)
-    compare(w, g, o, backward=True)
+    print(w.name, compare(w, g, o, backward=True))
 
 
 def test_deterministic():
