@@ -57,7 +57,8 @@ typedef enum {
   LAPNYS_ECUDA = 2,    /* a kernel launch failed */
   LAPNYS_ETIMEOUT = 3, /* reserved: a bounded device wait expired (no current kernel waits) */
   LAPNYS_ENOSPC = 4,   /* ctx or workspace smaller than the *_bytes functions require */
-  LAPNYS_ENOTSUP = 5   /* valid request outside what this build supports (e.g. d) */
+  LAPNYS_ENOTSUP = 5,  /* valid request outside what this build supports (e.g. d) */
+  LAPNYS_ESCRATCH = 6  /* problem too large for the built-in scratch of lapnys_fwd_static */
 } lapnys_status;
 
 enum { LAPNYS_F32 = 0, LAPNYS_BF16 = 1 };
@@ -89,6 +90,28 @@ int lapnys_fwd(const void* q, const void* k, const void* v, void* out,
                float lambda, float eps, int iters, int tied_qk, cudaStream_t stream,
                int dtype, unsigned flags, void* ctx, size_t ctx_bytes,
                void* ws, size_t ws_bytes);
+
+/* Inference forward that allocates nothing and takes no workspace.  No passage
+ * of the paper corresponds to it: it exists for callers that cannot call
+ * cudaMalloc, such as code running inside another framework's memory pool,
+ * allocator-free embedded runtimes, or code that must not allocate between
+ * two steps.  Same arguments and results as lapnys_fwd with ctx = NULL, minus
+ * ctx and ws.
+ *  - Scratch: a 32 MiB array compiled into the library (held on every GPU that
+ *    loads it, until the process exits).  A problem whose forward scratch
+ *    exceeds it returns LAPNYS_ESCRATCH before anything is enqueued; use
+ *    lapnys_fwd with a workspace instead.  (About: B*H*(m*d*16 + m*m*16 +
+ *    S*ceil(m/64)*64*d*4) bytes, S = token splits.)
+ *  - The first call on a device looks up the array's device address with that
+ *    device current; make that first call before any stream capture.
+ *  - Every call shares the one array.  Calls whose work overlaps on the GPU
+ *    (other streams, other host threads) race on it and give wrong results:
+ *    serialise them, e.g. on one stream.  Each call fully rewrites what it
+ *    reads, so leftovers of an earlier call do no harm. */
+int lapnys_fwd_static(const void* q, const void* k, const void* v, void* out,
+                      int B, int H, int N, int d, int grid_h, int grid_w, int m,
+                      float lambda, float eps, int iters, int tied_qk, cudaStream_t stream,
+                      int dtype, unsigned flags);
 
 /* Backward of lapnys_fwd for the upstream gradient dout.  Needs the ctx written
  * by the forward with the same q, k, v and parameters.  Writes dq, dk, dv

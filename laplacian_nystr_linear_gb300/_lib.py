@@ -11,7 +11,8 @@ import os
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liblapnys.so")
 
-LAPNYS_OK, LAPNYS_EINVAL, LAPNYS_ECUDA, LAPNYS_ETIMEOUT, LAPNYS_ENOSPC, LAPNYS_ENOTSUP = range(6)
+(LAPNYS_OK, LAPNYS_EINVAL, LAPNYS_ECUDA, LAPNYS_ETIMEOUT, LAPNYS_ENOSPC, LAPNYS_ENOTSUP,
+ LAPNYS_ESCRATCH) = range(7)
 LAPNYS_F32, LAPNYS_BF16 = 0, 1
 LAPNYS_NORM = 1
 
@@ -19,7 +20,7 @@ LAPNYS_NORM = 1
 EXPORTS = (
     "lapnys_ctx_bytes", "lapnys_workspace_bytes", "lapnys_fwd", "lapnys_bwd",
     "lapnys_ctx_offsets", "lapnys_pool", "lapnys_strerror", "lapnys_launch_count",
-    "lapnys_profile_enable", "lapnys_profile_read",
+    "lapnys_profile_enable", "lapnys_profile_read", "lapnys_fwd_static",
 )
 
 
@@ -48,6 +49,8 @@ def load() -> ctypes.CDLL:
     lib.lapnys_workspace_bytes.restype = S
     lib.lapnys_fwd.argtypes = [P, P, P, P, I, I, I, I, I, I, I, F, F, I, I, P, I, U, P, S, P, S]
     lib.lapnys_fwd.restype = I
+    lib.lapnys_fwd_static.argtypes = [P, P, P, P, I, I, I, I, I, I, I, F, F, I, I, P, I, U]
+    lib.lapnys_fwd_static.restype = I
     lib.lapnys_bwd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, F, I, I, P, I, U, P, S]
     lib.lapnys_bwd.restype = I
     lib.lapnys_ctx_offsets.argtypes = [I, I, I, I, I, I, U, ctypes.POINTER(CtxLayout)]

@@ -4,6 +4,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <mutex>
 #include <vector>
 
 #include "../../include/lapnys.h"
@@ -212,6 +213,39 @@ static int ns_forward_large(const Prob& p, const float* A, float* X, float* Y, i
 
 using namespace lapnys;
 
+// ---------------------------------------------------------------------------
+// Built-in forward scratch for callers that cannot allocate device memory.
+// 32 MiB of device memory per GPU that loads this library, held until exit.
+// Host code must not hand the array's name to a kernel (on the host it is a
+// stand-in, not a device address): lapnys_fwd_static looks the device address
+// up once per device with cudaGetSymbolAddress, with that device current.
+// ---------------------------------------------------------------------------
+static constexpr size_t kStaticScratchBytes = (size_t)32 << 20;
+static __device__ __align__(256) unsigned char g_fwd_scratch[kStaticScratchBytes];
+
+namespace {
+constexpr int kMaxScratchDevices = 256;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxScratchDevices];  // device address per device ordinal, set on first use
+
+// address of g_fwd_scratch on the current device (first call per device looks it up)
+cudaError_t static_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxScratchDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_addr[dev] == nullptr) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_fwd_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = ptr;
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+}  // namespace
+
 extern "C" {
 
 const char* lapnys_strerror(int status) {
@@ -222,6 +256,9 @@ const char* lapnys_strerror(int status) {
     case LAPNYS_ETIMEOUT: return "bounded device wait expired";
     case LAPNYS_ENOSPC: return "ctx or workspace buffer too small";
     case LAPNYS_ENOTSUP: return "unsupported configuration (d must be 16, 32, 64 or 128)";
+    case LAPNYS_ESCRATCH:
+      return "problem needs more scratch than the 32 MiB built into lapnys_fwd_static; "
+             "call lapnys_fwd with a caller-owned workspace";
   }
   return "unknown status";
 }
@@ -308,6 +345,64 @@ int lapnys_fwd(const void* q, const void* k, const void* v, void* out, int B, in
   CK(run_reduce_parts(p.BH, p.Sk, m, p.mp, d, kpart, W, stream));
   const float* XT = X + (long)(iters % c.nx) * mm;
   // W-hat = X_T W
+  CK(run_gemm2(false, false, false, p.BH, m, d, XT, m, c.nx * mm, W, d, (long)m * d, m, nullptr, 0,
+               0, nullptr, 0, 0, 0, What, d, (long)m * d, nullptr, d, 0, 1.f, 0.f, stream));
+  if (p.norm()) {
+    float* spart = (float*)(wb + w.spart);
+    CK(run_qstats(p, q, L, spart, stream));
+    CK(run_stats_final(p, spart, stats, stream));
+  }
+  CK(run_query_fwd(p, q, L, What, stats, out, stream));
+  return LAPNYS_OK;
+}
+
+int lapnys_fwd_static(const void* q, const void* k, const void* v, void* out, int B, int H, int N,
+                      int d, int grid_h, int grid_w, int m, float lambda, float eps, int iters,
+                      int tied_qk, cudaStream_t stream, int dtype, unsigned flags) {
+  int rc = check_common(B, H, N, d, grid_h, grid_w, m, lambda, eps, iters, dtype, flags);
+  if (rc != LAPNYS_OK) return rc;
+  if (tied_qk != 0 && tied_qk != 1) return LAPNYS_EINVAL;
+  if (tied_qk) {
+    if (k != nullptr && k != q) return LAPNYS_EINVAL;
+    k = q;
+  }
+  if (!q || !k || !v || !out) return LAPNYS_EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return LAPNYS_EINVAL;
+  Prob p = make_prob(B, H, N, d, grid_h, grid_w, m, lambda, eps, iters, tied_qk, dtype, flags);
+  const WsLayout w = ws_layout(p);
+  // the forward uses the leading part of the workspace layout: the stand-in
+  // for the saved state and the key-pass / statistics partials
+  if (w.dWhp > kStaticScratchBytes) return LAPNYS_ESCRATCH;
+  void* ws = nullptr;
+  CK(static_scratch(&ws));
+  const CtxLayout c = ctx_layout(p.BH, N, d, m, iters, false);
+  char* cb = (char*)ws + w.lite;
+  char* wb = (char*)ws;
+  float* L = (float*)(cb + c.L);
+  float* A = (float*)(cb + c.A);
+  float* alpha = (float*)(cb + c.alpha);
+  float* X = (float*)(cb + c.X);
+  float* Y = (float*)(cb + c.Y);
+  float* W = (float*)(cb + c.W);
+  float* What = (float*)(cb + c.What);
+  float* stats = (float*)(cb + c.stats);
+  int32_t* idx = (int32_t*)(cb + c.idx);
+  const long mm = (long)m * m;
+  // every scratch region below is fully written before it is read, so nothing
+  // left over from an earlier call needs clearing
+  CK(run_pool(p, k, L, idx, stream));
+  if (m <= kTile) {
+    CK(run_ns_small(p, L, A, alpha, X, Y, c.nx, c.ny, stream));
+  } else {
+    CK(run_gram(p, L, A, stream));
+    CK(run_alpha(p, A, alpha, X, c.nx * mm, stream));
+    rc = ns_forward_large(p, A, X, Y, c.nx, c.ny, stream);
+    if (rc != LAPNYS_OK) return rc;
+  }
+  float* kpart = (float*)(wb + w.kpart);
+  CK(run_key_fwd(p, k, v, L, kpart, stream));
+  CK(run_reduce_parts(p.BH, p.Sk, m, p.mp, d, kpart, W, stream));
+  const float* XT = X + (long)(iters % c.nx) * mm;
   CK(run_gemm2(false, false, false, p.BH, m, d, XT, m, c.nx * mm, W, d, (long)m * d, m, nullptr, 0,
                0, nullptr, 0, 0, 0, What, d, (long)m * d, nullptr, d, 0, 1.f, 0.f, stream));
   if (p.norm()) {

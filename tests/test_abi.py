@@ -58,7 +58,7 @@ def test_ctx_offsets_are_ordered_and_aligned(lib):
 
 
 def test_strerror(lib):
-    for code in range(6):
+    for code in range(7):
         assert lib.lapnys_strerror(code)
     assert b"unknown" in lib.lapnys_strerror(99)
 
