@@ -55,7 +55,7 @@ typedef enum {
   LAPNYS_OK = 0,
   LAPNYS_EINVAL = 1,   /* bad dimension, pointer, alignment or parameter */
   LAPNYS_ECUDA = 2,    /* a kernel launch failed */
-  LAPNYS_ETIMEOUT = 3, /* reserved: a bounded device wait expired (no current kernel waits) */
+  LAPNYS_ETIMEOUT = 3, /* a bounded device wait expired (see lapnys_device_status) */
   LAPNYS_ENOSPC = 4,   /* ctx or workspace smaller than the *_bytes functions require */
   LAPNYS_ENOTSUP = 5,  /* valid request outside what this build supports (e.g. d) */
   LAPNYS_ESCRATCH = 6  /* problem too large for the built-in scratch of lapnys_fwd_static */
@@ -147,6 +147,28 @@ int lapnys_ctx_offsets(int B, int H, int N, int d, int m, int iters, unsigned fl
  * (idx may be NULL).  Same rules as lapnys_fwd. */
 int lapnys_pool(const void* k, float* L, int32_t* idx, int B, int H, int N, int d,
                 int grid_h, int grid_w, int m, int dtype, cudaStream_t stream);
+
+/* Batched fp32 product C[b] = alpha * op(A[b]) * op(B[b]) + beta * E[b] for
+ * b < batch, the building block of the Newton-Schulz solver for m > 64 (the
+ * products X_t (A X_t) and their reverse).  Row-major device matrices; op(A)
+ * is M x K (A stored K x M when trans_a), op(B) is K x N (B stored N x K when
+ * trans_b); E may alias C; E may be NULL when beta == 0.
+ *  engine 0: FP32 FMA kernel (any shape).
+ *  engine 1: tcgen05 tensor cores, TF32 with the three-term split
+ *            hi*hi + hi*lo + lo*hi (fp32-level accuracy); needs M, N, K, the
+ *            leading dimensions and strides to be multiples of 4 and 16-byte
+ *            aligned pointers, else returns LAPNYS_ENOTSUP.
+ * Asynchronous on `stream`. */
+int lapnys_matmul(const float* A, const float* B, const float* E, float* C, int batch, int M, int N,
+                  int K, int trans_a, int trans_b, int lda, int ldb, int lde, int ldc,
+                  long long stride_a, long long stride_b, long long stride_e, long long stride_c,
+                  float alpha, float beta, int engine, cudaStream_t stream);
+
+/* Synchronises the current device and reports whether a bounded device-side
+ * wait (tensor-core pipeline barriers) expired since the last clear:
+ * LAPNYS_ETIMEOUT if so (the affected results are invalid), LAPNYS_OK if not,
+ * LAPNYS_ECUDA if the device reported an error.  clear != 0 resets the flag. */
+int lapnys_device_status(int clear);
 
 /* Human-readable text for a status code (static storage). */
 const char* lapnys_strerror(int status);

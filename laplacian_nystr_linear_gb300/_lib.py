@@ -20,7 +20,8 @@ LAPNYS_NORM = 1
 EXPORTS = (
     "lapnys_ctx_bytes", "lapnys_workspace_bytes", "lapnys_fwd", "lapnys_bwd",
     "lapnys_ctx_offsets", "lapnys_pool", "lapnys_strerror", "lapnys_launch_count",
-    "lapnys_profile_enable", "lapnys_profile_read", "lapnys_fwd_static",
+    "lapnys_profile_enable", "lapnys_profile_read", "lapnys_fwd_static", "lapnys_matmul",
+    "lapnys_device_status",
 )
 
 
@@ -51,6 +52,12 @@ def load() -> ctypes.CDLL:
     lib.lapnys_fwd.restype = I
     lib.lapnys_fwd_static.argtypes = [P, P, P, P, I, I, I, I, I, I, I, F, F, I, I, P, I, U]
     lib.lapnys_fwd_static.restype = I
+    LL = ctypes.c_longlong
+    lib.lapnys_matmul.argtypes = [P, P, P, P, I, I, I, I, I, I, I, I, I, I, LL, LL, LL, LL, F, F,
+                                  I, P]
+    lib.lapnys_matmul.restype = I
+    lib.lapnys_device_status.argtypes = [I]
+    lib.lapnys_device_status.restype = I
     lib.lapnys_bwd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, F, I, I, P, I, U, P, S]
     lib.lapnys_bwd.restype = I
     lib.lapnys_ctx_offsets.argtypes = [I, I, I, I, I, I, U, ctypes.POINTER(CtxLayout)]

@@ -70,6 +70,16 @@ cudaError_t run_gemm2(bool ta, bool tb, bool sym, int batch, int M, int N, const
                       int ldc, long sC, const float* E, int lde, long sE, float alpha, float beta,
                       cudaStream_t st);
 
+// tensor-core (tcgen05, three-term TF32 split) batched product; tc_gemm_ok tells
+// whether the shapes, strides and pointers meet its alignment needs
+bool tc_gemm_ok(int M, int N, int K, int lda, int ldb, int ldc, int lde, long sA, long sB, long sC,
+                long sE, const void* A, const void* B, const void* C, const void* E);
+cudaError_t run_tcgemm(bool ta, bool tb, int batch, int M, int N, int K, const float* A, int lda,
+                       long sA, const float* B, int ldb, long sB, float* C, int ldc, long sC,
+                       const float* E, int lde, long sE, float alpha, float beta, cudaStream_t st);
+// value of the device error word set by expired bounded waits (-1 on failure)
+int read_wait_error(bool clear);
+
 // forward passes
 cudaError_t run_key_fwd(const Prob& p, const void* k, const void* v, const float* L, float* part,
                         cudaStream_t st);

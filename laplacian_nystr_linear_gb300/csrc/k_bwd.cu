@@ -179,6 +179,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   float* Stage = sm + SM::Stage;
   __shared__ float mu_s[TA], rs_s[TA], m0_s[TA], m1_s[TA];
   __shared__ unsigned flag_bits[kMaxFlagBlocks / 32];
+  __shared__ float rowg_s[TJ], colg_s[TA];  // sums of g over the tile's landmarks / block's tokens
 
   const int lt = blockIdx.x, sp = blockIdx.y, bh = blockIdx.z;
   const int a0 = lt * TA;
@@ -235,26 +236,24 @@ __global__ void __launch_bounds__(kThreads, 2)
       Ss[rank * D + c] = v;
     }
     __syncthreads();
-    for (int b = b0; b < b1; ++b) {
-      bool tie = false;
-      for (int e = tid; e < TJ * D; e += kThreads) {
-        const int j = e / D, c = e % D;
-        const int n = b * TJ + j;
-        if (n >= N) break;
+    // one flat pass over every (token, feature) value of this CTA's blocks; a
+    // tie or an out-of-range value marks its block
+    const int per_blk = TJ * D;
+    const int total = (b1 - b0) * per_blk;
+#pragma unroll 4
+    for (int e = tid; e < total; e += kThreads) {
+      const int blk = e / per_blk, rem = e % per_blk;
+      const int n = (b0 + blk) * TJ + rem / D, c = rem % D;
+      if (n < N) {
         const float x = ldx(Xb + (size_t)n * D + c);
-        if (out_of_range(x)) {
-          tie = true;
-        } else {
-          int lo = 0;
+        bool tie = out_of_range(x);
+        int lo = 0;
 #pragma unroll
-          for (int step = TA / 2; step > 0; step >>= 1)
-            if (Ss[(lo + step - 1) * D + c] < x) lo += step;
-          if (lo < TA && Ss[lo * D + c] == x) tie = true;
-        }
+        for (int step = TA / 2; step > 0; step >>= 1)
+          if (Ss[(lo + step - 1) * D + c] < x) lo += step;
+        tie = tie || (lo < TA && Ss[lo * D + c] == x);
+        if (tie && blk < kMaxFlagBlocks) atomicOr(&flag_bits[blk >> 5], 1u << (blk & 31));
       }
-      const int any = __syncthreads_or(tie);
-      const int k = b - b0;
-      if (tid == 0 && any && k < kMaxFlagBlocks) flag_bits[k >> 5] |= 1u << (k & 31);
     }
   }
   __syncthreads();
@@ -289,24 +288,24 @@ __global__ void __launch_bounds__(kThreads, 2)
     load_rows<D, TJ>(Us, Ub, n0, N);
     __syncthreads();
 
-    // ---- phase 1: thread = tokens 4 warp .. +3, landmarks lane and lane + 32 ----
+    // ---- phase 1: thread = tokens 4 warp .. +3, landmarks 2 lane and 2 lane + 1 ----
     {
-      const int jb = 4 * warp;
+      const int jb = 4 * warp, la = 2 * lane;
       float dist[4][2], dot[4][2];
 #pragma unroll
       for (int r = 0; r < 4; ++r) dist[r][0] = dist[r][1] = dot[r][0] = dot[r][1] = 0.f;
 #pragma unroll 2
       for (int c = 0; c < D; c += 4) {
-        const float4 r0 = lds4(Rs + lane * (D + 4) + c);
-        const float4 r1 = lds4(Rs + (lane + 32) * (D + 4) + c);
+        const float4 r0 = lds4(Rs + la * (D + 4) + c);
+        const float4 r1 = lds4(Rs + (la + 1) * (D + 4) + c);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const float4 x4 = lds4(Xt + (c + q) * JS + jb);
-          const float lb0 = LBt[(c + q) * AS + lane], lb1 = LBt[(c + q) * AS + lane + 32];
-          dist[0][0] += fabsf(fmaf(x4.x, scale, lb0)); dist[0][1] += fabsf(fmaf(x4.x, scale, lb1));
-          dist[1][0] += fabsf(fmaf(x4.y, scale, lb0)); dist[1][1] += fabsf(fmaf(x4.y, scale, lb1));
-          dist[2][0] += fabsf(fmaf(x4.z, scale, lb0)); dist[2][1] += fabsf(fmaf(x4.z, scale, lb1));
-          dist[3][0] += fabsf(fmaf(x4.w, scale, lb0)); dist[3][1] += fabsf(fmaf(x4.w, scale, lb1));
+          const float2 lb = *reinterpret_cast<const float2*>(LBt + (c + q) * AS + la);
+          dist[0][0] += fabsf(fmaf(x4.x, scale, lb.x)); dist[0][1] += fabsf(fmaf(x4.x, scale, lb.y));
+          dist[1][0] += fabsf(fmaf(x4.y, scale, lb.x)); dist[1][1] += fabsf(fmaf(x4.y, scale, lb.y));
+          dist[2][0] += fabsf(fmaf(x4.z, scale, lb.x)); dist[2][1] += fabsf(fmaf(x4.z, scale, lb.y));
+          dist[3][0] += fabsf(fmaf(x4.w, scale, lb.x)); dist[3][1] += fabsf(fmaf(x4.w, scale, lb.y));
         }
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
@@ -322,10 +321,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
+      for (int r = 0; r < 4; ++r) {
+        const int j = jb + r;
+        float gv[2], zv[2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const int j = jb + r, a = lane + 32 * h;
+          const int a = la + h;
           const bool valid = (n0 + j < N) && (a < nv);
           const float kv = exp2f(dist[r][h] * ns_s);
           float g, zc;
@@ -338,11 +339,31 @@ __global__ void __launch_bounds__(kThreads, 2)
             g = dp * kv * inv_lam;
             zc = z;
           }
-          Gs[j * AS + a] = valid ? 2.f * g : 0.f;
-          Zs[j * AS + a] = valid ? zc : 0.f;
+          gv[h] = valid ? 2.f * g : 0.f;
+          zv[h] = valid ? zc : 0.f;
         }
+        *reinterpret_cast<float2*>(Gs + j * AS + la) = make_float2(gv[0], gv[1]);
+        *reinterpret_cast<float2*>(Zs + j * AS + la) = make_float2(zv[0], zv[1]);
+      }
     }
     __syncthreads();
+
+    // ---- per-token and per-landmark sums of g (the tile holds 2g) ----
+    if (tid < TJ) {
+      float sacc = 0.f;
+#pragma unroll 4
+      for (int a = 0; a < TA; a += 4) {
+        const float4 v = lds4(Gs + tid * AS + a);
+        sacc += (v.x + v.y) + (v.z + v.w);
+      }
+      rowg_s[tid] = 0.5f * sacc;
+    } else if (tid < TJ + TA) {
+      const int a = tid - TJ;
+      float sacc = 0.f;
+#pragma unroll 8
+      for (int j = 0; j < TJ; ++j) sacc += Gs[j * AS + a];
+      colg_s[a] = 0.5f * sacc;
+    }
 
     // ---- phase C: contractions ----
     if (kDWhat) {
@@ -407,47 +428,12 @@ __global__ void __launch_bounds__(kThreads, 2)
       // elements 2 jg, 2 jg + 1 of lanes 8 q + ag
       const float* qsrc = scr + 72 * jg + ag;
       const float* lsrc = scr + 8 * ag + 2 * jg;
-      float rowg, colg0, colg1;
-      {
-        float t8[8];
-#pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          t8[r] = 0.f;
-#pragma unroll
-          for (int t = 0; t < 8; ++t) t8[r] += g2[r][t];
-        }
-        st4(mine, make_float4(t8[0], t8[1], t8[2], t8[3]));
-        st4(mine + 4, make_float4(t8[4], t8[5], t8[6], t8[7]));
-        __syncwarp();
-        rowg = 0.f;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) rowg += qsrc[8 * q];
-        __syncwarp();
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          t8[t] = 0.f;
-#pragma unroll
-          for (int r = 0; r < 8; ++r) t8[t] += g2[r][t];
-        }
-        st4(mine, make_float4(t8[0], t8[1], t8[2], t8[3]));
-        st4(mine + 4, make_float4(t8[4], t8[5], t8[6], t8[7]));
-        __syncwarp();
-        colg0 = colg1 = 0.f;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float2 v = *reinterpret_cast<const float2*>(lsrc + 72 * q);
-          colg0 += v.x;
-          colg1 += v.y;
-        }
-        __syncwarp();
-      }
+      __syncthreads();  // g and Z tiles are free from here on (staging); sums are ready
+      const float rowg = rowg_s[j0 + ag];
       if (!exact) {
-        colg_acc0 += 0.5f * colg0;
-        colg_acc1 += 0.5f * colg1;
+        colg_acc0 += colg_s[al + 2 * jg];
+        colg_acc1 += colg_s[al + 2 * jg + 1];
       }
-      rowg *= 0.5f;  // the identities use sums of g, the tile holds 2g
-      __syncthreads();  // g and Z tiles are free from here on (staging)
-
       if (exact)
         sign_cols<D, true>(warp * CW, j0, al, jg, ag, g2, Xt, LBt, mine, qsrc, lsrc, rowg,
                            inv_scale, Stage, dLs);

@@ -189,6 +189,20 @@ static int check_common(int B, int H, int N, int d, int gh, int gw, int m, float
 // ---------------------------------------------------------------------------
 // Newton-Schulz for m > 64 via batched products (X slots: nx, Y slots: ny)
 // ---------------------------------------------------------------------------
+// One batched product of the Newton-Schulz solver: on the tensor cores
+// (three-term TF32 split, fp32-level accuracy) when the shapes and pointers are
+// 4-element aligned, otherwise on the FP32 FMA kernel.
+static cudaError_t ns_mm(const Prob& p, bool ta, bool tb, int M, int N, int K, const float* A,
+                         int lda, long sA, const float* B, int ldb, long sB, float* C, int ldc,
+                         long sC, const float* E, int lde, long sE, float alpha, float beta,
+                         cudaStream_t st) {
+  if (tc_gemm_ok(M, N, K, lda, ldb, ldc, lde, sA, sB, sC, sE, A, B, C, beta != 0.f ? E : nullptr))
+    return run_tcgemm(ta, tb, p.BH, M, N, K, A, lda, sA, B, ldb, sB, C, ldc, sC, E, lde, sE, alpha,
+                      beta, st);
+  return run_gemm2(ta, tb, false, p.BH, M, N, A, lda, sA, B, ldb, sB, K, nullptr, 0, 0, nullptr, 0,
+                   0, 0, C, ldc, sC, E, lde, sE, alpha, beta, st);
+}
+
 static int ns_forward_large(const Prob& p, const float* A, float* X, float* Y, int nx, int ny,
                             cudaStream_t st) {
   const int m = p.m;
@@ -199,12 +213,18 @@ static int ns_forward_large(const Prob& p, const float* A, float* X, float* Y, i
     float* Yt = Y + (long)(t % ny) * mm;
     // Y_t = A X_t, computed in full: forcing this product to be exactly
     // symmetric makes the fp32 iteration diverge in its unconverged directions
-    CK(run_gemm2(false, false, false, p.BH, m, m, A, m, mm, Xt, m, nx * mm, m, nullptr, 0, 0,
-                 nullptr, 0, 0, 0, Yt, m, ny * mm, nullptr, m, 0, 1.f, 0.f, st));
-    // X_{t+1} = 2 X_t - X_t Y_t, written symmetric (stable: the residual
-    // I - A X_{t+1} = (I - A X_t)^2 keeps contracting)
-    CK(run_gemm2(false, false, true, p.BH, m, m, Xt, m, nx * mm, Yt, m, ny * mm, m, nullptr, 0, 0,
-                 nullptr, 0, 0, 0, Xn, m, nx * mm, Xt, m, nx * mm, -1.f, 2.f, st));
+    CK(ns_mm(p, false, false, m, m, m, A, m, mm, Xt, m, nx * mm, Yt, m, ny * mm, nullptr, m, 0, 1.f,
+             0.f, st));
+    // X_{t+1} = 2 X_t - X_t Y_t.  The FMA kernel writes it symmetric (upper
+    // tiles mirrored; stable: the residual I - A X_{t+1} = (I - A X_t)^2 keeps
+    // contracting); the tensor-core kernel computes it in full.
+    if (tc_gemm_ok(m, m, m, m, m, m, m, nx * mm, ny * mm, nx * mm, nx * mm, Xt, Yt, Xn, Xt)) {
+      CK(run_tcgemm(false, false, p.BH, m, m, m, Xt, m, nx * mm, Yt, m, ny * mm, Xn, m, nx * mm, Xt,
+                    m, nx * mm, -1.f, 2.f, st));
+    } else {
+      CK(run_gemm2(false, false, true, p.BH, m, m, Xt, m, nx * mm, Yt, m, ny * mm, m, nullptr, 0, 0,
+                   nullptr, 0, 0, 0, Xn, m, nx * mm, Xt, m, nx * mm, -1.f, 2.f, st));
+    }
   }
   return LAPNYS_OK;
 }
@@ -345,8 +365,8 @@ int lapnys_fwd(const void* q, const void* k, const void* v, void* out, int B, in
   CK(run_reduce_parts(p.BH, p.Sk, m, p.mp, d, kpart, W, stream));
   const float* XT = X + (long)(iters % c.nx) * mm;
   // W-hat = X_T W
-  CK(run_gemm2(false, false, false, p.BH, m, d, XT, m, c.nx * mm, W, d, (long)m * d, m, nullptr, 0,
-               0, nullptr, 0, 0, 0, What, d, (long)m * d, nullptr, d, 0, 1.f, 0.f, stream));
+  CK(ns_mm(p, false, false, m, d, m, XT, m, c.nx * mm, W, d, (long)m * d, What, d, (long)m * d,
+           nullptr, d, 0, 1.f, 0.f, stream));
   if (p.norm()) {
     float* spart = (float*)(wb + w.spart);
     CK(run_qstats(p, q, L, spart, stream));
@@ -403,8 +423,8 @@ int lapnys_fwd_static(const void* q, const void* k, const void* v, void* out, in
   CK(run_key_fwd(p, k, v, L, kpart, stream));
   CK(run_reduce_parts(p.BH, p.Sk, m, p.mp, d, kpart, W, stream));
   const float* XT = X + (long)(iters % c.nx) * mm;
-  CK(run_gemm2(false, false, false, p.BH, m, d, XT, m, c.nx * mm, W, d, (long)m * d, m, nullptr, 0,
-               0, nullptr, 0, 0, 0, What, d, (long)m * d, nullptr, d, 0, 1.f, 0.f, stream));
+  CK(ns_mm(p, false, false, m, d, m, XT, m, c.nx * mm, W, d, (long)m * d, What, d, (long)m * d,
+           nullptr, d, 0, 1.f, 0.f, stream));
   if (p.norm()) {
     float* spart = (float*)(wb + w.spart);
     CK(run_qstats(p, q, L, spart, stream));
@@ -495,27 +515,27 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
     // The unconverged directions grow by about 2 per step in this recursion, so
     // it must not lean on X_t commuting with A: in fp32 that shortcut diverges.
     // G = dLoss/dX_T = dW-hat W^T ;  dW = X_T^T dW-hat
-    CK(run_gemm2(false, true, false, p.BH, m, m, dWh, d, md, W, d, md, d, nullptr, 0, 0, nullptr, 0,
-                 0, 0, G, m, mm, nullptr, m, 0, 1.f, 0.f, stream));
-    CK(run_gemm2(true, false, false, p.BH, m, d, XT, m, xs, dWh, d, md, m, nullptr, 0, 0, nullptr,
-                 0, 0, 0, dW, d, md, nullptr, d, 0, 1.f, 0.f, stream));
+    CK(ns_mm(p, false, true, m, m, d, dWh, d, md, W, d, md, G, m, mm, nullptr, m, 0, 1.f, 0.f,
+             stream));
+    CK(ns_mm(p, true, false, m, d, m, XT, m, xs, dWh, d, md, dW, d, md, nullptr, d, 0, 1.f, 0.f,
+             stream));
     if (iters == 0) CK(run_zero(dA, (size_t)p.BH * mm, stream));
     float* Sc = G;
     for (int t = iters - 1; t >= 0; --t) {
       const float* Xt = X + (long)t * mm;
       const float* Yt = Y + (long)t * mm;
       // XG = X_t^T G
-      CK(run_gemm2(true, false, false, p.BH, m, m, Xt, m, xs, Sc, m, mm, m, nullptr, 0, 0, nullptr,
-                   0, 0, 0, XG, m, mm, nullptr, m, 0, 1.f, 0.f, stream));
+      CK(ns_mm(p, true, false, m, m, m, Xt, m, xs, Sc, m, mm, XG, m, mm, nullptr, m, 0, 1.f, 0.f,
+               stream));
       // dA = dA - XG X_t^T   (the first step initialises dA)
-      CK(run_gemm2(false, true, false, p.BH, m, m, XG, m, mm, Xt, m, xs, m, nullptr, 0, 0, nullptr,
-                   0, 0, 0, dA, m, mm, dA, m, mm, -1.f, t == iters - 1 ? 0.f : 1.f, stream));
+      CK(ns_mm(p, false, true, m, m, m, XG, m, mm, Xt, m, xs, dA, m, mm, dA, m, mm, -1.f,
+               t == iters - 1 ? 0.f : 1.f, stream));
       // Tm = 2 G - G Y_t^T
-      CK(run_gemm2(false, true, false, p.BH, m, m, Sc, m, mm, Yt, m, ys, m, nullptr, 0, 0, nullptr,
-                   0, 0, 0, Tm, m, mm, Sc, m, mm, -1.f, 2.f, stream));
+      CK(ns_mm(p, false, true, m, m, m, Sc, m, mm, Yt, m, ys, Tm, m, mm, Sc, m, mm, -1.f, 2.f,
+               stream));
       // G = Tm - A^T XG
-      CK(run_gemm2(true, false, false, p.BH, m, m, A, m, mm, XG, m, mm, m, nullptr, 0, 0, nullptr, 0,
-                   0, 0, Sc, m, mm, Tm, m, mm, -1.f, 1.f, stream));
+      CK(ns_mm(p, true, false, m, m, m, A, m, mm, XG, m, mm, Sc, m, mm, Tm, m, mm, -1.f, 1.f,
+               stream));
     }
     CK(run_alpha_bwd(p, A, alpha, Sc, dA, stream));
   }
@@ -530,6 +550,36 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
   CK(run_reduce_dl(p, dLqp, dLcp, dLA, dL, stream));
   CK(run_finalize(p, dQp, dKp, dVp, dL, dq, dk, dv, stream));
   return LAPNYS_OK;
+}
+
+int lapnys_matmul(const float* A, const float* B, const float* E, float* C, int batch, int M, int N,
+                  int K, int trans_a, int trans_b, int lda, int ldb, int lde, int ldc,
+                  long long stride_a, long long stride_b, long long stride_e, long long stride_c,
+                  float alpha, float beta, int engine, cudaStream_t stream) {
+  if (!A || !B || !C || batch <= 0 || M <= 0 || N <= 0 || K <= 0) return LAPNYS_EINVAL;
+  if (beta != 0.f && !E) return LAPNYS_EINVAL;
+  if (lda <= 0 || ldb <= 0 || ldc <= 0 || (E && lde <= 0)) return LAPNYS_EINVAL;
+  if (engine == 1) {
+    if (!tc_gemm_ok(M, N, K, lda, ldb, ldc, lde, (long)stride_a, (long)stride_b, (long)stride_c,
+                    (long)stride_e, A, B, C, beta != 0.f ? E : nullptr))
+      return LAPNYS_ENOTSUP;
+    CK(run_tcgemm(trans_a != 0, trans_b != 0, batch, M, N, K, A, lda, (long)stride_a, B, ldb,
+                  (long)stride_b, C, ldc, (long)stride_c, E, lde, (long)stride_e, alpha, beta,
+                  stream));
+    return LAPNYS_OK;
+  }
+  if (engine != 0) return LAPNYS_EINVAL;
+  CK(run_gemm2(trans_a != 0, trans_b != 0, false, batch, M, N, A, lda, (long)stride_a, B, ldb,
+               (long)stride_b, K, nullptr, 0, 0, nullptr, 0, 0, 0, C, ldc, (long)stride_c, E, lde,
+               (long)stride_e, alpha, beta, stream));
+  return LAPNYS_OK;
+}
+
+int lapnys_device_status(int clear) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return LAPNYS_ECUDA;
+  const int v = read_wait_error(clear != 0);
+  if (v < 0) return LAPNYS_ECUDA;
+  return v ? LAPNYS_ETIMEOUT : LAPNYS_OK;
 }
 
 uint64_t lapnys_launch_count(void) { return g_launches; }
