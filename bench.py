@@ -73,6 +73,22 @@ def algorithmic_ops(w):
     return per
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """Largest value over all ranks (step times: the slowest rank sets the pace)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(tokens_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job tokens/s: every rank processes its own batch of the workload."""
+    return world * tokens_per_rank / (ms_per_step / 1e3)
+
+
 def clock_sampler(gpu_index: int):
     f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
     q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -229,13 +245,6 @@ def run_ours(args, rank, world, local_rank):
             dist.barrier()
         torch.cuda.synchronize()
 
-    def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        t = torch.tensor([x], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
     for _ in range(args.warmup):
         step()
     barrier()
@@ -254,8 +263,8 @@ def run_ours(args, rank, world, local_rank):
     prof = api.profile_read()
     api.profile_enable(False)
     launches = api.launch_count() - launches0
-    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps)
-    value = world * w.tokens / (ms / 1e3)
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    value = weak_scaling_value(w.tokens, world, ms)
 
     # forward alone (same buffers)
     for _ in range(2):
@@ -266,7 +275,7 @@ def run_ours(args, rank, world, local_rank):
         api.fwd(q, k, v, p, out=out, ctx=ctx, ws=ws)
     e1.record(stream)
     barrier()
-    ms_fwd = max_over_ranks(e0.elapsed_time(e1) / args.steps)
+    ms_fwd = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
 
     # roofline of the dominant kernel (FP32 lane-ops; the path is ALU-bound)
     ops = algorithmic_ops(w)
@@ -313,7 +322,7 @@ def run_ours(args, rank, world, local_rank):
             step_e2e()
         e1.record(stream)
         barrier()
-        ms_e2e = max_over_ranks(e0.elapsed_time(e1) / ne)
+        ms_e2e = max_over_ranks(e0.elapsed_time(e1) / ne, world, dev)
         nbytes = q.numel() * q.element_size()
         n_in = 3 if w.tied else 4
         n_out = 3 if w.tied else 4
