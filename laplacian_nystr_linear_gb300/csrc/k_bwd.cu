@@ -24,6 +24,8 @@
 //   phase S  (warp = D/8 features, lane = 8 tokens x 8 landmarks) sign term
 //   phase C  contraction: dW-hat_a += sum_j Z_ja dO_j (query side) or
 //            dV_j = sum_a C_ja dW_a (key side)
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -164,6 +166,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   constexpr int CW = D / 8;     // features per warp in phase S
   constexpr int CPT = D / 16;   // features per thread in phase C
   constexpr bool kDWhat = (MODE == 1) && !NORM;
+  // bf16 inputs: the dot (dO . W-hat or V . dW) and the key-side dV contraction
+  // run on the tensor cores in TF32; dW-hat stays in fp32 (it is amplified by
+  // the Newton-Schulz reverse, where TF32 rounding would cost ~5e-3 on dK)
+  constexpr bool kTC = std::is_same<T, __nv_bfloat16>::value && D >= 32;
   using SM = Smem<D>;
   extern __shared__ float4 sm4[];
   float* sm = reinterpret_cast<float*>(sm4);
@@ -288,6 +294,35 @@ __global__ void __launch_bounds__(kThreads, 2)
     load_rows<D, TJ>(Us, Ub, n0, N);
     __syncthreads();
 
+    if constexpr (kTC) {
+      // dot[j][a] = sum_c U[j][c] R[a][c] on the tensor cores, into the g tile
+      const int gq = lane >> 2, tg = lane & 3;
+      const int jt = (warp >> 2) * 16, wa = (warp & 3) * 16;
+      float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll 4
+      for (int k0 = 0; k0 < D; k0 += 8) {
+        uint32_t af[4];
+        af[0] = __float_as_uint(Us[(jt + gq) * (D + 4) + k0 + tg]);
+        af[1] = __float_as_uint(Us[(jt + gq + 8) * (D + 4) + k0 + tg]);
+        af[2] = __float_as_uint(Us[(jt + gq) * (D + 4) + k0 + tg + 4]);
+        af[3] = __float_as_uint(Us[(jt + gq + 8) * (D + 4) + k0 + tg + 4]);
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+          uint32_t bf[2];
+          bf[0] = to_tf32(Rs[(wa + 8 * n + gq) * (D + 4) + k0 + tg]);
+          bf[1] = to_tf32(Rs[(wa + 8 * n + gq) * (D + 4) + k0 + tg + 4]);
+          mma_16x8x8(acc[n], af, bf);
+        }
+      }
+#pragma unroll
+      for (int n = 0; n < 2; ++n) {
+        const int a = wa + 8 * n + 2 * tg;
+        *reinterpret_cast<float2*>(Gs + (jt + gq) * AS + a) = make_float2(acc[n][0], acc[n][1]);
+        *reinterpret_cast<float2*>(Gs + (jt + gq + 8) * AS + a) = make_float2(acc[n][2], acc[n][3]);
+      }
+      __syncthreads();
+    }
+
     // ---- phase 1: thread = tokens 4 warp .. +3, landmarks 2 lane and 2 lane + 1 ----
     {
       const int jb = 4 * warp, la = 2 * lane;
@@ -307,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 2)
           dist[2][0] += fabsf(fmaf(x4.z, scale, lb.x)); dist[2][1] += fabsf(fmaf(x4.z, scale, lb.y));
           dist[3][0] += fabsf(fmaf(x4.w, scale, lb.x)); dist[3][1] += fabsf(fmaf(x4.w, scale, lb.y));
         }
+        if (kTC) continue;  // the dot came from the tensor cores
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
           const float4 u4 = lds4(Us + (jb + r) * (D + 4) + c);
@@ -318,6 +354,14 @@ __global__ void __launch_bounds__(kThreads, 2)
           dot[r][1] = fmaf(u4.y, r1.y, dot[r][1]);
           dot[r][1] = fmaf(u4.z, r1.z, dot[r][1]);
           dot[r][1] = fmaf(u4.w, r1.w, dot[r][1]);
+        }
+      }
+      if constexpr (kTC) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const float2 dv2 = *reinterpret_cast<const float2*>(Gs + (jb + r) * AS + la);
+          dot[r][0] = dv2.x;
+          dot[r][1] = dv2.y;
         }
       }
 #pragma unroll
@@ -382,7 +426,42 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
       }
     }
-    if (MODE == 2) {
+    if constexpr (MODE == 2 && kTC) {
+      // dV[j][c] = sum_a C[j][a] dW[a][c] on the tensor cores (TF32)
+      constexpr int NCT2 = D / 32;
+      const int gq = lane >> 2, tg = lane & 3;
+      const int jt = (warp >> 2) * 16, wc = (warp & 3) * (D / 4);
+      float acc[NCT2][4];
+#pragma unroll
+      for (int n = 0; n < NCT2; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+#pragma unroll 4
+      for (int k0 = 0; k0 < TA; k0 += 8) {
+        uint32_t af[4];
+        af[0] = to_tf32(Zs[(jt + gq) * AS + k0 + tg]);
+        af[1] = to_tf32(Zs[(jt + gq + 8) * AS + k0 + tg]);
+        af[2] = to_tf32(Zs[(jt + gq) * AS + k0 + tg + 4]);
+        af[3] = to_tf32(Zs[(jt + gq + 8) * AS + k0 + tg + 4]);
+#pragma unroll
+        for (int n = 0; n < NCT2; ++n) {
+          uint32_t bf[2];
+          bf[0] = to_tf32(Rs[(k0 + tg) * (D + 4) + wc + 8 * n + gq]);
+          bf[1] = to_tf32(Rs[(k0 + tg + 4) * (D + 4) + wc + 8 * n + gq]);
+          mma_16x8x8(acc[n], af, bf);
+        }
+      }
+      const int j1 = n0 + jt + gq, j2 = j1 + 8;
+#pragma unroll
+      for (int n = 0; n < NCT2; ++n) {
+        const int c = wc + 8 * n + 2 * tg;
+        if (j1 < N)
+          *reinterpret_cast<float2*>(tok_part2 + (((size_t)lt * BH + bh) * N + j1) * D + c) =
+              make_float2(acc[n][0], acc[n][1]);
+        if (j2 < N)
+          *reinterpret_cast<float2*>(tok_part2 + (((size_t)lt * BH + bh) * N + j2) * D + c) =
+              make_float2(acc[n][2], acc[n][3]);
+      }
+    }
+    if constexpr (MODE == 2 && !kTC) {
       // dV_j = sum_a C_ja dW_a: thread = tokens {ty, ty + 16}, features tx CPT ..
       const int ty = tid >> 4, tx = tid & 15;
       float v0[CPT], v1[CPT];

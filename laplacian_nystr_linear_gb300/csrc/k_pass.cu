@@ -20,17 +20,18 @@
 
 namespace lapnys {
 
-__device__ __forceinline__ void split_range(int nblk, int S, int s, int& b0, int& b1) {
-  b0 = (int)((long long)nblk * s / S);
-  b1 = (int)((long long)nblk * (s + 1) / S);
-}
-
 template <typename T>
 struct TypeOf;
 template <>
 struct TypeOf<float> { static constexpr int id = 0; };
 template <>
 struct TypeOf<__nv_bfloat16> { static constexpr int id = 1; };
+
+__device__ __forceinline__ void split_range(int nblk, int S, int s, int& b0, int& b1) {
+  b0 = (int)((long long)nblk * s / S);
+  b1 = (int)((long long)nblk * (s + 1) / S);
+}
+
 
 // ===========================================================================
 // key pass: grid (landmark tile, split, slice).  Each CTA keeps its 64
@@ -42,11 +43,21 @@ __global__ void __launch_bounds__(kThreads, 2)
     k_key_fwd(const T* __restrict__ K, const T* __restrict__ V, const float* __restrict__ L,
               float* __restrict__ part, int N, int m, int mp, int S, int nblk, float ns) {
   constexpr int CPT = D / 16;
+  // bf16 inputs: the contraction runs on the tensor cores (TF32 kernel values)
+  constexpr bool kTC = TypeOf<T>::id == 1 && D >= 32;
+  constexpr int NCT = D / 16;  // 8-wide column tiles per warp (tensor-core path)
   extern __shared__ float4 sm4[];
   float* Ls = reinterpret_cast<float*>(sm4);
   float* Xs = Ls + tile_floats(D);
   float* Vs = Xs + tile_floats(D);
   float* Cs = Vs + tile_floats(D);  // [64 tokens][68]
+  // tensor-core fragment coordinates: warp -> landmark rows wa .. wa + 15, columns wc .. wc + D/2 - 1
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gq = lane >> 2, tg = lane & 3;
+  const int wa = (warp & 3) * 16, wc = (warp >> 2) * (D / 2);
+  float acc[NCT][4];
+#pragma unroll
+  for (int n = 0; n < NCT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
   const int lt = blockIdx.x, sp = blockIdx.y, bh = blockIdx.z;
   const int a0 = lt * kTile;
   const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
@@ -75,23 +86,52 @@ __global__ void __launch_bounds__(kThreads, 2)
         Cs[(4 * ty + r) * 68 + tx + 16 * s] = (j < N && a < m) ? exp2f(dist[r][s] * ns) : 0.f;
       }
     __syncthreads();
-#pragma unroll 4
-    for (int j = 0; j < kTile; ++j) {
-      const float4 c4 = lds4(Cs + j * 68 + 4 * ty);
-      float v[CPT];
-      lds_cpt<CPT>(Vs + j * row_stride(D) + tx * CPT, v);
+    if constexpr (kTC) {
+      // W[a][c] += sum_j C[j][a] V[j][c] on the tensor cores (TF32; V is bf16, exact in TF32)
+#pragma unroll 2
+      for (int k0 = 0; k0 < kTile; k0 += 8) {
+        uint32_t af[4];
+        af[0] = to_tf32(Cs[(k0 + tg) * 68 + wa + gq]);
+        af[1] = to_tf32(Cs[(k0 + tg) * 68 + wa + gq + 8]);
+        af[2] = to_tf32(Cs[(k0 + tg + 4) * 68 + wa + gq]);
+        af[3] = to_tf32(Cs[(k0 + tg + 4) * 68 + wa + gq + 8]);
 #pragma unroll
-      for (int c = 0; c < CPT; ++c) {
-        w[0][c] = fmaf(c4.x, v[c], w[0][c]);
-        w[1][c] = fmaf(c4.y, v[c], w[1][c]);
-        w[2][c] = fmaf(c4.z, v[c], w[2][c]);
-        w[3][c] = fmaf(c4.w, v[c], w[3][c]);
+        for (int n = 0; n < NCT; ++n) {
+          uint32_t bf[2];
+          bf[0] = __float_as_uint(Vs[(k0 + tg) * row_stride(D) + wc + 8 * n + gq]);
+          bf[1] = __float_as_uint(Vs[(k0 + tg + 4) * row_stride(D) + wc + 8 * n + gq]);
+          mma_16x8x8(acc[n], af, bf);
+        }
+      }
+    } else {
+#pragma unroll 4
+      for (int j = 0; j < kTile; ++j) {
+        const float4 c4 = lds4(Cs + j * 68 + 4 * ty);
+        float v[CPT];
+        lds_cpt<CPT>(Vs + j * row_stride(D) + tx * CPT, v);
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) {
+          w[0][c] = fmaf(c4.x, v[c], w[0][c]);
+          w[1][c] = fmaf(c4.y, v[c], w[1][c]);
+          w[2][c] = fmaf(c4.z, v[c], w[2][c]);
+          w[3][c] = fmaf(c4.w, v[c], w[3][c]);
+        }
       }
     }
   }
-  float* P = part + (((size_t)bh * S + sp) * mp + a0 + 4 * ty) * D + tx * CPT;
+  if constexpr (kTC) {
+    float* P = part + ((size_t)bh * S + sp) * mp * D;
 #pragma unroll
-  for (int s = 0; s < 4; ++s) st_cpt<CPT>(P + s * D, w[s]);
+    for (int n = 0; n < NCT; ++n) {
+      const int c = wc + 8 * n + 2 * tg;
+      *reinterpret_cast<float2*>(P + (size_t)(a0 + wa + gq) * D + c) = make_float2(acc[n][0], acc[n][1]);
+      *reinterpret_cast<float2*>(P + (size_t)(a0 + wa + gq + 8) * D + c) = make_float2(acc[n][2], acc[n][3]);
+    }
+  } else {
+    float* P = part + (((size_t)bh * S + sp) * mp + a0 + 4 * ty) * D + tx * CPT;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) st_cpt<CPT>(P + s * D, w[s]);
+  }
 }
 
 template <int D, typename T>
@@ -271,14 +311,20 @@ __global__ void __launch_bounds__(kThreads, 2)
     k_query_fwd(const T* __restrict__ Q, const float* __restrict__ L, const float* __restrict__ What,
                 const float* __restrict__ stats, T* __restrict__ O, int N, int m, int nt, float ns) {
   constexpr int CPT = D / 16;
+  // bf16 inputs: O += Z W-hat runs on the tensor cores (TF32)
+  constexpr bool kTC = TypeOf<T>::id == 1 && D >= 32;
+  constexpr int NCT = D / 16;
   extern __shared__ float4 sm4[];
   float* Xs = reinterpret_cast<float*>(sm4);
   float* Ls = Xs + tile_floats(D);
   float* Ws = Ls + tile_floats(D);
-  float* Pt = Ws + tile_floats(D);  // [64 landmarks][68 tokens]
+  float* Pt = Ws + tile_floats(D);  // [64 landmarks][68 tokens] (tensor-core path: [64 tokens][68 landmarks])
   __shared__ float mu_s[kTile], rs_s[kTile];
   const int b = blockIdx.x, bh = blockIdx.y;
   const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gq = lane >> 2, tg = lane & 3;
+  const int wj = (warp & 3) * 16, wc = (warp >> 2) * (D / 2);  // tensor-core fragment origin
   const T* Qb = Q + (size_t)bh * N * D;
   load_tile<D>(Xs, Qb, b * kTile, N);
   float o[4][CPT];
@@ -286,6 +332,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   for (int r = 0; r < 4; ++r)
 #pragma unroll
     for (int c = 0; c < CPT; ++c) o[r][c] = 0.f;
+  float acc[NCT][4];
+#pragma unroll
+  for (int n = 0; n < NCT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
   for (int lt = 0; lt < nt; ++lt) {
     const int a0 = lt * kTile;
     __syncthreads();
@@ -309,27 +358,64 @@ __global__ void __launch_bounds__(kThreads, 2)
           pv = exp2f(dist[r][s] * ns);
           if (NORM) pv = (pv - mu_s[a]) * rs_s[a];
         }
-        Pt[a * 68 + 4 * ty + r] = pv;
+        if (kTC)
+          Pt[(4 * ty + r) * 68 + a] = pv;
+        else
+          Pt[a * 68 + 4 * ty + r] = pv;
       }
     __syncthreads();
-#pragma unroll 4
-    for (int a = 0; a < kTile; ++a) {
-      const float4 p4 = lds4(Pt + a * 68 + 4 * ty);
-      float wv[CPT];
-      lds_cpt<CPT>(Ws + a * row_stride(D) + tx * CPT, wv);
+    if constexpr (kTC) {
+#pragma unroll 2
+      for (int k0 = 0; k0 < kTile; k0 += 8) {
+        uint32_t af[4];
+        af[0] = to_tf32(Pt[(wj + gq) * 68 + k0 + tg]);
+        af[1] = to_tf32(Pt[(wj + gq + 8) * 68 + k0 + tg]);
+        af[2] = to_tf32(Pt[(wj + gq) * 68 + k0 + tg + 4]);
+        af[3] = to_tf32(Pt[(wj + gq + 8) * 68 + k0 + tg + 4]);
 #pragma unroll
-      for (int c = 0; c < CPT; ++c) {
-        o[0][c] = fmaf(p4.x, wv[c], o[0][c]);
-        o[1][c] = fmaf(p4.y, wv[c], o[1][c]);
-        o[2][c] = fmaf(p4.z, wv[c], o[2][c]);
-        o[3][c] = fmaf(p4.w, wv[c], o[3][c]);
+        for (int n = 0; n < NCT; ++n) {
+          uint32_t bf[2];
+          bf[0] = to_tf32(Ws[(k0 + tg) * row_stride(D) + wc + 8 * n + gq]);
+          bf[1] = to_tf32(Ws[(k0 + tg + 4) * row_stride(D) + wc + 8 * n + gq]);
+          mma_16x8x8(acc[n], af, bf);
+        }
+      }
+    } else {
+#pragma unroll 4
+      for (int a = 0; a < kTile; ++a) {
+        const float4 p4 = lds4(Pt + a * 68 + 4 * ty);
+        float wv[CPT];
+        lds_cpt<CPT>(Ws + a * row_stride(D) + tx * CPT, wv);
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) {
+          o[0][c] = fmaf(p4.x, wv[c], o[0][c]);
+          o[1][c] = fmaf(p4.y, wv[c], o[1][c]);
+          o[2][c] = fmaf(p4.z, wv[c], o[2][c]);
+          o[3][c] = fmaf(p4.w, wv[c], o[3][c]);
+        }
       }
     }
   }
+  if constexpr (kTC) {
+    const int j1 = b * kTile + wj + gq, j2 = j1 + 8;
 #pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int j = b * kTile + 4 * ty + r;
-    if (j < N) st_cpt<CPT>(O + ((size_t)bh * N + j) * D + tx * CPT, o[r]);
+    for (int n = 0; n < NCT; ++n) {
+      const int c = wc + 8 * n + 2 * tg;
+      if (j1 < N) {
+        const __nv_bfloat162 v = __floats2bfloat162_rn(acc[n][0], acc[n][1]);
+        *reinterpret_cast<__nv_bfloat162*>(O + ((size_t)bh * N + j1) * D + c) = v;
+      }
+      if (j2 < N) {
+        const __nv_bfloat162 v = __floats2bfloat162_rn(acc[n][2], acc[n][3]);
+        *reinterpret_cast<__nv_bfloat162*>(O + ((size_t)bh * N + j2) * D + c) = v;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int j = b * kTile + 4 * ty + r;
+      if (j < N) st_cpt<CPT>(O + ((size_t)bh * N + j) * D + tx * CPT, o[r]);
+    }
   }
 }
 
