@@ -106,10 +106,18 @@ struct BwdArgs {
   float* lm_part;     // [BH][S][mp][d]: dL
   float* lm_part2;    // [BH][S][mp][d]: dWhat (modes 0, 1)
   float* ns_part;     // [BH][S][2][mp]: sum dZ, sum dZ*Z (mode 0)
+  const uint8_t* ties;  // [BH][ceil(N / 32)]: block needs the exact sign path (modes 1, 2)
 };
 cudaError_t run_bwd_tile(const Prob& p, int mode, const BwdArgs& a, cudaStream_t st);
 // modes 1 and 2 with the FMA-pipe sign term (32-token blocks)
 cudaError_t run_bwd_pair(const Prob& p, int mode, const BwdArgs& a, cudaStream_t st);
+// tie detection for the sign term: run_tie_prep reads the landmarks into
+// `scratch` (ties_scratch_bytes), run_ties flags the 32-token blocks of x
+// ([BH][ceil(N / 32)] bytes) that hold a value tied with a landmark value or
+// out of the fast path's range
+size_t ties_scratch_bytes(int BH, int m, int d);
+cudaError_t run_tie_prep(const Prob& p, const float* L, void* scratch, cudaStream_t st);
+cudaError_t run_ties(const Prob& p, const void* x, void* scratch, uint8_t* flags, cudaStream_t st);
 cudaError_t run_mdz(const Prob& p, const float* ns_part, float* mdz, cudaStream_t st);
 cudaError_t run_gram_bwd(const Prob& p, const float* L, const float* A, const float* dA, float* dLA,
                          cudaStream_t st);

@@ -14,12 +14,13 @@
 // 0 or 1 whenever x != l and both lie in {0} u [2^-40, 2^60] (the difference is
 // then at least 2^-64).  So the sign term costs three FMA-pipe operations per
 // (token, landmark, feature) instead of compare/select work on the half-rate
-// ALU pipe.  Ties and out-of-range values are found before the main loop by a
-// binary search over the sorted landmark columns; a token block that has one
-// takes an exact path with sgn(0) = 0.
+// ALU pipe.  Ties and out-of-range values are found ahead of these kernels
+// (k_ties.cu, one flag per 32-token block); a flagged block takes an exact
+// path with sgn(0) = 0.
 //
 // Work split per CTA: one 64-landmark tile and a contiguous range of 32-token
-// blocks; per block
+// blocks; the raw token and upstream rows of the next block are copied into
+// shared memory (cp.async) while the current block computes; per block
 //   phase 1  (thread = 4 tokens x 2 landmarks)  distance, dot, kernel value, g
 //   phase S  (warp = D/8 features, lane = 8 tokens x 8 landmarks) sign term
 //   phase C  contraction: dW-hat_a += sum_j Z_ja dO_j (query side) or
@@ -40,7 +41,6 @@ constexpr float kBig = 18446744073709551616.0f;   // 2^64
 constexpr float kInvBig = 5.42101086242752217e-20f;  // 2^-64
 constexpr float kLo = 9.094947017729282e-13f;        // 2^-40
 constexpr float kHi = 1.152921504606846976e18f;      // 2^60
-constexpr int kMaxFlagBlocks = 4096;                  // per-CTA block flags (bits)
 
 __device__ __forceinline__ float fma_sat(float a, float b, float c) {
   float d;
@@ -58,23 +58,53 @@ __device__ __forceinline__ float ldx(const __nv_bfloat16* p) {
   return __uint_as_float(((uint32_t)__ldg(reinterpret_cast<const unsigned short*>(p))) << 16);
 }
 
+// Shared-memory layout (floats).  The sign-term exchange area is only live in
+// phase S, when the Z tile (d <= 64; the token-side staging then fits in the g
+// tile) or else the U rows are no longer read, so it overlays one of them.
 template <int D>
 struct Smem {
   static constexpr int kScrWarp = 32 * 8 + 3 * 8;  // 8 floats per lane, 8 pad per 8 lanes
+  static constexpr int kScr = 8 * kScrWarp;
+  static constexpr bool kStageInG = TJ * (D + 4) <= TJ * AS;
   static constexpr int LBt = 0;                    // [D][AS]   -scale * l, transposed
   static constexpr int Rs = LBt + D * AS;          // [TA][D+4] R rows
   static constexpr int Xt = Rs + TA * (D + 4);     // [D][JS]   tokens, transposed
   static constexpr int Us = Xt + D * JS;           // [TJ][D+4] U rows
   static constexpr int Gs = Us + TJ * (D + 4);     // [TJ][AS]  2g
   static constexpr int Zs = Gs + TJ * AS;          // [TJ][AS]  Z (query side) or C (key side)
-  static constexpr int Scr = Zs + TJ * AS;         // per-warp exchange areas
-  static constexpr int dLs = Scr + 8 * kScrWarp;   // [D][TA]   landmark-side accumulator
-  static constexpr int total = dLs + D * TA;
-  static constexpr int Ss = Xt;                    // sorted landmark columns [TA][D], pre-pass only
-  static constexpr int Stage = Gs;                 // dX staging [TJ][D+4] over Gs and Zs
-  static_assert(TA * D <= dLs - Xt, "sorted columns must fit before the accumulator");
+  static constexpr int kZsSize = kStageInG && kScr > TJ * AS ? kScr : TJ * AS;
+  static constexpr int dLs = Zs + kZsSize;         // [D][TA]   landmark-side accumulator
+  static constexpr int Raw = dLs + D * TA;         // raw rows of the next block: X then U
+  static constexpr int Scr = kStageInG ? Zs : Us;  // per-warp exchange areas (phase S)
+  static constexpr int Stage = Gs;                 // dX staging [TJ][D+4] over Gs (and Zs)
+  template <typename T>
+  __host__ __device__ static constexpr int raw_pitch() { return D * (int)sizeof(T) + 16; }  // bytes per raw row
+  template <typename T>
+  __host__ __device__ static constexpr int total() { return Raw + 2 * TJ * raw_pitch<T>() / 4; }
   static_assert(TJ * (D + 4) <= 2 * TJ * AS, "staging must fit in the g and Z tiles");
+  static_assert(kStageInG || TJ * (D + 4) >= kScr, "exchange area must fit in the U rows");
 };
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// four consecutive elements (group c4) of a raw row in shared memory
+__device__ __forceinline__ float4 raw4(const uint8_t* row, int c4, const float*) {
+  return *reinterpret_cast<const float4*>(row + 16 * c4);
+}
+__device__ __forceinline__ float4 raw4(const uint8_t* row, int c4, const __nv_bfloat16*) {
+  const uint2 u = *reinterpret_cast<const uint2*>(row + 8 * c4);
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+}
 }  // namespace
 
 // Sign term for the warp's feature columns [cbase, cbase + D/8): lane (jg, ag)
@@ -156,13 +186,13 @@ __device__ __forceinline__ void sign_cols(int cbase, int j0, int al, int jg, int
 }
 
 template <int D, typename T, int MODE, bool NORM>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared memory allows one CTA
     k_bwd_pair(const T* __restrict__ X, const T* __restrict__ U, const float* __restrict__ L,
                const float* __restrict__ R, const float* __restrict__ stats,
                const float* __restrict__ mdz, float* __restrict__ tok_part,
                float* __restrict__ tok_part2, float* __restrict__ lm_part,
-               float* __restrict__ lm_part2, int N, int m, int mp, int S, int nblk, int BH,
-               float ns, float inv_lam) {
+               float* __restrict__ lm_part2, const uint8_t* __restrict__ tie_flags, int N,
+               int m, int mp, int S, int nblk, int BH, float ns, float inv_lam) {
   constexpr int CW = D / 8;     // features per warp in phase S
   constexpr int CPT = D / 16;   // features per thread in phase C
   constexpr bool kDWhat = (MODE == 1) && !NORM;
@@ -181,10 +211,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   float* Zs = sm + SM::Zs;
   float* Scr = sm + SM::Scr;
   float* dLs = sm + SM::dLs;
-  float* Ss = sm + SM::Ss;
   float* Stage = sm + SM::Stage;
+  uint8_t* raw = reinterpret_cast<uint8_t*>(sm + SM::Raw);
+  constexpr int RP = SM::template raw_pitch<T>();
   __shared__ float mu_s[TA], rs_s[TA], m0_s[TA], m1_s[TA];
-  __shared__ unsigned flag_bits[kMaxFlagBlocks / 32];
   __shared__ float rowg_s[TJ], colg_s[TA];  // sums of g over the tile's landmarks / block's tokens
 
   const int lt = blockIdx.x, sp = blockIdx.y, bh = blockIdx.z;
@@ -208,7 +238,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     m0_s[tid] = mdz[(size_t)bh * 2 * mp + a0 + tid];
     m1_s[tid] = mdz[(size_t)bh * 2 * mp + mp + a0 + tid];
   }
-  for (int e = tid; e < kMaxFlagBlocks / 32; e += kThreads) flag_bits[e] = 0u;
   for (int e = tid; e < D * TA; e += kThreads) dLs[e] = 0.f;
   // landmarks outside {0} u [2^-40, 2^60] force the exact path for the whole CTA;
   // then distances use scale 1 instead of 2^64
@@ -222,47 +251,24 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   __syncthreads();
 
-  int b0, b1;
-  b0 = (int)((long long)nblk * sp / S);
-  b1 = (int)((long long)nblk * (sp + 1) / S);
+  const int b0 = (int)((long long)nblk * sp / S);
+  const int b1 = (int)((long long)nblk * (sp + 1) / S);
 
-  // ---- tie / range pre-pass over this CTA's token blocks ----
-  if (!cta_exact) {
-    // sorted landmark columns (invalid landmarks sort last as +inf): a value's
-    // rank is the number of smaller values, ties broken by index
-    const float inf = __int_as_float(0x7f800000);
-    for (int e = tid; e < TA * D; e += kThreads) {
-      const int i = e / D, c = e % D;
-      const float v = i < nv ? LBt[c * AS + i] * -kInvBig : inf;
-      int rank = 0;
-      for (int k = 0; k < TA; ++k) {
-        const float w = k < nv ? LBt[c * AS + k] * -kInvBig : inf;
-        rank += (w < v) || (w == v && k < i);
-      }
-      Ss[rank * D + c] = v;
+  // raw rows of block b (X then U) into shared memory, zero past N
+  auto prefetch = [&](int b) {
+    if (b >= b1) return;
+    const int n0 = b * TJ;
+    constexpr int CH = D * (int)sizeof(T) / 16;  // 16-byte pieces per row
+    for (int id = tid; id < 2 * TJ * CH; id += kThreads) {
+      const int which = id / (TJ * CH), rem = id % (TJ * CH), j = rem / CH, ch = rem % CH;
+      const bool ok = n0 + j < N;
+      const T* src = (which ? Ub : Xb) + (size_t)(ok ? n0 + j : 0) * D;
+      cp_async16(smem_addr(raw + (which * TJ + j) * RP + 16 * ch),
+                 reinterpret_cast<const uint8_t*>(src) + 16 * ch, ok);
     }
-    __syncthreads();
-    // one flat pass over every (token, feature) value of this CTA's blocks; a
-    // tie or an out-of-range value marks its block
-    const int per_blk = TJ * D;
-    const int total = (b1 - b0) * per_blk;
-#pragma unroll 4
-    for (int e = tid; e < total; e += kThreads) {
-      const int blk = e / per_blk, rem = e % per_blk;
-      const int n = (b0 + blk) * TJ + rem / D, c = rem % D;
-      if (n < N) {
-        const float x = ldx(Xb + (size_t)n * D + c);
-        bool tie = out_of_range(x);
-        int lo = 0;
-#pragma unroll
-        for (int step = TA / 2; step > 0; step >>= 1)
-          if (Ss[(lo + step - 1) * D + c] < x) lo += step;
-        tie = tie || (lo < TA && Ss[lo * D + c] == x);
-        if (tie && blk < kMaxFlagBlocks) atomicOr(&flag_bits[blk >> 5], 1u << (blk & 31));
-      }
-    }
-  }
-  __syncthreads();
+    cp_commit();
+  };
+  prefetch(b0);
 
   // phase S ownership: warp -> features [warp*CW, +CW); lane (jg, ag) -> tokens
   // 8 jg .. 8 jg + 7 and landmarks 8 ag .. 8 ag + 7
@@ -277,22 +283,24 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   for (int b = b0; b < b1; ++b) {
     const int n0 = b * TJ;
-    const int k = b - b0;
-    const bool exact =
-        cta_exact || k >= kMaxFlagBlocks || ((flag_bits[k >> 5] >> (k & 31)) & 1u);
+    const bool exact = cta_exact || tie_flags[(size_t)bh * nblk + b] != 0;
+    cp_wait_all();
     __syncthreads();
-    // tokens transposed (Xt[c][j]) and U rows
+    // tokens transposed (Xt[c][j]) and U rows, from the raw copies
     for (int id = tid; id < TJ * (D / 4); id += kThreads) {
       const int c4 = id / TJ, j = id % TJ;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (n0 + j < N) v = ld4(Xb + (size_t)(n0 + j) * D + c4 * 4);
+      const float4 v = raw4(raw + j * RP, c4, Xb);
       Xt[(c4 * 4 + 0) * JS + j] = v.x;
       Xt[(c4 * 4 + 1) * JS + j] = v.y;
       Xt[(c4 * 4 + 2) * JS + j] = v.z;
       Xt[(c4 * 4 + 3) * JS + j] = v.w;
     }
-    load_rows<D, TJ>(Us, Ub, n0, N);
+    for (int id = tid; id < TJ * (D / 4); id += kThreads) {
+      const int j = id / (D / 4), c4 = id % (D / 4);
+      st4(Us + j * (D + 4) + 4 * c4, raw4(raw + (TJ + j) * RP, c4, Ub));
+    }
     __syncthreads();
+    prefetch(b + 1);
 
     if constexpr (kTC) {
       // dot[j][a] = sum_c U[j][c] R[a][c] on the tensor cores, into the g tile
@@ -550,15 +558,15 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 template <int D, typename T, int MODE, bool NORM>
 static cudaError_t bwd_pair_t2(const Prob& p, const BwdArgs& a, cudaStream_t st) {
-  const size_t smem = (size_t)Smem<D>::total * sizeof(float);
+  const size_t smem = (size_t)Smem<D>::template total<T>() * sizeof(float);
   static bool once = (allow_smem(k_bwd_pair<D, T, MODE, NORM>, smem), true);
   (void)once;
   static const char* names[3] = {"", "bwd_query", "bwd_key"};
   const int nblk = (p.N + TJ - 1) / TJ;
   return launch(names[MODE], k_bwd_pair<D, T, MODE, NORM>, dim3(p.nt, p.Sb, p.BH), dim3(kThreads),
                 smem, st, (const T*)a.X, (const T*)a.U, a.L, a.R, a.stats, a.mdz, a.tok_part,
-                a.tok_part2, a.lm_part, a.lm_part2, p.N, p.m, p.mp, p.Sb, nblk, p.BH, p.ns,
-                p.inv_lam);
+                a.tok_part2, a.lm_part, a.lm_part2, (const uint8_t*)a.ties, p.N, p.m, p.mp, p.Sb,
+                nblk, p.BH, p.ns, p.inv_lam);
 }
 
 template <int D, typename T>

@@ -1,0 +1,264 @@
+// Tie detection for the backward sign term of Laplacian-kernel Nystrom
+// attention.
+//
+// The kernel gradient carries sgn(x_c - l_c) per (token, landmark, feature)
+// ("LaplacianFormer", Dutch summary Methodology 1: the L1 norm keeps a
+// non-vanishing gradient); the backward tile kernels evaluate it as one
+// saturated FMA, which is exact except where x_c == l_c (sgn(0) = 0) or a value
+// lies outside {0} u [2^-40, 2^60].  These kernels find, ahead of the tile
+// kernels, every 32-token block holding such a value, so that only those
+// blocks take the exact path.
+//
+// k_tie_prep (one CTA per slice and group of 16 feature columns):
+//   - flags the slice when a landmark value is out of range;
+//   - marks, per feature column, the candidate values in a 8192-bit map keyed
+//     by 13 bits of the value (sign, 5 low exponent bits, 7 high mantissa
+//     bits).  A bf16 token can only equal a landmark value that bf16
+//     represents exactly, so for bf16 tokens only those values are candidates;
+//   - sorts each column's candidate values ascending (the others as +inf).
+// k_ties (many CTAs per slice): streams the tokens 16 bytes at a time; a
+// value that is out of range, or whose key is marked and which a binary search
+// of the sorted column finds, flags its block.
+#include <type_traits>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace lapnys {
+
+namespace {
+constexpr int TJ = 32;                              // tokens per flagged block
+constexpr int kCols = 16;                           // feature columns per prep CTA
+constexpr int kMapWords = 256;                      // 8192-bit map per column
+constexpr float kLo = 9.094947017729282e-13f;        // 2^-40
+constexpr float kHi = 1.152921504606846976e18f;      // 2^60
+constexpr int kMaxBlocks = 2048;                     // flag bits per k_ties CTA
+
+__device__ __forceinline__ bool out_of_range(float v) {
+  const float a = fabsf(v);
+  return !(a <= kHi) || (a != 0.f && a < kLo);
+}
+
+// 13-bit key of a value's bits; both zeros get the key of +0 (they compare equal)
+__device__ __forceinline__ uint32_t tie_key(uint32_t u) {
+  u = (u << 1) == 0u ? 0u : u;
+  return ((u >> 19) & 0x1000u) | ((u >> 16) & 0x0fffu);
+}
+
+template <typename T>
+__device__ __forceinline__ bool candidate(float l) {
+  return !std::is_same<T, __nv_bfloat16>::value || (__float_as_uint(l) & 0xffffu) == 0u;
+}
+
+size_t pow2_at_least(int m) {
+  size_t P = 1;
+  while ((int)P < m) P <<= 1;
+  return P;
+}
+}  // namespace
+
+// scratch: sorted [BH][P][D] f32, map [BH][D][kMapWords] u32, bad [BH][D / kCols] i32
+size_t ties_scratch_bytes(int BH, int m, int d) {
+  const size_t P = pow2_at_least(m);
+  return (size_t)BH * P * d * 4 + (size_t)BH * d * kMapWords * 4 + (size_t)BH * (d / kCols) * 4 +
+         256;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads) k_tie_prep(const float* __restrict__ L,
+                                                       float* __restrict__ sorted,
+                                                       uint32_t* __restrict__ map,
+                                                       int* __restrict__ bad, int m, int P, int D) {
+  extern __shared__ float4 sm4[];
+  float* a = reinterpret_cast<float*>(sm4);                        // [kCols][P]
+  uint32_t* mp = reinterpret_cast<uint32_t*>(a + kCols * P);       // [kCols][kMapWords]
+  const int bh = blockIdx.x, cg = blockIdx.y, c0 = cg * kCols, tid = threadIdx.x;
+  const float* Lb = L + (size_t)bh * m * D;
+  const float inf = __int_as_float(0x7f800000);
+  for (int e = tid; e < kCols * kMapWords; e += kThreads) mp[e] = 0u;
+  __syncthreads();
+  bool b = false;
+  for (int e = tid; e < kCols * P; e += kThreads) {
+    const int cc = e / P, i = e % P;
+    float v = inf;
+    if (i < m) {
+      const float l = __ldg(Lb + (size_t)i * D + c0 + cc);
+      b = b || out_of_range(l);
+      if (candidate<T>(l)) {
+        v = l;
+        const uint32_t k = tie_key(__float_as_uint(l));
+        atomicOr(&mp[cc * kMapWords + (k >> 5)], 1u << (k & 31));
+      }
+    }
+    a[e] = v;
+  }
+  const int any = __syncthreads_or(b);
+  if (tid == 0) bad[bh * (D / kCols) + cg] = any ? 1 : 0;
+  // bitonic sort of every column, ascending
+  for (int k = 2; k <= P; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int e = tid; e < kCols * (P / 2); e += kThreads) {
+        const int cc = e / (P / 2), t = e % (P / 2);
+        const int i = 2 * t - (t & (j - 1));  // lower index of the pair
+        float* col = a + cc * P;
+        const bool up = (i & k) == 0;
+        const float x = col[i], y = col[i + j];
+        if ((x > y) == up) {
+          col[i] = y;
+          col[i + j] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int e = tid; e < kCols * P; e += kThreads) {
+    const int i = e / kCols, cc = e % kCols;
+    sorted[((size_t)bh * P + i) * D + c0 + cc] = a[cc * P + i];
+  }
+  for (int e = tid; e < kCols * kMapWords; e += kThreads)
+    map[((size_t)bh * D + c0) * kMapWords + e] = mp[e];
+}
+
+template <int D, typename T>
+__global__ void __launch_bounds__(kThreads) k_ties(const T* __restrict__ X,
+                                                   const float* __restrict__ sorted,
+                                                   const uint32_t* __restrict__ map,
+                                                   const int* __restrict__ bad,
+                                                   uint8_t* __restrict__ flags, int N, int P,
+                                                   int nblk, int S) {
+  extern __shared__ float4 sm4[];
+  uint32_t* mp = reinterpret_cast<uint32_t*>(sm4);  // [D][kMapWords]
+  __shared__ unsigned bits[kMaxBlocks / 32];
+  constexpr int V = 16 / (int)sizeof(T);  // values per 16-byte load
+  constexpr int G = D / V;                // 16-byte groups per token row
+  static_assert(kThreads % G == 0, "a thread's columns must stay fixed");
+  const int sp = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
+  const int b0 = (int)((long long)nblk * sp / S), b1 = (int)((long long)nblk * (sp + 1) / S);
+  const T* Xb = X + (size_t)bh * N * D;
+  const float* Sb = sorted + (size_t)bh * P * D;
+  bool all = false;
+  for (int g = 0; g < D / kCols; ++g) all = all || bad[bh * (D / kCols) + g] != 0;
+  for (int e = tid; e < kMaxBlocks / 32; e += kThreads) bits[e] = 0u;
+  if (!all)
+    for (int e = tid; e < D * kMapWords / 4; e += kThreads)
+      sm4[e] = __ldg(reinterpret_cast<const float4*>(map + (size_t)bh * D * kMapWords) + e);
+  __syncthreads();
+  if (!all) {
+    const int c0 = (tid % G) * V;
+    const int n_lo = b0 * TJ, n_hi = min(N, b1 * TJ);
+#pragma unroll 2
+    for (int e = tid; e < (n_hi - n_lo) * G; e += kThreads) {
+      const int n = n_lo + e / G;
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(Xb + (size_t)n * D + c0));
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      uint32_t xb[V];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if constexpr (V == 8) {
+          xb[2 * q] = w[q] << 16;
+          xb[2 * q + 1] = w[q] & 0xffff0000u;
+        } else {
+          xb[q] = w[q];
+        }
+      }
+      bool tie = false;
+#pragma unroll
+      for (int q = 0; q < V; ++q) {
+        const float x = __uint_as_float(xb[q]);
+        const uint32_t k = tie_key(xb[q]);
+        const bool marked = (mp[(c0 + q) * kMapWords + (k >> 5)] >> (k & 31)) & 1u;
+        if (out_of_range(x)) {
+          tie = true;
+        } else if (marked) {
+          // exact check: is x among the column's sorted candidate values?
+          const float* col = Sb + c0 + q;
+          int lo = 0;
+          for (int step = P >> 1; step > 0; step >>= 1)
+            if (__ldg(col + (size_t)(lo + step - 1) * D) < x) lo += step;
+          tie = tie || __ldg(col + (size_t)lo * D) == x;
+        }
+      }
+      if (tie) {
+        const int k = n / TJ - b0;
+        if (k < kMaxBlocks) atomicOr(&bits[k >> 5], 1u << (k & 31));
+      }
+    }
+  }
+  __syncthreads();
+  for (int b = b0 + tid; b < b1; b += kThreads) {
+    const int k = b - b0;
+    const bool f = all || k >= kMaxBlocks || ((bits[k >> 5] >> (k & 31)) & 1u);
+    flags[(size_t)bh * nblk + b] = f ? 1 : 0;
+  }
+}
+
+namespace {
+struct TieScratch {
+  float* sorted;
+  uint32_t* map;
+  int* bad;
+  int P;
+};
+TieScratch tie_scratch(const Prob& p, void* scratch) {
+  TieScratch t;
+  t.P = (int)pow2_at_least(p.m);
+  t.sorted = reinterpret_cast<float*>(scratch);
+  t.map = reinterpret_cast<uint32_t*>(t.sorted + (size_t)p.BH * t.P * p.d);
+  t.bad = reinterpret_cast<int*>(t.map + (size_t)p.BH * p.d * kMapWords);
+  return t;
+}
+
+template <int D, typename T>
+cudaError_t ties_t(const Prob& p, const void* x, const TieScratch& t, uint8_t* flags,
+                   cudaStream_t st) {
+  const size_t smem = (size_t)D * kMapWords * 4;
+  static bool once = (allow_smem(k_ties<D, T>, smem), true);
+  (void)once;
+  const int nblk = (p.N + TJ - 1) / TJ;
+  // about four waves of CTAs over the GPU, at most kMaxBlocks blocks each
+  int S = (4 * 152 + p.BH - 1) / p.BH;
+  if (S < (nblk + kMaxBlocks - 1) / kMaxBlocks) S = (nblk + kMaxBlocks - 1) / kMaxBlocks;
+  if (S > nblk) S = nblk;
+  if (S < 1) S = 1;
+  return launch("ties", k_ties<D, T>, dim3(S, p.BH), dim3(kThreads), smem, st, (const T*)x,
+                (const float*)t.sorted, (const uint32_t*)t.map, (const int*)t.bad, flags, p.N,
+                t.P, nblk, S);
+}
+}  // namespace
+
+cudaError_t run_tie_prep(const Prob& p, const float* L, void* scratch, cudaStream_t st) {
+  const TieScratch t = tie_scratch(p, scratch);
+  const size_t smem = (size_t)kCols * t.P * 4 + (size_t)kCols * kMapWords * 4;
+  if (p.dtype == 1) {
+    static bool once = (allow_smem(k_tie_prep<__nv_bfloat16>, 96 * 1024), true);
+    (void)once;
+    return launch("tie_prep", k_tie_prep<__nv_bfloat16>, dim3(p.BH, p.d / kCols), dim3(kThreads),
+                  smem, st, L, t.sorted, t.map, t.bad, p.m, t.P, p.d);
+  }
+  static bool once = (allow_smem(k_tie_prep<float>, 96 * 1024), true);
+  (void)once;
+  return launch("tie_prep", k_tie_prep<float>, dim3(p.BH, p.d / kCols), dim3(kThreads), smem, st,
+                L, t.sorted, t.map, t.bad, p.m, t.P, p.d);
+}
+
+cudaError_t run_ties(const Prob& p, const void* x, void* scratch, uint8_t* flags, cudaStream_t st) {
+  const TieScratch t = tie_scratch(p, scratch);
+  if (p.dtype == 1) {
+    switch (p.d) {
+      case 16: return ties_t<16, __nv_bfloat16>(p, x, t, flags, st);
+      case 32: return ties_t<32, __nv_bfloat16>(p, x, t, flags, st);
+      case 64: return ties_t<64, __nv_bfloat16>(p, x, t, flags, st);
+      case 128: return ties_t<128, __nv_bfloat16>(p, x, t, flags, st);
+    }
+  } else {
+    switch (p.d) {
+      case 16: return ties_t<16, float>(p, x, t, flags, st);
+      case 32: return ties_t<32, float>(p, x, t, flags, st);
+      case 64: return ties_t<64, float>(p, x, t, flags, st);
+      case 128: return ties_t<128, float>(p, x, t, flags, st);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace lapnys

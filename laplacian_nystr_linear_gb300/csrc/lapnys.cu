@@ -133,6 +133,7 @@ struct WsLayout {
   size_t dWhp, dLqp, dLcp, nsp, mdz;           // backward landmark-side partials
   size_t dQp, dKp, dVp;                        // backward token-side partials
   size_t dWh, dW, dLA, dL, G, XG, Tm, dA;      // backward landmark-side results
+  size_t ties, tie_scratch;                    // tie flags (query, key) and their scratch
   size_t total;
 };
 
@@ -161,6 +162,8 @@ static WsLayout ws_layout(const Prob& p) {
   w.XG = o; o = align256(o + BH * m * m * f);
   w.Tm = o; o = align256(o + BH * m * m * f);
   w.dA = o; o = align256(o + BH * m * m * f);
+  w.ties = o; o = align256(o + 2 * BH * (size_t)((p.N + 31) / 32));
+  w.tie_scratch = o; o = align256(o + ties_scratch_bytes(p.BH, p.m, p.d));
   w.total = o;
   return w;
 }
@@ -486,11 +489,19 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
   const long mm = (long)m * m;
   const long md = (long)m * d;
 
+  // which 32-token blocks need the exact sign path (a value tied with a
+  // landmark value, or out of the fast path's range)
+  uint8_t* ties_q = (uint8_t*)(wb + w.ties);
+  uint8_t* ties_k = tied_qk ? ties_q : ties_q + (size_t)p.BH * ((N + 31) / 32);
+  CK(run_tie_prep(p, L, wb + w.tie_scratch, stream));
+  CK(run_ties(p, q, wb + w.tie_scratch, ties_q, stream));
+  if (!tied_qk) CK(run_ties(p, k, wb + w.tie_scratch, ties_k, stream));
+
   // ---- query side ----
   BwdArgs qa;
   memset(&qa, 0, sizeof(qa));
   qa.X = q; qa.U = dout; qa.L = L; qa.R = What; qa.stats = stats; qa.mdz = mdz;
-  qa.tok_part = dQp; qa.lm_part = dLqp; qa.lm_part2 = dWhp; qa.ns_part = nsp;
+  qa.tok_part = dQp; qa.lm_part = dLqp; qa.lm_part2 = dWhp; qa.ns_part = nsp; qa.ties = ties_q;
   if (p.norm()) {
     CK(run_bwd_tile(p, 0, qa, stream));
     CK(run_mdz(p, nsp, mdz, stream));
@@ -545,7 +556,7 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
   BwdArgs ka;
   memset(&ka, 0, sizeof(ka));
   ka.X = k; ka.U = v; ka.L = L; ka.R = dW;
-  ka.tok_part = dKp; ka.tok_part2 = dVp; ka.lm_part = dLcp;
+  ka.tok_part = dKp; ka.tok_part2 = dVp; ka.lm_part = dLcp; ka.ties = ties_k;
   CK(run_bwd_pair(p, 2, ka, stream));
   CK(run_reduce_dl(p, dLqp, dLcp, dLA, dL, stream));
   CK(run_finalize(p, dQp, dKp, dVp, dL, dq, dk, dv, stream));

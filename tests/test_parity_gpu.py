@@ -13,7 +13,8 @@ import pytest
 import torch
 
 from laplacian_nystr_linear_gb300 import api
-from laplacian_nystr_linear_gb300.inputs import WORKLOADS, Workload, make_inputs, random_inputs
+from laplacian_nystr_linear_gb300.inputs import (WORKLOADS, Workload, make_inputs, random_inputs,
+                                                 round_bf16)
 from oracle import lapnys_oracle as orc
 
 from tests._parity import compare, gpu_run, oracle_run, params_of, rel, to_dev
@@ -149,6 +150,9 @@ SMALL = [
     _small("tiny_grid", grid_h=2, grid_w=2, m=4, d=16, iters=5),
     _small("m81", grid_h=18, grid_w=18, m=81, d=32, iters=12, norm=True),
     _small("batch", B=3, H=2, grid_h=16, grid_w=16, m=16, d=64, iters=10),
+    # one landmark per token with Q = K: every token ties with its own landmark
+    _small("bf16_tied_mN", dtype="bf16", d=64, grid_h=4, grid_w=4, m=16, iters=6, tied=True),
+    _small("bf16_mN", dtype="bf16", d=32, grid_h=8, grid_w=8, m=64, iters=6),
 ]
 
 
@@ -170,6 +174,45 @@ def test_constant_inputs_use_zero_sign():
     g = gpu_run(w, inp, backward=True)
     o = oracle_run(w, inp, backward=True)
     print(w.name, compare(w, g, o, backward=True))
+
+
+def test_constant_bf16_inputs_use_zero_sign():
+    w = _small("const_bf16", dtype="bf16", grid_h=8, grid_w=8, m=16, d=64, iters=4)
+    inp = random_inputs(4, 2, 2, w.N, w.d, "bf16")
+    inp["q"] = np.full_like(inp["q"], -1.5)
+    inp["k"] = np.full_like(inp["k"], -1.5)
+    w = dataclasses.replace(w, B=2, H=2)
+    g = gpu_run(w, inp, backward=True)
+    o = oracle_run(w, inp, backward=True)
+    print(w.name, compare(w, g, o, backward=True))
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("m", [16, 64])
+def test_ties_in_a_few_columns(dtype, m):
+    # In 13 feature columns every K token of a pooling window holds the same
+    # bf16 value, so that window's landmark equals it exactly and the window's
+    # tokens tie with it (sgn(0) = 0); half of the Q tokens copy those values
+    # too, the other columns stay random.  Reading those ties as sgn = -1
+    # instead moves dq or dk of the oracle by at least 8e-3 (2.6e-2 and 4.5e-2
+    # at m = 16), so bf16 is held to 5e-3 here, about 3x the bf16 rounding error
+    # of the outputs, and fp32 to its usual 1e-4.
+    w = _small("col_ties", dtype=dtype, grid_h=16, grid_w=16, m=m, d=64, iters=6)
+    inp = random_inputs(11 + m, 1, 2, w.N, w.d, dtype)
+    w = dataclasses.replace(w, B=1, H=2)
+    s = int(round(m ** 0.5))
+    r = w.grid_h // s
+    rng = np.random.default_rng(m)
+    for c in range(3, 64, 5):
+        vals = round_bf16(rng.standard_normal((2, s, s)))
+        for h in range(2):
+            win = vals[h].repeat(r, 0).repeat(r, 1).reshape(-1)   # value of each token's window
+            inp["k"][0, h, :, c] = win
+            pick = rng.random(w.N) < 0.5
+            inp["q"][0, h, pick, c] = win[rng.permutation(w.N)[pick]]
+    g = gpu_run(w, inp, backward=True)
+    o = oracle_run(w, inp, backward=True)
+    print(w.name, dtype, m, compare(w, g, o, backward=True, tol=5e-3 if dtype == "bf16" else None))
 
 
 def test_deterministic():
