@@ -79,6 +79,14 @@ cudaError_t run_tcgemm(bool ta, bool tb, int batch, int M, int N, int K, const f
                        const float* E, int lde, long sE, float alpha, float beta, cudaStream_t st);
 // value of the device error word set by expired bounded waits (-1 on failure)
 int read_wait_error(bool clear);
+// device address of that word on the current device (null on failure)
+int* wait_error_address();
+// the whole Newton-Schulz iteration (reverse: its exact reverse) of every
+// slice in one cluster launch, for ns_cluster_ok(m); buffers as in the ctx and
+// workspace layouts ([BH][nx or ny or 1][m][m])
+bool ns_cluster_ok(int m);
+cudaError_t run_ns_cluster(const Prob& p, bool reverse, const float* A, float* X, float* Y, int nx,
+                           int ny, float* G, float* XG, float* Tm, float* dA, cudaStream_t st);
 
 // forward passes
 cudaError_t run_key_fwd(const Prob& p, const void* k, const void* v, const float* L, float* part,

@@ -21,6 +21,8 @@
 // Every wait is bounded: on expiry the kernel records an error in a device
 // word (read by lapnys_device_status), stops issuing work, waits a bounded
 // time for its MMAs, frees its TMEM and returns.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -384,6 +386,20 @@ cudaError_t run_tcgemm(bool ta, bool tb, int batch, int M, int N, int K, const f
   TC(false, false) TC(false, true) TC(true, false) TC(true, true)
 #undef TC
   return cudaErrorInvalidValue;
+}
+
+int* wait_error_address() {
+  static std::mutex mu;
+  static int* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_lapnys_wait_error) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<int*>(p);
+  }
+  return addr[dev];
 }
 
 int read_wait_error(bool clear) {

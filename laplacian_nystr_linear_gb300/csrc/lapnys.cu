@@ -210,6 +210,11 @@ static int ns_forward_large(const Prob& p, const float* A, float* X, float* Y, i
                             cudaStream_t st) {
   const int m = p.m;
   const long mm = (long)m * m;
+  if (ns_cluster_ok(m)) {
+    // every iteration of every slice in one launch (a cluster per slice)
+    CK(run_ns_cluster(p, false, A, X, Y, nx, ny, nullptr, nullptr, nullptr, nullptr, st));
+    return LAPNYS_OK;
+  }
   for (int t = 0; t < p.iters; ++t) {
     float* Xt = X + (long)(t % nx) * mm;
     float* Xn = X + (long)((t + 1) % nx) * mm;
@@ -532,7 +537,10 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
              stream));
     if (iters == 0) CK(run_zero(dA, (size_t)p.BH * mm, stream));
     float* Sc = G;
-    for (int t = iters - 1; t >= 0; --t) {
+    if (ns_cluster_ok(m))  // the whole reverse in one launch; G ends as dLoss/dX_0
+      CK(run_ns_cluster(p, true, A, const_cast<float*>(X), const_cast<float*>(Y), c.nx, c.ny, G,
+                        XG, Tm, dA, stream));
+    for (int t = ns_cluster_ok(m) ? -1 : iters - 1; t >= 0; --t) {
       const float* Xt = X + (long)t * mm;
       const float* Yt = Y + (long)t * mm;
       // XG = X_t^T G
