@@ -58,31 +58,25 @@ __device__ __forceinline__ float ldx(const __nv_bfloat16* p) {
   return __uint_as_float(((uint32_t)__ldg(reinterpret_cast<const unsigned short*>(p))) << 16);
 }
 
-// Shared-memory layout (floats).  The sign-term exchange area is only live in
-// phase S, when the Z tile (d <= 64; the token-side staging then fits in the g
-// tile) or else the U rows are no longer read, so it overlays one of them.
+// Shared-memory layout (floats).
 template <int D>
 struct Smem {
-  static constexpr int kScrWarp = 32 * 8 + 3 * 8;  // 8 floats per lane, 8 pad per 8 lanes
-  static constexpr int kScr = 8 * kScrWarp;
-  static constexpr bool kStageInG = TJ * (D + 4) <= TJ * AS;
   static constexpr int LBt = 0;                    // [D][AS]   -scale * l, transposed
   static constexpr int Rs = LBt + D * AS;          // [TA][D+4] R rows
   static constexpr int Xt = Rs + TA * (D + 4);     // [D][JS]   tokens, transposed
   static constexpr int Us = Xt + D * JS;           // [TJ][D+4] U rows
   static constexpr int Gs = Us + TJ * (D + 4);     // [TJ][AS]  2g
-  static constexpr int Zs = Gs + TJ * AS;          // [TJ][AS]  Z (query side) or C (key side)
-  static constexpr int kZsSize = kStageInG && kScr > TJ * AS ? kScr : TJ * AS;
-  static constexpr int dLs = Zs + kZsSize;         // [D][TA]   landmark-side accumulator
+  static constexpr int Zs = Gs + TJ * AS;          // [TJ][ZS]  Z (query side) or C (key side)
+  static constexpr int dLs = Zs + TJ * (AS + 4);   // [D][TA]   landmark-side accumulator
   static constexpr int Raw = dLs + D * TA;         // raw rows of the next block: X then U
-  static constexpr int Scr = kStageInG ? Zs : Us;  // per-warp exchange areas (phase S)
   static constexpr int Stage = Gs;                 // dX staging [TJ][D+4] over Gs (and Zs)
   template <typename T>
   __host__ __device__ static constexpr int raw_pitch() { return D * (int)sizeof(T) + 16; }  // bytes per raw row
   template <typename T>
   __host__ __device__ static constexpr int total() { return Raw + 2 * TJ * raw_pitch<T>() / 4; }
   static_assert(TJ * (D + 4) <= 2 * TJ * AS, "staging must fit in the g and Z tiles");
-  static_assert(kStageInG || TJ * (D + 4) >= kScr, "exchange area must fit in the U rows");
+  // row stride of the Z / C tile: query side AS + 4 (its tensor-core dW-hat
+  // reads columns of it), key side AS (its dV reads rows)
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -107,17 +101,27 @@ __device__ __forceinline__ float4 raw4(const uint8_t* row, int c4, const __nv_bf
 }
 }  // namespace
 
+// Landmark slot of landmark a (0..63) in the g and scaled-landmark tiles: 4
+// floats of padding after the first 32 put the 8-landmark groups read by
+// lanes ag and ag + 4 into different banks.
+__device__ __forceinline__ int pa(int a) { return a + ((a >> 5) << 2); }
+
 // Sign term for the warp's feature columns [cbase, cbase + D/8): lane (jg, ag)
-// holds 2g for tokens j0..j0+7 x landmarks al..al+7; partial sums are exchanged
-// through the warp's scratch area; the token-side result goes to Stage and the
+// holds 2g for tokens j0..j0+7 x landmarks al..al+7.  Per feature the lane's
+// 8 token partials are reduce-scattered over the 8 lanes of its jg group
+// (lane ag keeps token j0 + ag) and its 8 landmark partials over the 4 lanes
+// of its ag group (lane jg keeps landmarks al + 2 jg, al + 2 jg + 1), by warp
+// shuffles in a fixed order; the token-side result goes to Stage and the
 // landmark-side sum into dLs.
 template <int D, bool EXACT>
 __device__ __forceinline__ void sign_cols(int cbase, int j0, int al, int jg, int ag,
                                           const float (&g2)[8][8], const float* Xt,
-                                          const float* LBt, float* mine, const float* qsrc,
-                                          const float* lsrc, float rowg, float inv_scale,
+                                          const float* LBt, float rowg, float inv_scale,
                                           float* Stage, float* dLs) {
   constexpr int CW = D / 8;
+  constexpr unsigned kFull = 0xffffffffu;
+  const bool b2 = ag & 4, b1 = ag & 2, b0 = ag & 1;
+  const bool c1 = jg & 2, c0 = jg & 1;
 #pragma unroll 1
   for (int ci = 0; ci < CW; ++ci) {
     const int c = cbase + ci;
@@ -129,8 +133,8 @@ __device__ __forceinline__ void sign_cols(int cbase, int j0, int al, int jg, int
       x[4] = v.x; x[5] = v.y; x[6] = v.z; x[7] = v.w;
     }
     {
-      const float4 u = lds4(LBt + c * AS + al);
-      const float4 v = lds4(LBt + c * AS + al + 4);
+      const float4 u = lds4(LBt + c * AS + pa(al));
+      const float4 v = lds4(LBt + c * AS + pa(al) + 4);
       lb[0] = u.x; lb[1] = u.y; lb[2] = u.z; lb[3] = u.w;
       lb[4] = v.x; lb[5] = v.y; lb[6] = v.z; lb[7] = v.w;
     }
@@ -157,30 +161,40 @@ __device__ __forceinline__ void sign_cols(int cbase, int j0, int al, int jg, int
           pl[t] += v;
         }
     }
-    st4(mine, make_float4(pq[0], pq[1], pq[2], pq[3]));
-    st4(mine + 4, make_float4(pq[4], pq[5], pq[6], pq[7]));
-    __syncwarp();
-    float qs = 0.f;
+    // token side: halve the 8 partials three times across lanes ag ^ 4, ^ 2, ^ 1
+    float q4[4], q2[2], qs;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) qs += qsrc[8 * q];
-    __syncwarp();
-    st4(mine, make_float4(pl[0], pl[1], pl[2], pl[3]));
-    st4(mine + 4, make_float4(pl[4], pl[5], pl[6], pl[7]));
-    __syncwarp();
-    float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float2 v = *reinterpret_cast<const float2*>(lsrc + 72 * q);
-      ls0 += v.x;
-      ls1 += v.y;
+    for (int k = 0; k < 4; ++k) {
+      const float send = b2 ? pq[k] : pq[k + 4], keep = b2 ? pq[k + 4] : pq[k];
+      q4[k] = keep + __shfl_xor_sync(kFull, send, 4);
     }
-    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float send = b1 ? q4[k] : q4[k + 2], keep = b1 ? q4[k + 2] : q4[k];
+      q2[k] = keep + __shfl_xor_sync(kFull, send, 2);
+    }
+    {
+      const float send = b0 ? q2[0] : q2[1], keep = b0 ? q2[1] : q2[0];
+      qs = keep + __shfl_xor_sync(kFull, send, 1);
+    }
+    // landmark side: halve twice across lanes jg ^ 2, jg ^ 1 (lane bits 4, 3)
+    float l4[4], l2[2];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float send = c1 ? pl[k] : pl[k + 4], keep = c1 ? pl[k + 4] : pl[k];
+      l4[k] = keep + __shfl_xor_sync(kFull, send, 16);
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float send = c0 ? l4[k] : l4[k + 2], keep = c0 ? l4[k + 2] : l4[k];
+      l2[k] = keep + __shfl_xor_sync(kFull, send, 8);
+    }
     // fast path: dX = G_j - sum_a 2 g [x > l];  exact path: dX = -sum_a g sgn
     Stage[(j0 + ag) * (D + 4) + c] = EXACT ? -qs : rowg - qs;
     float2* dl = reinterpret_cast<float2*>(dLs + c * TA + al + 2 * jg);
     float2 o = *dl;
-    o.x += ls0;
-    o.y += ls1;
+    o.x += l2[0];
+    o.y += l2[1];
     *dl = o;
   }
 }
@@ -200,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
   // run on the tensor cores in TF32; dW-hat stays in fp32 (it is amplified by
   // the Newton-Schulz reverse, where TF32 rounding would cost ~5e-3 on dK)
   constexpr bool kTC = std::is_same<T, __nv_bfloat16>::value && D >= 32;
+  constexpr int ZS = MODE == 1 ? AS + 4 : AS;  // row stride of the Z / C tile
   using SM = Smem<D>;
   extern __shared__ float4 sm4[];
   float* sm = reinterpret_cast<float*>(sm4);
@@ -209,7 +224,6 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
   float* Us = sm + SM::Us;
   float* Gs = sm + SM::Gs;
   float* Zs = sm + SM::Zs;
-  float* Scr = sm + SM::Scr;
   float* dLs = sm + SM::dLs;
   float* Stage = sm + SM::Stage;
   uint8_t* raw = reinterpret_cast<uint8_t*>(sm + SM::Raw);
@@ -247,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
   const float ns_s = ns * inv_scale;  // exp2 argument per unit of scaled distance
   for (int e = tid; e < TA * D; e += kThreads) {
     const int c = e / TA, a = e % TA;
-    LBt[c * AS + a] = a < nv ? -scale * __ldg(Lb + (size_t)a * D + c) : 0.f;
+    LBt[c * AS + pa(a)] = a < nv ? -scale * __ldg(Lb + (size_t)a * D + c) : 0.f;
   }
   __syncthreads();
 
@@ -280,6 +294,12 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
   for (int s = 0; s < 4; ++s)
 #pragma unroll
     for (int c = 0; c < CPT; ++c) dw[s][c] = 0.f;
+  // tensor-core dW-hat (bf16 inputs): warp = landmarks 16 (warp & 3) .., features
+  // (warp >> 2) D/2 ..; mma C fragments per 8-feature tile
+  constexpr int NT8 = D / 16;
+  float dwt[NT8][4];
+#pragma unroll
+  for (int n = 0; n < NT8; ++n) dwt[n][0] = dwt[n][1] = dwt[n][2] = dwt[n][3] = 0.f;
 
   for (int b = b0; b < b1; ++b) {
     const int n0 = b * TJ;
@@ -325,8 +345,9 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
 #pragma unroll
       for (int n = 0; n < 2; ++n) {
         const int a = wa + 8 * n + 2 * tg;
-        *reinterpret_cast<float2*>(Gs + (jt + gq) * AS + a) = make_float2(acc[n][0], acc[n][1]);
-        *reinterpret_cast<float2*>(Gs + (jt + gq + 8) * AS + a) = make_float2(acc[n][2], acc[n][3]);
+        *reinterpret_cast<float2*>(Gs + (jt + gq) * AS + pa(a)) = make_float2(acc[n][0], acc[n][1]);
+        *reinterpret_cast<float2*>(Gs + (jt + gq + 8) * AS + pa(a)) =
+            make_float2(acc[n][2], acc[n][3]);
       }
       __syncthreads();
     }
@@ -344,30 +365,31 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const float4 x4 = lds4(Xt + (c + q) * JS + jb);
-          const float2 lb = *reinterpret_cast<const float2*>(LBt + (c + q) * AS + la);
+          const float2 lb = *reinterpret_cast<const float2*>(LBt + (c + q) * AS + pa(la));
           dist[0][0] += fabsf(fmaf(x4.x, scale, lb.x)); dist[0][1] += fabsf(fmaf(x4.x, scale, lb.y));
           dist[1][0] += fabsf(fmaf(x4.y, scale, lb.x)); dist[1][1] += fabsf(fmaf(x4.y, scale, lb.y));
           dist[2][0] += fabsf(fmaf(x4.z, scale, lb.x)); dist[2][1] += fabsf(fmaf(x4.z, scale, lb.y));
           dist[3][0] += fabsf(fmaf(x4.w, scale, lb.x)); dist[3][1] += fabsf(fmaf(x4.w, scale, lb.y));
         }
-        if (kTC) continue;  // the dot came from the tensor cores
+        if constexpr (!kTC) {  // (bf16: the dot came from the tensor cores)
 #pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const float4 u4 = lds4(Us + (jb + r) * (D + 4) + c);
-          dot[r][0] = fmaf(u4.x, r0.x, dot[r][0]);
-          dot[r][0] = fmaf(u4.y, r0.y, dot[r][0]);
-          dot[r][0] = fmaf(u4.z, r0.z, dot[r][0]);
-          dot[r][0] = fmaf(u4.w, r0.w, dot[r][0]);
-          dot[r][1] = fmaf(u4.x, r1.x, dot[r][1]);
-          dot[r][1] = fmaf(u4.y, r1.y, dot[r][1]);
-          dot[r][1] = fmaf(u4.z, r1.z, dot[r][1]);
-          dot[r][1] = fmaf(u4.w, r1.w, dot[r][1]);
+          for (int r = 0; r < 4; ++r) {
+            const float4 u4 = lds4(Us + (jb + r) * (D + 4) + c);
+            dot[r][0] = fmaf(u4.x, r0.x, dot[r][0]);
+            dot[r][0] = fmaf(u4.y, r0.y, dot[r][0]);
+            dot[r][0] = fmaf(u4.z, r0.z, dot[r][0]);
+            dot[r][0] = fmaf(u4.w, r0.w, dot[r][0]);
+            dot[r][1] = fmaf(u4.x, r1.x, dot[r][1]);
+            dot[r][1] = fmaf(u4.y, r1.y, dot[r][1]);
+            dot[r][1] = fmaf(u4.z, r1.z, dot[r][1]);
+            dot[r][1] = fmaf(u4.w, r1.w, dot[r][1]);
+          }
         }
       }
       if constexpr (kTC) {
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          const float2 dv2 = *reinterpret_cast<const float2*>(Gs + (jb + r) * AS + la);
+          const float2 dv2 = *reinterpret_cast<const float2*>(Gs + (jb + r) * AS + pa(la));
           dot[r][0] = dv2.x;
           dot[r][1] = dv2.y;
         }
@@ -394,8 +416,8 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
           gv[h] = valid ? 2.f * g : 0.f;
           zv[h] = valid ? zc : 0.f;
         }
-        *reinterpret_cast<float2*>(Gs + j * AS + la) = make_float2(gv[0], gv[1]);
-        *reinterpret_cast<float2*>(Zs + j * AS + la) = make_float2(zv[0], zv[1]);
+        *reinterpret_cast<float2*>(Gs + j * AS + pa(la)) = make_float2(gv[0], gv[1]);
+        *reinterpret_cast<float2*>(Zs + j * ZS + la) = make_float2(zv[0], zv[1]);
       }
     }
     __syncthreads();
@@ -405,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
       float sacc = 0.f;
 #pragma unroll 4
       for (int a = 0; a < TA; a += 4) {
-        const float4 v = lds4(Gs + tid * AS + a);
+        const float4 v = lds4(Gs + tid * AS + pa(a));
         sacc += (v.x + v.y) + (v.z + v.w);
       }
       rowg_s[tid] = 0.5f * sacc;
@@ -413,16 +435,40 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
       const int a = tid - TJ;
       float sacc = 0.f;
 #pragma unroll 8
-      for (int j = 0; j < TJ; ++j) sacc += Gs[j * AS + a];
+      for (int j = 0; j < TJ; ++j) sacc += Gs[j * AS + pa(a)];
       colg_s[a] = 0.5f * sacc;
     }
 
     // ---- phase C: contractions ----
-    if (kDWhat) {
+    if constexpr (kDWhat && kTC) {
+      // dW-hat[a][c] += sum_j Z[j][a] U[j][c] as (Z_hi + Z_lo)^T U on the tensor
+      // cores: bf16 U is exact in TF32 and the split of Z keeps fp32 accuracy
+      const int gq = lane >> 2, tg = lane & 3;
+      const int am = (warp & 3) * 16, cn = (warp >> 2) * (D / 2);
+#pragma unroll
+      for (int k0 = 0; k0 < TJ; k0 += 8) {
+        const float z[4] = {Zs[(k0 + tg) * ZS + am + gq], Zs[(k0 + tg) * ZS + am + gq + 8],
+                            Zs[(k0 + tg + 4) * ZS + am + gq], Zs[(k0 + tg + 4) * ZS + am + gq + 8]};
+        uint32_t ah[4], alo[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          ah[i] = to_tf32(z[i]);
+          alo[i] = to_tf32(z[i] - __uint_as_float(ah[i]));
+        }
+#pragma unroll
+        for (int n = 0; n < NT8; ++n) {
+          uint32_t bf[2];
+          bf[0] = __float_as_uint(Us[(k0 + tg) * (D + 4) + cn + 8 * n + gq]);
+          bf[1] = __float_as_uint(Us[(k0 + tg + 4) * (D + 4) + cn + 8 * n + gq]);
+          mma_16x8x8(dwt[n], ah, bf);
+          mma_16x8x8(dwt[n], alo, bf);
+        }
+      }
+    } else if constexpr (kDWhat) {
       const int ty = tid >> 4, tx = tid & 15;
 #pragma unroll 4
       for (int j = 0; j < TJ; ++j) {
-        const float4 z4 = lds4(Zs + j * AS + 4 * ty);
+        const float4 z4 = lds4(Zs + j * ZS + 4 * ty);
         float uv[CPT];
         lds_cpt<CPT>(Us + j * (D + 4) + tx * CPT, uv);
 #pragma unroll
@@ -445,10 +491,10 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
 #pragma unroll 4
       for (int k0 = 0; k0 < TA; k0 += 8) {
         uint32_t af[4];
-        af[0] = to_tf32(Zs[(jt + gq) * AS + k0 + tg]);
-        af[1] = to_tf32(Zs[(jt + gq + 8) * AS + k0 + tg]);
-        af[2] = to_tf32(Zs[(jt + gq) * AS + k0 + tg + 4]);
-        af[3] = to_tf32(Zs[(jt + gq + 8) * AS + k0 + tg + 4]);
+        af[0] = to_tf32(Zs[(jt + gq) * ZS + k0 + tg]);
+        af[1] = to_tf32(Zs[(jt + gq + 8) * ZS + k0 + tg]);
+        af[2] = to_tf32(Zs[(jt + gq) * ZS + k0 + tg + 4]);
+        af[3] = to_tf32(Zs[(jt + gq + 8) * ZS + k0 + tg + 4]);
 #pragma unroll
         for (int n = 0; n < NCT2; ++n) {
           uint32_t bf[2];
@@ -477,8 +523,8 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
       for (int c = 0; c < CPT; ++c) v0[c] = v1[c] = 0.f;
 #pragma unroll 2
       for (int a = 0; a < TA; a += 4) {
-        const float4 c0 = lds4(Zs + ty * AS + a);
-        const float4 c1 = lds4(Zs + (ty + 16) * AS + a);
+        const float4 c0 = lds4(Zs + ty * ZS + a);
+        const float4 c1 = lds4(Zs + (ty + 16) * ZS + a);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           float rv[CPT];
@@ -503,18 +549,11 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
       float g2[8][8];
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
-        const float4 u = lds4(Gs + (j0 + r) * AS + al);
-        const float4 v = lds4(Gs + (j0 + r) * AS + al + 4);
+        const float4 u = lds4(Gs + (j0 + r) * AS + pa(al));
+        const float4 v = lds4(Gs + (j0 + r) * AS + pa(al) + 4);
         g2[r][0] = u.x; g2[r][1] = u.y; g2[r][2] = u.z; g2[r][3] = u.w;
         g2[r][4] = v.x; g2[r][5] = v.y; g2[r][6] = v.z; g2[r][7] = v.w;
       }
-      // per-warp exchange area: lane l's 8 values at 8 l + 8 (l >> 3)
-      float* scr = Scr + warp * SM::kScrWarp;
-      float* mine = scr + 8 * lane + 8 * jg;
-      // token side gathers element ag of lanes 8 jg + q; landmark side gathers
-      // elements 2 jg, 2 jg + 1 of lanes 8 q + ag
-      const float* qsrc = scr + 72 * jg + ag;
-      const float* lsrc = scr + 8 * ag + 2 * jg;
       __syncthreads();  // g and Z tiles are free from here on (staging); sums are ready
       const float rowg = rowg_s[j0 + ag];
       if (!exact) {
@@ -522,11 +561,9 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
         colg_acc1 += colg_s[al + 2 * jg + 1];
       }
       if (exact)
-        sign_cols<D, true>(warp * CW, j0, al, jg, ag, g2, Xt, LBt, mine, qsrc, lsrc, rowg,
-                           inv_scale, Stage, dLs);
+        sign_cols<D, true>(warp * CW, j0, al, jg, ag, g2, Xt, LBt, rowg, inv_scale, Stage, dLs);
       else
-        sign_cols<D, false>(warp * CW, j0, al, jg, ag, g2, Xt, LBt, mine, qsrc, lsrc, rowg,
-                            inv_scale, Stage, dLs);
+        sign_cols<D, false>(warp * CW, j0, al, jg, ag, g2, Xt, LBt, rowg, inv_scale, Stage, dLs);
     }
     __syncthreads();
     // staged token-side results -> per-tile partial rows
@@ -548,7 +585,16 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
       o[(size_t)(a0 + al + 1) * D + c] = dLs[c * TA + al + 1] - colg_acc1;
     }
   }
-  if (kDWhat) {
+  if constexpr (kDWhat && kTC) {
+    const int gq = lane >> 2, tg = lane & 3;
+    const int am = (warp & 3) * 16, cn = (warp >> 2) * (D / 2);
+    float* o = lm_part2 + (((size_t)bh * S + sp) * mp + a0 + am + gq) * D + cn + 2 * tg;
+#pragma unroll
+    for (int n = 0; n < NT8; ++n) {
+      *reinterpret_cast<float2*>(o + 8 * n) = make_float2(dwt[n][0], dwt[n][1]);
+      *reinterpret_cast<float2*>(o + (size_t)8 * D + 8 * n) = make_float2(dwt[n][2], dwt[n][3]);
+    }
+  } else if constexpr (kDWhat) {
     const int ty = tid >> 4, tx = tid & 15;
     float* o = lm_part2 + (((size_t)bh * S + sp) * mp + a0 + 4 * ty) * D + tx * CPT;
 #pragma unroll
