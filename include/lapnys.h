@@ -128,16 +128,23 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout,
  * All float32 unless noted:
  *   L     [B*H][m][d]             landmarks
  *   A     [B*H][m][m]             k(L, L) + eps I
- *   alpha [B*H][4]                alpha, |A|_1, |A|_inf, and the int32 argmax
- *                                 column of |A|_1 stored bitwise in slot 3
+ *   alpha [B*H][4]                alpha, |A|_1, |A|_inf, and in slot 3 the int32
+ *                                 jc | (ir << 16) stored bitwise: jc the argmax
+ *                                 column of |A|_1, ir the argmax row of |A|_inf
  *   X     [B*H][iters+1][m][m]    Newton-Schulz iterates X_0 .. X_T
  *   Y     [B*H][iters][m][m]      products A X_t
  *   W     [B*H][m][d]             C . V
  *   What  [B*H][m][d]             X_T . W
  *   stats [B*H][3][m]             mu, var, 1/sqrt(var + 1e-5) (LAPNYS_NORM only)
- *   idx   int32 [N]               landmark of each token (same for all slices) */
+ *   idx   int32 [N]               landmark of each token (same for all slices)
+ *   P     [B*H][N][mp]            kernel values k(q_j, l_a) before the feature-map
+ *                                 normalisation, rows padded to mp = 64 ceil(m/64)
+ *   C     [B*H][N][mp]            kernel values k(l_a, k_j), token-major (the
+ *                                 transpose of the m x N matrix C)
+ * P and C are what the backward reads instead of recomputing the N x m
+ * kernel values. */
 typedef struct {
-  size_t L, A, alpha, X, Y, W, What, stats, idx, total;
+  size_t L, A, alpha, X, Y, W, What, stats, idx, P, C, total;
 } lapnys_ctx_layout;
 
 int lapnys_ctx_offsets(int B, int H, int N, int d, int m, int iters, unsigned flags,

@@ -27,7 +27,7 @@ EXPORTS = (
 
 class CtxLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
-                ("L", "A", "alpha", "X", "Y", "W", "What", "stats", "idx", "total")]
+                ("L", "A", "alpha", "X", "Y", "W", "What", "stats", "idx", "P", "C", "total")]
 
 
 _lib = None

@@ -159,6 +159,9 @@ def ctx_views(ctx: torch.Tensor, p: Params) -> dict:
     }
     if T > 0:
         views["Y"] = f32("Y", (p.B, p.H, T, m, m))
+    mp = (m + 63) // 64 * 64
+    views["P"] = f32("P", (p.B, p.H, p.N, mp))[..., :m]
+    views["C"] = f32("C", (p.B, p.H, p.N, mp))[..., :m]
     return views
 
 

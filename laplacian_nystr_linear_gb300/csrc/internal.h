@@ -88,15 +88,15 @@ bool ns_cluster_ok(int m);
 cudaError_t run_ns_cluster(const Prob& p, bool reverse, const float* A, float* X, float* Y, int nx,
                            int ny, float* G, float* XG, float* Tm, float* dA, cudaStream_t st);
 
-// forward passes
+// forward passes; kvout (may be null): the pass's kernel values [BH][N][mp]
 cudaError_t run_key_fwd(const Prob& p, const void* k, const void* v, const float* L, float* part,
-                        cudaStream_t st);
+                        float* kvout, cudaStream_t st);
 cudaError_t run_reduce_parts(int BH, int S, int m, int mp, int d, const float* part, float* out,
                              cudaStream_t st);
 cudaError_t run_qstats(const Prob& p, const void* q, const float* L, float* spart, cudaStream_t st);
 cudaError_t run_stats_final(const Prob& p, const float* spart, float* stats, cudaStream_t st);
 cudaError_t run_query_fwd(const Prob& p, const void* q, const float* L, const float* What,
-                          const float* stats, void* out, cudaStream_t st);
+                          const float* stats, void* out, float* kvout, cudaStream_t st);
 
 // backward
 // mode 0: query side statistics pass (LAPNYS_NORM only): dWhat and sum dZ, sum dZ*Z partials
@@ -115,6 +115,7 @@ struct BwdArgs {
   float* lm_part2;    // [BH][S][mp][d]: dWhat (modes 0, 1)
   float* ns_part;     // [BH][S][2][mp]: sum dZ, sum dZ*Z (mode 0)
   const uint8_t* ties;  // [BH][ceil(N / 32)]: block needs the exact sign path (modes 1, 2)
+  const float* kv;      // [BH][N][mp]: kernel values P (mode 1) or C (mode 2) of the forward
 };
 cudaError_t run_bwd_tile(const Prob& p, int mode, const BwdArgs& a, cudaStream_t st);
 // modes 1 and 2 with the FMA-pipe sign term (32-token blocks)

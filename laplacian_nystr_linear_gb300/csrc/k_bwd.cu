@@ -21,7 +21,8 @@
 // Work split per CTA: one 64-landmark tile and a contiguous range of 32-token
 // blocks; the raw token and upstream rows of the next block are copied into
 // shared memory (cp.async) while the current block computes; per block
-//   phase 1  (thread = 4 tokens x 2 landmarks)  distance, dot, kernel value, g
+//   phase 1  (thread = 4 tokens x 2 landmarks)  dot, g from the kernel values
+//            the forward kept ([N][mp] rows, copied in with the token rows)
 //   phase S  (warp = D/8 features, lane = 8 tokens x 8 landmarks) sign term
 //   phase C  contraction: dW-hat_a += sum_j Z_ja dO_j (query side) or
 //            dV_j = sum_a C_ja dW_a (key side)
@@ -68,7 +69,8 @@ struct Smem {
   static constexpr int Gs = Us + TJ * (D + 4);     // [TJ][AS]  2g
   static constexpr int Zs = Gs + TJ * AS;          // [TJ][ZS]  Z (query side) or C (key side)
   static constexpr int dLs = Zs + TJ * (AS + 4);   // [D][TA]   landmark-side accumulator
-  static constexpr int Raw = dLs + D * TA;         // raw rows of the next block: X then U
+  static constexpr int KVs = dLs + D * TA;         // [TJ][AS]  kernel values of the block
+  static constexpr int Raw = KVs + TJ * AS;        // raw rows of the next block: X then U
   static constexpr int Stage = Gs;                 // dX staging [TJ][D+4] over Gs (and Zs)
   template <typename T>
   __host__ __device__ static constexpr int raw_pitch() { return D * (int)sizeof(T) + 16; }  // bytes per raw row
@@ -205,8 +207,9 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
                const float* __restrict__ R, const float* __restrict__ stats,
                const float* __restrict__ mdz, float* __restrict__ tok_part,
                float* __restrict__ tok_part2, float* __restrict__ lm_part,
-               float* __restrict__ lm_part2, const uint8_t* __restrict__ tie_flags, int N,
-               int m, int mp, int S, int nblk, int BH, float ns, float inv_lam) {
+               float* __restrict__ lm_part2, const uint8_t* __restrict__ tie_flags,
+               const float* __restrict__ KV, int N, int m, int mp, int S, int nblk, int BH,
+               float inv_lam) {
   constexpr int CW = D / 8;     // features per warp in phase S
   constexpr int CPT = D / 16;   // features per thread in phase C
   constexpr bool kDWhat = (MODE == 1) && !NORM;
@@ -226,6 +229,7 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
   float* Zs = sm + SM::Zs;
   float* dLs = sm + SM::dLs;
   float* Stage = sm + SM::Stage;
+  float* KVs = sm + SM::KVs;
   uint8_t* raw = reinterpret_cast<uint8_t*>(sm + SM::Raw);
   constexpr int RP = SM::template raw_pitch<T>();
   __shared__ float mu_s[TA], rs_s[TA], m0_s[TA], m1_s[TA];
@@ -258,7 +262,6 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
   const bool cta_exact = __syncthreads_or(bad_l) != 0;
   const float scale = cta_exact ? 1.f : kBig;
   const float inv_scale = cta_exact ? 1.f : kInvBig;
-  const float ns_s = ns * inv_scale;  // exp2 argument per unit of scaled distance
   for (int e = tid; e < TA * D; e += kThreads) {
     const int c = e / TA, a = e % TA;
     LBt[c * AS + pa(a)] = a < nv ? -scale * __ldg(Lb + (size_t)a * D + c) : 0.f;
@@ -282,7 +285,20 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
     }
     cp_commit();
   };
+  // kernel values of block b (this tile's 64 landmarks), zero past N
+  const float* KVb = KV + (size_t)bh * N * mp + a0;
+  auto prefetch_kv = [&](int b) {
+    if (b >= b1) return;
+    const int n0 = b * TJ;
+    for (int id = tid; id < TJ * (TA / 4); id += kThreads) {
+      const int j = id / (TA / 4), ch = id % (TA / 4);
+      const bool ok = n0 + j < N;
+      cp_async16(smem_addr(KVs + j * AS + 4 * ch), KVb + (size_t)(ok ? n0 + j : 0) * mp + 4 * ch, ok);
+    }
+    cp_commit();
+  };
   prefetch(b0);
+  prefetch_kv(b0);
 
   // phase S ownership: warp -> features [warp*CW, +CW); lane (jg, ag) -> tokens
   // 8 jg .. 8 jg + 7 and landmarks 8 ag .. 8 ag + 7
@@ -355,23 +371,27 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
     // ---- phase 1: thread = tokens 4 warp .. +3, landmarks 2 lane and 2 lane + 1 ----
     {
       const int jb = 4 * warp, la = 2 * lane;
-      float dist[4][2], dot[4][2];
+      float kvv[4][2], dot[4][2];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) dist[r][0] = dist[r][1] = dot[r][0] = dot[r][1] = 0.f;
-#pragma unroll 2
-      for (int c = 0; c < D; c += 4) {
-        const float4 r0 = lds4(Rs + la * (D + 4) + c);
-        const float4 r1 = lds4(Rs + (la + 1) * (D + 4) + c);
+      for (int r = 0; r < 4; ++r) {
+        const float2 k2 = *reinterpret_cast<const float2*>(KVs + (jb + r) * AS + la);
+        kvv[r][0] = k2.x;
+        kvv[r][1] = k2.y;
+        dot[r][0] = dot[r][1] = 0.f;
+      }
+      if constexpr (kTC) {
+        // the dot came from the tensor cores
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 x4 = lds4(Xt + (c + q) * JS + jb);
-          const float2 lb = *reinterpret_cast<const float2*>(LBt + (c + q) * AS + pa(la));
-          dist[0][0] += fabsf(fmaf(x4.x, scale, lb.x)); dist[0][1] += fabsf(fmaf(x4.x, scale, lb.y));
-          dist[1][0] += fabsf(fmaf(x4.y, scale, lb.x)); dist[1][1] += fabsf(fmaf(x4.y, scale, lb.y));
-          dist[2][0] += fabsf(fmaf(x4.z, scale, lb.x)); dist[2][1] += fabsf(fmaf(x4.z, scale, lb.y));
-          dist[3][0] += fabsf(fmaf(x4.w, scale, lb.x)); dist[3][1] += fabsf(fmaf(x4.w, scale, lb.y));
+        for (int r = 0; r < 4; ++r) {
+          const float2 dv2 = *reinterpret_cast<const float2*>(Gs + (jb + r) * AS + pa(la));
+          dot[r][0] = dv2.x;
+          dot[r][1] = dv2.y;
         }
-        if constexpr (!kTC) {  // (bf16: the dot came from the tensor cores)
+      } else {
+#pragma unroll 2
+        for (int c = 0; c < D; c += 4) {
+          const float4 r0 = lds4(Rs + la * (D + 4) + c);
+          const float4 r1 = lds4(Rs + (la + 1) * (D + 4) + c);
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
             const float4 u4 = lds4(Us + (jb + r) * (D + 4) + c);
@@ -386,14 +406,6 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
           }
         }
       }
-      if constexpr (kTC) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const float2 dv2 = *reinterpret_cast<const float2*>(Gs + (jb + r) * AS + pa(la));
-          dot[r][0] = dv2.x;
-          dot[r][1] = dv2.y;
-        }
-      }
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
         const int j = jb + r;
@@ -402,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
         for (int h = 0; h < 2; ++h) {
           const int a = la + h;
           const bool valid = (n0 + j < N) && (a < nv);
-          const float kv = exp2f(dist[r][h] * ns_s);
+          const float kv = kvv[r][h];
           float g, zc;
           if (MODE == 2) {
             g = dot[r][h] * kv * inv_lam;
@@ -421,6 +433,7 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
       }
     }
     __syncthreads();
+    prefetch_kv(b + 1);  // this block's kernel values are read
 
     // ---- per-token and per-landmark sums of g (the tile holds 2g) ----
     if (tid < TJ) {
@@ -611,8 +624,8 @@ static cudaError_t bwd_pair_t2(const Prob& p, const BwdArgs& a, cudaStream_t st)
   const int nblk = (p.N + TJ - 1) / TJ;
   return launch(names[MODE], k_bwd_pair<D, T, MODE, NORM>, dim3(p.nt, p.Sb, p.BH), dim3(kThreads),
                 smem, st, (const T*)a.X, (const T*)a.U, a.L, a.R, a.stats, a.mdz, a.tok_part,
-                a.tok_part2, a.lm_part, a.lm_part2, (const uint8_t*)a.ties, p.N, p.m, p.mp, p.Sb,
-                nblk, p.BH, p.ns, p.inv_lam);
+                a.tok_part2, a.lm_part, a.lm_part2, (const uint8_t*)a.ties, a.kv, p.N, p.m, p.mp,
+                p.Sb, nblk, p.BH, p.inv_lam);
 }
 
 template <int D, typename T>

@@ -41,7 +41,8 @@ __device__ __forceinline__ void split_range(int nblk, int S, int s, int& b0, int
 template <int D, typename T>
 __global__ void __launch_bounds__(kThreads, 2)
     k_key_fwd(const T* __restrict__ K, const T* __restrict__ V, const float* __restrict__ L,
-              float* __restrict__ part, int N, int m, int mp, int S, int nblk, float ns) {
+              float* __restrict__ part, float* __restrict__ kvout, int N, int m, int mp, int S,
+              int nblk, float ns) {
   constexpr int CPT = D / 16;
   // bf16 inputs: the contraction runs on the tensor cores (TF32 kernel values)
   constexpr bool kTC = TypeOf<T>::id == 1 && D >= 32;
@@ -86,6 +87,15 @@ __global__ void __launch_bounds__(kThreads, 2)
         Cs[(4 * ty + r) * 68 + tx + 16 * s] = (j < N && a < m) ? exp2f(dist[r][s] * ns) : 0.f;
       }
     __syncthreads();
+    if (kvout) {
+      // keep the tile for the backward: kvout[bh][j][a0 .. a0 + 63], whole rows
+      float* base = kvout + (size_t)bh * N * mp + a0;
+      for (int id = threadIdx.x; id < kTile * (kTile / 4); id += kThreads) {
+        const int r = id / (kTile / 4), c4 = id % (kTile / 4);
+        const int j = b * kTile + r;
+        if (j < N) st4(base + (size_t)j * mp + 4 * c4, lds4(Cs + r * 68 + 4 * c4));
+      }
+    }
     if constexpr (kTC) {
       // W[a][c] += sum_j C[j][a] V[j][c] on the tensor cores (TF32; V is bf16, exact in TF32)
 #pragma unroll 2
@@ -136,12 +146,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 template <int D, typename T>
 static cudaError_t key_fwd_t(const Prob& p, const void* k, const void* v, const float* L, float* part,
-                             cudaStream_t st) {
+                             float* kvout, cudaStream_t st) {
   const size_t smem = (3 * (size_t)tile_floats(D) + 64 * 68) * sizeof(float);
   static bool once = (allow_smem(k_key_fwd<D, T>, smem), true);
   (void)once;
   return launch("key_fwd", k_key_fwd<D, T>, dim3(p.nt, p.Sk, p.BH), dim3(kThreads), smem, st,
-                (const T*)k, (const T*)v, L, part, p.N, p.m, p.mp, p.Sk, p.nblk, p.ns);
+                (const T*)k, (const T*)v, L, part, kvout, p.N, p.m, p.mp, p.Sk, p.nblk, p.ns);
 }
 
 #define DISPATCH_DT(FN, ...)                                                        \
@@ -165,8 +175,8 @@ static cudaError_t key_fwd_t(const Prob& p, const void* k, const void* v, const 
   } while (0)
 
 cudaError_t run_key_fwd(const Prob& p, const void* k, const void* v, const float* L, float* part,
-                        cudaStream_t st) {
-  DISPATCH_DT(key_fwd_t, p, k, v, L, part, st);
+                        float* kvout, cudaStream_t st) {
+  DISPATCH_DT(key_fwd_t, p, k, v, L, part, kvout, st);
 }
 
 // ===========================================================================
@@ -309,7 +319,8 @@ cudaError_t run_stats_final(const Prob& p, const float* spart, float* stats, cud
 template <int D, typename T, bool NORM>
 __global__ void __launch_bounds__(kThreads, 2)
     k_query_fwd(const T* __restrict__ Q, const float* __restrict__ L, const float* __restrict__ What,
-                const float* __restrict__ stats, T* __restrict__ O, int N, int m, int nt, float ns) {
+                const float* __restrict__ stats, T* __restrict__ O, float* __restrict__ kvout,
+                int N, int m, int nt, float ns) {
   constexpr int CPT = D / 16;
   // bf16 inputs: O += Z W-hat runs on the tensor cores (TF32)
   constexpr bool kTC = TypeOf<T>::id == 1 && D >= 32;
@@ -354,10 +365,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int s = 0; s < 4; ++s) {
         const int a = tx + 16 * s;
         float pv = 0.f;
-        if (a0 + a < m) {
-          pv = exp2f(dist[r][s] * ns);
-          if (NORM) pv = (pv - mu_s[a]) * rs_s[a];
-        }
+        if (a0 + a < m) pv = exp2f(dist[r][s] * ns);
+        // keep the kernel value (before normalisation) for the backward
+        const int j = b * kTile + 4 * ty + r;
+        if (kvout && j < N) kvout[((size_t)bh * N + j) * (nt * kTile) + a0 + a] = pv;
+        if (NORM && a0 + a < m) pv = (pv - mu_s[a]) * rs_s[a];
         if (kTC)
           Pt[(4 * ty + r) * 68 + a] = pv;
         else
@@ -421,24 +433,24 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 template <int D, typename T>
 static cudaError_t query_fwd_t(const Prob& p, const void* q, const float* L, const float* What,
-                               const float* stats, void* out, cudaStream_t st) {
+                               const float* stats, void* out, float* kvout, cudaStream_t st) {
   const size_t smem = (3 * (size_t)tile_floats(D) + 64 * 68) * sizeof(float);
   dim3 grid(p.nblk, p.BH);
   if (p.norm()) {
     static bool once = (allow_smem(k_query_fwd<D, T, true>, smem), true);
     (void)once;
     return launch("query_fwd", k_query_fwd<D, T, true>, grid, dim3(kThreads), smem, st,
-                  (const T*)q, L, What, stats, (T*)out, p.N, p.m, p.nt, p.ns);
+                  (const T*)q, L, What, stats, (T*)out, kvout, p.N, p.m, p.nt, p.ns);
   }
   static bool once2 = (allow_smem(k_query_fwd<D, T, false>, smem), true);
   (void)once2;
   return launch("query_fwd", k_query_fwd<D, T, false>, grid, dim3(kThreads), smem, st, (const T*)q,
-                L, What, stats, (T*)out, p.N, p.m, p.nt, p.ns);
+                L, What, stats, (T*)out, kvout, p.N, p.m, p.nt, p.ns);
 }
 
 cudaError_t run_query_fwd(const Prob& p, const void* q, const float* L, const float* What,
-                          const float* stats, void* out, cudaStream_t st) {
-  DISPATCH_DT(query_fwd_t, p, q, L, What, stats, out, st);
+                          const float* stats, void* out, float* kvout, cudaStream_t st) {
+  DISPATCH_DT(query_fwd_t, p, q, L, What, stats, out, kvout, st);
 }
 
 // ===========================================================================

@@ -104,7 +104,7 @@ static Prob make_prob(int B, int H, int N, int d, int gh, int gw, int m, float l
 }
 
 struct CtxLayout {
-  size_t L, A, alpha, X, Y, W, What, stats, idx, total;
+  size_t L, A, alpha, X, Y, W, What, stats, idx, P, C, total;
   int nx, ny;
 };
 
@@ -123,6 +123,10 @@ static CtxLayout ctx_layout(int BH, int N, int d, int m, int iters, bool full) {
   c.What = o; o = align256(o + (size_t)BH * m * d * f);
   c.stats = o; o = align256(o + (size_t)BH * 3 * m * f);
   c.idx = o; o = align256(o + (size_t)N * sizeof(int32_t));
+  // kernel values of both passes, kept for the backward (full layout only)
+  const size_t mp = (size_t)(m + kTile - 1) / kTile * kTile;
+  c.P = o; o = align256(o + (full ? (size_t)BH * N * mp * f : 0));
+  c.C = o; o = align256(o + (full ? (size_t)BH * N * mp * f : 0));
   c.total = o;
   return c;
 }
@@ -310,7 +314,8 @@ int lapnys_ctx_offsets(int B, int H, int N, int d, int m, int iters, unsigned fl
   if (out == nullptr || !dims_ok(B, H, N, d, m, iters)) return LAPNYS_EINVAL;
   const CtxLayout c = ctx_layout(B * H, N, d, m, iters, true);
   out->L = c.L; out->A = c.A; out->alpha = c.alpha; out->X = c.X; out->Y = c.Y;
-  out->W = c.W; out->What = c.What; out->stats = c.stats; out->idx = c.idx; out->total = c.total;
+  out->W = c.W; out->What = c.What; out->stats = c.stats; out->idx = c.idx; out->P = c.P;
+  out->C = c.C; out->total = c.total;
   return LAPNYS_OK;
 }
 
@@ -369,7 +374,7 @@ int lapnys_fwd(const void* q, const void* k, const void* v, void* out, int B, in
     if (rc != LAPNYS_OK) return rc;
   }
   float* kpart = (float*)(wb + w.kpart);
-  CK(run_key_fwd(p, k, v, L, kpart, stream));
+  CK(run_key_fwd(p, k, v, L, kpart, full ? (float*)(cb + c.C) : nullptr, stream));
   CK(run_reduce_parts(p.BH, p.Sk, m, p.mp, d, kpart, W, stream));
   const float* XT = X + (long)(iters % c.nx) * mm;
   // W-hat = X_T W
@@ -380,7 +385,7 @@ int lapnys_fwd(const void* q, const void* k, const void* v, void* out, int B, in
     CK(run_qstats(p, q, L, spart, stream));
     CK(run_stats_final(p, spart, stats, stream));
   }
-  CK(run_query_fwd(p, q, L, What, stats, out, stream));
+  CK(run_query_fwd(p, q, L, What, stats, out, full ? (float*)(cb + c.P) : nullptr, stream));
   return LAPNYS_OK;
 }
 
@@ -428,7 +433,7 @@ int lapnys_fwd_static(const void* q, const void* k, const void* v, void* out, in
     if (rc != LAPNYS_OK) return rc;
   }
   float* kpart = (float*)(wb + w.kpart);
-  CK(run_key_fwd(p, k, v, L, kpart, stream));
+  CK(run_key_fwd(p, k, v, L, kpart, nullptr, stream));
   CK(run_reduce_parts(p.BH, p.Sk, m, p.mp, d, kpart, W, stream));
   const float* XT = X + (long)(iters % c.nx) * mm;
   CK(ns_mm(p, false, false, m, d, m, XT, m, c.nx * mm, W, d, (long)m * d, What, d, (long)m * d,
@@ -438,7 +443,7 @@ int lapnys_fwd_static(const void* q, const void* k, const void* v, void* out, in
     CK(run_qstats(p, q, L, spart, stream));
     CK(run_stats_final(p, spart, stats, stream));
   }
-  CK(run_query_fwd(p, q, L, What, stats, out, stream));
+  CK(run_query_fwd(p, q, L, What, stats, out, nullptr, stream));
   return LAPNYS_OK;
 }
 
@@ -507,6 +512,7 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
   memset(&qa, 0, sizeof(qa));
   qa.X = q; qa.U = dout; qa.L = L; qa.R = What; qa.stats = stats; qa.mdz = mdz;
   qa.tok_part = dQp; qa.lm_part = dLqp; qa.lm_part2 = dWhp; qa.ns_part = nsp; qa.ties = ties_q;
+  qa.kv = (const float*)(cb + c.P);
   if (p.norm()) {
     CK(run_bwd_tile(p, 0, qa, stream));
     CK(run_mdz(p, nsp, mdz, stream));
@@ -565,6 +571,7 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
   memset(&ka, 0, sizeof(ka));
   ka.X = k; ka.U = v; ka.L = L; ka.R = dW;
   ka.tok_part = dKp; ka.tok_part2 = dVp; ka.lm_part = dLcp; ka.ties = ties_k;
+  ka.kv = (const float*)(cb + c.C);
   CK(run_bwd_pair(p, 2, ka, stream));
   CK(run_reduce_dl(p, dLqp, dLcp, dLA, dL, stream));
   CK(run_finalize(p, dQp, dKp, dVp, dL, dq, dk, dv, stream));

@@ -77,6 +77,9 @@ def test_forward_intermediates(wname):
     assert rel(c["W"][0, 0], s["W"]) < 1e-5
     assert rel(c["What"][0, 0], s["What"]) < 1e-4
     np.testing.assert_array_equal(c["idx"], s["idx"])
+    # kernel values kept for the backward: P = k(Q, L) and C = k(L, K), token-major
+    assert rel(c["P"][0, 0], s["P"]) < 1e-6
+    assert rel(c["C"][0, 0], s["C"].T) < 1e-6
 
 
 def test_norm_statistics():
