@@ -157,6 +157,29 @@ __device__ __forceinline__ void mma_16x8x8(float (&d)[4], const uint32_t (&a)[4]
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
+// ---- asynchronous copies global -> shared (cp.async, 16 bytes) ------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// four consecutive elements (group c4) of a raw row of T in shared memory,
+// as fp32 (the last argument only selects the element type)
+__device__ __forceinline__ float4 raw4(const uint8_t* row, int c4, const float*) {
+  return *reinterpret_cast<const float4*>(row + 16 * c4);
+}
+__device__ __forceinline__ float4 raw4(const uint8_t* row, int c4, const __nv_bfloat16*) {
+  const uint2 u = *reinterpret_cast<const uint2*>(row + 8 * c4);
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+}
+
 // sgn(t) * g with sgn(0) = 0
 __device__ __forceinline__ float sgn_times(float t, float g) {
   return t > 0.f ? g : (t < 0.f ? -g : 0.f);

@@ -81,26 +81,6 @@ struct Smem {
   // reads columns of it), key side AS (its dV reads rows)
 };
 
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "r"(valid ? 16 : 0)
-               : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-
-// four consecutive elements (group c4) of a raw row in shared memory
-__device__ __forceinline__ float4 raw4(const uint8_t* row, int c4, const float*) {
-  return *reinterpret_cast<const float4*>(row + 16 * c4);
-}
-__device__ __forceinline__ float4 raw4(const uint8_t* row, int c4, const __nv_bfloat16*) {
-  const uint2 u = *reinterpret_cast<const uint2*>(row + 8 * c4);
-  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
-                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
-}
 }  // namespace
 
 // Landmark slot of landmark a (0..63) in the g and scaled-landmark tiles: 4

@@ -1,5 +1,6 @@
-// Token-side passes of Laplacian-kernel Nystrom attention: the fused
-// L1-distance + exp tiles that never write the N x m kernel matrices to HBM.
+// Token-side passes of Laplacian-kernel Nystrom attention: fused L1-distance
+// + exp tiles.  The N x m kernel matrices are only written out (once, for the
+// backward) when the caller keeps a ctx; the inference forward never stores them.
 //
 //   key pass      W   = C V,     C_aj = k(L_a, K_j)                (forward)
 //   stats pass    mu, var of P_ia = k(Q_i, L_a) per landmark column (forward, norm)
@@ -36,7 +37,8 @@ __device__ __forceinline__ void split_range(int nblk, int S, int s, int& b0, int
 // ===========================================================================
 // key pass: grid (landmark tile, split, slice).  Each CTA keeps its 64
 // landmarks in shared memory, streams its share of the key/value tokens in
-// blocks of 64 and accumulates W[a][c] = sum_j C_aj V_jc in registers.
+// blocks of 64 (the raw rows of the next block are copied in with cp.async
+// while the current one computes) and accumulates W[a][c] = sum_j C_aj V_jc.
 // ===========================================================================
 template <int D, typename T>
 __global__ void __launch_bounds__(kThreads, 2)
@@ -52,6 +54,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   float* Xs = Ls + tile_floats(D);
   float* Vs = Xs + tile_floats(D);
   float* Cs = Vs + tile_floats(D);  // [64 tokens][68]
+  constexpr int RP = D * (int)sizeof(T) + 16;  // bytes per raw row
+  uint8_t* raw = reinterpret_cast<uint8_t*>(Cs + 64 * 68);  // next block: K rows, then V rows
   // tensor-core fragment coordinates: warp -> landmark rows wa .. wa + 15, columns wc .. wc + D/2 - 1
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gq = lane >> 2, tg = lane & 3;
@@ -72,11 +76,31 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int c = 0; c < CPT; ++c) w[s][c] = 0.f;
   int b0, b1;
   split_range(nblk, S, sp, b0, b1);
+  // raw K and V rows of block b into shared memory, zero past N
+  auto prefetch = [&](int b) {
+    if (b >= b1) return;
+    const int n0 = b * kTile;
+    constexpr int CH = D * (int)sizeof(T) / 16;  // 16-byte pieces per row
+    for (int id = threadIdx.x; id < 2 * kTile * CH; id += kThreads) {
+      const int which = id / (kTile * CH), rem = id % (kTile * CH), j = rem / CH, ch = rem % CH;
+      const bool ok = n0 + j < N;
+      const T* src = (which ? Vb : Kb) + (size_t)(ok ? n0 + j : 0) * D;
+      cp_async16(smem_addr(raw + (which * kTile + j) * RP + 16 * ch),
+                 reinterpret_cast<const uint8_t*>(src) + 16 * ch, ok);
+    }
+    cp_commit();
+  };
+  prefetch(b0);
   for (int b = b0; b < b1; ++b) {
+    cp_wait_all();
     __syncthreads();
-    load_tile<D>(Xs, Kb, b * kTile, N);
-    load_tile<D>(Vs, Vb, b * kTile, N);
+    for (int id = threadIdx.x; id < kTile * (D / 4); id += kThreads) {
+      const int r = id / (D / 4), c4 = id % (D / 4);
+      st4(Xs + r * row_stride(D) + 4 * c4, raw4(raw + r * RP, c4, Kb));
+      st4(Vs + r * row_stride(D) + 4 * c4, raw4(raw + (kTile + r) * RP, c4, Vb));
+    }
     __syncthreads();
+    prefetch(b + 1);
     float dist[4][4];
     dist_tile<D>(Xs, Ls, dist);
 #pragma unroll
@@ -147,7 +171,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 template <int D, typename T>
 static cudaError_t key_fwd_t(const Prob& p, const void* k, const void* v, const float* L, float* part,
                              float* kvout, cudaStream_t st) {
-  const size_t smem = (3 * (size_t)tile_floats(D) + 64 * 68) * sizeof(float);
+  const size_t smem = (3 * (size_t)tile_floats(D) + 64 * 68) * sizeof(float) +
+                      2 * (size_t)kTile * (D * sizeof(T) + 16);
   static bool once = (allow_smem(k_key_fwd<D, T>, smem), true);
   (void)once;
   return launch("key_fwd", k_key_fwd<D, T>, dim3(p.nt, p.Sk, p.BH), dim3(kThreads), smem, st,
@@ -313,8 +338,9 @@ cudaError_t run_stats_final(const Prob& p, const float* spart, float* stats, cud
 
 // ===========================================================================
 // query pass: grid (token block, slice).  Each CTA keeps 64 queries in shared
-// memory and walks the landmark tiles: P tile on the fly (never stored to
-// HBM), optional centring/whitening, then O += Z_tile W-hat_tile.
+// memory and walks the landmark tiles (the next landmark and W-hat tiles are
+// copied in with cp.async, double buffered): P tile on the fly, optional
+// centring/whitening, then O += Z_tile W-hat_tile.
 // ===========================================================================
 template <int D, typename T, bool NORM>
 __global__ void __launch_bounds__(kThreads, 2)
@@ -327,9 +353,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   constexpr int NCT = D / 16;
   extern __shared__ float4 sm4[];
   float* Xs = reinterpret_cast<float*>(sm4);
-  float* Ls = Xs + tile_floats(D);
-  float* Ws = Ls + tile_floats(D);
-  float* Pt = Ws + tile_floats(D);  // [64 landmarks][68 tokens] (tensor-core path: [64 tokens][68 landmarks])
+  float* LW = Xs + tile_floats(D);          // two buffers of (landmark tile, W-hat tile)
+  float* Pt = LW + 4 * tile_floats(D);      // [64 landmarks][68 tokens] (tensor-core path: [64 tokens][68 landmarks])
   __shared__ float mu_s[kTile], rs_s[kTile];
   const int b = blockIdx.x, bh = blockIdx.y;
   const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
@@ -346,11 +371,30 @@ __global__ void __launch_bounds__(kThreads, 2)
   float acc[NCT][4];
 #pragma unroll
   for (int n = 0; n < NCT; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+  // landmark and W-hat rows of tile lt into buffer lt % 2 (fp32 rows land in
+  // the padded tiles directly), zero past m
+  auto prefetch = [&](int lt) {
+    if (lt >= nt) return;
+    float* Lsb = LW + (lt & 1) * 2 * tile_floats(D);
+    float* Wsb = Lsb + tile_floats(D);
+    const int a0 = lt * kTile;
+    for (int id = threadIdx.x; id < 2 * kTile * (D / 4); id += kThreads) {
+      const int which = id / (kTile * (D / 4)), rem = id % (kTile * (D / 4));
+      const int r = rem / (D / 4), c4 = rem % (D / 4);
+      const bool ok = a0 + r < m;
+      const float* src = (which ? What : L) + ((size_t)bh * m + (ok ? a0 + r : 0)) * D + 4 * c4;
+      cp_async16(smem_addr((which ? Wsb : Lsb) + r * row_stride(D) + 4 * c4), src, ok);
+    }
+    cp_commit();
+  };
+  prefetch(0);
   for (int lt = 0; lt < nt; ++lt) {
     const int a0 = lt * kTile;
-    __syncthreads();
-    load_tile<D>(Ls, L + (size_t)bh * m * D, a0, m);
-    load_tile<D>(Ws, What + (size_t)bh * m * D, a0, m);
+    const float* Ls = LW + (lt & 1) * 2 * tile_floats(D);
+    const float* Ws = Ls + tile_floats(D);
+    cp_wait_all();
+    __syncthreads();  // tile lt has landed; every reader of the other buffer is done
+    prefetch(lt + 1);
     if (NORM && threadIdx.x < kTile) {
       const int a = a0 + threadIdx.x;
       mu_s[threadIdx.x] = a < m ? stats[(size_t)bh * 3 * m + a] : 0.f;
@@ -434,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 template <int D, typename T>
 static cudaError_t query_fwd_t(const Prob& p, const void* q, const float* L, const float* What,
                                const float* stats, void* out, float* kvout, cudaStream_t st) {
-  const size_t smem = (3 * (size_t)tile_floats(D) + 64 * 68) * sizeof(float);
+  const size_t smem = (5 * (size_t)tile_floats(D) + 64 * 68) * sizeof(float);
   dim3 grid(p.nblk, p.BH);
   if (p.norm()) {
     static bool once = (allow_smem(k_query_fwd<D, T, true>, smem), true);
