@@ -19,23 +19,28 @@
 // products; operands are read through L2 (ld.global.cg), never a stale L1
 // line.  Twelve warps with fixed roles (three per SM sub-partition, so that
 // each may hold up to 168 registers):
-//   warps 0-7  load each K-stage (16) of both operands from global memory into
-//           registers two stages ahead, split them into hi / lo and store
-//           them into a 3-stage shared-memory ring in the K-major core-matrix
+//   warps 0-7  copy each K-stage (16) of both operands from global memory into
+//           a 4-stage raw ring in shared memory (cp.async through L2, each
+//           thread copying exactly the pieces it later splits, so that its own
+//           wait_group is all the ordering needed), split them into hi / lo
+//           and store those into a 2-stage ring in the K-major core-matrix
 //           layout (8 rows x 16 bytes per core matrix; 8-row groups 144 bytes
 //           apart and K groups 32 bytes further apart than dense, which keeps
 //           the split stores free of bank conflicts).  An operand whose rows
 //           hold K contiguously is read four lanes per row (8 rows per warp
 //           load); one stored [k][row] is read in 4-row blocks along the row
 //           and transposed in registers.
-//   warps 8-11  read the accumulator back with tcgen05.ld (warp w reads TMEM
-//           lanes 32 (w % 4) ..), transpose 32 x 32 pieces through a small
-//           per-warp buffer and write C = alpha acc + beta E in whole lines;
-//           E is fetched two pieces ahead.  Warp 8 allocates TMEM, and its
-//           first lane issues each stage's six MMAs (2 k-steps x 3 split
-//           products), commits them to the stage's "free" mbarrier and, after
-//           a product's last stage, to the accumulator barrier, before taking
-//           its part of the epilogue.
+//   warp 8  allocates TMEM; its first lane issues each stage's six MMAs (2
+//           k-steps x 3 split products), commits them to the stage's "free"
+//           mbarrier and, after a product's last stage, to the accumulator
+//           barrier.
+//   all twelve warps then read the accumulator back with tcgen05.ld (warp w
+//           reads TMEM lanes 32 (w % 4) .., three warps per lane quarter, each
+//           taking every third 32-column piece), transpose 32 x 32 pieces
+//           through a small per-warp buffer (in split stage 0, idle between a
+//           product's last MMA and the next cluster barrier) and write
+//           C = alpha acc + beta E in whole lines; E is fetched two pieces
+//           ahead.
 //
 // Every mbarrier wait is bounded: on expiry the CTA records an error in the
 // device word read by lapnys_device_status and stops working, but still takes
@@ -52,7 +57,8 @@ namespace {
 constexpr int TM = 128;    // rows per CTA (MMA M)
 constexpr int TNMAX = 256; // largest MMA N
 constexpr int TK = 16;     // K per stage
-constexpr int NSPL = 3;    // shared-memory stages
+constexpr int NSPL = 2;    // split (hi / lo) stages
+constexpr int NRAW = 4;    // raw stages (copies in flight per splitter thread)
 constexpr int NSPW = 8;    // splitter warps
 constexpr int NSPT = NSPW * 32;
 constexpr int NEPW = 4;    // epilogue warps
@@ -64,9 +70,12 @@ constexpr uint32_t kLboB = (TNMAX / 8) * kSbo + 32;  // same, B tile
 constexpr uint32_t kTileA = (TK / 4) * kLboA;        // A hi (or lo) per stage
 constexpr uint32_t kTileB = (TK / 4) * kLboB;
 constexpr uint32_t kStage = 2 * kTileA + 2 * kTileB;
+constexpr uint32_t kRawA = TM * TK * 4;              // raw A pieces per stage (bytes)
+constexpr uint32_t kRawStage = kRawA + TNMAX * TK * 4;  // raw A then raw B
 constexpr uint32_t kEpiPitch = 36 * 4;               // staged row: 32 floats + 16-byte pad
 constexpr uint32_t kEpiWarp = 32 * kEpiPitch;
-constexpr size_t kSmem = (size_t)NSPL * kStage + (size_t)NEPW * kEpiWarp + 128;
+static_assert(NTH / 32 * kEpiWarp <= kStage, "epilogue staging fits in one split stage");
+constexpr size_t kSmem = (size_t)NSPL * kStage + (size_t)NRAW * kRawStage + 128;
 constexpr int kWaitLimit = 1 << 22;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -196,42 +205,52 @@ __device__ __forceinline__ Prod prod_of(const NsArgs& a, int s, int bh) {
   return p;
 }
 
-// One splitter thread's share of one stage (16 k) of both operands.
-// op(A): 128 rows i0 .. i0 + 127; op(B)^T: up to 256 rows (result columns).
-struct StageRegs {
-  float4 a[4], b[4];
-};
-
-__device__ __forceinline__ void load_stage(StageRegs& r, const Prod& p, int m, int i0, int k0,
-                                           int ts) {
-  // A operand
+// One splitter thread's share of one stage (16 k) of both operands, as 16-byte
+// pieces.  op(A): 128 rows i0 .. i0 + 127; op(B)^T: up to 256 rows (result
+// columns).  An operand whose rows hold K contiguously: unit u = (row u / 4,
+// k4 = u % 4), one piece, units ts and ts + 256 (A) or ts + 256 h (B).  One
+// stored [k][row]: unit (4-row block rb, k4), four pieces (k = 4 k4 + j) taken
+// along the rows and transposed at the split; A units only for ts < 128.
+// Piece i of thread ts sits at raw + 16 (i * NSPT + ts) (A: i < 4, B after
+// the A part), so a warp's copies and reads touch consecutive 16-byte words.
+__device__ __forceinline__ void issue_stage(uint8_t* raw, const Prod& p, int m, int i0, int k0,
+                                            int ts) {
+  uint8_t* ra = raw;
+  uint8_t* rb = raw + kRawA;
   if (p.ka) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int u = ts + h * NSPT, row = i0 + (u >> 2), kk = k0 + 4 * (u & 3);
-      r.a[h] = row < m && kk < m ? ldcg4(p.A + (size_t)row * m + kk) : make_float4(0, 0, 0, 0);
+      const bool ok = row < m && kk < m;
+      cp_async16(smem_addr(ra + 16 * (h * NSPT + ts)), p.A + (ok ? (size_t)row * m + kk : 0), ok);
     }
   } else if (ts < TM) {
     const int row = i0 + 4 * (ts % (TM / 4)), kk = k0 + 4 * (ts / (TM / 4));
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      r.a[j] = row < m && kk + j < m ? ldcg4(p.A + (size_t)(kk + j) * m + row)
-                                     : make_float4(0, 0, 0, 0);
+    for (int j = 0; j < 4; ++j) {
+      const bool ok = row < m && kk + j < m;
+      cp_async16(smem_addr(ra + 16 * (j * TM + ts)), p.A + (ok ? (size_t)(kk + j) * m + row : 0), ok);
+    }
   }
-  // B operand
   if (p.kb) {
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
       const int u = ts + h * NSPT, row = u >> 2, kk = k0 + 4 * (u & 3);
-      r.b[h] = row < m && kk < m ? ldcg4(p.B + (size_t)row * m + kk) : make_float4(0, 0, 0, 0);
+      const bool ok = row < m && kk < m;
+      cp_async16(smem_addr(rb + 16 * (h * NSPT + ts)), p.B + (ok ? (size_t)row * m + kk : 0), ok);
     }
   } else {
     const int row = 4 * (ts % (TNMAX / 4)), kk = k0 + 4 * (ts / (TNMAX / 4));
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      r.b[j] = row < m && kk + j < m ? ldcg4(p.B + (size_t)(kk + j) * m + row)
-                                     : make_float4(0, 0, 0, 0);
+    for (int j = 0; j < 4; ++j) {
+      const bool ok = row < m && kk + j < m;
+      cp_async16(smem_addr(rb + 16 * (j * NSPT + ts)), p.B + (ok ? (size_t)(kk + j) * m + row : 0), ok);
+    }
   }
+}
+
+__device__ __forceinline__ float4 raw_piece(const uint8_t* base, int i, int stride, int ts) {
+  return *reinterpret_cast<const float4*>(base + 16 * (i * stride + ts));
 }
 
 __device__ __forceinline__ void store_transposed(uint8_t* hi, uint8_t* lo, uint32_t lbo, int rb,
@@ -242,7 +261,9 @@ __device__ __forceinline__ void store_transposed(uint8_t* hi, uint8_t* lo, uint3
   store_split(hi, lo, kmaj_off(4 * rb + 3, k4, lbo), make_float4(x[0].w, x[1].w, x[2].w, x[3].w));
 }
 
-__device__ __forceinline__ void store_stage(const StageRegs& r, const Prod& p, uint8_t* sp, int ts) {
+__device__ __forceinline__ void split_stage(const uint8_t* raw, const Prod& p, uint8_t* sp, int ts) {
+  const uint8_t* ra = raw;
+  const uint8_t* rb = raw + kRawA;
   uint8_t* ahi = sp;
   uint8_t* alo = sp + kTileA;
   uint8_t* bhi = sp + 2 * kTileA;
@@ -251,19 +272,23 @@ __device__ __forceinline__ void store_stage(const StageRegs& r, const Prod& p, u
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int u = ts + h * NSPT;
-      store_split(ahi, alo, kmaj_off(u >> 2, u & 3, kLboA), r.a[h]);
+      store_split(ahi, alo, kmaj_off(u >> 2, u & 3, kLboA), raw_piece(ra, h, NSPT, ts));
     }
   } else if (ts < TM) {
-    store_transposed(ahi, alo, kLboA, ts % (TM / 4), ts / (TM / 4), r.a);
+    const float4 x[4] = {raw_piece(ra, 0, TM, ts), raw_piece(ra, 1, TM, ts), raw_piece(ra, 2, TM, ts),
+                         raw_piece(ra, 3, TM, ts)};
+    store_transposed(ahi, alo, kLboA, ts % (TM / 4), ts / (TM / 4), x);
   }
   if (p.kb) {
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
       const int u = ts + h * NSPT;
-      store_split(bhi, blo, kmaj_off(u >> 2, u & 3, kLboB), r.b[h]);
+      store_split(bhi, blo, kmaj_off(u >> 2, u & 3, kLboB), raw_piece(rb, h, NSPT, ts));
     }
   } else {
-    store_transposed(bhi, blo, kLboB, ts % (TNMAX / 4), ts / (TNMAX / 4), r.b);
+    const float4 x[4] = {raw_piece(rb, 0, NSPT, ts), raw_piece(rb, 1, NSPT, ts),
+                         raw_piece(rb, 2, NSPT, ts), raw_piece(rb, 3, NSPT, ts)};
+    store_transposed(bhi, blo, kLboB, ts % (TNMAX / 4), ts / (TNMAX / 4), x);
   }
 }
 }  // namespace
@@ -279,7 +304,8 @@ __global__ void __launch_bounds__(NTH, 1) k_ns_cluster(NsArgs a) {
   const int np = (m + 15) & ~15;  // MMA N
   uint8_t* tsm = tsm_raw + ((128u - (smem_u32(tsm_raw) & 127u)) & 127u);
   uint8_t* stage_base = tsm;
-  uint8_t* epi_base = tsm + NSPL * kStage;
+  uint8_t* raw_base = tsm + NSPL * kStage;
+  uint8_t* epi_base = stage_base;  // split stage 0 (see the header)
   const int nchunks = (m + TK - 1) / TK;
   const int nprod = a.reverse ? 4 * a.iters : 2 * a.iters;
 
@@ -316,31 +342,33 @@ __global__ void __launch_bounds__(NTH, 1) k_ns_cluster(NsArgs a) {
       // ---- splitters ----
       const int ts = tid;
       if (!abort_s) {
-        StageRegs r0, r1;
-        load_stage(r0, p, m, i0, 0, ts);
-        if (nchunks > 1) load_stage(r1, p, m, i0, TK, ts);
-        auto step = [&](int c, StageRegs& r) -> bool {
+        cp_wait_all();  // nothing of an earlier product is still in flight
+#pragma unroll
+        for (int c = 0; c < NRAW; ++c) {
+          if (c < nchunks) issue_stage(raw_base + c * kRawStage, p, m, i0, c * TK, ts);
+          cp_commit();
+        }
+        for (int c = 0; c < nchunks; ++c) {
           const int qq = q + c, u = qq % NSPL;
-          if (abort_s) return false;
+          if (abort_s) break;
           if (qq >= NSPL && !mbar_wait(smem_u32(&spl_free[u]), (uint32_t)((qq / NSPL - 1) & 1))) {
             fail();
-            return false;
+            break;
           }
-          store_stage(r, p, stage_base + u * kStage, ts);
+          asm volatile("cp.async.wait_group %0;" ::"n"(NRAW - 1) : "memory");  // stage c landed
+          uint8_t* raw = raw_base + (c % NRAW) * kRawStage;
+          split_stage(raw, p, stage_base + u * kStage, ts);
           // make the generic-proxy stores visible to the tensor core's async proxy
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           mbar_arrive(smem_u32(&spl_full[u]));
-          if (c + 2 < nchunks) load_stage(r, p, m, i0, (c + 2) * TK, ts);
-          return true;
-        };
-        for (int c = 0; c < nchunks; c += 2) {
-          if (!step(c, r0)) break;
-          if (c + 1 < nchunks && !step(c + 1, r1)) break;
+          // this thread's pieces of stage c are read: refill the slot
+          if (c + NRAW < nchunks) issue_stage(raw, p, m, i0, (c + NRAW) * TK, ts);
+          cp_commit();
         }
       }
-    } else {
-      if (warp == kMmaWarp) {
-        // ---- MMA issuer (first lane), then the epilogue with the others ----
+    } else if (warp == kMmaWarp) {
+      // ---- MMA issuer (first lane) ----
+      {
         if (lane == 0 && !abort_s) {
           const uint32_t id = idesc(np);
           for (int c = 0; c < nchunks; ++c) {
@@ -369,9 +397,12 @@ __global__ void __launch_bounds__(NTH, 1) k_ns_cluster(NsArgs a) {
         }
         __syncwarp();
       }
-      // ---- epilogue ----
-      const int quarter = warp & 3;
-      uint8_t* stg = epi_base + (warp - NSPW) * kEpiWarp;
+    }
+    {
+      // ---- epilogue, all twelve warps: three per TMEM lane quarter, each
+      // taking every third 32-column piece ----
+      const int quarter = warp & 3, slot = warp >> 2;
+      uint8_t* stg = epi_base + warp * kEpiWarp;
       const int c4 = lane & 7;
       const int r0 = i0 + 32 * quarter;
       auto load_e = [&](float4 (&e)[8], int cb) {
@@ -382,9 +413,10 @@ __global__ void __launch_bounds__(NTH, 1) k_ns_cluster(NsArgs a) {
           e[it] = row < m && col < m ? ldcg4(p.E + (size_t)row * m + col) : make_float4(0, 0, 0, 0);
         }
       };
+      const int npc = (np + 31) / 32;  // 32-column pieces
       float4 e0[8], e1[8];
-      load_e(e0, 0);
-      load_e(e1, 32);
+      load_e(e0, 32 * slot);
+      load_e(e1, 32 * (slot + 3));
       const bool ok = !abort_s && mbar_wait(smem_u32(&acc_full), (uint32_t)(s & 1));
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       // tcgen05.ld is warp-collective: the whole warp takes the same decision
@@ -427,11 +459,11 @@ __global__ void __launch_bounds__(NTH, 1) k_ns_cluster(NsArgs a) {
           __syncwarp();
         };
 #pragma unroll 1
-        for (int cb = 0; cb < np; cb += 64) {
-          piece(cb, e0);
-          load_e(e0, cb + 64);
-          if (cb + 32 < np) piece(cb + 32, e1);
-          load_e(e1, cb + 96);
+        for (int pi = slot; pi < npc; pi += 6) {
+          piece(32 * pi, e0);
+          load_e(e0, 32 * (pi + 6));
+          if (pi + 3 < npc) piece(32 * (pi + 3), e1);
+          load_e(e1, 32 * (pi + 9));
         }
       } else if (!ok) {
         fail();
