@@ -19,25 +19,32 @@
 // products; operands are read through L2 (ld.global.cg), never a stale L1
 // line.  Twelve warps with fixed roles (three per SM sub-partition, so that
 // each may hold up to 168 registers):
-//   warps 0-7  copy each K-stage (16) of both operands from global memory into
-//           a 4-stage raw ring in shared memory (cp.async through L2, each
-//           thread copying exactly the pieces it later splits, so that its own
-//           wait_group is all the ordering needed), split them into hi / lo
-//           and store those into a 2-stage ring in the K-major core-matrix
-//           layout (8 rows x 16 bytes per core matrix; 8-row groups 144 bytes
-//           apart and K groups 32 bytes further apart than dense, which keeps
-//           the split stores free of bank conflicts).  An operand whose rows
-//           hold K contiguously is read four lanes per row (8 rows per warp
-//           load); one stored [k][row] is read in 4-row blocks along the row
-//           and transposed in registers.
-//   warp 8  allocates TMEM; its first lane issues each stage's six MMAs (2
-//           k-steps x 3 split products), commits them to the stage's "free"
+//   warps 0-7  per K-stage (16): load their rows of op(A) straight into
+//           registers three stages ahead (lane = row, warp w covers TMEM lane
+//           quarter w % 4 and k-step w / 4), split them into TF32 hi / lo and
+//           write them into TMEM (tcgen05.st), where the MMA reads op(A); copy
+//           op(B) into a 4-stage raw ring in shared memory (cp.async through
+//           L2, each thread copying exactly the pieces it later splits, so its
+//           own wait_group is all the ordering needed), split it and store hi /
+//           lo into a 3-stage ring in the K-major core-matrix layout (8 rows x
+//           16 bytes per core matrix; 8-row groups 144 bytes apart and K groups
+//           32 bytes further apart than dense, which keeps the split stores free
+//           of bank conflicts).  An op(B) whose rows hold K contiguously is read
+//           four lanes per row (8 rows per warp copy); one stored [k][row] in
+//           4-row blocks along the row, transposed at the split.  Keeping op(A)
+//           out of shared memory removes its split stores and the tensor core's
+//           reads of it, a third of the shared-memory traffic that bounds the
+//           K loop.
+//   warp 8  allocates TMEM (accumulator: columns 0-255; op(A) stages: 32
+//           columns each from 256); its first lane issues each stage's six MMAs
+//           (2 k-steps x 3 split products, A from TMEM, B from shared memory),
+//           commits them to the stage's "free"
 //           mbarrier and, after a product's last stage, to the accumulator
 //           barrier.
 //   all twelve warps then read the accumulator back with tcgen05.ld (warp w
 //           reads TMEM lanes 32 (w % 4) .., three warps per lane quarter, each
 //           taking every third 32-column piece), transpose 32 x 32 pieces
-//           through a small per-warp buffer (in split stage 0, idle between a
+//           through a small per-warp buffer (in split stages 0-1, idle between a
 //           product's last MMA and the next cluster barrier) and write
 //           C = alpha acc + beta E in whole lines; E is fetched two pieces
 //           ahead.
@@ -57,7 +64,7 @@ namespace {
 constexpr int TM = 128;    // rows per CTA (MMA M)
 constexpr int TNMAX = 256; // largest MMA N
 constexpr int TK = 16;     // K per stage
-constexpr int NSPL = 2;    // split (hi / lo) stages
+constexpr int NSPL = 3;    // split (hi / lo) stages
 constexpr int NRAW = 4;    // raw stages (copies in flight per splitter thread)
 constexpr int NSPW = 8;    // splitter warps
 constexpr int NSPT = NSPW * 32;
@@ -65,16 +72,16 @@ constexpr int NEPW = 4;    // epilogue warps
 constexpr int NTH = NSPT + NEPW * 32;  // 384
 constexpr int kMmaWarp = NSPW;         // first epilogue warp
 constexpr uint32_t kSbo = 144;                       // bytes between 8-row groups
-constexpr uint32_t kLboA = (TM / 8) * kSbo + 32;     // bytes between 4-wide K groups, A tile
 constexpr uint32_t kLboB = (TNMAX / 8) * kSbo + 32;  // same, B tile
-constexpr uint32_t kTileA = (TK / 4) * kLboA;        // A hi (or lo) per stage
 constexpr uint32_t kTileB = (TK / 4) * kLboB;
-constexpr uint32_t kStage = 2 * kTileA + 2 * kTileB;
-constexpr uint32_t kRawA = TM * TK * 4;              // raw A pieces per stage (bytes)
-constexpr uint32_t kRawStage = kRawA + TNMAX * TK * 4;  // raw A then raw B
+constexpr uint32_t kStage = 2 * kTileB;              // B hi, B lo
+constexpr uint32_t kAcol = TNMAX;                     // first TMEM column of the op(A) stages
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kRawStage = TNMAX * TK * 4;       // raw B pieces per stage (bytes)
 constexpr uint32_t kEpiPitch = 36 * 4;               // staged row: 32 floats + 16-byte pad
 constexpr uint32_t kEpiWarp = 32 * kEpiPitch;
-static_assert(NTH / 32 * kEpiWarp <= kStage, "epilogue staging fits in one split stage");
+static_assert(NTH / 32 * kEpiWarp <= 2 * kStage, "epilogue staging fits in two split stages");
+static_assert(kAcol + NSPL * 32 <= kTmemCols, "op(A) stages fit in TMEM");
 constexpr size_t kSmem = (size_t)NSPL * kStage + (size_t)NRAW * kRawStage + 128;
 constexpr int kWaitLimit = 1 << 22;
 
@@ -101,13 +108,20 @@ __device__ __forceinline__ uint32_t kmaj_off(int row, int k4, uint32_t lbo) {
   return (uint32_t)k4 * lbo + (uint32_t)(row >> 3) * kSbo + (uint32_t)(row & 7) * 16u;
 }
 
+// x rounded to the nearest TF32 value (10 mantissa bits, halfway cases away
+// from zero) by integer arithmetic on the bits: add half a TF32 ulp to the
+// magnitude and clear the 13 low bits (a carry into the exponent is the
+// correct rounding).  Finite inputs only, which the iteration's are.
+__device__ __forceinline__ float tf32_hi(float x) {
+  return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
+}
+
 __device__ __forceinline__ void store_split(uint8_t* hi, uint8_t* lo, uint32_t off, float4 x) {
   float4 h, l;
-  uint32_t t;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(t) : "f"(x.x)); h.x = __uint_as_float(t); l.x = x.x - h.x;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(t) : "f"(x.y)); h.y = __uint_as_float(t); l.y = x.y - h.y;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(t) : "f"(x.z)); h.z = __uint_as_float(t); l.z = x.z - h.z;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(t) : "f"(x.w)); h.w = __uint_as_float(t); l.w = x.w - h.w;
+  h.x = tf32_hi(x.x); l.x = x.x - h.x;
+  h.y = tf32_hi(x.y); l.y = x.y - h.y;
+  h.z = tf32_hi(x.z); l.z = x.z - h.z;
+  h.w = tf32_hi(x.w); l.w = x.w - h.w;
   *reinterpret_cast<float4*>(hi + off) = h;
   *reinterpret_cast<float4*>(lo + off) = l;
 }
@@ -131,12 +145,20 @@ __device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity) {
   }
   return false;
 }
-__device__ __forceinline__ void mma_tf32(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
-                                         uint32_t id, uint32_t accumulate) {
+// D (TMEM) += A (TMEM, lane = row) * B (shared-memory descriptor)
+__device__ __forceinline__ void mma_tf32_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc,
+                                            uint32_t id, uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
-      "l"(adesc), "l"(bdesc), "r"(id), "r"(accumulate)
+      " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(id), "r"(accumulate)
+      : "memory");
+}
+// this lane's 8 consecutive TMEM columns at taddr (warp-collective)
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
       : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint32_t mbar) {
@@ -205,33 +227,46 @@ __device__ __forceinline__ Prod prod_of(const NsArgs& a, int s, int bh) {
   return p;
 }
 
-// One splitter thread's share of one stage (16 k) of both operands, as 16-byte
-// pieces.  op(A): 128 rows i0 .. i0 + 127; op(B)^T: up to 256 rows (result
-// columns).  An operand whose rows hold K contiguously: unit u = (row u / 4,
-// k4 = u % 4), one piece, units ts and ts + 256 (A) or ts + 256 h (B).  One
-// stored [k][row]: unit (4-row block rb, k4), four pieces (k = 4 k4 + j) taken
-// along the rows and transposed at the split; A units only for ts < 128.
-// Piece i of thread ts sits at raw + 16 (i * NSPT + ts) (A: i < 4, B after
-// the A part), so a warp's copies and reads touch consecutive 16-byte words.
-__device__ __forceinline__ void issue_stage(uint8_t* raw, const Prod& p, int m, int i0, int k0,
-                                            int ts) {
-  uint8_t* ra = raw;
-  uint8_t* rb = raw + kRawA;
+// op(A) for one splitter lane: row `row`, the 8 k values kb .. kb + 7 (zero
+// outside the matrix), through L2.
+struct ARegs {
+  float v[8];
+};
+__device__ __forceinline__ void load_a(ARegs& r, const Prod& p, int m, int row, int kb) {
   if (p.ka) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int u = ts + h * NSPT, row = i0 + (u >> 2), kk = k0 + 4 * (u & 3);
-      const bool ok = row < m && kk < m;
-      cp_async16(smem_addr(ra + 16 * (h * NSPT + ts)), p.A + (ok ? (size_t)row * m + kk : 0), ok);
+    for (int j = 0; j < 2; ++j) {
+      const float4 x = row < m && kb + 4 * j < m ? ldcg4(p.A + (size_t)row * m + kb + 4 * j)
+                                                 : make_float4(0, 0, 0, 0);
+      r.v[4 * j] = x.x; r.v[4 * j + 1] = x.y; r.v[4 * j + 2] = x.z; r.v[4 * j + 3] = x.w;
     }
-  } else if (ts < TM) {
-    const int row = i0 + 4 * (ts % (TM / 4)), kk = k0 + 4 * (ts / (TM / 4));
+  } else {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const bool ok = row < m && kk + j < m;
-      cp_async16(smem_addr(ra + 16 * (j * TM + ts)), p.A + (ok ? (size_t)(kk + j) * m + row : 0), ok);
-    }
+    for (int j = 0; j < 8; ++j)
+      r.v[j] = row < m && kb + j < m ? __ldcg(p.A + (size_t)(kb + j) * m + row) : 0.f;
   }
+}
+// split into TF32 hi / lo and write them to TMEM columns colh .. + 7 and
+// coll .. + 7 of this warp's lane quarter (warp-collective)
+__device__ __forceinline__ void store_a(const ARegs& r, uint32_t colh, uint32_t coll) {
+  uint32_t hi[8], lo[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float h = tf32_hi(r.v[j]);
+    hi[j] = __float_as_uint(h);
+    lo[j] = __float_as_uint(r.v[j] - h);
+  }
+  tmem_st8(colh, hi);
+  tmem_st8(coll, lo);
+}
+
+// One splitter thread's share of one stage (16 k) of op(B)^T (up to 256 rows:
+// the result columns), as 16-byte pieces.  Rows holding K contiguously: unit
+// u = (row u / 4, k4 = u % 4), units ts + 256 h.  Stored [k][row]: unit
+// (4-row block, k4), four pieces (k = 4 k4 + j) taken along the rows and
+// transposed at the split.  Piece i of thread ts sits at raw + 16 (i * NSPT +
+// ts), so a warp's copies and reads touch consecutive 16-byte words.
+__device__ __forceinline__ void issue_stage(uint8_t* rb, const Prod& p, int m, int k0, int ts) {
   if (p.kb) {
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
@@ -249,8 +284,8 @@ __device__ __forceinline__ void issue_stage(uint8_t* raw, const Prod& p, int m, 
   }
 }
 
-__device__ __forceinline__ float4 raw_piece(const uint8_t* base, int i, int stride, int ts) {
-  return *reinterpret_cast<const float4*>(base + 16 * (i * stride + ts));
+__device__ __forceinline__ float4 raw_piece(const uint8_t* base, int i, int ts) {
+  return *reinterpret_cast<const float4*>(base + 16 * (i * NSPT + ts));
 }
 
 __device__ __forceinline__ void store_transposed(uint8_t* hi, uint8_t* lo, uint32_t lbo, int rb,
@@ -261,33 +296,18 @@ __device__ __forceinline__ void store_transposed(uint8_t* hi, uint8_t* lo, uint3
   store_split(hi, lo, kmaj_off(4 * rb + 3, k4, lbo), make_float4(x[0].w, x[1].w, x[2].w, x[3].w));
 }
 
-__device__ __forceinline__ void split_stage(const uint8_t* raw, const Prod& p, uint8_t* sp, int ts) {
-  const uint8_t* ra = raw;
-  const uint8_t* rb = raw + kRawA;
-  uint8_t* ahi = sp;
-  uint8_t* alo = sp + kTileA;
-  uint8_t* bhi = sp + 2 * kTileA;
-  uint8_t* blo = sp + 2 * kTileA + kTileB;
-  if (p.ka) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int u = ts + h * NSPT;
-      store_split(ahi, alo, kmaj_off(u >> 2, u & 3, kLboA), raw_piece(ra, h, NSPT, ts));
-    }
-  } else if (ts < TM) {
-    const float4 x[4] = {raw_piece(ra, 0, TM, ts), raw_piece(ra, 1, TM, ts), raw_piece(ra, 2, TM, ts),
-                         raw_piece(ra, 3, TM, ts)};
-    store_transposed(ahi, alo, kLboA, ts % (TM / 4), ts / (TM / 4), x);
-  }
+__device__ __forceinline__ void split_stage(const uint8_t* rb, const Prod& p, uint8_t* sp, int ts) {
+  uint8_t* bhi = sp;
+  uint8_t* blo = sp + kTileB;
   if (p.kb) {
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
       const int u = ts + h * NSPT;
-      store_split(bhi, blo, kmaj_off(u >> 2, u & 3, kLboB), raw_piece(rb, h, NSPT, ts));
+      store_split(bhi, blo, kmaj_off(u >> 2, u & 3, kLboB), raw_piece(rb, h, ts));
     }
   } else {
-    const float4 x[4] = {raw_piece(rb, 0, NSPT, ts), raw_piece(rb, 1, NSPT, ts),
-                         raw_piece(rb, 2, NSPT, ts), raw_piece(rb, 3, NSPT, ts)};
+    const float4 x[4] = {raw_piece(rb, 0, ts), raw_piece(rb, 1, ts), raw_piece(rb, 2, ts),
+                         raw_piece(rb, 3, ts)};
     store_transposed(bhi, blo, kLboB, ts % (TNMAX / 4), ts / (TNMAX / 4), x);
   }
 }
@@ -312,13 +332,13 @@ __global__ void __launch_bounds__(NTH, 1) k_ns_cluster(NsArgs a) {
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&tmem_base_s)),
-                 "r"(TNMAX)
+                 "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (tid == 0) {
     for (int s = 0; s < NSPL; ++s) {
-      mbar_init(smem_u32(&spl_full[s]), NSPT);
+      mbar_init(smem_u32(&spl_full[s]), NSPW);  // one arrival per splitter warp
       mbar_init(smem_u32(&spl_free[s]), 1);
     }
     mbar_init(smem_u32(&acc_full), 1);
@@ -341,29 +361,56 @@ __global__ void __launch_bounds__(NTH, 1) k_ns_cluster(NsArgs a) {
     if (warp < NSPW) {
       // ---- splitters ----
       const int ts = tid;
-      if (!abort_s) {
+      constexpr unsigned kFull = 0xffffffffu;
+      // op(A): lane = row 32 (warp % 4) + lane of the CTA's panel, k-step warp / 4
+      const int aq = warp & 3, ah = warp >> 2;
+      const int arow = i0 + 32 * aq + lane;
+      const uint32_t alane = (uint32_t)(32 * aq) << 16;
+      if (!__any_sync(kFull, abort_s)) {
         cp_wait_all();  // nothing of an earlier product is still in flight
 #pragma unroll
         for (int c = 0; c < NRAW; ++c) {
-          if (c < nchunks) issue_stage(raw_base + c * kRawStage, p, m, i0, c * TK, ts);
+          if (c < nchunks) issue_stage(raw_base + c * kRawStage, p, m, c * TK, ts);
           cp_commit();
         }
-        for (int c = 0; c < nchunks; ++c) {
+        ARegs ra0, ra1, ra2;
+        load_a(ra0, p, m, arow, 0 * TK + 8 * ah);
+        if (nchunks > 1) load_a(ra1, p, m, arow, 1 * TK + 8 * ah);
+        if (nchunks > 2) load_a(ra2, p, m, arow, 2 * TK + 8 * ah);
+        auto step = [&](int c, ARegs& ra) -> bool {
           const int qq = q + c, u = qq % NSPL;
-          if (abort_s) break;
-          if (qq >= NSPL && !mbar_wait(smem_u32(&spl_free[u]), (uint32_t)((qq / NSPL - 1) & 1))) {
+          if (__any_sync(kFull, abort_s)) return false;
+          const bool free_ok =
+              qq < NSPL || mbar_wait(smem_u32(&spl_free[u]), (uint32_t)((qq / NSPL - 1) & 1));
+          if (!__all_sync(kFull, free_ok)) {
             fail();
-            break;
+            return false;
           }
-          asm volatile("cp.async.wait_group %0;" ::"n"(NRAW - 1) : "memory");  // stage c landed
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          // op(A) of stage c into TMEM (this warp's lanes and k-step)
+          const uint32_t col = tmem + alane + kAcol + 32u * u + 8u * ah;
+          store_a(ra, col, col + 16u);
+          if (c + 3 < nchunks) load_a(ra, p, m, arow, (c + 3) * TK + 8 * ah);
+          // op(B) of stage c: raw copy landed -> hi / lo tiles
+          asm volatile("cp.async.wait_group %0;" ::"n"(NRAW - 1) : "memory");
           uint8_t* raw = raw_base + (c % NRAW) * kRawStage;
           split_stage(raw, p, stage_base + u * kStage, ts);
-          // make the generic-proxy stores visible to the tensor core's async proxy
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          // generic-proxy stores visible to the tensor core's async proxy;
+          // TMEM stores ordered before the MMA warp's thread sync
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          mbar_arrive(smem_u32(&spl_full[u]));
+          asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&spl_full[u]));
           // this thread's pieces of stage c are read: refill the slot
-          if (c + NRAW < nchunks) issue_stage(raw, p, m, i0, (c + NRAW) * TK, ts);
+          if (c + NRAW < nchunks) issue_stage(raw, p, m, (c + NRAW) * TK, ts);
           cp_commit();
+          return true;
+        };
+        for (int c = 0; c < nchunks; c += 3) {
+          if (!step(c, ra0)) break;
+          if (c + 1 < nchunks && !step(c + 1, ra1)) break;
+          if (c + 2 < nchunks && !step(c + 2, ra2)) break;
         }
       }
     } else if (warp == kMmaWarp) {
@@ -379,17 +426,15 @@ __global__ void __launch_bounds__(NTH, 1) k_ns_cluster(NsArgs a) {
             }
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const uint32_t sp = smem_u32(stage_base + u * kStage);
-            const uint32_t a_hi = sp, a_lo = sp + kTileA, b_hi = sp + 2 * kTileA,
-                           b_lo = sp + 2 * kTileA + kTileB;
+            const uint32_t b_hi = sp, b_lo = sp + kTileB;
+            const uint32_t a_hi = tmem + kAcol + 32u * u, a_lo = a_hi + 16u;
 #pragma unroll
             for (int k = 0; k < TK / 8; ++k) {
-              const uint64_t dah = make_desc(a_hi + 2 * k * kLboA, kLboA);
-              const uint64_t dal = make_desc(a_lo + 2 * k * kLboA, kLboA);
               const uint64_t dbh = make_desc(b_hi + 2 * k * kLboB, kLboB);
               const uint64_t dbl = make_desc(b_lo + 2 * k * kLboB, kLboB);
-              mma_tf32(tmem, dah, dbh, id, (c > 0 || k > 0) ? 1u : 0u);
-              mma_tf32(tmem, dah, dbl, id, 1u);
-              mma_tf32(tmem, dal, dbh, id, 1u);
+              mma_tf32_ta(tmem, a_hi + 8u * k, dbh, id, (c > 0 || k > 0) ? 1u : 0u);
+              mma_tf32_ta(tmem, a_hi + 8u * k, dbl, id, 1u);
+              mma_tf32_ta(tmem, a_lo + 8u * k, dbh, id, 1u);
             }
             mma_commit(smem_u32(&spl_free[u]));
           }
@@ -485,7 +530,7 @@ __global__ void __launch_bounds__(NTH, 1) k_ns_cluster(NsArgs a) {
   __syncthreads();
   __syncwarp();
   if (warp == kMmaWarp)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TNMAX)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                  : "memory");
 }
 
