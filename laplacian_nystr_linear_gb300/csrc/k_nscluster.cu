@@ -16,42 +16,42 @@
 // [128 r, 128 r + 128) of every product, all m (rounded up to 16) columns in
 // one M = 128, N <= 256 MMA accumulator.  Products depend on each other's full
 // results, so a cluster barrier (release / acquire) separates consecutive
-// products; operands are read through L2 (ld.global.cg), never a stale L1
-// line.  Twelve warps with fixed roles (three per SM sub-partition, so that
-// each may hold up to 168 registers):
-//   warps 0-7  per K-stage (16): load their rows of op(A) straight into
-//           registers three stages ahead (lane = row, warp w covers TMEM lane
-//           quarter w % 4 and k-step w / 4), split them into TF32 hi / lo and
-//           write them into TMEM (tcgen05.st), where the MMA reads op(A); copy
-//           op(B) into a 4-stage raw ring in shared memory (cp.async through
-//           L2, each thread copying exactly the pieces it later splits, so its
-//           own wait_group is all the ordering needed), split it and store hi /
-//           lo into a 3-stage ring in the K-major core-matrix layout (8 rows x
-//           16 bytes per core matrix; 8-row groups 144 bytes apart and K groups
-//           32 bytes further apart than dense, which keeps the split stores free
-//           of bank conflicts).  An op(B) whose rows hold K contiguously is read
-//           four lanes per row (8 rows per warp copy); one stored [k][row] in
-//           4-row blocks along the row, transposed at the split.  Keeping op(A)
-//           out of shared memory removes its split stores and the tensor core's
-//           reads of it, a third of the shared-memory traffic that bounds the
-//           K loop.
+// products.  Twelve warps (three per SM sub-partition, so each may hold up to
+// 168 registers):
+//   warp 9, one lane  copies each K-stage (16) of both operands into a 4-stage
+//           raw ring in shared memory with TMA (cp.async.bulk.tensor).  An
+//           operand whose rows hold K contiguously goes through a 4-D tensor
+//           map {4 k, rows, k / 4, matrix} whose box lands in K-major 16-byte
+//           pieces; one stored [k][row] through a 3-D map {row, k, matrix}.
+//   warps 0-7  per stage: split op(A) (lane = row 32 (w % 4) + lane, k-step
+//           w / 4) into TF32 hi / lo and write them into TMEM (tcgen05.st),
+//           where the MMA reads op(A); split op(B) and store hi / lo into a
+//           3-stage ring in the K-major core-matrix layout (8 rows x 16 bytes
+//           per core matrix; 8-row groups 144 bytes apart and K groups 32 bytes
+//           further apart than dense, which keeps the split stores free of bank
+//           conflicts).  Their share of the work is shared-memory reads, the
+//           split and the stores: no address arithmetic or copy issue for
+//           global memory.
 //   warp 8  allocates TMEM (accumulator: columns 0-255; op(A) stages: 32
 //           columns each from 256); its first lane issues each stage's six MMAs
 //           (2 k-steps x 3 split products, A from TMEM, B from shared memory),
-//           commits them to the stage's "free"
-//           mbarrier and, after a product's last stage, to the accumulator
-//           barrier.
+//           commits them to the stage's "free" mbarrier and, after a product's
+//           last stage, to the accumulator barrier.
 //   all twelve warps then read the accumulator back with tcgen05.ld (warp w
 //           reads TMEM lanes 32 (w % 4) .., three warps per lane quarter, each
 //           taking every third 32-column piece), transpose 32 x 32 pieces
-//           through a small per-warp buffer (in split stages 0-1, idle between a
-//           product's last MMA and the next cluster barrier) and write
+//           through a small per-warp buffer (in split stages 0-1, idle between
+//           a product's last MMA and the next cluster barrier) and write
 //           C = alpha acc + beta E in whole lines; E is fetched two pieces
-//           ahead.
+//           ahead.  The stores are made visible to the next product's TMA reads
+//           (async proxy) before the cluster barrier.
 //
 // Every mbarrier wait is bounded: on expiry the CTA records an error in the
 // device word read by lapnys_device_status and stops working, but still takes
-// part in every cluster barrier, so that the other CTA of its cluster finishes.
+// part in every cluster barrier, so that the other CTA of its cluster finishes;
+// copies it issued are waited for (bounded) before it exits.
+#include <cuda.h>
+
 #include <mutex>
 #include <type_traits>
 
@@ -64,20 +64,23 @@ namespace {
 constexpr int TM = 128;    // rows per CTA (MMA M)
 constexpr int TNMAX = 256; // largest MMA N
 constexpr int TK = 16;     // K per stage
-constexpr int NSPL = 3;    // split (hi / lo) stages
-constexpr int NRAW = 4;    // raw stages (copies in flight per splitter thread)
+constexpr int NSPL = 3;    // split (hi / lo) stages of op(B)
+constexpr int NRAW = 4;    // raw (TMA) stages of both operands
 constexpr int NSPW = 8;    // splitter warps
 constexpr int NSPT = NSPW * 32;
-constexpr int NEPW = 4;    // epilogue warps
+constexpr int NEPW = 4;    // epilogue-only warps (8-11)
 constexpr int NTH = NSPT + NEPW * 32;  // 384
-constexpr int kMmaWarp = NSPW;         // first epilogue warp
+constexpr int kMmaWarp = NSPW;         // warp 8
+constexpr int kTmaWarp = NSPW + 1;     // warp 9
 constexpr uint32_t kSbo = 144;                       // bytes between 8-row groups
-constexpr uint32_t kLboB = (TNMAX / 8) * kSbo + 32;  // same, B tile
-constexpr uint32_t kTileB = (TK / 4) * kLboB;
+constexpr uint32_t kLboB = (TNMAX / 8) * kSbo + 32;  // bytes between 4-wide K groups, B tile
+constexpr uint32_t kTileB = (TK / 4) * kLboB;        // B hi (or lo) per stage
 constexpr uint32_t kStage = 2 * kTileB;              // B hi, B lo
-constexpr uint32_t kAcol = TNMAX;                     // first TMEM column of the op(A) stages
+constexpr uint32_t kAcol = TNMAX;                    // first TMEM column of the op(A) stages
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kRawStage = TNMAX * TK * 4;       // raw B pieces per stage (bytes)
+constexpr uint32_t kRawA = TM * TK * 4;              // raw op(A) box (bytes)
+constexpr uint32_t kRawB = TNMAX * TK * 4;           // raw op(B) box
+constexpr uint32_t kRawStage = kRawA + kRawB;
 constexpr uint32_t kEpiPitch = 36 * 4;               // staged row: 32 floats + 16-byte pad
 constexpr uint32_t kEpiWarp = 32 * kEpiPitch;
 static_assert(NTH / 32 * kEpiWarp <= 2 * kStage, "epilogue staging fits in two split stages");
@@ -132,6 +135,10 @@ __device__ __forceinline__ void mbar_init(uint32_t addr, uint32_t count) {
 __device__ __forceinline__ void mbar_arrive(uint32_t addr) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(addr) : "memory");
 }
+__device__ __forceinline__ void mbar_expect_tx(uint32_t addr, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(addr), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity) {
   for (int i = 0; i < kWaitLimit; ++i) {
     uint32_t ok;
@@ -144,6 +151,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity) {
     if (ok) return true;
   }
   return false;
+}
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, int c3, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(mbar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint32_t mbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(mbar)
+      : "memory");
 }
 // D (TMEM) += A (TMEM, lane = row) * B (shared-memory descriptor)
 __device__ __forceinline__ void mma_tf32_ta(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc,
@@ -172,20 +195,22 @@ __device__ __forceinline__ void cluster_sync() {
 __device__ __forceinline__ float4 ldcg4(const float* p) {
   return __ldcg(reinterpret_cast<const float4*>(p));
 }
-
-// one product of the program, slice-local m x m row-major matrices
-struct Prod {
-  const float* A;  // op(A) = A (ka) or A^T
-  const float* B;  // op(B) = B^T (kb) or B
-  float* C;
-  const float* E;  // null when beta == 0
-  bool ka, kb;     // the operand's rows hold K contiguously
-  float alpha, beta;
-};
 }  // namespace
 
+// Tensor maps of every operand use in the programs (encoded on the host per
+// launch).  A-role maps have 128-row boxes, B-role maps 256-row boxes; "kc":
+// rows hold K contiguously (4-D map), "mn": stored [k][row] (3-D map).  The
+// last dimension enumerates the m x m matrices of the buffer.
+struct NsMaps {
+  CUtensorMap a_kc, a_mn;          // landmark matrix A [BH]: A X (fwd), A^T XG (rev)
+  CUtensorMap x_akc, x_amn;        // iterates X [BH * nx]: X Y (fwd), X^T G (rev)
+  CUtensorMap x_bmn, x_bkc;        //   as B: A X (fwd), XG X^T (rev)
+  CUtensorMap y_bmn, y_bkc;        // products Y [BH * ny]: X Y (fwd), G Y^T (rev)
+  CUtensorMap g_akc, g_bmn;        // G [BH]: G Y^T, X^T G (rev)
+  CUtensorMap xg_akc, xg_bmn;      // XG [BH]: XG X^T, A^T XG (rev)
+};
+
 struct NsArgs {
-  const float* A;  // [BH][m][m]
   float* X;        // [BH][nx][m][m]: iterate t in slot t % nx
   float* Y;        // [BH][ny][m][m]: A X_t in slot t % ny
   float* G;        // reverse only: [BH][m][m]
@@ -197,18 +222,32 @@ struct NsArgs {
 };
 
 namespace {
-__device__ __forceinline__ Prod prod_of(const NsArgs& a, int s, int bh) {
+// one product of the program: C = alpha op(A) op(B) + beta E (slice-local)
+struct Prod {
+  const CUtensorMap* ma;  // op(A) rows: map and matrix index
+  int za;
+  bool ka;                // rows of op(A) hold K contiguously (4-D map)
+  const CUtensorMap* mb;  // op(B)^T rows (result columns)
+  int zb;
+  bool kb;
+  float* C;
+  const float* E;         // null when beta == 0
+  float alpha, beta;
+};
+
+__device__ __forceinline__ Prod prod_of(const NsMaps& mp, const NsArgs& a, int s, int bh) {
   const long mm = (long)a.m * a.m;
-  const float* Ab = a.A + bh * mm;
-  auto Xs = [&](int t) { return a.X + ((long)bh * a.nx + t % a.nx) * mm; };
-  auto Ys = [&](int t) { return a.Y + ((long)bh * a.ny + t % a.ny) * mm; };
+  const int xs0 = bh * a.nx, ys0 = bh * a.ny;
+  auto Xi = [&](int t) { return xs0 + t % a.nx; };
+  auto Yi = [&](int t) { return ys0 + t % a.ny; };
   Prod p;
   if (!a.reverse) {
     const int t = s >> 1;
     if ((s & 1) == 0) {  // Y_t = A X_t
-      p = Prod{Ab, Xs(t), Ys(t), nullptr, true, false, 1.f, 0.f};
+      p = Prod{&mp.a_kc, bh, true, &mp.x_bmn, Xi(t), false, a.Y + Yi(t) * mm, nullptr, 1.f, 0.f};
     } else {             // X_{t+1} = -X_t Y_t + 2 X_t
-      p = Prod{Xs(t), Ys(t), Xs(t + 1), Xs(t), true, false, -1.f, 2.f};
+      p = Prod{&mp.x_akc, Xi(t), true, &mp.y_bmn, Yi(t), false, a.X + Xi(t + 1) * mm,
+               a.X + Xi(t) * mm, -1.f, 2.f};
     }
   } else {
     const int t = a.iters - 1 - (s >> 2);
@@ -216,76 +255,64 @@ __device__ __forceinline__ Prod prod_of(const NsArgs& a, int s, int bh) {
     float* XG = a.XG + bh * mm;
     float* Tm = a.Tm + bh * mm;
     float* dA = a.dA + bh * mm;
+    const bool first = t == a.iters - 1;
     switch (s & 3) {
-      case 0: p = Prod{Xs(t), G, XG, nullptr, false, false, 1.f, 0.f}; break;       // X_t^T G
-      case 1: p = Prod{XG, Xs(t), dA, t == a.iters - 1 ? nullptr : dA, true, true, -1.f,
-                       t == a.iters - 1 ? 0.f : 1.f}; break;                         // -XG X_t^T + dA
-      case 2: p = Prod{G, Ys(t), Tm, G, true, true, -1.f, 2.f}; break;               // -G Y_t^T + 2G
-      default: p = Prod{Ab, XG, G, Tm, false, false, -1.f, 1.f}; break;              // -A^T XG + Tm
+      case 0:  // XG = X_t^T G
+        p = Prod{&mp.x_amn, Xi(t), false, &mp.g_bmn, bh, false, XG, nullptr, 1.f, 0.f};
+        break;
+      case 1:  // dA = -XG X_t^T + dA
+        p = Prod{&mp.xg_akc, bh, true, &mp.x_bkc, Xi(t), true, dA, first ? nullptr : dA, -1.f,
+                 first ? 0.f : 1.f};
+        break;
+      case 2:  // Tm = -G Y_t^T + 2 G
+        p = Prod{&mp.g_akc, bh, true, &mp.y_bkc, Yi(t), true, Tm, G, -1.f, 2.f};
+        break;
+      default:  // G = -A^T XG + Tm
+        p = Prod{&mp.a_mn, bh, false, &mp.xg_bmn, bh, false, G, Tm, -1.f, 1.f};
+        break;
     }
   }
   return p;
 }
 
-// op(A) for one splitter lane: row `row`, the 8 k values kb .. kb + 7 (zero
-// outside the matrix), through L2.
-struct ARegs {
+// issue the TMA copies of stage c (K = 16 c .. 16 c + 15) into one raw slot
+__device__ __forceinline__ void issue_stage(uint8_t* raw, const Prod& p, int i0, int c,
+                                            uint32_t bar) {
+  mbar_expect_tx(bar, kRawStage);
+  if (p.ka) tma_load_4d(smem_u32(raw), p.ma, 0, i0, c * (TK / 4), p.za, bar);
+  else tma_load_3d(smem_u32(raw), p.ma, i0, c * TK, p.za, bar);
+  if (p.kb) tma_load_4d(smem_u32(raw + kRawA), p.mb, 0, 0, c * (TK / 4), p.zb, bar);
+  else tma_load_3d(smem_u32(raw + kRawA), p.mb, 0, c * TK, p.zb, bar);
+}
+
+// op(A) of one stage for splitter lane `row` (0..127 of the panel), k-step ah
+// (k = 8 ah .. 8 ah + 7): split and written to TMEM columns colh, coll (+0..7)
+// of this warp's lane quarter (warp-collective).  Raw layout: 4-D box (kc):
+// piece (row, k4) at 16 (128 k4 + row); 3-D box (mn): value (k, row) at
+// 4 (128 k + row).
+__device__ __forceinline__ void split_a(const uint8_t* ra, bool kc, int row, int ah, uint32_t colh,
+                                        uint32_t coll) {
   float v[8];
-};
-__device__ __forceinline__ void load_a(ARegs& r, const Prod& p, int m, int row, int kb) {
-  if (p.ka) {
+  if (kc) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      const float4 x = row < m && kb + 4 * j < m ? ldcg4(p.A + (size_t)row * m + kb + 4 * j)
-                                                 : make_float4(0, 0, 0, 0);
-      r.v[4 * j] = x.x; r.v[4 * j + 1] = x.y; r.v[4 * j + 2] = x.z; r.v[4 * j + 3] = x.w;
+      const float4 x = *reinterpret_cast<const float4*>(ra + 16 * (TM * (2 * ah + j) + row));
+      v[4 * j] = x.x; v[4 * j + 1] = x.y; v[4 * j + 2] = x.z; v[4 * j + 3] = x.w;
     }
   } else {
+    const float* r = reinterpret_cast<const float*>(ra);
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      r.v[j] = row < m && kb + j < m ? __ldcg(p.A + (size_t)(kb + j) * m + row) : 0.f;
+    for (int j = 0; j < 8; ++j) v[j] = r[TM * (8 * ah + j) + row];
   }
-}
-// split into TF32 hi / lo and write them to TMEM columns colh .. + 7 and
-// coll .. + 7 of this warp's lane quarter (warp-collective)
-__device__ __forceinline__ void store_a(const ARegs& r, uint32_t colh, uint32_t coll) {
   uint32_t hi[8], lo[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const float h = tf32_hi(r.v[j]);
+    const float h = tf32_hi(v[j]);
     hi[j] = __float_as_uint(h);
-    lo[j] = __float_as_uint(r.v[j] - h);
+    lo[j] = __float_as_uint(v[j] - h);
   }
   tmem_st8(colh, hi);
   tmem_st8(coll, lo);
-}
-
-// One splitter thread's share of one stage (16 k) of op(B)^T (up to 256 rows:
-// the result columns), as 16-byte pieces.  Rows holding K contiguously: unit
-// u = (row u / 4, k4 = u % 4), units ts + 256 h.  Stored [k][row]: unit
-// (4-row block, k4), four pieces (k = 4 k4 + j) taken along the rows and
-// transposed at the split.  Piece i of thread ts sits at raw + 16 (i * NSPT +
-// ts), so a warp's copies and reads touch consecutive 16-byte words.
-__device__ __forceinline__ void issue_stage(uint8_t* rb, const Prod& p, int m, int k0, int ts) {
-  if (p.kb) {
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      const int u = ts + h * NSPT, row = u >> 2, kk = k0 + 4 * (u & 3);
-      const bool ok = row < m && kk < m;
-      cp_async16(smem_addr(rb + 16 * (h * NSPT + ts)), p.B + (ok ? (size_t)row * m + kk : 0), ok);
-    }
-  } else {
-    const int row = 4 * (ts % (TNMAX / 4)), kk = k0 + 4 * (ts / (TNMAX / 4));
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const bool ok = row < m && kk + j < m;
-      cp_async16(smem_addr(rb + 16 * (j * NSPT + ts)), p.B + (ok ? (size_t)(kk + j) * m + row : 0), ok);
-    }
-  }
-}
-
-__device__ __forceinline__ float4 raw_piece(const uint8_t* base, int i, int ts) {
-  return *reinterpret_cast<const float4*>(base + 16 * (i * NSPT + ts));
 }
 
 __device__ __forceinline__ void store_transposed(uint8_t* hi, uint8_t* lo, uint32_t lbo, int rb,
@@ -296,26 +323,37 @@ __device__ __forceinline__ void store_transposed(uint8_t* hi, uint8_t* lo, uint3
   store_split(hi, lo, kmaj_off(4 * rb + 3, k4, lbo), make_float4(x[0].w, x[1].w, x[2].w, x[3].w));
 }
 
-__device__ __forceinline__ void split_stage(const uint8_t* rb, const Prod& p, uint8_t* sp, int ts) {
+// op(B)^T of one stage (256 rows x 16 k), thread ts of the 256 splitters.
+// Raw 4-D box (kc): piece (row, k4) at 16 (256 k4 + row); thread ts takes row
+// ts, pieces k4 = 0..3.  Raw 3-D box (mn): [16 k][256 rows]; thread ts takes
+// the 4-row block rb = ts % 64 at k4 = ts / 64 (four pieces along the rows,
+// transposed).  Consecutive lanes read consecutive 16-byte words.
+__device__ __forceinline__ void split_b(const uint8_t* rbase, bool kc, uint8_t* sp, int ts) {
   uint8_t* bhi = sp;
   uint8_t* blo = sp + kTileB;
-  if (p.kb) {
+  if (kc) {
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      const int u = ts + h * NSPT;
-      store_split(bhi, blo, kmaj_off(u >> 2, u & 3, kLboB), raw_piece(rb, h, ts));
+    for (int k4 = 0; k4 < 4; ++k4) {
+      const float4 x = *reinterpret_cast<const float4*>(rbase + 16 * (TNMAX * k4 + ts));
+      store_split(bhi, blo, kmaj_off(ts, k4, kLboB), x);
     }
   } else {
-    const float4 x[4] = {raw_piece(rb, 0, ts), raw_piece(rb, 1, ts), raw_piece(rb, 2, ts),
-                         raw_piece(rb, 3, ts)};
-    store_transposed(bhi, blo, kLboB, ts % (TNMAX / 4), ts / (TNMAX / 4), x);
+    const int rb = ts % (TNMAX / 4), k4 = ts / (TNMAX / 4);
+    const float* r = reinterpret_cast<const float*>(rbase);
+    float4 x[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      x[j] = *reinterpret_cast<const float4*>(r + TNMAX * (4 * k4 + j) + 4 * rb);
+    store_transposed(bhi, blo, kLboB, rb, k4, x);
   }
 }
 }  // namespace
 
-__global__ void __launch_bounds__(NTH, 1) k_ns_cluster(NsArgs a) {
+__global__ void __launch_bounds__(NTH, 1)
+    k_ns_cluster(const __grid_constant__ NsMaps maps, NsArgs a) {
   extern __shared__ uint8_t tsm_raw[];
-  __shared__ __align__(8) uint64_t spl_full[NSPL], spl_free[NSPL], acc_full, mma_done;
+  __shared__ __align__(8) uint64_t spl_full[NSPL], spl_free[NSPL], raw_full[NRAW], raw_free[NRAW],
+      acc_full, mma_done;
   __shared__ uint32_t tmem_base_s;
   __shared__ volatile int abort_s;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -325,9 +363,10 @@ __global__ void __launch_bounds__(NTH, 1) k_ns_cluster(NsArgs a) {
   uint8_t* tsm = tsm_raw + ((128u - (smem_u32(tsm_raw) & 127u)) & 127u);
   uint8_t* stage_base = tsm;
   uint8_t* raw_base = tsm + NSPL * kStage;
-  uint8_t* epi_base = stage_base;  // split stage 0 (see the header)
+  uint8_t* epi_base = stage_base;  // split stages 0-1 (see the header)
   const int nchunks = (m + TK - 1) / TK;
   const int nprod = a.reverse ? 4 * a.iters : 2 * a.iters;
+  constexpr unsigned kFull = 0xffffffffu;
 
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -341,10 +380,19 @@ __global__ void __launch_bounds__(NTH, 1) k_ns_cluster(NsArgs a) {
       mbar_init(smem_u32(&spl_full[s]), NSPW);  // one arrival per splitter warp
       mbar_init(smem_u32(&spl_free[s]), 1);
     }
+    for (int s = 0; s < NRAW; ++s) {
+      mbar_init(smem_u32(&raw_full[s]), 1);
+      mbar_init(smem_u32(&raw_free[s]), NSPW);
+    }
     mbar_init(smem_u32(&acc_full), 1);
     mbar_init(smem_u32(&mma_done), 1);
     abort_s = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (tid == 32 * kTmaWarp) {
+    const CUtensorMap* all = &maps.a_kc;
+    for (int i = 0; i < (int)(sizeof(NsMaps) / sizeof(CUtensorMap)); ++i)
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(all + i)) : "memory");
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
@@ -355,93 +403,83 @@ __global__ void __launch_bounds__(NTH, 1) k_ns_cluster(NsArgs a) {
     abort_s = 1;
   };
 
-  int q = 0;  // stages of all earlier products (the same count in every role)
+  int q = 0;       // stages of all earlier products (the same count in every role)
+  int issued = 0;  // TMA stages issued (producer lane)
   for (int s = 0; s < nprod; ++s, q += nchunks) {
-    const Prod p = prod_of(a, s, bh);
+    const Prod p = prod_of(maps, a, s, bh);
     if (warp < NSPW) {
       // ---- splitters ----
       const int ts = tid;
-      constexpr unsigned kFull = 0xffffffffu;
-      // op(A): lane = row 32 (warp % 4) + lane of the CTA's panel, k-step warp / 4
-      const int aq = warp & 3, ah = warp >> 2;
-      const int arow = i0 + 32 * aq + lane;
+      const int aq = warp & 3, ah = warp >> 2;  // TMEM lane quarter, op(A) k-step
       const uint32_t alane = (uint32_t)(32 * aq) << 16;
-      if (!__any_sync(kFull, abort_s)) {
-        cp_wait_all();  // nothing of an earlier product is still in flight
-#pragma unroll
-        for (int c = 0; c < NRAW; ++c) {
-          if (c < nchunks) issue_stage(raw_base + c * kRawStage, p, m, c * TK, ts);
-          cp_commit();
+      for (int c = 0; c < nchunks; ++c) {
+        const int qq = q + c, u = qq % NSPL, r = qq % NRAW;
+        if (__any_sync(kFull, abort_s)) break;
+        const bool ok =
+            (qq < NSPL || mbar_wait(smem_u32(&spl_free[u]), (uint32_t)((qq / NSPL - 1) & 1))) &&
+            mbar_wait(smem_u32(&raw_full[r]), (uint32_t)((qq / NRAW) & 1));
+        if (!__all_sync(kFull, ok)) {
+          fail();
+          break;
         }
-        ARegs ra0, ra1, ra2;
-        load_a(ra0, p, m, arow, 0 * TK + 8 * ah);
-        if (nchunks > 1) load_a(ra1, p, m, arow, 1 * TK + 8 * ah);
-        if (nchunks > 2) load_a(ra2, p, m, arow, 2 * TK + 8 * ah);
-        auto step = [&](int c, ARegs& ra) -> bool {
-          const int qq = q + c, u = qq % NSPL;
-          if (__any_sync(kFull, abort_s)) return false;
-          const bool free_ok =
-              qq < NSPL || mbar_wait(smem_u32(&spl_free[u]), (uint32_t)((qq / NSPL - 1) & 1));
-          if (!__all_sync(kFull, free_ok)) {
-            fail();
-            return false;
-          }
-          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-          // op(A) of stage c into TMEM (this warp's lanes and k-step)
-          const uint32_t col = tmem + alane + kAcol + 32u * u + 8u * ah;
-          store_a(ra, col, col + 16u);
-          if (c + 3 < nchunks) load_a(ra, p, m, arow, (c + 3) * TK + 8 * ah);
-          // op(B) of stage c: raw copy landed -> hi / lo tiles
-          asm volatile("cp.async.wait_group %0;" ::"n"(NRAW - 1) : "memory");
-          uint8_t* raw = raw_base + (c % NRAW) * kRawStage;
-          split_stage(raw, p, stage_base + u * kStage, ts);
-          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-          // generic-proxy stores visible to the tensor core's async proxy;
-          // TMEM stores ordered before the MMA warp's thread sync
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&spl_full[u]));
-          // this thread's pieces of stage c are read: refill the slot
-          if (c + NRAW < nchunks) issue_stage(raw, p, m, (c + NRAW) * TK, ts);
-          cp_commit();
-          return true;
-        };
-        for (int c = 0; c < nchunks; c += 3) {
-          if (!step(c, ra0)) break;
-          if (c + 1 < nchunks && !step(c + 1, ra1)) break;
-          if (c + 2 < nchunks && !step(c + 2, ra2)) break;
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const uint8_t* raw = raw_base + r * kRawStage;
+        const uint32_t col = tmem + alane + kAcol + 32u * u + 8u * ah;
+        split_a(raw, p.ka, 32 * aq + lane, ah, col, col + 16u);
+        split_b(raw + kRawA, p.kb, stage_base + u * kStage, ts);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        // generic-proxy stores visible to the tensor core's async proxy; TMEM
+        // stores ordered before the MMA warp's thread sync
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&raw_free[r]));  // this warp has read the raw slot
+          mbar_arrive(smem_u32(&spl_full[u]));
         }
       }
+    } else if (warp == kTmaWarp) {
+      // ---- TMA producer (one lane) ----
+      if (lane == 0) {
+        for (int c = 0; c < nchunks; ++c) {
+          const int qq = q + c, r = qq % NRAW;
+          if (abort_s) break;
+          if (qq >= NRAW && !mbar_wait(smem_u32(&raw_free[r]), (uint32_t)((qq / NRAW - 1) & 1))) {
+            fail();
+            break;
+          }
+          issue_stage(raw_base + r * kRawStage, p, i0, c, smem_u32(&raw_full[r]));
+          issued = qq + 1;
+        }
+      }
+      __syncwarp();
     } else if (warp == kMmaWarp) {
       // ---- MMA issuer (first lane) ----
-      {
-        if (lane == 0 && !abort_s) {
-          const uint32_t id = idesc(np);
-          for (int c = 0; c < nchunks; ++c) {
-            const int qq = q + c, u = qq % NSPL;
-            if (!mbar_wait(smem_u32(&spl_full[u]), (uint32_t)((qq / NSPL) & 1))) {
-              fail();
-              break;
-            }
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            const uint32_t sp = smem_u32(stage_base + u * kStage);
-            const uint32_t b_hi = sp, b_lo = sp + kTileB;
-            const uint32_t a_hi = tmem + kAcol + 32u * u, a_lo = a_hi + 16u;
-#pragma unroll
-            for (int k = 0; k < TK / 8; ++k) {
-              const uint64_t dbh = make_desc(b_hi + 2 * k * kLboB, kLboB);
-              const uint64_t dbl = make_desc(b_lo + 2 * k * kLboB, kLboB);
-              mma_tf32_ta(tmem, a_hi + 8u * k, dbh, id, (c > 0 || k > 0) ? 1u : 0u);
-              mma_tf32_ta(tmem, a_hi + 8u * k, dbl, id, 1u);
-              mma_tf32_ta(tmem, a_lo + 8u * k, dbh, id, 1u);
-            }
-            mma_commit(smem_u32(&spl_free[u]));
+      if (lane == 0 && !abort_s) {
+        const uint32_t id = idesc(np);
+        for (int c = 0; c < nchunks; ++c) {
+          const int qq = q + c, u = qq % NSPL;
+          if (!mbar_wait(smem_u32(&spl_full[u]), (uint32_t)((qq / NSPL) & 1))) {
+            fail();
+            break;
           }
-          if (!abort_s) mma_commit(smem_u32(&acc_full));
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint32_t sp = smem_u32(stage_base + u * kStage);
+          const uint32_t b_hi = sp, b_lo = sp + kTileB;
+          const uint32_t a_hi = tmem + kAcol + 32u * u, a_lo = a_hi + 16u;
+#pragma unroll
+          for (int k = 0; k < TK / 8; ++k) {
+            const uint64_t dbh = make_desc(b_hi + 2 * k * kLboB, kLboB);
+            const uint64_t dbl = make_desc(b_lo + 2 * k * kLboB, kLboB);
+            mma_tf32_ta(tmem, a_hi + 8u * k, dbh, id, (c > 0 || k > 0) ? 1u : 0u);
+            mma_tf32_ta(tmem, a_hi + 8u * k, dbl, id, 1u);
+            mma_tf32_ta(tmem, a_lo + 8u * k, dbh, id, 1u);
+          }
+          mma_commit(smem_u32(&spl_free[u]));
         }
-        __syncwarp();
+        if (!abort_s) mma_commit(smem_u32(&acc_full));
       }
+      __syncwarp();
     }
     {
       // ---- epilogue, all twelve warps: three per TMEM lane quarter, each
@@ -465,7 +503,7 @@ __global__ void __launch_bounds__(NTH, 1) k_ns_cluster(NsArgs a) {
       const bool ok = !abort_s && mbar_wait(smem_u32(&acc_full), (uint32_t)(s & 1));
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       // tcgen05.ld is warp-collective: the whole warp takes the same decision
-      if (__all_sync(0xffffffffu, ok && !abort_s)) {
+      if (__all_sync(kFull, ok && !abort_s)) {
         auto piece = [&](int cb, const float4 (&e)[8]) {
           uint32_t v[32];
           const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)cb;
@@ -515,12 +553,20 @@ __global__ void __launch_bounds__(NTH, 1) k_ns_cluster(NsArgs a) {
       }
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     }
-    // the product is complete in global memory for the whole cluster before
-    // the next one reads it; the accumulator is free again
+    // the product is complete in global memory for the whole cluster (and
+    // visible to the async proxy that reads it with TMA) before the next one
+    // starts; the accumulator is free again
+    asm volatile("fence.proxy.async.global;" ::: "memory");
     cluster_sync();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   }
 
+  if (warp == kTmaWarp && lane == 0) {
+    // drain: every copy issued must have landed before the CTA may exit
+    for (int qq = issued > NRAW ? issued - NRAW : 0; qq < issued; ++qq)
+      if (!mbar_wait(smem_u32(&raw_full[qq % NRAW]), (uint32_t)((qq / NRAW) & 1)))
+        atomicExch(a.err, 1);
+  }
   if (warp == kMmaWarp && lane == 0) {
     // tracks every MMA issued above, also after an abort
     mma_commit(smem_u32(&mma_done));
@@ -565,10 +611,57 @@ bool cluster_fits(int ncta) {
   }
   return fits[dev][ncta] == 1;
 }
+
+// ---- tensor maps (the driver's encoder is looked up once through the
+// runtime, so the library does not link the driver) ----
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                 const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                 CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiled encoder() {
+  static EncodeTiled fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiled>(p);
+  });
+  return fn;
+}
+
+// nmat row-major m x m matrices at p, rows holding K contiguously: 4-D view
+// {4, m rows, m / 4 k-groups, nmat} read in {4, rows, 4, 1} boxes (K-major
+// 16-byte pieces, piece (row, k4) at 16 (rows k4 + row))
+bool map_kc(CUtensorMap* t, const float* p, int m, int nmat, int rows) {
+  const cuuint64_t dim[4] = {4, (cuuint64_t)m, (cuuint64_t)(m / 4), (cuuint64_t)nmat};
+  const cuuint64_t stride[3] = {(cuuint64_t)m * 4, 16, (cuuint64_t)m * m * 4};
+  const cuuint32_t box[4] = {4, (cuuint32_t)rows, TK / 4, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return encoder()(t, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(p), dim, stride, box,
+                   es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+// the same matrices read as [k][row] (row contiguous): 3-D view {m, m, nmat}
+// in {rows, TK, 1} boxes
+bool map_mn(CUtensorMap* t, const float* p, int m, int nmat, int rows) {
+  const cuuint64_t dim[3] = {(cuuint64_t)m, (cuuint64_t)m, (cuuint64_t)nmat};
+  const cuuint64_t stride[2] = {(cuuint64_t)m * 4, (cuuint64_t)m * m * 4};
+  const cuuint32_t box[3] = {(cuuint32_t)rows, TK, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return encoder()(t, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(p), dim, stride, box,
+                   es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 }  // namespace
 
 bool ns_cluster_ok(int m) {
-  return m > 64 && m <= 2 * TM && m % 4 == 0 && cluster_fits((m + TM - 1) / TM);
+  return m > 64 && m <= 2 * TM && m % 4 == 0 && encoder() != nullptr &&
+         cluster_fits((m + TM - 1) / TM);
 }
 
 cudaError_t run_ns_cluster(const Prob& p, bool reverse, const float* A, float* X, float* Y, int nx,
@@ -578,11 +671,25 @@ cudaError_t run_ns_cluster(const Prob& p, bool reverse, const float* A, float* X
   NsArgs a;
   a.err = wait_error_address();
   if (a.err == nullptr) return cudaErrorInvalidValue;
-  a.A = A; a.X = X; a.Y = Y; a.G = G; a.XG = XG; a.Tm = Tm; a.dA = dA;
+  a.X = X; a.Y = Y; a.G = G; a.XG = XG; a.Tm = Tm; a.dA = dA;
   a.m = p.m; a.iters = p.iters; a.nx = nx; a.ny = ny; a.reverse = reverse ? 1 : 0;
-  const int ncta = (p.m + TM - 1) / TM;
+  const int m = p.m, BH = p.BH;
+  // every map, also those the program does not use (the reverse buffers of a
+  // forward point at A: valid memory, never read)
+  const float* g = G ? G : A;
+  const float* xg = XG ? XG : A;
+  NsMaps mp;
+  memset(&mp, 0, sizeof(mp));
+  const bool ok = map_kc(&mp.a_kc, A, m, BH, TM) && map_mn(&mp.a_mn, A, m, BH, TM) &&
+                  map_kc(&mp.x_akc, X, m, BH * nx, TM) && map_mn(&mp.x_amn, X, m, BH * nx, TM) &&
+                  map_mn(&mp.x_bmn, X, m, BH * nx, TNMAX) && map_kc(&mp.x_bkc, X, m, BH * nx, TNMAX) &&
+                  map_mn(&mp.y_bmn, Y, m, BH * ny, TNMAX) && map_kc(&mp.y_bkc, Y, m, BH * ny, TNMAX) &&
+                  map_kc(&mp.g_akc, g, m, BH, TM) && map_mn(&mp.g_bmn, g, m, BH, TNMAX) &&
+                  map_kc(&mp.xg_akc, xg, m, BH, TM) && map_mn(&mp.xg_bmn, xg, m, BH, TNMAX);
+  if (!ok) return cudaErrorInvalidValue;
+  const int ncta = (m + TM - 1) / TM;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ncta, p.BH);
+  cfg.gridDim = dim3(ncta, BH);
   cfg.blockDim = dim3(NTH);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = st;
@@ -594,7 +701,7 @@ cudaError_t run_ns_cluster(const Prob& p, bool reverse, const float* A, float* X
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const int slot = prof_begin(reverse ? "ns_cluster_rev" : "ns_cluster", st);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, k_ns_cluster, a);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k_ns_cluster, mp, a);
   prof_end(slot, st);
   count_launch();
   return e;
