@@ -54,26 +54,40 @@ def parse():
 
 
 def algorithmic_ops(w):
-    """FP32-pipe lane-ops per step of the method's arithmetic, per kernel.
+    """Algorithmic FP32 lane-ops per step, per kernel, from the method's
+    formulas (the per-unit figures of the hot-path table: an L1 step = 2
+    lane-ops, an FMA = 1).  Per (token, landmark) pair and feature: key and
+    query passes 3 (distance 2, contraction 1), each backward side 7 (kernel
+    value 2, dot 1, contraction 1, sign term 3); Newton-Schulz 2 m^3 per forward
+    step and 6 m^3 per reverse step (all products of a step); norm statistics
+    2 per element.  The work is fixed by the method, not by where it runs:
+    contractions on the tensor cores and kernel values read back from the
+    forward still count."""
+    BH, N, m, d, T = w.B * w.H, w.N, w.m, w.d, w.iters
+    nmd = BH * N * m * d
+    return {
+        "key_fwd": 3 * nmd,
+        "query_fwd": 3 * nmd,
+        "qstats": 2 * nmd if w.norm else 0,
+        "bwd_query": 7 * nmd,
+        "bwd_key": 7 * nmd,
+        "bwd_qstats": 2 * nmd if w.norm else 0,
+        "ns_cluster": 2 * T * BH * m ** 3,
+        "ns_cluster_rev": 6 * T * BH * m ** 3,
+    }
 
-    Per (token, landmark, feature) element: the forward passes need the L1
-    distance (sub, abs-add: 2) and the contraction (1); the backward kernels
-    need the sign term (sub, select and the two accumulations: 4), the dot (1)
-    and the contraction (1); the kernel values themselves come from the
-    forward.  With bf16 inputs the contractions and dots run on the tensor
-    cores, so they are not FP32-pipe work and are not counted here; the
-    Newton-Schulz products are tensor-core work too."""
+
+def fp32_pipe_ops(w):
+    """The part of algorithmic_ops that this build executes on the FP32 pipes
+    with bf16 inputs: the distances of the forward passes (2) and the sign term
+    of the backward sides (4); dots, contractions and the Newton-Schulz
+    products run on the tensor cores and the backward reads the forward's
+    kernel values."""
     BH, N, m, d = w.B * w.H, w.N, w.m, w.d
     nmd = BH * N * m * d
     tc = w.dtype == "bf16"
-    return {
-        "key_fwd": (2 if tc else 3) * nmd,
-        "query_fwd": (2 if tc else 3) * nmd,
-        "qstats": 2 * nmd if w.norm else 0,
-        "bwd_query": (4 if tc else 6) * nmd,
-        "bwd_key": (4 if tc else 6) * nmd,
-        "bwd_qstats": 4 * nmd if w.norm else 0,
-    }
+    return {"key_fwd": (2 if tc else 3) * nmd, "query_fwd": (2 if tc else 3) * nmd,
+            "bwd_query": (4 if tc else 6) * nmd, "bwd_key": (4 if tc else 6) * nmd}
 
 
 def max_over_ranks(x: float, world: int, device) -> float:
@@ -291,12 +305,14 @@ def run_ours(args, rank, world, local_rank):
     dom_ms = kernel_ms[dom][1]
     achieved = per_launch_ops[dom] / (dom_ms / 1e3) / 1e12
     total_ops = sum(ops.values())
+    pipe = fp32_pipe_ops(w)
     roofline = {
         "bound": "alu", "kernel": dom, "achieved": achieved, "peak": ALU_PEAK_TOPS,
         "unit": "Tlaneop/s", "frac": achieved / ALU_PEAK_TOPS,
         "traffic": None,
         "peak_source": "152 SMs x 128 FP32 lanes x 2070 MHz",
         "step_frac": total_ops / (ms / 1e3) / 1e12 / ALU_PEAK_TOPS,
+        "fp32_pipe_frac": pipe[dom] / (dom_ms / 1e3) / 1e12 / ALU_PEAK_TOPS,
     }
 
     # end to end through the public API: pinned host inputs in, results back to host

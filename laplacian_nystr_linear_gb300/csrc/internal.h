@@ -114,19 +114,24 @@ struct BwdArgs {
   float* lm_part;     // [BH][S][mp][d]: dL
   float* lm_part2;    // [BH][S][mp][d]: dWhat (modes 0, 1)
   float* ns_part;     // [BH][S][2][mp]: sum dZ, sum dZ*Z (mode 0)
-  const uint8_t* ties;  // [BH][ceil(N / 32)]: block needs the exact sign path (modes 1, 2)
+  const uint32_t* ties; // [BH][ceil(N / 32)][kTieRec]: tie records (modes 1, 2)
   const float* kv;      // [BH][N][mp]: kernel values P (mode 1) or C (mode 2) of the forward
 };
 cudaError_t run_bwd_tile(const Prob& p, int mode, const BwdArgs& a, cudaStream_t st);
 // modes 1 and 2 with the FMA-pipe sign term (32-token blocks)
 cudaError_t run_bwd_pair(const Prob& p, int mode, const BwdArgs& a, cudaStream_t st);
 // tie detection for the sign term: run_tie_prep reads the landmarks into
-// `scratch` (ties_scratch_bytes), run_ties flags the 32-token blocks of x
-// ([BH][ceil(N / 32)] bytes) that hold a value tied with a landmark value or
-// out of the fast path's range
+// `scratch` (ties_scratch_bytes); run_ties writes one record of kTieRec words
+// per 32-token block of x ([BH][ceil(N / 32)][kTieRec]): word 0 is the number
+// of ties n, or kTieExact when the block must take the exact sign path (a value
+// out of the fast path's range, or more than kTieRec - 1 ties); words 1..n are
+// the ties, ascending, each packed as token-in-block | feature << 5 |
+// landmark << 12, for a token value equal to a landmark value
+constexpr int kTieRec = 16;
+constexpr uint32_t kTieExact = 0x80000000u;
 size_t ties_scratch_bytes(int BH, int m, int d);
 cudaError_t run_tie_prep(const Prob& p, const float* L, void* scratch, cudaStream_t st);
-cudaError_t run_ties(const Prob& p, const void* x, void* scratch, uint8_t* flags, cudaStream_t st);
+cudaError_t run_ties(const Prob& p, const void* x, void* scratch, uint32_t* rec, cudaStream_t st);
 cudaError_t run_mdz(const Prob& p, const float* ns_part, float* mdz, cudaStream_t st);
 cudaError_t run_gram_bwd(const Prob& p, const float* L, const float* A, const float* dA, float* dLA,
                          cudaStream_t st);

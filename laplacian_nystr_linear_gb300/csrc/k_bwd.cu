@@ -14,9 +14,11 @@
 // 0 or 1 whenever x != l and both lie in {0} u [2^-40, 2^60] (the difference is
 // then at least 2^-64).  So the sign term costs three FMA-pipe operations per
 // (token, landmark, feature) instead of compare/select work on the half-rate
-// ALU pipe.  Ties and out-of-range values are found ahead of these kernels
-// (k_ties.cu, one flag per 32-token block); a flagged block takes an exact
-// path with sgn(0) = 0.
+// ALU pipe.  A tie x == l reads as sgn = -1 there instead of 0: the fast path
+// then puts g_ja into dX_jc and -g_ja into dL_ac, which a correction takes back
+// for each tie the tie kernels listed for the block (k_ties.cu; a few per
+// block at most).  A block with an out-of-range value or too many ties takes an
+// exact path with sgn(0) = 0.
 //
 // Work split per CTA: one 64-landmark tile and a contiguous range of 32-token
 // blocks; the raw token and upstream rows of the next block are copied into
@@ -187,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
                const float* __restrict__ R, const float* __restrict__ stats,
                const float* __restrict__ mdz, float* __restrict__ tok_part,
                float* __restrict__ tok_part2, float* __restrict__ lm_part,
-               float* __restrict__ lm_part2, const uint8_t* __restrict__ tie_flags,
+               float* __restrict__ lm_part2, const uint32_t* __restrict__ tie_rec,
                const float* __restrict__ KV, int N, int m, int mp, int S, int nblk, int BH,
                float inv_lam) {
   constexpr int CW = D / 8;     // features per warp in phase S
@@ -214,6 +216,8 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
   constexpr int RP = SM::template raw_pitch<T>();
   __shared__ float mu_s[TA], rs_s[TA], m0_s[TA], m1_s[TA];
   __shared__ float rowg_s[TJ], colg_s[TA];  // sums of g over the tile's landmarks / block's tokens
+  __shared__ uint32_t tie_s[kTieRec];        // this block's ties in this tile (else ~0u)
+  __shared__ float tieg_s[kTieRec];          // g of each tie
 
   const int lt = blockIdx.x, sp = blockIdx.y, bh = blockIdx.z;
   const int a0 = lt * TA;
@@ -299,7 +303,10 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
 
   for (int b = b0; b < b1; ++b) {
     const int n0 = b * TJ;
-    const bool exact = cta_exact || tie_flags[(size_t)bh * nblk + b] != 0;
+    const uint32_t* rb = tie_rec + ((size_t)bh * nblk + b) * kTieRec;
+    const uint32_t rh = __ldg(rb);
+    const bool exact = cta_exact || (rh & kTieExact) != 0;
+    const int nties = exact ? 0 : (int)rh;
     cp_wait_all();
     __syncthreads();
     // tokens transposed (Xt[c][j]) and U rows, from the raw copies
@@ -547,6 +554,14 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
         g2[r][0] = u.x; g2[r][1] = u.y; g2[r][2] = u.z; g2[r][3] = u.w;
         g2[r][4] = v.x; g2[r][5] = v.y; g2[r][6] = v.z; g2[r][7] = v.w;
       }
+      if (tid < nties) {
+        // the tie's g, read before the g tile becomes staging space
+        const uint32_t t = __ldg(rb + 1 + tid);
+        const int a = (int)(t >> 12) - a0;
+        const bool mine = a >= 0 && a < nv;
+        tie_s[tid] = mine ? t : ~0u;
+        tieg_s[tid] = mine ? 0.5f * Gs[(int)(t & 31u) * AS + pa(a)] : 0.f;
+      }
       __syncthreads();  // g and Z tiles are free from here on (staging); sums are ready
       const float rowg = rowg_s[j0 + ag];
       if (!exact) {
@@ -559,6 +574,18 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
         sign_cols<D, false>(warp * CW, j0, al, jg, ag, g2, Xt, LBt, rowg, inv_scale, Stage, dLs);
     }
     __syncthreads();
+    if (nties > 0) {
+      // ties: the fast path counted sgn(0) as -1; take g back from dX, give it to dL
+      if (tid == 0)
+        for (int i = 0; i < nties; ++i) {
+          const uint32_t t = tie_s[i];
+          if (t == ~0u) continue;
+          const int j = (int)(t & 31u), c = (int)((t >> 5) & 127u), a = (int)(t >> 12) - a0;
+          Stage[j * (D + 4) + c] -= tieg_s[i];
+          dLs[c * TA + a] += tieg_s[i];
+        }
+      __syncthreads();
+    }
     // staged token-side results -> per-tile partial rows
     for (int id = tid; id < TJ * (D / 4); id += kThreads) {
       const int j = id / (D / 4), c = (id % (D / 4)) * 4;
@@ -604,7 +631,7 @@ static cudaError_t bwd_pair_t2(const Prob& p, const BwdArgs& a, cudaStream_t st)
   const int nblk = (p.N + TJ - 1) / TJ;
   return launch(names[MODE], k_bwd_pair<D, T, MODE, NORM>, dim3(p.nt, p.Sb, p.BH), dim3(kThreads),
                 smem, st, (const T*)a.X, (const T*)a.U, a.L, a.R, a.stats, a.mdz, a.tok_part,
-                a.tok_part2, a.lm_part, a.lm_part2, (const uint8_t*)a.ties, a.kv, p.N, p.m, p.mp,
+                a.tok_part2, a.lm_part, a.lm_part2, a.ties, a.kv, p.N, p.m, p.mp,
                 p.Sb, nblk, p.BH, p.inv_lam);
 }
 

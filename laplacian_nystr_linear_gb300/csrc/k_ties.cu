@@ -4,21 +4,27 @@
 // The kernel gradient carries sgn(x_c - l_c) per (token, landmark, feature)
 // ("LaplacianFormer", Dutch summary Methodology 1: the L1 norm keeps a
 // non-vanishing gradient); the backward tile kernels evaluate it as one
-// saturated FMA, which is exact except where x_c == l_c (sgn(0) = 0) or a value
-// lies outside {0} u [2^-40, 2^60].  These kernels find, ahead of the tile
-// kernels, every 32-token block holding such a value, so that only those
-// blocks take the exact path.
+// saturated FMA, which reads a tie x_c == l_c as sgn = -1 instead of 0 and is
+// exact otherwise, as long as every value lies in {0} u [2^-40, 2^60].  These
+// kernels list, ahead of the tile kernels, the ties of every 32-token block as
+// (token, feature, landmark) triples; the tile kernels take the fast path and
+// then correct the listed terms, which are few (bf16 tokens meet a landmark
+// value exactly a few times per block at most).  A block with an out-of-range
+// value, or with more ties than a record holds, is marked for the exact path.
 //
-// k_tie_prep (one CTA per slice and group of 16 feature columns):
+// k_tie_prep (one CTA per slice and group of 8 feature columns):
 //   - flags the slice when a landmark value is out of range;
 //   - marks, per feature column, the candidate values in a 8192-bit map keyed
 //     by 13 bits of the value (sign, 5 low exponent bits, 7 high mantissa
 //     bits).  A bf16 token can only equal a landmark value that bf16
 //     represents exactly, so for bf16 tokens only those values are candidates;
-//   - sorts each column's candidate values ascending (the others as +inf).
-// k_ties (many CTAs per slice): streams the tokens 16 bytes at a time; a
-// value that is out of range, or whose key is marked and which a binary search
-// of the sorted column finds, flags its block.
+//   - sorts each column's candidate values ascending with their landmark
+//     indices (the others as +inf).
+// k_ties (many CTAs per slice, at most 64 blocks each): streams the tokens 16
+// bytes at a time, eight loads in flight per thread; a value whose key is
+// marked is looked up in the sorted column and every landmark holding it gives
+// a triple.  Triples are gathered per block in shared memory and written
+// sorted, so the corrections are applied in a fixed order.
 #include <type_traits>
 
 #include "common.cuh"
@@ -27,12 +33,14 @@
 namespace lapnys {
 
 namespace {
-constexpr int TJ = 32;                              // tokens per flagged block
-constexpr int kCols = 16;                           // feature columns per prep CTA
+constexpr int TJ = 32;                              // tokens per block
+constexpr int kCols = 8;                            // feature columns per prep CTA
 constexpr int kMapWords = 256;                      // 8192-bit map per column
 constexpr float kLo = 9.094947017729282e-13f;        // 2^-40
 constexpr float kHi = 1.152921504606846976e18f;      // 2^60
-constexpr int kMaxBlocks = 2048;                     // flag bits per k_ties CTA
+constexpr int kMaxBlocks = 64;                       // blocks per k_ties CTA
+constexpr int kCap = kTieRec - 1;                    // triples per record
+constexpr int kUnroll = 8;                           // 16-byte loads in flight per thread
 
 __device__ __forceinline__ bool out_of_range(float v) {
   const float a = fabsf(v);
@@ -57,21 +65,24 @@ size_t pow2_at_least(int m) {
 }
 }  // namespace
 
-// scratch: sorted [BH][P][D] f32, map [BH][D][kMapWords] u32, bad [BH][D / kCols] i32
+// scratch: sorted values [BH][P][D] f32, their landmark indices [BH][P][D] i32,
+// map [BH][D][kMapWords] u32, bad [BH][D / kCols] i32
 size_t ties_scratch_bytes(int BH, int m, int d) {
   const size_t P = pow2_at_least(m);
-  return (size_t)BH * P * d * 4 + (size_t)BH * d * kMapWords * 4 + (size_t)BH * (d / kCols) * 4 +
-         256;
+  return 2 * (size_t)BH * P * d * 4 + (size_t)BH * d * kMapWords * 4 +
+         (size_t)BH * (d / kCols) * 4 + 256;
 }
 
 template <typename T>
 __global__ void __launch_bounds__(kThreads) k_tie_prep(const float* __restrict__ L,
                                                        float* __restrict__ sorted,
+                                                       int* __restrict__ sidx,
                                                        uint32_t* __restrict__ map,
                                                        int* __restrict__ bad, int m, int P, int D) {
   extern __shared__ float4 sm4[];
-  float* a = reinterpret_cast<float*>(sm4);                        // [kCols][P]
-  uint32_t* mp = reinterpret_cast<uint32_t*>(a + kCols * P);       // [kCols][kMapWords]
+  float* a = reinterpret_cast<float*>(sm4);                        // [kCols][P] values
+  int* ix = reinterpret_cast<int*>(a + kCols * P);                 // [kCols][P] landmark index
+  uint32_t* mp = reinterpret_cast<uint32_t*>(ix + kCols * P);      // [kCols][kMapWords]
   const int bh = blockIdx.x, cg = blockIdx.y, c0 = cg * kCols, tid = threadIdx.x;
   const float* Lb = L + (size_t)bh * m * D;
   const float inf = __int_as_float(0x7f800000);
@@ -91,21 +102,26 @@ __global__ void __launch_bounds__(kThreads) k_tie_prep(const float* __restrict__
       }
     }
     a[e] = v;
+    ix[e] = i;
   }
   const int any = __syncthreads_or(b);
   if (tid == 0) bad[bh * (D / kCols) + cg] = any ? 1 : 0;
-  // bitonic sort of every column, ascending
+  // bitonic sort of every column by value, ascending, carrying the indices
   for (int k = 2; k <= P; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
       for (int e = tid; e < kCols * (P / 2); e += kThreads) {
         const int cc = e / (P / 2), t = e % (P / 2);
         const int i = 2 * t - (t & (j - 1));  // lower index of the pair
         float* col = a + cc * P;
+        int* ci = ix + cc * P;
         const bool up = (i & k) == 0;
         const float x = col[i], y = col[i + j];
         if ((x > y) == up) {
           col[i] = y;
           col[i + j] = x;
+          const int t0 = ci[i];
+          ci[i] = ci[i + j];
+          ci[i + j] = t0;
         }
       }
       __syncthreads();
@@ -114,6 +130,7 @@ __global__ void __launch_bounds__(kThreads) k_tie_prep(const float* __restrict__
   for (int e = tid; e < kCols * P; e += kThreads) {
     const int i = e / kCols, cc = e % kCols;
     sorted[((size_t)bh * P + i) * D + c0 + cc] = a[cc * P + i];
+    sidx[((size_t)bh * P + i) * D + c0 + cc] = ix[cc * P + i];
   }
   for (int e = tid; e < kCols * kMapWords; e += kThreads)
     map[((size_t)bh * D + c0) * kMapWords + e] = mp[e];
@@ -122,13 +139,16 @@ __global__ void __launch_bounds__(kThreads) k_tie_prep(const float* __restrict__
 template <int D, typename T>
 __global__ void __launch_bounds__(kThreads) k_ties(const T* __restrict__ X,
                                                    const float* __restrict__ sorted,
+                                                   const int* __restrict__ sidx,
                                                    const uint32_t* __restrict__ map,
                                                    const int* __restrict__ bad,
-                                                   uint8_t* __restrict__ flags, int N, int P,
+                                                   uint32_t* __restrict__ rec, int N, int P,
                                                    int nblk, int S) {
   extern __shared__ float4 sm4[];
   uint32_t* mp = reinterpret_cast<uint32_t*>(sm4);  // [D][kMapWords]
-  __shared__ unsigned bits[kMaxBlocks / 32];
+  __shared__ unsigned oor[kMaxBlocks / 32];         // block holds an out-of-range value
+  __shared__ unsigned cnt[kMaxBlocks];              // ties found per block
+  __shared__ uint32_t lst[kMaxBlocks][kCap];        // the first kCap triples per block
   constexpr int V = 16 / (int)sizeof(T);  // values per 16-byte load
   constexpr int G = D / V;                // 16-byte groups per token row
   static_assert(kThreads % G == 0, "a thread's columns must stay fixed");
@@ -136,9 +156,11 @@ __global__ void __launch_bounds__(kThreads) k_ties(const T* __restrict__ X,
   const int b0 = (int)((long long)nblk * sp / S), b1 = (int)((long long)nblk * (sp + 1) / S);
   const T* Xb = X + (size_t)bh * N * D;
   const float* Sb = sorted + (size_t)bh * P * D;
+  const int* Ib = sidx + (size_t)bh * P * D;
   bool all = false;
   for (int g = 0; g < D / kCols; ++g) all = all || bad[bh * (D / kCols) + g] != 0;
-  for (int e = tid; e < kMaxBlocks / 32; e += kThreads) bits[e] = 0u;
+  for (int e = tid; e < kMaxBlocks; e += kThreads) cnt[e] = 0u;
+  if (tid < kMaxBlocks / 32) oor[tid] = 0u;
   if (!all)
     for (int e = tid; e < D * kMapWords / 4; e += kThreads)
       sm4[e] = __ldg(reinterpret_cast<const float4*>(map + (size_t)bh * D * kMapWords) + e);
@@ -146,55 +168,81 @@ __global__ void __launch_bounds__(kThreads) k_ties(const T* __restrict__ X,
   if (!all) {
     const int c0 = (tid % G) * V;
     const int n_lo = b0 * TJ, n_hi = min(N, b1 * TJ);
-#pragma unroll 2
-    for (int e = tid; e < (n_hi - n_lo) * G; e += kThreads) {
-      const int n = n_lo + e / G;
-      const uint4 u = __ldg(reinterpret_cast<const uint4*>(Xb + (size_t)n * D + c0));
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-      uint32_t xb[V];
+    const int total = (n_hi - n_lo) * G;
+    for (int e0 = tid; e0 < total; e0 += kUnroll * kThreads) {
+      uint4 u[kUnroll];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if constexpr (V == 8) {
-          xb[2 * q] = w[q] << 16;
-          xb[2 * q + 1] = w[q] & 0xffff0000u;
-        } else {
-          xb[q] = w[q];
-        }
+      for (int i = 0; i < kUnroll; ++i) {
+        const int e = e0 + i * kThreads;
+        u[i] = e < total ? __ldg(reinterpret_cast<const uint4*>(Xb + (size_t)(n_lo + e / G) * D + c0))
+                         : make_uint4(0u, 0u, 0u, 0u);
       }
-      bool tie = false;
 #pragma unroll
-      for (int q = 0; q < V; ++q) {
-        const float x = __uint_as_float(xb[q]);
-        const uint32_t k = tie_key(xb[q]);
-        const bool marked = (mp[(c0 + q) * kMapWords + (k >> 5)] >> (k & 31)) & 1u;
-        if (out_of_range(x)) {
-          tie = true;
-        } else if (marked) {
-          // exact check: is x among the column's sorted candidate values?
-          const float* col = Sb + c0 + q;
-          int lo = 0;
-          for (int step = P >> 1; step > 0; step >>= 1)
-            if (__ldg(col + (size_t)(lo + step - 1) * D) < x) lo += step;
-          tie = tie || __ldg(col + (size_t)lo * D) == x;
+      for (int i = 0; i < kUnroll; ++i) {
+        const int e = e0 + i * kThreads;
+        if (e >= total) break;
+        const int n = n_lo + e / G, k = n / TJ - b0, j = n % TJ;
+        const uint32_t w[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
+        uint32_t xb[V];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if constexpr (V == 8) {
+            xb[2 * q] = w[q] << 16;
+            xb[2 * q + 1] = w[q] & 0xffff0000u;
+          } else {
+            xb[q] = w[q];
+          }
         }
-      }
-      if (tie) {
-        const int k = n / TJ - b0;
-        if (k < kMaxBlocks) atomicOr(&bits[k >> 5], 1u << (k & 31));
+        bool bad_x = false;
+#pragma unroll
+        for (int q = 0; q < V; ++q) {
+          const float x = __uint_as_float(xb[q]);
+          const uint32_t key = tie_key(xb[q]);
+          bad_x = bad_x || out_of_range(x);
+          if ((mp[(c0 + q) * kMapWords + (key >> 5)] >> (key & 31)) & 1u) {
+            // lower bound of x in the column's sorted candidates, then every equal entry
+            const float* col = Sb + c0 + q;
+            int lo = 0;
+            for (int step = P >> 1; step > 0; step >>= 1)
+              if (__ldg(col + (size_t)(lo + step - 1) * D) < x) lo += step;
+            for (int t = lo; t < P && __ldg(col + (size_t)t * D) == x; ++t) {
+              const uint32_t a = (uint32_t)__ldg(Ib + (size_t)t * D + c0 + q);
+              const unsigned slot = atomicAdd(&cnt[k], 1u);
+              if (slot < (unsigned)kCap) lst[k][slot] = (uint32_t)j | (uint32_t)(c0 + q) << 5 | a << 12;
+            }
+          }
+        }
+        if (bad_x) atomicOr(&oor[k >> 5], 1u << (k & 31));
       }
     }
   }
   __syncthreads();
   for (int b = b0 + tid; b < b1; b += kThreads) {
     const int k = b - b0;
-    const bool f = all || k >= kMaxBlocks || ((bits[k >> 5] >> (k & 31)) & 1u);
-    flags[(size_t)bh * nblk + b] = f ? 1 : 0;
+    uint32_t* r = rec + ((size_t)bh * nblk + b) * kTieRec;
+    const unsigned n = cnt[k];
+    if (all || ((oor[k >> 5] >> (k & 31)) & 1u) || n > (unsigned)kCap) {
+      r[0] = kTieExact;
+      continue;
+    }
+    r[0] = n;
+    // insertion sort of the block's triples: a fixed order for the corrections
+    for (unsigned i = 0; i < n; ++i) {
+      uint32_t best = lst[k][i];
+      unsigned at = i;
+      for (unsigned t = i + 1; t < n; ++t)
+        if (lst[k][t] < best) { best = lst[k][t]; at = t; }
+      lst[k][at] = lst[k][i];
+      lst[k][i] = best;
+      r[1 + i] = best;
+    }
   }
 }
 
 namespace {
 struct TieScratch {
   float* sorted;
+  int* sidx;
   uint32_t* map;
   int* bad;
   int P;
@@ -203,13 +251,14 @@ TieScratch tie_scratch(const Prob& p, void* scratch) {
   TieScratch t;
   t.P = (int)pow2_at_least(p.m);
   t.sorted = reinterpret_cast<float*>(scratch);
-  t.map = reinterpret_cast<uint32_t*>(t.sorted + (size_t)p.BH * t.P * p.d);
+  t.sidx = reinterpret_cast<int*>(t.sorted + (size_t)p.BH * t.P * p.d);
+  t.map = reinterpret_cast<uint32_t*>(t.sidx + (size_t)p.BH * t.P * p.d);
   t.bad = reinterpret_cast<int*>(t.map + (size_t)p.BH * p.d * kMapWords);
   return t;
 }
 
 template <int D, typename T>
-cudaError_t ties_t(const Prob& p, const void* x, const TieScratch& t, uint8_t* flags,
+cudaError_t ties_t(const Prob& p, const void* x, const TieScratch& t, uint32_t* rec,
                    cudaStream_t st) {
   const size_t smem = (size_t)D * kMapWords * 4;
   static bool once = (allow_smem(k_ties<D, T>, smem), true);
@@ -221,41 +270,41 @@ cudaError_t ties_t(const Prob& p, const void* x, const TieScratch& t, uint8_t* f
   if (S > nblk) S = nblk;
   if (S < 1) S = 1;
   return launch("ties", k_ties<D, T>, dim3(S, p.BH), dim3(kThreads), smem, st, (const T*)x,
-                (const float*)t.sorted, (const uint32_t*)t.map, (const int*)t.bad, flags, p.N,
-                t.P, nblk, S);
+                (const float*)t.sorted, (const int*)t.sidx, (const uint32_t*)t.map,
+                (const int*)t.bad, rec, p.N, t.P, nblk, S);
 }
 }  // namespace
 
 cudaError_t run_tie_prep(const Prob& p, const float* L, void* scratch, cudaStream_t st) {
   const TieScratch t = tie_scratch(p, scratch);
-  const size_t smem = (size_t)kCols * t.P * 4 + (size_t)kCols * kMapWords * 4;
+  const size_t smem = (size_t)kCols * t.P * 8 + (size_t)kCols * kMapWords * 4;
   if (p.dtype == 1) {
     static bool once = (allow_smem(k_tie_prep<__nv_bfloat16>, 96 * 1024), true);
     (void)once;
     return launch("tie_prep", k_tie_prep<__nv_bfloat16>, dim3(p.BH, p.d / kCols), dim3(kThreads),
-                  smem, st, L, t.sorted, t.map, t.bad, p.m, t.P, p.d);
+                  smem, st, L, t.sorted, t.sidx, t.map, t.bad, p.m, t.P, p.d);
   }
   static bool once = (allow_smem(k_tie_prep<float>, 96 * 1024), true);
   (void)once;
   return launch("tie_prep", k_tie_prep<float>, dim3(p.BH, p.d / kCols), dim3(kThreads), smem, st,
-                L, t.sorted, t.map, t.bad, p.m, t.P, p.d);
+                L, t.sorted, t.sidx, t.map, t.bad, p.m, t.P, p.d);
 }
 
-cudaError_t run_ties(const Prob& p, const void* x, void* scratch, uint8_t* flags, cudaStream_t st) {
+cudaError_t run_ties(const Prob& p, const void* x, void* scratch, uint32_t* rec, cudaStream_t st) {
   const TieScratch t = tie_scratch(p, scratch);
   if (p.dtype == 1) {
     switch (p.d) {
-      case 16: return ties_t<16, __nv_bfloat16>(p, x, t, flags, st);
-      case 32: return ties_t<32, __nv_bfloat16>(p, x, t, flags, st);
-      case 64: return ties_t<64, __nv_bfloat16>(p, x, t, flags, st);
-      case 128: return ties_t<128, __nv_bfloat16>(p, x, t, flags, st);
+      case 16: return ties_t<16, __nv_bfloat16>(p, x, t, rec, st);
+      case 32: return ties_t<32, __nv_bfloat16>(p, x, t, rec, st);
+      case 64: return ties_t<64, __nv_bfloat16>(p, x, t, rec, st);
+      case 128: return ties_t<128, __nv_bfloat16>(p, x, t, rec, st);
     }
   } else {
     switch (p.d) {
-      case 16: return ties_t<16, float>(p, x, t, flags, st);
-      case 32: return ties_t<32, float>(p, x, t, flags, st);
-      case 64: return ties_t<64, float>(p, x, t, flags, st);
-      case 128: return ties_t<128, float>(p, x, t, flags, st);
+      case 16: return ties_t<16, float>(p, x, t, rec, st);
+      case 32: return ties_t<32, float>(p, x, t, rec, st);
+      case 64: return ties_t<64, float>(p, x, t, rec, st);
+      case 128: return ties_t<128, float>(p, x, t, rec, st);
     }
   }
   return cudaErrorInvalidValue;

@@ -137,7 +137,7 @@ struct WsLayout {
   size_t dWhp, dLqp, dLcp, nsp, mdz;           // backward landmark-side partials
   size_t dQp, dKp, dVp;                        // backward token-side partials
   size_t dWh, dW, dLA, dL, G, XG, Tm, dA;      // backward landmark-side results
-  size_t ties, tie_scratch;                    // tie flags (query, key) and their scratch
+  size_t ties, tie_scratch;                    // tie records (query, key) and their scratch
   size_t total;
 };
 
@@ -166,7 +166,7 @@ static WsLayout ws_layout(const Prob& p) {
   w.XG = o; o = align256(o + BH * m * m * f);
   w.Tm = o; o = align256(o + BH * m * m * f);
   w.dA = o; o = align256(o + BH * m * m * f);
-  w.ties = o; o = align256(o + 2 * BH * (size_t)((p.N + 31) / 32));
+  w.ties = o; o = align256(o + 2 * BH * (size_t)((p.N + 31) / 32) * kTieRec * 4);
   w.tie_scratch = o; o = align256(o + ties_scratch_bytes(p.BH, p.m, p.d));
   w.total = o;
   return w;
@@ -501,8 +501,8 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
 
   // which 32-token blocks need the exact sign path (a value tied with a
   // landmark value, or out of the fast path's range)
-  uint8_t* ties_q = (uint8_t*)(wb + w.ties);
-  uint8_t* ties_k = tied_qk ? ties_q : ties_q + (size_t)p.BH * ((N + 31) / 32);
+  uint32_t* ties_q = (uint32_t*)(wb + w.ties);
+  uint32_t* ties_k = tied_qk ? ties_q : ties_q + (size_t)p.BH * ((N + 31) / 32) * kTieRec;
   CK(run_tie_prep(p, L, wb + w.tie_scratch, stream));
   CK(run_ties(p, q, wb + w.tie_scratch, ties_q, stream));
   if (!tied_qk) CK(run_ties(p, k, wb + w.tie_scratch, ties_k, stream));

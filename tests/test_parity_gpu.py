@@ -218,6 +218,61 @@ def test_ties_in_a_few_columns(dtype, m):
     print(w.name, dtype, m, compare(w, g, o, backward=True, tol=5e-3 if dtype == "bf16" else None))
 
 
+def _tie_positions(x, L):
+    """(token, feature) positions where a token value equals a landmark value,
+    and the number of (token, feature, landmark) ties per 32-token block."""
+    N, d = x.shape
+    per = np.zeros((N, d), np.int64)
+    for c in range(d):
+        per[:, c] = (x[:, c][:, None] == L[:, c][None, :]).sum(1)
+    blocks = np.add.reduceat(per.sum(1), np.arange(0, N, 32))
+    return np.argwhere(per > 0), blocks
+
+
+@pytest.mark.parametrize("m", [16, 64])
+def test_sparse_ties_are_corrected(m):
+    # bf16 tokens meet a landmark value exactly a few times per 32-token block:
+    # the fast sign path reads those as sgn = -1 and the listed ties are then
+    # corrected.  Two ties are planted per block of Q (a Q value set to a
+    # bf16-exact landmark value of its column; Q does not move the landmarks);
+    # at m = 64 (16-token windows) natural ties come on both sides, in about
+    # 60 % of the blocks.  Missing a correction moves that dq or dk element by
+    # |g| (about 1/sqrt(m) of its size), so those elements are held to bf16
+    # output rounding.
+    w = _small("sparse_ties", dtype="bf16", grid_h=32, grid_w=32, m=m, d=64, iters=6)
+    w = dataclasses.replace(w, B=1, H=2)
+    inp = random_inputs(21, 1, 2, w.N, w.d, "bf16")
+    idx = orc.pool_index(w.grid_h, w.grid_w, w.m)
+    rng = np.random.default_rng(21)
+    Ls = []
+    for h in range(2):
+        L = orc.pool_landmarks(inp["k"][0, h].astype(np.float64), idx, w.m)
+        exact = (L.astype(np.float32).astype(np.float64) == L) & (round_bf16(L.astype(np.float32)) == L)
+        cand = np.argwhere(exact)          # (landmark, feature) with a bf16-exact value
+        assert len(cand) > 0
+        for b0 in range(0, w.N, 32):
+            for _ in range(2):
+                a, c = cand[rng.integers(len(cand))]
+                inp["q"][0, h, b0 + rng.integers(32), c] = L[a, c]
+        Ls.append(L)
+    g = gpu_run(w, inp, backward=True)
+    o = oracle_run(w, inp, backward=True)
+    print(w.name, m, compare(w, g, o, backward=True))
+    for gi, (name, x) in enumerate((("dq", "q"), ("dk", "k"))):
+        n_corr = 0
+        for h in range(2):
+            pos, blocks = _tie_positions(inp[x][0, h], Ls[h])
+            n_corr += int(((blocks > 0) & (blocks < 16)).sum())
+            full = o["grads"][(0, h)][gi]
+            ref = full[pos[:, 0], pos[:, 1]]
+            got = g[name][0, h][pos[:, 0], pos[:, 1]]
+            rms = np.sqrt(np.mean(full ** 2))
+            err = np.abs(got - ref)
+            assert np.all(err <= 2.0 ** -8 * np.abs(ref) + 1e-3 * rms), (name, h, err.max(), rms)
+        # blocks whose ties went through the correction (not the exact path)
+        assert n_corr >= (32 if x == "q" else (16 if m == 64 else 0)), (name, n_corr)
+
+
 def test_deterministic():
     w = WORKLOADS["pvt2"]
     inp = make_inputs(w)
