@@ -25,7 +25,8 @@
 // shared memory (cp.async) while the current block computes; per block
 //   phase 1  (thread = 4 tokens x 2 landmarks)  dot, g from the kernel values
 //            the forward kept ([N][mp] rows, copied in with the token rows)
-//   phase S  (warp = D/8 features, lane = 8 tokens x 8 landmarks) sign term
+//   phase S  (warp = D/8 features, lane = 8 tokens x 8 landmarks) sign term,
+//            both sums as paired FMAs over token pairs (fma.rn.f32x2)
 //   phase C  contraction: dW-hat_a += sum_j Z_ja dO_j (query side) or
 //            dV_j = sum_a C_ja dW_a (key side)
 #include <type_traits>
@@ -68,7 +69,7 @@ struct Smem {
   static constexpr int Rs = LBt + D * AS;          // [TA][D+4] R rows
   static constexpr int Xt = Rs + TA * (D + 4);     // [D][JS]   tokens, transposed
   static constexpr int Us = Xt + D * JS;           // [TJ][D+4] U rows
-  static constexpr int Gs = Us + TJ * (D + 4);     // [TJ][AS]  2g
+  static constexpr int Gs = Us + TJ * (D + 4);     // 2g, landmark-major: gt(a, j)
   static constexpr int Zs = Gs + TJ * AS;          // [TJ][ZS]  Z (query side) or C (key side)
   static constexpr int dLs = Zs + TJ * (AS + 4);   // [D][TA]   landmark-side accumulator
   static constexpr int KVs = dLs + D * TA;         // [TJ][AS]  kernel values of the block
@@ -79,6 +80,7 @@ struct Smem {
   template <typename T>
   __host__ __device__ static constexpr int total() { return Raw + 2 * TJ * raw_pitch<T>() / 4; }
   static_assert(TJ * (D + 4) <= 2 * TJ * AS, "staging must fit in the g and Z tiles");
+  static_assert(TA * TJ <= TJ * AS, "the g tile must fit its region");
   // row stride of the Z / C tile: query side AS + 4 (its tensor-core dW-hat
   // reads columns of it), key side AS (its dV reads rows)
 };
@@ -90,6 +92,16 @@ struct Smem {
 // lanes ag and ag + 4 into different banks.
 __device__ __forceinline__ int pa(int a) { return a + ((a >> 5) << 2); }
 
+// Slot of g[token j][landmark a] in the landmark-major g tile: one row of 32
+// tokens per landmark, rotated by 4 (a / 8 + a % 8) floats (mod 32).  The
+// rotation keeps 16-byte pieces whole and spreads over all banks both the
+// 16-byte loads of landmarks a, a + 8, ..., a + 56 (sign term) and the scalar
+// stores of an mma accumulator fragment (landmarks a, a + 2, a + 4, a + 6 x 8
+// tokens).
+__device__ __forceinline__ int gt(int a, int j) {
+  return a * TJ + ((j + 4 * ((a >> 3) + (a & 7))) & (TJ - 1));
+}
+
 // Sign term for the warp's feature columns [cbase, cbase + D/8): lane (jg, ag)
 // holds 2g for tokens j0..j0+7 x landmarks al..al+7.  Per feature the lane's
 // 8 token partials are reduce-scattered over the 8 lanes of its jg group
@@ -99,7 +111,7 @@ __device__ __forceinline__ int pa(int a) { return a + ((a >> 5) << 2); }
 // landmark-side sum into dLs.
 template <int D, bool EXACT>
 __device__ __forceinline__ void sign_cols(int cbase, int j0, int al, int jg, int ag,
-                                          const float (&g2)[8][8], const float* Xt,
+                                          const f32x2 (&gp)[4][8], const float* Xt,
                                           const float* LBt, float rowg, float inv_scale,
                                           float* Stage, float* dLs) {
   constexpr int CW = D / 8;
@@ -123,26 +135,46 @@ __device__ __forceinline__ void sign_cols(int cbase, int j0, int al, int jg, int
       lb[4] = v.x; lb[5] = v.y; lb[6] = v.z; lb[7] = v.w;
     }
     float pq[8], pl[8];
-#pragma unroll
-    for (int t = 0; t < 8; ++t) pq[t] = pl[t] = 0.f;
     if (!EXACT) {
+      // gp[rp][t] = (2g of tokens 2 rp, 2 rp + 1 at landmark t); the indicator
+      // pair p multiplies it into the token pair's sums and into landmark t's
+      // (even-token, odd-token) sums
+      f32x2 PQ[4];
 #pragma unroll
-      for (int r = 0; r < 8; ++r)
+      for (int rp = 0; rp < 4; ++rp) PQ[rp] = 0ull;
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const float p = fma_sat(x[r], kBig, lb[t]);
-          pq[r] = fmaf(g2[r][t], p, pq[r]);
-          pl[t] = fmaf(g2[r][t], p, pl[t]);
+      for (int t = 0; t < 8; ++t) {
+        f32x2 PL = 0ull;
+#pragma unroll
+        for (int rp = 0; rp < 4; ++rp) {
+          const f32x2 p = pack2(fma_sat(x[2 * rp], kBig, lb[t]), fma_sat(x[2 * rp + 1], kBig, lb[t]));
+          PQ[rp] = fma2(gp[rp][t], p, PQ[rp]);
+          PL = fma2(gp[rp][t], p, PL);
         }
+        const float2 v = unpack2(PL);
+        pl[t] = v.x + v.y;
+      }
+#pragma unroll
+      for (int rp = 0; rp < 4; ++rp) {
+        const float2 v = unpack2(PQ[rp]);
+        pq[2 * rp] = v.x;
+        pq[2 * rp + 1] = v.y;
+      }
     } else {
       // exact sgn with sgn(0) = 0; l = -lb / scale (a power of two: exact)
 #pragma unroll
-      for (int r = 0; r < 8; ++r)
+      for (int t = 0; t < 8; ++t) pq[t] = pl[t] = 0.f;
+#pragma unroll
+      for (int rp = 0; rp < 4; ++rp)
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
-          const float v = sgn_times(x[r] + lb[t] * inv_scale, 0.5f * g2[r][t]);
-          pq[r] += v;
-          pl[t] += v;
+          const float2 g = unpack2(gp[rp][t]);
+          const float v0 = sgn_times(x[2 * rp] + lb[t] * inv_scale, 0.5f * g.x);
+          const float v1 = sgn_times(x[2 * rp + 1] + lb[t] * inv_scale, 0.5f * g.y);
+          pq[2 * rp] += v0;
+          pq[2 * rp + 1] += v1;
+          pl[t] += v0;
+          pl[t] += v1;
         }
     }
     // token side: halve the 8 partials three times across lanes ag ^ 4, ^ 2, ^ 1
@@ -241,6 +273,11 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
     m1_s[tid] = mdz[(size_t)bh * 2 * mp + mp + a0 + tid];
   }
   for (int e = tid; e < D * TA; e += kThreads) dLs[e] = 0.f;
+  if constexpr (kTC) {
+    // R feeds only TF32 products here: round it once (each thread its own slots)
+    __syncthreads();
+    for (int e = tid; e < TA * (D + 4); e += kThreads) Rs[e] = __uint_as_float(to_tf32(Rs[e]));
+  }
   // landmarks outside {0} u [2^-40, 2^60] force the exact path for the whole CTA;
   // then distances use scale 1 instead of 2^64
   const bool cta_exact = __syncthreads_or(bad_l) != 0;
@@ -325,8 +362,25 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
     __syncthreads();
     prefetch(b + 1);
 
+    // g and the contraction operand Z (query side) or C (key side) of one
+    // (token, landmark) pair from its dot product and kernel value
+    auto gz = [&](int j, int a, float dot, float kv, float& g2, float& zc) {
+      const bool valid = (n0 + j < N) && (a < nv);
+      float g, z;
+      if (MODE == 2) {
+        g = dot * kv * inv_lam;
+        z = kTC ? __uint_as_float(to_tf32(kv)) : kv;  // the key side's dV reads C in TF32
+      } else {
+        z = NORM ? (kv - mu_s[a]) * rs_s[a] : kv;
+        const float dp = NORM ? (dot - m0_s[a] - z * m1_s[a]) * rs_s[a] : dot;
+        g = dp * kv * inv_lam;
+      }
+      g2 = valid ? 2.f * g : 0.f;
+      zc = valid ? z : 0.f;
+    };
     if constexpr (kTC) {
-      // dot[j][a] = sum_c U[j][c] R[a][c] on the tensor cores, into the g tile
+      // dot[j][a] = sum_c U[j][c] R[a][c] on the tensor cores (R is stored
+      // TF32-rounded); g and Z straight from the accumulator fragments
       const int gq = lane >> 2, tg = lane & 3;
       const int jt = (warp >> 2) * 16, wa = (warp & 3) * 16;
       float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -340,23 +394,28 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
 #pragma unroll
         for (int n = 0; n < 2; ++n) {
           uint32_t bf[2];
-          bf[0] = to_tf32(Rs[(wa + 8 * n + gq) * (D + 4) + k0 + tg]);
-          bf[1] = to_tf32(Rs[(wa + 8 * n + gq) * (D + 4) + k0 + tg + 4]);
+          bf[0] = __float_as_uint(Rs[(wa + 8 * n + gq) * (D + 4) + k0 + tg]);
+          bf[1] = __float_as_uint(Rs[(wa + 8 * n + gq) * (D + 4) + k0 + tg + 4]);
           mma_16x8x8(acc[n], af, bf);
         }
       }
 #pragma unroll
       for (int n = 0; n < 2; ++n) {
         const int a = wa + 8 * n + 2 * tg;
-        *reinterpret_cast<float2*>(Gs + (jt + gq) * AS + pa(a)) = make_float2(acc[n][0], acc[n][1]);
-        *reinterpret_cast<float2*>(Gs + (jt + gq + 8) * AS + pa(a)) =
-            make_float2(acc[n][2], acc[n][3]);
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int j = jt + gq + 8 * hr;
+          const float2 kv2 = *reinterpret_cast<const float2*>(KVs + j * AS + a);
+          float g0, g1, z0, z1;
+          gz(j, a, acc[n][2 * hr], kv2.x, g0, z0);
+          gz(j, a + 1, acc[n][2 * hr + 1], kv2.y, g1, z1);
+          Gs[gt(a, j)] = g0;
+          Gs[gt(a + 1, j)] = g1;
+          *reinterpret_cast<float2*>(Zs + j * ZS + a) = make_float2(z0, z1);
+        }
       }
-      __syncthreads();
-    }
-
-    // ---- phase 1: thread = tokens 4 warp .. +3, landmarks 2 lane and 2 lane + 1 ----
-    {
+    } else {
+      // ---- phase 1: thread = tokens 4 warp .. +3, landmarks 2 lane and 2 lane + 1 ----
       const int jb = 4 * warp, la = 2 * lane;
       float kvv[4][2], dot[4][2];
 #pragma unroll
@@ -366,76 +425,54 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
         kvv[r][1] = k2.y;
         dot[r][0] = dot[r][1] = 0.f;
       }
-      if constexpr (kTC) {
-        // the dot came from the tensor cores
+#pragma unroll 2
+      for (int c = 0; c < D; c += 4) {
+        const float4 r0 = lds4(Rs + la * (D + 4) + c);
+        const float4 r1 = lds4(Rs + (la + 1) * (D + 4) + c);
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          const float2 dv2 = *reinterpret_cast<const float2*>(Gs + (jb + r) * AS + pa(la));
-          dot[r][0] = dv2.x;
-          dot[r][1] = dv2.y;
-        }
-      } else {
-#pragma unroll 2
-        for (int c = 0; c < D; c += 4) {
-          const float4 r0 = lds4(Rs + la * (D + 4) + c);
-          const float4 r1 = lds4(Rs + (la + 1) * (D + 4) + c);
-#pragma unroll
-          for (int r = 0; r < 4; ++r) {
-            const float4 u4 = lds4(Us + (jb + r) * (D + 4) + c);
-            dot[r][0] = fmaf(u4.x, r0.x, dot[r][0]);
-            dot[r][0] = fmaf(u4.y, r0.y, dot[r][0]);
-            dot[r][0] = fmaf(u4.z, r0.z, dot[r][0]);
-            dot[r][0] = fmaf(u4.w, r0.w, dot[r][0]);
-            dot[r][1] = fmaf(u4.x, r1.x, dot[r][1]);
-            dot[r][1] = fmaf(u4.y, r1.y, dot[r][1]);
-            dot[r][1] = fmaf(u4.z, r1.z, dot[r][1]);
-            dot[r][1] = fmaf(u4.w, r1.w, dot[r][1]);
-          }
+          const float4 u4 = lds4(Us + (jb + r) * (D + 4) + c);
+          dot[r][0] = fmaf(u4.x, r0.x, dot[r][0]);
+          dot[r][0] = fmaf(u4.y, r0.y, dot[r][0]);
+          dot[r][0] = fmaf(u4.z, r0.z, dot[r][0]);
+          dot[r][0] = fmaf(u4.w, r0.w, dot[r][0]);
+          dot[r][1] = fmaf(u4.x, r1.x, dot[r][1]);
+          dot[r][1] = fmaf(u4.y, r1.y, dot[r][1]);
+          dot[r][1] = fmaf(u4.z, r1.z, dot[r][1]);
+          dot[r][1] = fmaf(u4.w, r1.w, dot[r][1]);
         }
       }
+      float gv[2][4];
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
-        const int j = jb + r;
-        float gv[2], zv[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int a = la + h;
-          const bool valid = (n0 + j < N) && (a < nv);
-          const float kv = kvv[r][h];
-          float g, zc;
-          if (MODE == 2) {
-            g = dot[r][h] * kv * inv_lam;
-            zc = kv;
-          } else {
-            const float z = NORM ? (kv - mu_s[a]) * rs_s[a] : kv;
-            const float dp = NORM ? (dot[r][h] - m0_s[a] - z * m1_s[a]) * rs_s[a] : dot[r][h];
-            g = dp * kv * inv_lam;
-            zc = z;
-          }
-          gv[h] = valid ? 2.f * g : 0.f;
-          zv[h] = valid ? zc : 0.f;
-        }
-        *reinterpret_cast<float2*>(Gs + j * AS + pa(la)) = make_float2(gv[0], gv[1]);
-        *reinterpret_cast<float2*>(Zs + j * ZS + la) = make_float2(zv[0], zv[1]);
+        float z0, z1;
+        gz(jb + r, la, dot[r][0], kvv[r][0], gv[0][r], z0);
+        gz(jb + r, la + 1, dot[r][1], kvv[r][1], gv[1][r], z1);
+        *reinterpret_cast<float2*>(Zs + (jb + r) * ZS + la) = make_float2(z0, z1);
       }
+      st4(Gs + gt(la, jb), make_float4(gv[0][0], gv[0][1], gv[0][2], gv[0][3]));
+      st4(Gs + gt(la + 1, jb), make_float4(gv[1][0], gv[1][1], gv[1][2], gv[1][3]));
     }
     __syncthreads();
     prefetch_kv(b + 1);  // this block's kernel values are read
 
     // ---- per-token and per-landmark sums of g (the tile holds 2g) ----
     if (tid < TJ) {
-      float sacc = 0.f;
-#pragma unroll 4
-      for (int a = 0; a < TA; a += 4) {
-        const float4 v = lds4(Gs + tid * AS + pa(a));
-        sacc += (v.x + v.y) + (v.z + v.w);
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll 8
+      for (int a = 0; a < TA; a += 2) {
+        s0 += Gs[gt(a, tid)];
+        s1 += Gs[gt(a + 1, tid)];
       }
-      rowg_s[tid] = 0.5f * sacc;
+      rowg_s[tid] = 0.5f * (s0 + s1);
     } else if (tid < TJ + TA) {
       const int a = tid - TJ;
       float sacc = 0.f;
-#pragma unroll 8
-      for (int j = 0; j < TJ; ++j) sacc += Gs[j * AS + pa(a)];
+#pragma unroll
+      for (int j = 0; j < TJ; j += 4) {
+        const float4 v = lds4(Gs + gt(a, j));
+        sacc += (v.x + v.y) + (v.z + v.w);
+      }
       colg_s[a] = 0.5f * sacc;
     }
 
@@ -491,15 +528,15 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
 #pragma unroll 4
       for (int k0 = 0; k0 < TA; k0 += 8) {
         uint32_t af[4];
-        af[0] = to_tf32(Zs[(jt + gq) * ZS + k0 + tg]);
-        af[1] = to_tf32(Zs[(jt + gq + 8) * ZS + k0 + tg]);
-        af[2] = to_tf32(Zs[(jt + gq) * ZS + k0 + tg + 4]);
-        af[3] = to_tf32(Zs[(jt + gq + 8) * ZS + k0 + tg + 4]);
+        af[0] = __float_as_uint(Zs[(jt + gq) * ZS + k0 + tg]);
+        af[1] = __float_as_uint(Zs[(jt + gq + 8) * ZS + k0 + tg]);
+        af[2] = __float_as_uint(Zs[(jt + gq) * ZS + k0 + tg + 4]);
+        af[3] = __float_as_uint(Zs[(jt + gq + 8) * ZS + k0 + tg + 4]);
 #pragma unroll
         for (int n = 0; n < NCT2; ++n) {
           uint32_t bf[2];
-          bf[0] = to_tf32(Rs[(k0 + tg) * (D + 4) + wc + 8 * n + gq]);
-          bf[1] = to_tf32(Rs[(k0 + tg + 4) * (D + 4) + wc + 8 * n + gq]);
+          bf[0] = __float_as_uint(Rs[(k0 + tg) * (D + 4) + wc + 8 * n + gq]);
+          bf[1] = __float_as_uint(Rs[(k0 + tg + 4) * (D + 4) + wc + 8 * n + gq]);
           mma_16x8x8(acc[n], af, bf);
         }
       }
@@ -546,13 +583,12 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
     // ---- phase S: sign term ----
     {
       const int j0 = 8 * jg, al = 8 * ag;
-      float g2[8][8];
+      f32x2 gp[4][8];
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const float4 u = lds4(Gs + (j0 + r) * AS + pa(al));
-        const float4 v = lds4(Gs + (j0 + r) * AS + pa(al) + 4);
-        g2[r][0] = u.x; g2[r][1] = u.y; g2[r][2] = u.z; g2[r][3] = u.w;
-        g2[r][4] = v.x; g2[r][5] = v.y; g2[r][6] = v.z; g2[r][7] = v.w;
+      for (int t = 0; t < 8; ++t) {
+        const ulonglong2 u = *reinterpret_cast<const ulonglong2*>(Gs + gt(al + t, j0));
+        const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(Gs + gt(al + t, j0 + 4));
+        gp[0][t] = u.x; gp[1][t] = u.y; gp[2][t] = v.x; gp[3][t] = v.y;
       }
       if (tid < nties) {
         // the tie's g, read before the g tile becomes staging space
@@ -560,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
         const int a = (int)(t >> 12) - a0;
         const bool mine = a >= 0 && a < nv;
         tie_s[tid] = mine ? t : ~0u;
-        tieg_s[tid] = mine ? 0.5f * Gs[(int)(t & 31u) * AS + pa(a)] : 0.f;
+        tieg_s[tid] = mine ? 0.5f * Gs[gt(a, (int)(t & 31u))] : 0.f;
       }
       __syncthreads();  // g and Z tiles are free from here on (staging); sums are ready
       const float rowg = rowg_s[j0 + ag];
@@ -569,9 +605,9 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
         colg_acc1 += colg_s[al + 2 * jg + 1];
       }
       if (exact)
-        sign_cols<D, true>(warp * CW, j0, al, jg, ag, g2, Xt, LBt, rowg, inv_scale, Stage, dLs);
+        sign_cols<D, true>(warp * CW, j0, al, jg, ag, gp, Xt, LBt, rowg, inv_scale, Stage, dLs);
       else
-        sign_cols<D, false>(warp * CW, j0, al, jg, ag, g2, Xt, LBt, rowg, inv_scale, Stage, dLs);
+        sign_cols<D, false>(warp * CW, j0, al, jg, ag, gp, Xt, LBt, rowg, inv_scale, Stage, dLs);
     }
     __syncthreads();
     if (nties > 0) {
