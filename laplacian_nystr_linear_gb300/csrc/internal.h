@@ -18,6 +18,7 @@ struct Prob {
   int mp;         // nt * 64
   int nblk;       // token blocks of 64
   int Sk, Sq, Sb; // token splits of the key pass, statistics pass, backward passes
+  int Skt;        // token splits of the tensor-core key pass (0 when it is not used)
   bool norm() const { return flags & 1u; }
 };
 
@@ -44,6 +45,19 @@ inline cudaError_t allow_smem(Kern kern, size_t bytes) {
 }
 
 // ---- launchers (return the first CUDA error, cudaSuccess otherwise) -------
+// tensor-core forward passes (bf16, d = 32 or 64, m > 64): the query pass
+// reads landmark and W-hat tiles packed by run_pack_q (pack_q_floats floats);
+// the key pass writes [BH][Skt][mp][d] partials of W
+bool fwd_tc_shape(int d, int m);
+bool fwd_tc_ok(const Prob& p);
+int key_tc_splits(int BH, int m, int nblk);
+size_t pack_q_floats(const Prob& p);
+cudaError_t run_pack_q(const Prob& p, const float* L, const float* What, float* pack,
+                       cudaStream_t st);
+cudaError_t run_query_tc(const Prob& p, const void* q, const float* pack, const float* stats,
+                         void* out, float* kvout, cudaStream_t st);
+cudaError_t run_key_tc(const Prob& p, const void* k, const void* v, const float* L, float* part,
+                       float* kvout, cudaStream_t st);
 // landmarks: L [BH][m][d] f32, idx [N] int32 (may be null)
 cudaError_t run_pool(const Prob& p, const void* k, float* L, int32_t* idx, cudaStream_t st);
 

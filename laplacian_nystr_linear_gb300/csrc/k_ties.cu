@@ -21,7 +21,7 @@
 //   - sorts each column's candidate values ascending with their landmark
 //     indices (the others as +inf).
 // k_ties (many CTAs per slice, at most 64 blocks each): streams the tokens 16
-// bytes at a time, eight loads in flight per thread; a value whose key is
+// bytes at a time; a value whose key is
 // marked is looked up in the sorted column and every landmark holding it gives
 // a triple.  Triples are gathered per block in shared memory and written
 // sorted, so the corrections are applied in a fixed order.
@@ -40,7 +40,6 @@ constexpr float kLo = 9.094947017729282e-13f;        // 2^-40
 constexpr float kHi = 1.152921504606846976e18f;      // 2^60
 constexpr int kMaxBlocks = 64;                       // blocks per k_ties CTA
 constexpr int kCap = kTieRec - 1;                    // triples per record
-constexpr int kUnroll = 8;                           // 16-byte loads in flight per thread
 
 __device__ __forceinline__ bool out_of_range(float v) {
   const float a = fabsf(v);
@@ -168,21 +167,12 @@ __global__ void __launch_bounds__(kThreads) k_ties(const T* __restrict__ X,
   if (!all) {
     const int c0 = (tid % G) * V;
     const int n_lo = b0 * TJ, n_hi = min(N, b1 * TJ);
-    const int total = (n_hi - n_lo) * G;
-    for (int e0 = tid; e0 < total; e0 += kUnroll * kThreads) {
-      uint4 u[kUnroll];
-#pragma unroll
-      for (int i = 0; i < kUnroll; ++i) {
-        const int e = e0 + i * kThreads;
-        u[i] = e < total ? __ldg(reinterpret_cast<const uint4*>(Xb + (size_t)(n_lo + e / G) * D + c0))
-                         : make_uint4(0u, 0u, 0u, 0u);
-      }
-#pragma unroll
-      for (int i = 0; i < kUnroll; ++i) {
-        const int e = e0 + i * kThreads;
-        if (e >= total) break;
-        const int n = n_lo + e / G, k = n / TJ - b0, j = n % TJ;
-        const uint32_t w[4] = {u[i].x, u[i].y, u[i].z, u[i].w};
+#pragma unroll 2
+    for (int e = tid; e < (n_hi - n_lo) * G; e += kThreads) {
+      const int n = n_lo + e / G, k = n / TJ - b0, j = n % TJ;
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(Xb + (size_t)n * D + c0));
+      {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
         uint32_t xb[V];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {

@@ -100,6 +100,8 @@ static Prob make_prob(int B, int H, int N, int d, int gh, int gw, int m, float l
   p.Sk = splits_for(p.nblk, p.nt, p.BH);
   p.Sq = p.Sk;
   p.Sb = p.Sk;
+  // sized from the shape alone (the workspace query takes no dtype); used for bf16
+  p.Skt = fwd_tc_shape(d, m) ? key_tc_splits(p.BH, m, p.nblk) : 0;
   return p;
 }
 
@@ -133,7 +135,7 @@ static CtxLayout ctx_layout(int BH, int N, int d, int m, int iters, bool full) {
 
 struct WsLayout {
   size_t lite;                                 // ctx stand-in when the forward gets no ctx
-  size_t kpart, spart;                         // forward partials
+  size_t kpart, spart, fpack;                  // forward partials, packed query-pass tiles
   size_t dWhp, dLqp, dLcp, nsp, mdz;           // backward landmark-side partials
   size_t dQp, dKp, dVp;                        // backward token-side partials
   size_t dWh, dW, dLA, dL, G, XG, Tm, dA;      // backward landmark-side results
@@ -147,8 +149,9 @@ static WsLayout ws_layout(const Prob& p) {
   const size_t BH = p.BH, m = p.m, d = p.d, mp = p.mp;
   size_t o = 0;
   w.lite = o; o = align256(o + ctx_layout(p.BH, p.N, p.d, p.m, p.iters, false).total);
-  w.kpart = o; o = align256(o + BH * p.Sk * mp * d * f);
+  w.kpart = o; o = align256(o + BH * (p.Skt > p.Sk ? p.Skt : p.Sk) * mp * d * f);
   w.spart = o; o = align256(o + BH * p.Sq * 3 * mp * f);
+  w.fpack = o; o = align256(o + (p.Skt > 0 ? pack_q_floats(p) * f : 0));
   w.dWhp = o; o = align256(o + BH * p.Sb * mp * d * f);
   w.dLqp = o; o = align256(o + BH * p.Sb * mp * d * f);
   w.dLcp = o; o = align256(o + BH * p.Sb * mp * d * f);
@@ -374,8 +377,14 @@ int lapnys_fwd(const void* q, const void* k, const void* v, void* out, int B, in
     if (rc != LAPNYS_OK) return rc;
   }
   float* kpart = (float*)(wb + w.kpart);
-  CK(run_key_fwd(p, k, v, L, kpart, full ? (float*)(cb + c.C) : nullptr, stream));
-  CK(run_reduce_parts(p.BH, p.Sk, m, p.mp, d, kpart, W, stream));
+  const bool tc = fwd_tc_ok(p);
+  if (tc) {
+    CK(run_key_tc(p, k, v, L, kpart, full ? (float*)(cb + c.C) : nullptr, stream));
+    CK(run_reduce_parts(p.BH, p.Skt, m, p.mp, d, kpart, W, stream));
+  } else {
+    CK(run_key_fwd(p, k, v, L, kpart, full ? (float*)(cb + c.C) : nullptr, stream));
+    CK(run_reduce_parts(p.BH, p.Sk, m, p.mp, d, kpart, W, stream));
+  }
   const float* XT = X + (long)(iters % c.nx) * mm;
   // W-hat = X_T W
   CK(ns_mm(p, false, false, m, d, m, XT, m, c.nx * mm, W, d, (long)m * d, What, d, (long)m * d,
@@ -385,7 +394,13 @@ int lapnys_fwd(const void* q, const void* k, const void* v, void* out, int B, in
     CK(run_qstats(p, q, L, spart, stream));
     CK(run_stats_final(p, spart, stats, stream));
   }
-  CK(run_query_fwd(p, q, L, What, stats, out, full ? (float*)(cb + c.P) : nullptr, stream));
+  if (tc) {
+    float* fpack = (float*)(wb + w.fpack);
+    CK(run_pack_q(p, L, What, fpack, stream));
+    CK(run_query_tc(p, q, fpack, stats, out, full ? (float*)(cb + c.P) : nullptr, stream));
+  } else {
+    CK(run_query_fwd(p, q, L, What, stats, out, full ? (float*)(cb + c.P) : nullptr, stream));
+  }
   return LAPNYS_OK;
 }
 
@@ -433,8 +448,14 @@ int lapnys_fwd_static(const void* q, const void* k, const void* v, void* out, in
     if (rc != LAPNYS_OK) return rc;
   }
   float* kpart = (float*)(wb + w.kpart);
-  CK(run_key_fwd(p, k, v, L, kpart, nullptr, stream));
-  CK(run_reduce_parts(p.BH, p.Sk, m, p.mp, d, kpart, W, stream));
+  const bool tc = fwd_tc_ok(p);
+  if (tc) {
+    CK(run_key_tc(p, k, v, L, kpart, nullptr, stream));
+    CK(run_reduce_parts(p.BH, p.Skt, m, p.mp, d, kpart, W, stream));
+  } else {
+    CK(run_key_fwd(p, k, v, L, kpart, nullptr, stream));
+    CK(run_reduce_parts(p.BH, p.Sk, m, p.mp, d, kpart, W, stream));
+  }
   const float* XT = X + (long)(iters % c.nx) * mm;
   CK(ns_mm(p, false, false, m, d, m, XT, m, c.nx * mm, W, d, (long)m * d, What, d, (long)m * d,
            nullptr, d, 0, 1.f, 0.f, stream));
@@ -443,7 +464,13 @@ int lapnys_fwd_static(const void* q, const void* k, const void* v, void* out, in
     CK(run_qstats(p, q, L, spart, stream));
     CK(run_stats_final(p, spart, stats, stream));
   }
-  CK(run_query_fwd(p, q, L, What, stats, out, nullptr, stream));
+  if (tc) {
+    float* fpack = (float*)(wb + w.fpack);
+    CK(run_pack_q(p, L, What, fpack, stream));
+    CK(run_query_tc(p, q, fpack, stats, out, nullptr, stream));
+  } else {
+    CK(run_query_fwd(p, q, L, What, stats, out, nullptr, stream));
+  }
   return LAPNYS_OK;
 }
 

@@ -82,6 +82,29 @@ def test_forward_intermediates(wname):
     assert rel(c["C"][0, 0], s["C"].T) < 1e-6
 
 
+# bf16 with d = 32 / 64 and m > 64 takes the tensor-core forward passes (tcgen05,
+# 128-row tiles): ragged token counts, landmark counts off the 64 / 128 tiles
+TC_FWD = [
+    _small("tc_m100", dtype="bf16", d=64, grid_h=20, grid_w=20, m=100, iters=8),
+    _small("tc_m81_norm", dtype="bf16", d=32, grid_h=18, grid_w=18, m=81, iters=8, norm=True),
+    _small("tc_m144_batch", dtype="bf16", d=64, grid_h=24, grid_w=24, m=144, iters=8, B=2, H=2),
+    _small("tc_mN_tied", dtype="bf16", d=64, grid_h=16, grid_w=16, m=256, iters=6, tied=True),
+]
+
+
+@pytest.mark.parametrize("w", TC_FWD, ids=lambda w: w.name)
+def test_tensor_core_forward_intermediates(w):
+    inp = random_inputs(31 + w.m, w.B, w.H, w.N, w.d, w.dtype, tied=w.tied)
+    g = gpu_run(w, inp, backward=True)
+    o = oracle_run(w, inp, backward=True)
+    print(w.name, compare(w, g, o, backward=True))
+    for (b, h), s in o["saved"].items():
+        c = g["ctx"]
+        assert rel(c["W"][b, h], s["W"]) < 1e-3          # C V with C rounded to TF32
+        assert rel(c["P"][b, h], s["P"]) < 1e-6          # kernel values stored as computed
+        assert rel(c["C"][b, h], s["C"].T) < 1e-6
+
+
 def test_norm_statistics():
     w = WORKLOADS["pvt3"]
     inp = make_inputs(w)
