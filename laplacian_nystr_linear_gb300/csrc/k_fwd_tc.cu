@@ -9,11 +9,11 @@
 // Methodology 1; Arabic summary 2a) and the Nystrom product read as
 // O = k(Q, L) A^+ (k(L, K) V) ("SOFT" review, Proposed method).
 //
-// The L1 distances run on the FP32 pipe: each thread holds an 8 x 4 block of
-// distances (summed over the features in ascending order) and reads both
-// operands from feature-major tiles, one 16-byte load per four values.  The
-// kernel values, rounded to TF32, go straight into the K-major operand layout
-// of the MMA: a thread's 8 x 4 block is exactly one core matrix (8 rows x 16
+// The L1 distances run on the FP32 pipe: each of 512 threads holds a 4 x 4
+// block of distances (summed over the features in ascending order) and reads
+// both operands from feature-major tiles, one 16-byte load per four values.
+// The kernel values, rounded to TF32, go straight into the K-major operand
+// layout of the MMA: a thread's 4 x 4 block is half a core matrix (8 rows x 16
 // bytes).  One thread then issues the tile's tcgen05.mma (kind::tf32, M = 128)
 // into a TMEM accumulator and commits them to an mbarrier while every warp
 // moves on to the next tile's distances; a shared-memory operand buffer is
@@ -45,6 +45,7 @@ constexpr uint32_t kSbo = 128;                  // A: 8-row groups 128 bytes apa
 constexpr uint32_t kLboA = (QM / 8) * kSbo + 16;  // A: 4-wide K groups 2064 bytes apart (bank spread)
 constexpr uint32_t kTileA = (TL / 4) * kLboA;   // one A tile (M = 128, K = 64)
 constexpr uint32_t kSboVB = 144;                // key-pass B (V^T): 8-row groups 144 bytes apart
+constexpr int NTH = 512;                        // threads per CTA (4 warps per SM sub-partition)
 
 template <int D>
 struct QSmem {
@@ -75,7 +76,12 @@ struct KSmem {
 
 __host__ __device__ constexpr uint32_t tmem_cols(int d) { return d < 32 ? 32u : (uint32_t)d; }
 
-__device__ __forceinline__ float tf32f(float x) { return __uint_as_float(to_tf32(x)); }
+// x rounded to the nearest TF32 value, halfway cases away from zero (as
+// cvt.rna.tf32.f32): add half a TF32 ulp to the magnitude bits and clear the
+// 13 low bits; a carry into the exponent is the correct rounding.  Finite x.
+__device__ __forceinline__ float tf32f(float x) {
+  return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
+}
 
 __device__ __forceinline__ void flag_timeout(int* err, bool ok) {
   if (!ok) atomicOr(err, 1);
@@ -133,7 +139,7 @@ struct QArgs {
 };
 
 template <int D, bool NORM>
-__global__ void __launch_bounds__(kThreads, 1) k_query_tc(QArgs a) {
+__global__ void __launch_bounds__(NTH, 1) k_query_tc(QArgs a) {
   using S = QSmem<D>;
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ __align__(8) uint64_t full[3];   // tile operands landed (bulk copies)
@@ -141,7 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_query_tc(QArgs a) {
   __shared__ uint32_t tmem_s;
   float* Xt = reinterpret_cast<float*>(sm + S::Xt);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ty = tid >> 4, tx = tid & 15;  // queries 8 ty .. 8 ty + 7, landmarks 4 tx .. 4 tx + 3
+  const int ty = tid >> 4, tx = tid & 15;  // queries 4 ty .. 4 ty + 3, landmarks 4 tx .. 4 tx + 3
   constexpr uint32_t kCols = tmem_cols(D);
   const uint32_t id = tc::idesc_tf32(QM, D);
 
@@ -170,7 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_query_tc(QArgs a) {
     if (item >= a.items) return;
     const int bh = item / a.nb, j0 = (item % a.nb) * QM;
     constexpr int CH = D / 8;  // 16-byte pieces per row
-    for (int e = tid; e < QM * CH; e += kThreads) {
+    for (int e = tid; e < QM * CH; e += NTH) {
       const int j = e % QM, ch = e / QM;
       const bool ok = j0 + j < a.N;
       const __nv_bfloat16* src = a.Q + ((size_t)bh * a.N + (ok ? j0 + j : 0)) * D + 8 * ch;
@@ -189,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_query_tc(QArgs a) {
     {
       // raw rows -> feature-major f32 (lanes take consecutive queries)
       constexpr int CH = D / 8;
-      for (int e = tid; e < QM * CH; e += kThreads) {
+      for (int e = tid; e < QM * CH; e += NTH) {
         const int j = e % QM, ch = e / QM;
         float f[8];
         bf16x8(*reinterpret_cast<const uint4*>(sm + S::Raw + j * S::kRow + 16 * ch), f);
@@ -213,21 +219,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_query_tc(QArgs a) {
         }
       }
       const float* Lt = reinterpret_cast<const float*>(sm + S::Lt + (g & 1) * S::kTileB);
-      float acc[8][4];
+      float acc[4][4];
 #pragma unroll
-      for (int r = 0; r < 8; ++r)
+      for (int r = 0; r < 4; ++r)
 #pragma unroll
         for (int s = 0; s < 4; ++s) acc[r][s] = 0.f;
       {
-        const float* xp = Xt + 8 * ty;
+        const float* xp = Xt + 4 * ty;
         const float* lp = Lt + 4 * tx;
-#pragma unroll 4
+#pragma unroll 8
         for (int c = 0; c < D; ++c) {
-          const float4 x0 = lds4(xp + c * QM), x1 = lds4(xp + c * QM + 4), l = lds4(lp + c * TL);
-          const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+          const float4 x0 = lds4(xp + c * QM), l = lds4(lp + c * TL);
+          const float x[4] = {x0.x, x0.y, x0.z, x0.w};
           const float lv[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
-          for (int r = 0; r < 8; ++r)
+          for (int r = 0; r < 4; ++r)
 #pragma unroll
             for (int s = 0; s < 4; ++s) acc[r][s] += fabsf(x[r] - lv[s]);
         }
@@ -246,10 +252,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_query_tc(QArgs a) {
             rs[s] = ok ? __ldg(st + 2 * a.m + ab + s) : 0.f;
           }
         }
-        uint8_t* pa = sm + S::Pa + (g & 1) * kTileA + tx * kLboA + ty * kSbo;
+        uint8_t* pa = sm + S::Pa + (g & 1) * kTileA + tx * kLboA + (ty >> 1) * kSbo + (ty & 1) * 64;
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          const int j = j0 + 8 * ty + r;
+        for (int r = 0; r < 4; ++r) {
+          const int j = j0 + 4 * ty + r;
           float pv[4], z[4];
 #pragma unroll
           for (int s = 0; s < 4; ++s) {
@@ -280,11 +286,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_query_tc(QArgs a) {
       }
     }
     // the item's accumulator: lane quarter w % 4 holds queries 32 (w % 4) .., the
-    // warp pair w, w + 4 splits the columns
+    // four warps w, w + 4, w + 8, w + 12 split the columns
     flag_timeout(a.err, tc::mbar_wait(tc::smem_u32(&mdone[(g - 1) & 1]), ((g - 1) >> 1) & 1));
     tc::fence_after();
     {
-      constexpr int HC = D / 2;
+      constexpr int HC = D / 4;
       const int q = warp & 3, h = warp >> 2;
       uint32_t v[HC];
       tc::tmem_ld<HC>(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(h * HC), v);
@@ -329,7 +335,7 @@ struct KArgs {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) k_key_tc(KArgs a) {
+__global__ void __launch_bounds__(NTH, 1) k_key_tc(KArgs a) {
   using S = KSmem<D>;
   extern __shared__ __align__(1024) uint8_t sm[];
   __shared__ __align__(8) uint64_t mdone[2];  // MMAs reading operand buffer b completed
@@ -337,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_key_tc(KArgs a) {
   float* Lt = reinterpret_cast<float*>(sm + S::Lt);
   float* Kt = reinterpret_cast<float*>(sm + S::Kt);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ty = tid >> 4, tx = tid & 15;  // landmarks 8 ty .. 8 ty + 7, tokens 4 tx .. 4 tx + 3
+  const int ty = tid >> 4, tx = tid & 15;  // landmarks 4 ty .. 4 ty + 3, tokens 4 tx .. 4 tx + 3
   const int lt = blockIdx.x, sp = blockIdx.y, bh = blockIdx.z;
   const int a0 = lt * QM;
   constexpr uint32_t kCols = tmem_cols(D);
@@ -351,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_key_tc(KArgs a) {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   // the CTA's landmarks, feature-major (zero past m)
-  for (int e = tid; e < QM * D; e += kThreads) {
+  for (int e = tid; e < QM * D; e += NTH) {
     const int al = e % QM, c = e / QM;
     Lt[c * QM + al] = a0 + al < a.m ? __ldg(a.L + ((size_t)bh * a.m + a0 + al) * D + c) : 0.f;
   }
@@ -367,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_key_tc(KArgs a) {
     const int n0 = b * TL;
     constexpr int CH = D / 8;
     uint8_t* rb = sm + S::Raw + buf * S::kRawBuf;
-    for (int e = tid; e < 2 * TL * CH; e += kThreads) {
+    for (int e = tid; e < 2 * TL * CH; e += NTH) {
       const int which = e / (TL * CH), rem = e % (TL * CH), j = rem % TL, ch = rem / TL;
       const bool ok = n0 + j < a.N;
       const __nv_bfloat16* src = (which ? Vb : Kb) + (size_t)(ok ? n0 + j : 0) * D + 8 * ch;
@@ -387,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_key_tc(KArgs a) {
       const uint8_t* rb = sm + S::Raw + buf * S::kRawBuf;
       constexpr int CH = D / 8;
       // keys -> feature-major f32 (lanes take consecutive tokens)
-      for (int e = tid; e < TL * CH; e += kThreads) {
+      for (int e = tid; e < TL * CH; e += NTH) {
         const int j = e % TL, ch = e / TL;
         float f[8];
         bf16x8(*reinterpret_cast<const uint4*>(rb + j * S::kRow + 16 * ch), f);
@@ -396,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_key_tc(KArgs a) {
       }
       // values -> B operand (row = feature, k = token); lanes: 8 feature groups x 4 tokens
       uint8_t* vb = sm + S::Vb + buf * S::kTileB;
-      for (int e = tid; e < TL * CH; e += kThreads) {
+      for (int e = tid; e < TL * CH; e += NTH) {
         const int ch = e % CH, j = e / CH;
         float f[8];
         bf16x8(*reinterpret_cast<const uint4*>(rb + (TL + j) * S::kRow + 16 * ch), f);
@@ -408,50 +414,48 @@ __global__ void __launch_bounds__(kThreads, 1) k_key_tc(KArgs a) {
     __syncthreads();
     prefetch(b + 1, buf ^ 1);
 
-    float acc[8][4];
+    float acc[4][4];
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
+    for (int r = 0; r < 4; ++r)
 #pragma unroll
       for (int s = 0; s < 4; ++s) acc[r][s] = 0.f;
     {
-      const float* lp = Lt + 8 * ty;
+      const float* lp = Lt + 4 * ty;
       const float* xp = Kt + 4 * tx;
-#pragma unroll 4
+#pragma unroll 8
       for (int c = 0; c < D; ++c) {
-        const float4 l0 = lds4(lp + c * QM), l1 = lds4(lp + c * QM + 4), x = lds4(xp + c * TL);
-        const float lv[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
+        const float4 l0 = lds4(lp + c * QM), x = lds4(xp + c * TL);
+        const float lv[4] = {l0.x, l0.y, l0.z, l0.w};
         const float xv[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-        for (int r = 0; r < 8; ++r)
+        for (int r = 0; r < 4; ++r)
 #pragma unroll
           for (int s = 0; s < 4; ++s) acc[r][s] += fabsf(xv[s] - lv[r]);
       }
     }
     {
       const int n0 = b * TL;
-      float cv[8][4];
+      float cv[4][4];
 #pragma unroll
-      for (int r = 0; r < 8; ++r)
+      for (int r = 0; r < 4; ++r)
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
-          const bool ok = (a0 + 8 * ty + r < a.m) && (n0 + 4 * tx + s < a.N);
+          const bool ok = (a0 + 4 * ty + r < a.m) && (n0 + 4 * tx + s < a.N);
           cv[r][s] = ok ? exp2f(acc[r][s] * a.ns) : 0.f;
         }
-      if (a.kvout != nullptr && a0 + 8 * ty < a.mp) {
+      if (a.kvout != nullptr && a0 + 4 * ty < a.mp) {
         // keep the kernel values for the backward: token-major rows
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
           const int j = n0 + 4 * tx + s;
-          if (j < a.N) {
-            float* o = a.kvout + ((size_t)bh * a.N + j) * a.mp + a0 + 8 * ty;
-            st4(o, make_float4(cv[0][s], cv[1][s], cv[2][s], cv[3][s]));
-            st4(o + 4, make_float4(cv[4][s], cv[5][s], cv[6][s], cv[7][s]));
-          }
+          if (j < a.N)
+            st4(a.kvout + ((size_t)bh * a.N + j) * a.mp + a0 + 4 * ty,
+                make_float4(cv[0][s], cv[1][s], cv[2][s], cv[3][s]));
         }
       }
-      uint8_t* ca = sm + S::Ca + buf * kTileA + tx * kLboA + ty * kSbo;
+      uint8_t* ca = sm + S::Ca + buf * kTileA + tx * kLboA + (ty >> 1) * kSbo + (ty & 1) * 64;
 #pragma unroll
-      for (int r = 0; r < 8; ++r)
+      for (int r = 0; r < 4; ++r)
         *reinterpret_cast<float4*>(ca + r * 16) =
             make_float4(tf32f(cv[r][0]), tf32f(cv[r][1]), tf32f(cv[r][2]), tf32f(cv[r][3]));
     }
@@ -471,11 +475,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_key_tc(KArgs a) {
     }
   }
   // partial W of this range: lane quarter w % 4 holds landmarks 32 (w % 4) .., the
-  // warp pair w, w + 4 splits the columns
+  // four warps w, w + 4, w + 8, w + 12 split the columns
   if (i > 0) flag_timeout(a.err, tc::mbar_wait(tc::smem_u32(&mdone[(i - 1) & 1]), ((i - 1) >> 1) & 1));
   tc::fence_after();
   {
-    constexpr int HC = D / 2;
+    constexpr int HC = D / 4;
     const int q = warp & 3, h = warp >> 2;
     uint32_t v[HC];
     tc::tmem_ld<HC>(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(h * HC), v);
@@ -558,7 +562,7 @@ static cudaError_t query_tc_t(const Prob& p, const void* q, const float* pack, c
   a.items = a.nb * p.BH;
   a.ns = p.ns;
   const int grid = a.items < sm_count() ? a.items : sm_count();
-  return launch("query_fwd", k_query_tc<D, NORM>, dim3(grid), dim3(kThreads), smem, st, a);
+  return launch("query_fwd", k_query_tc<D, NORM>, dim3(grid), dim3(NTH), smem, st, a);
 }
 
 cudaError_t run_query_tc(const Prob& p, const void* q, const float* pack, const float* stats,
@@ -586,7 +590,7 @@ static cudaError_t key_tc_t(const Prob& p, const void* k, const void* v, const f
   a.N = p.N; a.m = p.m; a.mp = p.mp; a.S = p.Skt; a.nblk = p.nblk;
   a.ns = p.ns;
   const int nt = (p.m + QM - 1) / QM;
-  return launch("key_fwd", k_key_tc<D>, dim3(nt, p.Skt, p.BH), dim3(kThreads), smem, st, a);
+  return launch("key_fwd", k_key_tc<D>, dim3(nt, p.Skt, p.BH), dim3(NTH), smem, st, a);
 }
 
 cudaError_t run_key_tc(const Prob& p, const void* k, const void* v, const float* L, float* part,
