@@ -90,6 +90,27 @@ def fp32_pipe_ops(w):
             "bwd_query": (4 if tc else 6) * nmd, "bwd_key": (4 if tc else 6) * nmd}
 
 
+def measured_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch of `kernel` from the ncu capture recorded in
+    profiles/traffic_<workload>.json, or None when there is no record for it
+    or its source file has changed since the counters were taken."""
+    import hashlib
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles",
+                        f"traffic_{workload}.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        if rec.get("kernel") != kernel:
+            return None
+        src = os.path.join(os.path.dirname(os.path.abspath(__file__)), rec["source"])
+        with open(src, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != rec["source_sha256"]:
+                return None
+        return float(rec["bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def max_over_ranks(x: float, world: int, device) -> float:
     """Largest value over all ranks (step times: the slowest rank sets the pace)."""
     if world == 1:
@@ -306,10 +327,11 @@ def run_ours(args, rank, world, local_rank):
     achieved = per_launch_ops[dom] / (dom_ms / 1e3) / 1e12
     total_ops = sum(ops.values())
     pipe = fp32_pipe_ops(w)
+    traffic = measured_traffic(w.name, dom)
     roofline = {
         "bound": "alu", "kernel": dom, "achieved": achieved, "peak": ALU_PEAK_TOPS,
         "unit": "Tlaneop/s", "frac": achieved / ALU_PEAK_TOPS,
-        "traffic": None,
+        "traffic": traffic,
         "peak_source": "152 SMs x 128 FP32 lanes x 2070 MHz",
         "step_frac": total_ops / (ms / 1e3) / 1e12 / ALU_PEAK_TOPS,
         "fp32_pipe_frac": pipe[dom] / (dom_ms / 1e3) / 1e12 / ALU_PEAK_TOPS,
