@@ -249,6 +249,57 @@ static int ns_forward_large(const Prob& p, const float* A, float* X, float* Y, i
 using namespace lapnys;
 
 // ---------------------------------------------------------------------------
+// Side stream: the Newton-Schulz kernels of a slice set fill one cluster of
+// 1-2 SMs per slice (64 of 152 SMs for the benchmark), while the key-side
+// backward does not depend on their reverse (it needs dW, not dA).  lapnys_bwd
+// therefore runs the solver's reverse and the gram backward on a per-device
+// stream of the highest priority (its clusters get their SMs first) and the
+// key-side tile kernel on the caller's stream, joined by events.  (The
+// forward's key pass could run beside the forward iteration the same way, but
+// measured no faster: both slow each other down by about what the overlap
+// saves.)  Enqueueing is serialised per device so the shared events stay
+// consistent.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr int kMaxSideDevices = 256;
+struct Side {
+  cudaStream_t hi = nullptr;
+  cudaEvent_t ev[2] = {nullptr, nullptr};
+  std::mutex mu;
+};
+Side g_side[kMaxSideDevices];
+std::mutex g_side_init_mu;
+
+// the current device's side stream and events, created on first use; null if
+// they cannot be created (the caller then stays on one stream)
+Side* side() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxSideDevices) return nullptr;
+  Side& sd = g_side[dev];
+  std::lock_guard<std::mutex> lock(g_side_init_mu);
+  if (sd.hi == nullptr) {
+    int least = 0, greatest = 0;
+    if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) return nullptr;
+    for (int i = 0; i < 2; ++i)
+      if (sd.ev[i] == nullptr && cudaEventCreateWithFlags(&sd.ev[i], cudaEventDisableTiming) != cudaSuccess)
+        return nullptr;
+    cudaStream_t s = nullptr;
+    if (cudaStreamCreateWithPriority(&s, cudaStreamNonBlocking, greatest) != cudaSuccess)
+      return nullptr;
+    sd.hi = s;
+  }
+  return &sd;
+}
+
+// make `to` wait for everything enqueued on `from` so far
+cudaError_t join(cudaStream_t to, cudaStream_t from, cudaEvent_t ev) {
+  cudaError_t e = cudaEventRecord(ev, from);
+  if (e != cudaSuccess) return e;
+  return cudaStreamWaitEvent(to, ev, 0);
+}
+}  // namespace
+
+// ---------------------------------------------------------------------------
 // Built-in forward scratch for callers that cannot allocate device memory.
 // 32 MiB of device memory per GPU that loads this library, held until exit.
 // Host code must not hand the array's name to a kernel (on the host it is a
@@ -548,50 +599,59 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
   CK(run_bwd_pair(p, 1, qa, stream));
   if (!p.norm()) CK(run_reduce_parts(p.BH, p.Sb, m, p.mp, d, dWhp, dWh, stream));
 
-  // ---- W-hat = X_T W and the Newton-Schulz iteration ----
+  // ---- G = dLoss/dX_T = dW-hat W^T and dW = X_T^T dW-hat ----
   const float* XT = X + (long)iters * mm;
   const long xs = (long)(iters + 1) * mm;
   const long ys = (long)c.ny * mm;
   if (m <= kTile) {
-    // G = dLoss/dX_T = dW-hat W^T ;  dW = X_T^T dW-hat
     CK(run_bgemm(false, true, p.BH, m, m, d, dWh, d, md, W, d, md, G, m, mm, nullptr, m, 0, 1.f,
                  0.f, stream));
     CK(run_bgemm(true, false, p.BH, m, d, m, XT, m, xs, dWh, d, md, dW, d, md, nullptr, d, 0, 1.f,
                  0.f, stream));
-    CK(run_ns_bwd_small(p, A, alpha, X, Y, G, dA, stream));
   } else {
-    // Exact reverse of the forward's own products (Y_t = A X_t, then X_t Y_t).
-    // The unconverged directions grow by about 2 per step in this recursion, so
-    // it must not lean on X_t commuting with A: in fp32 that shortcut diverges.
-    // G = dLoss/dX_T = dW-hat W^T ;  dW = X_T^T dW-hat
     CK(ns_mm(p, false, true, m, m, d, dWh, d, md, W, d, md, G, m, mm, nullptr, m, 0, 1.f, 0.f,
              stream));
     CK(ns_mm(p, true, false, m, d, m, XT, m, xs, dWh, d, md, dW, d, md, nullptr, d, 0, 1.f, 0.f,
              stream));
-    if (iters == 0) CK(run_zero(dA, (size_t)p.BH * mm, stream));
+  }
+
+  // ---- the Newton-Schulz reverse and the gram backward, on the side stream
+  // (they need G; the key side below needs only dW) ----
+  Side* sd = side();
+  std::unique_lock<std::mutex> lock;
+  if (sd) lock = std::unique_lock<std::mutex>(sd->mu);
+  const cudaStream_t ss = sd ? sd->hi : stream;
+  if (sd) CK(join(ss, stream, sd->ev[0]));
+  if (m <= kTile) {
+    CK(run_ns_bwd_small(p, A, alpha, X, Y, G, dA, ss));
+  } else {
+    // Exact reverse of the forward's own products (Y_t = A X_t, then X_t Y_t).
+    // The unconverged directions grow by about 2 per step in this recursion, so
+    // it must not lean on X_t commuting with A: in fp32 that shortcut diverges.
+    if (iters == 0) CK(run_zero(dA, (size_t)p.BH * mm, ss));
     float* Sc = G;
     if (ns_cluster_ok(m))  // the whole reverse in one launch; G ends as dLoss/dX_0
       CK(run_ns_cluster(p, true, A, const_cast<float*>(X), const_cast<float*>(Y), c.nx, c.ny, G,
-                        XG, Tm, dA, stream));
+                        XG, Tm, dA, ss));
     for (int t = ns_cluster_ok(m) ? -1 : iters - 1; t >= 0; --t) {
       const float* Xt = X + (long)t * mm;
       const float* Yt = Y + (long)t * mm;
       // XG = X_t^T G
       CK(ns_mm(p, true, false, m, m, m, Xt, m, xs, Sc, m, mm, XG, m, mm, nullptr, m, 0, 1.f, 0.f,
-               stream));
+               ss));
       // dA = dA - XG X_t^T   (the first step initialises dA)
       CK(ns_mm(p, false, true, m, m, m, XG, m, mm, Xt, m, xs, dA, m, mm, dA, m, mm, -1.f,
-               t == iters - 1 ? 0.f : 1.f, stream));
+               t == iters - 1 ? 0.f : 1.f, ss));
       // Tm = 2 G - G Y_t^T
       CK(ns_mm(p, false, true, m, m, m, Sc, m, mm, Yt, m, ys, Tm, m, mm, Sc, m, mm, -1.f, 2.f,
-               stream));
+               ss));
       // G = Tm - A^T XG
       CK(ns_mm(p, true, false, m, m, m, A, m, mm, XG, m, mm, Sc, m, mm, Tm, m, mm, -1.f, 1.f,
-               stream));
+               ss));
     }
-    CK(run_alpha_bwd(p, A, alpha, Sc, dA, stream));
+    CK(run_alpha_bwd(p, A, alpha, Sc, dA, ss));
   }
-  CK(run_gram_bwd(p, L, A, dA, dLA, stream));
+  CK(run_gram_bwd(p, L, A, dA, dLA, ss));
 
   // ---- key side ----
   BwdArgs ka;
@@ -600,6 +660,7 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
   ka.tok_part = dKp; ka.tok_part2 = dVp; ka.lm_part = dLcp; ka.ties = ties_k;
   ka.kv = (const float*)(cb + c.C);
   CK(run_bwd_pair(p, 2, ka, stream));
+  if (sd) CK(join(stream, ss, sd->ev[1]));
   CK(run_reduce_dl(p, dLqp, dLcp, dLA, dL, stream));
   CK(run_finalize(p, dQp, dKp, dVp, dL, dq, dk, dv, stream));
   return LAPNYS_OK;
