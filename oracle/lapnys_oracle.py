@@ -1,4 +1,5 @@
-"""Plain, slow, fp64 CPU oracle for Laplacian-kernel Nystrom attention.
+"""Plain, slow, fp64 CPU oracle for Laplacian-kernel Nystrom attention, and
+for its Gaussian-kernel (SOFT) variant.
 
 TEST INFRASTRUCTURE.  Only the tests, the smoke check and the benchmark's CPU
 baseline may import this module.  It shares no code with the CUDA library and
@@ -14,7 +15,8 @@ Sources (page title, then section / equation):
   [SOFT]   "[Paper review] SOFT: Softmax-free Transformer with Linear
            Complexity", Proposed method: S-hat = P^T A^+ P, A_0 = alpha A,
            A_{k+1} = 2 A_k - A_k A A_k, bottleneck tokens by average pooling,
-           kernel used "without further normalisation".
+           kernel used "without further normalisation"; the attention there is
+           a symmetric, [0, 1]-valued Gaussian kernel exp(Q (-) K).
 
 Every step follows those passages in their order; where they are silent the
 reading taken is stated next to the step.  The method is an approximation with a
@@ -30,6 +32,10 @@ Per (b, h) slice, with Q, K, V in R^{N x d}, m landmarks and T iterations:
   P      = k(Q, L)  (N x m);  Z = P, or Z = (P - mu) / sqrt(sigma^2 + eta)
   O      = Z W-hat
 The backward pass is reverse-mode differentiation of exactly these steps.
+
+kernel="gauss" replaces k by the Gaussian kernel of [SOFT], read (the page
+prints no scale) as k(x, y) = exp(-||x - y||_2^2 / lam) with the same lam;
+everything else is unchanged.
 """
 from __future__ import annotations
 
@@ -56,6 +62,36 @@ def l1_distances(X: np.ndarray, Y: np.ndarray) -> np.ndarray:
 
 def laplacian_kernel(X: np.ndarray, Y: np.ndarray, lam: float) -> np.ndarray:
     return np.exp(-l1_distances(X, Y) / lam)
+
+
+# --------------------------------------------------------------------------
+# Gaussian kernel  [SOFT Proposed method: symmetric, [0, 1]-valued Gaussian
+#  kernel attention; reading: k(x, y) = exp(-||x - y||_2^2 / lam)]
+# --------------------------------------------------------------------------
+def sq_distances(X: np.ndarray, Y: np.ndarray) -> np.ndarray:
+    """D[i, j] = sum_c (X[i, c] - Y[j, c])^2, by direct broadcasting (chunked)."""
+    X = np.asarray(X, dtype=np.float64)
+    Y = np.asarray(Y, dtype=np.float64)
+    out = np.empty((X.shape[0], Y.shape[0]))
+    rows = max(1, (1 << 22) // max(1, Y.shape[0] * X.shape[1]))
+    for s in range(0, X.shape[0], rows):
+        out[s:s + rows] = ((X[s:s + rows, None, :] - Y[None, :, :]) ** 2).sum(axis=-1)
+    return out
+
+
+def gaussian_kernel(X: np.ndarray, Y: np.ndarray, lam: float) -> np.ndarray:
+    return np.exp(-sq_distances(X, Y) / lam)
+
+
+KERNELS = ("laplace", "gauss")
+
+
+def kernel_matrix(X: np.ndarray, Y: np.ndarray, lam: float, kernel: str = "laplace") -> np.ndarray:
+    if kernel == "laplace":
+        return laplacian_kernel(X, Y, lam)
+    if kernel == "gauss":
+        return gaussian_kernel(X, Y, lam)
+    raise ValueError(f"unknown kernel {kernel!r}")
 
 
 # --------------------------------------------------------------------------
@@ -92,8 +128,8 @@ def pool_landmarks(K: np.ndarray, idx: np.ndarray, m: int) -> np.ndarray:
 # Readings: eps only on A's diagonal; alpha = 1 / (|A|_1 |A|_inf) on A including
 # eps I; "iters" = T updates after X_0, returning X_T.
 # --------------------------------------------------------------------------
-def landmark_matrix(L: np.ndarray, lam: float, eps: float) -> np.ndarray:
-    return laplacian_kernel(L, L, lam) + eps * np.eye(L.shape[0])
+def landmark_matrix(L: np.ndarray, lam: float, eps: float, kernel: str = "laplace") -> np.ndarray:
+    return kernel_matrix(L, L, lam, kernel) + eps * np.eye(L.shape[0])
 
 
 def ns_scale(A: np.ndarray):
@@ -139,22 +175,22 @@ def feature_map(P: np.ndarray, norm: bool):
 # forward  [SOFT Proposed method: S-hat = P^T A^+ P, read for separate Q and K as
 #  O = k(Q, L) A^+ (k(L, K) V), no row normalisation]
 # --------------------------------------------------------------------------
-def forward_slice(q, k, v, grid_h, grid_w, m, lam, eps, iters, norm=False):
+def forward_slice(q, k, v, grid_h, grid_w, m, lam, eps, iters, norm=False, kernel="laplace"):
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
     idx = pool_index(grid_h, grid_w, m)
     L = pool_landmarks(k, idx, m)
-    A = landmark_matrix(L, lam, eps)
+    A = landmark_matrix(L, lam, eps, kernel)
     X, Y = newton_schulz(A, iters)
-    C = laplacian_kernel(L, k, lam)
+    C = kernel_matrix(L, k, lam, kernel)
     W = C @ v
     What = X[-1] @ W
-    P = laplacian_kernel(q, L, lam)
+    P = kernel_matrix(q, L, lam, kernel)
     Z, stats = feature_map(P, norm)
     O = Z @ What
     saved = dict(q=q, k=k, v=v, idx=idx, L=L, A=A, X=X, Y=Y, C=C, W=W, What=What,
-                 P=P, Z=Z, stats=stats, lam=lam, eps=eps, m=m, norm=norm)
+                 P=P, Z=Z, stats=stats, lam=lam, eps=eps, m=m, norm=norm, kernel=kernel)
     return O, saved
 
 
@@ -168,24 +204,31 @@ def _sgn(x):
     return np.sign(x)
 
 
-def _kernel_grad_x(G, X, Y, lam):
+def _kernel_grad_x(G, X, Y, lam, kernel="laplace"):
     """For K = k(X, Y) and upstream G_ij = dLoss/dK_ij * K_ij, return dLoss/dX.
 
-    dK_ij/dX_ic = -(K_ij / lam) sgn(X_ic - Y_jc).
+    Laplacian: dK_ij/dX_ic = -(K_ij / lam) sgn(X_ic - Y_jc).
+    Gaussian:  dK_ij/dX_ic = -(2 K_ij / lam) (X_ic - Y_jc).
     """
     dX = np.zeros_like(X)
     for c in range(X.shape[1]):
-        S = _sgn(X[:, c][:, None] - Y[:, c][None, :])
-        dX[:, c] = -(G * S).sum(axis=1) / lam
+        Dc = X[:, c][:, None] - Y[:, c][None, :]
+        if kernel == "gauss":
+            dX[:, c] = -2.0 * (G * Dc).sum(axis=1) / lam
+        else:
+            dX[:, c] = -(G * _sgn(Dc)).sum(axis=1) / lam
     return dX
 
 
-def _kernel_grad_y(G, X, Y, lam):
+def _kernel_grad_y(G, X, Y, lam, kernel="laplace"):
     """Same as _kernel_grad_x but with respect to the second argument Y."""
     dY = np.zeros_like(Y)
     for c in range(Y.shape[1]):
-        S = _sgn(X[:, c][:, None] - Y[:, c][None, :])
-        dY[:, c] = (G * S).sum(axis=0) / lam
+        Dc = X[:, c][:, None] - Y[:, c][None, :]
+        if kernel == "gauss":
+            dY[:, c] = 2.0 * (G * Dc).sum(axis=0) / lam
+        else:
+            dY[:, c] = (G * _sgn(Dc)).sum(axis=0) / lam
     return dY
 
 
@@ -196,6 +239,7 @@ def backward_slice(saved, dO, tied=False):
     L, A, X, Y, C, W, What = (saved[n] for n in ("L", "A", "X", "Y", "C", "W", "What"))
     P, Z, q, k, v = saved["P"], saved["Z"], saved["q"], saved["k"], saved["v"]
     m = saved["m"]
+    kern = saved.get("kernel", "laplace")
 
     # O = Z W-hat
     dWhat = Z.T @ dO
@@ -207,8 +251,8 @@ def backward_slice(saved, dO, tied=False):
     else:
         dP = dZ
     # P = k(q, L)
-    dq = _kernel_grad_x(dP * P, q, L, lam)
-    dL = _kernel_grad_y(dP * P, q, L, lam)
+    dq = _kernel_grad_x(dP * P, q, L, lam, kern)
+    dL = _kernel_grad_y(dP * P, q, L, lam, kern)
 
     # W-hat = X_T W
     T = len(Y)
@@ -229,14 +273,14 @@ def backward_slice(saved, dO, tied=False):
     # A = k(L, L) + eps I: both arguments are L; the eps I term has no gradient
     Akern = A - saved["eps"] * np.eye(m)
     GA = dA * Akern
-    dL += _kernel_grad_x(GA, L, L, lam) + _kernel_grad_y(GA, L, L, lam)
+    dL += _kernel_grad_x(GA, L, L, lam, kern) + _kernel_grad_y(GA, L, L, lam, kern)
 
     # W = C V, C = k(L, k)
     dv = C.T @ dW
     dC = dW @ v.T
     GC = dC * C
-    dL += _kernel_grad_x(GC, L, k, lam)
-    dk = _kernel_grad_y(GC, L, k, lam)
+    dL += _kernel_grad_x(GC, L, k, lam, kern)
+    dk = _kernel_grad_y(GC, L, k, lam, kern)
 
     # L = window mean of k
     idx = saved["idx"]
@@ -251,7 +295,8 @@ def backward_slice(saved, dO, tied=False):
 # --------------------------------------------------------------------------
 # batched drivers over [B, H, N, d]
 # --------------------------------------------------------------------------
-def forward(q, k, v, grid_h, grid_w, m, lam, eps, iters, norm=False, slices=None):
+def forward(q, k, v, grid_h, grid_w, m, lam, eps, iters, norm=False, slices=None,
+            kernel="laplace"):
     """O [B, H, N, d] and the per-slice saved state (list)."""
     B, H, N, d = q.shape
     O = np.zeros((B, H, N, d))
@@ -261,7 +306,7 @@ def forward(q, k, v, grid_h, grid_w, m, lam, eps, iters, norm=False, slices=None
             if slices is not None and (b, h) not in slices:
                 continue
             O[b, h], saved[(b, h)] = forward_slice(q[b, h], k[b, h], v[b, h], grid_h, grid_w,
-                                                   m, lam, eps, iters, norm)
+                                                   m, lam, eps, iters, norm, kernel)
     return O, saved
 
 
@@ -273,5 +318,5 @@ def backward(saved, dO, tied=False):
     return out
 
 
-def attention(q, k, v, grid_h, grid_w, m, lam, eps, iters, norm=False):
-    return forward(q, k, v, grid_h, grid_w, m, lam, eps, iters, norm)[0]
+def attention(q, k, v, grid_h, grid_w, m, lam, eps, iters, norm=False, kernel="laplace"):
+    return forward(q, k, v, grid_h, grid_w, m, lam, eps, iters, norm, kernel=kernel)[0]

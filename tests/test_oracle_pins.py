@@ -13,6 +13,11 @@ not against the oracle's own formulas.
   exact full-kernel attention S V, brute-forced.
 - lambda -> infinity closed form; centring/whitening invariants.
 - Backward against central finite differences of the forward.
+- The Gaussian-kernel variant (SOFT review, Proposed method: a symmetric,
+  [0, 1]-valued Gaussian kernel; read as exp(-|x - y|_2^2 / lambda)): kernel
+  values by loops and by the factorisation exp(-|x|^2/l) exp(-|y|^2/l)
+  exp(2 x.y / l); positive definiteness; exact full-kernel attention with one
+  landmark per token; lambda -> infinity; finite differences; dV = M^T dO.
 """
 import math
 
@@ -156,7 +161,7 @@ def test_feature_map_invariants():
     np.testing.assert_allclose(Z.var(axis=0), var / (var + orc.ETA), rtol=1e-10)
 
 
-def _fd_check(tied, norm, seed):
+def _fd_check(tied, norm, seed, kernel="laplace"):
     rng = np.random.default_rng(seed)
     gh = gw = 4
     N, d, m, T, lam, eps = 16, 4, 4, 3, 4.0, 1e-3
@@ -166,10 +171,11 @@ def _fd_check(tied, norm, seed):
     R = rng.standard_normal((N, d))
 
     def loss(q_, k_, v_):
-        O, _ = orc.forward_slice(q_, q_ if tied else k_, v_, gh, gw, m, lam, eps, T, norm)
+        O, _ = orc.forward_slice(q_, q_ if tied else k_, v_, gh, gw, m, lam, eps, T, norm,
+                                 kernel)
         return float((O * R).sum())
 
-    _, saved = orc.forward_slice(q, k, v, gh, gw, m, lam, eps, T, norm)
+    _, saved = orc.forward_slice(q, k, v, gh, gw, m, lam, eps, T, norm, kernel)
     dq, dk, dv = orc.backward_slice(saved, R, tied=tied)
     h = 1e-6
     names = ("q", "v") if tied else ("q", "k", "v")
@@ -201,6 +207,85 @@ def test_dv_is_linear_map_transpose():
     N, d, m = 36, 4, 9
     q, k, v, dO = (rng.standard_normal((N, d)) for _ in range(4))
     O, s = orc.forward_slice(q, k, v, 6, 6, m, float(d), 1e-3, 6, norm=True)
+    M = s["Z"] @ s["X"][-1] @ s["C"]
+    np.testing.assert_allclose(O, M @ v, rtol=1e-12, atol=1e-12)
+    _, _, dv = orc.backward_slice(s, dO)
+    np.testing.assert_allclose(dv, M.T @ dO, rtol=1e-12, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# Gaussian-kernel variant
+# --------------------------------------------------------------------------
+def _loop_gauss(X, Y, lam):
+    out = [[0.0] * len(Y) for _ in range(len(X))]
+    for i, x in enumerate(X):
+        for j, y in enumerate(Y):
+            s = 0.0
+            for c in range(len(x)):
+                t = float(x[c]) - float(y[c])
+                s += t * t
+            out[i][j] = math.exp(-s / lam)
+    return np.array(out)
+
+
+def test_gaussian_kernel_by_loops_factorisation_and_range():
+    rng = np.random.default_rng(20)
+    X = rng.standard_normal((7, 5))
+    Y = rng.standard_normal((6, 5)) * 1.5
+    lam = 3.5
+    Kx = orc.gaussian_kernel(X, Y, lam)
+    np.testing.assert_allclose(Kx, _loop_gauss(X, Y, lam), rtol=1e-13, atol=0)
+    # |x - y|^2 = |x|^2 + |y|^2 - 2 x.y
+    fac = (np.exp(-(X ** 2).sum(1) / lam)[:, None] * np.exp(-(Y ** 2).sum(1) / lam)[None, :]
+           * np.exp(2.0 * (X @ Y.T) / lam))
+    np.testing.assert_allclose(Kx, fac, rtol=1e-12, atol=0)
+    assert np.all(Kx > 0) and np.all(Kx <= 1)
+    Kxx = orc.kernel_matrix(X, X, lam, "gauss")
+    np.testing.assert_array_equal(np.diag(Kxx), 1.0)
+    np.testing.assert_array_equal(Kxx, Kxx.T)
+
+
+def test_gaussian_landmark_matrix_is_spd():
+    rng = np.random.default_rng(21)
+    L = rng.standard_normal((49, 8))
+    G = orc.kernel_matrix(L, L, 8.0, "gauss")
+    assert np.linalg.eigvalsh(G).min() > -1e-12   # a Gaussian gram matrix is positive semidefinite
+    A = orc.landmark_matrix(L, 8.0, 1e-3, "gauss")
+    np.testing.assert_allclose(np.diag(A), 1.0 + 1e-3, rtol=0, atol=1e-15)
+    assert np.linalg.eigvalsh(A).min() >= 1e-3 - 1e-12
+
+
+def test_gaussian_one_landmark_per_token_equals_full_kernel_attention():
+    rng = np.random.default_rng(22)
+    N, d = 16, 4
+    q, k, v = (rng.standard_normal((N, d)) * 0.5 for _ in range(3))
+    lam = 2.0 * math.sqrt(d)
+    O, _ = orc.forward_slice(q, k, v, 4, 4, N, lam, 1e-3, 60, kernel="gauss")
+    S = _loop_gauss(q, k, lam)
+    G = _loop_gauss(k, k, lam)
+    Oref = S @ np.linalg.solve(G + 1e-3 * np.eye(N), G @ v)
+    np.testing.assert_allclose(O, Oref, rtol=1e-8, atol=1e-8)
+
+
+def test_gaussian_large_lambda_closed_form():
+    rng = np.random.default_rng(23)
+    N, d, m, eps = 36, 8, 9, 1e-3
+    q, k, v = (rng.standard_normal((N, d)) for _ in range(3))
+    O, _ = orc.forward_slice(q, k, v, 6, 6, m, 1e300, eps, 5, kernel="gauss")
+    expect = np.broadcast_to(m / (m + eps) * v.sum(axis=0), (N, d))
+    np.testing.assert_allclose(O, expect, rtol=1e-10, atol=1e-10)
+
+
+@pytest.mark.parametrize("tied,norm", [(False, False), (False, True), (True, False)])
+def test_gaussian_backward_matches_finite_differences(tied, norm):
+    _fd_check(tied, norm, seed=30 + 2 * tied + norm, kernel="gauss")
+
+
+def test_gaussian_dv_is_linear_map_transpose():
+    rng = np.random.default_rng(24)
+    N, d, m = 36, 4, 9
+    q, k, v, dO = (rng.standard_normal((N, d)) for _ in range(4))
+    O, s = orc.forward_slice(q, k, v, 6, 6, m, float(d), 1e-3, 6, norm=True, kernel="gauss")
     M = s["Z"] @ s["X"][-1] @ s["C"]
     np.testing.assert_allclose(O, M @ v, rtol=1e-12, atol=1e-12)
     _, _, dv = orc.backward_slice(s, dO)
