@@ -63,9 +63,15 @@ typedef enum {
 
 enum { LAPNYS_F32 = 0, LAPNYS_BF16 = 1 };
 
-/* flags: centre each landmark column of P over the slice's N queries and divide
- * by sqrt(biased variance + 1e-5) (the "injective" normalised feature map). */
-enum { LAPNYS_NORM = 1u << 0 };
+/* flags:
+ * LAPNYS_NORM   centre each landmark column of P over the slice's N queries and
+ *               divide by sqrt(biased variance + 1e-5) (the "injective"
+ *               normalised feature map of "LaplacianFormer", Arabic summary 2b);
+ * LAPNYS_GAUSS  use the Gaussian kernel k(x, y) = exp(-|x - y|_2^2 / lambda)
+ *               (the SOFT review's Proposed method: a symmetric, [0, 1]-valued
+ *               Gaussian kernel) instead of the Laplacian kernel
+ *               exp(-|x - y|_1 / lambda).  Same ctx, workspace and entry points. */
+enum { LAPNYS_NORM = 1u << 0, LAPNYS_GAUSS = 1u << 1 };
 
 /* Limits of this build: d in {16, 32, 64, 128}; 1 <= m <= N; m a perfect
  * square dividing the grid as above; 0 <= iters <= 64; lambda > 0; eps >= 0;

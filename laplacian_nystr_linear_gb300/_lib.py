@@ -14,7 +14,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liblapnys.s
 (LAPNYS_OK, LAPNYS_EINVAL, LAPNYS_ECUDA, LAPNYS_ETIMEOUT, LAPNYS_ENOSPC, LAPNYS_ENOTSUP,
  LAPNYS_ESCRATCH) = range(7)
 LAPNYS_F32, LAPNYS_BF16 = 0, 1
-LAPNYS_NORM = 1
+LAPNYS_NORM, LAPNYS_GAUSS = 1, 2
 
 # every symbol include/lapnys.h declares
 EXPORTS = (

@@ -27,6 +27,7 @@ class Params:
     iters: int = 20
     tied: bool = False
     norm: bool = False
+    kernel: str = "laplace"  # or "gauss"
 
     @property
     def N(self) -> int:
@@ -34,17 +35,21 @@ class Params:
 
     @property
     def flags(self) -> int:
-        return _lib.LAPNYS_NORM if self.norm else 0
+        if self.kernel not in ("laplace", "gauss"):
+            raise ValueError(f"unknown kernel {self.kernel!r}")
+        return ((_lib.LAPNYS_NORM if self.norm else 0)
+                | (_lib.LAPNYS_GAUSS if self.kernel == "gauss" else 0))
 
     def dims(self):
         return (self.B, self.H, self.N, self.d, self.grid_h, self.grid_w, self.m)
 
     @staticmethod
-    def of(q: torch.Tensor, grid, m: int, lam=None, eps=1e-3, iters=20, tied=False, norm=False):
+    def of(q: torch.Tensor, grid, m: int, lam=None, eps=1e-3, iters=20, tied=False, norm=False,
+           kernel="laplace"):
         B, H, N, d = q.shape
         gh, gw = grid
         return Params(B, H, gh, gw, d, m, float(d if lam is None else lam), float(eps), int(iters),
-                      bool(tied), bool(norm))
+                      bool(tied), bool(norm), str(kernel))
 
 
 def ctx_bytes(p: Params) -> int:
@@ -202,13 +207,15 @@ class _Attention(torch.autograd.Function):
         return dq, dk, dv, None
 
 
-def attention(q, k, v, grid, m, lam=None, eps=1e-3, iters=20, tied=False, norm=False):
-    """Laplacian-kernel Nystrom attention O = Z . X_T . (k(L, K) . V) with autograd.
+def attention(q, k, v, grid, m, lam=None, eps=1e-3, iters=20, tied=False, norm=False,
+              kernel="laplace"):
+    """Kernel Nystrom attention O = Z . X_T . (k(L, K) . V) with autograd, for the
+    Laplacian kernel (kernel="laplace") or the Gaussian kernel (kernel="gauss").
 
     q, k, v: [B, H, N, d] CUDA tensors (float32 or bfloat16), N = grid[0] * grid[1].
     In tied mode pass k=None (or k=q); the gradient of the shared tensor goes to q.
     """
-    p = Params.of(q, grid, m, lam, eps, iters, tied, norm)
+    p = Params.of(q, grid, m, lam, eps, iters, tied, norm, kernel)
     if tied:
         k = q
     return _Attention.apply(q, k, v, p)

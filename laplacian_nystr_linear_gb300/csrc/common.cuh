@@ -128,10 +128,17 @@ __device__ __forceinline__ void st_cpt(__nv_bfloat16* p, const float (&v)[CPT]) 
   }
 }
 
-// Register-blocked L1 distances between 4 token rows (j = 4*ty + r) and 4
+// |t| (Laplacian kernel) or t^2 (Gaussian kernel) added to a distance
+template <bool GAUSS>
+__device__ __forceinline__ float dist_add(float acc, float t) {
+  return GAUSS ? fmaf(t, t, acc) : acc + fabsf(t);
+}
+
+// Register-blocked distances between 4 token rows (j = 4*ty + r) and 4
 // landmark rows (a = tx + 16*s) of two shared tiles:
-//   dist[r][s] = sum_c |X[j][c] - L[a][c]|   (c ascending)
-template <int D>
+//   dist[r][s] = sum_c |X[j][c] - L[a][c]|  (L1), or sum_c (X[j][c] - L[a][c])^2
+//   (squared L2, GAUSS)   (c ascending)
+template <int D, bool GAUSS = false>
 __device__ __forceinline__ void dist_tile(const float* __restrict__ Xs, const float* __restrict__ Ls,
                                           float dist[4][4]) {
   const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
@@ -150,10 +157,10 @@ __device__ __forceinline__ void dist_tile(const float* __restrict__ Xs, const fl
     for (int r = 0; r < 4; ++r)
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
-        dist[r][s] += fabsf(x[r].x - l[s].x);
-        dist[r][s] += fabsf(x[r].y - l[s].y);
-        dist[r][s] += fabsf(x[r].z - l[s].z);
-        dist[r][s] += fabsf(x[r].w - l[s].w);
+        dist[r][s] = dist_add<GAUSS>(dist[r][s], x[r].x - l[s].x);
+        dist[r][s] = dist_add<GAUSS>(dist[r][s], x[r].y - l[s].y);
+        dist[r][s] = dist_add<GAUSS>(dist[r][s], x[r].z - l[s].z);
+        dist[r][s] = dist_add<GAUSS>(dist[r][s], x[r].w - l[s].w);
       }
   }
 }

@@ -20,6 +20,7 @@ struct Prob {
   int Sk, Sq, Sb; // token splits of the key pass, statistics pass, backward passes
   int Skt;        // token splits of the tensor-core key pass (0 when it is not used)
   bool norm() const { return flags & 1u; }
+  bool gauss() const { return flags & 2u; }  // Gaussian kernel instead of the Laplacian
 };
 
 // ---- instrumentation -------------------------------------------------------

@@ -20,6 +20,12 @@
 // block at most).  A block with an out-of-range value or too many ties takes an
 // exact path with sgn(0) = 0.
 //
+// Gaussian kernel k(x, l) = exp(-|x - l|_2^2 / lambda) (the SOFT review's
+// Proposed method): dk/dx_c = -(2 k / lambda) (x_c - l_c), so with the same g
+//     dX_jc  = 2 (sum_a g_ja l_ac - G_j x_jc)
+//     dL_ac += 2 (sum_j g_ja x_jc - G'_a l_ac)
+// two paired FMAs per (token, landmark, feature) and no ties (GAUSS = true).
+//
 // Work split per CTA: one 64-landmark tile and a contiguous range of 32-token
 // blocks; the raw token and upstream rows of the next block are copied into
 // shared memory (cp.async) while the current block computes; per block
@@ -109,7 +115,7 @@ __device__ __forceinline__ int gt(int a, int j) {
 // of its ag group (lane jg keeps landmarks al + 2 jg, al + 2 jg + 1), by warp
 // shuffles in a fixed order; the token-side result goes to Stage and the
 // landmark-side sum into dLs.
-template <int D, bool EXACT>
+template <int D, bool EXACT, bool GAUSS>
 __device__ __forceinline__ void sign_cols(int cbase, int j0, int al, int jg, int ag,
                                           const f32x2 (&gp)[4][8], const float* Xt,
                                           const float* LBt, float rowg, float inv_scale,
@@ -135,7 +141,31 @@ __device__ __forceinline__ void sign_cols(int cbase, int j0, int al, int jg, int
       lb[4] = v.x; lb[5] = v.y; lb[6] = v.z; lb[7] = v.w;
     }
     float pq[8], pl[8];
-    if (!EXACT) {
+    if constexpr (GAUSS) {
+      // token pair (2 rp, 2 rp + 1): sum_t 2g l_t; landmark t: sum over the
+      // lane's tokens of 2g x (even-token, odd-token halves)
+      f32x2 PQ[4];
+#pragma unroll
+      for (int rp = 0; rp < 4; ++rp) PQ[rp] = 0ull;
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const f32x2 lt = pack2(lb[t], lb[t]);
+        f32x2 PL = 0ull;
+#pragma unroll
+        for (int rp = 0; rp < 4; ++rp) {
+          PQ[rp] = fma2(gp[rp][t], lt, PQ[rp]);
+          PL = fma2(gp[rp][t], pack2(x[2 * rp], x[2 * rp + 1]), PL);
+        }
+        const float2 v = unpack2(PL);
+        pl[t] = v.x + v.y;
+      }
+#pragma unroll
+      for (int rp = 0; rp < 4; ++rp) {
+        const float2 v = unpack2(PQ[rp]);
+        pq[2 * rp] = v.x;
+        pq[2 * rp + 1] = v.y;
+      }
+    } else if (!EXACT) {
       // gp[rp][t] = (2g of tokens 2 rp, 2 rp + 1 at landmark t); the indicator
       // pair p multiplies it into the token pair's sums and into landmark t's
       // (even-token, odd-token) sums
@@ -205,8 +235,10 @@ __device__ __forceinline__ void sign_cols(int cbase, int j0, int al, int jg, int
       const float send = c0 ? l4[k] : l4[k + 2], keep = c0 ? l4[k + 2] : l4[k];
       l2[k] = keep + __shfl_xor_sync(kFull, send, 8);
     }
-    // fast path: dX = G_j - sum_a 2 g [x > l];  exact path: dX = -sum_a g sgn
-    Stage[(j0 + ag) * (D + 4) + c] = EXACT ? -qs : rowg - qs;
+    // fast path: dX = G_j - sum_a 2 g [x > l];  exact path: dX = -sum_a g sgn;
+    // Gaussian: dX = sum_a 2 g l - 2 G_j x
+    Stage[(j0 + ag) * (D + 4) + c] =
+        GAUSS ? qs - 2.f * rowg * Xt[c * JS + j0 + ag] : (EXACT ? -qs : rowg - qs);
     float2* dl = reinterpret_cast<float2*>(dLs + c * TA + al + 2 * jg);
     float2 o = *dl;
     o.x += l2[0];
@@ -215,7 +247,7 @@ __device__ __forceinline__ void sign_cols(int cbase, int j0, int al, int jg, int
   }
 }
 
-template <int D, typename T, int MODE, bool NORM>
+template <int D, typename T, int MODE, bool NORM, bool GAUSS>
 __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared memory allows one CTA
     k_bwd_pair(const T* __restrict__ X, const T* __restrict__ U, const float* __restrict__ L,
                const float* __restrict__ R, const float* __restrict__ stats,
@@ -261,8 +293,9 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
 
   // ---- landmark range check, R tile, statistics ----
   bool bad_l = false;
-  for (int e = tid; e < nv * D; e += kThreads)
-    if (out_of_range(__ldg(Lb + e))) bad_l = true;
+  if (!GAUSS)
+    for (int e = tid; e < nv * D; e += kThreads)
+      if (out_of_range(__ldg(Lb + e))) bad_l = true;
   load_tile<D>(Rs, R + (size_t)bh * m * D, a0, m);
   if (NORM && tid < TA) {
     const int a = a0 + tid;
@@ -281,7 +314,8 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
   // landmarks outside {0} u [2^-40, 2^60] force the exact path for the whole CTA;
   // then distances use scale 1 instead of 2^64
   const bool cta_exact = __syncthreads_or(bad_l) != 0;
-  const float scale = cta_exact ? 1.f : kBig;
+  // the landmark tile: -scale l for the saturated-FMA sign term, l itself for GAUSS
+  const float scale = GAUSS ? -1.f : (cta_exact ? 1.f : kBig);
   const float inv_scale = cta_exact ? 1.f : kInvBig;
   for (int e = tid; e < TA * D; e += kThreads) {
     const int c = e / TA, a = e % TA;
@@ -340,8 +374,8 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
 
   for (int b = b0; b < b1; ++b) {
     const int n0 = b * TJ;
-    const uint32_t* rb = tie_rec + ((size_t)bh * nblk + b) * kTieRec;
-    const uint32_t rh = __ldg(rb);
+    const uint32_t* rb = GAUSS ? nullptr : tie_rec + ((size_t)bh * nblk + b) * kTieRec;
+    const uint32_t rh = GAUSS ? 0u : __ldg(rb);
     const bool exact = cta_exact || (rh & kTieExact) != 0;
     const int nties = exact ? 0 : (int)rh;
     cp_wait_all();
@@ -604,10 +638,17 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
         colg_acc0 += colg_s[al + 2 * jg];
         colg_acc1 += colg_s[al + 2 * jg + 1];
       }
-      if (exact)
-        sign_cols<D, true>(warp * CW, j0, al, jg, ag, gp, Xt, LBt, rowg, inv_scale, Stage, dLs);
-      else
-        sign_cols<D, false>(warp * CW, j0, al, jg, ag, gp, Xt, LBt, rowg, inv_scale, Stage, dLs);
+      if constexpr (GAUSS) {
+        sign_cols<D, false, true>(warp * CW, j0, al, jg, ag, gp, Xt, LBt, rowg, inv_scale, Stage,
+                                  dLs);
+      } else {
+        if (exact)
+          sign_cols<D, true, false>(warp * CW, j0, al, jg, ag, gp, Xt, LBt, rowg, inv_scale, Stage,
+                                    dLs);
+        else
+          sign_cols<D, false, false>(warp * CW, j0, al, jg, ag, gp, Xt, LBt, rowg, inv_scale,
+                                     Stage, dLs);
+      }
     }
     __syncthreads();
     if (nties > 0) {
@@ -637,8 +678,15 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
 #pragma unroll
     for (int ci = 0; ci < CW; ++ci) {
       const int c = warp * CW + ci;
-      o[(size_t)(a0 + al) * D + c] = dLs[c * TA + al] - colg_acc0;
-      o[(size_t)(a0 + al + 1) * D + c] = dLs[c * TA + al + 1] - colg_acc1;
+      if (GAUSS) {
+        // LBt holds l: dL = sum_j 2 g x - 2 G'_a l
+        o[(size_t)(a0 + al) * D + c] = dLs[c * TA + al] - 2.f * colg_acc0 * LBt[c * AS + pa(al)];
+        o[(size_t)(a0 + al + 1) * D + c] =
+            dLs[c * TA + al + 1] - 2.f * colg_acc1 * LBt[c * AS + pa(al + 1)];
+      } else {
+        o[(size_t)(a0 + al) * D + c] = dLs[c * TA + al] - colg_acc0;
+        o[(size_t)(a0 + al + 1) * D + c] = dLs[c * TA + al + 1] - colg_acc1;
+      }
     }
   }
   if constexpr (kDWhat && kTC) {
@@ -658,26 +706,31 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
   }
 }
 
-template <int D, typename T, int MODE, bool NORM>
+template <int D, typename T, int MODE, bool NORM, bool GAUSS>
 static cudaError_t bwd_pair_t2(const Prob& p, const BwdArgs& a, cudaStream_t st) {
   const size_t smem = (size_t)Smem<D>::template total<T>() * sizeof(float);
-  static bool once = (allow_smem(k_bwd_pair<D, T, MODE, NORM>, smem), true);
+  static bool once = (allow_smem(k_bwd_pair<D, T, MODE, NORM, GAUSS>, smem), true);
   (void)once;
   static const char* names[3] = {"", "bwd_query", "bwd_key"};
   const int nblk = (p.N + TJ - 1) / TJ;
-  return launch(names[MODE], k_bwd_pair<D, T, MODE, NORM>, dim3(p.nt, p.Sb, p.BH), dim3(kThreads),
+  return launch(names[MODE], k_bwd_pair<D, T, MODE, NORM, GAUSS>, dim3(p.nt, p.Sb, p.BH), dim3(kThreads),
                 smem, st, (const T*)a.X, (const T*)a.U, a.L, a.R, a.stats, a.mdz, a.tok_part,
                 a.tok_part2, a.lm_part, a.lm_part2, a.ties, a.kv, p.N, p.m, p.mp,
                 p.Sb, nblk, p.BH, p.inv_lam);
 }
 
+template <int D, typename T, bool GAUSS>
+static cudaError_t bwd_pair_t3(const Prob& p, int mode, const BwdArgs& a, cudaStream_t st) {
+  if (mode == 1) {
+    if (p.norm()) return bwd_pair_t2<D, T, 1, true, GAUSS>(p, a, st);
+    return bwd_pair_t2<D, T, 1, false, GAUSS>(p, a, st);
+  }
+  return bwd_pair_t2<D, T, 2, false, GAUSS>(p, a, st);
+}
+
 template <int D, typename T>
 static cudaError_t bwd_pair_t(const Prob& p, int mode, const BwdArgs& a, cudaStream_t st) {
-  if (mode == 1) {
-    if (p.norm()) return bwd_pair_t2<D, T, 1, true>(p, a, st);
-    return bwd_pair_t2<D, T, 1, false>(p, a, st);
-  }
-  return bwd_pair_t2<D, T, 2, false>(p, a, st);
+  return p.gauss() ? bwd_pair_t3<D, T, true>(p, mode, a, st) : bwd_pair_t3<D, T, false>(p, mode, a, st);
 }
 
 cudaError_t run_bwd_pair(const Prob& p, int mode, const BwdArgs& a, cudaStream_t st) {

@@ -1,6 +1,6 @@
-// Token-side forward passes of Laplacian-kernel Nystrom attention with the
-// contractions on the 5th-generation tensor cores (bf16 inputs, d = 32 or 64,
-// m > 64):
+// Token-side forward passes of Laplacian-kernel Nystrom attention (and of its
+// Gaussian-kernel variant) with the contractions on the 5th-generation tensor
+// cores (bf16 inputs, d = 32 or 64, m > 64):
 //
 //   query pass   O = Z W-hat,  Z = P or (P - mu) / sqrt(var + eta),  P_ia = k(Q_i, L_a)
 //   key pass     W = C V,      C_aj = k(L_a, K_j)
@@ -138,7 +138,7 @@ struct QArgs {
   float ns;
 };
 
-template <int D, bool NORM>
+template <int D, bool NORM, bool GAUSS>
 __global__ void __launch_bounds__(NTH, 1) k_query_tc(QArgs a) {
   using S = QSmem<D>;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(NTH, 1) k_query_tc(QArgs a) {
 #pragma unroll
           for (int r = 0; r < 4; ++r)
 #pragma unroll
-            for (int s = 0; s < 4; ++s) acc[r][s] += fabsf(x[r] - lv[s]);
+            for (int s = 0; s < 4; ++s) acc[r][s] = dist_add<GAUSS>(acc[r][s], x[r] - lv[s]);
         }
       }
       // the A buffer of this tile was read by MMA g - 2
@@ -334,7 +334,7 @@ struct KArgs {
   float ns;
 };
 
-template <int D>
+template <int D, bool GAUSS>
 __global__ void __launch_bounds__(NTH, 1) k_key_tc(KArgs a) {
   using S = KSmem<D>;
   extern __shared__ __align__(1024) uint8_t sm[];
@@ -430,7 +430,7 @@ __global__ void __launch_bounds__(NTH, 1) k_key_tc(KArgs a) {
 #pragma unroll
         for (int r = 0; r < 4; ++r)
 #pragma unroll
-          for (int s = 0; s < 4; ++s) acc[r][s] += fabsf(xv[s] - lv[r]);
+          for (int s = 0; s < 4; ++s) acc[r][s] = dist_add<GAUSS>(acc[r][s], xv[s] - lv[r]);
       }
     }
     {
@@ -543,11 +543,11 @@ cudaError_t run_pack_q(const Prob& p, const float* L, const float* What, float* 
   return cudaErrorInvalidValue;
 }
 
-template <int D, bool NORM>
+template <int D, bool NORM, bool GAUSS>
 static cudaError_t query_tc_t(const Prob& p, const void* q, const float* pack, const float* stats,
                               void* out, float* kvout, cudaStream_t st) {
   const size_t smem = QSmem<D>::total;
-  static bool once = (allow_smem(k_query_tc<D, NORM>, smem), true);
+  static bool once = (allow_smem(k_query_tc<D, NORM, GAUSS>, smem), true);
   (void)once;
   QArgs a;
   a.Q = (const __nv_bfloat16*)q;
@@ -562,23 +562,31 @@ static cudaError_t query_tc_t(const Prob& p, const void* q, const float* pack, c
   a.items = a.nb * p.BH;
   a.ns = p.ns;
   const int grid = a.items < sm_count() ? a.items : sm_count();
-  return launch("query_fwd", k_query_tc<D, NORM>, dim3(grid), dim3(NTH), smem, st, a);
+  return launch("query_fwd", k_query_tc<D, NORM, GAUSS>, dim3(grid), dim3(NTH), smem, st, a);
 }
 
 cudaError_t run_query_tc(const Prob& p, const void* q, const float* pack, const float* stats,
                          void* out, float* kvout, cudaStream_t st) {
-  if (p.d == 32) return p.norm() ? query_tc_t<32, true>(p, q, pack, stats, out, kvout, st)
-                                 : query_tc_t<32, false>(p, q, pack, stats, out, kvout, st);
-  if (p.d == 64) return p.norm() ? query_tc_t<64, true>(p, q, pack, stats, out, kvout, st)
-                                 : query_tc_t<64, false>(p, q, pack, stats, out, kvout, st);
+#define QTC(DD, NN)                                                                   \
+  return p.gauss() ? query_tc_t<DD, NN, true>(p, q, pack, stats, out, kvout, st)     \
+                   : query_tc_t<DD, NN, false>(p, q, pack, stats, out, kvout, st)
+  if (p.d == 32) {
+    if (p.norm()) QTC(32, true);
+    QTC(32, false);
+  }
+  if (p.d == 64) {
+    if (p.norm()) QTC(64, true);
+    QTC(64, false);
+  }
+#undef QTC
   return cudaErrorInvalidValue;
 }
 
-template <int D>
+template <int D, bool GAUSS>
 static cudaError_t key_tc_t(const Prob& p, const void* k, const void* v, const float* L, float* part,
                             float* kvout, cudaStream_t st) {
   const size_t smem = KSmem<D>::total;
-  static bool once = (allow_smem(k_key_tc<D>, smem), true);
+  static bool once = (allow_smem(k_key_tc<D, GAUSS>, smem), true);
   (void)once;
   KArgs a;
   a.K = (const __nv_bfloat16*)k;
@@ -590,13 +598,17 @@ static cudaError_t key_tc_t(const Prob& p, const void* k, const void* v, const f
   a.N = p.N; a.m = p.m; a.mp = p.mp; a.S = p.Skt; a.nblk = p.nblk;
   a.ns = p.ns;
   const int nt = (p.m + QM - 1) / QM;
-  return launch("key_fwd", k_key_tc<D>, dim3(nt, p.Skt, p.BH), dim3(NTH), smem, st, a);
+  return launch("key_fwd", k_key_tc<D, GAUSS>, dim3(nt, p.Skt, p.BH), dim3(NTH), smem, st, a);
 }
 
 cudaError_t run_key_tc(const Prob& p, const void* k, const void* v, const float* L, float* part,
                        float* kvout, cudaStream_t st) {
-  if (p.d == 32) return key_tc_t<32>(p, k, v, L, part, kvout, st);
-  if (p.d == 64) return key_tc_t<64>(p, k, v, L, part, kvout, st);
+  if (p.d == 32)
+    return p.gauss() ? key_tc_t<32, true>(p, k, v, L, part, kvout, st)
+                     : key_tc_t<32, false>(p, k, v, L, part, kvout, st);
+  if (p.d == 64)
+    return p.gauss() ? key_tc_t<64, true>(p, k, v, L, part, kvout, st)
+                     : key_tc_t<64, false>(p, k, v, L, part, kvout, st);
   return cudaErrorInvalidValue;
 }
 

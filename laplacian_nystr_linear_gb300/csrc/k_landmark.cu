@@ -164,7 +164,7 @@ __device__ void alpha_of_tile(const float* As, int m, float* info_g, float* alph
 // ---------------------------------------------------------------------------
 // gram + alpha + Newton-Schulz for m <= 64: one CTA per slice
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, bool GAUSS>
 __global__ void __launch_bounds__(kThreads) k_ns_small(const float* __restrict__ L, float* __restrict__ A,
                                                        float* __restrict__ alpha, float* __restrict__ X,
                                                        float* __restrict__ Y, int m, int iters, int nx,
@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(kThreads) k_ns_small(const float* __restrict__
   __syncthreads();
   {
     float dist[4][4];
-    dist_tile<D>(Ls, Ls, dist);
+    dist_tile<D, GAUSS>(Ls, Ls, dist);
     const int tx = threadIdx.x & 15;
 #pragma unroll
     for (int r = 0; r < 4; ++r)
@@ -235,10 +235,16 @@ cudaError_t run_ns_small(const Prob& p, const float* L, float* A, float* alpha, 
 #define NS_SMALL_CASE(DD)                                                                   \
   case DD: {                                                                                \
     const size_t smem = (size_t)(tile_floats(DD) + 4 * 64 * kMS) * sizeof(float);           \
-    static bool once = (allow_smem(k_ns_small<DD>, smem), true);                            \
+    if (p.gauss()) {                                                                        \
+      static bool once = (allow_smem(k_ns_small<DD, true>, smem), true);                    \
+      (void)once;                                                                           \
+      return launch("ns_small", k_ns_small<DD, true>, dim3(p.BH), dim3(kThreads), smem, st, \
+                    L, A, alpha, X, Y, p.m, p.iters, nx, ny, p.ns, p.eps);                  \
+    }                                                                                       \
+    static bool once = (allow_smem(k_ns_small<DD, false>, smem), true);                     \
     (void)once;                                                                             \
-    return launch("ns_small", k_ns_small<DD>, dim3(p.BH), dim3(kThreads), smem, st, L, A,   \
-                  alpha, X, Y, p.m, p.iters, nx, ny, p.ns, p.eps);                          \
+    return launch("ns_small", k_ns_small<DD, false>, dim3(p.BH), dim3(kThreads), smem, st,  \
+                  L, A, alpha, X, Y, p.m, p.iters, nx, ny, p.ns, p.eps);                    \
   }
   switch (p.d) {
     NS_SMALL_CASE(16)
@@ -254,7 +260,7 @@ cudaError_t run_ns_small(const Prob& p, const float* L, float* A, float* alpha, 
 // ---------------------------------------------------------------------------
 // gram tiles for any m: grid (column tile, row tile, slice)
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, bool GAUSS>
 __global__ void __launch_bounds__(kThreads) k_gram(const float* __restrict__ L, float* __restrict__ A,
                                                    int m, float ns, float eps) {
   extern __shared__ float4 sm4[];
@@ -266,7 +272,7 @@ __global__ void __launch_bounds__(kThreads) k_gram(const float* __restrict__ L, 
   load_tile<D>(Ls, Lb, jt * 64, m);
   __syncthreads();
   float dist[4][4];
-  dist_tile<D>(Xs, Ls, dist);
+  dist_tile<D, GAUSS>(Xs, Ls, dist);
   const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
 #pragma unroll
   for (int r = 0; r < 4; ++r)
@@ -283,9 +289,16 @@ cudaError_t run_gram(const Prob& p, const float* L, float* A, cudaStream_t st) {
 #define GRAM_CASE(DD)                                                                        \
   case DD: {                                                                                 \
     const size_t smem = 2 * (size_t)tile_floats(DD) * sizeof(float);                         \
-    static bool once = (allow_smem(k_gram<DD>, smem), true);                                 \
+    if (p.gauss()) {                                                                         \
+      static bool once = (allow_smem(k_gram<DD, true>, smem), true);                         \
+      (void)once;                                                                            \
+      return launch("gram", k_gram<DD, true>, grid, dim3(kThreads), smem, st, L, A, p.m,     \
+                    p.ns, p.eps);                                                            \
+    }                                                                                        \
+    static bool once = (allow_smem(k_gram<DD, false>, smem), true);                          \
     (void)once;                                                                              \
-    return launch("gram", k_gram<DD>, grid, dim3(kThreads), smem, st, L, A, p.m, p.ns, p.eps); \
+    return launch("gram", k_gram<DD, false>, grid, dim3(kThreads), smem, st, L, A, p.m, p.ns, \
+                  p.eps);                                                                    \
   }
   switch (p.d) {
     GRAM_CASE(16)
@@ -345,11 +358,13 @@ cudaError_t run_alpha(const Prob& p, const float* A, float* alpha, float* X0, lo
 // ---------------------------------------------------------------------------
 // backward of A = k(L, L) + eps I:
 //   dL_A[a][c] = -(1/lambda) sum_{b != a} (dA_ab + dA_ba) A_ab sgn(L_ac - L_bc)
+// or, for the Gaussian kernel (dk/dx = -(2/lambda) (x - y) k),
+//   dL_A[a][c] = -(2/lambda) sum_{b != a} (dA_ab + dA_ba) A_ab (L_ac - L_bc)
 // block = (D columns) x (256 / D landmarks); grid (landmark groups, slice)
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kThreads) k_gram_bwd(const float* __restrict__ L, const float* __restrict__ A,
                                                        const float* __restrict__ dA, float* __restrict__ dLA,
-                                                       int m, int d, float inv_lam) {
+                                                       int m, int d, float inv_lam, int gauss) {
   const int lpb = kThreads / d;
   const int c = threadIdx.x % d;
   const int a = blockIdx.x * lpb + threadIdx.x / d;
@@ -363,7 +378,8 @@ __global__ void __launch_bounds__(kThreads) k_gram_bwd(const float* __restrict__
   for (int b = 0; b < m; ++b) {
     if (b == a) continue;
     const float w = (dAb[(size_t)a * m + b] + dAb[(size_t)b * m + a]) * Ab[(size_t)a * m + b];
-    s += sgn_times(la - Lb[(size_t)b * d + c], w);
+    const float t = la - Lb[(size_t)b * d + c];
+    s += gauss ? 2.f * t * w : sgn_times(t, w);
   }
   dLA[((size_t)bh * m + a) * d + c] = -inv_lam * s;
 }
@@ -373,7 +389,7 @@ cudaError_t run_gram_bwd(const Prob& p, const float* L, const float* A, const fl
   const int lpb = kThreads / p.d;
   dim3 grid((p.m + lpb - 1) / lpb, p.BH);
   return launch("gram_bwd", k_gram_bwd, grid, dim3(kThreads), 0, st, L, A, dA, dLA, p.m, p.d,
-                p.inv_lam);
+                p.inv_lam, p.gauss() ? 1 : 0);
 }
 
 // ---------------------------------------------------------------------------

@@ -40,7 +40,7 @@ __device__ __forceinline__ void split_range(int nblk, int S, int s, int& b0, int
 // blocks of 64 (the raw rows of the next block are copied in with cp.async
 // while the current one computes) and accumulates W[a][c] = sum_j C_aj V_jc.
 // ===========================================================================
-template <int D, typename T>
+template <int D, typename T, bool GAUSS>
 __global__ void __launch_bounds__(kThreads, 2)
     k_key_fwd(const T* __restrict__ K, const T* __restrict__ V, const float* __restrict__ L,
               float* __restrict__ part, float* __restrict__ kvout, int N, int m, int mp, int S,
@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     __syncthreads();
     prefetch(b + 1);
     float dist[4][4];
-    dist_tile<D>(Xs, Ls, dist);
+    dist_tile<D, GAUSS>(Xs, Ls, dist);
 #pragma unroll
     for (int r = 0; r < 4; ++r)
 #pragma unroll
@@ -173,9 +173,15 @@ static cudaError_t key_fwd_t(const Prob& p, const void* k, const void* v, const 
                              float* kvout, cudaStream_t st) {
   const size_t smem = (3 * (size_t)tile_floats(D) + 64 * 68) * sizeof(float) +
                       2 * (size_t)kTile * (D * sizeof(T) + 16);
-  static bool once = (allow_smem(k_key_fwd<D, T>, smem), true);
+  if (p.gauss()) {
+    static bool once = (allow_smem(k_key_fwd<D, T, true>, smem), true);
+    (void)once;
+    return launch("key_fwd", k_key_fwd<D, T, true>, dim3(p.nt, p.Sk, p.BH), dim3(kThreads), smem,
+                  st, (const T*)k, (const T*)v, L, part, kvout, p.N, p.m, p.mp, p.Sk, p.nblk, p.ns);
+  }
+  static bool once = (allow_smem(k_key_fwd<D, T, false>, smem), true);
   (void)once;
-  return launch("key_fwd", k_key_fwd<D, T>, dim3(p.nt, p.Sk, p.BH), dim3(kThreads), smem, st,
+  return launch("key_fwd", k_key_fwd<D, T, false>, dim3(p.nt, p.Sk, p.BH), dim3(kThreads), smem, st,
                 (const T*)k, (const T*)v, L, part, kvout, p.N, p.m, p.mp, p.Sk, p.nblk, p.ns);
 }
 
@@ -250,7 +256,7 @@ __device__ __forceinline__ void chan_merge(float& n, float& mean, float& M2, flo
   n = nn;
 }
 
-template <int D, typename T>
+template <int D, typename T, bool GAUSS>
 __global__ void __launch_bounds__(kThreads, 2)
     k_qstats(const T* __restrict__ Q, const float* __restrict__ L, float* __restrict__ spart, int N,
              int m, int mp, int S, int nblk, float ns) {
@@ -271,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     load_tile<D>(Xs, Qb, b * kTile, N);
     __syncthreads();
     float dist[4][4];
-    dist_tile<D>(Xs, Ls, dist);
+    dist_tile<D, GAUSS>(Xs, Ls, dist);
 #pragma unroll
     for (int r = 0; r < 4; ++r)
 #pragma unroll
@@ -302,9 +308,15 @@ template <int D, typename T>
 static cudaError_t qstats_t(const Prob& p, const void* q, const float* L, float* spart,
                             cudaStream_t st) {
   const size_t smem = (2 * (size_t)tile_floats(D) + 64 * 68) * sizeof(float);
-  static bool once = (allow_smem(k_qstats<D, T>, smem), true);
+  if (p.gauss()) {
+    static bool once = (allow_smem(k_qstats<D, T, true>, smem), true);
+    (void)once;
+    return launch("qstats", k_qstats<D, T, true>, dim3(p.nt, p.Sq, p.BH), dim3(kThreads), smem,
+                  st, (const T*)q, L, spart, p.N, p.m, p.mp, p.Sq, p.nblk, p.ns);
+  }
+  static bool once = (allow_smem(k_qstats<D, T, false>, smem), true);
   (void)once;
-  return launch("qstats", k_qstats<D, T>, dim3(p.nt, p.Sq, p.BH), dim3(kThreads), smem, st,
+  return launch("qstats", k_qstats<D, T, false>, dim3(p.nt, p.Sq, p.BH), dim3(kThreads), smem, st,
                 (const T*)q, L, spart, p.N, p.m, p.mp, p.Sq, p.nblk, p.ns);
 }
 
@@ -342,7 +354,7 @@ cudaError_t run_stats_final(const Prob& p, const float* spart, float* stats, cud
 // copied in with cp.async, double buffered): P tile on the fly, optional
 // centring/whitening, then O += Z_tile W-hat_tile.
 // ===========================================================================
-template <int D, typename T, bool NORM>
+template <int D, typename T, bool NORM, bool GAUSS>
 __global__ void __launch_bounds__(kThreads, 2)
     k_query_fwd(const T* __restrict__ Q, const float* __restrict__ L, const float* __restrict__ What,
                 const float* __restrict__ stats, T* __restrict__ O, float* __restrict__ kvout,
@@ -402,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     __syncthreads();
     float dist[4][4];
-    dist_tile<D>(Xs, Ls, dist);
+    dist_tile<D, GAUSS>(Xs, Ls, dist);
 #pragma unroll
     for (int r = 0; r < 4; ++r)
 #pragma unroll
@@ -480,16 +492,20 @@ static cudaError_t query_fwd_t(const Prob& p, const void* q, const float* L, con
                                const float* stats, void* out, float* kvout, cudaStream_t st) {
   const size_t smem = (5 * (size_t)tile_floats(D) + 64 * 68) * sizeof(float);
   dim3 grid(p.nblk, p.BH);
+#define QF_LAUNCH(NN, GG)                                                                      \
+  do {                                                                                         \
+    static bool once = (allow_smem(k_query_fwd<D, T, NN, GG>, smem), true);                    \
+    (void)once;                                                                                \
+    return launch("query_fwd", k_query_fwd<D, T, NN, GG>, grid, dim3(kThreads), smem, st,      \
+                  (const T*)q, L, What, stats, (T*)out, kvout, p.N, p.m, p.nt, p.ns);          \
+  } while (0)
   if (p.norm()) {
-    static bool once = (allow_smem(k_query_fwd<D, T, true>, smem), true);
-    (void)once;
-    return launch("query_fwd", k_query_fwd<D, T, true>, grid, dim3(kThreads), smem, st,
-                  (const T*)q, L, What, stats, (T*)out, kvout, p.N, p.m, p.nt, p.ns);
+    if (p.gauss()) QF_LAUNCH(true, true);
+    QF_LAUNCH(true, false);
   }
-  static bool once2 = (allow_smem(k_query_fwd<D, T, false>, smem), true);
-  (void)once2;
-  return launch("query_fwd", k_query_fwd<D, T, false>, grid, dim3(kThreads), smem, st, (const T*)q,
-                L, What, stats, (T*)out, kvout, p.N, p.m, p.nt, p.ns);
+  if (p.gauss()) QF_LAUNCH(false, true);
+  QF_LAUNCH(false, false);
+#undef QF_LAUNCH
 }
 
 cudaError_t run_query_fwd(const Prob& p, const void* q, const float* L, const float* What,
@@ -514,7 +530,7 @@ cudaError_t run_query_fwd(const Prob& p, const void* q, const float* L, const fl
 // (key side, per landmark tile).  MODE 0 is the query-side statistics pass of
 // the normalised map (sum dZ, sum dZ Z and dW-hat only).
 // ===========================================================================
-template <int D, typename T, int MODE, bool NORM>
+template <int D, typename T, int MODE, bool NORM, bool GAUSS>
 __global__ void __launch_bounds__(kThreads, 2)
     k_bwd_tile(const T* __restrict__ X, const T* __restrict__ U, const float* __restrict__ L,
                const float* __restrict__ R, const float* __restrict__ stats,
@@ -588,10 +604,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int r = 0; r < 4; ++r)
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
-          dist[r][s] += fabsf(x[r].x - l[s].x);
-          dist[r][s] += fabsf(x[r].y - l[s].y);
-          dist[r][s] += fabsf(x[r].z - l[s].z);
-          dist[r][s] += fabsf(x[r].w - l[s].w);
+          dist[r][s] = dist_add<GAUSS>(dist[r][s], x[r].x - l[s].x);
+          dist[r][s] = dist_add<GAUSS>(dist[r][s], x[r].y - l[s].y);
+          dist[r][s] = dist_add<GAUSS>(dist[r][s], x[r].z - l[s].z);
+          dist[r][s] = dist_add<GAUSS>(dist[r][s], x[r].w - l[s].w);
         }
 #pragma unroll
       for (int r = 0; r < 4; ++r) x[r] = lds4(Us + (4 * ty + r) * row_stride(D) + c);
@@ -739,26 +755,25 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
 }
 
-template <int D, typename T, int MODE, bool NORM>
+template <int D, typename T, int MODE, bool NORM, bool GAUSS>
 static cudaError_t bwd_tile_t2(const Prob& p, const BwdArgs& a, cudaStream_t st) {
   const size_t smem = (4 * (size_t)tile_floats(D) + 2 * 64 * 68) * sizeof(float);
-  static bool once = (allow_smem(k_bwd_tile<D, T, MODE, NORM>, smem), true);
+  static bool once = (allow_smem(k_bwd_tile<D, T, MODE, NORM, GAUSS>, smem), true);
   (void)once;
   static const char* names[3] = {"bwd_qstats", "bwd_query", "bwd_key"};
-  return launch(names[MODE], k_bwd_tile<D, T, MODE, NORM>, dim3(p.nt, p.Sb, p.BH), dim3(kThreads),
+  return launch(names[MODE], k_bwd_tile<D, T, MODE, NORM, GAUSS>, dim3(p.nt, p.Sb, p.BH), dim3(kThreads),
                 smem, st, (const T*)a.X, (const T*)a.U, a.L, a.R, a.stats, a.mdz, a.tok_part,
                 a.tok_part2, a.lm_part, a.lm_part2, a.ns_part, p.N, p.m, p.mp, p.Sb, p.nblk, p.BH,
                 p.ns, p.inv_lam);
 }
 
+// only the statistics pass (mode 0) of this kernel is used; the token-side
+// modes run in k_bwd_pair (k_bwd.cu)
 template <int D, typename T>
 static cudaError_t bwd_tile_t(const Prob& p, int mode, const BwdArgs& a, cudaStream_t st) {
-  if (mode == 0) return bwd_tile_t2<D, T, 0, true>(p, a, st);
-  if (mode == 1) {
-    if (p.norm()) return bwd_tile_t2<D, T, 1, true>(p, a, st);
-    return bwd_tile_t2<D, T, 1, false>(p, a, st);
-  }
-  return bwd_tile_t2<D, T, 2, false>(p, a, st);
+  if (mode != 0) return cudaErrorInvalidValue;
+  if (p.gauss()) return bwd_tile_t2<D, T, 0, true, true>(p, a, st);
+  return bwd_tile_t2<D, T, 0, true, false>(p, a, st);
 }
 
 cudaError_t run_bwd_tile(const Prob& p, int mode, const BwdArgs& a, cudaStream_t st) {

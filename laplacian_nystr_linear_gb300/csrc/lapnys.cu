@@ -186,7 +186,7 @@ static int check_common(int B, int H, int N, int d, int gh, int gw, int m, float
   if (!(lam > 0.f) || !isfinite(lam)) return LAPNYS_EINVAL;
   if (!(eps >= 0.f) || !isfinite(eps)) return LAPNYS_EINVAL;
   if (dtype != LAPNYS_F32 && dtype != LAPNYS_BF16) return LAPNYS_EINVAL;
-  if ((flags & ~(unsigned)LAPNYS_NORM) != 0) return LAPNYS_EINVAL;
+  if ((flags & ~(unsigned)(LAPNYS_NORM | LAPNYS_GAUSS)) != 0) return LAPNYS_EINVAL;
   if (!d_supported(d)) return LAPNYS_ENOTSUP;
   return LAPNYS_OK;
 }
@@ -581,9 +581,11 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
   // landmark value, or out of the fast path's range)
   uint32_t* ties_q = (uint32_t*)(wb + w.ties);
   uint32_t* ties_k = tied_qk ? ties_q : ties_q + (size_t)p.BH * ((N + 31) / 32) * kTieRec;
-  CK(run_tie_prep(p, L, wb + w.tie_scratch, stream));
-  CK(run_ties(p, q, wb + w.tie_scratch, ties_q, stream));
-  if (!tied_qk) CK(run_ties(p, k, wb + w.tie_scratch, ties_k, stream));
+  if (!p.gauss()) {  // the Gaussian kernel's gradient has no sign term, hence no ties
+    CK(run_tie_prep(p, L, wb + w.tie_scratch, stream));
+    CK(run_ties(p, q, wb + w.tie_scratch, ties_q, stream));
+    if (!tied_qk) CK(run_ties(p, k, wb + w.tie_scratch, ties_k, stream));
+  }
 
   // ---- query side ----
   BwdArgs qa;

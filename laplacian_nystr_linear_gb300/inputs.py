@@ -42,6 +42,7 @@ class Workload:
     norm: bool = False
     outliers: bool = False
     backward: bool = False
+    kernel: str = "laplace"   # "laplace" or "gauss" (a name only; no arithmetic here)
 
     @property
     def N(self) -> int:

@@ -296,6 +296,38 @@ def test_sparse_ties_are_corrected(m):
         assert n_corr >= (32 if x == "q" else (16 if m == 64 else 0)), (name, n_corr)
 
 
+# ---------------------------------------------------------------------------
+# Gaussian-kernel variant (LAPNYS_GAUSS): k(x, y) = exp(-|x - y|_2^2 / lambda)
+# ---------------------------------------------------------------------------
+GAUSS_NAMES = ("f32", "f32_norm", "f32_tied", "bf16", "ragged", "ragged_large_m", "m1", "iters0",
+               "d128", "m81", "batch", "bf16_mN")
+GAUSS_SMALL = ([dataclasses.replace(w, name="gauss_" + w.name, kernel="gauss")
+                for w in SMALL if w.name in GAUSS_NAMES]
+               + [dataclasses.replace(w, name="gauss_" + w.name, kernel="gauss") for w in TC_FWD])
+
+
+@pytest.mark.parametrize("w", GAUSS_SMALL, ids=lambda w: w.name)
+def test_gaussian_backward_small_cases(w):
+    inp = random_inputs(41 + w.m + w.d, w.B, w.H, w.N, w.d, w.dtype, tied=w.tied)
+    g = gpu_run(w, inp, backward=True)
+    o = oracle_run(w, inp, backward=True)
+    print(w.name, compare(w, g, o, backward=True))
+    for (b, h), s in o["saved"].items():
+        c = g["ctx"]
+        assert rel(c["A"][b, h], s["A"]) < 1e-6            # Gaussian landmark matrix
+        assert rel(c["P"][b, h], s["P"]) < 1e-5            # kernel values stored as computed
+        assert rel(c["C"][b, h], s["C"].T) < 1e-5
+
+
+@pytest.mark.parametrize("backward", [False, True])
+def test_gaussian_hires16k(backward):
+    w = dataclasses.replace(WORKLOADS["hires16k"], kernel="gauss")
+    inp = make_inputs(w, with_grad=backward)
+    g = gpu_run(w, inp, backward=backward)
+    o = oracle_run(w, inp, slices={(3, 5)} if backward else {(0, 0), (7, 7)}, backward=backward)
+    print(w.name, "gauss", compare(w, g, o, backward=backward))
+
+
 def test_deterministic():
     w = WORKLOADS["pvt2"]
     inp = make_inputs(w)
