@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--kernel", choices=["laplace", "gauss"], default="laplace",
+                    help="Laplacian kernel (the method) or its Gaussian-kernel variant")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override B (smaller profiling cases)")
@@ -65,12 +67,14 @@ def algorithmic_ops(w):
     forward still count."""
     BH, N, m, d, T = w.B * w.H, w.N, w.m, w.d, w.iters
     nmd = BH * N * m * d
+    # Gaussian kernel: the gradient term is two FMAs (sum g l, sum g x), not the 3-op sign term
+    side = 6 if w.kernel == "gauss" else 7
     return {
         "key_fwd": 3 * nmd,
         "query_fwd": 3 * nmd,
         "qstats": 2 * nmd if w.norm else 0,
-        "bwd_query": 7 * nmd,
-        "bwd_key": 7 * nmd,
+        "bwd_query": side * nmd,
+        "bwd_key": side * nmd,
         "bwd_qstats": 2 * nmd if w.norm else 0,
         "ns_cluster": 2 * T * BH * m ** 3,
         "ns_cluster_rev": 6 * T * BH * m ** 3,
@@ -86,21 +90,23 @@ def fp32_pipe_ops(w):
     BH, N, m, d = w.B * w.H, w.N, w.m, w.d
     nmd = BH * N * m * d
     tc = w.dtype == "bf16"
+    grad = 2 if w.kernel == "gauss" else 4   # Gaussian term: two FMAs; sign term: indicator + two FMAs
     return {"key_fwd": (2 if tc else 3) * nmd, "query_fwd": (2 if tc else 3) * nmd,
-            "bwd_query": (4 if tc else 6) * nmd, "bwd_key": (4 if tc else 6) * nmd}
+            "bwd_query": (grad if tc else grad + 2) * nmd, "bwd_key": (grad if tc else grad + 2) * nmd}
 
 
-def measured_traffic(workload: str, kernel: str):
+def measured_traffic(workload: str, method_kernel: str, kernel: str):
     """DRAM bytes per launch of `kernel` from the ncu capture recorded in
     profiles/traffic_<workload>.json, or None when there is no record for it
-    or its source file has changed since the counters were taken."""
+    (this GPU kernel, this attention kernel) or its source file has changed
+    since the counters were taken."""
     import hashlib
     path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles",
                         f"traffic_{workload}.json")
     try:
         with open(path) as f:
             rec = json.load(f)
-        if rec.get("kernel") != kernel:
+        if rec.get("kernel") != kernel or rec.get("method_kernel", "laplace") != method_kernel:
             return None
         src = os.path.join(os.path.dirname(os.path.abspath(__file__)), rec["source"])
         with open(src, "rb") as f:
@@ -174,16 +180,16 @@ def clock_summary(proc, path):
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline and reference arm): one (b, h) slice, forward + backward
 # ---------------------------------------------------------------------------
-def _oracle_slice(wname: str):
+def _oracle_slice(wname: str, kernel: str = "laplace"):
     import dataclasses
 
     from laplacian_nystr_linear_gb300.inputs import WORKLOADS, make_inputs
     from oracle import lapnys_oracle as orc
-    w = dataclasses.replace(WORKLOADS[wname], B=1, H=1)
+    w = dataclasses.replace(WORKLOADS[wname], B=1, H=1, kernel=kernel)
     inp = make_inputs(w, with_grad=True)
     t0 = time.perf_counter()
     _, saved = orc.forward(inp["q"], inp["k"], inp["v"], w.grid_h, w.grid_w, w.m, w.lam, w.eps,
-                           w.iters, w.norm)
+                           w.iters, w.norm, kernel=kernel)
     orc.backward(saved, inp["dout"], tied=w.tied)
     return time.perf_counter() - t0, w.N
 
@@ -195,11 +201,11 @@ def _single_thread_env():
     return env
 
 
-def cpu_baseline(wname: str):
+def cpu_baseline(wname: str, kernel: str = "laplace"):
     """The oracle as it stands, one process, one thread, on whole (b, h) slices
     of the workload (at least 10 s of work)."""
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-worker",
-                        "--workload", wname], capture_output=True, text=True,
+                        "--workload", wname, "--kernel", kernel], capture_output=True, text=True,
                        env=_single_thread_env(), timeout=1800)
     if r.returncode != 0:
         return {"error": r.stderr.strip().splitlines()[-1:]}
@@ -209,10 +215,10 @@ def cpu_baseline(wname: str):
                       f"{sec:.1f} s single-threaded"}
 
 
-def _pool_task(wname):
+def _pool_task(task):
     os.environ.update({k: "1" for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS",
                                          "MKL_NUM_THREADS")})
-    return _oracle_slice(wname)
+    return _oracle_slice(*task)
 
 
 def run_reference(args, rank, world):
@@ -223,9 +229,10 @@ def run_reference(args, rank, world):
     cores = max(1, min(os.cpu_count() or 1, max(args.steps, args.warmup)))
     ctx = mp.get_context("spawn")
     with ctx.Pool(cores) as pool:
-        pool.map(_pool_task, [args.workload] * max(args.warmup, 1))
+        task = (args.workload, args.kernel)
+        pool.map(_pool_task, [task] * max(args.warmup, 1))
         t0 = time.perf_counter()
-        res = pool.map(_pool_task, [args.workload] * args.steps)
+        res = pool.map(_pool_task, [task] * args.steps)
         wall = time.perf_counter() - t0
     tokens = sum(t for _, t in res)
     value = tokens / wall
@@ -233,7 +240,8 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": args.workload, "sample": "one (b,h) slice per step"},
+        "data": "synthetic", "config": {"workload": args.workload, "kernel": args.kernel,
+                                        "sample": "one (b,h) slice per step"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{args.steps} steps x one (b,h) slice of {args.workload}, "
                                    f"fwd+bwd, fp64, {cores} processes x 1 thread"},
@@ -257,11 +265,12 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
-    w = WORKLOADS[args.workload]
+    import dataclasses
+    w = dataclasses.replace(WORKLOADS[args.workload], kernel=args.kernel)
     if args.batch or args.heads:
-        import dataclasses
         w = dataclasses.replace(w, B=args.batch or w.B, H=args.heads or w.H)
-    p = api.Params(w.B, w.H, w.grid_h, w.grid_w, w.d, w.m, w.lam, w.eps, w.iters, w.tied, w.norm)
+    p = api.Params(w.B, w.H, w.grid_h, w.grid_w, w.d, w.m, w.lam, w.eps, w.iters, w.tied, w.norm,
+                   w.kernel)
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     inp = make_inputs(w, with_grad=True)
     host = {n: torch.from_numpy(np.ascontiguousarray(inp[n])).to(tdt) for n in ("q", "k", "v", "dout")}
@@ -327,7 +336,7 @@ def run_ours(args, rank, world, local_rank):
     achieved = per_launch_ops[dom] / (dom_ms / 1e3) / 1e12
     total_ops = sum(ops.values())
     pipe = fp32_pipe_ops(w)
-    traffic = measured_traffic(w.name, dom)
+    traffic = measured_traffic(w.name, w.kernel, dom)
     roofline = {
         "bound": "alu", "kernel": dom, "achieved": achieved, "peak": ALU_PEAK_TOPS,
         "unit": "Tlaneop/s", "frac": achieved / ALU_PEAK_TOPS,
@@ -376,13 +385,14 @@ def run_ours(args, rank, world, local_rank):
         return
     base = None
     if world == 1 and not args.no_cpu_baseline:
-        base = cpu_baseline(args.workload)
+        base = cpu_baseline(args.workload, args.kernel)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic (seeded N(0,1) plus 1% Student-t tokens in Q and K)",
-        "config": {"workload": args.workload, "B": w.B, "H": w.H, "N": w.N, "grid": [w.grid_h, w.grid_w],
+        "config": {"workload": args.workload, "kernel": w.kernel, "B": w.B, "H": w.H, "N": w.N,
+                   "grid": [w.grid_h, w.grid_w],
                    "d": w.d, "m": w.m, "iters": w.iters, "lambda": w.lam, "eps": w.eps,
                    "norm": w.norm, "tied": w.tied, "pass": "fwd+bwd",
                    "l2": "inputs larger than L2 (Q, K, V, dO 134 MB each, 129 MB L2); no flush",
@@ -405,7 +415,7 @@ def main():
         # whole slices until at least 10 s of CPU work (a bounded sample)
         sec = tokens = n = 0
         while sec < 10.0 or n == 0:
-            s1, t1 = _oracle_slice(args.workload)
+            s1, t1 = _oracle_slice(args.workload, args.kernel)
             sec, tokens, n = sec + s1, tokens + t1, n + 1
         print(json.dumps([sec, tokens, n]))
         return
