@@ -59,6 +59,15 @@ cudaError_t run_query_tc(const Prob& p, const void* q, const float* pack, const 
                          void* out, float* kvout, cudaStream_t st);
 cudaError_t run_key_tc(const Prob& p, const void* k, const void* v, const float* L, float* part,
                        float* kvout, cudaStream_t st);
+// the same passes for the Gaussian kernel with the distances on the tensor
+// cores too (|x|^2 + |l|^2 - 2 x.l); run_pack_qg writes the landmark records
+// (BH * nt * (64 d + 64) floats) at packL and the W-hat tiles at packW
+cudaError_t run_pack_qg(const Prob& p, const float* L, const float* What, void* packL, float* packW,
+                        cudaStream_t st);
+cudaError_t run_query_gtc(const Prob& p, const void* q, const void* packL, const float* packW,
+                          const float* stats, void* out, float* kvout, cudaStream_t st);
+cudaError_t run_key_gtc(const Prob& p, const void* k, const void* v, const float* L, float* part,
+                        float* kvout, cudaStream_t st);
 // landmarks: L [BH][m][d] f32, idx [N] int32 (may be null)
 cudaError_t run_pool(const Prob& p, const void* k, float* L, int32_t* idx, cudaStream_t st);
 

@@ -525,7 +525,9 @@ int key_tc_splits(int BH, int m, int nblk) {
   return s;
 }
 
-size_t pack_q_floats(const Prob& p) { return 2 * (size_t)p.BH * p.nt * p.d * TL; }
+// landmark and W-hat tiles; the Gaussian variant's landmark records also carry
+// the 64 squared norms of each tile
+size_t pack_q_floats(const Prob& p) { return 2 * (size_t)p.BH * p.nt * p.d * TL + (size_t)p.BH * p.nt * TL; }
 
 template <int D>
 static cudaError_t pack_q_t(const Prob& p, const float* L, const float* What, float* pack,

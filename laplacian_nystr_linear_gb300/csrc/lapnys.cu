@@ -430,7 +430,10 @@ int lapnys_fwd(const void* q, const void* k, const void* v, void* out, int B, in
   float* kpart = (float*)(wb + w.kpart);
   const bool tc = fwd_tc_ok(p);
   if (tc) {
-    CK(run_key_tc(p, k, v, L, kpart, full ? (float*)(cb + c.C) : nullptr, stream));
+    if (p.gauss())
+      CK(run_key_gtc(p, k, v, L, kpart, full ? (float*)(cb + c.C) : nullptr, stream));
+    else
+      CK(run_key_tc(p, k, v, L, kpart, full ? (float*)(cb + c.C) : nullptr, stream));
     CK(run_reduce_parts(p.BH, p.Skt, m, p.mp, d, kpart, W, stream));
   } else {
     CK(run_key_fwd(p, k, v, L, kpart, full ? (float*)(cb + c.C) : nullptr, stream));
@@ -447,8 +450,14 @@ int lapnys_fwd(const void* q, const void* k, const void* v, void* out, int B, in
   }
   if (tc) {
     float* fpack = (float*)(wb + w.fpack);
-    CK(run_pack_q(p, L, What, fpack, stream));
-    CK(run_query_tc(p, q, fpack, stats, out, full ? (float*)(cb + c.P) : nullptr, stream));
+    if (p.gauss()) {
+      float* packW = fpack + (size_t)p.BH * p.nt * (64 * d + 64);
+      CK(run_pack_qg(p, L, What, fpack, packW, stream));
+      CK(run_query_gtc(p, q, fpack, packW, stats, out, full ? (float*)(cb + c.P) : nullptr, stream));
+    } else {
+      CK(run_pack_q(p, L, What, fpack, stream));
+      CK(run_query_tc(p, q, fpack, stats, out, full ? (float*)(cb + c.P) : nullptr, stream));
+    }
   } else {
     CK(run_query_fwd(p, q, L, What, stats, out, full ? (float*)(cb + c.P) : nullptr, stream));
   }
@@ -501,7 +510,10 @@ int lapnys_fwd_static(const void* q, const void* k, const void* v, void* out, in
   float* kpart = (float*)(wb + w.kpart);
   const bool tc = fwd_tc_ok(p);
   if (tc) {
-    CK(run_key_tc(p, k, v, L, kpart, nullptr, stream));
+    if (p.gauss())
+      CK(run_key_gtc(p, k, v, L, kpart, nullptr, stream));
+    else
+      CK(run_key_tc(p, k, v, L, kpart, nullptr, stream));
     CK(run_reduce_parts(p.BH, p.Skt, m, p.mp, d, kpart, W, stream));
   } else {
     CK(run_key_fwd(p, k, v, L, kpart, nullptr, stream));
@@ -517,8 +529,14 @@ int lapnys_fwd_static(const void* q, const void* k, const void* v, void* out, in
   }
   if (tc) {
     float* fpack = (float*)(wb + w.fpack);
-    CK(run_pack_q(p, L, What, fpack, stream));
-    CK(run_query_tc(p, q, fpack, stats, out, nullptr, stream));
+    if (p.gauss()) {
+      float* packW = fpack + (size_t)p.BH * p.nt * (64 * d + 64);
+      CK(run_pack_qg(p, L, What, fpack, packW, stream));
+      CK(run_query_gtc(p, q, fpack, packW, stats, out, nullptr, stream));
+    } else {
+      CK(run_pack_q(p, L, What, fpack, stream));
+      CK(run_query_tc(p, q, fpack, stats, out, nullptr, stream));
+    }
   } else {
     CK(run_query_fwd(p, q, L, What, stats, out, nullptr, stream));
   }

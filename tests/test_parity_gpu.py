@@ -312,11 +312,14 @@ def test_gaussian_backward_small_cases(w):
     g = gpu_run(w, inp, backward=True)
     o = oracle_run(w, inp, backward=True)
     print(w.name, compare(w, g, o, backward=True))
+    # bf16 with d = 32 / 64 and m > 64 forms the distances on the tensor cores with the
+    # landmarks rounded to TF32 (moved by at most 2^-11 relative): kernel values to 1e-4
+    tc = w.dtype == "bf16" and w.d in (32, 64) and w.m > 64
     for (b, h), s in o["saved"].items():
         c = g["ctx"]
         assert rel(c["A"][b, h], s["A"]) < 1e-6            # Gaussian landmark matrix
-        assert rel(c["P"][b, h], s["P"]) < 1e-5            # kernel values stored as computed
-        assert rel(c["C"][b, h], s["C"].T) < 1e-5
+        assert rel(c["P"][b, h], s["P"]) < (1e-4 if tc else 1e-5)
+        assert rel(c["C"][b, h], s["C"].T) < (1e-4 if tc else 1e-5)
 
 
 @pytest.mark.parametrize("backward", [False, True])
