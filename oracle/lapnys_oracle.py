@@ -97,20 +97,46 @@ def kernel_matrix(X: np.ndarray, Y: np.ndarray, lam: float, kernel: str = "lapla
 # --------------------------------------------------------------------------
 # landmarks  [LF-ar 2c.1: landmark keys chosen by average pooling;
 #             SOFT Proposed method: average pooling preferred]
-# Reading: non-overlapping sqrt(m) x sqrt(m) windows that tile the grid exactly;
-# landmark a = i * mw + j for window row i, column j (row-major).
+# Readings: a grid of mh x mw landmarks, m = mh mw, in row-major order.  A
+# square m takes mh = mw = sqrt(m); any other m the factor pair whose shape is
+# closest to the token grid's (|log(mh / mw) - log(H / W)| smallest, ties to the
+# smaller mh).  Window row i spans token rows [floor(i H / mh), floor((i+1) H / mh))
+# and window column j token columns [floor(j W / mw), floor((j+1) W / mw)): the
+# windows partition the grid, all of one size when mh | H and mw | W, otherwise
+# of sizes floor and ceil of H / mh (adaptive pooling without overlap).
 # --------------------------------------------------------------------------
+def landmark_grid(grid_h: int, grid_w: int, m: int):
+    """(mh, mw) for m landmarks on a grid_h x grid_w token grid."""
+    if m < 1:
+        raise ValueError("m must be positive")
+    r = math.isqrt(m)
+    if r * r == m:
+        mh, mw = r, r
+    else:
+        best = None
+        for a in range(1, m + 1):
+            if m % a:
+                continue
+            key = abs(math.log(a / (m // a)) - math.log(grid_h / grid_w))
+            if best is None or key < best[0] - 1e-12:
+                best = (key, a, m // a)
+        mh, mw = best[1], best[2]
+    if mh > grid_h or mw > grid_w:
+        raise ValueError("more landmark rows or columns than token rows or columns")
+    return mh, mw
+
+
 def pool_index(grid_h: int, grid_w: int, m: int) -> np.ndarray:
     """token n = y * grid_w + x  ->  landmark of the window containing (y, x)."""
-    mh = math.isqrt(m)
-    if mh * mh != m or grid_h % mh or grid_w % mh:
-        raise ValueError("m must be a square whose root divides both grid sides")
-    mw = mh
-    sh, sw = grid_h // mh, grid_w // mw
+    mh, mw = landmark_grid(grid_h, grid_w, m)
     idx = np.empty(grid_h * grid_w, dtype=np.int64)
-    for y in range(grid_h):
-        for x in range(grid_w):
-            idx[y * grid_w + x] = (y // sh) * mw + (x // sw)
+    for i in range(mh):
+        y0, y1 = (i * grid_h) // mh, ((i + 1) * grid_h) // mh
+        for j in range(mw):
+            x0, x1 = (j * grid_w) // mw, ((j + 1) * grid_w) // mw
+            for y in range(y0, y1):
+                for x in range(x0, x1):
+                    idx[y * grid_w + x] = i * mw + j
     return idx
 
 

@@ -5,7 +5,10 @@ not against the oracle's own formulas.
   symmetry  (LaplacianFormer, Methodology 1 / Arabic summary 2a; SOFT review,
   Proposed method: the kernel is symmetric with values in [0, 1]).
 - Average-pooling windows enumerated by coordinates (LaplacianFormer Arabic
-  summary 2c.1; SOFT review, Proposed method: average pooling).
+  summary 2c.1; SOFT review, Proposed method: average pooling); adaptive
+  windows (the reading for grids the landmark grid does not divide, and for
+  non-square m) checked as a partition of the grid, by a worked example and by
+  finite differences through the pooling.
 - eps I makes A strictly positive definite (LaplacianFormer Methodology 2).
 - Truncated Newton-Schulz against its closed form through a library eigensolver;
   the residual |I - A X_t| falls monotonically (SOFT review, Proposed method).
@@ -76,9 +79,76 @@ def test_pool_windows_by_enumeration(gh, gw, m):
 
 
 def test_pool_rejects_bad_geometry():
-    for args in [(14, 14, 48), (14, 14, 16), (10, 12, 9)]:
+    # more landmark rows or columns than the grid has, or no landmarks
+    for args in [(4, 4, 25), (2, 8, 9), (4, 4, 7), (4, 4, 0)]:
         with pytest.raises(ValueError):
             orc.pool_index(*args)
+
+
+def test_landmark_grid_shapes():
+    # square m keeps a square landmark grid; other m take the factor pair shaped like the grid
+    assert orc.landmark_grid(14, 14, 49) == (7, 7)
+    assert orc.landmark_grid(14, 14, 16) == (4, 4)       # not dividing 14: adaptive windows
+    assert orc.landmark_grid(128, 64, 128) == (16, 8)
+    assert orc.landmark_grid(20, 10, 50) == (10, 5)
+    assert orc.landmark_grid(8, 16, 32) == (4, 8)
+    assert orc.landmark_grid(14, 14, 48) == (6, 8)       # shapes 6 x 8 and 8 x 6 tie: smaller mh
+
+
+@pytest.mark.parametrize("gh,gw,m", [(14, 14, 16), (10, 12, 9), (7, 9, 6), (5, 5, 4), (20, 10, 50)])
+def test_adaptive_windows_partition_the_grid(gh, gw, m):
+    idx = orc.pool_index(gh, gw, m)
+    mh, mw = orc.landmark_grid(gh, gw, m)
+    assert idx.min() == 0 and idx.max() == m - 1
+    grid = idx.reshape(gh, gw)
+    rows, cols = grid // mw, grid % mw
+    # each window row is one band of consecutive token rows, each window column one band of columns
+    for y in range(gh):
+        assert len(set(rows[y])) == 1
+    for x in range(gw):
+        assert len(set(cols[:, x])) == 1
+    rsize = np.bincount(rows[:, 0], minlength=mh)
+    csize = np.bincount(cols[0], minlength=mw)
+    assert set(rsize) <= {gh // mh, -(-gh // mh)} and rsize.sum() == gh
+    assert set(csize) <= {gw // mw, -(-gw // mw)} and csize.sum() == gw
+    assert np.all(np.diff(rows[:, 0]) >= 0) and np.all(np.diff(cols[0]) >= 0)
+
+
+def test_adaptive_windows_worked_example():
+    # 14 token rows into 4 window rows: starts floor(i * 14 / 4) = 0, 3, 7, 10 (sizes 3, 4, 3, 4)
+    idx = orc.pool_index(14, 14, 16).reshape(14, 14)
+    np.testing.assert_array_equal(idx[:, 0] // 4, [0, 0, 0, 1, 1, 1, 1, 2, 2, 2, 3, 3, 3, 3])
+    np.testing.assert_array_equal(idx[0] % 4, [0, 0, 0, 1, 1, 1, 1, 2, 2, 2, 3, 3, 3, 3])
+    # window means by loops
+    rng = np.random.default_rng(9)
+    K = rng.standard_normal((196, 2))
+    L = orc.pool_landmarks(K, idx.reshape(-1), 16)
+    for a in range(16):
+        members = [n for n in range(196) if idx.reshape(-1)[n] == a]
+        np.testing.assert_allclose(L[a], K[members].mean(axis=0), rtol=1e-13, atol=1e-15)
+
+
+def test_backward_through_adaptive_pooling_matches_finite_differences():
+    rng = np.random.default_rng(40)
+    gh, gw, m, d, T, lam, eps = 5, 5, 4, 3, 3, 3.0, 1e-3
+    N = gh * gw
+    q, k, v, R = (rng.standard_normal((N, d)) for _ in range(4))
+
+    def loss(k_):
+        O, _ = orc.forward_slice(q, k_, v, gh, gw, m, lam, eps, T)
+        return float((O * R).sum())
+
+    _, saved = orc.forward_slice(q, k, v, gh, gw, m, lam, eps, T)
+    _, dk, _ = orc.backward_slice(saved, R)
+    h = 1e-6
+    fd = np.zeros_like(k)
+    for i in range(N):
+        for c in range(d):
+            kp, km = k.copy(), k.copy()
+            kp[i, c] += h
+            km[i, c] -= h
+            fd[i, c] = (loss(kp) - loss(km)) / (2 * h)
+    assert np.linalg.norm(dk - fd) / np.linalg.norm(fd) < 1e-6
 
 
 def test_one_landmark_per_token_is_identity():
