@@ -25,9 +25,14 @@
  *    [B][H][N][d] arrays (d innermost), token n = y * grid_w + x on the
  *    grid_h x grid_w grid, 16-byte aligned, all of one element type `dtype`
  *    (LAPNYS_F32 = float, LAPNYS_BF16 = bfloat16).  Arithmetic is float32.
- *  - Landmarks: m = r * r, r divides grid_h and grid_w; landmark a = i * r + j
- *    is the mean of the (grid_h / r) x (grid_w / r) window in window-row i,
- *    window-column j.
+ *  - Landmarks: an mh x mw grid of windows, m = mh * mw; a square m has
+ *    mh = mw = sqrt(m), any other m the factor pair shaped most like the token
+ *    grid (smallest |log(mh / mw) - log(grid_h / grid_w)|, ties to the smaller
+ *    mh).  Landmark a = i * mw + j is the mean of token rows
+ *    [floor(i grid_h / mh), floor((i + 1) grid_h / mh)) and columns
+ *    [floor(j grid_w / mw), floor((j + 1) grid_w / mw)): equal windows when
+ *    mh | grid_h and mw | grid_w, otherwise adaptive windows that still
+ *    partition the grid (EINVAL when mh > grid_h or mw > grid_w).
  *  - The caller owns and allocates everything: out, gradients, `ctx` (state
  *    saved by the forward for the backward) and `ws` (scratch).  The library
  *    allocates no device memory, does not synchronise, and enqueues all work
@@ -73,8 +78,8 @@ enum { LAPNYS_F32 = 0, LAPNYS_BF16 = 1 };
  *               exp(-|x - y|_1 / lambda).  Same ctx, workspace and entry points. */
 enum { LAPNYS_NORM = 1u << 0, LAPNYS_GAUSS = 1u << 1 };
 
-/* Limits of this build: d in {16, 32, 64, 128}; 1 <= m <= N; m a perfect
- * square dividing the grid as above; 0 <= iters <= 64; lambda > 0; eps >= 0;
+/* Limits of this build: d in {16, 32, 64, 128}; 1 <= m <= min(N, 1024); a
+ * landmark grid as above; 0 <= iters <= 64; lambda > 0; eps >= 0;
  * B * H * N * d < 2^31. */
 
 /* Bytes of the caller-owned context written by lapnys_fwd and read by

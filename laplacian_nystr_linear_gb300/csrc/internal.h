@@ -9,7 +9,7 @@
 namespace lapnys {
 
 struct Prob {
-  int B, H, BH, N, d, gh, gw, m, r, sh, sw, iters, tied, dtype;
+  int B, H, BH, N, d, gh, gw, m, mh, mw, iters, tied, dtype;  // mh x mw landmark grid
   unsigned flags;
   float lam, eps;
   float ns;       // -log2(e) / lambda: k = exp2(ns * distance)

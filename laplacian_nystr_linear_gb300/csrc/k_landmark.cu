@@ -13,22 +13,28 @@
 namespace lapnys {
 
 // ---------------------------------------------------------------------------
-// pooling: one CTA per (landmark, slice); threads = (token group, 4-wide chunk)
+// pooling: one CTA per (landmark, slice); threads = (token group, 4-wide chunk).
+// Landmark a = wi * mw + wj averages token rows [wi gh / mh, (wi + 1) gh / mh)
+// and columns [wj gw / mw, (wj + 1) gw / mw) (floors): equal windows when the
+// grid divides, otherwise windows of the floor and ceil sizes.
 // ---------------------------------------------------------------------------
 template <typename T>
 __global__ void __launch_bounds__(kThreads) k_pool(const T* __restrict__ K, float* __restrict__ L,
-                                                   int32_t* __restrict__ idx, int N, int d, int gw,
-                                                   int r, int sh, int sw, int m) {
+                                                   int32_t* __restrict__ idx, int N, int d, int gh,
+                                                   int gw, int mh, int mw, int m) {
   __shared__ float4 red[kThreads];
   const int a = blockIdx.x, bh = blockIdx.y;
-  const int wi = a / r, wj = a % r;
+  const int wi = a / mw, wj = a % mw;
+  const int y0 = wi * gh / mh, y1 = (wi + 1) * gh / mh;
+  const int x0 = wj * gw / mw, x1 = (wj + 1) * gw / mw;
+  const int sw = x1 - x0;
   const int C4 = d / 4, groups = kThreads / C4;
   const int chunk = threadIdx.x % C4, g = threadIdx.x / C4;
-  const int wsz = sh * sw;
+  const int wsz = (y1 - y0) * sw;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   const T* Kb = K + (size_t)bh * N * d;
   for (int t = g; t < wsz; t += groups) {
-    const int n = (wi * sh + t / sw) * gw + wj * sw + t % sw;
+    const int n = (y0 + t / sw) * gw + x0 + t % sw;
     const float4 v = ld4(Kb + (size_t)n * d + chunk * 4);
     acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
   }
@@ -45,17 +51,16 @@ __global__ void __launch_bounds__(kThreads) k_pool(const T* __restrict__ K, floa
         make_float4(s.x * inv, s.y * inv, s.z * inv, s.w * inv));
   }
   if (idx != nullptr && bh == 0)
-    for (int t = threadIdx.x; t < wsz; t += kThreads)
-      idx[(wi * sh + t / sw) * gw + wj * sw + t % sw] = a;
+    for (int t = threadIdx.x; t < wsz; t += kThreads) idx[(y0 + t / sw) * gw + x0 + t % sw] = a;
 }
 
 cudaError_t run_pool(const Prob& p, const void* k, float* L, int32_t* idx, cudaStream_t st) {
   dim3 grid(p.m, p.BH);
   if (p.dtype == 1)
     return launch("pool", k_pool<__nv_bfloat16>, grid, dim3(kThreads), 0, st,
-                  (const __nv_bfloat16*)k, L, idx, p.N, p.d, p.gw, p.r, p.sh, p.sw, p.m);
+                  (const __nv_bfloat16*)k, L, idx, p.N, p.d, p.gh, p.gw, p.mh, p.mw, p.m);
   return launch("pool", k_pool<float>, grid, dim3(kThreads), 0, st, (const float*)k, L, idx, p.N,
-                p.d, p.gw, p.r, p.sh, p.sw, p.m);
+                p.d, p.gh, p.gw, p.mh, p.mw, p.m);
 }
 
 // ---------------------------------------------------------------------------

@@ -831,10 +831,9 @@ template <typename T>
 __global__ void k_finalize(const float* __restrict__ dQp, const float* __restrict__ dKp,
                            const float* __restrict__ dVp, const float* __restrict__ dL,
                            T* __restrict__ dq, T* __restrict__ dk, T* __restrict__ dv, int BH, int N,
-                           int d, int nt, int m, int gw, int r, int sh, int sw, int tied) {
+                           int d, int nt, int m, int gh, int gw, int mh, int mw, int tied) {
   const size_t total4 = (size_t)BH * N * d / 4;
   const size_t plane = (size_t)BH * N * d;
-  const float inv = 1.0f / (float)(sh * sw);
   for (size_t e4 = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e4 < total4;
        e4 += (size_t)gridDim.x * blockDim.x) {
     const size_t e = e4 * 4;
@@ -851,8 +850,12 @@ __global__ void k_finalize(const float* __restrict__ dQp, const float* __restric
       k4.x += b.x; k4.y += b.y; k4.z += b.z; k4.w += b.w;
       v4.x += v.x; v4.y += v.y; v4.z += v.z; v4.w += v.w;
     }
+    // the token's pooling window (rows [wi gh / mh, (wi + 1) gh / mh), floors) and its size
     const int y = n / gw, x = n % gw;
-    const int a = (y / sh) * r + x / sw;
+    const int wi = ((y + 1) * mh - 1) / gh, wj = ((x + 1) * mw - 1) / gw;
+    const int a = wi * mw + wj;
+    const float inv = 1.0f / (float)(((wi + 1) * gh / mh - wi * gh / mh) *
+                                     ((wj + 1) * gw / mw - wj * gw / mw));
     const float4 l4 = *reinterpret_cast<const float4*>(dL + (bh * m + a) * d + c);
     k4.x += l4.x * inv; k4.y += l4.y * inv; k4.z += l4.z * inv; k4.w += l4.w * inv;
     if (tied) {
@@ -872,10 +875,10 @@ cudaError_t run_finalize(const Prob& p, const float* dQp, const float* dKp, cons
   if (p.dtype == 1)
     return launch("finalize", k_finalize<__nv_bfloat16>, dim3(grid_for(n4)), dim3(kThreads), 0, st,
                   dQp, dKp, dVp, dL, (__nv_bfloat16*)dq, (__nv_bfloat16*)dk, (__nv_bfloat16*)dv,
-                  p.BH, p.N, p.d, p.nt, p.m, p.gw, p.r, p.sh, p.sw, p.tied);
+                  p.BH, p.N, p.d, p.nt, p.m, p.gh, p.gw, p.mh, p.mw, p.tied);
   return launch("finalize", k_finalize<float>, dim3(grid_for(n4)), dim3(kThreads), 0, st, dQp, dKp,
-                dVp, dL, (float*)dq, (float*)dk, (float*)dv, p.BH, p.N, p.d, p.nt, p.m, p.gw, p.r,
-                p.sh, p.sw, p.tied);
+                dVp, dL, (float*)dq, (float*)dk, (float*)dv, p.BH, p.N, p.d, p.nt, p.m, p.gh, p.gw,
+                p.mh, p.mw, p.tied);
 }
 
 // zero-fill (used when the Newton-Schulz backward has no step to initialise dA)

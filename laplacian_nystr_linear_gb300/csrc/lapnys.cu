@@ -61,6 +61,37 @@ static int isqrt_exact(int m) {
 
 static int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
+// The mh x mw landmark grid of m landmarks on a gh x gw token grid (average
+// pooling: "LaplacianFormer", Arabic summary 2c.1; "SOFT" review, Proposed
+// method).  Reading: a square m keeps mh = mw = sqrt(m); any other m takes the
+// factor pair shaped most like the token grid (smallest |log(mh / mw) -
+// log(gh / gw)|, ties to the smaller mh).  Window row i spans token rows
+// [floor(i gh / mh), floor((i + 1) gh / mh)), columns alike: a partition of the
+// grid (adaptive pooling without overlap when the grid is not divisible).
+// False when the grid has fewer rows or columns than the landmark grid.
+static bool landmark_grid(int gh, int gw, int m, int* mh, int* mw) {
+  if (gh <= 0 || gw <= 0 || m <= 0) return false;
+  int a = isqrt_exact(m), b = a;
+  if (a < 0) {
+    double best = 0.0;
+    a = -1;
+    const double target = log((double)gh / (double)gw);
+    for (int f = 1; f <= m; ++f) {
+      if (m % f) continue;
+      const double key = fabs(log((double)f / (double)(m / f)) - target);
+      if (a < 0 || key < best - 1e-12) {
+        best = key;
+        a = f;
+        b = m / f;
+      }
+    }
+  }
+  if (a > gh || b > gw) return false;
+  *mh = a;
+  *mw = b;
+  return true;
+}
+
 // token splits so that each pass has roughly 8 CTAs per SM of a 152-SM part;
 // depends on the dimensions only, so results do not depend on the device.
 static int splits_for(int nblk, int nt, int BH) {
@@ -75,7 +106,6 @@ static bool dims_ok(int B, int H, int N, int d, int m, int iters) {
   if (B <= 0 || H <= 0 || N <= 0 || m <= 0 || m > N || iters < 0 || iters > 64) return false;
   if (d <= 0) return false;
   if (m > 1024) return false;
-  if (isqrt_exact(m) < 0) return false;
   if ((long long)B * H * N * d >= (1LL << 31)) return false;
   return true;
 }
@@ -87,9 +117,7 @@ static Prob make_prob(int B, int H, int N, int d, int gh, int gw, int m, float l
   Prob p;
   memset(&p, 0, sizeof(p));
   p.B = B; p.H = H; p.BH = B * H; p.N = N; p.d = d; p.gh = gh; p.gw = gw; p.m = m;
-  p.r = isqrt_exact(m);
-  p.sh = p.r > 0 ? gh / p.r : 0;
-  p.sw = p.r > 0 ? gw / p.r : 0;
+  if (!landmark_grid(gh, gw, m, &p.mh, &p.mw)) p.mh = p.mw = 0;
   p.iters = iters; p.tied = tied; p.dtype = dtype; p.flags = flags;
   p.lam = lam; p.eps = eps;
   p.ns = (float)(-1.4426950408889634 / (double)lam);
@@ -181,8 +209,8 @@ static int check_common(int B, int H, int N, int d, int gh, int gw, int m, float
                         int iters, int dtype, unsigned flags) {
   if (!dims_ok(B, H, N, d, m, iters)) return LAPNYS_EINVAL;
   if (gh <= 0 || gw <= 0 || (long long)gh * gw != N) return LAPNYS_EINVAL;
-  const int r = isqrt_exact(m);
-  if (gh % r != 0 || gw % r != 0) return LAPNYS_EINVAL;
+  int mh = 0, mw = 0;
+  if (!landmark_grid(gh, gw, m, &mh, &mw)) return LAPNYS_EINVAL;
   if (!(lam > 0.f) || !isfinite(lam)) return LAPNYS_EINVAL;
   if (!(eps >= 0.f) || !isfinite(eps)) return LAPNYS_EINVAL;
   if (dtype != LAPNYS_F32 && dtype != LAPNYS_BF16) return LAPNYS_EINVAL;
@@ -357,8 +385,8 @@ size_t lapnys_ctx_bytes(int B, int H, int N, int d, int m, int iters, unsigned f
 
 size_t lapnys_workspace_bytes(int B, int H, int N, int d, int m, int iters, unsigned flags) {
   if (!dims_ok(B, H, N, d, m, iters)) return 0;
-  const int r = isqrt_exact(m);
-  Prob p = make_prob(B, H, N, d, r, N / r, m, 1.f, 0.f, iters, 0, 0, flags);
+  // the workspace depends on the sizes only, not on the grid's shape
+  Prob p = make_prob(B, H, N, d, 1, N, m, 1.f, 0.f, iters, 0, 0, flags);
   return ws_layout(p).total;
 }
 

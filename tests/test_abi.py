@@ -41,7 +41,8 @@ def test_sizes(lib):
     assert c >= 64 * 49 * 256 * 256 * 4
     assert lib.lapnys_workspace_bytes(8, 8, 16384, 64, 256, 24, 0) > 0
     # invalid dimensions give 0
-    assert lib.lapnys_ctx_bytes(1, 1, 196, 32, 48, 20, 0) == 0      # m not square
+    assert lib.lapnys_ctx_bytes(1, 1, 196, 32, 48, 20, 0) > 0       # a non-square m is fine
+    assert lib.lapnys_ctx_bytes(1, 1, 2048, 32, 1089, 20, 0) == 0   # m > 1024
     assert lib.lapnys_ctx_bytes(1, 1, 16, 32, 25, 20, 0) == 0       # m > N
     assert lib.lapnys_ctx_bytes(1, 1, 196, 32, 49, -1, 0) == 0      # iters < 0
     assert lib.lapnys_workspace_bytes(0, 1, 196, 32, 49, 20, 0) == 0
@@ -79,8 +80,12 @@ def _fwd(lib, **kw):
 def test_fwd_rejects_bad_arguments(lib):
     from laplacian_nystr_linear_gb300._lib import LAPNYS_EINVAL, LAPNYS_ENOSPC, LAPNYS_ENOTSUP
     assert _fwd(lib, N=195) == LAPNYS_EINVAL                       # N != grid_h * grid_w
-    assert _fwd(lib, m=48) == LAPNYS_EINVAL                        # m not square
-    assert _fwd(lib, m=36) == LAPNYS_EINVAL                        # 6 does not divide 14
+    assert _fwd(lib, m=225) == LAPNYS_EINVAL                       # a 15 x 15 landmark grid on 14 x 14 tokens
+    assert _fwd(lib, m=58) == LAPNYS_EINVAL                        # 58 = 2 x 29: 29 > 14 columns
+    assert _fwd(lib, m=0) == LAPNYS_EINVAL
+    # adaptive windows (6 does not divide 14) and non-square m pass validation (then fail on ws)
+    assert _fwd(lib, m=36) == LAPNYS_ENOSPC
+    assert _fwd(lib, m=48) == LAPNYS_ENOSPC
     assert _fwd(lib, lam=0.0) == LAPNYS_EINVAL
     assert _fwd(lib, lam=float("nan")) == LAPNYS_EINVAL
     assert _fwd(lib, eps=-1.0) == LAPNYS_EINVAL

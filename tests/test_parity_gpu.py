@@ -40,7 +40,13 @@ def _small(name, **kw):
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("gh,gw,m,d,dtype", [(14, 14, 49, 32, "f32"), (56, 56, 49, 64, "bf16"),
                                              (128, 128, 256, 64, "bf16"), (10, 12, 4, 16, "f32"),
-                                             (8, 8, 64, 128, "f32"), (6, 6, 1, 64, "bf16")])
+                                             (8, 8, 64, 128, "f32"), (6, 6, 1, 64, "bf16"),
+                                             # adaptive windows (grid not divisible)
+                                             (14, 14, 16, 32, "f32"), (10, 12, 9, 16, "bf16"),
+                                             (18, 22, 100, 64, "bf16"),
+                                             # non-square m
+                                             (16, 8, 32, 64, "f32"), (20, 12, 15, 32, "f32"),
+                                             (7, 9, 6, 16, "bf16"), (24, 16, 96, 32, "bf16")])
 def test_pool_indices_exact_and_values(gh, gw, m, d, dtype):
     inp = random_inputs(100 + m, 2, 3, gh * gw, d, dtype)
     k = to_dev(inp["k"], dtype)
@@ -294,6 +300,37 @@ def test_sparse_ties_are_corrected(m):
             assert np.all(err <= 2.0 ** -8 * np.abs(ref) + 1e-3 * rms), (name, h, err.max(), rms)
         # blocks whose ties went through the correction (not the exact path)
         assert n_corr >= (32 if x == "q" else (16 if m == 64 else 0)), (name, n_corr)
+
+
+# ---------------------------------------------------------------------------
+# landmark grids beyond equal square windows: adaptive windows (the grid is not
+# divisible by the landmark grid) and non-square m
+# ---------------------------------------------------------------------------
+GRIDS = [
+    _small("adaptive_f32", grid_h=14, grid_w=14, m=16, d=32, iters=8),
+    _small("adaptive_bf16_norm", dtype="bf16", grid_h=10, grid_w=12, m=9, d=64, iters=8, norm=True),
+    _small("adaptive_tc", dtype="bf16", grid_h=18, grid_w=22, m=100, d=64, iters=8),
+    _small("nonsquare_f32", grid_h=16, grid_w=8, m=32, d=32, iters=8),
+    _small("nonsquare_bf16", dtype="bf16", grid_h=20, grid_w=12, m=15, d=64, iters=8, tied=True),
+    _small("nonsquare_tc_cluster", dtype="bf16", grid_h=24, grid_w=16, m=96, d=32, iters=10),
+]
+
+
+@pytest.mark.parametrize("w", GRIDS, ids=lambda w: w.name)
+def test_landmark_grids(w):
+    inp = random_inputs(51 + w.m, w.B, w.H, w.N, w.d, w.dtype, tied=w.tied)
+    g = gpu_run(w, inp, backward=True)
+    o = oracle_run(w, inp, backward=True)
+    print(w.name, compare(w, g, o, backward=True))
+    np.testing.assert_array_equal(g["ctx"]["idx"], orc.pool_index(w.grid_h, w.grid_w, w.m))
+
+
+def test_landmark_grid_gaussian():
+    w = dataclasses.replace(GRIDS[2], name="adaptive_tc_gauss", kernel="gauss")
+    inp = random_inputs(61, w.B, w.H, w.N, w.d, w.dtype)
+    g = gpu_run(w, inp, backward=True)
+    o = oracle_run(w, inp, backward=True)
+    print(w.name, compare(w, g, o, backward=True))
 
 
 # ---------------------------------------------------------------------------
