@@ -188,11 +188,16 @@ def newton_schulz(A: np.ndarray, iters: int):
 # queries; biased variance; eta inside the square root; gradients flow
 # through mean and variance; applied to P only, never to C.
 # --------------------------------------------------------------------------
-def feature_map(P: np.ndarray, norm: bool):
+def feature_map(P: np.ndarray, norm: bool, stats=None):
+    """Z from P; `stats` = (mu, var) taken over a larger set of queries (the
+    batch-pooled variant) instead of this slice's."""
     if not norm:
         return P, None
-    mu = P.mean(axis=0)
-    var = ((P - mu) ** 2).mean(axis=0)
+    if stats is None:
+        mu = P.mean(axis=0)
+        var = ((P - mu) ** 2).mean(axis=0)
+    else:
+        mu, var = stats
     s = np.sqrt(var + ETA)
     return (P - mu) / s, (mu, var, s)
 
@@ -201,7 +206,8 @@ def feature_map(P: np.ndarray, norm: bool):
 # forward  [SOFT Proposed method: S-hat = P^T A^+ P, read for separate Q and K as
 #  O = k(Q, L) A^+ (k(L, K) V), no row normalisation]
 # --------------------------------------------------------------------------
-def forward_slice(q, k, v, grid_h, grid_w, m, lam, eps, iters, norm=False, kernel="laplace"):
+def forward_slice(q, k, v, grid_h, grid_w, m, lam, eps, iters, norm=False, kernel="laplace",
+                  stats=None):
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
     v = np.asarray(v, dtype=np.float64)
@@ -213,7 +219,7 @@ def forward_slice(q, k, v, grid_h, grid_w, m, lam, eps, iters, norm=False, kerne
     W = C @ v
     What = X[-1] @ W
     P = kernel_matrix(q, L, lam, kernel)
-    Z, stats = feature_map(P, norm)
+    Z, stats = feature_map(P, norm, stats)
     O = Z @ What
     saved = dict(q=q, k=k, v=v, idx=idx, L=L, A=A, X=X, Y=Y, C=C, W=W, What=What,
                  P=P, Z=Z, stats=stats, lam=lam, eps=eps, m=m, norm=norm, kernel=kernel)
@@ -258,8 +264,11 @@ def _kernel_grad_y(G, X, Y, lam, kernel="laplace"):
     return dY
 
 
-def backward_slice(saved, dO, tied=False):
-    """Return (dq, dk, dv); with tied=True, dq holds the whole gradient of the shared tensor."""
+def backward_slice(saved, dO, tied=False, dz_means=None):
+    """Return (dq, dk, dv); with tied=True, dq holds the whole gradient of the shared tensor.
+
+    dz_means = (mean dZ, mean dZ*Z) over the queries the statistics were taken
+    over (the batch-pooled variant); by default this slice's."""
     dO = np.asarray(dO, dtype=np.float64)
     lam = saved["lam"]
     L, A, X, Y, C, W, What = (saved[n] for n in ("L", "A", "X", "Y", "C", "W", "What"))
@@ -273,7 +282,8 @@ def backward_slice(saved, dO, tied=False):
     # feature map (batch-norm style reverse of centring and diagonal whitening)
     if saved["norm"]:
         _, _, s = saved["stats"]
-        dP = (dZ - dZ.mean(axis=0) - Z * (dZ * Z).mean(axis=0)) / s
+        m0, m1 = (dZ.mean(axis=0), (dZ * Z).mean(axis=0)) if dz_means is None else dz_means
+        dP = (dZ - m0 - Z * m1) / s
     else:
         dP = dZ
     # P = k(q, L)
@@ -321,28 +331,61 @@ def backward_slice(saved, dO, tied=False):
 # --------------------------------------------------------------------------
 # batched drivers over [B, H, N, d]
 # --------------------------------------------------------------------------
+# Batch-pooled statistics (norm_batch), the other reading of the feature-map
+#  statistics  [LF-ar 2b: the diagonal estimate normalises each feature
+#  dimension on its own, taken over the batch]: mean and variance per head and
+#  landmark column over the B * N queries of all B slices of that head, instead
+#  of over one slice's N queries.  The backward's column means of dZ and dZ * Z
+#  are then taken over the same B * N queries.
+def _batch_stats(q, k, grid_h, grid_w, m, lam, kernel, h):
+    """(mu, var) of P over the B * N queries of head h."""
+    idx = pool_index(grid_h, grid_w, m)
+    Ps = [kernel_matrix(np.asarray(q[b, h], np.float64),
+                        pool_landmarks(k[b, h], idx, m), lam, kernel) for b in range(q.shape[0])]
+    P = np.concatenate(Ps, axis=0)
+    mu = P.mean(axis=0)
+    return mu, ((P - mu) ** 2).mean(axis=0)
+
+
 def forward(q, k, v, grid_h, grid_w, m, lam, eps, iters, norm=False, slices=None,
-            kernel="laplace"):
+            kernel="laplace", norm_batch=False):
     """O [B, H, N, d] and the per-slice saved state (list)."""
     B, H, N, d = q.shape
     O = np.zeros((B, H, N, d))
     saved = {}
-    for b in range(B):
-        for h in range(H):
+    for h in range(H):
+        if slices is not None and not any((b, h) in slices for b in range(B)):
+            continue
+        st = _batch_stats(q, k, grid_h, grid_w, m, lam, kernel, h) if norm and norm_batch else None
+        for b in range(B):
             if slices is not None and (b, h) not in slices:
                 continue
             O[b, h], saved[(b, h)] = forward_slice(q[b, h], k[b, h], v[b, h], grid_h, grid_w,
-                                                   m, lam, eps, iters, norm, kernel)
+                                                   m, lam, eps, iters, norm, kernel, st)
+            saved[(b, h)]["norm_batch"] = bool(norm and norm_batch)
     return O, saved
 
 
 def backward(saved, dO, tied=False):
-    """Gradients for every slice in `saved`; returns dicts keyed by (b, h)."""
+    """Gradients for every slice in `saved`; returns dicts keyed by (b, h).
+
+    With batch-pooled statistics every slice of a head must be in `saved`."""
+    means = {}
+    for (b, h), s in saved.items():
+        if s.get("norm_batch") and h not in means:
+            keys = [kk for kk in saved if kk[1] == h]
+            dZ = [dO[kk[0], kk[1]] @ saved[kk]["What"].T for kk in keys]
+            Zs = [saved[kk]["Z"] for kk in keys]
+            dz = np.concatenate(dZ, axis=0)
+            zz = np.concatenate([a * z for a, z in zip(dZ, Zs)], axis=0)
+            means[h] = (dz.mean(axis=0), zz.mean(axis=0))
     out = {}
     for key, s in saved.items():
-        out[key] = backward_slice(s, dO[key[0], key[1]], tied)
+        out[key] = backward_slice(s, dO[key[0], key[1]], tied, means.get(key[1]))
     return out
 
 
-def attention(q, k, v, grid_h, grid_w, m, lam, eps, iters, norm=False, kernel="laplace"):
-    return forward(q, k, v, grid_h, grid_w, m, lam, eps, iters, norm, kernel=kernel)[0]
+def attention(q, k, v, grid_h, grid_w, m, lam, eps, iters, norm=False, kernel="laplace",
+              norm_batch=False):
+    return forward(q, k, v, grid_h, grid_w, m, lam, eps, iters, norm, kernel=kernel,
+                   norm_batch=norm_batch)[0]

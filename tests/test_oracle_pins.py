@@ -360,3 +360,78 @@ def test_gaussian_dv_is_linear_map_transpose():
     np.testing.assert_allclose(O, M @ v, rtol=1e-12, atol=1e-12)
     _, _, dv = orc.backward_slice(s, dO)
     np.testing.assert_allclose(dv, M.T @ dO, rtol=1e-12, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
+# batch-pooled feature-map statistics
+# --------------------------------------------------------------------------
+def _batch(seed, B, H, N, d, tied=False):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((B, H, N, d))
+    k = q.copy() if tied else rng.standard_normal((B, H, N, d))
+    v = rng.standard_normal((B, H, N, d))
+    return q, k, v
+
+
+def test_batch_stats_invariants():
+    # pooled over the B slices of a head: zero column means and the whitened
+    # variance over all B * N queries, but not within one slice
+    B, H, N, d, m = 3, 2, 64, 8, 16
+    q, k, v = _batch(31, B, H, N, d)
+    _, saved = orc.forward(q, k, v, 8, 8, m, float(d), 1e-3, 5, norm=True, norm_batch=True)
+    for h in range(H):
+        Z = np.concatenate([saved[(b, h)]["Z"] for b in range(B)], axis=0)
+        P = np.concatenate([saved[(b, h)]["P"] for b in range(B)], axis=0)
+        np.testing.assert_allclose(Z.mean(axis=0), 0.0, atol=1e-12)
+        var = P.var(axis=0)
+        np.testing.assert_allclose(Z.var(axis=0), var / (var + orc.ETA), rtol=1e-10)
+        assert np.abs(saved[(0, h)]["Z"].mean(axis=0)).max() > 1e-3
+
+
+def test_batch_stats_reduce_to_per_slice():
+    # one slice per head, or every slice of a head the same: the pooled
+    # statistics are the slice's own
+    q, k, v = _batch(32, 1, 2, 36, 4)
+    a = orc.attention(q, k, v, 6, 6, 9, 4.0, 1e-3, 6, norm=True)
+    b = orc.attention(q, k, v, 6, 6, 9, 4.0, 1e-3, 6, norm=True, norm_batch=True)
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-12)
+    q2, k2, v2 = (np.concatenate([t, t, t], axis=0) for t in (q, k, v))
+    c = orc.attention(q2, k2, v2, 6, 6, 9, 4.0, 1e-3, 6, norm=True, norm_batch=True)
+    for bb in range(3):
+        np.testing.assert_allclose(c[bb], a[0], rtol=1e-10, atol=1e-12)
+    # without norm the flag changes nothing
+    np.testing.assert_array_equal(orc.attention(q2, k2, v2, 6, 6, 9, 4.0, 1e-3, 6),
+                                  orc.attention(q2, k2, v2, 6, 6, 9, 4.0, 1e-3, 6,
+                                                norm_batch=True))
+
+
+@pytest.mark.parametrize("tied,kernel", [(False, "laplace"), (True, "laplace"),
+                                         (False, "gauss")])
+def test_batch_stats_backward_matches_finite_differences(tied, kernel):
+    # the statistics couple the B slices of a head (not the heads): the loss
+    # is summed over every slice, and every input entry is perturbed
+    B, H, N, d, m, T, lam, eps = 2, 2, 16, 4, 4, 3, 4.0, 1e-3
+    q, k, v = _batch(33 + tied, B, H, N, d, tied)
+    R = np.random.default_rng(40).standard_normal((B, H, N, d))
+
+    def loss(q_, k_, v_):
+        O = orc.attention(q_, q_ if tied else k_, v_, 4, 4, m, lam, eps, T, True, kernel, True)
+        return float((O * R).sum())
+
+    _, saved = orc.forward(q, k, v, 4, 4, m, lam, eps, T, True, kernel=kernel, norm_batch=True)
+    g = orc.backward(saved, R, tied=tied)
+    grads = {n: np.stack([np.stack([g[(b, hh)][i] for hh in range(H)]) for b in range(B)])
+             for i, n in enumerate(("q", "k", "v"))}
+    h = 1e-6
+    for name in (("q", "v") if tied else ("q", "k", "v")):
+        base = {"q": q, "k": k, "v": v}
+        fd = np.zeros(q.shape)
+        for ix in np.ndindex(q.shape):
+            plus = {n: a.copy() for n, a in base.items()}
+            minus = {n: a.copy() for n, a in base.items()}
+            plus[name][ix] += h
+            minus[name][ix] -= h
+            fd[ix] = (loss(plus["q"], plus["k"], plus["v"])
+                      - loss(minus["q"], minus["k"], minus["v"])) / (2 * h)
+        err = np.linalg.norm(grads[name] - fd) / np.linalg.norm(fd)
+        assert err < 1e-6, (name, err)
