@@ -389,3 +389,64 @@ def attention(q, k, v, grid_h, grid_w, m, lam, eps, iters, norm=False, kernel="l
               norm_batch=False):
     return forward(q, k, v, grid_h, grid_w, m, lam, eps, iters, norm, kernel=kernel,
                    norm_batch=norm_batch)[0]
+
+
+# --------------------------------------------------------------------------
+# attention block: projections around the path
+#  [SOFT Proposed method: the attention is instantiated as one layer of a
+#   pyramid vision-transformer backbone with embedding width d_e and h heads]
+# Readings: the plain multi-head layer — Q, K, V = X W + b from one weight
+# w_qkv [C, S*H*d] whose column blocks are (Q | K | V), each H heads of d
+# columns, head h at columns h*d .. h*d + d - 1 of its block (S = 2 with the
+# (Q = K | V) blocks in tied mode); the heads' outputs concatenated in the same
+# order and projected by w_o [H*d, C] plus b_o.  Biases may be None (zero).
+# --------------------------------------------------------------------------
+def _heads(Y, B, N, H, d):
+    """[B, N, H*d] -> [B, H, N, d]"""
+    return Y.reshape(B, N, H, d).transpose(0, 2, 1, 3)
+
+
+def _unheads(Y):
+    """[B, H, N, d] -> [B, N, H*d]"""
+    B, H, N, d = Y.shape
+    return Y.transpose(0, 2, 1, 3).reshape(B, N, H * d)
+
+
+def block_forward(x, w_qkv, b_qkv, w_o, b_o, H, d, grid_h, grid_w, m, lam, eps, iters,
+                  norm=False, kernel="laplace", norm_batch=False, tied=False):
+    """y [B, N, C] and the saved state of the block."""
+    x = np.asarray(x, np.float64)
+    B, N, C = x.shape
+    S = 2 if tied else 3
+    w_qkv = np.asarray(w_qkv, np.float64)
+    assert w_qkv.shape == (C, S * H * d)
+    qkv = x @ w_qkv + (0.0 if b_qkv is None else np.asarray(b_qkv, np.float64))
+    blocks = [_heads(qkv[..., s * H * d:(s + 1) * H * d], B, N, H, d) for s in range(S)]
+    q, v = blocks[0], blocks[-1]
+    k = q if tied else blocks[1]
+    O, saved = forward(q, k, v, grid_h, grid_w, m, lam, eps, iters, norm, kernel=kernel,
+                       norm_batch=norm_batch)
+    Ot = _unheads(O)
+    y = Ot @ np.asarray(w_o, np.float64) + (0.0 if b_o is None else np.asarray(b_o, np.float64))
+    st = dict(x=x, w_qkv=w_qkv, w_o=np.asarray(w_o, np.float64), Ot=Ot, attn=saved, H=H, d=d,
+              tied=tied, qkv=qkv)
+    return y, st
+
+
+def block_backward(st, dy):
+    """(dx, dw_qkv, db_qkv, dw_o, db_o) for the block."""
+    dy = np.asarray(dy, np.float64)
+    B, N, C = dy.shape
+    H, d = st["H"], st["d"]
+    dw_o = np.einsum("bnk,bnc->kc", st["Ot"], dy)
+    db_o = dy.sum(axis=(0, 1))
+    dO = _heads(dy @ st["w_o"].T, B, N, H, d)
+    g = backward(st["attn"], dO, tied=st["tied"])
+    grad = {n: np.stack([np.stack([g[(b, h)][i] for h in range(H)]) for b in range(B)])
+            for i, n in enumerate(("q", "k", "v"))}
+    parts = [grad["q"], grad["v"]] if st["tied"] else [grad["q"], grad["k"], grad["v"]]
+    dqkv = np.concatenate([_unheads(t) for t in parts], axis=-1)
+    dw_qkv = np.einsum("bnc,bnk->ck", st["x"], dqkv)
+    db_qkv = dqkv.sum(axis=(0, 1))
+    dx = dqkv @ st["w_qkv"].T
+    return dx, dw_qkv, db_qkv, dw_o, db_o

@@ -435,3 +435,106 @@ def test_batch_stats_backward_matches_finite_differences(tied, kernel):
                       - loss(minus["q"], minus["k"], minus["v"])) / (2 * h)
         err = np.linalg.norm(grads[name] - fd) / np.linalg.norm(fd)
         assert err < 1e-6, (name, err)
+
+
+# --------------------------------------------------------------------------
+# attention block (projections around the path)
+# --------------------------------------------------------------------------
+def _block_args(seed, B=2, N=16, C=6, H=2, d=4, tied=False, bias=True):
+    rng = np.random.default_rng(seed)
+    S = 2 if tied else 3
+    x = rng.standard_normal((B, N, C))
+    w = rng.standard_normal((C, S * H * d)) / np.sqrt(C)
+    b = rng.standard_normal(S * H * d) * 0.3 if bias else None
+    wo = rng.standard_normal((H * d, C)) / np.sqrt(H * d)
+    bo = rng.standard_normal(C) * 0.3 if bias else None
+    return x, w, b, wo, bo
+
+
+BLK = dict(grid_h=4, grid_w=4, m=4, lam=4.0, eps=1e-3, iters=3)
+
+
+def _blk(x, w, b, wo, bo, H, d, **kw):
+    a = dict(BLK)
+    a.update(kw)
+    return orc.block_forward(x, w, b, wo, bo, H, d, a["grid_h"], a["grid_w"], a["m"], a["lam"],
+                             a["eps"], a["iters"], a.get("norm", False), a.get("kernel", "laplace"),
+                             a.get("norm_batch", False), a.get("tied", False))
+
+
+def test_block_one_head_is_projected_attention():
+    x, w, b, wo, bo = _block_args(50, H=1, d=4)
+    y, _ = _blk(x, w, b, wo, bo, 1, 4, norm=True)
+    q, k, v = (x @ w[:, 4 * s:4 * s + 4] + b[4 * s:4 * s + 4] for s in range(3))
+    O = orc.attention(q[:, None], k[:, None], v[:, None], 4, 4, 4, 4.0, 1e-3, 3, norm=True)
+    np.testing.assert_allclose(y, O[:, 0] @ wo + bo, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("tied", [False, True])
+def test_block_head_permutation_invariance(tied):
+    # relabelling the heads (their column blocks in every projection, their row
+    # blocks in w_o) leaves the layer unchanged
+    H, d = 3, 4
+    x, w, b, wo, bo = _block_args(51, C=5, H=H, d=d, tied=tied)
+    perm = [2, 0, 1]
+    S = 2 if tied else 3
+    cols = np.concatenate([s * H * d + np.arange(h * d, h * d + d) for s in range(S) for h in perm])
+    rows = np.concatenate([np.arange(h * d, h * d + d) for h in perm])
+    y0, _ = _blk(x, w, b, wo, bo, H, d, tied=tied)
+    y1, _ = _blk(x, w[:, cols], b[cols], wo[rows], bo, H, d, tied=tied)
+    np.testing.assert_allclose(y1, y0, rtol=1e-12, atol=1e-12)
+    # swapping two coordinates inside a head of Q: with Q = K every distance
+    # |q - l|_1 keeps its value (both sides move together); with a separate K
+    # the layer changes
+    wq = w.copy()
+    wq[:, [0, 1]] = wq[:, [1, 0]]
+    bq = b.copy()
+    bq[[0, 1]] = bq[[1, 0]]
+    y2, _ = _blk(x, wq, bq, wo, bo, H, d, tied=tied)
+    if tied:
+        np.testing.assert_allclose(y2, y0, rtol=1e-12, atol=1e-12)
+    else:
+        assert np.abs(y2 - y0).max() > 1e-6
+
+
+def test_block_bias_is_a_constant_input_feature():
+    # a bias equals one more input feature fixed at 1 whose weight row is the bias
+    x, w, b, wo, bo = _block_args(52)
+    y0, st0 = _blk(x, w, b, wo, bo, 2, 4, norm=True)
+    xa = np.concatenate([x, np.ones(x.shape[:2] + (1,))], axis=-1)
+    y1, st1 = _blk(xa, np.vstack([w, b]), None, wo, bo, 2, 4, norm=True)
+    np.testing.assert_allclose(y1, y0, rtol=1e-12, atol=1e-12)
+    dy = np.random.default_rng(53).standard_normal(y0.shape)
+    g0 = orc.block_backward(st0, dy)
+    g1 = orc.block_backward(st1, dy)
+    np.testing.assert_allclose(g1[1][-1], g0[2], rtol=1e-10, atol=1e-12)   # db_qkv
+    np.testing.assert_allclose(g1[1][:-1], g0[1], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(g1[0][..., :-1], g0[0], rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("tied,norm_batch", [(False, False), (True, False), (False, True)])
+def test_block_backward_matches_finite_differences(tied, norm_batch):
+    H, d = 2, 4
+    x, w, b, wo, bo = _block_args(54 + tied + 2 * norm_batch, tied=tied)
+    R = np.random.default_rng(57).standard_normal(x.shape)
+    kw = dict(tied=tied, norm=True, norm_batch=norm_batch)
+    args = dict(x=x, w=w, b=b, wo=wo, bo=bo)
+
+    def loss(a):
+        y, _ = _blk(a["x"], a["w"], a["b"], a["wo"], a["bo"], H, d, **kw)
+        return float((y * R).sum())
+
+    _, st = _blk(x, w, b, wo, bo, H, d, **kw)
+    dx, dw, db, dwo, dbo = orc.block_backward(st, R)
+    grads = dict(x=dx, w=dw, b=db, wo=dwo, bo=dbo)
+    h = 1e-6
+    for name, base in args.items():
+        fd = np.zeros(base.shape)
+        for ix in np.ndindex(base.shape):
+            plus = {n: a.copy() for n, a in args.items()}
+            minus = {n: a.copy() for n, a in args.items()}
+            plus[name][ix] += h
+            minus[name][ix] -= h
+            fd[ix] = (loss(plus) - loss(minus)) / (2 * h)
+        err = np.linalg.norm(grads[name] - fd) / np.linalg.norm(fd)
+        assert err < 1e-6, (name, err)
