@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--kernel", choices=["laplace", "gauss"], default="laplace",
                     help="Laplacian kernel (the method) or its Gaussian-kernel variant")
+    ap.add_argument("--norm-batch", action="store_true",
+                    help="normalised workloads: feature-map statistics over the B slices of a head")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override B (smaller profiling cases)")
@@ -180,18 +182,22 @@ def clock_summary(proc, path):
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline and reference arm): one (b, h) slice, forward + backward
 # ---------------------------------------------------------------------------
-def _oracle_slice(wname: str, kernel: str = "laplace"):
+def _oracle_slice(wname: str, kernel: str = "laplace", norm_batch: bool = False):
+    """One unit of oracle work: a (b, h) slice, or with batch-pooled statistics
+    (which couple them) the B slices of one head."""
     import dataclasses
 
     from laplacian_nystr_linear_gb300.inputs import WORKLOADS, make_inputs
     from oracle import lapnys_oracle as orc
-    w = dataclasses.replace(WORKLOADS[wname], B=1, H=1, kernel=kernel)
+    w0 = WORKLOADS[wname]
+    nb = bool(norm_batch and w0.norm)
+    w = dataclasses.replace(w0, B=w0.B if nb else 1, H=1, kernel=kernel, norm_batch=nb)
     inp = make_inputs(w, with_grad=True)
     t0 = time.perf_counter()
     _, saved = orc.forward(inp["q"], inp["k"], inp["v"], w.grid_h, w.grid_w, w.m, w.lam, w.eps,
-                           w.iters, w.norm, kernel=kernel)
+                           w.iters, w.norm, kernel=kernel, norm_batch=nb)
     orc.backward(saved, inp["dout"], tied=w.tied)
-    return time.perf_counter() - t0, w.N
+    return time.perf_counter() - t0, w.B * w.N
 
 
 def _single_thread_env():
@@ -201,18 +207,20 @@ def _single_thread_env():
     return env
 
 
-def cpu_baseline(wname: str, kernel: str = "laplace"):
+def cpu_baseline(wname: str, kernel: str = "laplace", norm_batch: bool = False):
     """The oracle as it stands, one process, one thread, on whole (b, h) slices
     of the workload (at least 10 s of work)."""
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-worker",
-                        "--workload", wname, "--kernel", kernel], capture_output=True, text=True,
+                        "--workload", wname, "--kernel", kernel]
+                       + (["--norm-batch"] if norm_batch else []), capture_output=True, text=True,
                        env=_single_thread_env(), timeout=1800)
     if r.returncode != 0:
         return {"error": r.stderr.strip().splitlines()[-1:]}
     sec, tokens, n = json.loads(r.stdout.strip().splitlines()[-1])
     return {"value": tokens / sec, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{n} (b,h) slice(s) of {wname} ({tokens} tokens), fwd+bwd, fp64, "
-                      f"{sec:.1f} s single-threaded"}
+            "sample": (f"{n} head(s) x all B slices (batch-pooled statistics)" if norm_batch
+                       else f"{n} (b,h) slice(s)")
+                      + f" of {wname} ({tokens} tokens), fwd+bwd, fp64, {sec:.1f} s single-threaded"}
 
 
 def _pool_task(task):
@@ -229,7 +237,7 @@ def run_reference(args, rank, world):
     cores = max(1, min(os.cpu_count() or 1, max(args.steps, args.warmup)))
     ctx = mp.get_context("spawn")
     with ctx.Pool(cores) as pool:
-        task = (args.workload, args.kernel)
+        task = (args.workload, args.kernel, args.norm_batch)
         pool.map(_pool_task, [task] * max(args.warmup, 1))
         t0 = time.perf_counter()
         res = pool.map(_pool_task, [task] * args.steps)
@@ -241,7 +249,9 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": args.workload, "kernel": args.kernel,
-                                        "sample": "one (b,h) slice per step"},
+                                        "norm_batch": args.norm_batch,
+                                        "sample": "one (b,h) slice per step (one head's B slices "
+                                                  "with batch-pooled statistics)"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": f"{args.steps} steps x one (b,h) slice of {args.workload}, "
                                    f"fwd+bwd, fp64, {cores} processes x 1 thread"},
@@ -267,10 +277,14 @@ def run_ours(args, rank, world, local_rank):
         dist.init_process_group("nccl", device_id=dev)
     import dataclasses
     w = dataclasses.replace(WORKLOADS[args.workload], kernel=args.kernel)
+    if args.norm_batch:
+        if not w.norm:
+            raise SystemExit(f"--norm-batch needs a normalised workload; {w.name} has norm=False")
+        w = dataclasses.replace(w, norm_batch=True)
     if args.batch or args.heads:
         w = dataclasses.replace(w, B=args.batch or w.B, H=args.heads or w.H)
     p = api.Params(w.B, w.H, w.grid_h, w.grid_w, w.d, w.m, w.lam, w.eps, w.iters, w.tied, w.norm,
-                   w.kernel)
+                   w.kernel, w.norm_batch)
     tdt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     inp = make_inputs(w, with_grad=True)
     host = {n: torch.from_numpy(np.ascontiguousarray(inp[n])).to(tdt) for n in ("q", "k", "v", "dout")}
@@ -293,37 +307,56 @@ def run_ours(args, rank, world, local_rank):
             dist.barrier()
         torch.cuda.synchronize()
 
+    stream = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # inputs smaller than L2 (Q, K, V, dO together): flush L2 between timed
+    # steps by writing a buffer of twice its size, outside the timed intervals
+    L2_BYTES = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 129e6)
+    in_bytes = 4 * q.numel() * q.element_size()
+    flush = None if in_bytes > L2_BYTES else torch.empty(2 * L2_BYTES // 4, dtype=torch.float32,
+                                                          device=dev)
+
+    def timed(fn, n):
+        """Device milliseconds per call of fn over n calls on this stream."""
+        if flush is None:
+            e0.record(stream)
+            for _ in range(n):
+                fn()
+            e1.record(stream)
+            barrier()
+            return e0.elapsed_time(e1) / n
+        evs = []
+        for _ in range(n):
+            flush.fill_(float(len(evs)))
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            evs.append((a, b))
+        barrier()
+        return sum(a.elapsed_time(b) for a, b in evs) / n
+
     for _ in range(args.warmup):
         step()
     barrier()
     sampler, cpath = clock_sampler(local_rank)
     time.sleep(0.3)
-    stream = torch.cuda.current_stream(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = api.launch_count()
     api.profile_enable(True)
-    e0.record(stream)
-    for _ in range(args.steps):
-        step()
-    e1.record(stream)
-    barrier()
+    ms_local = timed(step, args.steps)
     clocks = clock_summary(sampler, cpath)
     prof = api.profile_read()
     api.profile_enable(False)
     launches = api.launch_count() - launches0
-    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    ms = max_over_ranks(ms_local, world, dev)
     value = weak_scaling_value(w.tokens, world, ms)
 
     # forward alone (same buffers)
     for _ in range(2):
         api.fwd(q, k, v, p, out=out, ctx=ctx, ws=ws)
     barrier()
-    e0.record(stream)
-    for _ in range(args.steps):
-        api.fwd(q, k, v, p, out=out, ctx=ctx, ws=ws)
-    e1.record(stream)
-    barrier()
-    ms_fwd = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, dev)
+    ms_fwd = max_over_ranks(timed(lambda: api.fwd(q, k, v, p, out=out, ctx=ctx, ws=ws), args.steps),
+                            world, dev)
 
     # roofline of the dominant kernel (FP32 lane-ops; the path is ALU-bound)
     ops = algorithmic_ops(w)
@@ -368,12 +401,7 @@ def run_ours(args, rank, world, local_rank):
 
         step_e2e()
         barrier()
-        e0.record(stream)
-        for _ in range(ne):
-            step_e2e()
-        e1.record(stream)
-        barrier()
-        ms_e2e = max_over_ranks(e0.elapsed_time(e1) / ne, world, dev)
+        ms_e2e = max_over_ranks(timed(step_e2e, ne), world, dev)
         nbytes = q.numel() * q.element_size()
         n_in = 3 if w.tied else 4
         n_out = 3 if w.tied else 4
@@ -385,7 +413,7 @@ def run_ours(args, rank, world, local_rank):
         return
     base = None
     if world == 1 and not args.no_cpu_baseline:
-        base = cpu_baseline(args.workload, args.kernel)
+        base = cpu_baseline(args.workload, args.kernel, w.norm_batch)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -394,8 +422,12 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": args.workload, "kernel": w.kernel, "B": w.B, "H": w.H, "N": w.N,
                    "grid": [w.grid_h, w.grid_w],
                    "d": w.d, "m": w.m, "iters": w.iters, "lambda": w.lam, "eps": w.eps,
-                   "norm": w.norm, "tied": w.tied, "pass": "fwd+bwd",
-                   "l2": "inputs larger than L2 (Q, K, V, dO 134 MB each, 129 MB L2); no flush",
+                   "norm": w.norm, "norm_batch": w.norm_batch, "tied": w.tied,
+                   "pass": "fwd+bwd",
+                   "l2": (f"inputs larger than L2 (Q, K, V, dO {in_bytes / 4e6:.0f} MB each, "
+                          f"{L2_BYTES / 1e6:.0f} MB L2); no flush" if flush is None else
+                          f"inputs {in_bytes / 1e6:.0f} MB < L2: {2 * L2_BYTES / 1e6:.0f} MB "
+                          "written between timed steps, outside the timed intervals"),
                    "parallelism": f"replicas x{world}"},
         "fwd_tokens_per_s": world * w.tokens / (ms_fwd / 1e3), "ms_fwd": ms_fwd,
         "roofline": roofline,
@@ -415,7 +447,7 @@ def main():
         # whole slices until at least 10 s of CPU work (a bounded sample)
         sec = tokens = n = 0
         while sec < 10.0 or n == 0:
-            s1, t1 = _oracle_slice(args.workload, args.kernel)
+            s1, t1 = _oracle_slice(args.workload, args.kernel, args.norm_batch)
             sec, tokens, n = sec + s1, tokens + t1, n + 1
         print(json.dumps([sec, tokens, n]))
         return

@@ -75,8 +75,14 @@ enum { LAPNYS_F32 = 0, LAPNYS_BF16 = 1 };
  * LAPNYS_GAUSS  use the Gaussian kernel k(x, y) = exp(-|x - y|_2^2 / lambda)
  *               (the SOFT review's Proposed method: a symmetric, [0, 1]-valued
  *               Gaussian kernel) instead of the Laplacian kernel
- *               exp(-|x - y|_1 / lambda).  Same ctx, workspace and entry points. */
-enum { LAPNYS_NORM = 1u << 0, LAPNYS_GAUSS = 1u << 1 };
+ *               exp(-|x - y|_1 / lambda).  Same ctx, workspace and entry points;
+ * LAPNYS_NORM_BATCH  with LAPNYS_NORM only (alone it is LAPNYS_EINVAL): take
+ *               the mean and variance of each landmark column over the B * N
+ *               queries of all B slices of a head (the same summary's diagonal
+ *               estimate read as taken over the batch) instead of per slice; the
+ *               backward then couples the B slices of a head through those
+ *               statistics, so lapnys_bwd must see the same B as lapnys_fwd. */
+enum { LAPNYS_NORM = 1u << 0, LAPNYS_GAUSS = 1u << 1, LAPNYS_NORM_BATCH = 1u << 2 };
 
 /* Limits of this build: d in {16, 32, 64, 128}; 1 <= m <= min(N, 1024); a
  * landmark grid as above; 0 <= iters <= 64; lambda > 0; eps >= 0;
@@ -181,6 +187,52 @@ int lapnys_matmul(const float* A, const float* B, const float* E, float* C, int 
                   int K, int trans_a, int trans_b, int lda, int ldb, int lde, int ldc,
                   long long stride_a, long long stride_b, long long stride_e, long long stride_c,
                   float alpha, float beta, int engine, cudaStream_t stream);
+
+/* ---- the attention block around the path -------------------------------
+ * One multi-head layer (the SOFT review, Proposed method: the attention as one
+ * layer of a pyramid vision-transformer backbone with embedding width C and H
+ * heads):
+ *
+ *     [Q | K | V] = X W_qkv + b_qkv,   O_h = attention(Q_h, K_h, V_h),
+ *     Y = [O_1 | ... | O_H] W_o + b_o,
+ *
+ * with the attention of lapnys_fwd for every (batch, head).
+ *  - x, y, dy, dx: [B][N][C] (token n on the grid as in lapnys_fwd);
+ *    w_qkv [C][S*H*d] row-major with column blocks (Q | K | V), S = 3 (tied = 0)
+ *    or (Q = K | V), S = 2 (tied = 1), head h at columns h*d .. h*d + d - 1 of
+ *    each block; b_qkv [S*H*d]; w_o [H*d][C]; b_o [C].  All DEVICE pointers of
+ *    element type `dtype`, 16-byte aligned; b_qkv and b_o may be NULL (no bias).
+ *  - C a multiple of 8 (at most 65536), B*N*max(3*H*d, C) < 2^31; the
+ *    attention arguments (H, N, d, grid, m, lambda, eps, iters, flags) follow
+ *    lapnys_fwd's rules and return its status codes.
+ *  - The projections are cuBLAS GEMMs with float32 accumulation (float32
+ *    operands are not rounded to TF32); the first call on a device creates a
+ *    cuBLAS handle there (cuBLAS's own small state), after which the calls
+ *    allocate nothing: the GEMM workspace is part of `ws`.  Q, K, V, the
+ *    projected outputs and every gradient are rounded once to `dtype`.
+ *  - lapnys_block_fwd writes y; with ctx != NULL it also saves, in ctx, the
+ *    attention context and the Q, K, V and concatenated head outputs that
+ *    lapnys_block_bwd reads (ctx == NULL: inference, they live in ws).
+ *  - lapnys_block_bwd writes dx, dw_qkv, dw_o, and db_qkv / db_o unless NULL
+ *    (column sums of the output gradients in a fixed order: deterministic).
+ *  - Sizes: lapnys_block_ctx_bytes / lapnys_block_workspace_bytes (0 for
+ *    invalid arguments); one workspace serves both entry points.
+ *  - Errors as for lapnys_fwd; argument errors are found before anything is
+ *    enqueued; a failed GEMM or launch returns LAPNYS_ECUDA. */
+size_t lapnys_block_ctx_bytes(int B, int N, int C, int H, int d, int m, int iters, int tied,
+                              int dtype, unsigned flags);
+size_t lapnys_block_workspace_bytes(int B, int N, int C, int H, int d, int m, int iters, int tied,
+                                    int dtype, unsigned flags);
+int lapnys_block_fwd(const void* x, const void* w_qkv, const void* b_qkv, const void* w_o,
+                     const void* b_o, void* y, int B, int N, int C, int H, int d, int grid_h,
+                     int grid_w, int m, float lambda, float eps, int iters, int tied,
+                     cudaStream_t stream, int dtype, unsigned flags, void* ctx, size_t ctx_bytes,
+                     void* ws, size_t ws_bytes);
+int lapnys_block_bwd(const void* x, const void* w_qkv, const void* w_o, const void* dy,
+                     const void* ctx, void* dx, void* dw_qkv, void* db_qkv, void* dw_o, void* db_o,
+                     int B, int N, int C, int H, int d, int grid_h, int grid_w, int m, float lambda,
+                     float eps, int iters, int tied, cudaStream_t stream, int dtype,
+                     unsigned flags, void* ws, size_t ws_bytes);
 
 /* Synchronises the current device and reports whether a bounded device-side
  * wait (tensor-core pipeline barriers) expired since the last clear:

@@ -14,14 +14,15 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "liblapnys.s
 (LAPNYS_OK, LAPNYS_EINVAL, LAPNYS_ECUDA, LAPNYS_ETIMEOUT, LAPNYS_ENOSPC, LAPNYS_ENOTSUP,
  LAPNYS_ESCRATCH) = range(7)
 LAPNYS_F32, LAPNYS_BF16 = 0, 1
-LAPNYS_NORM, LAPNYS_GAUSS = 1, 2
+LAPNYS_NORM, LAPNYS_GAUSS, LAPNYS_NORM_BATCH = 1, 2, 4
 
 # every symbol include/lapnys.h declares
 EXPORTS = (
     "lapnys_ctx_bytes", "lapnys_workspace_bytes", "lapnys_fwd", "lapnys_bwd",
     "lapnys_ctx_offsets", "lapnys_pool", "lapnys_strerror", "lapnys_launch_count",
     "lapnys_profile_enable", "lapnys_profile_read", "lapnys_fwd_static", "lapnys_matmul",
-    "lapnys_device_status",
+    "lapnys_device_status", "lapnys_block_ctx_bytes", "lapnys_block_workspace_bytes",
+    "lapnys_block_fwd", "lapnys_block_bwd",
 )
 
 
@@ -56,6 +57,16 @@ def load() -> ctypes.CDLL:
     lib.lapnys_matmul.argtypes = [P, P, P, P, I, I, I, I, I, I, I, I, I, I, LL, LL, LL, LL, F, F,
                                   I, P]
     lib.lapnys_matmul.restype = I
+    lib.lapnys_block_ctx_bytes.argtypes = [I, I, I, I, I, I, I, I, I, U]
+    lib.lapnys_block_ctx_bytes.restype = S
+    lib.lapnys_block_workspace_bytes.argtypes = [I, I, I, I, I, I, I, I, I, U]
+    lib.lapnys_block_workspace_bytes.restype = S
+    lib.lapnys_block_fwd.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, F, I, I, P, I, U,
+                                     P, S, P, S]
+    lib.lapnys_block_fwd.restype = I
+    lib.lapnys_block_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, F, I,
+                                     I, P, I, U, P, S]
+    lib.lapnys_block_bwd.restype = I
     lib.lapnys_device_status.argtypes = [I]
     lib.lapnys_device_status.restype = I
     lib.lapnys_bwd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, F, I, I, P, I, U, P, S]

@@ -28,6 +28,7 @@ class Params:
     tied: bool = False
     norm: bool = False
     kernel: str = "laplace"  # or "gauss"
+    norm_batch: bool = False  # with norm: statistics over the B slices of a head
 
     @property
     def N(self) -> int:
@@ -38,18 +39,19 @@ class Params:
         if self.kernel not in ("laplace", "gauss"):
             raise ValueError(f"unknown kernel {self.kernel!r}")
         return ((_lib.LAPNYS_NORM if self.norm else 0)
-                | (_lib.LAPNYS_GAUSS if self.kernel == "gauss" else 0))
+                | (_lib.LAPNYS_GAUSS if self.kernel == "gauss" else 0)
+                | (_lib.LAPNYS_NORM_BATCH if self.norm_batch else 0))
 
     def dims(self):
         return (self.B, self.H, self.N, self.d, self.grid_h, self.grid_w, self.m)
 
     @staticmethod
     def of(q: torch.Tensor, grid, m: int, lam=None, eps=1e-3, iters=20, tied=False, norm=False,
-           kernel="laplace"):
+           kernel="laplace", norm_batch=False):
         B, H, N, d = q.shape
         gh, gw = grid
         return Params(B, H, gh, gw, d, m, float(d if lam is None else lam), float(eps), int(iters),
-                      bool(tied), bool(norm), str(kernel))
+                      bool(tied), bool(norm), str(kernel), bool(norm_batch))
 
 
 def ctx_bytes(p: Params) -> int:
@@ -208,14 +210,16 @@ class _Attention(torch.autograd.Function):
 
 
 def attention(q, k, v, grid, m, lam=None, eps=1e-3, iters=20, tied=False, norm=False,
-              kernel="laplace"):
+              kernel="laplace", norm_batch=False):
     """Kernel Nystrom attention O = Z . X_T . (k(L, K) . V) with autograd, for the
     Laplacian kernel (kernel="laplace") or the Gaussian kernel (kernel="gauss").
 
     q, k, v: [B, H, N, d] CUDA tensors (float32 or bfloat16), N = grid[0] * grid[1].
     In tied mode pass k=None (or k=q); the gradient of the shared tensor goes to q.
+    With norm=True, norm_batch=True takes the feature-map statistics over the B
+    slices of each head instead of per slice.
     """
-    p = Params.of(q, grid, m, lam, eps, iters, tied, norm, kernel)
+    p = Params.of(q, grid, m, lam, eps, iters, tied, norm, kernel, norm_batch)
     if tied:
         k = q
     return _Attention.apply(q, k, v, p)

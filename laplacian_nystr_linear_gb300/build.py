@@ -14,10 +14,15 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblapnys.so")
 SOURCES = ["lapnys.cu", "k_landmark.cu", "k_gemm.cu", "k_pass.cu", "k_bwd.cu", "k_gemm2.cu", "k_tcgemm.cu",
-           "k_ties.cu", "k_nscluster.cu", "k_fwd_tc.cu", "k_gauss_tc.cu"]
+           "k_ties.cu", "k_nscluster.cu", "k_fwd_tc.cu", "k_gauss_tc.cu", "k_block.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "internal.h", "tc.cuh")] + [
     os.path.join(ROOT, "include", "lapnys.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+# cuBLAS for the attention block's plain projection GEMMs (found at run time
+# through the toolkit's library directory)
+_CUDA_LIB = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(
+    shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"))), "lib64")
+LINK = ["-L" + _CUDA_LIB, "-Xlinker", "-rpath=" + _CUDA_LIB, "-lcublas"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "-I" + os.path.join(ROOT, "include")]
 
@@ -61,7 +66,7 @@ def build(verbose: bool = False, ptxas_verbose: bool = False, force: bool = Fals
             if r.returncode != 0:
                 raise RuntimeError("nvcc failed for " + cmd[-3])
     if force or jobs or _stale(LIB, objs):
-        cmd = [nvcc, *ARCH, "-shared", "-o", LIB, *objs]
+        cmd = [nvcc, *ARCH, "-shared", "-o", LIB, *objs, *LINK]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("link failed:\n" + r.stdout + r.stderr)

@@ -21,7 +21,12 @@ struct Prob {
   int Skt;        // token splits of the tensor-core key pass (0 when it is not used)
   bool norm() const { return flags & 1u; }
   bool gauss() const { return flags & 2u; }  // Gaussian kernel instead of the Laplacian
+  bool norm_batch() const { return flags & 4u; }  // statistics over the B slices of a head
 };
+
+// the attention entry points' argument checks (LAPNYS_OK or the status they return)
+int check_attention(int B, int H, int N, int d, int gh, int gw, int m, float lam, float eps,
+                    int iters, int dtype, unsigned flags);
 
 // ---- instrumentation -------------------------------------------------------
 int prof_begin(const char* name, cudaStream_t s);

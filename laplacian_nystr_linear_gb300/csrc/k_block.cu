@@ -1,0 +1,414 @@
+// The attention block around the path: the QKV projection, the per-head
+// attention of this library, and the output projection, forward and backward.
+//
+// "[Paper review] SOFT: Softmax-free Transformer with Linear Complexity",
+// Proposed method: the attention is instantiated as one layer of a pyramid
+// vision-transformer backbone (embedding width d_e, h heads).  Read as the
+// plain multi-head layer: [Q | K | V] = X W_qkv + b_qkv, heads of d columns,
+// Y = concat_h(O_h) W_o + b_o.
+//
+// The six projections are plain dense GEMMs and go to cuBLAS (fp32
+// accumulation; no TF32 for float32 operands).  Everything between them is
+// HBM-bound layout work done by the kernels below: the [B*N][S*H*d] <->
+// [B][H][N][d] head transposes fused with the bias addition and the rounding
+// to the element type, and fixed-order column sums for the bias gradients.
+#include <cublas_v2.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "lapnys.h"
+
+namespace lapnys {
+namespace {
+
+constexpr int kBlockThreads = 256;
+constexpr size_t kBlasWs = 32u << 20;  // cuBLAS workspace carved out of the caller's ws
+constexpr int kColSplits = 512;        // row splits of the bias-gradient column sums (max)
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T>
+__device__ __forceinline__ T from_f(float v);
+template <>
+__device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+// ---- layout kernels ---------------------------------------------------------
+// One thread per 4 consecutive elements of a head row (d is a multiple of 16).
+
+// src [B*N][S*H*d] float32 (+ bias [S*H*d]) -> dst_s [B][H][N][d] of T, s < S
+template <typename T>
+__global__ void k_split_heads(const float* __restrict__ src, const T* __restrict__ bias,
+                              T* __restrict__ d0, T* __restrict__ d1, T* __restrict__ d2, int N,
+                              int H, int d, int S, long long n4) {
+  const long long e4 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e4 >= n4) return;
+  const long long e = e4 * 4;
+  const int HD = H * d, W = S * HD;
+  const long long row = e / W;
+  const int col = (int)(e - row * W);
+  const int s = col / HD, hc = col - s * HD, h = hc / d, j = hc - h * d;
+  const long long b = row / N, n = row - b * N;
+  float4 v = ld4(src + e);
+  if (bias != nullptr) {
+    const float4 bv = ld4(bias + col);
+    v.x += bv.x; v.y += bv.y; v.z += bv.z; v.w += bv.w;
+  }
+  T* dst = s == 0 ? d0 : (s == 1 ? d1 : d2);
+  st4(dst + ((b * H + h) * N + n) * d + j, v);
+}
+
+// src_s [B][H][N][d] of T, s < S -> dst [B*N][S*H*d] of T
+template <typename T>
+__global__ void k_merge_heads(const T* __restrict__ s0, const T* __restrict__ s1,
+                              const T* __restrict__ s2, T* __restrict__ dst, int N, int H, int d,
+                              int S, long long n4) {
+  const long long e4 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e4 >= n4) return;
+  const long long e = e4 * 4;
+  const int HD = H * d, W = S * HD;
+  const long long row = e / W;
+  const int col = (int)(e - row * W);
+  const int s = col / HD, hc = col - s * HD, h = hc / d, j = hc - h * d;
+  const long long b = row / N, n = row - b * N;
+  const T* src = s == 0 ? s0 : (s == 1 ? s1 : s2);
+  st4(dst + e, ld4(src + ((b * H + h) * N + n) * d + j));
+}
+
+// dst [rows][C] of T = src [rows][C] float32 + bias [C] (bias may be null)
+template <typename T>
+__global__ void k_bias_rows(const float* __restrict__ src, const T* __restrict__ bias,
+                            T* __restrict__ dst, int C, long long n4) {
+  const long long e4 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e4 >= n4) return;
+  const long long e = e4 * 4;
+  float4 v = ld4(src + e);
+  if (bias != nullptr) {
+    const float4 bv = ld4(bias + (int)(e % C));
+    v.x += bv.x; v.y += bv.y; v.z += bv.z; v.w += bv.w;
+  }
+  st4(dst + e, v);
+}
+
+// part[split][col] = sum of G[r][col] over the split's rows, in row order
+template <typename T>
+__global__ void k_colsum_part(const T* __restrict__ G, float* __restrict__ part, long long rows,
+                              int cols, long long rows_per) {
+  const int col = blockIdx.x * blockDim.x + threadIdx.x;
+  if (col >= cols) return;
+  const long long r0 = (long long)blockIdx.y * rows_per;
+  const long long r1 = r0 + rows_per < rows ? r0 + rows_per : rows;
+  float acc = 0.f;
+  for (long long r = r0; r < r1; ++r) acc += to_f(G[r * cols + col]);
+  part[(size_t)blockIdx.y * cols + col] = acc;
+}
+
+// out[col] = sum over splits in order
+template <typename T>
+__global__ void k_colsum_final(const float* __restrict__ part, T* __restrict__ out, int splits,
+                               int cols) {
+  const int col = blockIdx.x * blockDim.x + threadIdx.x;
+  if (col >= cols) return;
+  float acc = 0.f;
+  for (int s = 0; s < splits; ++s) acc += part[(size_t)s * cols + col];
+  out[col] = from_f<T>(acc);
+}
+
+unsigned blocks_for(long long n4) { return (unsigned)((n4 + kBlockThreads - 1) / kBlockThreads); }
+
+template <typename T>
+cudaError_t split_heads_t(const float* src, const void* bias, void* d0, void* d1, void* d2, int B,
+                          int N, int H, int d, int S, cudaStream_t st) {
+  const long long n4 = (long long)B * N * S * H * d / 4;
+  return launch("block_split_heads", k_split_heads<T>, dim3(blocks_for(n4)), dim3(kBlockThreads), 0,
+                st, src, (const T*)bias, (T*)d0, (T*)d1, (T*)d2, N, H, d, S, n4);
+}
+template <typename T>
+cudaError_t merge_heads_t(const void* s0, const void* s1, const void* s2, void* dst, int B, int N,
+                          int H, int d, int S, cudaStream_t st) {
+  const long long n4 = (long long)B * N * S * H * d / 4;
+  return launch("block_merge_heads", k_merge_heads<T>, dim3(blocks_for(n4)), dim3(kBlockThreads), 0,
+                st, (const T*)s0, (const T*)s1, (const T*)s2, (T*)dst, N, H, d, S, n4);
+}
+template <typename T>
+cudaError_t bias_rows_t(const float* src, const void* bias, void* dst, long long rows, int C,
+                        cudaStream_t st) {
+  const long long n4 = rows * C / 4;
+  return launch("block_bias_rows", k_bias_rows<T>, dim3(blocks_for(n4)), dim3(kBlockThreads), 0, st,
+                src, (const T*)bias, (T*)dst, C, n4);
+}
+
+int col_splits(long long rows, int cols) {
+  const long long cb = (cols + kBlockThreads - 1) / kBlockThreads;
+  long long s = (4LL * 152) / cb;
+  if (s < 1) s = 1;
+  if (s > kColSplits) s = kColSplits;
+  if (s > rows) s = rows;
+  return (int)s;
+}
+
+template <typename T>
+cudaError_t colsum_t(const void* G, float* part, void* out, long long rows, int cols,
+                     cudaStream_t st) {
+  const int S = col_splits(rows, cols);
+  const long long per = (rows + S - 1) / S;
+  const unsigned cb = (unsigned)((cols + kBlockThreads - 1) / kBlockThreads);
+  cudaError_t e = launch("block_colsum", k_colsum_part<T>, dim3(cb, S), dim3(kBlockThreads), 0, st,
+                         (const T*)G, part, rows, cols, per);
+  if (e != cudaSuccess) return e;
+  return launch("block_colsum_final", k_colsum_final<T>, dim3(cb), dim3(kBlockThreads), 0, st,
+                (const float*)part, (T*)out, S, cols);
+}
+
+#define DT_CALL(dtype, fn, ...) \
+  ((dtype) == LAPNYS_BF16 ? fn<__nv_bfloat16>(__VA_ARGS__) : fn<float>(__VA_ARGS__))
+
+// ---- cuBLAS -----------------------------------------------------------------
+// One handle per device, created on first use; the stream and the workspace
+// (a slice of the caller's ws) are set for every call under the mutex.
+struct Blas {
+  cublasHandle_t h = nullptr;
+  std::mutex mu;
+};
+constexpr int kMaxDevices = 64;
+
+Blas* blas_for_current_device() {
+  static Blas handles[kMaxDevices];
+  static std::mutex create_mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> g(create_mu);
+  Blas* b = &handles[dev];
+  if (b->h == nullptr) {
+    if (cublasCreate(&b->h) != CUBLAS_STATUS_SUCCESS) {
+      b->h = nullptr;
+      return nullptr;
+    }
+    cublasSetMathMode(b->h, CUBLAS_DEFAULT_MATH);  // float32 stays float32 (no TF32)
+  }
+  return b;
+}
+
+// row-major C[M][N] (ldc) = op(A) op(B); op(A) is M x K (A stored K x M when ta),
+// op(B) is K x N (B stored N x K when tb); operands of type tab, C of type tc
+bool gemm_rm(cublasHandle_t h, bool ta, bool tb, int M, int N, int K, const void* A, int lda,
+             const void* B, int ldb, void* C, int ldc, cudaDataType tab, cudaDataType tc) {
+  const float one = 1.f, zero = 0.f;
+  // column-major view: C^T = op(B)^T op(A)^T, with the same transpose flags
+  return cublasGemmEx(h, tb ? CUBLAS_OP_T : CUBLAS_OP_N, ta ? CUBLAS_OP_T : CUBLAS_OP_N, N, M, K,
+                      &one, B, tab, ldb, A, tab, lda, &zero, C, tc, ldc, CUBLAS_COMPUTE_32F,
+                      CUBLAS_GEMM_DEFAULT) == CUBLAS_STATUS_SUCCESS;
+}
+
+// ---- sizes ------------------------------------------------------------------
+struct BlockLayout {
+  // ctx: attention ctx, then the saved q, k (untied), v, and Ot [B*N][H*d]
+  size_t c_attn, c_q, c_k, c_v, c_ot, c_total, attn_ctx;
+  // forward ws: f32 scratch, O, saved tensors when there is no ctx, attention ws, cuBLAS
+  size_t f_s32, f_o, f_lite, f_attn, f_blas, f_total;
+  // backward ws: f32 scratch, dO, dq, dk, dv, dqkv, column-sum partials, attention ws, cuBLAS
+  size_t b_s32, b_do, b_dq, b_dk, b_dv, b_dqkv, b_part, b_attn, b_blas, b_total;
+  size_t attn_ws;
+};
+
+bool block_dims_ok(int B, int N, int C, int H, int d) {
+  if (B <= 0 || N <= 0 || C <= 0 || H <= 0 || d <= 0) return false;
+  if (C % 8 != 0 || C > (1 << 16)) return false;
+  const long long rows = (long long)B * N;
+  const long long wide = 3LL * H * d > C ? 3LL * H * d : C;
+  return rows * wide < (1LL << 31);
+}
+
+BlockLayout block_layout(int B, int N, int C, int H, int d, int m, int iters, int tied, int dtype,
+                         unsigned flags) {
+  BlockLayout L;
+  memset(&L, 0, sizeof(L));
+  const size_t es = dtype == LAPNYS_BF16 ? 2 : 4;
+  const size_t rows = (size_t)B * N, HD = (size_t)H * d, S = tied ? 2 : 3;
+  const size_t head = rows * HD * es;  // one [B][H][N][d] tensor
+  L.attn_ctx = lapnys_ctx_bytes(B, H, N, d, m, iters, flags);
+  L.attn_ws = lapnys_workspace_bytes(B, H, N, d, m, iters, flags);
+  size_t o = 0;
+  L.c_attn = o; o = align256(o + L.attn_ctx);
+  const size_t saved0 = o;
+  L.c_q = o; o = align256(o + head);
+  L.c_k = o; o = align256(o + (tied ? 0 : head));
+  L.c_v = o; o = align256(o + head);
+  L.c_ot = o; o = align256(o + head);
+  L.c_total = o;
+  const size_t saved = o - saved0;
+
+  const size_t wide = (S * HD > (size_t)C ? S * HD : (size_t)C);
+  o = 0;
+  L.f_s32 = o; o = align256(o + rows * wide * 4);
+  L.f_o = o; o = align256(o + head);
+  L.f_lite = o; o = align256(o + saved);
+  L.f_attn = o; o = align256(o + L.attn_ws);
+  L.f_blas = o; o = align256(o + kBlasWs);
+  L.f_total = o;
+
+  o = 0;
+  L.b_s32 = o; o = align256(o + rows * HD * 4);
+  L.b_do = o; o = align256(o + head);
+  L.b_dq = o; o = align256(o + head);
+  L.b_dk = o; o = align256(o + (tied ? 0 : head));
+  L.b_dv = o; o = align256(o + head);
+  L.b_dqkv = o; o = align256(o + rows * S * HD * es);
+  L.b_part = o; o = align256(o + (size_t)kColSplits * wide * 4);
+  L.b_attn = o; o = align256(o + L.attn_ws);
+  L.b_blas = o; o = align256(o + kBlasWs);
+  L.b_total = o;
+  return L;
+}
+
+bool a16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+bool a16_or_null(const void* p) { return p == nullptr || a16(p); }
+
+#define CKB(x)                                   \
+  do {                                           \
+    if ((x) != cudaSuccess) return LAPNYS_ECUDA; \
+  } while (0)
+#define CKG(x)                    \
+  do {                            \
+    if (!(x)) return LAPNYS_ECUDA; \
+  } while (0)
+
+}  // namespace
+}  // namespace lapnys
+
+using namespace lapnys;
+
+extern "C" {
+
+size_t lapnys_block_ctx_bytes(int B, int N, int C, int H, int d, int m, int iters, int tied,
+                              int dtype, unsigned flags) {
+  if (!block_dims_ok(B, N, C, H, d) || (tied != 0 && tied != 1)) return 0;
+  if (dtype != LAPNYS_F32 && dtype != LAPNYS_BF16) return 0;
+  if (lapnys_ctx_bytes(B, H, N, d, m, iters, flags) == 0) return 0;
+  return block_layout(B, N, C, H, d, m, iters, tied, dtype, flags).c_total;
+}
+
+size_t lapnys_block_workspace_bytes(int B, int N, int C, int H, int d, int m, int iters, int tied,
+                                    int dtype, unsigned flags) {
+  if (!block_dims_ok(B, N, C, H, d) || (tied != 0 && tied != 1)) return 0;
+  if (dtype != LAPNYS_F32 && dtype != LAPNYS_BF16) return 0;
+  if (lapnys_workspace_bytes(B, H, N, d, m, iters, flags) == 0) return 0;
+  const BlockLayout L = block_layout(B, N, C, H, d, m, iters, tied, dtype, flags);
+  return L.f_total > L.b_total ? L.f_total : L.b_total;
+}
+
+int lapnys_block_fwd(const void* x, const void* w_qkv, const void* b_qkv, const void* w_o,
+                     const void* b_o, void* y, int B, int N, int C, int H, int d, int grid_h,
+                     int grid_w, int m, float lambda, float eps, int iters, int tied,
+                     cudaStream_t stream, int dtype, unsigned flags, void* ctx, size_t ctx_bytes,
+                     void* ws, size_t ws_bytes) {
+  if (!block_dims_ok(B, N, C, H, d) || (tied != 0 && tied != 1)) return LAPNYS_EINVAL;
+  int rc = check_attention(B, H, N, d, grid_h, grid_w, m, lambda, eps, iters, dtype, flags);
+  if (rc != LAPNYS_OK) return rc;
+  if (!x || !w_qkv || !w_o || !y || !ws) return LAPNYS_EINVAL;
+  if (!a16(x) || !a16(w_qkv) || !a16(w_o) || !a16(y) || !a16(ws) || !a16_or_null(b_qkv) ||
+      !a16_or_null(b_o) || !a16_or_null(ctx))
+    return LAPNYS_EINVAL;
+  const BlockLayout L = block_layout(B, N, C, H, d, m, iters, tied, dtype, flags);
+  if (ws_bytes < L.f_total) return LAPNYS_ENOSPC;
+  if (ctx != nullptr && ctx_bytes < L.c_total) return LAPNYS_ENOSPC;
+  Blas* bl = blas_for_current_device();
+  if (bl == nullptr) return LAPNYS_ECUDA;
+
+  const int S = tied ? 2 : 3, HD = H * d;
+  const int rows = B * N;
+  char* wb = (char*)ws;
+  // saved tensors live in ctx for training, in ws for inference
+  char* sb = ctx != nullptr ? (char*)ctx : wb + L.f_lite - L.c_q;
+  void* q = sb + L.c_q;
+  void* k = tied ? q : (void*)(sb + L.c_k);
+  void* v = sb + L.c_v;
+  void* ot = sb + L.c_ot;
+  float* s32 = (float*)(wb + L.f_s32);
+  void* O = wb + L.f_o;
+  const cudaDataType tab = dtype == LAPNYS_BF16 ? CUDA_R_16BF : CUDA_R_32F;
+
+  std::lock_guard<std::mutex> lock(bl->mu);
+  CKG(cublasSetStream(bl->h, stream) == CUBLAS_STATUS_SUCCESS);
+  CKG(cublasSetWorkspace(bl->h, wb + L.f_blas, kBlasWs) == CUBLAS_STATUS_SUCCESS);
+  // [Q | K | V] = X W_qkv (+ b_qkv, in the head split)
+  CKG(gemm_rm(bl->h, false, false, rows, S * HD, C, x, C, w_qkv, S * HD, s32, S * HD, tab,
+              CUDA_R_32F));
+  CKB(DT_CALL(dtype, split_heads_t, s32, b_qkv, q, tied ? v : k, v, B, N, H, d, S, stream));
+  rc = lapnys_fwd(q, tied ? nullptr : k, v, O, B, H, N, d, grid_h, grid_w, m, lambda, eps, iters,
+                  tied, stream, dtype, flags, ctx != nullptr ? (char*)ctx + L.c_attn : nullptr,
+                  L.attn_ctx, wb + L.f_attn, L.attn_ws);
+  if (rc != LAPNYS_OK) return rc;
+  // Y = concat_h(O_h) W_o + b_o
+  CKB(DT_CALL(dtype, merge_heads_t, O, nullptr, nullptr, ot, B, N, H, d, 1, stream));
+  CKG(gemm_rm(bl->h, false, false, rows, C, HD, ot, HD, w_o, C, s32, C, tab, CUDA_R_32F));
+  CKB(DT_CALL(dtype, bias_rows_t, s32, b_o, y, (long long)rows, C, stream));
+  return LAPNYS_OK;
+}
+
+int lapnys_block_bwd(const void* x, const void* w_qkv, const void* w_o, const void* dy,
+                     const void* ctx, void* dx, void* dw_qkv, void* db_qkv, void* dw_o, void* db_o,
+                     int B, int N, int C, int H, int d, int grid_h, int grid_w, int m, float lambda,
+                     float eps, int iters, int tied, cudaStream_t stream, int dtype,
+                     unsigned flags, void* ws, size_t ws_bytes) {
+  if (!block_dims_ok(B, N, C, H, d) || (tied != 0 && tied != 1)) return LAPNYS_EINVAL;
+  int rc = check_attention(B, H, N, d, grid_h, grid_w, m, lambda, eps, iters, dtype, flags);
+  if (rc != LAPNYS_OK) return rc;
+  if (!x || !w_qkv || !w_o || !dy || !ctx || !dx || !dw_qkv || !dw_o || !ws) return LAPNYS_EINVAL;
+  if (!a16(x) || !a16(w_qkv) || !a16(w_o) || !a16(dy) || !a16(ctx) || !a16(dx) || !a16(dw_qkv) ||
+      !a16(dw_o) || !a16(ws) || !a16_or_null(db_qkv) || !a16_or_null(db_o))
+    return LAPNYS_EINVAL;
+  const BlockLayout L = block_layout(B, N, C, H, d, m, iters, tied, dtype, flags);
+  if (ws_bytes < L.b_total) return LAPNYS_ENOSPC;
+  Blas* bl = blas_for_current_device();
+  if (bl == nullptr) return LAPNYS_ECUDA;
+
+  const int S = tied ? 2 : 3, HD = H * d;
+  const int rows = B * N;
+  const char* cb = (const char*)ctx;
+  const void* q = cb + L.c_q;
+  const void* k = tied ? q : (const void*)(cb + L.c_k);
+  const void* v = cb + L.c_v;
+  const void* ot = cb + L.c_ot;
+  char* wb = (char*)ws;
+  float* s32 = (float*)(wb + L.b_s32);
+  void* dO = wb + L.b_do;
+  void* dq = wb + L.b_dq;
+  void* dk = tied ? nullptr : (void*)(wb + L.b_dk);
+  void* dv = wb + L.b_dv;
+  void* dqkv = wb + L.b_dqkv;
+  float* part = (float*)(wb + L.b_part);
+  const cudaDataType tab = dtype == LAPNYS_BF16 ? CUDA_R_16BF : CUDA_R_32F;
+
+  std::lock_guard<std::mutex> lock(bl->mu);
+  CKG(cublasSetStream(bl->h, stream) == CUBLAS_STATUS_SUCCESS);
+  CKG(cublasSetWorkspace(bl->h, wb + L.b_blas, kBlasWs) == CUBLAS_STATUS_SUCCESS);
+  // output projection: dO = dY W_o^T (to heads), dW_o = Ot^T dY, db_o = column sums of dY
+  CKG(gemm_rm(bl->h, false, true, rows, HD, C, dy, C, w_o, C, s32, HD, tab, CUDA_R_32F));
+  CKB(DT_CALL(dtype, split_heads_t, s32, nullptr, dO, nullptr, nullptr, B, N, H, d, 1, stream));
+  CKG(gemm_rm(bl->h, true, false, HD, C, rows, ot, HD, dy, C, dw_o, C, tab, tab));
+  if (db_o != nullptr) CKB(DT_CALL(dtype, colsum_t, dy, part, db_o, (long long)rows, C, stream));
+  // the attention
+  rc = lapnys_bwd(q, tied ? nullptr : k, v, dO, (const char*)ctx + L.c_attn, dq, dk, dv, B, H, N,
+                  d, grid_h, grid_w, m, lambda, eps, iters, tied, stream, dtype, flags,
+                  wb + L.b_attn, L.attn_ws);
+  if (rc != LAPNYS_OK) return rc;
+  // QKV projection: dqkv = [dQ | dK | dV], dW_qkv = X^T dqkv, db_qkv, dX = dqkv W_qkv^T
+  CKB(DT_CALL(dtype, merge_heads_t, dq, tied ? dv : dk, dv, dqkv, B, N, H, d, S, stream));
+  CKG(gemm_rm(bl->h, true, false, C, S * HD, rows, x, C, dqkv, S * HD, dw_qkv, S * HD, tab, tab));
+  if (db_qkv != nullptr)
+    CKB(DT_CALL(dtype, colsum_t, dqkv, part, db_qkv, (long long)rows, S * HD, stream));
+  CKG(gemm_rm(bl->h, false, true, rows, C, S * HD, dqkv, S * HD, w_qkv, S * HD, dx, C, tab, tab));
+  return LAPNYS_OK;
+}
+
+}  // extern "C"

@@ -324,7 +324,11 @@ cudaError_t run_qstats(const Prob& p, const void* q, const float* L, float* spar
   DISPATCH_DT(qstats_t, p, q, L, spart, st);
 }
 
-// stats [BH][3][m]: mu, var (biased), 1 / sqrt(var + 1e-5)
+// Statistics are taken per slice, or (batch-pooled) over the B slices of a
+// head: group g < H, member r < B is slice r H + g.
+//
+// stats [BH][3][m]: mu, var (biased), 1 / sqrt(var + 1e-5).  Per slice: one
+// thread per (slice, landmark) merges its splits in order.
 __global__ void k_stats_final(const float* __restrict__ spart, float* __restrict__ stats, int BH,
                               int S, int m, int mp, int N) {
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
@@ -342,7 +346,51 @@ __global__ void k_stats_final(const float* __restrict__ spart, float* __restrict
   st[2 * m + a] = 1.0f / sqrtf(var + 1e-5f);
 }
 
+// Batch-pooled: CTA (head g, 32 landmarks), 8 rows of 32 lanes; row y merges
+// the (member, split) partials y, y + 8, ... in order, then row 0 merges the 8
+// row results in order (a fixed tree: deterministic), and all rows write the
+// result to every member.
+constexpr int kGrpRows = 8;
+__global__ void __launch_bounds__(32 * kGrpRows)
+    k_stats_final_grouped(const float* __restrict__ spart, float* __restrict__ stats, int H, int R,
+                          int S, int m, int mp, int N) {
+  __shared__ float sn[kGrpRows][32], smean[kGrpRows][32], sM2[kGrpRows][32];
+  const int g = blockIdx.x, a = blockIdx.y * 32 + threadIdx.x, y = threadIdx.y;
+  float n = 0.f, mean = 0.f, M2 = 0.f;
+  if (a < m) {
+    for (int i = y; i < R * S; i += kGrpRows) {
+      const int r = i / S, s = i - r * S;
+      const float* o = spart + ((size_t)(r * H + g) * S + s) * 3 * mp + a;
+      chan_merge(n, mean, M2, o[0], o[mp], o[2 * mp]);
+    }
+  }
+  sn[y][threadIdx.x] = n;
+  smean[y][threadIdx.x] = mean;
+  sM2[y][threadIdx.x] = M2;
+  __syncthreads();
+  if (y == 0) {
+    for (int j = 1; j < kGrpRows; ++j)
+      chan_merge(n, mean, M2, sn[j][threadIdx.x], smean[j][threadIdx.x], sM2[j][threadIdx.x]);
+    smean[0][threadIdx.x] = mean;
+    sM2[0][threadIdx.x] = M2 / ((float)N * (float)R);
+  }
+  __syncthreads();
+  if (a >= m) return;
+  mean = smean[0][threadIdx.x];
+  const float var = sM2[0][threadIdx.x];
+  const float rs = 1.0f / sqrtf(var + 1e-5f);
+  for (int r = y; r < R; r += kGrpRows) {
+    float* st = stats + (size_t)(r * H + g) * 3 * m;
+    st[a] = mean;
+    st[m + a] = var;
+    st[2 * m + a] = rs;
+  }
+}
+
 cudaError_t run_stats_final(const Prob& p, const float* spart, float* stats, cudaStream_t st) {
+  if (p.norm_batch() && p.B > 1)
+    return launch("stats_final", k_stats_final_grouped, dim3(p.H, (p.m + 31) / 32),
+                  dim3(32, kGrpRows), 0, st, spart, stats, p.H, p.B, p.Sq, p.m, p.mp, p.N);
   const int n = p.BH * p.m;
   return launch("stats_final", k_stats_final, dim3((n + 255) / 256), dim3(256), 0, st, spart, stats,
                 p.BH, p.Sq, p.m, p.mp, p.N);
@@ -796,7 +844,46 @@ __global__ void k_mdz(const float* __restrict__ ns_part, float* __restrict__ mdz
   mdz[(size_t)bh * 2 * mp + mp + a] = s1 / (float)N;
 }
 
+// Batch-pooled: the same two means over the B * N queries of head g, summed
+// with the fixed tree of k_stats_final_grouped and written to every member.
+__global__ void __launch_bounds__(32 * kGrpRows)
+    k_mdz_grouped(const float* __restrict__ ns_part, float* __restrict__ mdz, int H, int R, int S,
+                  int mp, int N) {
+  __shared__ float p0[kGrpRows][32], p1[kGrpRows][32];
+  const int g = blockIdx.x, a = blockIdx.y * 32 + threadIdx.x, y = threadIdx.y;
+  float s0 = 0.f, s1 = 0.f;
+  for (int i = y; i < R * S; i += kGrpRows) {
+    const int r = i / S, s = i - r * S;
+    const float* o = ns_part + ((size_t)(r * H + g) * S + s) * 2 * mp + a;
+    s0 += o[0];
+    s1 += o[mp];
+  }
+  p0[y][threadIdx.x] = s0;
+  p1[y][threadIdx.x] = s1;
+  __syncthreads();
+  if (y == 0) {
+    for (int j = 1; j < kGrpRows; ++j) {
+      s0 += p0[j][threadIdx.x];
+      s1 += p1[j][threadIdx.x];
+    }
+    const float n = (float)N * (float)R;
+    p0[0][threadIdx.x] = s0 / n;
+    p1[0][threadIdx.x] = s1 / n;
+  }
+  __syncthreads();
+  s0 = p0[0][threadIdx.x];
+  s1 = p1[0][threadIdx.x];
+  for (int r = y; r < R; r += kGrpRows) {
+    float* o = mdz + (size_t)(r * H + g) * 2 * mp;
+    o[a] = s0;
+    o[mp + a] = s1;
+  }
+}
+
 cudaError_t run_mdz(const Prob& p, const float* ns_part, float* mdz, cudaStream_t st) {
+  if (p.norm_batch() && p.B > 1)
+    return launch("mdz", k_mdz_grouped, dim3(p.H, p.mp / 32), dim3(32, kGrpRows), 0, st, ns_part,
+                  mdz, p.H, p.B, p.Sb, p.mp, p.N);
   const int n = p.BH * p.mp;
   return launch("mdz", k_mdz, dim3((n + 255) / 256), dim3(256), 0, st, ns_part, mdz, p.BH, p.Sb, p.mp,
                 p.N);

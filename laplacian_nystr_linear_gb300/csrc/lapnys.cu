@@ -214,9 +214,16 @@ static int check_common(int B, int H, int N, int d, int gh, int gw, int m, float
   if (!(lam > 0.f) || !isfinite(lam)) return LAPNYS_EINVAL;
   if (!(eps >= 0.f) || !isfinite(eps)) return LAPNYS_EINVAL;
   if (dtype != LAPNYS_F32 && dtype != LAPNYS_BF16) return LAPNYS_EINVAL;
-  if ((flags & ~(unsigned)(LAPNYS_NORM | LAPNYS_GAUSS)) != 0) return LAPNYS_EINVAL;
+  if ((flags & ~(unsigned)(LAPNYS_NORM | LAPNYS_GAUSS | LAPNYS_NORM_BATCH)) != 0)
+    return LAPNYS_EINVAL;
+  if ((flags & LAPNYS_NORM_BATCH) && !(flags & LAPNYS_NORM)) return LAPNYS_EINVAL;
   if (!d_supported(d)) return LAPNYS_ENOTSUP;
   return LAPNYS_OK;
+}
+
+int check_attention(int B, int H, int N, int d, int gh, int gw, int m, float lam, float eps,
+                    int iters, int dtype, unsigned flags) {
+  return check_common(B, H, N, d, gh, gw, m, lam, eps, iters, dtype, flags);
 }
 
 #define CK(x)                                  \

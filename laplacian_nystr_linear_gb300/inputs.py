@@ -43,6 +43,7 @@ class Workload:
     outliers: bool = False
     backward: bool = False
     kernel: str = "laplace"   # "laplace" or "gauss" (a name only; no arithmetic here)
+    norm_batch: bool = False  # with norm: statistics over the B slices of a head
 
     @property
     def N(self) -> int:

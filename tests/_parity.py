@@ -15,7 +15,7 @@ TDT = {"f32": torch.float32, "bf16": torch.bfloat16}
 
 def params_of(w: Workload) -> api.Params:
     return api.Params(w.B, w.H, w.grid_h, w.grid_w, w.d, w.m, w.lam, w.eps, w.iters, w.tied, w.norm,
-                      w.kernel)
+                      w.kernel, w.norm_batch)
 
 
 def to_dev(x: np.ndarray, dtype: str) -> torch.Tensor:
@@ -45,7 +45,8 @@ def gpu_run(w: Workload, inp: dict, backward: bool = False):
 
 def oracle_run(w: Workload, inp: dict, slices=None, backward: bool = False):
     O, saved = orc.forward(inp["q"], inp["k"], inp["v"], w.grid_h, w.grid_w, w.m, w.lam, w.eps,
-                           w.iters, w.norm, slices=slices, kernel=w.kernel)
+                           w.iters, w.norm, slices=slices, kernel=w.kernel,
+                           norm_batch=w.norm_batch)
     res = {"out": O, "saved": saved}
     if backward:
         res["grads"] = orc.backward(saved, inp["dout"], tied=w.tied)

@@ -91,7 +91,10 @@ def test_fwd_rejects_bad_arguments(lib):
     assert _fwd(lib, eps=-1.0) == LAPNYS_EINVAL
     assert _fwd(lib, iters=-1) == LAPNYS_EINVAL
     assert _fwd(lib, dtype=7) == LAPNYS_EINVAL
-    assert _fwd(lib, flags=4) == LAPNYS_EINVAL  # unknown flag bit (1: norm, 2: Gaussian kernel)
+    assert _fwd(lib, flags=8) == LAPNYS_EINVAL  # unknown bit (1: norm, 2: Gaussian, 4: batch stats)
+    assert _fwd(lib, flags=4) == LAPNYS_EINVAL  # batch-pooled statistics without the norm
+    assert _fwd(lib, flags=5) == LAPNYS_ENOSPC  # with it: valid (then fails on ws)
+    assert _fwd(lib, flags=7) == LAPNYS_ENOSPC
     assert _fwd(lib, q=None) == LAPNYS_EINVAL
     assert _fwd(lib, out=ctypes.c_void_p((1 << 20) + 4)) == LAPNYS_EINVAL   # misaligned
     assert _fwd(lib, tied=1, k=ctypes.c_void_p(2 << 20)) == LAPNYS_EINVAL  # tied but k != q

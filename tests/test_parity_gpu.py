@@ -334,6 +334,60 @@ def test_landmark_grid_gaussian():
 
 
 # ---------------------------------------------------------------------------
+# batch-pooled feature-map statistics (LAPNYS_NORM_BATCH): mean and variance of
+# each landmark column over the B * N queries of a head's B slices
+# ---------------------------------------------------------------------------
+BATCH_STATS = [
+    _small("bstats_f32", B=3, H=2, grid_h=16, grid_w=16, m=16, d=32, iters=8, norm=True,
+           norm_batch=True),
+    _small("bstats_f32_tied_ragged", B=4, H=1, grid_h=10, grid_w=12, m=9, d=16, iters=6,
+           norm=True, norm_batch=True, tied=True),
+    _small("bstats_bf16", dtype="bf16", B=2, H=3, grid_h=14, grid_w=14, m=49, d=64, iters=10,
+           norm=True, norm_batch=True),
+    _small("bstats_tc", dtype="bf16", B=3, H=2, grid_h=20, grid_w=20, m=100, d=64, iters=10,
+           norm=True, norm_batch=True),
+    _small("bstats_tc_gauss", dtype="bf16", B=2, H=2, grid_h=16, grid_w=16, m=128, d=32, iters=10,
+           norm=True, norm_batch=True, kernel="gauss"),
+    _small("bstats_d128", B=2, H=2, grid_h=8, grid_w=8, m=64, d=128, iters=6, norm=True,
+           norm_batch=True),
+]
+
+
+@pytest.mark.parametrize("w", BATCH_STATS, ids=lambda w: w.name)
+def test_batch_pooled_statistics(w):
+    inp = random_inputs(71 + w.m + w.B, w.B, w.H, w.N, w.d, w.dtype, tied=w.tied)
+    g = gpu_run(w, inp, backward=True)
+    o = oracle_run(w, inp, backward=True)
+    print(w.name, compare(w, g, o, backward=True))
+    st = g["ctx"]["stats"]
+    for h in range(w.H):
+        for b in range(1, w.B):   # one set of statistics per head, the same bits in every slice
+            np.testing.assert_array_equal(st[b, h], st[0, h])
+        mu, var, _ = o["saved"][(0, h)]["stats"]
+        assert rel(st[0, h, 0], mu) < 1e-5 and rel(st[0, h, 1], var) < 1e-4
+
+
+def test_batch_pooled_statistics_one_slice_per_head_is_per_slice():
+    # B = 1: the pooled statistics are the slice's own, bit for bit
+    w = _small("bstats_b1", B=1, H=3, grid_h=12, grid_w=12, m=16, d=64, iters=8, norm=True)
+    inp = random_inputs(77, w.B, w.H, w.N, w.d, w.dtype)
+    a = gpu_run(w, inp, backward=True)
+    b = gpu_run(dataclasses.replace(w, norm_batch=True), inp, backward=True)
+    for n in ("out", "dq", "dk", "dv"):
+        np.testing.assert_array_equal(a[n], b[n])
+
+
+def test_batch_pooled_statistics_pvt2_full_batch():
+    # the PVT stage-2 workload (B = 32, H = 2, 28 x 28 tokens, m = 49), one head's
+    # 32 slices against the oracle (the statistics couple all of them)
+    w = dataclasses.replace(WORKLOADS["pvt2"], norm_batch=True)
+    inp = make_inputs(w, with_grad=True)
+    g = gpu_run(w, inp, backward=True)
+    o = oracle_run(w, inp, slices={(b, 1) for b in range(w.B)}, backward=True)
+    print(w.name, "norm_batch", compare(w, g, o, backward=True))
+
+
+# ---------------------------------------------------------------------------
 # Gaussian-kernel variant (LAPNYS_GAUSS): k(x, y) = exp(-|x - y|_2^2 / lambda)
 # ---------------------------------------------------------------------------
 GAUSS_NAMES = ("f32", "f32_norm", "f32_tied", "bf16", "ragged", "ragged_large_m", "m1", "iters0",
