@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--kernel", choices=["laplace", "gauss"], default="laplace",
                     help="Laplacian kernel (the method) or its Gaussian-kernel variant")
+    ap.add_argument("--block", action="store_true",
+                    help="the whole attention layer: QKV projection, attention, output projection "
+                         "(C = H * d)")
     ap.add_argument("--norm-batch", action="store_true",
                     help="normalised workloads: feature-map statistics over the B slices of a head")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -182,14 +185,29 @@ def clock_summary(proc, path):
 # ---------------------------------------------------------------------------
 # CPU oracle (baseline and reference arm): one (b, h) slice, forward + backward
 # ---------------------------------------------------------------------------
-def _oracle_slice(wname: str, kernel: str = "laplace", norm_batch: bool = False):
+def _oracle_slice(wname: str, kernel: str = "laplace", norm_batch: bool = False,
+                  block: bool = False):
     """One unit of oracle work: a (b, h) slice, or with batch-pooled statistics
-    (which couple them) the B slices of one head."""
+    (which couple them) the B slices of one head; for the whole layer, one
+    head's share of it for one batch element (its Q, K, V columns of the
+    projection, the attention slice, its rows of the output projection),
+    credited with N / H tokens."""
     import dataclasses
 
-    from laplacian_nystr_linear_gb300.inputs import WORKLOADS, make_inputs
+    from laplacian_nystr_linear_gb300.inputs import WORKLOADS, block_inputs, make_inputs
     from oracle import lapnys_oracle as orc
     w0 = WORKLOADS[wname]
+    if block:
+        import numpy as np
+        C, d, S = w0.H * w0.d, w0.d, 2 if w0.tied else 3
+        b = block_inputs(6000 + w0.cfg, 1, w0.N, C, w0.H, d, w0.dtype, w0.tied, True)
+        cols = np.concatenate([np.arange(s * C, s * C + d) for s in range(S)])
+        t0 = time.perf_counter()
+        _, st = orc.block_forward(b["x"], b["w_qkv"][:, cols], b["b_qkv"][cols], b["w_o"][:d],
+                                  b["b_o"], 1, d, w0.grid_h, w0.grid_w, w0.m, w0.lam, w0.eps,
+                                  w0.iters, w0.norm, kernel, False, w0.tied)
+        orc.block_backward(st, b["dy"])
+        return time.perf_counter() - t0, w0.N / w0.H
     nb = bool(norm_batch and w0.norm)
     w = dataclasses.replace(w0, B=w0.B if nb else 1, H=1, kernel=kernel, norm_batch=nb)
     inp = make_inputs(w, with_grad=True)
@@ -207,18 +225,20 @@ def _single_thread_env():
     return env
 
 
-def cpu_baseline(wname: str, kernel: str = "laplace", norm_batch: bool = False):
+def cpu_baseline(wname: str, kernel: str = "laplace", norm_batch: bool = False,
+                 block: bool = False):
     """The oracle as it stands, one process, one thread, on whole (b, h) slices
     of the workload (at least 10 s of work)."""
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-worker",
                         "--workload", wname, "--kernel", kernel]
-                       + (["--norm-batch"] if norm_batch else []), capture_output=True, text=True,
-                       env=_single_thread_env(), timeout=1800)
+                       + (["--norm-batch"] if norm_batch else []) + (["--block"] if block else []),
+                       capture_output=True, text=True, env=_single_thread_env(), timeout=1800)
     if r.returncode != 0:
         return {"error": r.stderr.strip().splitlines()[-1:]}
     sec, tokens, n = json.loads(r.stdout.strip().splitlines()[-1])
     return {"value": tokens / sec, "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": (f"{n} head(s) x all B slices (batch-pooled statistics)" if norm_batch
+                       else f"{n} (b,h) share(s) of the layer (projections + attention)" if block
                        else f"{n} (b,h) slice(s)")
                       + f" of {wname} ({tokens} tokens), fwd+bwd, fp64, {sec:.1f} s single-threaded"}
 
@@ -237,7 +257,7 @@ def run_reference(args, rank, world):
     cores = max(1, min(os.cpu_count() or 1, max(args.steps, args.warmup)))
     ctx = mp.get_context("spawn")
     with ctx.Pool(cores) as pool:
-        task = (args.workload, args.kernel, args.norm_batch)
+        task = (args.workload, args.kernel, args.norm_batch, args.block)
         pool.map(_pool_task, [task] * max(args.warmup, 1))
         t0 = time.perf_counter()
         res = pool.map(_pool_task, [task] * args.steps)
@@ -249,7 +269,7 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": args.workload, "kernel": args.kernel,
-                                        "norm_batch": args.norm_batch,
+                                        "norm_batch": args.norm_batch, "block": args.block,
                                         "sample": "one (b,h) slice per step (one head's B slices "
                                                   "with batch-pooled statistics)"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -277,6 +297,8 @@ def run_ours(args, rank, world, local_rank):
         dist.init_process_group("nccl", device_id=dev)
     import dataclasses
     w = dataclasses.replace(WORKLOADS[args.workload], kernel=args.kernel)
+    if args.block and args.norm_batch:
+        raise SystemExit("--block times per-slice statistics; drop --norm-batch")
     if args.norm_batch:
         if not w.norm:
             raise SystemExit(f"--norm-batch needs a normalised workload; {w.name} has norm=False")
@@ -301,6 +323,34 @@ def run_ours(args, rank, world, local_rank):
         api.fwd(q, k, v, p, out=out, ctx=ctx, ws=ws)
         api.bwd(q, k, v, dout, ctx, p, dq=dq, dk=dk, dv=dv, ws=ws)
 
+    def fwd_only():
+        api.fwd(q, k, v, p, out=out, ctx=ctx, ws=ws)
+
+    if args.block:
+        # the layer around the attention: x [B, N, C] with C = H * d, seeded weights
+        from laplacian_nystr_linear_gb300.inputs import block_inputs
+        del q, k, v, dout, out, dq, dk, dv, ctx, ws
+        C = w.H * w.d
+        bp = api.BlockParams(p, C)
+        binp = block_inputs(6000 + w.cfg, w.B, w.N, C, w.H, w.d, w.dtype, w.tied, True)
+        host = {n: torch.from_numpy(binp[n]).to(tdt) for n in ("x", "dy")}
+        x, dy = host["x"].to(dev), host["dy"].to(dev)
+        wq, bq, wo, bo = (torch.from_numpy(binp[n]).to(tdt).to(dev)
+                          for n in ("w_qkv", "b_qkv", "w_o", "b_o"))
+        y, dx = torch.empty_like(x), torch.empty_like(x)
+        gw_q, gb_q, gw_o, gb_o = (torch.empty_like(t) for t in (wq, bq, wo, bo))
+        ctx = torch.empty(api.block_ctx_bytes(bp, tdt), dtype=torch.uint8, device=dev)
+        ws = torch.empty(api.block_workspace_bytes(bp, tdt), dtype=torch.uint8, device=dev)
+        q = x  # for the input-size and e2e byte counts below
+
+        def step():
+            api.block_fwd(x, wq, bq, wo, bo, bp, y=y, ctx=ctx, ws=ws)
+            api.block_bwd(x, wq, wo, dy, ctx, bp, dx=dx, dw_qkv=gw_q, db_qkv=gb_q, dw_o=gw_o,
+                          db_o=gb_o, ws=ws)
+
+        def fwd_only():
+            api.block_fwd(x, wq, bq, wo, bo, bp, y=y, ctx=ctx, ws=ws)
+
     def barrier():
         torch.cuda.synchronize()
         if world > 1:
@@ -312,7 +362,7 @@ def run_ours(args, rank, world, local_rank):
     # inputs smaller than L2 (Q, K, V, dO together): flush L2 between timed
     # steps by writing a buffer of twice its size, outside the timed intervals
     L2_BYTES = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 129e6)
-    in_bytes = 4 * q.numel() * q.element_size()
+    in_bytes = (2 if args.block else 4) * q.numel() * q.element_size()
     flush = None if in_bytes > L2_BYTES else torch.empty(2 * L2_BYTES // 4, dtype=torch.float32,
                                                           device=dev)
 
@@ -353,10 +403,9 @@ def run_ours(args, rank, world, local_rank):
 
     # forward alone (same buffers)
     for _ in range(2):
-        api.fwd(q, k, v, p, out=out, ctx=ctx, ws=ws)
+        fwd_only()
     barrier()
-    ms_fwd = max_over_ranks(timed(lambda: api.fwd(q, k, v, p, out=out, ctx=ctx, ws=ws), args.steps),
-                            world, dev)
+    ms_fwd = max_over_ranks(timed(fwd_only, args.steps), world, dev)
 
     # roofline of the dominant kernel (FP32 lane-ops; the path is ALU-bound)
     ops = algorithmic_ops(w)
@@ -381,7 +430,29 @@ def run_ours(args, rank, world, local_rank):
 
     # end to end through the public API: pinned host inputs in, results back to host
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.block:
+        # per step: x and dy in; y and dx out (weights and their gradients stay resident)
+        pin = {n: host[n].pin_memory() for n in host}
+        back = {n: torch.empty(x.shape, dtype=tdt).pin_memory() for n in ("y", "dx")}
+        ne = max(3, min(args.steps, 10))
+
+        def step_e2e():
+            xd = pin["x"].to(dev, non_blocking=True)
+            dyd = pin["dy"].to(dev, non_blocking=True)
+            yo, c = api.block_fwd(xd, wq, bq, wo, bo, bp, y=y, ctx=ctx, ws=ws)
+            g = api.block_bwd(xd, wq, wo, dyd, c, bp, dx=dx, dw_qkv=gw_q, db_qkv=gb_q, dw_o=gw_o,
+                              db_o=gb_o, ws=ws)
+            back["y"].copy_(yo, non_blocking=True)
+            back["dx"].copy_(g[0], non_blocking=True)
+
+        step_e2e()
+        barrier()
+        ms_e2e = max_over_ranks(timed(step_e2e, ne), world, dev)
+        nbytes = x.numel() * x.element_size()
+        e2e = {"value": world * w.tokens / (ms_e2e / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": 2 * nbytes, "d2h_bytes_per_step": 2 * nbytes,
+               "ms_per_step": ms_e2e}
+    elif not args.no_e2e:
         pin = {n: host[n].pin_memory() for n in host}
         back = {n: torch.empty(q.shape, dtype=tdt).pin_memory() for n in ("out", "dq", "dk", "dv")}
         ne = max(3, min(args.steps, 10))
@@ -413,7 +484,7 @@ def run_ours(args, rank, world, local_rank):
         return
     base = None
     if world == 1 and not args.no_cpu_baseline:
-        base = cpu_baseline(args.workload, args.kernel, w.norm_batch)
+        base = cpu_baseline(args.workload, args.kernel, w.norm_batch, args.block)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -424,6 +495,8 @@ def run_ours(args, rank, world, local_rank):
                    "d": w.d, "m": w.m, "iters": w.iters, "lambda": w.lam, "eps": w.eps,
                    "norm": w.norm, "norm_batch": w.norm_batch, "tied": w.tied,
                    "pass": "fwd+bwd",
+                   "block": ({"C": w.H * w.d, "projections": "cuBLAS bf16/fp32 GEMMs, fp32 "
+                              "accumulation", "e2e": "x, dy in; y, dx out"} if args.block else None),
                    "l2": (f"inputs larger than L2 (Q, K, V, dO {in_bytes / 4e6:.0f} MB each, "
                           f"{L2_BYTES / 1e6:.0f} MB L2); no flush" if flush is None else
                           f"inputs {in_bytes / 1e6:.0f} MB < L2: {2 * L2_BYTES / 1e6:.0f} MB "
@@ -447,7 +520,7 @@ def main():
         # whole slices until at least 10 s of CPU work (a bounded sample)
         sec = tokens = n = 0
         while sec < 10.0 or n == 0:
-            s1, t1 = _oracle_slice(args.workload, args.kernel, args.norm_batch)
+            s1, t1 = _oracle_slice(args.workload, args.kernel, args.norm_batch, args.block)
             sec, tokens, n = sec + s1, tokens + t1, n + 1
         print(json.dumps([sec, tokens, n]))
         return

@@ -223,3 +223,133 @@ def attention(q, k, v, grid, m, lam=None, eps=1e-3, iters=20, tied=False, norm=F
     if tied:
         k = q
     return _Attention.apply(q, k, v, p)
+
+
+# ---------------------------------------------------------------------------
+# the attention block: [Q | K | V] = X W_qkv + b_qkv, per-head attention,
+# Y = concat_h(O_h) W_o + b_o  (lapnys_block_fwd / lapnys_block_bwd)
+# ---------------------------------------------------------------------------
+@dataclasses.dataclass(frozen=True)
+class BlockParams:
+    """The attention's parameters plus the embedding width C of x [B, N, C]."""
+    attn: Params
+    C: int
+
+    @property
+    def S(self) -> int:
+        return 2 if self.attn.tied else 3
+
+    def dims(self):
+        a = self.attn
+        return (a.B, a.N, self.C, a.H, a.d, a.grid_h, a.grid_w, a.m)
+
+    def sizes(self):
+        a = self.attn
+        return (a.B, a.N, self.C, a.H, a.d, a.m, a.iters, int(a.tied))
+
+
+def block_ctx_bytes(bp: BlockParams, dtype: torch.dtype) -> int:
+    return load().lapnys_block_ctx_bytes(*bp.sizes(), _DT[dtype], bp.attn.flags)
+
+
+def block_workspace_bytes(bp: BlockParams, dtype: torch.dtype) -> int:
+    return load().lapnys_block_workspace_bytes(*bp.sizes(), _DT[dtype], bp.attn.flags)
+
+
+def _check_param(t, name, shape, like):
+    if t is None:
+        return
+    if not t.is_cuda or not t.is_contiguous() or t.dtype != like.dtype or tuple(t.shape) != shape:
+        raise ValueError(f"{name} must be a contiguous CUDA tensor of shape {shape} and {like.dtype}")
+
+
+def _check_block(x, w_qkv, b_qkv, w_o, b_o, bp: BlockParams):
+    a = bp.attn
+    HD = a.H * a.d
+    _check_param(x, "x", (a.B, a.N, bp.C), x)
+    _check_param(w_qkv, "w_qkv", (bp.C, bp.S * HD), x)
+    _check_param(b_qkv, "b_qkv", (bp.S * HD,), x)
+    _check_param(w_o, "w_o", (HD, bp.C), x)
+    _check_param(b_o, "b_o", (bp.C,), x)
+
+
+def block_fwd(x, w_qkv, b_qkv, w_o, b_o, bp: BlockParams, y=None, ctx=None, ws=None,
+              need_ctx=True):
+    """lapnys_block_fwd: returns (y, ctx); ctx is None when need_ctx is False."""
+    _check_block(x, w_qkv, b_qkv, w_o, b_o, bp)
+    a = bp.attn
+    dev = x.device
+    y = torch.empty_like(x) if y is None else y
+    _check_param(y, "y", tuple(x.shape), x)
+    if need_ctx and ctx is None:
+        ctx = torch.empty(block_ctx_bytes(bp, x.dtype), dtype=torch.uint8, device=dev)
+    if ws is None:
+        ws = torch.empty(block_workspace_bytes(bp, x.dtype), dtype=torch.uint8, device=dev)
+    rc = load().lapnys_block_fwd(
+        _ptr(x), _ptr(w_qkv), _ptr(b_qkv), _ptr(w_o), _ptr(b_o), _ptr(y), *bp.dims(), a.lam, a.eps,
+        a.iters, int(a.tied), _stream(dev), _dtype(x), a.flags,
+        _ptr(ctx) if need_ctx else None, ctx.numel() if need_ctx else 0, _ptr(ws), ws.numel())
+    check(rc, "lapnys_block_fwd")
+    return y, (ctx if need_ctx else None)
+
+
+def block_bwd(x, w_qkv, w_o, dy, ctx, bp: BlockParams, bias_grads=True, dx=None, dw_qkv=None,
+              db_qkv=None, dw_o=None, db_o=None, ws=None):
+    """lapnys_block_bwd: returns (dx, dw_qkv, db_qkv, dw_o, db_o); the bias
+    gradients are None when bias_grads is False."""
+    _check_block(x, w_qkv, None, w_o, None, bp)
+    _check_param(dy, "dy", tuple(x.shape), x)
+    a = bp.attn
+    dev = x.device
+    HD = a.H * a.d
+    dx = torch.empty_like(x) if dx is None else dx
+    dw_qkv = torch.empty_like(w_qkv) if dw_qkv is None else dw_qkv
+    dw_o = torch.empty_like(w_o) if dw_o is None else dw_o
+    if bias_grads:
+        db_qkv = x.new_empty((bp.S * HD,)) if db_qkv is None else db_qkv
+        db_o = x.new_empty((bp.C,)) if db_o is None else db_o
+    else:
+        db_qkv = db_o = None
+    if ws is None:
+        ws = torch.empty(block_workspace_bytes(bp, x.dtype), dtype=torch.uint8, device=dev)
+    rc = load().lapnys_block_bwd(
+        _ptr(x), _ptr(w_qkv), _ptr(w_o), _ptr(dy), _ptr(ctx), _ptr(dx), _ptr(dw_qkv), _ptr(db_qkv),
+        _ptr(dw_o), _ptr(db_o), *bp.dims(), a.lam, a.eps, a.iters, int(a.tied), _stream(dev),
+        _dtype(x), a.flags, _ptr(ws), ws.numel())
+    check(rc, "lapnys_block_bwd")
+    return dx, dw_qkv, db_qkv, dw_o, db_o
+
+
+class _Block(torch.autograd.Function):
+    @staticmethod
+    def forward(fctx, x, w_qkv, b_qkv, w_o, b_o, bp: BlockParams):
+        y, ctx = block_fwd(x, w_qkv, b_qkv, w_o, b_o, bp, need_ctx=True)
+        fctx.bp = bp
+        fctx.has_bias = (b_qkv is not None, b_o is not None)
+        fctx.save_for_backward(x, w_qkv, w_o, ctx)
+        return y
+
+    @staticmethod
+    def backward(fctx, dy):
+        x, w_qkv, w_o, ctx = fctx.saved_tensors
+        dx, dw, db, dwo, dbo = block_bwd(x, w_qkv, w_o, dy.contiguous(), ctx, fctx.bp,
+                                         bias_grads=any(fctx.has_bias))
+        return (dx, dw, db if fctx.has_bias[0] else None, dwo, dbo if fctx.has_bias[1] else None,
+                None)
+
+
+def attention_block(x, w_qkv, b_qkv, w_o, b_o, grid, heads, m, lam=None, eps=1e-3, iters=20,
+                    tied=False, norm=False, kernel="laplace", norm_batch=False):
+    """One multi-head layer with autograd: [Q | K | V] = x w_qkv + b_qkv, the
+    Nystrom attention per head, y = concat(heads) w_o + b_o.
+
+    x: [B, N, C] CUDA tensor (float32 or bfloat16), N = grid[0] * grid[1];
+    w_qkv: [C, S * heads * d] with column blocks (Q | K | V) (S = 3) or, tied,
+    (Q = K | V) (S = 2); w_o: [heads * d, C]; biases [S * heads * d] and [C] or None.
+    lam defaults to d.
+    """
+    B, N, C = x.shape
+    d = w_o.shape[0] // heads
+    a = Params(B, heads, grid[0], grid[1], d, m, float(d if lam is None else lam), float(eps),
+               int(iters), bool(tied), bool(norm), str(kernel), bool(norm_batch))
+    return _Block.apply(x, w_qkv, b_qkv, w_o, b_o, BlockParams(a, C))

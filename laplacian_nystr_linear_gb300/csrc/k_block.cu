@@ -253,7 +253,7 @@ BlockLayout block_layout(int B, int N, int C, int H, int d, int m, int iters, in
   L.f_o = o; o = align256(o + head);
   L.f_lite = o; o = align256(o + saved);
   L.f_attn = o; o = align256(o + L.attn_ws);
-  L.f_blas = o; o = align256(o + kBlasWs);
+  L.f_blas = o; o = align256(o + kBlasWs + 256);
   L.f_total = o;
 
   o = 0;
@@ -265,12 +265,14 @@ BlockLayout block_layout(int B, int N, int C, int H, int d, int m, int iters, in
   L.b_dqkv = o; o = align256(o + rows * S * HD * es);
   L.b_part = o; o = align256(o + (size_t)kColSplits * wide * 4);
   L.b_attn = o; o = align256(o + L.attn_ws);
-  L.b_blas = o; o = align256(o + kBlasWs);
+  L.b_blas = o; o = align256(o + kBlasWs + 256);
   L.b_total = o;
   return L;
 }
 
 bool a16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+// cuBLAS wants its workspace 256-byte aligned; the slice has 256 bytes of slack
+void* blas_ws(char* p) { return (void*)(((uintptr_t)p + 255) & ~(uintptr_t)255); }
 bool a16_or_null(const void* p) { return p == nullptr || a16(p); }
 
 #define CKB(x)                                   \
@@ -339,7 +341,7 @@ int lapnys_block_fwd(const void* x, const void* w_qkv, const void* b_qkv, const 
 
   std::lock_guard<std::mutex> lock(bl->mu);
   CKG(cublasSetStream(bl->h, stream) == CUBLAS_STATUS_SUCCESS);
-  CKG(cublasSetWorkspace(bl->h, wb + L.f_blas, kBlasWs) == CUBLAS_STATUS_SUCCESS);
+  CKG(cublasSetWorkspace(bl->h, blas_ws(wb + L.f_blas), kBlasWs) == CUBLAS_STATUS_SUCCESS);
   // [Q | K | V] = X W_qkv (+ b_qkv, in the head split)
   CKG(gemm_rm(bl->h, false, false, rows, S * HD, C, x, C, w_qkv, S * HD, s32, S * HD, tab,
               CUDA_R_32F));
@@ -391,7 +393,7 @@ int lapnys_block_bwd(const void* x, const void* w_qkv, const void* w_o, const vo
 
   std::lock_guard<std::mutex> lock(bl->mu);
   CKG(cublasSetStream(bl->h, stream) == CUBLAS_STATUS_SUCCESS);
-  CKG(cublasSetWorkspace(bl->h, wb + L.b_blas, kBlasWs) == CUBLAS_STATUS_SUCCESS);
+  CKG(cublasSetWorkspace(bl->h, blas_ws(wb + L.b_blas), kBlasWs) == CUBLAS_STATUS_SUCCESS);
   // output projection: dO = dY W_o^T (to heads), dW_o = Ot^T dY, db_o = column sums of dY
   CKG(gemm_rm(bl->h, false, true, rows, HD, C, dy, C, w_o, C, s32, HD, tab, CUDA_R_32F));
   CKB(DT_CALL(dtype, split_heads_t, s32, nullptr, dO, nullptr, nullptr, B, N, H, d, 1, stream));

@@ -150,3 +150,25 @@ def random_inputs(seed: int, B: int, H: int, N: int, d: int, dtype: str = "f32",
 def isqrt_exact(m: int) -> int:
     r = math.isqrt(m)
     return r if r * r == m else -1
+
+
+def block_inputs(seed: int, B: int, N: int, C: int, H: int, d: int, dtype: str = "f32",
+                 tied: bool = False, bias: bool = True) -> dict:
+    """Seeded inputs of the attention block: x and dy [B, N, C] ~ N(0, 1), the
+    projection weights ~ N(0, 1 / fan_in) (so Q, K, V come out ~ N(0, 1)) and
+    biases ~ N(0, 0.1^2) (None when bias is False); float32 arrays, rounded to
+    bf16 values when dtype is "bf16"."""
+    rng = np.random.default_rng(seed)
+    S = 2 if tied else 3
+    f32 = np.float32
+    out = {
+        "x": rng.standard_normal((B, N, C), dtype=f32),
+        "w_qkv": (rng.standard_normal((C, S * H * d), dtype=f32) / np.sqrt(C)).astype(f32),
+        "b_qkv": (rng.standard_normal(S * H * d, dtype=f32) * 0.1).astype(f32) if bias else None,
+        "w_o": (rng.standard_normal((H * d, C), dtype=f32) / np.sqrt(H * d)).astype(f32),
+        "b_o": (rng.standard_normal(C, dtype=f32) * 0.1).astype(f32) if bias else None,
+        "dy": rng.standard_normal((B, N, C), dtype=f32),
+    }
+    if dtype == "bf16":
+        out = {n: (None if a is None else round_bf16(a)) for n, a in out.items()}
+    return out

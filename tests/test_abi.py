@@ -123,3 +123,60 @@ def test_bwd_rejects_bad_arguments(lib):
 
 def test_launch_counter_starts_at_zero_without_gpu(lib):
     assert lib.lapnys_launch_count() == 0
+
+
+# ---- the attention block -------------------------------------------------------
+def test_block_sizes(lib):
+    # PVT-like layer: 8 x 16384 tokens, C = 512, 8 heads of 64, m = 256
+    c = lib.lapnys_block_ctx_bytes(8, 16384, 512, 8, 64, 256, 24, 0, 1, 0)
+    attn = lib.lapnys_ctx_bytes(8, 8, 16384, 64, 256, 24, 0)
+    assert c >= attn + 4 * 8 * 16384 * 512 * 2       # + saved Q, K, V, concatenated heads (bf16)
+    assert lib.lapnys_block_ctx_bytes(8, 16384, 512, 8, 64, 256, 24, 1, 1, 0) < c   # tied: no K
+    assert lib.lapnys_block_workspace_bytes(8, 16384, 512, 8, 64, 256, 24, 0, 1, 0) > 0
+    assert lib.lapnys_block_ctx_bytes(1, 196, 12, 1, 32, 49, 20, 0, 0, 0) == 0    # C % 8 != 0
+    assert lib.lapnys_block_ctx_bytes(1, 196, 64, 1, 32, 49, 20, 2, 0, 0) == 0    # tied not 0/1
+    assert lib.lapnys_block_ctx_bytes(1, 196, 64, 1, 32, 49, 20, 0, 7, 0) == 0    # dtype
+    assert lib.lapnys_block_workspace_bytes(1, 16, 64, 1, 32, 25, 20, 0, 0, 0) == 0  # m > N
+
+
+def _block_fwd(lib, **kw):
+    a = dict(x=FAKE, w=FAKE, b=None, wo=FAKE, bo=None, y=FAKE, B=1, N=196, C=64, H=2, d=32, gh=14,
+             gw=14, m=49, lam=32.0, eps=1e-3, iters=20, tied=0, dtype=0, flags=0, ctx=None,
+             ctx_bytes=0, ws=FAKE, ws_bytes=0)
+    a.update(kw)
+    return lib.lapnys_block_fwd(a["x"], a["w"], a["b"], a["wo"], a["bo"], a["y"], a["B"], a["N"],
+                                a["C"], a["H"], a["d"], a["gh"], a["gw"], a["m"], a["lam"], a["eps"],
+                                a["iters"], a["tied"], None, a["dtype"], a["flags"], a["ctx"],
+                                a["ctx_bytes"], a["ws"], a["ws_bytes"])
+
+
+def test_block_fwd_rejects_bad_arguments(lib):
+    from laplacian_nystr_linear_gb300._lib import LAPNYS_EINVAL, LAPNYS_ENOSPC, LAPNYS_ENOTSUP
+    assert _block_fwd(lib, C=12) == LAPNYS_EINVAL                  # C not a multiple of 8
+    assert _block_fwd(lib, N=195) == LAPNYS_EINVAL                 # N != grid_h * grid_w
+    assert _block_fwd(lib, tied=2) == LAPNYS_EINVAL
+    assert _block_fwd(lib, flags=4) == LAPNYS_EINVAL               # batch statistics without norm
+    assert _block_fwd(lib, x=None) == LAPNYS_EINVAL
+    assert _block_fwd(lib, y=ctypes.c_void_p((1 << 20) + 8)) == LAPNYS_EINVAL   # misaligned
+    assert _block_fwd(lib, b=ctypes.c_void_p((1 << 20) + 4)) == LAPNYS_EINVAL   # misaligned bias
+    assert _block_fwd(lib, d=24) == LAPNYS_ENOTSUP
+    assert _block_fwd(lib, ws_bytes=16) == LAPNYS_ENOSPC
+    need = lib.lapnys_block_workspace_bytes(1, 196, 64, 2, 32, 49, 20, 0, 0, 0)
+    assert _block_fwd(lib, ws_bytes=need, ctx=FAKE, ctx_bytes=16) == LAPNYS_ENOSPC
+
+
+def test_block_bwd_rejects_bad_arguments(lib):
+    from laplacian_nystr_linear_gb300._lib import LAPNYS_EINVAL, LAPNYS_ENOSPC
+
+    def bwd(**kw):
+        a = dict(ctx=FAKE, dx=FAKE, dw=FAKE, db=None, dwo=FAKE, dbo=None, ws_bytes=0)
+        a.update(kw)
+        return lib.lapnys_block_bwd(FAKE, FAKE, FAKE, FAKE, a["ctx"], a["dx"], a["dw"], a["db"],
+                                    a["dwo"], a["dbo"], 1, 196, 64, 2, 32, 14, 14, 49, 32.0, 1e-3, 20,
+                                    0, None, 0, 0, FAKE, a["ws_bytes"])
+
+    assert bwd(ctx=None) == LAPNYS_EINVAL
+    assert bwd(dx=None) == LAPNYS_EINVAL
+    assert bwd(dwo=None) == LAPNYS_EINVAL
+    assert bwd(db=ctypes.c_void_p((1 << 20) + 4)) == LAPNYS_EINVAL
+    assert bwd() == LAPNYS_ENOSPC
