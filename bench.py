@@ -436,14 +436,28 @@ def run_ours(args, rank, world, local_rank):
         back = {n: torch.empty(x.shape, dtype=tdt).pin_memory() for n in ("y", "dx")}
         ne = max(3, min(args.steps, 10))
 
+        cs = torch.cuda.Stream(dev)
+        dy_dev = torch.empty_like(x)
+        ev = [torch.cuda.Event() for _ in range(3)]
+
         def step_e2e():
+            # dy comes in while the forward runs, y goes out while the backward runs
             xd = pin["x"].to(dev, non_blocking=True)
-            dyd = pin["dy"].to(dev, non_blocking=True)
+            cs.wait_stream(stream)
+            with torch.cuda.stream(cs):
+                dy_dev.copy_(pin["dy"], non_blocking=True)
+                ev[0].record(cs)
             yo, c = api.block_fwd(xd, wq, bq, wo, bo, bp, y=y, ctx=ctx, ws=ws)
-            g = api.block_bwd(xd, wq, wo, dyd, c, bp, dx=dx, dw_qkv=gw_q, db_qkv=gb_q, dw_o=gw_o,
-                              db_o=gb_o, ws=ws)
-            back["y"].copy_(yo, non_blocking=True)
+            ev[1].record(stream)
+            with torch.cuda.stream(cs):
+                cs.wait_event(ev[1])
+                back["y"].copy_(yo, non_blocking=True)
+                ev[2].record(cs)
+            stream.wait_event(ev[0])
+            g = api.block_bwd(xd, wq, wo, dy_dev, c, bp, dx=dx, dw_qkv=gw_q, db_qkv=gb_q,
+                              dw_o=gw_o, db_o=gb_o, ws=ws)
             back["dx"].copy_(g[0], non_blocking=True)
+            stream.wait_event(ev[2])
 
         step_e2e()
         barrier()
@@ -457,18 +471,32 @@ def run_ours(args, rank, world, local_rank):
         back = {n: torch.empty(q.shape, dtype=tdt).pin_memory() for n in ("out", "dq", "dk", "dv")}
         ne = max(3, min(args.steps, 10))
 
+        cs = torch.cuda.Stream(dev)
+        dd = torch.empty_like(q)
+        ev = [torch.cuda.Event() for _ in range(3)]
+
         def step_e2e():
+            # dO comes in while the forward runs, out goes back while the backward runs
             qd = pin["q"].to(dev, non_blocking=True)
             kd = qd if w.tied else pin["k"].to(dev, non_blocking=True)
             vd = pin["v"].to(dev, non_blocking=True)
-            dd = pin["dout"].to(dev, non_blocking=True)
+            cs.wait_stream(stream)
+            with torch.cuda.stream(cs):
+                dd.copy_(pin["dout"], non_blocking=True)
+                ev[0].record(cs)
             o, c = api.fwd(qd, kd, vd, p, out=out, ctx=ctx, ws=ws)
+            ev[1].record(stream)
+            with torch.cuda.stream(cs):
+                cs.wait_event(ev[1])
+                back["out"].copy_(o, non_blocking=True)
+                ev[2].record(cs)
+            stream.wait_event(ev[0])
             gq, gk, gv = api.bwd(qd, kd, vd, dd, c, p, dq=dq, dk=dk, dv=dv, ws=ws)
-            back["out"].copy_(o, non_blocking=True)
             back["dq"].copy_(gq, non_blocking=True)
             if gk is not None:
                 back["dk"].copy_(gk, non_blocking=True)
             back["dv"].copy_(gv, non_blocking=True)
+            stream.wait_event(ev[2])
 
         step_e2e()
         barrier()

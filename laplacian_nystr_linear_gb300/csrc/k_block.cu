@@ -27,7 +27,6 @@ namespace {
 
 constexpr int kBlockThreads = 256;
 constexpr size_t kBlasWs = 32u << 20;  // cuBLAS workspace carved out of the caller's ws
-constexpr int kColSplits = 512;        // row splits of the bias-gradient column sums (max)
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -43,130 +42,165 @@ __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
 }
 
 // ---- layout kernels ---------------------------------------------------------
-// One thread per 4 consecutive elements of a head row (d is a multiple of 16).
+// A CTA takes kRows consecutive token rows; a thread takes column groups of 4
+// (d is a multiple of 16, so a group stays inside one head row), works out the
+// group's (block s, head h, offset j) once and walks the rows.  Rows are
+// contiguous in the [B*N][W] side, head rows in the [B][H][N][d] side: both
+// sides move 16-byte (fp32) or 8-byte (bf16) pieces, consecutive across the
+// threads of a head.
+constexpr int kRows = 64;
 
-// src [B*N][S*H*d] float32 (+ bias [S*H*d]) -> dst_s [B][H][N][d] of T, s < S
+struct ColMap {
+  int s, h, j;
+};
+__device__ __forceinline__ ColMap col_map(int col, int HD, int d) {
+  ColMap c;
+  c.s = col / HD;
+  const int hc = col - c.s * HD;
+  c.h = hc / d;
+  c.j = hc - c.h * d;
+  return c;
+}
+
+// src [rows][S*H*d] float32 (+ bias [S*H*d]) -> dst_s [B][H][N][d] of T
 template <typename T>
 __global__ void k_split_heads(const float* __restrict__ src, const T* __restrict__ bias,
                               T* __restrict__ d0, T* __restrict__ d1, T* __restrict__ d2, int N,
-                              int H, int d, int S, long long n4) {
-  const long long e4 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (e4 >= n4) return;
-  const long long e = e4 * 4;
+                              int H, int d, int S, int rows) {
   const int HD = H * d, W = S * HD;
-  const long long row = e / W;
-  const int col = (int)(e - row * W);
-  const int s = col / HD, hc = col - s * HD, h = hc / d, j = hc - h * d;
-  const long long b = row / N, n = row - b * N;
-  float4 v = ld4(src + e);
-  if (bias != nullptr) {
-    const float4 bv = ld4(bias + col);
-    v.x += bv.x; v.y += bv.y; v.z += bv.z; v.w += bv.w;
+  const int r0 = blockIdx.x * kRows, r1 = min(r0 + kRows, rows);
+  for (int col = threadIdx.x * 4; col < W; col += blockDim.x * 4) {
+    const ColMap c = col_map(col, HD, d);
+    T* dst = c.s == 0 ? d0 : (c.s == 1 ? d1 : d2);
+    float4 bv = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (bias != nullptr) bv = ld4(bias + col);
+    int b = r0 / N, n = r0 - b * N;
+#pragma unroll 4
+    for (int r = r0; r < r1; ++r) {
+      float4 v = ld4(src + (size_t)r * W + col);
+      v.x += bv.x; v.y += bv.y; v.z += bv.z; v.w += bv.w;
+      st4(dst + (((size_t)b * H + c.h) * N + n) * d + c.j, v);
+      if (++n == N) { n = 0; ++b; }
+    }
   }
-  T* dst = s == 0 ? d0 : (s == 1 ? d1 : d2);
-  st4(dst + ((b * H + h) * N + n) * d + j, v);
 }
 
-// src_s [B][H][N][d] of T, s < S -> dst [B*N][S*H*d] of T
+// src_s [B][H][N][d] of T -> dst [rows][S*H*d] of T; with part != null also
+// part[cta][col] = the column sums of the CTA's rows (in row order)
 template <typename T>
 __global__ void k_merge_heads(const T* __restrict__ s0, const T* __restrict__ s1,
-                              const T* __restrict__ s2, T* __restrict__ dst, int N, int H, int d,
-                              int S, long long n4) {
-  const long long e4 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (e4 >= n4) return;
-  const long long e = e4 * 4;
+                              const T* __restrict__ s2, T* __restrict__ dst,
+                              float* __restrict__ part, int N, int H, int d, int S, int rows) {
   const int HD = H * d, W = S * HD;
-  const long long row = e / W;
-  const int col = (int)(e - row * W);
-  const int s = col / HD, hc = col - s * HD, h = hc / d, j = hc - h * d;
-  const long long b = row / N, n = row - b * N;
-  const T* src = s == 0 ? s0 : (s == 1 ? s1 : s2);
-  st4(dst + e, ld4(src + ((b * H + h) * N + n) * d + j));
+  const int r0 = blockIdx.x * kRows, r1 = min(r0 + kRows, rows);
+  for (int col = threadIdx.x * 4; col < W; col += blockDim.x * 4) {
+    const ColMap c = col_map(col, HD, d);
+    const T* src = c.s == 0 ? s0 : (c.s == 1 ? s1 : s2);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int b = r0 / N, n = r0 - b * N;
+#pragma unroll 4
+    for (int r = r0; r < r1; ++r) {
+      const float4 v = ld4(src + (((size_t)b * H + c.h) * N + n) * d + c.j);
+      st4(dst + (size_t)r * W + col, v);  // v holds T values: stored exactly
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      if (++n == N) { n = 0; ++b; }
+    }
+    if (part != nullptr) st4(part + (size_t)blockIdx.x * W + col, acc);
+  }
 }
 
 // dst [rows][C] of T = src [rows][C] float32 + bias [C] (bias may be null)
 template <typename T>
 __global__ void k_bias_rows(const float* __restrict__ src, const T* __restrict__ bias,
-                            T* __restrict__ dst, int C, long long n4) {
-  const long long e4 = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (e4 >= n4) return;
-  const long long e = e4 * 4;
-  float4 v = ld4(src + e);
-  if (bias != nullptr) {
-    const float4 bv = ld4(bias + (int)(e % C));
-    v.x += bv.x; v.y += bv.y; v.z += bv.z; v.w += bv.w;
+                            T* __restrict__ dst, int C, int rows) {
+  const int r0 = blockIdx.x * kRows, r1 = min(r0 + kRows, rows);
+  for (int col = threadIdx.x * 4; col < C; col += blockDim.x * 4) {
+    float4 bv = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (bias != nullptr) bv = ld4(bias + col);
+#pragma unroll 4
+    for (int r = r0; r < r1; ++r) {
+      float4 v = ld4(src + (size_t)r * C + col);
+      v.x += bv.x; v.y += bv.y; v.z += bv.z; v.w += bv.w;
+      st4(dst + (size_t)r * C + col, v);
+    }
   }
-  st4(dst + e, v);
 }
 
-// part[split][col] = sum of G[r][col] over the split's rows, in row order
+// part[cta][col] = sum of G[r][col] over the CTA's rows, in row order
 template <typename T>
-__global__ void k_colsum_part(const T* __restrict__ G, float* __restrict__ part, long long rows,
-                              int cols, long long rows_per) {
-  const int col = blockIdx.x * blockDim.x + threadIdx.x;
-  if (col >= cols) return;
-  const long long r0 = (long long)blockIdx.y * rows_per;
-  const long long r1 = r0 + rows_per < rows ? r0 + rows_per : rows;
-  float acc = 0.f;
-  for (long long r = r0; r < r1; ++r) acc += to_f(G[r * cols + col]);
-  part[(size_t)blockIdx.y * cols + col] = acc;
+__global__ void k_colsum_rows(const T* __restrict__ G, float* __restrict__ part, int cols,
+                              int rows) {
+  const int r0 = blockIdx.x * kRows, r1 = min(r0 + kRows, rows);
+  for (int col = threadIdx.x * 4; col < cols; col += blockDim.x * 4) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int r = r0; r < r1; ++r) {
+      const float4 v = ld4(G + (size_t)r * cols + col);
+      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    st4(part + (size_t)blockIdx.x * cols + col, acc);
+  }
 }
 
-// out[col] = sum over splits in order
+// out[col] = sum of the CTAs' partial sums: CTA (32 columns) x 32 rows of
+// lanes; row y adds partials y, y + 32, ... in order, then row 0 adds the 32
+// row sums in order (a fixed tree: deterministic)
+constexpr int kSumRows = 32;
 template <typename T>
-__global__ void k_colsum_final(const float* __restrict__ part, T* __restrict__ out, int splits,
-                               int cols) {
-  const int col = blockIdx.x * blockDim.x + threadIdx.x;
-  if (col >= cols) return;
+__global__ void __launch_bounds__(32 * kSumRows)
+    k_colsum_final(const float* __restrict__ part, T* __restrict__ out, int splits, int cols) {
+  __shared__ float acc_s[kSumRows][33];
+  const int col = blockIdx.x * 32 + threadIdx.x, y = threadIdx.y;
   float acc = 0.f;
-  for (int s = 0; s < splits; ++s) acc += part[(size_t)s * cols + col];
+  if (col < cols)
+    for (int s = y; s < splits; s += kSumRows) acc += part[(size_t)s * cols + col];
+  acc_s[y][threadIdx.x] = acc;
+  __syncthreads();
+  if (y != 0 || col >= cols) return;
+  for (int j = 1; j < kSumRows; ++j) acc += acc_s[j][threadIdx.x];
   out[col] = from_f<T>(acc);
 }
 
-unsigned blocks_for(long long n4) { return (unsigned)((n4 + kBlockThreads - 1) / kBlockThreads); }
+int row_ctas(int rows) { return (rows + kRows - 1) / kRows; }
+// threads of a row CTA: one per column group of 4, at most 512, whole warps
+int row_threads(int cols) {
+  int t = ((cols / 4 + 31) / 32) * 32;
+  return t > 512 ? 512 : t;
+}
 
 template <typename T>
 cudaError_t split_heads_t(const float* src, const void* bias, void* d0, void* d1, void* d2, int B,
                           int N, int H, int d, int S, cudaStream_t st) {
-  const long long n4 = (long long)B * N * S * H * d / 4;
-  return launch("block_split_heads", k_split_heads<T>, dim3(blocks_for(n4)), dim3(kBlockThreads), 0,
-                st, src, (const T*)bias, (T*)d0, (T*)d1, (T*)d2, N, H, d, S, n4);
+  const int rows = B * N;
+  return launch("block_split_heads", k_split_heads<T>, dim3(row_ctas(rows)),
+                dim3(row_threads(S * H * d)), 0, st, src, (const T*)bias, (T*)d0, (T*)d1, (T*)d2,
+                N, H, d, S, rows);
 }
 template <typename T>
-cudaError_t merge_heads_t(const void* s0, const void* s1, const void* s2, void* dst, int B, int N,
-                          int H, int d, int S, cudaStream_t st) {
-  const long long n4 = (long long)B * N * S * H * d / 4;
-  return launch("block_merge_heads", k_merge_heads<T>, dim3(blocks_for(n4)), dim3(kBlockThreads), 0,
-                st, (const T*)s0, (const T*)s1, (const T*)s2, (T*)dst, N, H, d, S, n4);
+cudaError_t merge_heads_t(const void* s0, const void* s1, const void* s2, void* dst, float* part,
+                          int B, int N, int H, int d, int S, cudaStream_t st) {
+  const int rows = B * N;
+  return launch("block_merge_heads", k_merge_heads<T>, dim3(row_ctas(rows)),
+                dim3(row_threads(S * H * d)), 0, st, (const T*)s0, (const T*)s1, (const T*)s2,
+                (T*)dst, part, N, H, d, S, rows);
 }
 template <typename T>
-cudaError_t bias_rows_t(const float* src, const void* bias, void* dst, long long rows, int C,
+cudaError_t bias_rows_t(const float* src, const void* bias, void* dst, int rows, int C,
                         cudaStream_t st) {
-  const long long n4 = rows * C / 4;
-  return launch("block_bias_rows", k_bias_rows<T>, dim3(blocks_for(n4)), dim3(kBlockThreads), 0, st,
-                src, (const T*)bias, (T*)dst, C, n4);
+  return launch("block_bias_rows", k_bias_rows<T>, dim3(row_ctas(rows)), dim3(row_threads(C)), 0,
+                st, src, (const T*)bias, (T*)dst, C, rows);
 }
-
-int col_splits(long long rows, int cols) {
-  const long long cb = (cols + kBlockThreads - 1) / kBlockThreads;
-  long long s = (4LL * 152) / cb;
-  if (s < 1) s = 1;
-  if (s > kColSplits) s = kColSplits;
-  if (s > rows) s = rows;
-  return (int)s;
-}
-
 template <typename T>
-cudaError_t colsum_t(const void* G, float* part, void* out, long long rows, int cols,
-                     cudaStream_t st) {
-  const int S = col_splits(rows, cols);
-  const long long per = (rows + S - 1) / S;
-  const unsigned cb = (unsigned)((cols + kBlockThreads - 1) / kBlockThreads);
-  cudaError_t e = launch("block_colsum", k_colsum_part<T>, dim3(cb, S), dim3(kBlockThreads), 0, st,
-                         (const T*)G, part, rows, cols, per);
+cudaError_t colsum_final_t(const float* part, void* out, int rows, int cols, cudaStream_t st) {
+  return launch("block_colsum_final", k_colsum_final<T>, dim3((cols + 31) / 32),
+                dim3(32, kSumRows), 0, st, part, (T*)out, row_ctas(rows), cols);
+}
+template <typename T>
+cudaError_t colsum_t(const void* G, float* part, void* out, int rows, int cols, cudaStream_t st) {
+  cudaError_t e = launch("block_colsum", k_colsum_rows<T>, dim3(row_ctas(rows)),
+                         dim3(row_threads(cols)), 0, st, (const T*)G, part, cols, rows);
   if (e != cudaSuccess) return e;
-  return launch("block_colsum_final", k_colsum_final<T>, dim3(cb), dim3(kBlockThreads), 0, st,
-                (const float*)part, (T*)out, S, cols);
+  return colsum_final_t<T>(part, out, rows, cols, st);
 }
 
 #define DT_CALL(dtype, fn, ...) \
@@ -263,7 +297,7 @@ BlockLayout block_layout(int B, int N, int C, int H, int d, int m, int iters, in
   L.b_dk = o; o = align256(o + (tied ? 0 : head));
   L.b_dv = o; o = align256(o + head);
   L.b_dqkv = o; o = align256(o + rows * S * HD * es);
-  L.b_part = o; o = align256(o + (size_t)kColSplits * wide * 4);
+  L.b_part = o; o = align256(o + (size_t)row_ctas((int)rows) * wide * 4);
   L.b_attn = o; o = align256(o + L.attn_ws);
   L.b_blas = o; o = align256(o + kBlasWs + 256);
   L.b_total = o;
@@ -351,9 +385,9 @@ int lapnys_block_fwd(const void* x, const void* w_qkv, const void* b_qkv, const 
                   L.attn_ctx, wb + L.f_attn, L.attn_ws);
   if (rc != LAPNYS_OK) return rc;
   // Y = concat_h(O_h) W_o + b_o
-  CKB(DT_CALL(dtype, merge_heads_t, O, nullptr, nullptr, ot, B, N, H, d, 1, stream));
+  CKB(DT_CALL(dtype, merge_heads_t, O, nullptr, nullptr, ot, nullptr, B, N, H, d, 1, stream));
   CKG(gemm_rm(bl->h, false, false, rows, C, HD, ot, HD, w_o, C, s32, C, tab, CUDA_R_32F));
-  CKB(DT_CALL(dtype, bias_rows_t, s32, b_o, y, (long long)rows, C, stream));
+  CKB(DT_CALL(dtype, bias_rows_t, s32, b_o, y, rows, C, stream));
   return LAPNYS_OK;
 }
 
@@ -398,17 +432,18 @@ int lapnys_block_bwd(const void* x, const void* w_qkv, const void* w_o, const vo
   CKG(gemm_rm(bl->h, false, true, rows, HD, C, dy, C, w_o, C, s32, HD, tab, CUDA_R_32F));
   CKB(DT_CALL(dtype, split_heads_t, s32, nullptr, dO, nullptr, nullptr, B, N, H, d, 1, stream));
   CKG(gemm_rm(bl->h, true, false, HD, C, rows, ot, HD, dy, C, dw_o, C, tab, tab));
-  if (db_o != nullptr) CKB(DT_CALL(dtype, colsum_t, dy, part, db_o, (long long)rows, C, stream));
+  if (db_o != nullptr) CKB(DT_CALL(dtype, colsum_t, dy, part, db_o, rows, C, stream));
   // the attention
   rc = lapnys_bwd(q, tied ? nullptr : k, v, dO, (const char*)ctx + L.c_attn, dq, dk, dv, B, H, N,
                   d, grid_h, grid_w, m, lambda, eps, iters, tied, stream, dtype, flags,
                   wb + L.b_attn, L.attn_ws);
   if (rc != LAPNYS_OK) return rc;
   // QKV projection: dqkv = [dQ | dK | dV], dW_qkv = X^T dqkv, db_qkv, dX = dqkv W_qkv^T
-  CKB(DT_CALL(dtype, merge_heads_t, dq, tied ? dv : dk, dv, dqkv, B, N, H, d, S, stream));
+  CKB(DT_CALL(dtype, merge_heads_t, dq, tied ? dv : dk, dv, dqkv,
+              db_qkv != nullptr ? part : nullptr, B, N, H, d, S, stream));
   CKG(gemm_rm(bl->h, true, false, C, S * HD, rows, x, C, dqkv, S * HD, dw_qkv, S * HD, tab, tab));
   if (db_qkv != nullptr)
-    CKB(DT_CALL(dtype, colsum_t, dqkv, part, db_qkv, (long long)rows, S * HD, stream));
+    CKB(DT_CALL(dtype, colsum_final_t, part, db_qkv, rows, S * HD, stream));
   CKG(gemm_rm(bl->h, false, true, rows, C, S * HD, dqkv, S * HD, w_qkv, S * HD, dx, C, tab, tab));
   return LAPNYS_OK;
 }

@@ -346,11 +346,11 @@ __global__ void k_stats_final(const float* __restrict__ spart, float* __restrict
   st[2 * m + a] = 1.0f / sqrtf(var + 1e-5f);
 }
 
-// Batch-pooled: CTA (head g, 32 landmarks), 8 rows of 32 lanes; row y merges
-// the (member, split) partials y, y + 8, ... in order, then row 0 merges the 8
-// row results in order (a fixed tree: deterministic), and all rows write the
+// Batch-pooled: CTA (head g, 32 landmarks), 32 rows of 32 lanes; row y merges
+// the (member, split) partials y, y + 32, ... in order, then row 0 merges the
+// 32 row results in order (a fixed tree: deterministic), and all rows write the
 // result to every member.
-constexpr int kGrpRows = 8;
+constexpr int kGrpRows = 32;
 __global__ void __launch_bounds__(32 * kGrpRows)
     k_stats_final_grouped(const float* __restrict__ spart, float* __restrict__ stats, int H, int R,
                           int S, int m, int mp, int N) {

@@ -15,7 +15,7 @@ Sources (page title, then section / equation):
   [SOFT]   "[Paper review] SOFT: Softmax-free Transformer with Linear
            Complexity", Proposed method: S-hat = P^T A^+ P, A_0 = alpha A,
            A_{k+1} = 2 A_k - A_k A A_k, bottleneck tokens by average pooling,
-           kernel used "without further normalisation"; the attention there is
+           the kernel values enter with no normalisation step; the attention there is
            a symmetric, [0, 1]-valued Gaussian kernel exp(Q (-) K).
 
 Every step follows those passages in their order; where they are silent the
@@ -95,7 +95,7 @@ def kernel_matrix(X: np.ndarray, Y: np.ndarray, lam: float, kernel: str = "lapla
 
 
 # --------------------------------------------------------------------------
-# landmarks  [LF-ar 2c.1: landmark keys chosen by average pooling;
+# landmarks  [LF-ar 2c.1: the landmarks are average-pooled keys;
 #             SOFT Proposed method: average pooling preferred]
 # Readings: a grid of mh x mw landmarks, m = mh mw, in row-major order.  A
 # square m takes mh = mw = sqrt(m); any other m the factor pair whose shape is
