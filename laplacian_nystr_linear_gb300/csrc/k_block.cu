@@ -42,13 +42,52 @@ __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) {
 }
 
 // ---- layout kernels ---------------------------------------------------------
-// A CTA takes kRows consecutive token rows; a thread takes column groups of 4
-// (d is a multiple of 16, so a group stays inside one head row), works out the
-// group's (block s, head h, offset j) once and walks the rows.  Rows are
-// contiguous in the [B*N][W] side, head rows in the [B][H][N][d] side: both
-// sides move 16-byte (fp32) or 8-byte (bf16) pieces, consecutive across the
-// threads of a head.
-constexpr int kRows = 64;
+// A CTA takes `rpc` consecutive token rows; a thread takes pieces of
+// consecutive columns (d is a multiple of 16, so a piece stays inside one head
+// row), works out the piece's (block s, head h, offset j) once and walks the
+// rows.  Rows are contiguous in the [B*N][W] side, head rows in the
+// [B][H][N][d] side; consecutive threads of a head take consecutive pieces.
+// Pieces: 4 columns where one side is float32, otherwise 16 bytes of T.
+constexpr int kRowsWide = 64;    // rows per CTA when the CTA also sums its columns
+constexpr int kRowsNarrow = 16;  // otherwise: more CTAs in flight per SM
+
+template <typename T>
+struct Piece {
+  static constexpr int n = 16 / (int)sizeof(T);
+};
+
+__device__ __forceinline__ void ldp(const float* p, float (&v)[4]) {
+  const float4 u = ld4(p);
+  v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+}
+__device__ __forceinline__ void stp(float* p, const float (&v)[4]) {
+  st4(p, make_float4(v[0], v[1], v[2], v[3]));
+}
+__device__ __forceinline__ void ldp(const __nv_bfloat16* p, float (&v)[4]) {
+  const float4 u = ld4(p);
+  v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+}
+__device__ __forceinline__ void stp(__nv_bfloat16* p, const float (&v)[4]) {
+  st4(p, make_float4(v[0], v[1], v[2], v[3]));
+}
+__device__ __forceinline__ void ldp(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 u = __ldg(reinterpret_cast<const uint4*>(p));
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {  // bf16 -> fp32 is exact: the high half of the bits
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+__device__ __forceinline__ void stp(__nv_bfloat16* p, const float (&v)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    w[i] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+}
 
 struct ColMap {
   int s, h, j;
@@ -66,9 +105,9 @@ __device__ __forceinline__ ColMap col_map(int col, int HD, int d) {
 template <typename T>
 __global__ void k_split_heads(const float* __restrict__ src, const T* __restrict__ bias,
                               T* __restrict__ d0, T* __restrict__ d1, T* __restrict__ d2, int N,
-                              int H, int d, int S, int rows) {
+                              int H, int d, int S, int rows, int rpc) {
   const int HD = H * d, W = S * HD;
-  const int r0 = blockIdx.x * kRows, r1 = min(r0 + kRows, rows);
+  const int r0 = blockIdx.x * rpc, r1 = min(r0 + rpc, rows);
   for (int col = threadIdx.x * 4; col < W; col += blockDim.x * 4) {
     const ColMap c = col_map(col, HD, d);
     T* dst = c.s == 0 ? d0 : (c.s == 1 ? d1 : d2);
@@ -87,33 +126,42 @@ __global__ void k_split_heads(const float* __restrict__ src, const T* __restrict
 
 // src_s [B][H][N][d] of T -> dst [rows][S*H*d] of T; with part != null also
 // part[cta][col] = the column sums of the CTA's rows (in row order)
-template <typename T>
+template <typename T, int P>
 __global__ void k_merge_heads(const T* __restrict__ s0, const T* __restrict__ s1,
                               const T* __restrict__ s2, T* __restrict__ dst,
-                              float* __restrict__ part, int N, int H, int d, int S, int rows) {
+                              float* __restrict__ part, int N, int H, int d, int S, int rows,
+                              int rpc) {
   const int HD = H * d, W = S * HD;
-  const int r0 = blockIdx.x * kRows, r1 = min(r0 + kRows, rows);
-  for (int col = threadIdx.x * 4; col < W; col += blockDim.x * 4) {
+  const int r0 = blockIdx.x * rpc, r1 = min(r0 + rpc, rows);
+  for (int col = threadIdx.x * P; col < W; col += blockDim.x * P) {
     const ColMap c = col_map(col, HD, d);
     const T* src = c.s == 0 ? s0 : (c.s == 1 ? s1 : s2);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float acc[P];
+#pragma unroll
+    for (int i = 0; i < P; ++i) acc[i] = 0.f;
     int b = r0 / N, n = r0 - b * N;
 #pragma unroll 4
     for (int r = r0; r < r1; ++r) {
-      const float4 v = ld4(src + (((size_t)b * H + c.h) * N + n) * d + c.j);
-      st4(dst + (size_t)r * W + col, v);  // v holds T values: stored exactly
-      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      float v[P];
+      ldp(src + (((size_t)b * H + c.h) * N + n) * d + c.j, v);
+      stp(dst + (size_t)r * W + col, v);  // v holds T values: stored exactly
+#pragma unroll
+      for (int i = 0; i < P; ++i) acc[i] += v[i];
       if (++n == N) { n = 0; ++b; }
     }
-    if (part != nullptr) st4(part + (size_t)blockIdx.x * W + col, acc);
+    if (part != nullptr)
+#pragma unroll
+      for (int i = 0; i < P; i += 4)
+        st4(part + (size_t)blockIdx.x * W + col + i,
+            make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]));
   }
 }
 
 // dst [rows][C] of T = src [rows][C] float32 + bias [C] (bias may be null)
 template <typename T>
 __global__ void k_bias_rows(const float* __restrict__ src, const T* __restrict__ bias,
-                            T* __restrict__ dst, int C, int rows) {
-  const int r0 = blockIdx.x * kRows, r1 = min(r0 + kRows, rows);
+                            T* __restrict__ dst, int C, int rows, int rpc) {
+  const int r0 = blockIdx.x * rpc, r1 = min(r0 + rpc, rows);
   for (int col = threadIdx.x * 4; col < C; col += blockDim.x * 4) {
     float4 bv = make_float4(0.f, 0.f, 0.f, 0.f);
     if (bias != nullptr) bv = ld4(bias + col);
@@ -129,16 +177,24 @@ __global__ void k_bias_rows(const float* __restrict__ src, const T* __restrict__
 // part[cta][col] = sum of G[r][col] over the CTA's rows, in row order
 template <typename T>
 __global__ void k_colsum_rows(const T* __restrict__ G, float* __restrict__ part, int cols,
-                              int rows) {
-  const int r0 = blockIdx.x * kRows, r1 = min(r0 + kRows, rows);
-  for (int col = threadIdx.x * 4; col < cols; col += blockDim.x * 4) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                              int rows, int rpc) {
+  constexpr int P = 4;
+  const int r0 = blockIdx.x * rpc, r1 = min(r0 + rpc, rows);
+  for (int col = threadIdx.x * P; col < cols; col += blockDim.x * P) {
+    float acc[P];
+#pragma unroll
+    for (int i = 0; i < P; ++i) acc[i] = 0.f;
 #pragma unroll 4
     for (int r = r0; r < r1; ++r) {
-      const float4 v = ld4(G + (size_t)r * cols + col);
-      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      float v[P];
+      ldp(G + (size_t)r * cols + col, v);
+#pragma unroll
+      for (int i = 0; i < P; ++i) acc[i] += v[i];
     }
-    st4(part + (size_t)blockIdx.x * cols + col, acc);
+#pragma unroll
+    for (int i = 0; i < P; i += 4)
+      st4(part + (size_t)blockIdx.x * cols + col + i,
+          make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]));
   }
 }
 
@@ -161,10 +217,10 @@ __global__ void __launch_bounds__(32 * kSumRows)
   out[col] = from_f<T>(acc);
 }
 
-int row_ctas(int rows) { return (rows + kRows - 1) / kRows; }
-// threads of a row CTA: one per column group of 4, at most 512, whole warps
-int row_threads(int cols) {
-  int t = ((cols / 4 + 31) / 32) * 32;
+int row_ctas(int rows, int rpc) { return (rows + rpc - 1) / rpc; }
+// threads of a row CTA: one per piece of `piece` columns, at most 512, whole warps
+int row_threads(int cols, int piece) {
+  int t = ((cols / piece + 31) / 32) * 32;
   return t > 512 ? 512 : t;
 }
 
@@ -172,33 +228,45 @@ template <typename T>
 cudaError_t split_heads_t(const float* src, const void* bias, void* d0, void* d1, void* d2, int B,
                           int N, int H, int d, int S, cudaStream_t st) {
   const int rows = B * N;
-  return launch("block_split_heads", k_split_heads<T>, dim3(row_ctas(rows)),
-                dim3(row_threads(S * H * d)), 0, st, src, (const T*)bias, (T*)d0, (T*)d1, (T*)d2,
-                N, H, d, S, rows);
+  // wide rows (at least 1024 columns) keep a CTA busy with 64 rows; narrow ones
+  // take 16 so that more CTAs are in flight (measured on the 8-head layer)
+  const int rpc = S * H * d >= 1024 ? kRowsWide : kRowsNarrow;
+  return launch("block_split_heads", k_split_heads<T>, dim3(row_ctas(rows, rpc)),
+                dim3(row_threads(S * H * d, 4)), 0, st, src, (const T*)bias, (T*)d0, (T*)d1,
+                (T*)d2, N, H, d, S, rows, rpc);
 }
 template <typename T>
 cudaError_t merge_heads_t(const void* s0, const void* s1, const void* s2, void* dst, float* part,
                           int B, int N, int H, int d, int S, cudaStream_t st) {
   const int rows = B * N;
-  return launch("block_merge_heads", k_merge_heads<T>, dim3(row_ctas(rows)),
-                dim3(row_threads(S * H * d)), 0, st, (const T*)s0, (const T*)s1, (const T*)s2,
-                (T*)dst, part, N, H, d, S, rows);
+  // measured on the 128 x 128, 8-head layer: with the column sums, 4-column
+  // pieces and 64-row CTAs; without, 16-byte pieces and 16-row CTAs
+  if (part != nullptr)
+    return launch("block_merge_heads", k_merge_heads<T, 4>, dim3(row_ctas(rows, kRowsWide)),
+                  dim3(row_threads(S * H * d, 4)), 0, st, (const T*)s0, (const T*)s1,
+                  (const T*)s2, (T*)dst, part, N, H, d, S, rows, kRowsWide);
+  return launch("block_merge_heads", k_merge_heads<T, Piece<T>::n>,
+                dim3(row_ctas(rows, kRowsNarrow)), dim3(row_threads(S * H * d, Piece<T>::n)), 0,
+                st, (const T*)s0, (const T*)s1, (const T*)s2, (T*)dst, part, N, H, d, S, rows,
+                kRowsNarrow);
 }
 template <typename T>
 cudaError_t bias_rows_t(const float* src, const void* bias, void* dst, int rows, int C,
                         cudaStream_t st) {
-  return launch("block_bias_rows", k_bias_rows<T>, dim3(row_ctas(rows)), dim3(row_threads(C)), 0,
-                st, src, (const T*)bias, (T*)dst, C, rows);
+  return launch("block_bias_rows", k_bias_rows<T>, dim3(row_ctas(rows, kRowsNarrow)),
+                dim3(row_threads(C, 4)), 0, st, src, (const T*)bias, (T*)dst, C, rows,
+                kRowsNarrow);
 }
 template <typename T>
 cudaError_t colsum_final_t(const float* part, void* out, int rows, int cols, cudaStream_t st) {
   return launch("block_colsum_final", k_colsum_final<T>, dim3((cols + 31) / 32),
-                dim3(32, kSumRows), 0, st, part, (T*)out, row_ctas(rows), cols);
+                dim3(32, kSumRows), 0, st, part, (T*)out, row_ctas(rows, kRowsWide), cols);
 }
 template <typename T>
 cudaError_t colsum_t(const void* G, float* part, void* out, int rows, int cols, cudaStream_t st) {
-  cudaError_t e = launch("block_colsum", k_colsum_rows<T>, dim3(row_ctas(rows)),
-                         dim3(row_threads(cols)), 0, st, (const T*)G, part, cols, rows);
+  cudaError_t e = launch("block_colsum", k_colsum_rows<T>, dim3(row_ctas(rows, kRowsWide)),
+                         dim3(row_threads(cols, 4)), 0, st, (const T*)G, part, cols, rows,
+                         kRowsWide);
   if (e != cudaSuccess) return e;
   return colsum_final_t<T>(part, out, rows, cols, st);
 }
@@ -297,7 +365,7 @@ BlockLayout block_layout(int B, int N, int C, int H, int d, int m, int iters, in
   L.b_dk = o; o = align256(o + (tied ? 0 : head));
   L.b_dv = o; o = align256(o + head);
   L.b_dqkv = o; o = align256(o + rows * S * HD * es);
-  L.b_part = o; o = align256(o + (size_t)row_ctas((int)rows) * wide * 4);
+  L.b_part = o; o = align256(o + (size_t)row_ctas((int)rows, kRowsWide) * wide * 4);
   L.b_attn = o; o = align256(o + L.attn_ws);
   L.b_blas = o; o = align256(o + kBlasWs + 256);
   L.b_total = o;
