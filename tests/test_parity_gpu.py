@@ -334,6 +334,27 @@ def test_landmark_grid_gaussian():
 
 
 # ---------------------------------------------------------------------------
+# the limits of the build: m = 1024 (the largest; per-product solver for m > 256),
+# iters = 64 (the largest), m > 256 with adaptive windows and a ragged landmark
+# tile on the tensor-core forward
+# ---------------------------------------------------------------------------
+LIMITS = [
+    _small("m1024", grid_h=64, grid_w=64, m=1024, d=16, iters=4),
+    _small("iters64_tied_norm", m=16, d=32, iters=64, tied=True, norm=True),
+    _small("m324_bf16_adaptive", dtype="bf16", grid_h=24, grid_w=24, m=324, d=64, iters=8),
+]
+
+
+@pytest.mark.parametrize("w", LIMITS, ids=lambda w: w.name)
+def test_limits(w):
+    inp = random_inputs(5, w.B, w.H, w.N, w.d, w.dtype, tied=w.tied)
+    g = gpu_run(w, inp, backward=True)
+    o = oracle_run(w, inp, backward=True)
+    print(w.name, compare(w, g, o, backward=True))
+    np.testing.assert_array_equal(g["ctx"]["idx"], orc.pool_index(w.grid_h, w.grid_w, w.m))
+
+
+# ---------------------------------------------------------------------------
 # batch-pooled feature-map statistics (LAPNYS_NORM_BATCH): mean and variance of
 # each landmark column over the B * N queries of a head's B slices
 # ---------------------------------------------------------------------------
