@@ -36,6 +36,8 @@ namespace {
 constexpr int TJ = 32;                              // tokens per block
 constexpr int kCols = 8;                            // feature columns per prep CTA
 constexpr int kMapWords = 256;                      // 8192-bit map per column
+constexpr int kMapStride = kMapWords + 1;           // shared-memory column stride: odd, so the
+                                                    // columns' words fall in different banks
 constexpr float kLo = 9.094947017729282e-13f;        // 2^-40
 constexpr float kHi = 1.152921504606846976e18f;      // 2^60
 constexpr int kMaxBlocks = 64;                       // blocks per k_ties CTA
@@ -135,8 +137,10 @@ __global__ void __launch_bounds__(kThreads) k_tie_prep(const float* __restrict__
     map[((size_t)bh * D + c0) * kMapWords + e] = mp[e];
 }
 
+// shared memory (the bitmap, 64 KB at d = 64) allows about three CTAs per SM:
+// give the scan the registers that occupancy leaves
 template <int D, typename T>
-__global__ void __launch_bounds__(kThreads) k_ties(const T* __restrict__ X,
+__global__ void __launch_bounds__(kThreads, 3) k_ties(const T* __restrict__ X,
                                                    const float* __restrict__ sorted,
                                                    const int* __restrict__ sidx,
                                                    const uint32_t* __restrict__ map,
@@ -144,7 +148,7 @@ __global__ void __launch_bounds__(kThreads) k_ties(const T* __restrict__ X,
                                                    uint32_t* __restrict__ rec, int N, int P,
                                                    int nblk, int S) {
   extern __shared__ float4 sm4[];
-  uint32_t* mp = reinterpret_cast<uint32_t*>(sm4);  // [D][kMapWords]
+  uint32_t* mp = reinterpret_cast<uint32_t*>(sm4);  // [D][kMapStride]
   __shared__ unsigned oor[kMaxBlocks / 32];         // block holds an out-of-range value
   __shared__ unsigned cnt[kMaxBlocks];              // ties found per block
   __shared__ uint32_t lst[kMaxBlocks][kCap];        // the first kCap triples per block
@@ -161,49 +165,68 @@ __global__ void __launch_bounds__(kThreads) k_ties(const T* __restrict__ X,
   for (int e = tid; e < kMaxBlocks; e += kThreads) cnt[e] = 0u;
   if (tid < kMaxBlocks / 32) oor[tid] = 0u;
   if (!all)
-    for (int e = tid; e < D * kMapWords / 4; e += kThreads)
-      sm4[e] = __ldg(reinterpret_cast<const float4*>(map + (size_t)bh * D * kMapWords) + e);
+    for (int e = tid; e < D * kMapWords / 4; e += kThreads) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(map + (size_t)bh * D * kMapWords) + e);
+      uint32_t* o = mp + (4 * e / kMapWords) * kMapStride + (4 * e) % kMapWords;  // one column
+      o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+    }
   __syncthreads();
   if (!all) {
     const int c0 = (tid % G) * V;
     const int n_lo = b0 * TJ, n_hi = min(N, b1 * TJ);
-#pragma unroll 2
-    for (int e = tid; e < (n_hi - n_lo) * G; e += kThreads) {
+    const int total = (n_hi - n_lo) * G;
+    // one 16-byte piece (V values of token n, columns c0 ..): flag out-of-range
+    // values, look each value's key up in its column's map, and search the
+    // sorted column on a hit
+    auto scan = [&](int e, uint4 u) {
       const int n = n_lo + e / G, k = n / TJ - b0, j = n % TJ;
-      const uint4 u = __ldg(reinterpret_cast<const uint4*>(Xb + (size_t)n * D + c0));
-      {
-        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-        uint32_t xb[V];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      uint32_t xb[V];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if constexpr (V == 8) {
-            xb[2 * q] = w[q] << 16;
-            xb[2 * q + 1] = w[q] & 0xffff0000u;
-          } else {
-            xb[q] = w[q];
-          }
+      for (int q = 0; q < 4; ++q) {
+        if constexpr (V == 8) {
+          xb[2 * q] = w[q] << 16;
+          xb[2 * q + 1] = w[q] & 0xffff0000u;
+        } else {
+          xb[q] = w[q];
         }
-        bool bad_x = false;
-#pragma unroll
-        for (int q = 0; q < V; ++q) {
-          const float x = __uint_as_float(xb[q]);
-          const uint32_t key = tie_key(xb[q]);
-          bad_x = bad_x || out_of_range(x);
-          if ((mp[(c0 + q) * kMapWords + (key >> 5)] >> (key & 31)) & 1u) {
-            // lower bound of x in the column's sorted candidates, then every equal entry
-            const float* col = Sb + c0 + q;
-            int lo = 0;
-            for (int step = P >> 1; step > 0; step >>= 1)
-              if (__ldg(col + (size_t)(lo + step - 1) * D) < x) lo += step;
-            for (int t = lo; t < P && __ldg(col + (size_t)t * D) == x; ++t) {
-              const uint32_t a = (uint32_t)__ldg(Ib + (size_t)t * D + c0 + q);
-              const unsigned slot = atomicAdd(&cnt[k], 1u);
-              if (slot < (unsigned)kCap) lst[k][slot] = (uint32_t)j | (uint32_t)(c0 + q) << 5 | a << 12;
-            }
-          }
-        }
-        if (bad_x) atomicOr(&oor[k >> 5], 1u << (k & 31));
       }
+      bool bad_x = false;
+#pragma unroll
+      for (int q = 0; q < V; ++q) {
+        const float x = __uint_as_float(xb[q]);
+        const uint32_t key = tie_key(xb[q]);
+        bad_x = bad_x || out_of_range(x);
+        if ((mp[(c0 + q) * kMapStride + (key >> 5)] >> (key & 31)) & 1u) {
+          // lower bound of x in the column's sorted candidates, then every equal entry
+          const float* col = Sb + c0 + q;
+          int lo = 0;
+          for (int step = P >> 1; step > 0; step >>= 1)
+            if (__ldg(col + (size_t)(lo + step - 1) * D) < x) lo += step;
+          for (int t = lo; t < P && __ldg(col + (size_t)t * D) == x; ++t) {
+            const uint32_t a = (uint32_t)__ldg(Ib + (size_t)t * D + c0 + q);
+            const unsigned slot = atomicAdd(&cnt[k], 1u);
+            if (slot < (unsigned)kCap) lst[k][slot] = (uint32_t)j | (uint32_t)(c0 + q) << 5 | a << 12;
+          }
+        }
+      }
+      if (bad_x) atomicOr(&oor[k >> 5], 1u << (k & 31));
+    };
+    // four pieces in flight per thread (the thread's columns stay c0 ..)
+    constexpr int kIn = 4;
+    for (int e0 = tid; e0 < total; e0 += kIn * kThreads) {
+      uint4 u[kIn];
+#pragma unroll
+      for (int i = 0; i < kIn; ++i) {
+        const int e = e0 + i * kThreads;
+        if (e < total) {
+          const int n = n_lo + e / G;
+          u[i] = __ldg(reinterpret_cast<const uint4*>(Xb + (size_t)n * D + c0));
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kIn; ++i)
+        if (e0 + i * kThreads < total) scan(e0 + i * kThreads, u[i]);
     }
   }
   __syncthreads();
@@ -250,7 +273,7 @@ TieScratch tie_scratch(const Prob& p, void* scratch) {
 template <int D, typename T>
 cudaError_t ties_t(const Prob& p, const void* x, const TieScratch& t, uint32_t* rec,
                    cudaStream_t st) {
-  const size_t smem = (size_t)D * kMapWords * 4;
+  const size_t smem = (size_t)D * kMapStride * 4;
   static bool once = (allow_smem(k_ties<D, T>, smem), true);
   (void)once;
   const int nblk = (p.N + TJ - 1) / TJ;
