@@ -365,36 +365,84 @@ cudaError_t run_alpha(const Prob& p, const float* A, float* alpha, float* X0, lo
 //   dL_A[a][c] = -(1/lambda) sum_{b != a} (dA_ab + dA_ba) A_ab sgn(L_ac - L_bc)
 // or, for the Gaussian kernel (dk/dx = -(2/lambda) (x - y) k),
 //   dL_A[a][c] = -(2/lambda) sum_{b != a} (dA_ab + dA_ba) A_ab (L_ac - L_bc)
-// block = (D columns) x (256 / D landmarks); grid (landmark groups, slice)
+// CTA = kGB landmarks of one slice: their weights w_ab = (dA_ab + dA_ba) A_ab
+// (0 at b = a) for every b go to shared memory first (coalesced reads of rows
+// and of the 16-wide column strips of dA), then thread (feature c, landmark
+// group ag) walks b once, reusing each L_bc for its D / 16 landmarks.  Each
+// (a, c) sums over b in ascending order.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) k_gram_bwd(const float* __restrict__ L, const float* __restrict__ A,
-                                                       const float* __restrict__ dA, float* __restrict__ dLA,
-                                                       int m, int d, float inv_lam, int gauss) {
-  const int lpb = kThreads / d;
-  const int c = threadIdx.x % d;
-  const int a = blockIdx.x * lpb + threadIdx.x / d;
-  const int bh = blockIdx.y;
-  if (a >= m) return;
-  const float* Lb = L + (size_t)bh * m * d;
+constexpr int kGB = 16;  // landmarks per CTA
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) k_gram_bwd(const float* __restrict__ L,
+                                                       const float* __restrict__ A,
+                                                       const float* __restrict__ dA,
+                                                       float* __restrict__ dLA, int m,
+                                                       float inv_lam, int gauss) {
+  constexpr int LPT = D / 16;           // landmarks per thread: kGB / (kThreads / D)
+  constexpr int NG = kThreads / D;      // landmark groups
+  extern __shared__ float4 sm4[];
+  float* w = reinterpret_cast<float*>(sm4);  // [kGB][m]
+  const int a0 = blockIdx.x * kGB, bh = blockIdx.y;
+  const float* Lb = L + (size_t)bh * m * D;
   const float* Ab = A + (size_t)bh * m * m;
   const float* dAb = dA + (size_t)bh * m * m;
-  const float la = Lb[(size_t)a * d + c];
-  float s = 0.f;
-  for (int b = 0; b < m; ++b) {
-    if (b == a) continue;
-    const float w = (dAb[(size_t)a * m + b] + dAb[(size_t)b * m + a]) * Ab[(size_t)a * m + b];
-    const float t = la - Lb[(size_t)b * d + c];
-    s += gauss ? 2.f * t * w : sgn_times(t, w);
+  for (int e = threadIdx.x; e < kGB * m; e += kThreads) {  // rows a: dA_ab
+    const int i = e / m, b = e - i * m, a = a0 + i;
+    w[e] = a < m ? dAb[(size_t)a * m + b] : 0.f;
   }
-  dLA[((size_t)bh * m + a) * d + c] = -inv_lam * s;
+  __syncthreads();
+  for (int e = threadIdx.x; e < kGB * m; e += kThreads) {  // columns a: + dA_ba, then * A_ab
+    const int b = e / kGB, i = e - b * kGB, a = a0 + i;
+    if (a < m) {
+      const float v = (w[i * m + b] + dAb[(size_t)b * m + a]) * Ab[(size_t)a * m + b];
+      w[i * m + b] = b == a ? 0.f : v;
+    }
+  }
+  __syncthreads();
+  const int c = threadIdx.x % D, ag = threadIdx.x / D;
+  float la[LPT], acc[LPT];
+#pragma unroll
+  for (int k = 0; k < LPT; ++k) {
+    const int a = a0 + ag + NG * k;
+    la[k] = a < m ? Lb[(size_t)a * D + c] : 0.f;
+    acc[k] = 0.f;
+  }
+#pragma unroll 4
+  for (int b = 0; b < m; ++b) {
+    const float lb = __ldg(Lb + (size_t)b * D + c);
+#pragma unroll
+    for (int k = 0; k < LPT; ++k) {
+      const float wv = w[(ag + NG * k) * m + b];
+      const float t = la[k] - lb;
+      acc[k] += gauss ? 2.f * t * wv : sgn_times(t, wv);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < LPT; ++k) {
+    const int a = a0 + ag + NG * k;
+    if (a < m) dLA[((size_t)bh * m + a) * D + c] = -inv_lam * acc[k];
+  }
+}
+
+template <int D>
+static cudaError_t gram_bwd_t(const Prob& p, const float* L, const float* A, const float* dA,
+                              float* dLA, cudaStream_t st) {
+  const size_t smem = (size_t)kGB * p.m * sizeof(float);
+  static bool once = (allow_smem(k_gram_bwd<D>, (size_t)kGB * 1024 * sizeof(float)), true);
+  (void)once;
+  return launch("gram_bwd", k_gram_bwd<D>, dim3((p.m + kGB - 1) / kGB, p.BH), dim3(kThreads), smem,
+                st, L, A, dA, dLA, p.m, p.inv_lam, p.gauss() ? 1 : 0);
 }
 
 cudaError_t run_gram_bwd(const Prob& p, const float* L, const float* A, const float* dA, float* dLA,
                          cudaStream_t st) {
-  const int lpb = kThreads / p.d;
-  dim3 grid((p.m + lpb - 1) / lpb, p.BH);
-  return launch("gram_bwd", k_gram_bwd, grid, dim3(kThreads), 0, st, L, A, dA, dLA, p.m, p.d,
-                p.inv_lam, p.gauss() ? 1 : 0);
+  switch (p.d) {
+    case 16: return gram_bwd_t<16>(p, L, A, dA, dLA, st);
+    case 32: return gram_bwd_t<32>(p, L, A, dA, dLA, st);
+    case 64: return gram_bwd_t<64>(p, L, A, dA, dLA, st);
+    default: return gram_bwd_t<128>(p, L, A, dA, dLA, st);
+  }
 }
 
 // ---------------------------------------------------------------------------
