@@ -318,28 +318,60 @@ cudaError_t run_gram(const Prob& p, const float* L, float* A, cudaStream_t st) {
 // ---------------------------------------------------------------------------
 // alpha for any m (m <= 1024): one CTA per slice; also X_0 = alpha A
 // ---------------------------------------------------------------------------
+// (value, index) pairs: the larger value wins, the lower index on equal values
+__device__ __forceinline__ void argmax_pair(float& v, int& i, float v2, int i2) {
+  if (v2 > v || (v2 == v && i2 < i)) {
+    v = v2;
+    i = i2;
+  }
+}
+
+// column sums by a thread per column (rows in order), row sums by a warp per
+// row (lanes over the row, a fixed shuffle tree), the two argmaxes by a
+// parallel reduction that keeps the lowest index among equal sums
 __global__ void __launch_bounds__(kThreads) k_alpha(const float* __restrict__ A, float* __restrict__ info,
                                                     float* __restrict__ X0, long x_bstride, int m) {
   __shared__ float csum[1024], rsum[1024];
+  __shared__ float bv[2][kThreads / 32];
+  __shared__ int bi[2][kThreads / 32];
   __shared__ float al_s;
-  const int bh = blockIdx.x;
+  const int bh = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const float* Ab = A + (size_t)bh * m * m;
   for (int j = threadIdx.x; j < m; j += kThreads) {
-    float cs = 0.f, rs = 0.f;
-    for (int i = 0; i < m; ++i) {
-      cs += Ab[(size_t)i * m + j];
-      rs += Ab[(size_t)j * m + i];
-    }
+    float cs = 0.f;
+    for (int i = 0; i < m; ++i) cs += Ab[(size_t)i * m + j];
     csum[j] = cs;
-    rsum[j] = rs;
+  }
+  for (int r = warp; r < m; r += kThreads / 32) {
+    float rs = 0.f;
+    for (int i = lane; i < m; i += 32) rs += Ab[(size_t)r * m + i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) rs += __shfl_xor_sync(0xffffffffu, rs, o);
+    if (lane == 0) rsum[r] = rs;
+  }
+  __syncthreads();
+  float cv = -1.f, rv = -1.f;  // sums of positive entries: any real sum beats -1
+  int ci = 0, ri = 0;
+  for (int j = threadIdx.x; j < m; j += kThreads) {
+    argmax_pair(cv, ci, csum[j], j);
+    argmax_pair(rv, ri, rsum[j], j);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    argmax_pair(cv, ci, __shfl_xor_sync(0xffffffffu, cv, o), __shfl_xor_sync(0xffffffffu, ci, o));
+    argmax_pair(rv, ri, __shfl_xor_sync(0xffffffffu, rv, o), __shfl_xor_sync(0xffffffffu, ri, o));
+  }
+  if (lane == 0) {
+    bv[0][warp] = cv; bi[0][warp] = ci;
+    bv[1][warp] = rv; bi[1][warp] = ri;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    int jc = 0, ir = 0;
-    for (int i = 1; i < m; ++i) {
-      if (csum[i] > csum[jc]) jc = i;
-      if (rsum[i] > rsum[ir]) ir = i;
+    for (int w = 1; w < kThreads / 32; ++w) {
+      argmax_pair(cv, ci, bv[0][w], bi[0][w]);
+      argmax_pair(rv, ri, bv[1][w], bi[1][w]);
     }
+    const int jc = ci, ir = ri;
     const float n1 = csum[jc], ninf = rsum[ir];
     const float al = 1.0f / (n1 * ninf);
     al_s = al;
