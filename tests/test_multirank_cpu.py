@@ -8,6 +8,7 @@ import socket
 import subprocess
 import sys
 
+import pytest
 import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
@@ -62,3 +63,18 @@ def test_reference_arm_prints_once_under_torchrun():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+@pytest.mark.parametrize("extra", [["--block"], ["--kernel", "gauss"]])
+def test_reference_arm_variants(extra):
+    # the oracle's variants behind --block and --kernel gauss, one process
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+           "tiny", "--steps", "2", "--warmup", "1"] + extra
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "tokens/s"
+    assert d["config"]["block"] == ("--block" in extra)
+    assert d["config"]["kernel"] == ("gauss" if "gauss" in extra else "laplace")
