@@ -13,7 +13,9 @@
 namespace lapnys {
 
 // ---------------------------------------------------------------------------
-// pooling: one CTA per (landmark, slice); threads = (token group, 4-wide chunk).
+// pooling: one CTA per (row of landmark windows, slice); thread = (landmark
+// column wj = g, g + groups, ..; 4-wide feature chunk) sums its window's tokens
+// in row-major order and writes the mean (no cross-thread reduction).
 // Landmark a = wi * mw + wj averages token rows [wi gh / mh, (wi + 1) gh / mh)
 // and columns [wj gw / mw, (wj + 1) gw / mw) (floors): equal windows when the
 // grid divides, otherwise windows of the floor and ceil sizes.
@@ -22,40 +24,33 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads) k_pool(const T* __restrict__ K, float* __restrict__ L,
                                                    int32_t* __restrict__ idx, int N, int d, int gh,
                                                    int gw, int mh, int mw, int m) {
-  __shared__ float4 red[kThreads];
-  const int a = blockIdx.x, bh = blockIdx.y;
-  const int wi = a / mw, wj = a % mw;
-  const int y0 = wi * gh / mh, y1 = (wi + 1) * gh / mh;
-  const int x0 = wj * gw / mw, x1 = (wj + 1) * gw / mw;
-  const int sw = x1 - x0;
+  const int wi = blockIdx.x, bh = blockIdx.y;
   const int C4 = d / 4, groups = kThreads / C4;
   const int chunk = threadIdx.x % C4, g = threadIdx.x / C4;
-  const int wsz = (y1 - y0) * sw;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  const T* Kb = K + (size_t)bh * N * d;
-  for (int t = g; t < wsz; t += groups) {
-    const int n = (y0 + t / sw) * gw + x0 + t % sw;
-    const float4 v = ld4(Kb + (size_t)n * d + chunk * 4);
-    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-  }
-  red[threadIdx.x] = acc;
-  __syncthreads();
-  if (threadIdx.x < C4) {
-    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int q = 0; q < groups; ++q) {
-      const float4 v = red[q * C4 + threadIdx.x];
-      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+  const int y0 = wi * gh / mh, y1 = (wi + 1) * gh / mh;
+  const T* Kb = K + (size_t)bh * N * d + chunk * 4;
+  for (int wj = g; wj < mw; wj += groups) {
+    const int x0 = wj * gw / mw, x1 = (wj + 1) * gw / mw;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int y = y0; y < y1; ++y) {
+#pragma unroll 4
+      for (int x = x0; x < x1; ++x) {
+        const float4 v = ld4(Kb + ((size_t)y * gw + x) * d);
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      }
     }
-    const float inv = 1.0f / (float)wsz;
-    st4(L + ((size_t)bh * m + a) * d + threadIdx.x * 4,
-        make_float4(s.x * inv, s.y * inv, s.z * inv, s.w * inv));
+    const int a = wi * mw + wj;
+    const float inv = 1.0f / (float)((y1 - y0) * (x1 - x0));
+    st4(L + ((size_t)bh * m + a) * d + chunk * 4,
+        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+    if (idx != nullptr && bh == 0 && chunk == 0)
+      for (int y = y0; y < y1; ++y)
+        for (int x = x0; x < x1; ++x) idx[y * gw + x] = a;
   }
-  if (idx != nullptr && bh == 0)
-    for (int t = threadIdx.x; t < wsz; t += kThreads) idx[(y0 + t / sw) * gw + x0 + t % sw] = a;
 }
 
 cudaError_t run_pool(const Prob& p, const void* k, float* L, int32_t* idx, cudaStream_t st) {
-  dim3 grid(p.m, p.BH);
+  dim3 grid(p.mh, p.BH);
   if (p.dtype == 1)
     return launch("pool", k_pool<__nv_bfloat16>, grid, dim3(kThreads), 0, st,
                   (const __nv_bfloat16*)k, L, idx, p.N, p.d, p.gh, p.gw, p.mh, p.mw, p.m);

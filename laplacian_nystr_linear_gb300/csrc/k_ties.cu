@@ -81,17 +81,18 @@ __global__ void __launch_bounds__(kThreads) k_tie_prep(const float* __restrict__
                                                        uint32_t* __restrict__ map,
                                                        int* __restrict__ bad, int m, int P, int D) {
   extern __shared__ float4 sm4[];
-  float* a = reinterpret_cast<float*>(sm4);                        // [kCols][P] values
-  int* ix = reinterpret_cast<int*>(a + kCols * P);                 // [kCols][P] landmark index
-  uint32_t* mp = reinterpret_cast<uint32_t*>(ix + kCols * P);      // [kCols][kMapWords]
+  const int CP = P + 1;  // column stride: odd, so a row's kCols values fall in different banks
+  float* a = reinterpret_cast<float*>(sm4);                        // [kCols][CP] values
+  int* ix = reinterpret_cast<int*>(a + kCols * CP);                // [kCols][CP] landmark index
+  uint32_t* mp = reinterpret_cast<uint32_t*>(ix + kCols * CP);     // [kCols][kMapWords]
   const int bh = blockIdx.x, cg = blockIdx.y, c0 = cg * kCols, tid = threadIdx.x;
   const float* Lb = L + (size_t)bh * m * D;
   const float inf = __int_as_float(0x7f800000);
   for (int e = tid; e < kCols * kMapWords; e += kThreads) mp[e] = 0u;
   __syncthreads();
   bool b = false;
-  for (int e = tid; e < kCols * P; e += kThreads) {
-    const int cc = e / P, i = e % P;
+  for (int e = tid; e < kCols * P; e += kThreads) {  // row-major: kCols consecutive values
+    const int i = e / kCols, cc = e % kCols;
     float v = inf;
     if (i < m) {
       const float l = __ldg(Lb + (size_t)i * D + c0 + cc);
@@ -102,8 +103,8 @@ __global__ void __launch_bounds__(kThreads) k_tie_prep(const float* __restrict__
         atomicOr(&mp[cc * kMapWords + (k >> 5)], 1u << (k & 31));
       }
     }
-    a[e] = v;
-    ix[e] = i;
+    a[cc * CP + i] = v;
+    ix[cc * CP + i] = i;
   }
   const int any = __syncthreads_or(b);
   if (tid == 0) bad[bh * (D / kCols) + cg] = any ? 1 : 0;
@@ -113,8 +114,8 @@ __global__ void __launch_bounds__(kThreads) k_tie_prep(const float* __restrict__
       for (int e = tid; e < kCols * (P / 2); e += kThreads) {
         const int cc = e / (P / 2), t = e % (P / 2);
         const int i = 2 * t - (t & (j - 1));  // lower index of the pair
-        float* col = a + cc * P;
-        int* ci = ix + cc * P;
+        float* col = a + cc * CP;
+        int* ci = ix + cc * CP;
         const bool up = (i & k) == 0;
         const float x = col[i], y = col[i + j];
         if ((x > y) == up) {
@@ -130,8 +131,8 @@ __global__ void __launch_bounds__(kThreads) k_tie_prep(const float* __restrict__
   }
   for (int e = tid; e < kCols * P; e += kThreads) {
     const int i = e / kCols, cc = e % kCols;
-    sorted[((size_t)bh * P + i) * D + c0 + cc] = a[cc * P + i];
-    sidx[((size_t)bh * P + i) * D + c0 + cc] = ix[cc * P + i];
+    sorted[((size_t)bh * P + i) * D + c0 + cc] = a[cc * CP + i];
+    sidx[((size_t)bh * P + i) * D + c0 + cc] = ix[cc * CP + i];
   }
   for (int e = tid; e < kCols * kMapWords; e += kThreads)
     map[((size_t)bh * D + c0) * kMapWords + e] = mp[e];
@@ -290,7 +291,7 @@ cudaError_t ties_t(const Prob& p, const void* x, const TieScratch& t, uint32_t* 
 
 cudaError_t run_tie_prep(const Prob& p, const float* L, void* scratch, cudaStream_t st) {
   const TieScratch t = tie_scratch(p, scratch);
-  const size_t smem = (size_t)kCols * t.P * 8 + (size_t)kCols * kMapWords * 4;
+  const size_t smem = (size_t)kCols * (t.P + 1) * 8 + (size_t)kCols * kMapWords * 4;
   if (p.dtype == 1) {
     static bool once = (allow_smem(k_tie_prep<__nv_bfloat16>, 96 * 1024), true);
     (void)once;
