@@ -14,8 +14,8 @@
 //
 // k_tie_prep (one CTA per slice and group of 8 feature columns):
 //   - flags the slice when a landmark value is out of range;
-//   - marks, per feature column, the candidate values in a 8192-bit map keyed
-//     by 13 bits of the value (sign, 5 low exponent bits, 7 high mantissa
+//   - marks, per feature column, the candidate values in a 2048-bit map keyed
+//     by 11 bits of the value (sign, 5 low exponent bits, 5 high mantissa
 //     bits).  A bf16 token can only equal a landmark value that bf16
 //     represents exactly, so for bf16 tokens only those values are candidates;
 //   - sorts each column's candidate values ascending with their landmark
@@ -35,7 +35,7 @@ namespace lapnys {
 namespace {
 constexpr int TJ = 32;                              // tokens per block
 constexpr int kCols = 8;                            // feature columns per prep CTA
-constexpr int kMapWords = 256;                      // 8192-bit map per column
+constexpr int kMapWords = 64;                       // 2048-bit map per column (11-bit keys)
 constexpr int kMapStride = kMapWords + 1;           // shared-memory column stride: odd, so the
                                                     // columns' words fall in different banks
 constexpr float kLo = 9.094947017729282e-13f;        // 2^-40
@@ -48,10 +48,12 @@ __device__ __forceinline__ bool out_of_range(float v) {
   return !(a <= kHi) || (a != 0.f && a < kLo);
 }
 
-// 13-bit key of a value's bits; both zeros get the key of +0 (they compare equal)
+// 11-bit key of a value's bits (sign, the exponent's low 5 bits, the top 5
+// mantissa bits): equal values have equal keys, both zeros get the key of +0
+// (they compare equal); a key hit is only a candidate, checked exactly
 __device__ __forceinline__ uint32_t tie_key(uint32_t u) {
   u = (u << 1) == 0u ? 0u : u;
-  return ((u >> 19) & 0x1000u) | ((u >> 16) & 0x0fffu);
+  return ((u >> 21) & 0x400u) | ((u >> 18) & 0x3ffu);
 }
 
 template <typename T>
@@ -138,10 +140,10 @@ __global__ void __launch_bounds__(kThreads) k_tie_prep(const float* __restrict__
     map[((size_t)bh * D + c0) * kMapWords + e] = mp[e];
 }
 
-// shared memory (the bitmap, 64 KB at d = 64) allows about three CTAs per SM:
-// give the scan the registers that occupancy leaves
+// four CTAs per SM (the bitmaps take 16 KB at d = 64): the register budget
+// that occupancy leaves goes to the loads in flight
 template <int D, typename T>
-__global__ void __launch_bounds__(kThreads, 3) k_ties(const T* __restrict__ X,
+__global__ void __launch_bounds__(kThreads, 4) k_ties(const T* __restrict__ X,
                                                    const float* __restrict__ sorted,
                                                    const int* __restrict__ sidx,
                                                    const uint32_t* __restrict__ map,
