@@ -658,25 +658,24 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
   const float* XT = X + (long)iters * mm;
   const long xs = (long)(iters + 1) * mm;
   const long ys = (long)c.ny * mm;
-  if (m <= kTile) {
-    CK(run_bgemm(false, true, p.BH, m, m, d, dWh, d, md, W, d, md, G, m, mm, nullptr, m, 0, 1.f,
-                 0.f, stream));
-    CK(run_bgemm(true, false, p.BH, m, d, m, XT, m, xs, dWh, d, md, dW, d, md, nullptr, d, 0, 1.f,
-                 0.f, stream));
-  } else {
-    CK(ns_mm(p, false, true, m, m, d, dWh, d, md, W, d, md, G, m, mm, nullptr, m, 0, 1.f, 0.f,
-             stream));
-    CK(ns_mm(p, true, false, m, d, m, XT, m, xs, dWh, d, md, dW, d, md, nullptr, d, 0, 1.f, 0.f,
-             stream));
-  }
-
-  // ---- the Newton-Schulz reverse and the gram backward, on the side stream
-  // (they need G; the key side below needs only dW) ----
+  // ---- G, the Newton-Schulz reverse and the gram backward on the side stream
+  // (they need G); dW and the key side below on this stream (they need dW) ----
   Side* sd = side();
   std::unique_lock<std::mutex> lock;
   if (sd) lock = std::unique_lock<std::mutex>(sd->mu);
   const cudaStream_t ss = sd ? sd->hi : stream;
   if (sd) CK(join(ss, stream, sd->ev[0]));
+  if (m <= kTile) {
+    CK(run_bgemm(false, true, p.BH, m, m, d, dWh, d, md, W, d, md, G, m, mm, nullptr, m, 0, 1.f,
+                 0.f, ss));
+    CK(run_bgemm(true, false, p.BH, m, d, m, XT, m, xs, dWh, d, md, dW, d, md, nullptr, d, 0, 1.f,
+                 0.f, stream));
+  } else {
+    CK(ns_mm(p, false, true, m, m, d, dWh, d, md, W, d, md, G, m, mm, nullptr, m, 0, 1.f, 0.f,
+             ss));
+    CK(ns_mm(p, true, false, m, d, m, XT, m, xs, dWh, d, md, dW, d, md, nullptr, d, 0, 1.f, 0.f,
+             stream));
+  }
   if (m <= kTile) {
     CK(run_ns_bwd_small(p, A, alpha, X, Y, G, dA, ss));
   } else {
