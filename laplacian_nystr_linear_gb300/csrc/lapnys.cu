@@ -454,12 +454,20 @@ int lapnys_fwd(const void* q, const void* k, const void* v, void* out, int B, in
   const long mm = (long)m * m;
 
   CK(run_pool(p, k, L, idx, stream));
+  // the solver (landmark matrix, alpha, Newton-Schulz) on the side stream,
+  // queued first so that its CTAs take their SMs at once; the key pass on this
+  // stream meanwhile; both end before W-hat = X_T W
+  Side* sd = side();
+  std::unique_lock<std::mutex> lock;
+  if (sd) lock = std::unique_lock<std::mutex>(sd->mu);
+  const cudaStream_t ss = sd ? sd->hi : stream;
+  if (sd) CK(join(ss, stream, sd->ev[0]));
   if (m <= kTile) {
-    CK(run_ns_small(p, L, A, alpha, X, Y, c.nx, c.ny, stream));
+    CK(run_ns_small(p, L, A, alpha, X, Y, c.nx, c.ny, ss));
   } else {
-    CK(run_gram(p, L, A, stream));
-    CK(run_alpha(p, A, alpha, X, c.nx * mm, stream));
-    rc = ns_forward_large(p, A, X, Y, c.nx, c.ny, stream);
+    CK(run_gram(p, L, A, ss));
+    CK(run_alpha(p, A, alpha, X, c.nx * mm, ss));
+    rc = ns_forward_large(p, A, X, Y, c.nx, c.ny, ss);
     if (rc != LAPNYS_OK) return rc;
   }
   float* kpart = (float*)(wb + w.kpart);
@@ -474,6 +482,7 @@ int lapnys_fwd(const void* q, const void* k, const void* v, void* out, int B, in
     CK(run_key_fwd(p, k, v, L, kpart, full ? (float*)(cb + c.C) : nullptr, stream));
     CK(run_reduce_parts(p.BH, p.Sk, m, p.mp, d, kpart, W, stream));
   }
+  if (sd) CK(join(stream, ss, sd->ev[1]));
   const float* XT = X + (long)(iters % c.nx) * mm;
   // W-hat = X_T W
   CK(ns_mm(p, false, false, m, d, m, XT, m, c.nx * mm, W, d, (long)m * d, What, d, (long)m * d,
