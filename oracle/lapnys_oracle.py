@@ -35,7 +35,10 @@ The backward pass is reverse-mode differentiation of exactly these steps.
 
 kernel="gauss" replaces k by the Gaussian kernel of [SOFT], read (the page
 prints no scale) as k(x, y) = exp(-||x - y||_2^2 / lam) with the same lam;
-everything else is unchanged.
+everything else is unchanged.  norm_batch=True takes mu and sigma^2 over the
+B slices of each head instead of per slice (forward() / backward()).
+block_forward() / block_backward() put the multi-head projections around the
+attention: [Q | K | V] = X W_qkv + b_qkv, Y = concat_h(O_h) W_o + b_o.
 """
 from __future__ import annotations
 
