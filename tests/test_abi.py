@@ -180,3 +180,45 @@ def test_block_bwd_rejects_bad_arguments(lib):
     assert bwd(dwo=None) == LAPNYS_EINVAL
     assert bwd(db=ctypes.c_void_p((1 << 20) + 4)) == LAPNYS_EINVAL
     assert bwd() == LAPNYS_ENOSPC
+
+
+def test_matmul_rejects_bad_arguments(lib):
+    from laplacian_nystr_linear_gb300._lib import LAPNYS_EINVAL, LAPNYS_ENOTSUP
+
+    def mm(**kw):
+        a = dict(A=FAKE, B=FAKE, E=None, C=FAKE, batch=1, M=64, N=64, K=64, lda=64, ldb=64, lde=0,
+                 ldc=64, beta=0.0, engine=0)
+        a.update(kw)
+        return lib.lapnys_matmul(a["A"], a["B"], a["E"], a["C"], a["batch"], a["M"], a["N"], a["K"],
+                                 0, 0, a["lda"], a["ldb"], a["lde"], a["ldc"], 0, 0, 0, 0, 1.0,
+                                 a["beta"], a["engine"], None)
+
+    assert mm(A=None) == LAPNYS_EINVAL
+    assert mm(batch=0) == LAPNYS_EINVAL
+    assert mm(K=0) == LAPNYS_EINVAL
+    assert mm(beta=1.0) == LAPNYS_EINVAL            # beta != 0 needs E
+    assert mm(lda=0) == LAPNYS_EINVAL
+    assert mm(engine=2) == LAPNYS_EINVAL            # no such engine
+    assert mm(engine=1, M=62, lda=62) == LAPNYS_ENOTSUP   # tensor cores want multiples of 4
+
+
+def test_static_forward_and_pool_reject_bad_arguments(lib):
+    from laplacian_nystr_linear_gb300._lib import LAPNYS_EINVAL, LAPNYS_ESCRATCH
+
+    def fs(**kw):
+        a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, B=1, H=1, N=196, d=32, gh=14, gw=14, m=49,
+                 tied=0, flags=0)
+        a.update(kw)
+        return lib.lapnys_fwd_static(a["q"], a["k"], a["v"], a["out"], a["B"], a["H"], a["N"],
+                                     a["d"], a["gh"], a["gw"], a["m"], 32.0, 1e-3, 20, a["tied"],
+                                     None, 0, a["flags"])
+
+    assert fs(N=195) == LAPNYS_EINVAL
+    assert fs(q=None) == LAPNYS_EINVAL
+    assert fs(tied=1, k=ctypes.c_void_p(2 << 20)) == LAPNYS_EINVAL
+    assert fs(out=ctypes.c_void_p((1 << 20) + 4)) == LAPNYS_EINVAL
+    # the 16K-token workload needs far more forward scratch than the built-in 32 MiB
+    assert fs(B=8, H=8, N=16384, d=64, gh=128, gw=128, m=256) == LAPNYS_ESCRATCH
+    assert lib.lapnys_pool(FAKE, FAKE, None, 1, 1, 195, 32, 14, 14, 49, 0, None) == LAPNYS_EINVAL
+    assert lib.lapnys_pool(None, FAKE, None, 1, 1, 196, 32, 14, 14, 49, 0, None) == LAPNYS_EINVAL
+    assert lib.lapnys_pool(FAKE, FAKE, None, 1, 1, 196, 32, 14, 14, 225, 0, None) == LAPNYS_EINVAL
