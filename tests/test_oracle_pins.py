@@ -512,12 +512,15 @@ def test_block_bias_is_a_constant_input_feature():
     np.testing.assert_allclose(g1[0][..., :-1], g0[0], rtol=1e-10, atol=1e-12)
 
 
-@pytest.mark.parametrize("tied,norm_batch", [(False, False), (True, False), (False, True)])
-def test_block_backward_matches_finite_differences(tied, norm_batch):
+@pytest.mark.parametrize("tied,norm,norm_batch,kernel", [(False, True, False, "laplace"),
+                                                         (True, True, False, "laplace"),
+                                                         (False, True, True, "laplace"),
+                                                         (False, False, False, "gauss")])
+def test_block_backward_matches_finite_differences(tied, norm, norm_batch, kernel):
     H, d = 2, 4
     x, w, b, wo, bo = _block_args(54 + tied + 2 * norm_batch, tied=tied)
     R = np.random.default_rng(57).standard_normal(x.shape)
-    kw = dict(tied=tied, norm=True, norm_batch=norm_batch)
+    kw = dict(tied=tied, norm=norm, norm_batch=norm_batch, kernel=kernel)
     args = dict(x=x, w=w, b=b, wo=wo, bo=bo)
 
     def loss(a):
