@@ -35,9 +35,15 @@
  *    partition the grid (EINVAL when mh > grid_h or mw > grid_w).
  *  - The caller owns and allocates everything: out, gradients, `ctx` (state
  *    saved by the forward for the backward) and `ws` (scratch).  The library
- *    allocates no device memory, does not synchronise, and enqueues all work
- *    on `stream` (0 = legacy default stream).  Sizes come from
- *    lapnys_ctx_bytes / lapnys_workspace_bytes.
+ *    allocates no device memory and does not synchronise.  Work is ordered on
+ *    `stream` (0 = legacy default stream): lapnys_fwd and lapnys_bwd run part
+ *    of it (the landmark solver and its reverse) on one high-priority stream
+ *    per device that the library creates on its first call there; that part
+ *    starts after the work already on `stream` and `stream` waits for it
+ *    before the call's last kernel (CUDA events), so to the caller the call
+ *    behaves as if all of it were on `stream`.  Calls from several host
+ *    threads on one device take turns on that stream (a mutex).  Sizes come
+ *    from lapnys_ctx_bytes / lapnys_workspace_bytes.
  *  - Return value: LAPNYS_OK, or an error code.  Argument errors (EINVAL,
  *    ENOSPC, ENOTSUP) are detected on the host before anything is enqueued, so
  *    nothing has been written.  ECUDA reports a failed launch (the CUDA error
