@@ -98,6 +98,25 @@ def _normal(seed: int, shape) -> np.ndarray:
     return np.random.default_rng(seed).standard_normal(shape, dtype=np.float32)
 
 
+def _outlier_draws(w: Workload):
+    """(mask [B, H, N], heavy-tailed rows) for Q, then K unless tied, in draw order."""
+    shape = (w.B, w.H, w.N, w.d)
+    rng = np.random.default_rng(5000 + w.cfg)
+    for _ in range(1 if w.tied else 2):
+        mask = rng.random(shape[:-1]) < 0.01
+        yield mask, _student_t3(rng, (int(mask.sum()), w.d))
+
+
+def outlier_counts(w: Workload) -> np.ndarray:
+    """Heavy-tailed tokens per (b, h) slice, Q and K together ([B, H] int; zeros
+    when the workload has none)."""
+    n = np.zeros((w.B, w.H), np.int64)
+    if w.outliers:
+        for mask, _ in _outlier_draws(w):
+            n += mask.sum(axis=-1)
+    return n
+
+
 def make_inputs(w: Workload, with_grad: bool | None = None) -> dict:
     """Return {"q","k","v"[,"dout"]} as float32 arrays of shape [B, H, N, d].
 
@@ -109,10 +128,7 @@ def make_inputs(w: Workload, with_grad: bool | None = None) -> dict:
     k = q if w.tied else _normal(2000 + c, shape)
     v = _normal(3000 + c, shape)
     if w.outliers:
-        rng = np.random.default_rng(5000 + c)
-        for t in ((q,) if w.tied else (q, k)):
-            mask = rng.random(shape[:-1]) < 0.01
-            heavy = _student_t3(rng, (int(mask.sum()), w.d))
+        for t, (mask, heavy) in zip((q,) if w.tied else (q, k), _outlier_draws(w)):
             t[mask] = heavy
     out = {"q": q, "k": k, "v": v}
     if with_grad if with_grad is not None else w.backward:

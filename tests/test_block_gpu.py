@@ -2,9 +2,10 @@
 through the C ABI against the fp64 oracle's block on seeded inputs (needs a GPU).
 
 Tolerance: relative Frobenius error <= 1e-4 (float32) and <= 2e-2 (bf16) for y
-and for every gradient (dx, dW_qkv, db_qkv, dW_o, db_o); Q, K, V and the
-gradients are rounded once to the element type, as the attention's own
-tolerance already allows.
+and for every gradient (dx, dW_qkv, db_qkv, dW_o, db_o), and per element
+|gpu - oracle| <= R |oracle| + A rms(oracle tensor) with the attention's (R, A)
+(tests/_parity.py); Q, K, V and the gradients are rounded once to the element
+type, as the attention's own tolerance already allows.
 """
 import dataclasses
 
@@ -16,7 +17,7 @@ from laplacian_nystr_linear_gb300 import api
 from laplacian_nystr_linear_gb300.inputs import block_inputs
 from oracle import lapnys_oracle as orc
 
-from tests._parity import TOL, rel, to_dev, to_np
+from tests._parity import EW, TOL, _log, elementwise_excess, rel, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -96,10 +97,16 @@ def test_block_matches_oracle(c):
     g = run_gpu(c, inp)
     o = run_oracle(c, inp)
     errs = {n: rel(g[n], o[n]) for n in o if g.get(n) is not None}
-    print(c.name, errs)
+    r, a = EW[c.dtype]
+    ew = {n: elementwise_excess(g[n], o[n], r)[0] for n in errs}
+    print(c.name, errs, ew)
+    _log({"workload": "block_" + c.name, "dtype": c.dtype, "fro": errs, "ew_excess": ew,
+          "R": r, "A": a})
     assert not c.bias or len(errs) == 6
     bad = {n: e for n, e in errs.items() if not e <= TOL[c.dtype]}
     assert not bad, f"{c.name}: {bad}"
+    bad = {n: e for n, e in ew.items() if not e <= a}
+    assert not bad, f"{c.name}: element-wise excess / rms above {a}: {bad}"
 
 
 def test_block_autograd_wrapper_matches_raw_calls():
@@ -141,8 +148,12 @@ def test_block_hires16k_layer():
     y0, _ = orc.block_forward(inp["x"][:1], inp["w_qkv"], inp["b_qkv"], inp["w_o"], inp["b_o"],
                               c.H, c.d, c.grid_h, c.grid_w, c.m, float(c.d), 1e-3, c.iters)
     e = rel(g["y"][0], y0[0])
-    print("hires16k_layer y[0]", e)
-    assert e <= TOL["bf16"]
+    r, a = EW["bf16"]
+    ex = elementwise_excess(g["y"][0], y0[0], r)[0]
+    print("hires16k_layer y[0]", e, ex)
+    _log({"workload": "block_hires16k_layer", "dtype": "bf16", "fro": {"y": e},
+          "ew_excess": {"y": ex}, "R": r, "A": a})
+    assert e <= TOL["bf16"] and ex <= a
     dy = inp["dy"].astype(np.float64)
     assert rel(g["db_o"], dy.sum(axis=(0, 1))) <= TOL["bf16"]
     assert np.isfinite(g["dx"]).all() and np.isfinite(g["dw_qkv"]).all()

@@ -67,3 +67,34 @@ def test_block_sizes_track_the_shapes(lib):
     assert ws(2) >= lib.lapnys_workspace_bytes(2, 4, 1024, 64, 64, 8, 0)
     # the saved Q, K, V and concatenated heads: four [B][H][N][d] tensors of bf16
     assert ctx(2) - lib.lapnys_ctx_bytes(2, 4, 1024, 64, 64, 8, 0) >= 4 * 2 * 4 * 1024 * 64 * 2
+
+
+def test_outlier_counts_match_the_drawn_tokens():
+    # the counts are those of the heavy-tailed rows make_inputs writes: on a small
+    # copy of the high-resolution workload, the rows that differ from the plain
+    # N(0, 1) draw of the same seed are exactly the counted ones
+    from laplacian_nystr_linear_gb300.inputs import outlier_counts
+    w = WORKLOADS["hires16k"].scaled(B=2, H=3, grid_h=16, grid_w=16)
+    with_out = make_inputs(w)
+    plain = make_inputs(w.scaled(outliers=False))
+    changed = ((with_out["q"] != plain["q"]).any(-1).sum(-1)
+               + (with_out["k"] != plain["k"]).any(-1).sum(-1))
+    np.testing.assert_array_equal(outlier_counts(w), changed)
+    assert outlier_counts(w).sum() > 0
+    assert not outlier_counts(w.scaled(outliers=False)).any()
+
+
+def test_top_outlier_slices_are_the_largest_counts():
+    from laplacian_nystr_linear_gb300.inputs import outlier_counts
+    from tests._parity import top_outlier_slices
+    w = WORKLOADS["hires16k"]
+    c = outlier_counts(w)
+    top = top_outlier_slices(w, 6)
+    assert len(top) == 6
+    assert min(c[b, h] for b, h in top) >= max(c[b, h] for b in range(w.B) for h in range(w.H)
+                                                 if (b, h) not in top)
+
+
+def test_oracle_pool_matches_the_serial_oracle():
+    from tests._oracle_pool import _check_matches_serial
+    _check_matches_serial()

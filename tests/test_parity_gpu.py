@@ -1,10 +1,11 @@
 """CUDA path against the fp64 oracle on seeded inputs (needs a GPU).
 
 Tolerance: per (b, h) slice, |gpu - oracle|_F / |oracle|_F <= 1e-4 for float32
-tensors and <= 2e-2 for bf16 tensors (fp32 accumulation); landmark indices
-bit-exact.  Full-size workloads are checked on sampled slices, computed by the
-oracle one slice at a time, in the same launch configuration the benchmark
-times (the same library call on the whole batch).
+tensors and <= 2e-2 for bf16 tensors (fp32 accumulation), and per element
+|gpu - oracle| <= R |oracle| + A rms(oracle slice) (tests/_parity.py); landmark
+indices bit-exact.  Full-size workloads are checked on sampled slices, computed
+by the oracle one slice at a time, in the same launch configuration the
+benchmark times (the same library call on the whole batch).
 """
 import dataclasses
 
@@ -17,7 +18,9 @@ from laplacian_nystr_linear_gb300.inputs import (WORKLOADS, Workload, make_input
                                                  round_bf16)
 from oracle import lapnys_oracle as orc
 
-from tests._parity import compare, gpu_run, oracle_run, params_of, rel, to_dev
+from tests._oracle_pool import oracle_slices
+from tests._parity import (compare, gpu_run, oracle_run, params_of, rel, to_dev,
+                           top_outlier_slices)
 
 pytestmark = pytest.mark.gpu
 
@@ -127,10 +130,15 @@ def test_norm_statistics():
 # ---------------------------------------------------------------------------
 # forward outputs at the workload shapes
 # ---------------------------------------------------------------------------
+# The full-size workloads: the four slices with the most heavy-tailed tokens
+# plus the first and the last slice (hires16k), and four heads spread over the
+# batch of the tied 65K-token workload; the oracle runs them in parallel.
 FWD_SLICES = {
     "tiny": None, "tiny_mN": None, "pvt1": None, "pvt2": None, "pvt3": None,
-    "hires16k": {(0, 0), (7, 7)}, "tied64k": {(0, 0), (0, 15)},
+    "hires16k": top_outlier_slices(WORKLOADS["hires16k"], 4) | {(0, 0), (7, 7)},
+    "tied64k": {(0, 0), (0, 5), (0, 10), (0, 15)},
 }
+POOLED = {"hires16k", "tied64k"}
 
 
 @pytest.mark.parametrize("wname", list(FWD_SLICES))
@@ -138,25 +146,34 @@ def test_forward_workloads(wname):
     w = WORKLOADS[wname]
     inp = make_inputs(w, with_grad=False)
     g = gpu_run(w, inp)
-    o = oracle_run(w, inp, slices=FWD_SLICES[wname])
-    compare(w, g, o, backward=False)
+    del inp
+    if wname in POOLED:
+        o = oracle_slices(w, FWD_SLICES[wname])
+    else:
+        o = oracle_run(w, make_inputs(w, with_grad=False), slices=FWD_SLICES[wname])
+    print(w.name, compare(w, g, o, backward=False))
 
 
 def test_one_landmark_per_token_reaches_exact_attention():
-    # m = N, eps = 0, converged iteration: Nystrom equals k(Q, K) V
+    # m = N, eps = 0, 30 iterations: the landmark matrix of this slice has
+    # condition number ~240 and the iteration has converged (residual factor
+    # (1 - alpha sigma_min^2)^(2^30) underflows), so Nystrom equals k(Q, K) V up
+    # to fp32 rounding: the fp32 tolerance holds against exact attention too
     w = dataclasses.replace(WORKLOADS["tiny_mN"], eps=0.0, iters=30)
     inp = make_inputs(w)
     g = gpu_run(w, inp)
+    compare(w, g, oracle_run(w, inp), backward=False)
     q, k, v = (inp[n][0, 0].astype(np.float64) for n in ("q", "k", "v"))
     S = orc.laplacian_kernel(q, k, w.lam)
-    assert rel(g["out"][0, 0], S @ v) < 1e-3
+    assert rel(g["out"][0, 0], S @ v) < 1e-4
 
 
 # ---------------------------------------------------------------------------
 # backward
 # ---------------------------------------------------------------------------
+# hires16k: the six slices with the most heavy-tailed tokens, the first and the last
 BWD_SLICES = {"pvt2": {(0, 0), (17, 1), (31, 1)}, "pvt3": {(0, 0), (31, 4)},
-              "hires16k": {(3, 5)}}
+              "hires16k": top_outlier_slices(WORKLOADS["hires16k"], 6) | {(0, 0), (7, 7)}}
 
 
 @pytest.mark.parametrize("wname", list(BWD_SLICES))
@@ -164,8 +181,12 @@ def test_backward_workloads(wname):
     w = WORKLOADS[wname]
     inp = make_inputs(w)
     g = gpu_run(w, inp, backward=True)
-    o = oracle_run(w, inp, slices=BWD_SLICES[wname], backward=True)
-    print(w.name, compare(w, g, o, backward=True))
+    if wname in POOLED:
+        del inp
+        o = oracle_slices(w, BWD_SLICES[wname], backward=True)
+    else:
+        o = oracle_run(w, inp, slices=BWD_SLICES[wname], backward=True)
+    print(w.name, len(BWD_SLICES[wname]), compare(w, g, o, backward=True))
 
 
 SMALL = [
@@ -439,7 +460,8 @@ def test_gaussian_hires16k(backward):
     w = dataclasses.replace(WORKLOADS["hires16k"], kernel="gauss")
     inp = make_inputs(w, with_grad=backward)
     g = gpu_run(w, inp, backward=backward)
-    o = oracle_run(w, inp, slices={(3, 5)} if backward else {(0, 0), (7, 7)}, backward=backward)
+    del inp
+    o = oracle_slices(w, top_outlier_slices(w, 2) | {(0, 0), (7, 7)}, backward=backward)
     print(w.name, "gauss", compare(w, g, o, backward=backward))
 
 
