@@ -404,6 +404,30 @@ def attention(q, k, v, grid_h, grid_w, m, lam, eps, iters, norm=False, kernel="l
 # (Q = K | V) blocks in tied mode); the heads' outputs concatenated in the same
 # order and projected by w_o [H*d, C] plus b_o.  Biases may be None (zero).
 # --------------------------------------------------------------------------
+# A bf16 layer stores its activations and gradients in bf16 (reading): Q, K, V
+# after the bias, the heads' outputs, the upstream gradient of the heads and
+# the attention's gradients are rounded once to bf16, everything else is exact.
+# store="f64" keeps every value exact (the float32 layer, whose rounding is at
+# the level of fp32 arithmetic).
+def round_bf16(x):
+    """Each value rounded to the nearest bf16 number (8 significant bits, the
+    float32 exponent range), ties to the even significand; from the definition:
+    scale by the power of two that puts the last kept bit at 1, round half to
+    even (numpy's rint), scale back.  Zeros, infinities and NaNs pass through."""
+    x = np.asarray(x, np.float64)
+    out = x.copy()
+    nz = np.isfinite(x) & (x != 0)
+    e = np.floor(np.log2(np.abs(x[nz])))
+    e = np.maximum(e, -126.0)                # subnormal bf16 numbers share 2^-126's spacing
+    q = np.ldexp(1.0, (e - 7).astype(np.int64))   # spacing of bf16 numbers at |x|
+    out[nz] = np.rint(x[nz] / q) * q
+    return out
+
+
+def _store(a, store):
+    return round_bf16(a) if store == "bf16" else a
+
+
 def _heads(Y, B, N, H, d):
     """[B, N, H*d] -> [B, H, N, d]"""
     return Y.reshape(B, N, H, d).transpose(0, 2, 1, 3)
@@ -416,23 +440,26 @@ def _unheads(Y):
 
 
 def block_forward(x, w_qkv, b_qkv, w_o, b_o, H, d, grid_h, grid_w, m, lam, eps, iters,
-                  norm=False, kernel="laplace", norm_batch=False, tied=False):
-    """y [B, N, C] and the saved state of the block."""
+                  norm=False, kernel="laplace", norm_batch=False, tied=False, store="f64"):
+    """y [B, N, C] and the saved state of the block; store="bf16" rounds the
+    stored activations as a bf16 layer does (see round_bf16)."""
+    if store not in ("f64", "bf16"):
+        raise ValueError(f"unknown store {store!r}")
     x = np.asarray(x, np.float64)
     B, N, C = x.shape
     S = 2 if tied else 3
     w_qkv = np.asarray(w_qkv, np.float64)
     assert w_qkv.shape == (C, S * H * d)
-    qkv = x @ w_qkv + (0.0 if b_qkv is None else np.asarray(b_qkv, np.float64))
+    qkv = _store(x @ w_qkv + (0.0 if b_qkv is None else np.asarray(b_qkv, np.float64)), store)
     blocks = [_heads(qkv[..., s * H * d:(s + 1) * H * d], B, N, H, d) for s in range(S)]
     q, v = blocks[0], blocks[-1]
     k = q if tied else blocks[1]
     O, saved = forward(q, k, v, grid_h, grid_w, m, lam, eps, iters, norm, kernel=kernel,
                        norm_batch=norm_batch)
-    Ot = _unheads(O)
+    Ot = _store(_unheads(O), store)
     y = Ot @ np.asarray(w_o, np.float64) + (0.0 if b_o is None else np.asarray(b_o, np.float64))
     st = dict(x=x, w_qkv=w_qkv, w_o=np.asarray(w_o, np.float64), Ot=Ot, attn=saved, H=H, d=d,
-              tied=tied, qkv=qkv)
+              tied=tied, qkv=qkv, store=store)
     return y, st
 
 
@@ -443,10 +470,12 @@ def block_backward(st, dy):
     H, d = st["H"], st["d"]
     dw_o = np.einsum("bnk,bnc->kc", st["Ot"], dy)
     db_o = dy.sum(axis=(0, 1))
-    dO = _heads(dy @ st["w_o"].T, B, N, H, d)
+    store = st.get("store", "f64")
+    dO = _store(_heads(dy @ st["w_o"].T, B, N, H, d), store)
     g = backward(st["attn"], dO, tied=st["tied"])
-    grad = {n: np.stack([np.stack([g[(b, h)][i] for h in range(H)]) for b in range(B)])
-            for i, n in enumerate(("q", "k", "v"))}
+    grad = {n: _store(np.stack([np.stack([g[(b, h)][i] for h in range(H)]) for b in range(B)]),
+                      store)
+            for i, n in enumerate(("q", "k", "v")) if n != "k" or not st["tied"]}
     parts = [grad["q"], grad["v"]] if st["tied"] else [grad["q"], grad["k"], grad["v"]]
     dqkv = np.concatenate([_unheads(t) for t in parts], axis=-1)
     dw_qkv = np.einsum("bnc,bnk->ck", st["x"], dqkv)

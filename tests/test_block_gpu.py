@@ -84,9 +84,12 @@ def run_gpu(c: Case, inp: dict):
 
 
 def run_oracle(c: Case, inp: dict):
+    # a bf16 layer stores Q, K, V, the heads' outputs and the gradients in bf16
+    # (the block's reading); the oracle rounds at the same points
     y, st = orc.block_forward(inp["x"], inp["w_qkv"], inp["b_qkv"], inp["w_o"], inp["b_o"], c.H,
                               c.d, c.grid_h, c.grid_w, c.m, float(c.d), 1e-3, c.iters, c.norm,
-                              c.kernel, c.norm_batch, c.tied)
+                              c.kernel, c.norm_batch, c.tied,
+                              store="bf16" if c.dtype == "bf16" else "f64")
     g = orc.block_backward(st, inp["dy"])
     return dict(zip(("y", "dx", "dw_qkv", "db_qkv", "dw_o", "db_o"), (y,) + g))
 
@@ -146,7 +149,8 @@ def test_block_hires16k_layer():
     inp = block_inputs(7, c.B, c.N, c.C, c.H, c.d, c.dtype, c.tied, True)
     g = run_gpu(c, inp)
     y0, _ = orc.block_forward(inp["x"][:1], inp["w_qkv"], inp["b_qkv"], inp["w_o"], inp["b_o"],
-                              c.H, c.d, c.grid_h, c.grid_w, c.m, float(c.d), 1e-3, c.iters)
+                              c.H, c.d, c.grid_h, c.grid_w, c.m, float(c.d), 1e-3, c.iters,
+                              store="bf16")
     e = rel(g["y"][0], y0[0])
     r, a = EW["bf16"]
     ex = elementwise_excess(g["y"][0], y0[0], r)[0]

@@ -541,3 +541,53 @@ def test_block_backward_matches_finite_differences(tied, norm, norm_batch, kerne
             fd[ix] = (loss(plus) - loss(minus)) / (2 * h)
         err = np.linalg.norm(grads[name] - fd) / np.linalg.norm(fd)
         assert err < 1e-6, (name, err)
+
+
+# ---------------------------------------------------------------------------
+# bf16 storage of the attention block (reading: a bf16 layer rounds Q, K, V,
+# the heads' outputs and the gradients once to bf16)
+# ---------------------------------------------------------------------------
+def test_round_bf16_follows_the_definition():
+    # worked cases: 8 significant bits, ties to the even significand
+    cases = {1.0: 1.0, 1.0 + 2 ** -8: 1.0, 1.0 + 3 * 2 ** -8: 1.0 + 2 ** -6,
+             1.0 + 2 ** -7: 1.0 + 2 ** -7, 1.0 + 2 ** -8 + 2 ** -30: 1.0 + 2 ** -7,
+             -3.0 - 2 ** -7: -3.0, 255.5: 256.0, 0.0: 0.0, 2.0 ** -130: 2.0 ** -130,
+             3 * 2.0 ** -134: 4 * 2.0 ** -134}
+    got = orc.round_bf16(np.array(list(cases)))
+    np.testing.assert_array_equal(got, np.array(list(cases.values())))
+    # against the seeded inputs' independent bit-level rounding of float32 values
+    from laplacian_nystr_linear_gb300.inputs import round_bf16 as round_bits
+    x = np.random.default_rng(3).standard_normal(20000).astype(np.float32) * 7.0
+    np.testing.assert_array_equal(orc.round_bf16(x.astype(np.float64)),
+                                  round_bits(x).astype(np.float64))
+    # idempotent, and every result is a bf16 value (16 low bits of its float32 zero)
+    r = orc.round_bf16(x.astype(np.float64))
+    np.testing.assert_array_equal(orc.round_bf16(r), r)
+    assert not (r.astype(np.float32).view(np.uint32) & 0xFFFF).any()
+
+
+def test_block_bf16_storage_rounds_only_the_stored_values():
+    a = dict(B=1, N=16, C=8, H=2, d=4, grid_h=4, grid_w=4, m=4, lam=4.0, eps=1e-3, iters=3)
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((a["B"], a["N"], a["C"]))
+    w = rng.standard_normal((a["C"], 3 * a["H"] * a["d"])) / 3
+    wo = rng.standard_normal((a["H"] * a["d"], a["C"])) / 3
+    dy = rng.standard_normal((a["B"], a["N"], a["C"]))
+
+    def run(store):
+        y, st = orc.block_forward(x, w, None, wo, None, a["H"], a["d"], a["grid_h"], a["grid_w"],
+                                  a["m"], a["lam"], a["eps"], a["iters"], store=store)
+        return y, st, orc.block_backward(st, dy)
+
+    y0, st0, g0 = run("f64")
+    y1, st1, g1 = run("bf16")
+    # the stored Q, K, V and heads' outputs are the f64 layer's values rounded
+    np.testing.assert_array_equal(st1["qkv"], orc.round_bf16(st0["qkv"]))
+    assert not (st1["Ot"].astype(np.float32).view(np.uint32) & 0xFFFF).any()
+    # and the results move by about bf16 rounding, not more
+    assert 0 < np.linalg.norm(y1 - y0) / np.linalg.norm(y0) < 2e-2
+    for a0, a1 in zip(g0, g1):
+        assert np.linalg.norm(a1 - a0) / np.linalg.norm(a0) < 5e-2
+    with pytest.raises(ValueError):
+        orc.block_forward(x, w, None, wo, None, a["H"], a["d"], a["grid_h"], a["grid_w"], a["m"],
+                          a["lam"], a["eps"], a["iters"], store="f16")
