@@ -33,9 +33,38 @@ METRIC = "tokens/sec Laplacian-Nyström attn fwd & fwd+bwd; % of ALU/HBM rooflin
 UNIT = "tokens/s"
 WORKLOAD = "hires16k"
 
-# FP32 lane-op peak of the part: 152 SMs x 128 FP32 lanes x 2070 MHz (max SM clock);
-# one lane-op = one FADD / FMUL / FFMA / select result.
-ALU_PEAK_TOPS = 152 * 128 * 2070e6 / 1e12
+# FP32 lanes per SM of the part (sm_100 family: 4 sub-partitions x 32); the ALU
+# peak is SMs x lanes x maximum SM clock, with the SM count and the clock read
+# from the device.  One lane-op = one FADD / FMUL / FFMA / select result.
+FP32_LANES_PER_SM = 128
+
+
+def max_sm_clock_mhz(gpu_index: int):
+    """Maximum SM clock (MHz) as nvidia-smi reports it, or None."""
+    try:
+        r = subprocess.run(["nvidia-smi", "--query-gpu=clocks.max.sm", "--format=csv,noheader,nounits",
+                            "-i", str(gpu_index)], capture_output=True, text=True, timeout=30)
+        return float(r.stdout.strip().splitlines()[0])
+    except (OSError, ValueError, IndexError, subprocess.SubprocessError):
+        return None
+
+
+def fma_probe_rates(api, torch, dev):
+    """Measured FP32 FMA rate (Tlane-op/s), scalar and paired: best of five
+    launches of the library's FMA probe, CUDA events on the current stream."""
+    sink = torch.zeros(4, dtype=torch.float32, device=dev)
+    out = {}
+    for paired in (False, True):
+        best = 0.0
+        for _ in range(6):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            n = api.fma_probe(paired, 1 << 16, sink)
+            b.record()
+            b.synchronize()
+            best = max(best, n / (a.elapsed_time(b) / 1e3) / 1e12)
+        out["paired" if paired else "scalar"] = best
+    return out
 
 
 def parse():
@@ -392,14 +421,22 @@ def run_ours(args, rank, world, local_rank):
     sampler, cpath = clock_sampler(local_rank)
     time.sleep(0.3)
     launches0 = api.launch_count()
-    api.profile_enable(True)
-    ms_local = timed(step, args.steps)
+    ms_local = timed(step, args.steps)          # no per-launch events in this pass
     clocks = clock_summary(sampler, cpath)
-    prof = api.profile_read()
-    api.profile_enable(False)
     launches = api.launch_count() - launches0
     ms = max_over_ranks(ms_local, world, dev)
     value = weak_scaling_value(w.tokens, world, ms)
+
+    # per-kernel CUDA-event times, in two more passes of the same steps: as the
+    # step runs them (the solver overlapping the key side on a side stream), and
+    # serialised on one stream (each kernel's time its own)
+    api.profile_enable(True)
+    timed(step, args.steps)
+    prof = api.profile_read()
+    api.profile_enable(True, serial=True)
+    timed(step, args.steps)
+    prof_alone = api.profile_read()
+    api.profile_enable(False)
 
     # forward alone (same buffers)
     for _ in range(2):
@@ -408,24 +445,40 @@ def run_ours(args, rank, world, local_rank):
     ms_fwd = max_over_ranks(timed(fwd_only, args.steps), world, dev)
 
     # roofline of the dominant kernel (FP32 lane-ops; the path is ALU-bound)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    mhz = clocks.get("sm_max_mhz") or max_sm_clock_mhz(local_rank)
+    if not mhz:
+        raise SystemExit("bench: the maximum SM clock could not be read (nvidia-smi)")
+    peak = sms * FP32_LANES_PER_SM * mhz * 1e6 / 1e12
+    probe = fma_probe_rates(api, torch, dev)
     ops = algorithmic_ops(w)
     per_launch_ops = {"bwd_key": ops["bwd_key"], "bwd_query": ops["bwd_query"],
                       "key_fwd": ops["key_fwd"], "query_fwd": ops["query_fwd"]}
     kernel_ms = {n: (c, t / c) for n, (c, t) in prof.items() if c}
+    kernel_ms_alone = {n: (c, t / c) for n, (c, t) in prof_alone.items() if c}
     step_ms_sum = sum(t for _, t in prof.values()) / args.steps
     dom = max(per_launch_ops, key=lambda n: prof.get(n, (0, 0.0))[1])
     dom_ms = kernel_ms[dom][1]
+    dom_ms_alone = kernel_ms_alone[dom][1]
     achieved = per_launch_ops[dom] / (dom_ms / 1e3) / 1e12
+    achieved_alone = per_launch_ops[dom] / (dom_ms_alone / 1e3) / 1e12
     total_ops = sum(ops.values())
     pipe = fp32_pipe_ops(w)
     traffic = measured_traffic(w.name, w.kernel, dom)
     roofline = {
-        "bound": "alu", "kernel": dom, "achieved": achieved, "peak": ALU_PEAK_TOPS,
-        "unit": "Tlaneop/s", "frac": achieved / ALU_PEAK_TOPS,
+        "bound": "alu", "kernel": dom, "achieved": achieved, "peak": peak,
+        "unit": "Tlaneop/s", "frac": achieved / peak,
         "traffic": traffic,
-        "peak_source": "152 SMs x 128 FP32 lanes x 2070 MHz",
-        "step_frac": total_ops / (ms / 1e3) / 1e12 / ALU_PEAK_TOPS,
-        "fp32_pipe_frac": pipe[dom] / (dom_ms / 1e3) / 1e12 / ALU_PEAK_TOPS,
+        "peak_source": (f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x {mhz:.0f} MHz (SM count "
+                        "from the device, maximum SM clock from nvidia-smi); measured by the "
+                        f"library's FMA probe: {probe['scalar']:.1f} (scalar FFMA) and "
+                        f"{probe['paired']:.1f} (paired f32x2) Tlane-op/s"),
+        "peak_measured": probe,
+        "ms_per_launch": dom_ms, "ms_per_launch_alone": dom_ms_alone,
+        "achieved_alone": achieved_alone, "frac_alone": achieved_alone / peak,
+        "step_frac": total_ops / (ms / 1e3) / 1e12 / peak,
+        "fp32_pipe_frac": pipe[dom] / (dom_ms / 1e3) / 1e12 / peak,
+        "fp32_pipe_frac_alone": pipe[dom] / (dom_ms_alone / 1e3) / 1e12 / peak,
     }
 
     # end to end through the public API: pinned host inputs in, results back to host
@@ -533,6 +586,8 @@ def run_ours(args, rank, world, local_rank):
         "fwd_tokens_per_s": world * w.tokens / (ms_fwd / 1e3), "ms_fwd": ms_fwd,
         "roofline": roofline,
         "kernels_ms_per_step": {n: t / args.steps for n, (c, t) in sorted(prof.items(), key=lambda x: -x[1][1])},
+        "kernels_ms_per_step_alone": {n: t / args.steps for n, (c, t)
+                                      in sorted(prof_alone.items(), key=lambda x: -x[1][1])},
         "kernel_sum_ms_per_step": step_ms_sum,
         "gpu_launches": launches,
         "clocks": clocks,

@@ -121,12 +121,25 @@ int lapnys_fwd(const void* q, const void* k, const void* v, void* out,
  * two steps.  Same arguments and results as lapnys_fwd with ctx = NULL, minus
  * ctx and ws.
  *  - Scratch: a 32 MiB array compiled into the library (held on every GPU that
- *    loads it, until the process exits).  A problem whose forward scratch
- *    exceeds it returns LAPNYS_ESCRATCH before anything is enqueued; use
- *    lapnys_fwd with a workspace instead.  (About: B*H*(m*d*16 + m*m*16 +
- *    S*ceil(m/64)*64*d*4) bytes, S = token splits.)
- *  - The first call on a device looks up the array's device address with that
- *    device current; make that first call before any stream capture.
+ *    loads it, until the process exits).  The forward uses these regions of
+ *    it, each rounded up to 256 bytes (f = 4 bytes, mp = 64 ceil(m / 64), S the
+ *    token splits of the key pass: about 1216 / (B H ceil(m / 64)), between 1
+ *    and ceil(N / 64)):
+ *      landmarks (two parts), W, W-hat  4 B H m d f
+ *      A, two iterates, A X_t           4 B H m^2 f
+ *      alpha record, statistics         B H (4 + 3 m) f
+ *      token -> landmark index          N f
+ *      key-pass partial sums            B H S mp d f
+ *      statistics partials              3 B H S mp f
+ *      packed query-pass tiles (bf16, d in {32, 64}, m > 64 only)
+ *                                       B H mp (2 d + 1) f
+ *    A problem whose regions add up to more than 32 MiB returns
+ *    LAPNYS_ESCRATCH before anything is enqueued; use lapnys_fwd with a
+ *    workspace instead.
+ *  - Every call looks up the array's address in the current context (a
+ *    host-side query; nothing is allocated).  The first call in a context may
+ *    load the library's device code there: make that first call before any
+ *    stream capture.
  *  - Every call shares the one array.  Calls whose work overlaps on the GPU
  *    (other streams, other host threads) race on it and give wrong results:
  *    serialise them, e.g. on one stream.  Each call fully rewrites what it
@@ -149,7 +162,11 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout,
 
 /* Byte offsets of the intermediates inside ctx, for inspection and tests.
  * All float32 unless noted:
- *   L     [B*H][m][d]             landmarks
+ *   L     [B*H][m][d]             landmarks: the fp32 value nearest to each
+ *                                 window's exact mean
+ *   Llo   [B*H][m][d]             the exact mean minus L (the backward decides
+ *                                 sgn(x - l) against the exact mean: by L where
+ *                                 x != L, by -sgn(Llo) where x == L)
  *   A     [B*H][m][m]             k(L, L) + eps I
  *   alpha [B*H][4]                alpha, |A|_1, |A|_inf, and in slot 3 the int32
  *                                 jc | (ir << 16) stored bitwise: jc the argmax
@@ -167,7 +184,7 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout,
  * P and C are what the backward reads instead of recomputing the N x m
  * kernel values. */
 typedef struct {
-  size_t L, A, alpha, X, Y, W, What, stats, idx, P, C, total;
+  size_t L, Llo, A, alpha, X, Y, W, What, stats, idx, P, C, total;
 } lapnys_ctx_layout;
 
 int lapnys_ctx_offsets(int B, int H, int N, int d, int m, int iters, unsigned flags,
@@ -246,22 +263,46 @@ int lapnys_block_bwd(const void* x, const void* w_qkv, const void* w_o, const vo
  * LAPNYS_ECUDA if the device reported an error.  clear != 0 resets the flag. */
 int lapnys_device_status(int clear);
 
+/* Self-test of the failure detection (no passage of the paper corresponds to
+ * it).  Enqueues on `stream` one CTA that waits, with the bounded wait the
+ * tensor-core kernels use but at most `polls` polls (1 <= polls <= 2^22), on
+ * an mbarrier that nothing arrives on.  The wait expires, the kernel records the
+ * expiry in the device word lapnys_device_status reads and returns, with no copy,
+ * MMA or tensor memory in flight: afterwards lapnys_device_status(1) returns
+ * LAPNYS_ETIMEOUT (and clears the word) while the context stays usable.
+ * LAPNYS_EINVAL for polls out of range (nothing enqueued). */
+int lapnys_wait_selftest(int polls, cudaStream_t stream);
+
 /* Human-readable text for a status code (static storage). */
 const char* lapnys_strerror(int status);
 
 /* Instrumentation (host side, process-wide, not thread-safe):
  *  lapnys_launch_count: kernels this library has enqueued since load.
- *  lapnys_profile_enable(1): from then on record a CUDA event pair around
- *    every launch (on the launch's stream); lapnys_profile_read, called after
- *    the caller synchronised, adds up elapsed times per kernel name and
- *    clears them.  Up to 4096 launches are recorded between reads; later ones
- *    are counted but not timed.
+ *  lapnys_profile_enable(mode): mode 1 records a CUDA event pair around every
+ *    launch from then on (on the launch's stream); mode 2 does the same and
+ *    also runs lapnys_fwd / lapnys_bwd entirely on the caller's stream (no
+ *    side stream), so that each kernel's time is its own rather than shared
+ *    with the kernels that normally overlap it; mode 0 turns both off
+ *    (LAPNYS_EINVAL for other values).  lapnys_profile_read, called after the
+ *    caller synchronised, adds up elapsed times per kernel name and clears
+ *    them.  Up to 4096 launches are recorded between reads; later ones are
+ *    counted but not timed.
  *  lapnys_profile_read fills at most max_kernels entries (name pointer with
  *    static storage, launches, total milliseconds) and returns how many kernel
- *    names it found, or -1 if an event query failed. */
+ *    names it found, or -1 if an event query failed.
+ *  lapnys_fma_probe: enqueues on `stream` a kernel of 8 CTAs of 256 threads per
+ *    SM in which every thread runs `iters` (1 .. 2^24) steps of 8 independent
+ *    FP32 FMA chains, scalar (paired = 0) or as packed pairs (paired = 1,
+ *    fma.rn.f32x2: two lane-ops per instruction), and stores in *lane_ops the
+ *    FP32 lane-ops it executes; timing it gives the measured FP32 FMA rate of
+ *    the device.  `sink` is a device float the kernel never writes in
+ *    practice (it keeps the chains live).  No passage of the paper corresponds
+ *    to it. */
 uint64_t lapnys_launch_count(void);
-int lapnys_profile_enable(int on);
+int lapnys_profile_enable(int mode);
 int lapnys_profile_read(const char** names, int* launches, double* total_ms, int max_kernels);
+int lapnys_fma_probe(int paired, int iters, float* sink, unsigned long long* lane_ops,
+                     cudaStream_t stream);
 
 #ifdef __cplusplus
 }

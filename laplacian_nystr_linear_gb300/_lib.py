@@ -22,13 +22,15 @@ EXPORTS = (
     "lapnys_ctx_offsets", "lapnys_pool", "lapnys_strerror", "lapnys_launch_count",
     "lapnys_profile_enable", "lapnys_profile_read", "lapnys_fwd_static", "lapnys_matmul",
     "lapnys_device_status", "lapnys_block_ctx_bytes", "lapnys_block_workspace_bytes",
-    "lapnys_block_fwd", "lapnys_block_bwd",
+    "lapnys_block_fwd", "lapnys_block_bwd", "lapnys_wait_selftest",
+    "lapnys_fma_probe",
 )
 
 
 class CtxLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
-                ("L", "A", "alpha", "X", "Y", "W", "What", "stats", "idx", "P", "C", "total")]
+                ("L", "Llo", "A", "alpha", "X", "Y", "W", "What", "stats", "idx", "P", "C",
+                 "total")]
 
 
 _lib = None
@@ -67,6 +69,10 @@ def load() -> ctypes.CDLL:
     lib.lapnys_block_bwd.argtypes = [P, P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, F, I,
                                      I, P, I, U, P, S]
     lib.lapnys_block_bwd.restype = I
+    lib.lapnys_fma_probe.argtypes = [I, I, P, ctypes.POINTER(ctypes.c_ulonglong), P]
+    lib.lapnys_fma_probe.restype = I
+    lib.lapnys_wait_selftest.argtypes = [I, P]
+    lib.lapnys_wait_selftest.restype = I
     lib.lapnys_device_status.argtypes = [I]
     lib.lapnys_device_status.restype = I
     lib.lapnys_bwd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, F, I, I, P, I, U, P, S]

@@ -156,6 +156,7 @@ def ctx_views(ctx: torch.Tensor, p: Params) -> dict:
 
     views = {
         "L": f32("L", (p.B, p.H, m, d)),
+        "Llo": f32("Llo", (p.B, p.H, m, d)),
         "A": f32("A", (p.B, p.H, m, m)),
         "alpha": f32("alpha", (p.B, p.H, 4)),
         "X": f32("X", (p.B, p.H, T + 1, m, m)),
@@ -172,12 +173,33 @@ def ctx_views(ctx: torch.Tensor, p: Params) -> dict:
     return views
 
 
+def device_status(clear: bool = False) -> int:
+    """lapnys_device_status: synchronises the current device; LAPNYS_ETIMEOUT if a
+    bounded device wait expired since the last clear."""
+    return int(load().lapnys_device_status(1 if clear else 0))
+
+
+def wait_selftest(polls: int, device=None) -> None:
+    """lapnys_wait_selftest on the current stream: a bounded wait that expires."""
+    check(load().lapnys_wait_selftest(int(polls), _stream(device)), "lapnys_wait_selftest")
+
+
 def launch_count() -> int:
     return int(load().lapnys_launch_count())
 
 
-def profile_enable(on: bool) -> None:
-    load().lapnys_profile_enable(1 if on else 0)
+def profile_enable(on, serial: bool = False) -> None:
+    """Per-launch CUDA-event timing on (on) or off; serial=True also runs each
+    call on the caller's stream alone, so each kernel's time is its own."""
+    check(load().lapnys_profile_enable((2 if serial else 1) if on else 0), "lapnys_profile_enable")
+
+
+def fma_probe(paired: bool, iters: int, sink: torch.Tensor) -> int:
+    """Enqueue the FP32 FMA-rate probe on the current stream; returns its lane-ops."""
+    n = ctypes.c_ulonglong(0)
+    check(load().lapnys_fma_probe(int(paired), int(iters), _ptr(sink), ctypes.byref(n),
+                                  _stream(sink.device)), "lapnys_fma_probe")
+    return int(n.value)
 
 
 def profile_read(max_kernels: int = 64) -> dict:

@@ -19,6 +19,7 @@ struct Prob {
   int nblk;       // token blocks of 64
   int Sk, Sq, Sb; // token splits of the key pass, statistics pass, backward passes
   int Skt;        // token splits of the tensor-core key pass (0 when it is not used)
+  int Stc;        // token splits of the tensor-core backward
   bool norm() const { return flags & 1u; }
   bool gauss() const { return flags & 2u; }  // Gaussian kernel instead of the Laplacian
   bool norm_batch() const { return flags & 4u; }  // statistics over the B slices of a head
@@ -73,8 +74,10 @@ cudaError_t run_query_gtc(const Prob& p, const void* q, const void* packL, const
                           const float* stats, void* out, float* kvout, cudaStream_t st);
 cudaError_t run_key_gtc(const Prob& p, const void* k, const void* v, const float* L, float* part,
                         float* kvout, cudaStream_t st);
-// landmarks: L [BH][m][d] f32, idx [N] int32 (may be null)
-cudaError_t run_pool(const Prob& p, const void* k, float* L, int32_t* idx, cudaStream_t st);
+// landmarks: L [BH][m][d] f32 (the fp32 window means), Llo [BH][m][d] (the exact
+// means minus L; may be null), idx [N] int32 (may be null)
+cudaError_t run_pool(const Prob& p, const void* k, float* L, float* Llo, int32_t* idx,
+                     cudaStream_t st);
 
 // gram + alpha + Newton-Schulz, m <= 64: one CTA per slice, everything on chip.
 // X has nx slots per slice, Y ny slots; slot of iterate t is t % nx (t % ny).
@@ -108,8 +111,18 @@ cudaError_t run_tcgemm(bool ta, bool tb, int batch, int M, int N, int K, const f
                        const float* E, int lde, long sE, float alpha, float beta, cudaStream_t st);
 // value of the device error word set by expired bounded waits (-1 on failure)
 int read_wait_error(bool clear);
-// device address of that word on the current device (null on failure)
+// device address of that word in the current context (null on failure)
 int* wait_error_address();
+// one CTA whose bounded wait (at most `polls` polls) expires on purpose and
+// sets that word
+cudaError_t run_wait_selftest(int polls, cudaStream_t st);
+// polls of the bounded waits in the tensor-core kernels
+int tc_wait_limit();
+// FP32 FMA-rate probe: a grid of 8 CTAs of 256 threads per SM, each thread
+// `iters` x 8 independent FMAs (paired: fma.rn.f32x2, two lane-ops each);
+// *lane_ops = the FP32 lane-ops the launch executes
+cudaError_t run_fma_probe(bool paired, int iters, float* sink, unsigned long long* lane_ops,
+                          cudaStream_t st);
 // the whole Newton-Schulz iteration (reverse: its exact reverse) of every
 // slice in one cluster launch, for ns_cluster_ok(m); buffers as in the ctx and
 // workspace layouts ([BH][nx or ny or 1][m][m])
@@ -135,6 +148,7 @@ struct BwdArgs {
   const void* X;      // q (modes 0, 1) or k (mode 2)
   const void* U;      // dout (modes 0, 1) or v (mode 2)
   const float* L;     // landmarks
+  const float* Llo;   // exact landmark means minus L
   const float* R;     // What (modes 0, 1) or dW (mode 2)
   const float* stats; // mu, var, rs [BH][3][m] (norm)
   const float* mdz;   // [BH][2][mp] mean dZ, mean dZ*Z (norm, mode 1)
@@ -162,18 +176,47 @@ size_t ties_scratch_bytes(int BH, int m, int d);
 cudaError_t run_tie_prep(const Prob& p, const float* L, void* scratch, cudaStream_t st);
 cudaError_t run_ties(const Prob& p, const void* x, void* scratch, uint32_t* rec, cudaStream_t st);
 cudaError_t run_mdz(const Prob& p, const float* ns_part, float* mdz, cudaStream_t st);
-cudaError_t run_gram_bwd(const Prob& p, const float* L, const float* A, const float* dA, float* dLA,
-                         cudaStream_t st);
+cudaError_t run_gram_bwd(const Prob& p, const float* L, const float* Llo, const float* A,
+                         const float* dA, float* dLA, cudaStream_t st);
 // Newton-Schulz backward for m <= 64 (full ctx: iters + 1 iterates, iters products);
 // GT = dLoss/dX_T; writes dA including the alpha term
 cudaError_t run_ns_bwd_small(const Prob& p, const float* A, const float* alpha, const float* X,
                              const float* Y, const float* GT, float* dA, cudaStream_t st);
 cudaError_t run_alpha_bwd(const Prob& p, const float* A, const float* alpha, const float* G,
                           float* dA, cudaStream_t st);
-cudaError_t run_reduce_dl(const Prob& p, const float* dLq, const float* dLc, const float* dLA,
+// dL = sum over S splits of dLq and of dLc, plus dLA ([BH][S][mp][d] partials)
+cudaError_t run_reduce_dl(const Prob& p, int S, const float* dLq, const float* dLc, const float* dLA,
                           float* dL, cudaStream_t st);
 cudaError_t run_zero(float* x, size_t n, cudaStream_t st);
 cudaError_t run_finalize(const Prob& p, const float* dQp, const float* dKp, const float* dVp,
                          const float* dL, void* dq, void* dk, void* dv, cudaStream_t st);
+// token gradients after the tensor-core backward: nq planes of dQ partials (0:
+// dq was written already), nk planes of dK partials, one plane of dV (fp32)
+cudaError_t run_finalize_tc(const Prob& p, int nq, const float* dQp, int nk, const float* dKp,
+                            const float* dVp, const float* dL, void* dq, void* dk, void* dv,
+                            cudaStream_t st);
+
+// tensor-core backward tile kernel (bf16 tokens, d = 64): one CTA per token
+// range and group of up to 256 landmarks; grid (S, bwd_tc_groups(m), BH)
+struct BwdTcArgs {
+  const void* X;          // q (mode 1) or k (mode 2)
+  const void* U;          // dout (mode 1) or v (mode 2)
+  const float* L;         // landmarks (fp32 means) and their low parts
+  const float* Llo;
+  const float* R;         // What (mode 1) or dW (mode 2)
+  const float* stats;     // [BH][3][m] (norm)
+  const float* mdz;       // [BH][2][mp] (norm, mode 1)
+  const float* kv;        // [BH][N][mp]: P (mode 1) or C (mode 2)
+  const uint32_t* ties;   // tie records of x
+  void* out;              // dq itself (mode 1, untied, one landmark group), else null
+  float* tok_part;        // [NG][BH][N][d] token partials when out is null
+  float* lm_part;         // [BH][S][mp][d] dL partials
+  float* lm_part2;        // [BH][S][mp][d] dW-hat partials (mode 1 without norm)
+  int S;
+};
+bool bwd_tc_shape(int dtype, int d);
+int bwd_tc_groups(int m);
+int bwd_tc_splits(int BH, int m, int N);
+cudaError_t run_bwd_tc(const Prob& p, int mode, const BwdTcArgs& a, cudaStream_t st);
 
 }  // namespace lapnys

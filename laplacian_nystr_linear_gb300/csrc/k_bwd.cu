@@ -14,11 +14,13 @@
 // 0 or 1 whenever x != l and both lie in {0} u [2^-40, 2^60] (the difference is
 // then at least 2^-64).  So the sign term costs three FMA-pipe operations per
 // (token, landmark, feature) instead of compare/select work on the half-rate
-// ALU pipe.  A tie x == l reads as sgn = -1 there instead of 0: the fast path
-// then puts g_ja into dX_jc and -g_ja into dL_ac, which a correction takes back
-// for each tie the tie kernels listed for the block (k_ties.cu; a few per
+// ALU pipe.  Landmark values are l = hi + lo (hi the fp32 window mean, lo the
+// rest of the exact mean), compared by hi; a tie x == hi reads as sgn = -1 on
+// the fast path while the exact mean gives -sgn(lo): the fast path then put
+// g_ja into dX_jc and -g_ja into dL_ac, and a correction moves g_ja (1 - sgn(lo))
+// back for each tie the tie kernels listed for the block (k_ties.cu; a few per
 // block at most).  A block with an out-of-range value or too many ties takes an
-// exact path with sgn(0) = 0.
+// exact path with sgn(x - hi), and -sgn(lo) where x == hi.
 //
 // Gaussian kernel k(x, l) = exp(-|x - l|_2^2 / lambda) (the SOFT review's
 // Proposed method): dk/dx_c = -(2 k / lambda) (x_c - l_c), so with the same g
@@ -119,7 +121,7 @@ template <int D, bool EXACT, bool GAUSS>
 __device__ __forceinline__ void sign_cols(int cbase, int j0, int al, int jg, int ag,
                                           const f32x2 (&gp)[4][8], const float* Xt,
                                           const float* LBt, float rowg, float inv_scale,
-                                          float* Stage, float* dLs) {
+                                          float* Stage, float* dLs, const float* llo, int nv) {
   constexpr int CW = D / 8;
   constexpr unsigned kFull = 0xffffffffu;
   const bool b2 = ag & 4, b1 = ag & 2, b0 = ag & 1;
@@ -191,7 +193,8 @@ __device__ __forceinline__ void sign_cols(int cbase, int j0, int al, int jg, int
         pq[2 * rp + 1] = v.y;
       }
     } else {
-      // exact sgn with sgn(0) = 0; l = -lb / scale (a power of two: exact)
+      // exact sgn(x - hi), and -sgn(lo) where x == hi; hi = -lb / scale (a power
+      // of two: exact)
 #pragma unroll
       for (int t = 0; t < 8; ++t) pq[t] = pl[t] = 0.f;
 #pragma unroll
@@ -199,8 +202,15 @@ __device__ __forceinline__ void sign_cols(int cbase, int j0, int al, int jg, int
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
           const float2 g = unpack2(gp[rp][t]);
-          const float v0 = sgn_times(x[2 * rp] + lb[t] * inv_scale, 0.5f * g.x);
-          const float v1 = sgn_times(x[2 * rp + 1] + lb[t] * inv_scale, 0.5f * g.y);
+          const float d0 = x[2 * rp] + lb[t] * inv_scale, d1 = x[2 * rp + 1] + lb[t] * inv_scale;
+          float v0 = sgn_times(d0, 0.5f * g.x);
+          float v1 = sgn_times(d1, 0.5f * g.y);
+          if ((d0 == 0.f || d1 == 0.f) && al + t < nv) {
+            const float lo = __ldg(llo + (size_t)(al + t) * D + c);
+            const float sl = lo > 0.f ? -1.f : (lo < 0.f ? 1.f : 0.f);
+            if (d0 == 0.f) v0 = sl * 0.5f * g.x;
+            if (d1 == 0.f) v1 = sl * 0.5f * g.y;
+          }
           pq[2 * rp] += v0;
           pq[2 * rp + 1] += v1;
           pl[t] += v0;
@@ -250,7 +260,8 @@ __device__ __forceinline__ void sign_cols(int cbase, int j0, int al, int jg, int
 template <int D, typename T, int MODE, bool NORM, bool GAUSS>
 __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared memory allows one CTA
     k_bwd_pair(const T* __restrict__ X, const T* __restrict__ U, const float* __restrict__ L,
-               const float* __restrict__ R, const float* __restrict__ stats,
+               const float* __restrict__ Llo, const float* __restrict__ R,
+               const float* __restrict__ stats,
                const float* __restrict__ mdz, float* __restrict__ tok_part,
                float* __restrict__ tok_part2, float* __restrict__ lm_part,
                float* __restrict__ lm_part2, const uint32_t* __restrict__ tie_rec,
@@ -625,12 +636,18 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
         gp[0][t] = u.x; gp[1][t] = u.y; gp[2][t] = v.x; gp[3][t] = v.y;
       }
       if (tid < nties) {
-        // the tie's g, read before the g tile becomes staging space
+        // the tie's correction g (1 - sgn(lo)), read before the g tile becomes
+        // staging space
         const uint32_t t = __ldg(rb + 1 + tid);
         const int a = (int)(t >> 12) - a0;
         const bool mine = a >= 0 && a < nv;
         tie_s[tid] = mine ? t : ~0u;
-        tieg_s[tid] = mine ? 0.5f * Gs[gt(a, (int)(t & 31u))] : 0.f;
+        float corr = 0.f;
+        if (mine) {
+          const float lo = __ldg(Llo + ((size_t)bh * m + a0 + a) * D + ((t >> 5) & 127u));
+          corr = 0.5f * Gs[gt(a, (int)(t & 31u))] * (lo > 0.f ? 0.f : (lo < 0.f ? 2.f : 1.f));
+        }
+        tieg_s[tid] = corr;
       }
       __syncthreads();  // g and Z tiles are free from here on (staging); sums are ready
       const float rowg = rowg_s[j0 + ag];
@@ -638,16 +655,17 @@ __global__ void __launch_bounds__(kThreads, D <= 64 ? 2 : 1)  // d = 128: shared
         colg_acc0 += colg_s[al + 2 * jg];
         colg_acc1 += colg_s[al + 2 * jg + 1];
       }
+      const float* llo = Llo + ((size_t)bh * m + a0) * D;
       if constexpr (GAUSS) {
         sign_cols<D, false, true>(warp * CW, j0, al, jg, ag, gp, Xt, LBt, rowg, inv_scale, Stage,
-                                  dLs);
+                                  dLs, llo, nv);
       } else {
         if (exact)
           sign_cols<D, true, false>(warp * CW, j0, al, jg, ag, gp, Xt, LBt, rowg, inv_scale, Stage,
-                                    dLs);
+                                    dLs, llo, nv);
         else
           sign_cols<D, false, false>(warp * CW, j0, al, jg, ag, gp, Xt, LBt, rowg, inv_scale,
-                                     Stage, dLs);
+                                     Stage, dLs, llo, nv);
       }
     }
     __syncthreads();
@@ -714,7 +732,7 @@ static cudaError_t bwd_pair_t2(const Prob& p, const BwdArgs& a, cudaStream_t st)
   static const char* names[3] = {"", "bwd_query", "bwd_key"};
   const int nblk = (p.N + TJ - 1) / TJ;
   return launch(names[MODE], k_bwd_pair<D, T, MODE, NORM, GAUSS>, dim3(p.nt, p.Sb, p.BH), dim3(kThreads),
-                smem, st, (const T*)a.X, (const T*)a.U, a.L, a.R, a.stats, a.mdz, a.tok_part,
+                smem, st, (const T*)a.X, (const T*)a.U, a.L, a.Llo, a.R, a.stats, a.mdz, a.tok_part,
                 a.tok_part2, a.lm_part, a.lm_part2, a.ties, a.kv, p.N, p.m, p.mp,
                 p.Sb, nblk, p.BH, p.inv_lam);
 }

@@ -60,16 +60,22 @@ struct QSmem {
   static constexpr uint32_t kTileB = D * TL * 4;
 };
 
+// key pass: the contraction W += C^T V runs as kind::f16 MMAs on bf16 operands,
+// V exact and C as three bf16 planes c1 + c2 + c3 (24 significant bits): W
+// enters W-hat = X_T W, whose unconverged directions amplify a single rounding
+// of C (TF32: ~2e-4 in W) about a hundredfold.
+constexpr uint32_t kLboC = (QM / 8) * kSbo + 16;  // A (C^T planes): 8-token K groups, 2064 bytes apart
+constexpr uint32_t kPlaneC = (TL / 8) * kLboC;
 template <int D>
 struct KSmem {
   static constexpr uint32_t Lt = 0;                            // [D][QM] f32, feature-major landmarks
   static constexpr uint32_t Kt = Lt + D * QM * 4;              // [D][TL] f32, feature-major keys
-  static constexpr uint32_t kLboB = (D / 8) * kSboVB;          // B (V^T): K groups
-  static constexpr uint32_t kTileB = (TL / 4) * kLboB;
+  static constexpr uint32_t kLboB = (D / 8) * kSboVB;          // B (V^T, bf16): 8-token K groups
+  static constexpr uint32_t kTileB = (TL / 8) * kLboB;
   static constexpr uint32_t Vb = Kt + D * TL * 4;              // 2 x B tiles (V^T)
-  static constexpr uint32_t Ca = Vb + 2 * kTileB;              // 2 x A tiles (C^T, TF32)
+  static constexpr uint32_t Ca = Vb + 2 * kTileB;              // 2 x 3 A planes (C^T, bf16)
   static constexpr uint32_t kRow = D * 2 + 16;                 // padded raw row
-  static constexpr uint32_t Raw = Ca + 2 * kTileA;             // 2 x (64 key rows, 64 value rows)
+  static constexpr uint32_t Raw = Ca + 6 * kPlaneC;            // 2 x (64 key rows, 64 value rows)
   static constexpr uint32_t kRawBuf = 2 * TL * kRow;
   static constexpr uint32_t total = Raw + 2 * kRawBuf;
 };
@@ -83,8 +89,11 @@ __device__ __forceinline__ float tf32f(float x) {
   return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
 }
 
-__device__ __forceinline__ void flag_timeout(int* err, bool ok) {
+// bounded wait for a phase of an mbarrier; on expiry the error word is set
+__device__ __forceinline__ bool wait_or_flag(int* err, uint32_t bar, uint32_t parity) {
+  const bool ok = tc::mbar_wait(bar, parity);
   if (!ok) atomicOr(err, 1);
+  return ok;
 }
 
 // 8 bf16 values (16 bytes) -> 8 floats
@@ -185,13 +194,27 @@ __global__ void __launch_bounds__(NTH, 1) k_query_tc(QArgs a) {
     cp_commit();
   };
 
+  // An expired wait (bad) stops the CTA at its next barrier, taken by all
+  // threads alike (__syncthreads_or): no further copy or MMA is issued, and the
+  // copies and MMAs already in flight are waited for (bounded) before the
+  // tensor memory is freed.
   uint32_t g = 0;
-  if (tid == 0 && (int)blockIdx.x < a.items) issue_tile(0, blockIdx.x, 0);
+  bool bad = false, abort = false;
+  int last_mma = -1;     // last tile whose MMAs were issued
+  uint32_t issued = 0;   // tiles whose operand copies were issued (thread 0)
+  if (tid == 0 && (int)blockIdx.x < a.items) {
+    issue_tile(0, blockIdx.x, 0);
+    issued = 1;
+  }
   prefetch_q(blockIdx.x);
   for (int item = blockIdx.x; item < a.items; item += gridDim.x) {
     const int bh = item / a.nb, j0 = (item % a.nb) * QM;
     cp_wait_all();
-    __syncthreads();  // this item's rows landed; the previous item's distances are done
+    // this item's rows landed; the previous item's distances are done
+    if (__syncthreads_or(bad)) {
+      abort = true;
+      break;
+    }
     {
       // raw rows -> feature-major f32 (lanes take consecutive queries)
       constexpr int CH = D / 8;
@@ -207,15 +230,18 @@ __global__ void __launch_bounds__(NTH, 1) k_query_tc(QArgs a) {
     prefetch_q(item + gridDim.x);
 
     for (int t = 0; t < a.nt; ++t, ++g) {
-      flag_timeout(a.err, tc::mbar_wait(tc::smem_u32(&full[g % 3]), (g / 3) & 1));
-      if (tid == 0) {
+      bad |= !wait_or_flag(a.err, tc::smem_u32(&full[g % 3]), (g / 3) & 1);
+      if (tid == 0 && !bad) {
         // tile g + 1: its landmark buffer was read by tile g - 1's distances
         // (finished before the last barrier), its W-hat buffer by MMA g - 2
         int nitem = item, nt1 = t + 1;
         if (nt1 == a.nt) { nitem = item + gridDim.x; nt1 = 0; }
         if (nitem < a.items) {
-          if (g >= 2) flag_timeout(a.err, tc::mbar_wait(tc::smem_u32(&mdone[g & 1]), ((g - 2) >> 1) & 1));
-          issue_tile(g + 1, nitem, nt1);
+          if (g >= 2) bad |= !wait_or_flag(a.err, tc::smem_u32(&mdone[g & 1]), ((g - 2) >> 1) & 1);
+          if (!bad) {
+            issue_tile(g + 1, nitem, nt1);
+            issued = g + 2;
+          }
         }
       }
       const float* Lt = reinterpret_cast<const float*>(sm + S::Lt + (g & 1) * S::kTileB);
@@ -239,7 +265,7 @@ __global__ void __launch_bounds__(NTH, 1) k_query_tc(QArgs a) {
         }
       }
       // the A buffer of this tile was read by MMA g - 2
-      if (g >= 2) flag_timeout(a.err, tc::mbar_wait(tc::smem_u32(&mdone[g & 1]), ((g - 2) >> 1) & 1));
+      if (g >= 2) bad |= !wait_or_flag(a.err, tc::smem_u32(&mdone[g & 1]), ((g - 2) >> 1) & 1);
       {
         const int ab = t * TL + 4 * tx;  // first landmark of this thread
         float mu[4], rs[4];
@@ -272,7 +298,10 @@ __global__ void __launch_bounds__(NTH, 1) k_query_tc(QArgs a) {
       }
       tc::fence_async_smem();
       tc::fence_before();
-      __syncthreads();
+      if (__syncthreads_or(bad)) {
+        abort = true;
+        break;
+      }
       if (tid == 0) {
         tc::fence_after();
         const uint32_t pa = tc::smem_u32(sm + S::Pa + (g & 1) * kTileA);
@@ -284,10 +313,12 @@ __global__ void __launch_bounds__(NTH, 1) k_query_tc(QArgs a) {
                      (t > 0 || k8 > 0) ? 1u : 0u);
         tc::commit(tc::smem_u32(&mdone[g & 1]));
       }
+      last_mma = (int)g;
     }
+    if (abort) break;
     // the item's accumulator: lane quarter w % 4 holds queries 32 (w % 4) .., the
     // four warps w, w + 4, w + 8, w + 12 split the columns
-    flag_timeout(a.err, tc::mbar_wait(tc::smem_u32(&mdone[(g - 1) & 1]), ((g - 1) >> 1) & 1));
+    bad |= !wait_or_flag(a.err, tc::smem_u32(&mdone[(g - 1) & 1]), ((g - 1) >> 1) & 1);
     tc::fence_after();
     {
       constexpr int HC = D / 4;
@@ -315,6 +346,15 @@ __global__ void __launch_bounds__(NTH, 1) k_query_tc(QArgs a) {
     tc::fence_before();
   }
   cp_wait_all();
+  if (abort) {
+    // drain what this CTA issued: the last MMAs, and operand tiles not yet waited for
+    if (last_mma >= 0)
+      wait_or_flag(a.err, tc::smem_u32(&mdone[last_mma & 1]), ((uint32_t)last_mma >> 1) & 1);
+    if (tid == 0)
+      for (uint32_t gi = g; gi < issued; ++gi)
+        wait_or_flag(a.err, tc::smem_u32(&full[gi % 3]), (gi / 3) & 1);
+    tc::fence_before();
+  }
   __syncthreads();
   tc::fence_after();
   if (warp == 0) tc::tmem_dealloc(tmem, kCols);
@@ -347,7 +387,7 @@ __global__ void __launch_bounds__(NTH, 1) k_key_tc(KArgs a) {
   const int lt = blockIdx.x, sp = blockIdx.y, bh = blockIdx.z;
   const int a0 = lt * QM;
   constexpr uint32_t kCols = tmem_cols(D);
-  const uint32_t id = tc::idesc_tf32(QM, D);
+  const uint32_t id = tc::idesc_bf16(QM, D);
   const __nv_bfloat16* Kb = a.K + (size_t)bh * a.N * D;
   const __nv_bfloat16* Vb = a.V + (size_t)bh * a.N * D;
 
@@ -382,13 +422,17 @@ __global__ void __launch_bounds__(NTH, 1) k_key_tc(KArgs a) {
     cp_commit();
   };
   prefetch(b0, 0);
+  // An expired wait (bad) stops the CTA before its next MMAs, decided by all
+  // threads alike (__syncthreads_or); the MMAs already issued and the copies in
+  // flight are waited for (bounded) before the tensor memory is freed.
+  bool bad = false, abort = false;
   int i = 0;
   for (int b = b0; b < b1; ++b, ++i) {
     const int buf = i & 1;
     cp_wait_all();
     __syncthreads();  // block b's rows landed; the previous block's distances are done
     // the V^T and C^T buffers of this block were read by MMA i - 2
-    if (i >= 2) flag_timeout(a.err, tc::mbar_wait(tc::smem_u32(&mdone[buf]), ((i - 2) >> 1) & 1));
+    if (i >= 2) bad |= !wait_or_flag(a.err, tc::smem_u32(&mdone[buf]), ((i - 2) >> 1) & 1);
     {
       const uint8_t* rb = sm + S::Raw + buf * S::kRawBuf;
       constexpr int CH = D / 8;
@@ -400,15 +444,21 @@ __global__ void __launch_bounds__(NTH, 1) k_key_tc(KArgs a) {
 #pragma unroll
         for (int q = 0; q < 8; ++q) Kt[(8 * ch + q) * TL + j] = f[q];
       }
-      // values -> B operand (row = feature, k = token); lanes: 8 feature groups x 4 tokens
+      // values -> bf16 B operand (row = feature, k = token); a thread takes a
+      // token pair and 8 features, lanes: 8 feature groups x 4 token pairs
       uint8_t* vb = sm + S::Vb + buf * S::kTileB;
-      for (int e = tid; e < TL * CH; e += NTH) {
-        const int ch = e % CH, j = e / CH;
-        float f[8];
-        bf16x8(*reinterpret_cast<const uint4*>(rb + (TL + j) * S::kRow + 16 * ch), f);
+      for (int e = tid; e < (TL / 2) * CH; e += NTH) {
+        const int ch = e % CH, j = 2 * (e / CH);
+        const uint4 u0 = *reinterpret_cast<const uint4*>(rb + (TL + j) * S::kRow + 16 * ch);
+        const uint4 u1 = *reinterpret_cast<const uint4*>(rb + (TL + j + 1) * S::kRow + 16 * ch);
+        const uint32_t w0[4] = {u0.x, u0.y, u0.z, u0.w}, w1[4] = {u1.x, u1.y, u1.z, u1.w};
+        uint8_t* dst = vb + (j >> 3) * S::kLboB + ch * kSboVB + (j & 7) * 2;
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          *reinterpret_cast<float*>(vb + (j >> 2) * S::kLboB + ch * kSboVB + q * 16 + (j & 3) * 4) = f[q];
+        for (int q = 0; q < 4; ++q) {
+          // features 8 ch + 2 q (low halves) and 8 ch + 2 q + 1 (high halves)
+          *reinterpret_cast<uint32_t*>(dst + (2 * q) * 16) = (w0[q] & 0xffffu) | (w1[q] << 16);
+          *reinterpret_cast<uint32_t*>(dst + (2 * q + 1) * 16) = (w0[q] >> 16) | (w1[q] & 0xffff0000u);
+        }
       }
     }
     __syncthreads();
@@ -453,32 +503,59 @@ __global__ void __launch_bounds__(NTH, 1) k_key_tc(KArgs a) {
                 make_float4(cv[0][s], cv[1][s], cv[2][s], cv[3][s]));
         }
       }
-      uint8_t* ca = sm + S::Ca + buf * kTileA + tx * kLboA + (ty >> 1) * kSbo + (ty & 1) * 64;
+      // C^T as three bf16 planes (row = landmark 4 ty + r, k = tokens 4 tx .. 4 tx + 3)
+      uint8_t* ca = sm + S::Ca + buf * 3 * kPlaneC + (tx >> 1) * kLboC + (ty >> 1) * kSbo +
+                    (ty & 1) * 64 + (tx & 1) * 8;
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
-        *reinterpret_cast<float4*>(ca + r * 16) =
-            make_float4(tf32f(cv[r][0]), tf32f(cv[r][1]), tf32f(cv[r][2]), tf32f(cv[r][3]));
+      for (int r = 0; r < 4; ++r) {
+        uint32_t pl[3][2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t b[3][2];
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            float v = cv[r][2 * h + t];
+#pragma unroll
+            for (int p = 0; p < 3; ++p) {
+              const __nv_bfloat16 hb = __float2bfloat16_rn(v);
+              b[p][t] = *reinterpret_cast<const uint16_t*>(&hb);
+              v -= __bfloat162float(hb);
+            }
+          }
+#pragma unroll
+          for (int p = 0; p < 3; ++p) pl[p][h] = b[p][0] | (b[p][1] << 16);
+        }
+#pragma unroll
+        for (int p = 0; p < 3; ++p)
+          *reinterpret_cast<uint2*>(ca + p * kPlaneC + r * 16) = make_uint2(pl[p][0], pl[p][1]);
+      }
     }
     tc::fence_async_smem();
     tc::fence_before();
-    __syncthreads();
+    if (__syncthreads_or(bad)) {
+      abort = true;
+      break;
+    }
     if (tid == 0) {
       tc::fence_after();
-      const uint32_t ca = tc::smem_u32(sm + S::Ca + buf * kTileA);
+      const uint32_t ca = tc::smem_u32(sm + S::Ca + buf * 3 * kPlaneC);
       const uint32_t vbs = tc::smem_u32(sm + S::Vb + buf * S::kTileB);
 #pragma unroll
-      for (int k8 = 0; k8 < TL / 8; ++k8)
-        tc::mma_ss(tmem, tc::desc(ca + k8 * 2 * kLboA, kLboA, kSbo),
-                   tc::desc(vbs + k8 * 2 * S::kLboB, S::kLboB, kSboVB), id,
-                   (i > 0 || k8 > 0) ? 1u : 0u);
+      for (int p = 0; p < 3; ++p)
+#pragma unroll
+        for (int k16 = 0; k16 < TL / 16; ++k16)
+          tc::mma_bf16(tmem, tc::desc(ca + p * kPlaneC + k16 * 2 * kLboC, kLboC, kSbo),
+                       tc::desc(vbs + k16 * 2 * S::kLboB, S::kLboB, kSboVB), id,
+                       (i > 0 || p > 0 || k16 > 0) ? 1u : 0u);
       tc::commit(tc::smem_u32(&mdone[buf]));
     }
   }
+  cp_wait_all();  // the next block's rows, when the loop stopped early
   // partial W of this range: lane quarter w % 4 holds landmarks 32 (w % 4) .., the
-  // four warps w, w + 4, w + 8, w + 12 split the columns
-  if (i > 0) flag_timeout(a.err, tc::mbar_wait(tc::smem_u32(&mdone[(i - 1) & 1]), ((i - 1) >> 1) & 1));
+  // four warps w, w + 4, w + 8, w + 12 split the columns (MMAs of blocks < i)
+  if (i > 0) wait_or_flag(a.err, tc::smem_u32(&mdone[(i - 1) & 1]), ((i - 1) >> 1) & 1);
   tc::fence_after();
-  {
+  if (!abort) {
     constexpr int HC = D / 4;
     const int q = warp & 3, h = warp >> 2;
     uint32_t v[HC];
@@ -505,21 +582,22 @@ __global__ void __launch_bounds__(NTH, 1) k_key_tc(KArgs a) {
 bool fwd_tc_shape(int d, int m) { return (d == 32 || d == 64) && m > kTile; }
 bool fwd_tc_ok(const Prob& p) { return p.dtype == 1 && fwd_tc_shape(p.d, p.m); }
 
+// SMs of the current device (the persistent query pass's grid; the items it
+// processes, and so its results, do not depend on it)
 static int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
-  }
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 1;
   return n;
 }
 
 int key_tc_splits(int BH, int m, int nblk) {
   const int nt = (m + QM - 1) / QM;
-  // about six waves of one CTA per SM
-  int s = (6 * sm_count() + BH * nt / 2) / (BH * nt);
+  // about six waves of one CTA per SM of a 152-SM part; from the dimensions
+  // alone, so the summation order (and the workspace size) does not depend on
+  // the device
+  int s = (6 * 152 + BH * nt / 2) / (BH * nt);
   if (s < 1) s = 1;
   if (s > nblk) s = nblk;
   return s;

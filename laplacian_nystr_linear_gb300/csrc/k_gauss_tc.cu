@@ -38,13 +38,20 @@ constexpr uint32_t kLbo64 = (TL / 8) * kSbo;   // K groups of a 64-row operand
 constexpr uint32_t kTileP = (TL / 4) * kLbo128;  // 128 x 64 A operand of the second MMA
 constexpr uint32_t kSboVB = 144;             // key pass V^T: 8-row groups 144 bytes apart
 constexpr uint32_t kScol = 128;              // first TMEM column of the two S buffers
+// key pass: W += C^T V as kind::f16 MMAs with V exact in bf16 and C as three bf16
+// planes (24 significant bits; W is amplified by X_T in W-hat = X_T W)
+constexpr uint32_t kLboC = (QM / 8) * kSbo + 16;  // C^T planes: 8-key K groups, 2064 bytes apart
+constexpr uint32_t kPlaneC = (TL / 8) * kLboC;
 constexpr uint32_t kCols = 256;              // TMEM columns: accumulator [0, d), S at 128, 192
 
 __device__ __forceinline__ float tf32f(float x) {
   return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
 }
-__device__ __forceinline__ void flag_timeout(int* err, bool ok) {
+// bounded wait for a phase of an mbarrier; on expiry the error word is set
+__device__ __forceinline__ bool wait_or_flag(int* err, uint32_t bar, uint32_t parity) {
+  const bool ok = tc::mbar_wait(bar, parity);
   if (!ok) atomicOr(err, 1);
+  return ok;
 }
 __device__ __forceinline__ void bf16x8(uint4 u, float (&f)[8]) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -81,16 +88,16 @@ template <int D>
 struct GK {
   static constexpr uint32_t kTileL = (D / 4) * kLbo128;      // landmarks as A of S
   static constexpr uint32_t kTileK = (D / 4) * kLbo64;       // keys as B of S
-  static constexpr uint32_t kLboV = (D / 8) * kSboVB;        // V^T as B of W
-  static constexpr uint32_t kTileV = (TL / 4) * kLboV;
+  static constexpr uint32_t kLboV = (D / 8) * kSboVB;        // V^T (bf16) as B of W
+  static constexpr uint32_t kTileV = (TL / 8) * kLboV;
   static constexpr uint32_t La = 0;
   static constexpr uint32_t Ln = La + kTileL;                // |l~|^2 of the CTA's landmarks
   static constexpr uint32_t Kb = Ln + QM * 4;
   static constexpr uint32_t Kn = Kb + kTileK;                // |k|^2 of the block's keys
   static constexpr uint32_t Vb = Kn + TL * 4;                // 2 x V^T tiles
-  static constexpr uint32_t Ca = Vb + 2 * kTileV;            // 2 x C^T tiles (A of W)
+  static constexpr uint32_t Ca = Vb + 2 * kTileV;            // 2 x 3 C^T planes (A of W)
   static constexpr uint32_t kRow = D * 2 + 16;
-  static constexpr uint32_t Raw = Ca + 2 * kTileP;           // 2 x (64 key rows, 64 value rows)
+  static constexpr uint32_t Raw = Ca + 6 * kPlaneC;          // 2 x (64 key rows, 64 value rows)
   static constexpr uint32_t kRawBuf = 2 * TL * kRow;
   static constexpr uint32_t total = Raw + 2 * kRawBuf;
 };
@@ -195,13 +202,28 @@ __global__ void __launch_bounds__(NTH, 1) k_query_gtc(GQArgs a) {
     cp_commit();
   };
 
+  // An expired wait (bad) stops the CTA at its next barrier, taken by all
+  // threads alike (__syncthreads_or): no further copy or MMA is issued, and the
+  // copies and MMAs already in flight are waited for (bounded) before the
+  // tensor memory is freed.
   uint32_t g = 0;
-  if (tid == 0 && (int)blockIdx.x < a.items) issue_tile(0, blockIdx.x, 0);
+  bool bad = false, abort = false;
+  int last_mma = -1;     // last tile whose contraction MMAs were issued
+  int last_s = -1;       // last tile whose distance MMAs were issued (thread 0)
+  uint32_t issued = 0;   // tiles whose operand copies were issued (thread 0)
+  if (tid == 0 && (int)blockIdx.x < a.items) {
+    issue_tile(0, blockIdx.x, 0);
+    issued = 1;
+  }
   prefetch_q(blockIdx.x);
   for (int item = blockIdx.x; item < a.items; item += gridDim.x) {
     const int bh = item / a.nb, j0 = (item % a.nb) * QM;
     cp_wait_all();
-    __syncthreads();  // this item's rows landed; the previous item's MMAs have completed
+    // this item's rows landed; the previous item's MMAs have completed
+    if (__syncthreads_or(bad)) {
+      abort = true;
+      break;
+    }
     {
       // raw rows -> A operand of S (bf16 is exact in TF32); lanes take consecutive queries
       constexpr int CH = D / 8;
@@ -234,9 +256,9 @@ __global__ void __launch_bounds__(NTH, 1) k_query_gtc(GQArgs a) {
     prefetch_q(item + gridDim.x);
 
     for (int t = 0; t < a.nt; ++t, ++g) {
-      flag_timeout(a.err, tc::mbar_wait(tc::smem_u32(&full[g % 3]), (g / 3) & 1));
+      bad |= !wait_or_flag(a.err, tc::smem_u32(&full[g % 3]), (g / 3) & 1);
       const uint32_t sbuf = kScol + (g & 1) * TL;
-      if (tid == 0) {
+      if (tid == 0 && !bad) {
         tc::fence_after();
         const uint32_t xa = tc::smem_u32(sm + S::Xa);
         const uint32_t lb = tc::smem_u32(sm + S::Lb + (g & 1) * S::kRec);
@@ -245,21 +267,27 @@ __global__ void __launch_bounds__(NTH, 1) k_query_gtc(GQArgs a) {
           tc::mma_ss(tmem + sbuf, tc::desc(xa + k8 * 2 * kLbo128, kLbo128, kSbo),
                      tc::desc(lb + k8 * 2 * kLbo64, kLbo64, kSbo), idS, k8 > 0 ? 1u : 0u);
         tc::commit(tc::smem_u32(&sdone));
+        last_s = (int)g;
         // tile g + 1: its landmark record goes where tile g - 1's was (that S MMA
         // completed before tile g - 1's epilogue); its W-hat^T where MMA g - 2 read
         int nitem = item, nt1 = t + 1;
         if (nt1 == a.nt) { nitem = item + gridDim.x; nt1 = 0; }
         if (nitem < a.items) {
-          if (g >= 2) flag_timeout(a.err, tc::mbar_wait(tc::smem_u32(&mdone[g & 1]), ((g - 2) >> 1) & 1));
-          issue_tile(g + 1, nitem, nt1);
+          if (g >= 2) bad |= !wait_or_flag(a.err, tc::smem_u32(&mdone[g & 1]), ((g - 2) >> 1) & 1);
+          if (!bad) {
+            issue_tile(g + 1, nitem, nt1);
+            issued = g + 2;
+          }
         }
       }
-      flag_timeout(a.err, tc::mbar_wait(tc::smem_u32(&sdone), g & 1));
+      // (thread 0 skips the distance MMAs after an expired wait; the others' wait
+      // for them then expires too, and the barrier below stops the CTA)
+      bad |= !wait_or_flag(a.err, tc::smem_u32(&sdone), g & 1);
       tc::fence_after();
       uint32_t v[16];
       tc::tmem_ld<16>(tmem + ((uint32_t)(32 * quarter) << 16) + sbuf + 16 * cg, v);
       // the A buffer of O for this tile was read by MMA g - 2
-      if (g >= 2) flag_timeout(a.err, tc::mbar_wait(tc::smem_u32(&mdone[g & 1]), ((g - 2) >> 1) & 1));
+      if (g >= 2) bad |= !wait_or_flag(a.err, tc::smem_u32(&mdone[g & 1]), ((g - 2) >> 1) & 1);
       {
         const int jl = 32 * quarter + lane, j = j0 + jl;
         const int al0 = 16 * cg, ab = t * TL + al0;  // this thread's 16 landmarks
@@ -292,7 +320,10 @@ __global__ void __launch_bounds__(NTH, 1) k_query_gtc(GQArgs a) {
       }
       tc::fence_async_smem();
       tc::fence_before();
-      __syncthreads();
+      if (__syncthreads_or(bad)) {
+        abort = true;
+        break;
+      }
       if (tid == 0) {
         tc::fence_after();
         const uint32_t pa = tc::smem_u32(sm + S::Pa + (g & 1) * kTileP);
@@ -304,10 +335,12 @@ __global__ void __launch_bounds__(NTH, 1) k_query_gtc(GQArgs a) {
                      (t > 0 || k8 > 0) ? 1u : 0u);
         tc::commit(tc::smem_u32(&mdone[g & 1]));
       }
+      last_mma = (int)g;
     }
+    if (abort) break;
     // the item's accumulator: lane quarter w % 4 holds queries 32 (w % 4) .., the
     // four warps of a quarter split the columns
-    flag_timeout(a.err, tc::mbar_wait(tc::smem_u32(&mdone[(g - 1) & 1]), ((g - 1) >> 1) & 1));
+    bad |= !wait_or_flag(a.err, tc::smem_u32(&mdone[(g - 1) & 1]), ((g - 1) >> 1) & 1);
     tc::fence_after();
     {
       constexpr int HC = D / 4;
@@ -334,6 +367,18 @@ __global__ void __launch_bounds__(NTH, 1) k_query_gtc(GQArgs a) {
     tc::fence_before();
   }
   cp_wait_all();
+  if (abort) {
+    // drain what this CTA issued: the last MMAs (a commit covers every earlier
+    // MMA of its thread) and the operand tiles not yet waited for
+    if (last_mma >= 0)
+      wait_or_flag(a.err, tc::smem_u32(&mdone[last_mma & 1]), ((uint32_t)last_mma >> 1) & 1);
+    if (tid == 0) {
+      if (last_s > last_mma) wait_or_flag(a.err, tc::smem_u32(&sdone), (uint32_t)last_s & 1);
+      for (uint32_t gi = g; gi < issued; ++gi)
+        wait_or_flag(a.err, tc::smem_u32(&full[gi % 3]), (gi / 3) & 1);
+    }
+    tc::fence_before();
+  }
   __syncthreads();
   tc::fence_after();
   if (warp == 0) tc::tmem_dealloc(tmem, kCols);
@@ -364,7 +409,7 @@ __global__ void __launch_bounds__(NTH, 1) k_key_gtc(GKArgs a) {
   const int quarter = warp & 3, cg = warp >> 2;
   const int lt = blockIdx.x, sp = blockIdx.y, bh = blockIdx.z;
   const int a0 = lt * QM;
-  const uint32_t idS = tc::idesc_tf32(QM, TL), idW = tc::idesc_tf32(QM, D);
+  const uint32_t idS = tc::idesc_tf32(QM, TL), idW = tc::idesc_bf16(QM, D);
   const __nv_bfloat16* Kb = a.K + (size_t)bh * a.N * D;
   const __nv_bfloat16* Vb = a.V + (size_t)bh * a.N * D;
 
@@ -410,13 +455,18 @@ __global__ void __launch_bounds__(NTH, 1) k_key_gtc(GKArgs a) {
     cp_commit();
   };
   prefetch(b0, 0);
+  // An expired wait (bad) stops the CTA before its next MMAs, decided by all
+  // threads alike (__syncthreads_or); the MMAs already issued and the copies in
+  // flight are waited for (bounded) before the tensor memory is freed.
+  bool bad = false, abort = false;
+  int s_block = -1;  // last block whose distance MMAs were issued
   int i = 0;
   for (int b = b0; b < b1; ++b, ++i) {
     const int buf = i & 1;
     cp_wait_all();
     __syncthreads();  // block b's rows landed; block i - 1's S was read out
     // Vb[buf] and Ca[buf] were last read by MMA i - 2
-    if (i >= 2) flag_timeout(a.err, tc::mbar_wait(tc::smem_u32(&mdone[buf]), ((i - 2) >> 1) & 1));
+    if (i >= 2) bad |= !wait_or_flag(a.err, tc::smem_u32(&mdone[buf]), ((i - 2) >> 1) & 1);
     {
       const uint8_t* rb = sm + S::Raw + buf * S::kRawBuf;
       constexpr int CH = D / 8;
@@ -430,15 +480,20 @@ __global__ void __launch_bounds__(NTH, 1) k_key_gtc(GKArgs a) {
         *reinterpret_cast<float4*>(sm + S::Kb + kmaj(j, 8 * ch + 4, kLbo64, kSbo)) =
             make_float4(f[4], f[5], f[6], f[7]);
       }
-      // values -> B operand of W (row = feature, k = key); lanes: feature groups x keys
+      // values -> bf16 B operand of W (row = feature, k = key); a thread takes a
+      // key pair and 8 features, lanes: 8 feature groups x 4 key pairs
       uint8_t* vb = sm + S::Vb + buf * S::kTileV;
-      for (int e = tid; e < TL * CH; e += NTH) {
-        const int ch = e % CH, j = e / CH;
-        float f[8];
-        bf16x8(*reinterpret_cast<const uint4*>(rb + (TL + j) * S::kRow + 16 * ch), f);
+      for (int e = tid; e < (TL / 2) * CH; e += NTH) {
+        const int ch = e % CH, j = 2 * (e / CH);
+        const uint4 u0 = *reinterpret_cast<const uint4*>(rb + (TL + j) * S::kRow + 16 * ch);
+        const uint4 u1 = *reinterpret_cast<const uint4*>(rb + (TL + j + 1) * S::kRow + 16 * ch);
+        const uint32_t w0[4] = {u0.x, u0.y, u0.z, u0.w}, w1[4] = {u1.x, u1.y, u1.z, u1.w};
+        uint8_t* dst = vb + (j >> 3) * S::kLboV + ch * kSboVB + (j & 7) * 2;
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          *reinterpret_cast<float*>(vb + (j >> 2) * S::kLboV + ch * kSboVB + q * 16 + (j & 3) * 4) = f[q];
+        for (int q = 0; q < 4; ++q) {
+          *reinterpret_cast<uint32_t*>(dst + (2 * q) * 16) = (w0[q] & 0xffffu) | (w1[q] << 16);
+          *reinterpret_cast<uint32_t*>(dst + (2 * q + 1) * 16) = (w0[q] >> 16) | (w1[q] & 0xffff0000u);
+        }
       }
       if (tid < TL) {
         // |k|^2 of each key, features in ascending order
@@ -454,7 +509,10 @@ __global__ void __launch_bounds__(NTH, 1) k_key_gtc(GKArgs a) {
     }
     tc::fence_async_smem();
     tc::fence_before();
-    __syncthreads();
+    if (__syncthreads_or(bad)) {
+      abort = true;
+      break;
+    }
     prefetch(b + 1, buf ^ 1);
     if (tid == 0) {
       tc::fence_after();
@@ -465,7 +523,8 @@ __global__ void __launch_bounds__(NTH, 1) k_key_gtc(GKArgs a) {
                    tc::desc(kb + k8 * 2 * kLbo64, kLbo64, kSbo), idS, k8 > 0 ? 1u : 0u);
       tc::commit(tc::smem_u32(&sdone));
     }
-    flag_timeout(a.err, tc::mbar_wait(tc::smem_u32(&sdone), i & 1));
+    s_block = i;
+    bad |= !wait_or_flag(a.err, tc::smem_u32(&sdone), i & 1);
     tc::fence_after();
     {
       uint32_t v[16];
@@ -488,30 +547,60 @@ __global__ void __launch_bounds__(NTH, 1) k_key_gtc(GKArgs a) {
           if (j < a.N) a.kvout[((size_t)bh * a.N + j) * a.mp + aa] = c[q];
         }
       }
-      uint8_t* ca = sm + S::Ca + buf * kTileP;
+      // C^T as three bf16 planes (row = landmark al, k = keys jl0 .. jl0 + 15)
+      uint8_t* ca = sm + S::Ca + buf * 3 * kPlaneC + (uint32_t)(al >> 3) * kSbo +
+                    (uint32_t)(al & 7) * 16u;
+      uint32_t pl[3][8];
 #pragma unroll
-      for (int q = 0; q < 16; q += 4)
-        *reinterpret_cast<float4*>(ca + kmaj(al, jl0 + q, kLbo128, kSbo)) =
-            make_float4(tf32f(c[q]), tf32f(c[q + 1]), tf32f(c[q + 2]), tf32f(c[q + 3]));
+      for (int q = 0; q < 16; q += 2) {
+        uint32_t b[3][2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          float v = c[q + t];
+#pragma unroll
+          for (int p = 0; p < 3; ++p) {
+            const __nv_bfloat16 hb = __float2bfloat16_rn(v);
+            b[p][t] = *reinterpret_cast<const uint16_t*>(&hb);
+            v -= __bfloat162float(hb);
+          }
+        }
+#pragma unroll
+        for (int p = 0; p < 3; ++p) pl[p][q / 2] = b[p][0] | (b[p][1] << 16);
+      }
+#pragma unroll
+      for (int p = 0; p < 3; ++p)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          *reinterpret_cast<uint4*>(ca + p * kPlaneC + (uint32_t)((jl0 >> 3) + h) * kLboC) =
+              make_uint4(pl[p][4 * h], pl[p][4 * h + 1], pl[p][4 * h + 2], pl[p][4 * h + 3]);
     }
     tc::fence_async_smem();
     tc::fence_before();
-    __syncthreads();
+    if (__syncthreads_or(bad)) {
+      abort = true;
+      break;
+    }
     if (tid == 0) {
       tc::fence_after();
-      const uint32_t ca = tc::smem_u32(sm + S::Ca + buf * kTileP);
+      const uint32_t ca = tc::smem_u32(sm + S::Ca + buf * 3 * kPlaneC);
       const uint32_t vbs = tc::smem_u32(sm + S::Vb + buf * S::kTileV);
 #pragma unroll
-      for (int k8 = 0; k8 < TL / 8; ++k8)
-        tc::mma_ss(tmem, tc::desc(ca + k8 * 2 * kLbo128, kLbo128, kSbo),
-                   tc::desc(vbs + k8 * 2 * S::kLboV, S::kLboV, kSboVB), idW,
-                   (i > 0 || k8 > 0) ? 1u : 0u);
+      for (int p = 0; p < 3; ++p)
+#pragma unroll
+        for (int k16 = 0; k16 < TL / 16; ++k16)
+          tc::mma_bf16(tmem, tc::desc(ca + p * kPlaneC + k16 * 2 * kLboC, kLboC, kSbo),
+                       tc::desc(vbs + k16 * 2 * S::kLboV, S::kLboV, kSboVB), idW,
+                       (i > 0 || p > 0 || k16 > 0) ? 1u : 0u);
       tc::commit(tc::smem_u32(&mdone[buf]));
     }
   }
-  if (i > 0) flag_timeout(a.err, tc::mbar_wait(tc::smem_u32(&mdone[(i - 1) & 1]), ((i - 1) >> 1) & 1));
+  cp_wait_all();  // the next block's rows, when the loop stopped early
+  // the contraction MMAs of blocks < i, and the distance MMAs of block i when the
+  // loop stopped after issuing them (a commit covers every earlier MMA)
+  if (i > 0) wait_or_flag(a.err, tc::smem_u32(&mdone[(i - 1) & 1]), ((i - 1) >> 1) & 1);
+  if (abort && s_block == i) wait_or_flag(a.err, tc::smem_u32(&sdone), (uint32_t)i & 1);
   tc::fence_after();
-  {
+  if (!abort) {
     constexpr int HC = D / 4;
     uint32_t v[HC];
     tc::tmem_ld<HC>(tmem + ((uint32_t)(32 * quarter) << 16) + (uint32_t)(cg * HC), v);
@@ -545,14 +634,12 @@ cudaError_t run_pack_qg(const Prob& p, const float* L, const float* What, void* 
   return cudaErrorInvalidValue;
 }
 
+// SMs of the current device (the persistent query pass's grid only)
 static int sm_count_g() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
-  }
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 1;
   return n;
 }
 

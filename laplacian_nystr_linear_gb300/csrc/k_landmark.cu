@@ -19,9 +19,33 @@ namespace lapnys {
 // Landmark a = wi * mw + wj averages token rows [wi gh / mh, (wi + 1) gh / mh)
 // and columns [wj gw / mw, (wj + 1) gw / mw) (floors): equal windows when the
 // grid divides, otherwise windows of the floor and ceil sizes.
+//
+// The window sum is kept error-free as a pair s + e (each addition's rounding
+// error, by TwoSum, goes into e), and the mean is written as hi = the fp32
+// value nearest to (s + e) / n and lo = the rest, (s + e - n hi) / n (n hi is
+// subtracted exactly by an FMA).  The sign of x - l in the backward is then
+// decided by hi where x != hi and by -sgn(lo) where x == hi, i.e. against the
+// exact mean of the window.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void two_sum_acc(float& s, float& e, float v) {
+  const float t = s + v;
+  const float bp = t - s;
+  e += (s - (t - bp)) + (v - bp);
+  s = t;
+}
+
+__device__ __forceinline__ void mean_hi_lo(float s, float e, float n, float& hi, float& lo) {
+  const float sh = s + e;  // renormalise the pair (TwoSum)
+  const float bp = sh - s;
+  const float sl = (s - (sh - bp)) + (e - bp);
+  hi = __fdiv_rn(sh, n);
+  const float r = fmaf(-hi, n, sh);  // exact: the remainder of a rounded quotient
+  lo = __fdiv_rn(r + sl, n);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads) k_pool(const T* __restrict__ K, float* __restrict__ L,
+                                                   float* __restrict__ Llo,
                                                    int32_t* __restrict__ idx, int N, int d, int gh,
                                                    int gw, int mh, int mw, int m) {
   const int wi = blockIdx.x, bh = blockIdx.y;
@@ -31,31 +55,40 @@ __global__ void __launch_bounds__(kThreads) k_pool(const T* __restrict__ K, floa
   const T* Kb = K + (size_t)bh * N * d + chunk * 4;
   for (int wj = g; wj < mw; wj += groups) {
     const int x0 = wj * gw / mw, x1 = (wj + 1) * gw / mw;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f), e = s;
     for (int y = y0; y < y1; ++y) {
 #pragma unroll 4
       for (int x = x0; x < x1; ++x) {
         const float4 v = ld4(Kb + ((size_t)y * gw + x) * d);
-        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        two_sum_acc(s.x, e.x, v.x);
+        two_sum_acc(s.y, e.y, v.y);
+        two_sum_acc(s.z, e.z, v.z);
+        two_sum_acc(s.w, e.w, v.w);
       }
     }
     const int a = wi * mw + wj;
-    const float inv = 1.0f / (float)((y1 - y0) * (x1 - x0));
-    st4(L + ((size_t)bh * m + a) * d + chunk * 4,
-        make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+    const float n = (float)((y1 - y0) * (x1 - x0));
+    float4 hi, lo;
+    mean_hi_lo(s.x, e.x, n, hi.x, lo.x);
+    mean_hi_lo(s.y, e.y, n, hi.y, lo.y);
+    mean_hi_lo(s.z, e.z, n, hi.z, lo.z);
+    mean_hi_lo(s.w, e.w, n, hi.w, lo.w);
+    st4(L + ((size_t)bh * m + a) * d + chunk * 4, hi);
+    if (Llo != nullptr) st4(Llo + ((size_t)bh * m + a) * d + chunk * 4, lo);
     if (idx != nullptr && bh == 0 && chunk == 0)
       for (int y = y0; y < y1; ++y)
         for (int x = x0; x < x1; ++x) idx[y * gw + x] = a;
   }
 }
 
-cudaError_t run_pool(const Prob& p, const void* k, float* L, int32_t* idx, cudaStream_t st) {
+cudaError_t run_pool(const Prob& p, const void* k, float* L, float* Llo, int32_t* idx,
+                     cudaStream_t st) {
   dim3 grid(p.mh, p.BH);
   if (p.dtype == 1)
     return launch("pool", k_pool<__nv_bfloat16>, grid, dim3(kThreads), 0, st,
-                  (const __nv_bfloat16*)k, L, idx, p.N, p.d, p.gh, p.gw, p.mh, p.mw, p.m);
-  return launch("pool", k_pool<float>, grid, dim3(kThreads), 0, st, (const float*)k, L, idx, p.N,
-                p.d, p.gh, p.gw, p.mh, p.mw, p.m);
+                  (const __nv_bfloat16*)k, L, Llo, idx, p.N, p.d, p.gh, p.gw, p.mh, p.mw, p.m);
+  return launch("pool", k_pool<float>, grid, dim3(kThreads), 0, st, (const float*)k, L, Llo, idx,
+                p.N, p.d, p.gh, p.gw, p.mh, p.mw, p.m);
 }
 
 // ---------------------------------------------------------------------------
@@ -392,6 +425,7 @@ cudaError_t run_alpha(const Prob& p, const float* A, float* alpha, float* X0, lo
 //   dL_A[a][c] = -(1/lambda) sum_{b != a} (dA_ab + dA_ba) A_ab sgn(L_ac - L_bc)
 // or, for the Gaussian kernel (dk/dx = -(2/lambda) (x - y) k),
 //   dL_A[a][c] = -(2/lambda) sum_{b != a} (dA_ab + dA_ba) A_ab (L_ac - L_bc)
+// (landmark values l = hi + lo: equal his compare by their lo parts)
 // CTA = kGB landmarks of one slice: their weights w_ab = (dA_ab + dA_ba) A_ab
 // (0 at b = a) for every b go to shared memory first (coalesced reads of rows
 // and of the 16-wide column strips of dA), then thread (feature c, landmark
@@ -402,6 +436,7 @@ constexpr int kGB = 16;  // landmarks per CTA
 
 template <int D>
 __global__ void __launch_bounds__(kThreads) k_gram_bwd(const float* __restrict__ L,
+                                                       const float* __restrict__ Llo,
                                                        const float* __restrict__ A,
                                                        const float* __restrict__ dA,
                                                        float* __restrict__ dLA, int m,
@@ -441,7 +476,10 @@ __global__ void __launch_bounds__(kThreads) k_gram_bwd(const float* __restrict__
 #pragma unroll
     for (int k = 0; k < LPT; ++k) {
       const float wv = w[(ag + NG * k) * m + b];
-      const float t = la[k] - lb;
+      float t = la[k] - lb;
+      if (t == 0.f && !gauss && Llo != nullptr && a0 + ag + NG * k < m)
+        t = __ldg(Llo + ((size_t)bh * m + a0 + ag + NG * k) * D + c) -
+            __ldg(Llo + ((size_t)bh * m + b) * D + c);
       acc[k] += gauss ? 2.f * t * wv : sgn_times(t, wv);
     }
   }
@@ -453,22 +491,22 @@ __global__ void __launch_bounds__(kThreads) k_gram_bwd(const float* __restrict__
 }
 
 template <int D>
-static cudaError_t gram_bwd_t(const Prob& p, const float* L, const float* A, const float* dA,
-                              float* dLA, cudaStream_t st) {
+static cudaError_t gram_bwd_t(const Prob& p, const float* L, const float* Llo, const float* A,
+                              const float* dA, float* dLA, cudaStream_t st) {
   const size_t smem = (size_t)kGB * p.m * sizeof(float);
   static bool once = (allow_smem(k_gram_bwd<D>, (size_t)kGB * 1024 * sizeof(float)), true);
   (void)once;
   return launch("gram_bwd", k_gram_bwd<D>, dim3((p.m + kGB - 1) / kGB, p.BH), dim3(kThreads), smem,
-                st, L, A, dA, dLA, p.m, p.inv_lam, p.gauss() ? 1 : 0);
+                st, L, Llo, A, dA, dLA, p.m, p.inv_lam, p.gauss() ? 1 : 0);
 }
 
-cudaError_t run_gram_bwd(const Prob& p, const float* L, const float* A, const float* dA, float* dLA,
-                         cudaStream_t st) {
+cudaError_t run_gram_bwd(const Prob& p, const float* L, const float* Llo, const float* A,
+                         const float* dA, float* dLA, cudaStream_t st) {
   switch (p.d) {
-    case 16: return gram_bwd_t<16>(p, L, A, dA, dLA, st);
-    case 32: return gram_bwd_t<32>(p, L, A, dA, dLA, st);
-    case 64: return gram_bwd_t<64>(p, L, A, dA, dLA, st);
-    default: return gram_bwd_t<128>(p, L, A, dA, dLA, st);
+    case 16: return gram_bwd_t<16>(p, L, Llo, A, dA, dLA, st);
+    case 32: return gram_bwd_t<32>(p, L, Llo, A, dA, dLA, st);
+    case 64: return gram_bwd_t<64>(p, L, Llo, A, dA, dLA, st);
+    default: return gram_bwd_t<128>(p, L, Llo, A, dA, dLA, st);
   }
 }
 

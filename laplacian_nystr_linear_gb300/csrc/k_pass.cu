@@ -121,20 +121,26 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
     if constexpr (kTC) {
-      // W[a][c] += sum_j C[j][a] V[j][c] on the tensor cores (TF32; V is bf16, exact in TF32)
+      // W[a][c] += sum_j C[j][a] V[j][c] on the tensor cores as (C_hi + C_lo) V with
+      // the TF32 split of C (V is bf16, exact in TF32): W enters W-hat = X_T W, whose
+      // unconverged directions amplify a single TF32 rounding of C about a hundredfold
 #pragma unroll 2
       for (int k0 = 0; k0 < kTile; k0 += 8) {
-        uint32_t af[4];
-        af[0] = to_tf32(Cs[(k0 + tg) * 68 + wa + gq]);
-        af[1] = to_tf32(Cs[(k0 + tg) * 68 + wa + gq + 8]);
-        af[2] = to_tf32(Cs[(k0 + tg + 4) * 68 + wa + gq]);
-        af[3] = to_tf32(Cs[(k0 + tg + 4) * 68 + wa + gq + 8]);
+        const float cv[4] = {Cs[(k0 + tg) * 68 + wa + gq], Cs[(k0 + tg) * 68 + wa + gq + 8],
+                             Cs[(k0 + tg + 4) * 68 + wa + gq], Cs[(k0 + tg + 4) * 68 + wa + gq + 8]};
+        uint32_t ah[4], al[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          ah[i] = to_tf32(cv[i]);
+          al[i] = to_tf32(cv[i] - __uint_as_float(ah[i]));
+        }
 #pragma unroll
         for (int n = 0; n < NCT; ++n) {
           uint32_t bf[2];
           bf[0] = __float_as_uint(Vs[(k0 + tg) * row_stride(D) + wc + 8 * n + gq]);
           bf[1] = __float_as_uint(Vs[(k0 + tg + 4) * row_stride(D) + wc + 8 * n + gq]);
-          mma_16x8x8(acc[n], af, bf);
+          mma_16x8x8(acc[n], ah, bf);
+          mma_16x8x8(acc[n], al, bf);
         }
       }
     } else {
@@ -481,19 +487,30 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     __syncthreads();
     if constexpr (kTC) {
+      // O += Z W-hat on the tensor cores with both factors split into TF32 hi + lo
+      // (Z_hi W_hi + Z_hi W_lo + Z_lo W_hi): fp32-level accuracy
 #pragma unroll 2
       for (int k0 = 0; k0 < kTile; k0 += 8) {
-        uint32_t af[4];
-        af[0] = to_tf32(Pt[(wj + gq) * 68 + k0 + tg]);
-        af[1] = to_tf32(Pt[(wj + gq + 8) * 68 + k0 + tg]);
-        af[2] = to_tf32(Pt[(wj + gq) * 68 + k0 + tg + 4]);
-        af[3] = to_tf32(Pt[(wj + gq + 8) * 68 + k0 + tg + 4]);
+        const float zv[4] = {Pt[(wj + gq) * 68 + k0 + tg], Pt[(wj + gq + 8) * 68 + k0 + tg],
+                             Pt[(wj + gq) * 68 + k0 + tg + 4], Pt[(wj + gq + 8) * 68 + k0 + tg + 4]};
+        uint32_t ah[4], al[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          ah[i] = to_tf32(zv[i]);
+          al[i] = to_tf32(zv[i] - __uint_as_float(ah[i]));
+        }
 #pragma unroll
         for (int n = 0; n < NCT; ++n) {
-          uint32_t bf[2];
-          bf[0] = to_tf32(Ws[(k0 + tg) * row_stride(D) + wc + 8 * n + gq]);
-          bf[1] = to_tf32(Ws[(k0 + tg + 4) * row_stride(D) + wc + 8 * n + gq]);
-          mma_16x8x8(acc[n], af, bf);
+          const float w0 = Ws[(k0 + tg) * row_stride(D) + wc + 8 * n + gq];
+          const float w1 = Ws[(k0 + tg + 4) * row_stride(D) + wc + 8 * n + gq];
+          uint32_t bh[2], bl[2];
+          bh[0] = to_tf32(w0);
+          bh[1] = to_tf32(w1);
+          bl[0] = to_tf32(w0 - __uint_as_float(bh[0]));
+          bl[1] = to_tf32(w1 - __uint_as_float(bh[1]));
+          mma_16x8x8(acc[n], ah, bh);
+          mma_16x8x8(acc[n], ah, bl);
+          mma_16x8x8(acc[n], al, bh);
         }
       }
     } else {
@@ -905,11 +922,11 @@ __global__ void k_reduce_dl(const float* __restrict__ dLq, const float* __restri
   }
 }
 
-cudaError_t run_reduce_dl(const Prob& p, const float* dLq, const float* dLc, const float* dLA,
+cudaError_t run_reduce_dl(const Prob& p, int S, const float* dLq, const float* dLc, const float* dLA,
                           float* dL, cudaStream_t st) {
   const size_t n = (size_t)p.BH * p.m * p.d;
   return launch("reduce_dl", k_reduce_dl, dim3(grid_for(n)), dim3(kThreads), 0, st, dLq, dLc, dLA, dL,
-                p.BH, p.Sb, p.m, p.mp, p.d);
+                p.BH, S, p.m, p.mp, p.d);
 }
 
 // token gradients: sum the per-landmark-tile partials in tile order, add the
@@ -954,6 +971,65 @@ __global__ void k_finalize(const float* __restrict__ dQp, const float* __restric
     }
     st4(dv + e, v4);
   }
+}
+
+// token gradients of the tensor-core backward: dK = the sum of its nk partial
+// planes (landmark groups, in order) plus the pooling path dL[a(n)] / window size;
+// dQ the sum of its nq planes (nq = 0: dq was written by the tile kernel); dV
+// one fp32 plane; tied: dq = dQ + dK; all converted to the tensor type.
+template <typename T>
+__global__ void k_finalize_tc(const float* __restrict__ dQp, const float* __restrict__ dKp,
+                              const float* __restrict__ dVp, const float* __restrict__ dL,
+                              T* __restrict__ dq, T* __restrict__ dk, T* __restrict__ dv, int BH,
+                              int N, int d, int nq, int nk, int m, int gh, int gw, int mh, int mw,
+                              int tied) {
+  const size_t total4 = (size_t)BH * N * d / 4;
+  const size_t plane = (size_t)BH * N * d;
+  for (size_t e4 = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e4 < total4;
+       e4 += (size_t)gridDim.x * blockDim.x) {
+    const size_t e = e4 * 4;
+    const size_t row = e / d;
+    const int c = (int)(e % d);
+    const int n = (int)(row % N);
+    const size_t bh = row / N;
+    float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f), k4 = q4;
+    for (int t = 0; t < nq; ++t) {
+      const float4 a = *reinterpret_cast<const float4*>(dQp + t * plane + e);
+      q4.x += a.x; q4.y += a.y; q4.z += a.z; q4.w += a.w;
+    }
+    for (int t = 0; t < nk; ++t) {
+      const float4 b = *reinterpret_cast<const float4*>(dKp + t * plane + e);
+      k4.x += b.x; k4.y += b.y; k4.z += b.z; k4.w += b.w;
+    }
+    const int y = n / gw, x = n % gw;
+    const int wi = ((y + 1) * mh - 1) / gh, wj = ((x + 1) * mw - 1) / gw;
+    const int a = wi * mw + wj;
+    const float inv = 1.0f / (float)(((wi + 1) * gh / mh - wi * gh / mh) *
+                                     ((wj + 1) * gw / mw - wj * gw / mw));
+    const float4 l4 = *reinterpret_cast<const float4*>(dL + (bh * m + a) * d + c);
+    k4.x += l4.x * inv; k4.y += l4.y * inv; k4.z += l4.z * inv; k4.w += l4.w * inv;
+    if (tied) {
+      q4.x += k4.x; q4.y += k4.y; q4.z += k4.z; q4.w += k4.w;
+      st4(dq + e, q4);
+    } else {
+      if (nq > 0) st4(dq + e, q4);
+      st4(dk + e, k4);
+    }
+    st4(dv + e, *reinterpret_cast<const float4*>(dVp + e));
+  }
+}
+
+cudaError_t run_finalize_tc(const Prob& p, int nq, const float* dQp, int nk, const float* dKp,
+                            const float* dVp, const float* dL, void* dq, void* dk, void* dv,
+                            cudaStream_t st) {
+  const size_t n4 = (size_t)p.BH * p.N * p.d / 4;
+  if (p.dtype == 1)
+    return launch("finalize", k_finalize_tc<__nv_bfloat16>, dim3(grid_for(n4)), dim3(kThreads), 0,
+                  st, dQp, dKp, dVp, dL, (__nv_bfloat16*)dq, (__nv_bfloat16*)dk, (__nv_bfloat16*)dv,
+                  p.BH, p.N, p.d, nq, nk, p.m, p.gh, p.gw, p.mh, p.mw, p.tied);
+  return launch("finalize", k_finalize_tc<float>, dim3(grid_for(n4)), dim3(kThreads), 0, st, dQp,
+                dKp, dVp, dL, (float*)dq, (float*)dk, (float*)dv, p.BH, p.N, p.d, nq, nk, p.m, p.gh,
+                p.gw, p.mh, p.mw, p.tied);
 }
 
 cudaError_t run_finalize(const Prob& p, const float* dQp, const float* dKp, const float* dVp,

@@ -25,6 +25,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc.cuh"
 
 __device__ int g_lapnys_wait_error;  // nonzero once a bounded wait expired
 
@@ -383,18 +384,34 @@ cudaError_t run_tcgemm(bool ta, bool tb, int batch, int M, int N, int K, const f
   return cudaErrorInvalidValue;
 }
 
+// Self-test of the bounded waits: one thread initialises an mbarrier that
+// expects one arrival, which nothing makes, and waits on its first phase with
+// the same bounded wait the tensor-core kernels use (at most `polls` polls).  The
+// wait expires, the error word is set, and the kernel returns: nothing is in
+// flight (no copy, no MMA, no TMEM), so the context stays usable.
+__global__ void k_wait_selftest(int polls) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  const uint32_t a = tc::smem_u32(&bar);
+  tc::mbar_init(a, 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  if (!tc::mbar_wait(a, 0u, polls)) atomicExch(&g_lapnys_wait_error, 1);
+}
+
+int tc_wait_limit() { return tc::kWaitLimit; }
+
+cudaError_t run_wait_selftest(int polls, cudaStream_t st) {
+  return launch("wait_selftest", k_wait_selftest, dim3(1), dim3(32), 0, st, polls);
+}
+
+// The address of the error word in the current context, looked up on every
+// call: a symbol's device address belongs to a context (a reset device or a
+// second context on the same device has its own copy), so caching it per
+// device ordinal could hand a kernel a dead address.
 int* wait_error_address() {
-  static std::mutex mu;
-  static int* addr[64] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_lapnys_wait_error) != cudaSuccess) return nullptr;
-    addr[dev] = static_cast<int*>(p);
-  }
-  return addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_lapnys_wait_error) != cudaSuccess) return nullptr;
+  return static_cast<int*>(p);
 }
 
 int read_wait_error(bool clear) {

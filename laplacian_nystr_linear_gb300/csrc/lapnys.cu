@@ -23,6 +23,7 @@ struct Rec {
   cudaEvent_t a, b;
 };
 bool g_prof = false;
+bool g_serial = false;  // profile mode 2: everything on the caller's stream
 std::vector<Rec> g_rec;
 int g_used = 0;
 uint64_t g_launches = 0;
@@ -130,11 +131,13 @@ static Prob make_prob(int B, int H, int N, int d, int gh, int gw, int m, float l
   p.Sb = p.Sk;
   // sized from the shape alone (the workspace query takes no dtype); used for bf16
   p.Skt = fwd_tc_shape(d, m) ? key_tc_splits(p.BH, m, p.nblk) : 0;
+  // splits of the tensor-core backward (bf16, d = 64); sized from the shape alone
+  p.Stc = bwd_tc_splits(p.BH, m, N);
   return p;
 }
 
 struct CtxLayout {
-  size_t L, A, alpha, X, Y, W, What, stats, idx, P, C, total;
+  size_t L, Llo, A, alpha, X, Y, W, What, stats, idx, P, C, total;
   int nx, ny;
 };
 
@@ -145,6 +148,7 @@ static CtxLayout ctx_layout(int BH, int N, int d, int m, int iters, bool full) {
   const size_t f = sizeof(float);
   size_t o = 0;
   c.L = o; o = align256(o + (size_t)BH * m * d * f);
+  c.Llo = o; o = align256(o + (size_t)BH * m * d * f);
   c.A = o; o = align256(o + (size_t)BH * m * m * f);
   c.alpha = o; o = align256(o + (size_t)BH * 4 * f);
   c.X = o; o = align256(o + (size_t)BH * c.nx * m * m * f);
@@ -175,15 +179,16 @@ static WsLayout ws_layout(const Prob& p) {
   WsLayout w;
   const size_t f = sizeof(float);
   const size_t BH = p.BH, m = p.m, d = p.d, mp = p.mp;
+  const size_t Sb = (size_t)(p.Stc > p.Sb ? p.Stc : p.Sb);  // either backward's splits
   size_t o = 0;
   w.lite = o; o = align256(o + ctx_layout(p.BH, p.N, p.d, p.m, p.iters, false).total);
   w.kpart = o; o = align256(o + BH * (p.Skt > p.Sk ? p.Skt : p.Sk) * mp * d * f);
   w.spart = o; o = align256(o + BH * p.Sq * 3 * mp * f);
   w.fpack = o; o = align256(o + (p.Skt > 0 ? pack_q_floats(p) * f : 0));
-  w.dWhp = o; o = align256(o + BH * p.Sb * mp * d * f);
-  w.dLqp = o; o = align256(o + BH * p.Sb * mp * d * f);
-  w.dLcp = o; o = align256(o + BH * p.Sb * mp * d * f);
-  w.nsp = o; o = align256(o + BH * p.Sb * 2 * mp * f);
+  w.dWhp = o; o = align256(o + BH * Sb * mp * d * f);
+  w.dLqp = o; o = align256(o + BH * Sb * mp * d * f);
+  w.dLcp = o; o = align256(o + BH * Sb * mp * d * f);
+  w.nsp = o; o = align256(o + BH * Sb * 2 * mp * f);
   w.mdz = o; o = align256(o + BH * 2 * mp * f);
   const size_t tok = (size_t)p.nt * BH * p.N * d * f;
   w.dQp = o; o = align256(o + tok);
@@ -308,6 +313,7 @@ std::mutex g_side_init_mu;
 // the current device's side stream and events, created on first use; null if
 // they cannot be created (the caller then stays on one stream)
 Side* side() {
+  if (g_serial) return nullptr;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxSideDevices) return nullptr;
   Side& sd = g_side[dev];
@@ -339,30 +345,21 @@ cudaError_t join(cudaStream_t to, cudaStream_t from, cudaEvent_t ev) {
 // 32 MiB of device memory per GPU that loads this library, held until exit.
 // Host code must not hand the array's name to a kernel (on the host it is a
 // stand-in, not a device address): lapnys_fwd_static looks the device address
-// up once per device with cudaGetSymbolAddress, with that device current.
+// up with cudaGetSymbolAddress on every call, with the caller's device and
+// context current.  The address belongs to a context, not to a device ordinal
+// (a reset device or another context on the same device has its own copy), so
+// nothing is cached; the lookup is a host-side query that allocates nothing.
 // ---------------------------------------------------------------------------
 static constexpr size_t kStaticScratchBytes = (size_t)32 << 20;
 static __device__ __align__(256) unsigned char g_fwd_scratch[kStaticScratchBytes];
 
 namespace {
-constexpr int kMaxScratchDevices = 256;
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxScratchDevices];  // device address per device ordinal, set on first use
-
-// address of g_fwd_scratch on the current device (first call per device looks it up)
+// address of g_fwd_scratch in the current context
 cudaError_t static_scratch(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* ptr = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&ptr, g_fwd_scratch);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxScratchDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (g_scratch_addr[dev] == nullptr) {
-    void* ptr = nullptr;
-    e = cudaGetSymbolAddress(&ptr, g_fwd_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = ptr;
-  }
-  *out = g_scratch_addr[dev];
+  *out = ptr;
   return cudaSuccess;
 }
 }  // namespace
@@ -402,7 +399,7 @@ int lapnys_ctx_offsets(int B, int H, int N, int d, int m, int iters, unsigned fl
   (void)flags;
   if (out == nullptr || !dims_ok(B, H, N, d, m, iters)) return LAPNYS_EINVAL;
   const CtxLayout c = ctx_layout(B * H, N, d, m, iters, true);
-  out->L = c.L; out->A = c.A; out->alpha = c.alpha; out->X = c.X; out->Y = c.Y;
+  out->L = c.L; out->Llo = c.Llo; out->A = c.A; out->alpha = c.alpha; out->X = c.X; out->Y = c.Y;
   out->W = c.W; out->What = c.What; out->stats = c.stats; out->idx = c.idx; out->P = c.P;
   out->C = c.C; out->total = c.total;
   return LAPNYS_OK;
@@ -414,7 +411,7 @@ int lapnys_pool(const void* k, float* L, int32_t* idx, int B, int H, int N, int 
   if (rc != LAPNYS_OK) return rc;
   if (k == nullptr || L == nullptr || !aligned16(k) || !aligned16(L)) return LAPNYS_EINVAL;
   Prob p = make_prob(B, H, N, d, grid_h, grid_w, m, 1.f, 0.f, 0, 0, dtype, 0);
-  CK(run_pool(p, k, L, idx, stream));
+  CK(run_pool(p, k, L, nullptr, idx, stream));
   return LAPNYS_OK;
 }
 
@@ -443,6 +440,7 @@ int lapnys_fwd(const void* q, const void* k, const void* v, void* out, int B, in
   char* cb = full ? (char*)ctx : (char*)ws + w.lite;
   char* wb = (char*)ws;
   float* L = (float*)(cb + c.L);
+  float* Llo = (float*)(cb + c.Llo);
   float* A = (float*)(cb + c.A);
   float* alpha = (float*)(cb + c.alpha);
   float* X = (float*)(cb + c.X);
@@ -453,7 +451,7 @@ int lapnys_fwd(const void* q, const void* k, const void* v, void* out, int B, in
   int32_t* idx = (int32_t*)(cb + c.idx);
   const long mm = (long)m * m;
 
-  CK(run_pool(p, k, L, idx, stream));
+  CK(run_pool(p, k, L, Llo, idx, stream));
   // the solver (landmark matrix, alpha, Newton-Schulz) on the side stream,
   // queued first so that its CTAs take their SMs at once; the key pass on this
   // stream meanwhile; both end before W-hat = X_T W
@@ -531,6 +529,7 @@ int lapnys_fwd_static(const void* q, const void* k, const void* v, void* out, in
   char* cb = (char*)ws + w.lite;
   char* wb = (char*)ws;
   float* L = (float*)(cb + c.L);
+  float* Llo = (float*)(cb + c.Llo);
   float* A = (float*)(cb + c.A);
   float* alpha = (float*)(cb + c.alpha);
   float* X = (float*)(cb + c.X);
@@ -542,7 +541,7 @@ int lapnys_fwd_static(const void* q, const void* k, const void* v, void* out, in
   const long mm = (long)m * m;
   // every scratch region below is fully written before it is read, so nothing
   // left over from an earlier call needs clearing
-  CK(run_pool(p, k, L, idx, stream));
+  CK(run_pool(p, k, L, Llo, idx, stream));
   if (m <= kTile) {
     CK(run_ns_small(p, L, A, alpha, X, Y, c.nx, c.ny, stream));
   } else {
@@ -613,6 +612,7 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
   const char* cb = (const char*)ctx;
   char* wb = (char*)ws;
   const float* L = (const float*)(cb + c.L);
+  const float* Llo = (const float*)(cb + c.Llo);
   const float* A = (const float*)(cb + c.A);
   const float* alpha = (const float*)(cb + c.alpha);
   const float* X = (const float*)(cb + c.X);
@@ -649,10 +649,17 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
     if (!tied_qk) CK(run_ties(p, k, wb + w.tie_scratch, ties_k, stream));
   }
 
+  // the bf16, d = 64 backward finishes each token's gradient in one CTA per
+  // group of 256 landmarks (tensor-core dot products, no per-tile partials)
+  const bool tcb = bwd_tc_shape(p.dtype, d);
+  const int ng = bwd_tc_groups(m);
+  const int Sl = tcb ? p.Stc : p.Sb;  // splits of the landmark-side partials
+  const bool dq_direct = tcb && !tied_qk && ng == 1;
+
   // ---- query side ----
   BwdArgs qa;
   memset(&qa, 0, sizeof(qa));
-  qa.X = q; qa.U = dout; qa.L = L; qa.R = What; qa.stats = stats; qa.mdz = mdz;
+  qa.X = q; qa.U = dout; qa.L = L; qa.Llo = Llo; qa.R = What; qa.stats = stats; qa.mdz = mdz;
   qa.tok_part = dQp; qa.lm_part = dLqp; qa.lm_part2 = dWhp; qa.ns_part = nsp; qa.ties = ties_q;
   qa.kv = (const float*)(cb + c.P);
   if (p.norm()) {
@@ -660,8 +667,18 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
     CK(run_mdz(p, nsp, mdz, stream));
     CK(run_reduce_parts(p.BH, p.Sb, m, p.mp, d, dWhp, dWh, stream));
   }
-  CK(run_bwd_pair(p, 1, qa, stream));
-  if (!p.norm()) CK(run_reduce_parts(p.BH, p.Sb, m, p.mp, d, dWhp, dWh, stream));
+  if (tcb) {
+    BwdTcArgs qt;
+    memset(&qt, 0, sizeof(qt));
+    qt.X = q; qt.U = dout; qt.L = L; qt.Llo = Llo; qt.R = What; qt.stats = stats; qt.mdz = mdz;
+    qt.kv = (const float*)(cb + c.P); qt.ties = ties_q; qt.out = dq_direct ? dq : nullptr;
+    qt.tok_part = dQp; qt.lm_part = dLqp; qt.lm_part2 = dWhp; qt.S = p.Stc;
+    CK(run_bwd_tc(p, 1, qt, stream));
+    if (!p.norm()) CK(run_reduce_parts(p.BH, p.Stc, m, p.mp, d, dWhp, dWh, stream));
+  } else {
+    CK(run_bwd_pair(p, 1, qa, stream));
+    if (!p.norm()) CK(run_reduce_parts(p.BH, p.Sb, m, p.mp, d, dWhp, dWh, stream));
+  }
 
   // ---- G = dLoss/dX_T = dW-hat W^T and dW = X_T^T dW-hat ----
   const float* XT = X + (long)iters * mm;
@@ -714,18 +731,34 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
     }
     CK(run_alpha_bwd(p, A, alpha, Sc, dA, ss));
   }
-  CK(run_gram_bwd(p, L, A, dA, dLA, ss));
+  CK(run_gram_bwd(p, L, Llo, A, dA, dLA, ss));
 
   // ---- key side ----
-  BwdArgs ka;
-  memset(&ka, 0, sizeof(ka));
-  ka.X = k; ka.U = v; ka.L = L; ka.R = dW;
-  ka.tok_part = dKp; ka.tok_part2 = dVp; ka.lm_part = dLcp; ka.ties = ties_k;
-  ka.kv = (const float*)(cb + c.C);
-  CK(run_bwd_pair(p, 2, ka, stream));
+  if (tcb) {
+    BwdTcArgs kt;
+    memset(&kt, 0, sizeof(kt));
+    kt.X = k; kt.U = v; kt.L = L; kt.Llo = Llo; kt.R = dW;
+    kt.kv = (const float*)(cb + c.C); kt.ties = ties_k; kt.out = nullptr;
+    kt.tok_part = dKp; kt.lm_part = dLcp; kt.S = p.Stc;
+    CK(run_bwd_tc(p, 2, kt, stream));
+    // dV = C dW, with the kernel values C the forward kept (token-major [N][mp])
+    const float* Cm = (const float*)(cb + c.C);
+    CK(ns_mm(p, false, false, N, d, m, Cm, p.mp, (long)N * p.mp, dW, d, md, dVp, d, (long)N * d,
+             nullptr, d, 0, 1.f, 0.f, stream));
+  } else {
+    BwdArgs ka;
+    memset(&ka, 0, sizeof(ka));
+    ka.X = k; ka.U = v; ka.L = L; ka.Llo = Llo; ka.R = dW;
+    ka.tok_part = dKp; ka.tok_part2 = dVp; ka.lm_part = dLcp; ka.ties = ties_k;
+    ka.kv = (const float*)(cb + c.C);
+    CK(run_bwd_pair(p, 2, ka, stream));
+  }
   if (sd) CK(join(stream, ss, sd->ev[1]));
-  CK(run_reduce_dl(p, dLqp, dLcp, dLA, dL, stream));
-  CK(run_finalize(p, dQp, dKp, dVp, dL, dq, dk, dv, stream));
+  CK(run_reduce_dl(p, Sl, dLqp, dLcp, dLA, dL, stream));
+  if (tcb)
+    CK(run_finalize_tc(p, dq_direct ? 0 : ng, dQp, ng, dKp, dVp, dL, dq, dk, dv, stream));
+  else
+    CK(run_finalize(p, dQp, dKp, dVp, dL, dq, dk, dv, stream));
   return LAPNYS_OK;
 }
 
@@ -752,6 +785,12 @@ int lapnys_matmul(const float* A, const float* B, const float* E, float* C, int 
   return LAPNYS_OK;
 }
 
+int lapnys_wait_selftest(int polls, cudaStream_t stream) {
+  if (polls < 1 || polls > tc_wait_limit()) return LAPNYS_EINVAL;
+  CK(run_wait_selftest(polls, stream));
+  return LAPNYS_OK;
+}
+
 int lapnys_device_status(int clear) {
   if (cudaDeviceSynchronize() != cudaSuccess) return LAPNYS_ECUDA;
   const int v = read_wait_error(clear != 0);
@@ -762,8 +801,20 @@ int lapnys_device_status(int clear) {
 uint64_t lapnys_launch_count(void) { return g_launches; }
 
 int lapnys_profile_enable(int on) {
+  if (on < 0 || on > 2) return LAPNYS_EINVAL;
   g_prof = on != 0;
+  g_serial = on == 2;
   g_used = 0;
+  return LAPNYS_OK;
+}
+
+int lapnys_fma_probe(int paired, int iters, float* sink, unsigned long long* lane_ops,
+                     cudaStream_t stream) {
+  if ((paired != 0 && paired != 1) || iters < 1 || iters > (1 << 24) || !sink || !lane_ops)
+    return LAPNYS_EINVAL;
+  unsigned long long n = 0;
+  CK(run_fma_probe(paired != 0, iters, sink, &n, stream));
+  *lane_ops = n;
   return LAPNYS_OK;
 }
 

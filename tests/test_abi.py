@@ -222,3 +222,26 @@ def test_static_forward_and_pool_reject_bad_arguments(lib):
     assert lib.lapnys_pool(FAKE, FAKE, None, 1, 1, 195, 32, 14, 14, 49, 0, None) == LAPNYS_EINVAL
     assert lib.lapnys_pool(None, FAKE, None, 1, 1, 196, 32, 14, 14, 49, 0, None) == LAPNYS_EINVAL
     assert lib.lapnys_pool(FAKE, FAKE, None, 1, 1, 196, 32, 14, 14, 225, 0, None) == LAPNYS_EINVAL
+
+
+def test_wait_selftest_rejects_poll_counts_out_of_range(lib):
+    from laplacian_nystr_linear_gb300 import _lib
+    before = lib.lapnys_launch_count()
+    assert lib.lapnys_wait_selftest(0, None) == _lib.LAPNYS_EINVAL
+    assert lib.lapnys_wait_selftest(-5, None) == _lib.LAPNYS_EINVAL
+    assert lib.lapnys_wait_selftest((1 << 22) + 1, None) == _lib.LAPNYS_EINVAL
+    assert lib.lapnys_launch_count() == before
+
+
+def test_instrumentation_rejects_bad_arguments(lib):
+    import ctypes as ct
+    from laplacian_nystr_linear_gb300 import _lib
+    assert lib.lapnys_profile_enable(3) == _lib.LAPNYS_EINVAL
+    assert lib.lapnys_profile_enable(-1) == _lib.LAPNYS_EINVAL
+    assert lib.lapnys_profile_enable(0) == _lib.LAPNYS_OK
+    n = ct.c_ulonglong(0)
+    before = lib.lapnys_launch_count()
+    assert lib.lapnys_fma_probe(2, 10, ct.c_void_p(16), ct.byref(n), None) == _lib.LAPNYS_EINVAL
+    assert lib.lapnys_fma_probe(0, 0, ct.c_void_p(16), ct.byref(n), None) == _lib.LAPNYS_EINVAL
+    assert lib.lapnys_fma_probe(0, 10, None, ct.byref(n), None) == _lib.LAPNYS_EINVAL
+    assert lib.lapnys_launch_count() == before

@@ -109,7 +109,7 @@ def test_tensor_core_forward_intermediates(w):
     print(w.name, compare(w, g, o, backward=True))
     for (b, h), s in o["saved"].items():
         c = g["ctx"]
-        assert rel(c["W"][b, h], s["W"]) < 1e-3          # C V with C rounded to TF32
+        assert rel(c["W"][b, h], s["W"]) < 1e-5          # C V with C as three bf16 planes
         assert rel(c["P"][b, h], s["P"]) < 1e-6          # kernel values stored as computed
         assert rel(c["C"][b, h], s["C"].T) < 1e-6
 
