@@ -15,7 +15,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblapnys.so")
 SOURCES = ["lapnys.cu", "k_landmark.cu", "k_gemm.cu", "k_pass.cu", "k_bwd.cu", "k_gemm2.cu", "k_tcgemm.cu",
            "k_ties.cu", "k_nscluster.cu", "k_fwd_tc.cu", "k_gauss_tc.cu", "k_block.cu",
-           "k_probe.cu", "k_bwd_tc.cu"]
+           "k_probe.cu", "k_bwd_tc.cu", "k_dv.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "internal.h", "tc.cuh")] + [
     os.path.join(ROOT, "include", "lapnys.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

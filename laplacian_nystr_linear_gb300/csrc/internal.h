@@ -2,6 +2,7 @@
 // launch counting and optional per-launch CUDA-event timing, and the launch
 // functions each translation unit provides.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -118,6 +119,16 @@ int* wait_error_address();
 cudaError_t run_wait_selftest(int polls, cudaStream_t st);
 // polls of the bounded waits in the tensor-core kernels
 int tc_wait_limit();
+// the driver's tensor-map encoder (looked up through the runtime; null when the
+// driver lacks it) and a tiled fp32 map: dims / strides (bytes, rank - 1 of
+// them) / box as for cuTensorMapEncodeTiled, no swizzle, zero fill out of bounds
+void* tensor_map_encoder();
+bool encode_tiled_f32(CUtensorMap* t, int rank, const void* p, const cuuint64_t* dim,
+                      const cuuint64_t* stride, const cuuint32_t* box);
+// dV = C dW for bf16 tokens (d = 32 / 64) from the kept kernel values C
+// [BH][N][mp] and dW [BH][m][d]; writes dv [BH][N][d] in bf16
+bool dv_tc_ok(const Prob& p);
+cudaError_t run_dv(const Prob& p, const float* C, const float* dW, void* dv, cudaStream_t st);
 // FP32 FMA-rate probe: a grid of 8 CTAs of 256 threads per SM, each thread
 // `iters` x 8 independent FMAs (paired: fma.rn.f32x2, two lane-ops each);
 // *lane_ops = the FP32 lane-ops the launch executes

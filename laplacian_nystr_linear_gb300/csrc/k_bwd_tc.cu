@@ -150,6 +150,8 @@ __global__ void __launch_bounds__(NTH, 1) k_bwd_tc(BtcArgs a) {
   __shared__ __align__(8) uint64_t wdone;         // dW-hat MMAs of a block done
   __shared__ uint32_t tmem_s;
   __shared__ float gsum_s[TJ];                    // G_j of the block
+  __shared__ float colg_s[NTH];                   // per-thread G'_a partials (g phase)
+  __shared__ float nc_s[NORM ? 4 * MC : 1];       // mu, rs, mean dZ, mean dZ Z per landmark
   __shared__ uint32_t tie_s[kTieRec];             // the block's tie record
 
   const int sp = blockIdx.x, gi = blockIdx.y, bh = blockIdx.z;
@@ -210,15 +212,17 @@ __global__ void __launch_bounds__(NTH, 1) k_bwd_tc(BtcArgs a) {
   const int tok0 = HF == 2 ? 8 * (wg >> 1) : 4 * wg;
   const int ag = 128 * ghf + 32 * q + lane;
   const bool gact = 32 * q < MC;                  // warp-uniform: this warp has landmarks
-  float mu = 0.f, rs = 0.f, m0 = 0.f, m1 = 0.f;
-  if (NORM && ag < mg) {
-    const float* stb = a.stats + (size_t)bh * 3 * a.m + abase;
-    mu = __ldg(stb + ag);
-    rs = __ldg(stb + 2 * a.m + ag);
-    m0 = __ldg(a.mdz + (size_t)bh * 2 * a.mp + abase + ag);
-    m1 = __ldg(a.mdz + (size_t)bh * 2 * a.mp + a.mp + abase + ag);
+  if (NORM) {
+    for (int e = tid; e < MC; e += NTH) {
+      const bool ok = e < mg;
+      const float* stb = a.stats + (size_t)bh * 3 * a.m + abase;
+      nc_s[e] = ok ? __ldg(stb + e) : 0.f;
+      nc_s[MC + e] = ok ? __ldg(stb + 2 * a.m + e) : 0.f;
+      nc_s[2 * MC + e] = ok ? __ldg(a.mdz + (size_t)bh * 2 * a.mp + abase + e) : 0.f;
+      nc_s[3 * MC + e] = ok ? __ldg(a.mdz + (size_t)bh * 2 * a.mp + a.mp + abase + e) : 0.f;
+    }
   }
-  float colg = 0.f;                               // G'_a over the fast-path blocks
+  colg_s[tid] = 0.f;                              // G'_a over the fast-path blocks
   // sign phase: feature c, landmarks gr * LPT .. gr * LPT + LPT - 1 of the group
   const int c = 32 * (warp % FWARPS) + lane, gr = warp / FWARPS;
   float l[LPT];
@@ -301,14 +305,25 @@ __global__ void __launch_bounds__(NTH, 1) k_bwd_tc(BtcArgs a) {
     }
   }
 
+  // tie record of the 32-token block that block b is half of: its header (all
+  // threads) and its tie words (thread k holds word k), loaded one block ahead so
+  // that the load's latency hides behind a block's work
+  auto rec_of = [&](int b) { return a.ties + ((size_t)bh * a.nblk + (b >> 1)) * kTieRec; };
+  uint32_t rh_n = 0u, tw_n = 0u;
+  if (!GAUSS && nb > 0) {
+    rh_n = __ldg(rec_of(b0));
+    if (tid >= 1 && tid < kTieRec) tw_n = __ldg(rec_of(b0) + tid);
+  }
   int i = 0;
   for (int b = b0; b < b1 && !abort; ++b, ++i) {
     const int st = i % NST, ds = i & 1;
     const int n0 = b * TJ, nv = min(TJ, a.N - n0);
     const uint8_t* sb = sm + S::St + st * S::kStage;
-    // the tie record of the 32-token block this block is half of
-    const uint32_t* rec = a.ties + ((size_t)bh * a.nblk + (b >> 1)) * kTieRec;
-    const uint32_t rh = GAUSS ? 0u : __ldg(rec);
+    const uint32_t rh = rh_n, tw = tw_n;
+    if (!GAUSS && b + 1 < b1) {
+      rh_n = __ldg(rec_of(b + 1));
+      if (tid >= 1 && tid < kTieRec) tw_n = __ldg(rec_of(b + 1) + tid);
+    }
     const bool exact = (rh & kTieExact) != 0;
     const int nties = exact ? 0 : (int)rh;
     // g of this block: buffer i & 1 (the previous block's g is still read by its
@@ -325,6 +340,9 @@ __global__ void __launch_bounds__(NTH, 1) k_bwd_tc(BtcArgs a) {
       const float* pr = reinterpret_cast<const float*>(sb + S::kPr);
       float* gs = gsb;
       float z[TPT];
+      float cg = 0.f;
+      const float mu = NORM ? nc_s[ag] : 0.f, rs = NORM ? nc_s[MC + ag] : 0.f;
+      const float m0 = NORM ? nc_s[2 * MC + ag] : 0.f, m1 = NORM ? nc_s[3 * MC + ag] : 0.f;
 #pragma unroll
       for (int t = 0; t < TPT; ++t) {
         const int j = tok0 + t;
@@ -343,8 +361,9 @@ __global__ void __launch_bounds__(NTH, 1) k_bwd_tc(BtcArgs a) {
         g = valid ? g : 0.f;
         z[t] = valid ? zz : 0.f;
         gs[j * MC + ag] = g;
-        if (!exact) colg += g;
+        cg += g;
       }
+      if (!exact) colg_s[tid] += cg;
       if constexpr (DW) {
         // Z^T as three bf16 planes z1 + z2 + z3 (row = landmark, k = token)
         const int r = ag & 127;
@@ -399,7 +418,7 @@ __global__ void __launch_bounds__(NTH, 1) k_bwd_tc(BtcArgs a) {
       abort = true;
       break;
     }
-    if (tid < kTieRec) tie_s[tid] = (tid >= 1 && tid <= nties) ? __ldg(rec + tid) : 0u;
+    if (tid < kTieRec) tie_s[tid] = (tid >= 1 && tid <= nties) ? tw : 0u;
     if (b + 1 < b1) ++ndot;
     if (DW) ++nw;
     if (tid == 0) {
@@ -576,8 +595,8 @@ __global__ void __launch_bounds__(NTH, 1) k_bwd_tc(BtcArgs a) {
   __syncthreads();
 
   // ---- landmark-side sums: G'_a over the threads of each landmark ----
-  float* colg_s = reinterpret_cast<float*>(sm + S::Ps);  // [4 / HF][MC]
-  if (gact) colg_s[(HF == 2 ? (wg >> 1) : wg) * MC + ag] = colg;
+  float* colg_m = reinterpret_cast<float*>(sm + S::Ps);  // [4 / HF][MC]
+  if (gact) colg_m[(HF == 2 ? (wg >> 1) : wg) * MC + ag] = colg_s[tid];
   __syncthreads();
   if (!abort) {
 #pragma unroll
@@ -589,7 +608,7 @@ __global__ void __launch_bounds__(NTH, 1) k_bwd_tc(BtcArgs a) {
         if (al >= mg) continue;
         float cg = 0.f;
 #pragma unroll
-        for (int k = 0; k < 4 / HF; ++k) cg += colg_s[k * MC + al];
+        for (int k = 0; k < 4 / HF; ++k) cg += colg_m[k * MC + al];
         const float v = h ? u.y : u.x;
         a.lm_part[(((size_t)bh * a.S + sp) * a.mp + abase + al) * D + c] =
             GAUSS ? 2.f * (v - cg * l[2 * p + h]) : 2.f * v - cg;

@@ -976,7 +976,8 @@ __global__ void k_finalize(const float* __restrict__ dQp, const float* __restric
 // token gradients of the tensor-core backward: dK = the sum of its nk partial
 // planes (landmark groups, in order) plus the pooling path dL[a(n)] / window size;
 // dQ the sum of its nq planes (nq = 0: dq was written by the tile kernel); dV
-// one fp32 plane; tied: dq = dQ + dK; all converted to the tensor type.
+// one fp32 plane (null: dv was written already); tied: dq = dQ + dK; all
+// converted to the tensor type.
 template <typename T>
 __global__ void k_finalize_tc(const float* __restrict__ dQp, const float* __restrict__ dKp,
                               const float* __restrict__ dVp, const float* __restrict__ dL,
@@ -1015,7 +1016,7 @@ __global__ void k_finalize_tc(const float* __restrict__ dQp, const float* __rest
       if (nq > 0) st4(dq + e, q4);
       st4(dk + e, k4);
     }
-    st4(dv + e, *reinterpret_cast<const float4*>(dVp + e));
+    if (dVp != nullptr) st4(dv + e, *reinterpret_cast<const float4*>(dVp + e));
   }
 }
 

@@ -741,10 +741,14 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
     kt.kv = (const float*)(cb + c.C); kt.ties = ties_k; kt.out = nullptr;
     kt.tok_part = dKp; kt.lm_part = dLcp; kt.S = p.Stc;
     CK(run_bwd_tc(p, 2, kt, stream));
-    // dV = C dW, with the kernel values C the forward kept (token-major [N][mp])
+    // dV = C dW, with the kernel values C the forward kept (token-major [N][mp]):
+    // bf16 directly when the streaming kernel applies, else through fp32 partials
     const float* Cm = (const float*)(cb + c.C);
-    CK(ns_mm(p, false, false, N, d, m, Cm, p.mp, (long)N * p.mp, dW, d, md, dVp, d, (long)N * d,
-             nullptr, d, 0, 1.f, 0.f, stream));
+    if (dv_tc_ok(p))
+      CK(run_dv(p, Cm, dW, dv, stream));
+    else
+      CK(ns_mm(p, false, false, N, d, m, Cm, p.mp, (long)N * p.mp, dW, d, md, dVp, d, (long)N * d,
+               nullptr, d, 0, 1.f, 0.f, stream));
   } else {
     BwdArgs ka;
     memset(&ka, 0, sizeof(ka));
@@ -756,7 +760,8 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
   if (sd) CK(join(stream, ss, sd->ev[1]));
   CK(run_reduce_dl(p, Sl, dLqp, dLcp, dLA, dL, stream));
   if (tcb)
-    CK(run_finalize_tc(p, dq_direct ? 0 : ng, dQp, ng, dKp, dVp, dL, dq, dk, dv, stream));
+    CK(run_finalize_tc(p, dq_direct ? 0 : ng, dQp, ng, dKp, dv_tc_ok(p) ? nullptr : dVp, dL, dq, dk,
+                       dv, stream));
   else
     CK(run_finalize(p, dQp, dKp, dVp, dL, dq, dk, dv, stream));
   return LAPNYS_OK;
