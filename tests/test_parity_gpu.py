@@ -323,6 +323,28 @@ def test_sparse_ties_are_corrected(m):
         assert n_corr >= (32 if x == "q" else (16 if m == 64 else 0)), (name, n_corr)
 
 
+@pytest.mark.parametrize("m", [16, 64, 256])
+def test_out_of_range_values_take_the_exact_path(m):
+    # The fast sign term (a saturated FMA with 2^64 scaling) is exact only for
+    # values in {0} u [2^-40, 2^60].  Head 0: three feature columns of K scaled by
+    # 2^-48, so landmarks of those columns fall below the range and every block
+    # of the slice takes the exact path.  Head 1: 5 % of the Q values replaced by
+    # bf16 values of size about 2^-45, so the blocks holding them take the exact
+    # path while the other blocks stay on the fast one.
+    w = _small("oor", dtype="bf16", grid_h=32, grid_w=32, m=m, d=64, iters=6)
+    w = dataclasses.replace(w, B=1, H=2)
+    inp = random_inputs(31 + m, 1, 2, w.N, w.d, "bf16")
+    for c in (5, 17, 40):
+        inp["k"][0, 0, :, c] = round_bf16(inp["k"][0, 0, :, c] * 2.0 ** -48)
+    rng = np.random.default_rng(m)
+    pick = rng.random((w.N, w.d)) < 0.05
+    tiny = round_bf16(rng.standard_normal((w.N, w.d)) * 2.0 ** -45)
+    inp["q"][0, 1][pick] = tiny[pick]
+    g = gpu_run(w, inp, backward=True)
+    o = oracle_run(w, inp, backward=True)
+    print(w.name, m, compare(w, g, o, backward=True))
+
+
 # ---------------------------------------------------------------------------
 # landmark grids beyond equal square windows: adaptive windows (the grid is not
 # divisible by the landmark grid) and non-square m
