@@ -576,8 +576,8 @@ def run_ours(args, rank, world, local_rank):
                    "d": w.d, "m": w.m, "iters": w.iters, "lambda": w.lam, "eps": w.eps,
                    "norm": w.norm, "norm_batch": w.norm_batch, "tied": w.tied,
                    "pass": "fwd+bwd",
-                   "block": ({"C": w.H * w.d, "projections": "cuBLAS bf16/fp32 GEMMs, fp32 "
-                              "accumulation", "e2e": "x, dy in; y, dx out"} if args.block else None),
+                   "block": ({"C": w.H * w.d, "projections": "tcgen05 bf16 GEMMs of this library, fp32 "
+                              "accumulation, head split and bias fused", "e2e": "x, dy in; y, dx out"} if args.block else None),
                    "l2": (f"inputs larger than L2 (Q, K, V, dO {in_bytes / 4e6:.0f} MB each, "
                           f"{L2_BYTES / 1e6:.0f} MB L2); no flush" if flush is None else
                           f"inputs {in_bytes / 1e6:.0f} MB < L2: {2 * L2_BYTES / 1e6:.0f} MB "

@@ -228,14 +228,17 @@ int lapnys_matmul(const float* A, const float* B, const float* E, float* C, int 
  *  - C a multiple of 8 (at most 65536), B*N*max(3*H*d, C) < 2^31; the
  *    attention arguments (H, N, d, grid, m, lambda, eps, iters, flags) follow
  *    lapnys_fwd's rules and return its status codes.
- *  - The projections are cuBLAS GEMMs with float32 accumulation (float32
- *    operands are not rounded to TF32); the first call on a device creates a
- *    cuBLAS handle there (cuBLAS's own small state), after which the calls
- *    allocate nothing: the GEMM workspace is part of `ws`.  Q, K, V, the
- *    projected outputs and every gradient are rounded once to `dtype`.
+ *  - The projections are this library's kernels with float32 accumulation:
+ *    bf16 on the tcgen05 tensor cores (bf16 operands read in place, also the
+ *    per-head tensors, with the bias, the rounding and the split into heads
+ *    in the product's epilogue and the bias gradients summed by the product);
+ *    float32 on the FP32 FMA pipe (plain fp32 products).  bf16 also needs
+ *    H*d to be a multiple of 8 (else LAPNYS_ENOTSUP).
+ *    The calls allocate nothing: every buffer is part of `ws` or ctx.  Q, K,
+ *    V, the projected outputs and every gradient are rounded once to `dtype`.
  *  - lapnys_block_fwd writes y; with ctx != NULL it also saves, in ctx, the
- *    attention context and the Q, K, V and concatenated head outputs that
- *    lapnys_block_bwd reads (ctx == NULL: inference, they live in ws).
+ *    attention context and the Q, K, V and head outputs that lapnys_block_bwd
+ *    reads (ctx == NULL: inference, they live in ws).
  *  - lapnys_block_bwd writes dx, dw_qkv, dw_o, and db_qkv / db_o unless NULL
  *    (column sums of the output gradients in a fixed order: deterministic).
  *  - Sizes: lapnys_block_ctx_bytes / lapnys_block_workspace_bytes (0 for

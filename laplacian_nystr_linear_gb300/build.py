@@ -15,15 +15,12 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblapnys.so")
 SOURCES = ["lapnys.cu", "k_landmark.cu", "k_gemm.cu", "k_pass.cu", "k_bwd.cu", "k_gemm2.cu", "k_tcgemm.cu",
            "k_ties.cu", "k_nscluster.cu", "k_fwd_tc.cu", "k_gauss_tc.cu", "k_block.cu",
-           "k_probe.cu", "k_bwd_tc.cu", "k_dv.cu"]
+           "k_probe.cu", "k_bwd_tc.cu", "k_dv.cu", "k_proj.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "internal.h", "tc.cuh")] + [
     os.path.join(ROOT, "include", "lapnys.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-# cuBLAS for the attention block's plain projection GEMMs (found at run time
-# through the toolkit's library directory)
-_CUDA_LIB = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(
-    shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"))), "lib64")
-LINK = ["-L" + _CUDA_LIB, "-Xlinker", "-rpath=" + _CUDA_LIB, "-lcublas"]
+# no library beyond the CUDA runtime: every product is this library's own kernel
+LINK: list = []
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "-I" + os.path.join(ROOT, "include")]
 

@@ -125,6 +125,47 @@ int tc_wait_limit();
 void* tensor_map_encoder();
 bool encode_tiled_f32(CUtensorMap* t, int rank, const void* p, const cuuint64_t* dim,
                       const cuuint64_t* stride, const cuuint32_t* box);
+// a tiled bf16 map with the 128-byte swizzle (box rows of 64 elements)
+bool encode_tiled_bf16_sw128(CUtensorMap* t, int rank, const void* p, const cuuint64_t* dim,
+                             const cuuint64_t* stride, const cuuint32_t* box);
+
+// ---- bf16 products of the attention block (k_proj.cu) ---------------------
+// Geometry: B batch entries of N tokens, embedding width C, H heads of d, S
+// projection blocks (3, or 2 when Q = K).  Operand sources (bf16):
+enum : int {
+  GOP_ROWS_K = 0,    // rows = tokens of [B][N][F], k = feature (contiguous)
+  GOP_HEADS_K = 1,   // rows = tokens, k = (s, h, c) of the S tensors [B][H][N][d]
+  GOP_W_K = 2,       // rows = n of a weight stored [n][k]
+  GOP_TOK_MN = 3,    // rows = features of [B][N][F], k = tokens
+  GOP_HEADS_MN = 4,  // rows = (s, h, c) of the tensors [B][H][N][d], k = tokens
+  GOP_W_MN = 5,      // rows = n of a weight stored [k][n]
+};
+// epilogues: bf16 to the per-head tensors (+ bias), bf16 rows [B N][n] (+ bias),
+// fp32 rows
+enum : int { GEP_HEADS = 0, GEP_ROWS = 1, GEP_F32 = 2 };
+struct GemmDims {
+  int B, N, C, H, d, S;
+};
+// the product's needs: C and H d multiples of 8, a tensor-map encoder
+bool gemm_bf16_ok(const GemmDims& g);
+// ... and for the per-head operands: d = 64 or 128 (a head row holds whole 64-wide
+// pieces)
+bool gemm_heads_ok(const GemmDims& g);
+// fp32 partial tiles the weight-gradient products need (the larger of the two)
+size_t gemm_wgrad_floats(const GemmDims& g);
+// D[tokens][Nn] = src (tokens x Kf) * w (Kf x Nn): src GOP_ROWS_K (src[0]) or
+// GOP_HEADS_K (src[s], Kf = s H d); w GOP_W_K or GOP_W_MN; epilogue epi into
+// out[] (GEP_HEADS: out[s] per block of H d columns), bias (bf16, Nn) or null
+cudaError_t run_gemm_rows(const char* name, const GemmDims& g, int src_kind,
+                          const void* const* src, int Kf, int w_kind, const void* w, int Nn,
+                          int epi, void* const* out, const void* bias, cudaStream_t st);
+// dw[Mf][Nn] = A^T B over all tokens (A: GOP_TOK_MN or GOP_HEADS_MN with Mf
+// features, B likewise with Nn), bf16; db[Nn] = the column sums of B (when not
+// null); part holds gemm_wgrad_floats(g) floats
+cudaError_t run_gemm_wgrad(const char* name, const GemmDims& g, int a_kind,
+                           const void* const* asrc, int Mf, int b_kind, const void* const* bsrc,
+                           int Nn, float* part, void* dw, void* db, cudaStream_t st);
+
 // dV = C dW for bf16 tokens (d = 32 / 64) from the kept kernel values C
 // [BH][N][mp] and dW [BH][m][d]; writes dv [BH][N][d] in bf16
 bool dv_tc_ok(const Prob& p);

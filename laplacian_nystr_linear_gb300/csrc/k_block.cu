@@ -7,16 +7,18 @@
 // plain multi-head layer: [Q | K | V] = X W_qkv + b_qkv, heads of d columns,
 // Y = concat_h(O_h) W_o + b_o.
 //
-// The six projections are plain dense GEMMs and go to cuBLAS (fp32
-// accumulation; no TF32 for float32 operands).  Everything between them is
-// HBM-bound layout work done by the kernels below: the [B*N][S*H*d] <->
-// [B][H][N][d] head transposes fused with the bias addition and the rounding
-// to the element type, and fixed-order column sums for the bias gradients.
-#include <cublas_v2.h>
-
+// The six projections are this library's own products.  bf16 layers: the
+// tcgen05 GEMM of k_proj.cu, which reads the per-head tensors [B][H][N][d] in
+// place and writes them from its epilogue (bias and rounding fused), so no head
+// transpose runs between the products, and which sums the bias gradients
+// through a row of ones; heads of d = 16 or 32 (a head row narrower than the
+// product's 64-wide pieces) go through the layout kernels below and the same
+// GEMM on row-major operands.  float32 layers: the FP32 FMA product
+// of k_gemm2.cu, with the layout kernels below: the [B*N][S*H*d] <-> [B][H][N][d] head
+// transposes fused with the bias addition and the rounding to the element type,
+// and fixed-order column sums for the bias gradients.
 #include <cmath>
 #include <cstring>
-#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -26,7 +28,6 @@ namespace lapnys {
 namespace {
 
 constexpr int kBlockThreads = 256;
-constexpr size_t kBlasWs = 32u << 20;  // cuBLAS workspace carved out of the caller's ws
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -274,51 +275,28 @@ cudaError_t colsum_t(const void* G, float* part, void* out, int rows, int cols, 
 #define DT_CALL(dtype, fn, ...) \
   ((dtype) == LAPNYS_BF16 ? fn<__nv_bfloat16>(__VA_ARGS__) : fn<float>(__VA_ARGS__))
 
-// ---- cuBLAS -----------------------------------------------------------------
-// One handle per device, created on first use; the stream and the workspace
-// (a slice of the caller's ws) are set for every call under the mutex.
-struct Blas {
-  cublasHandle_t h = nullptr;
-  std::mutex mu;
-};
-constexpr int kMaxDevices = 64;
-
-Blas* blas_for_current_device() {
-  static Blas handles[kMaxDevices];
-  static std::mutex create_mu;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> g(create_mu);
-  Blas* b = &handles[dev];
-  if (b->h == nullptr) {
-    if (cublasCreate(&b->h) != CUBLAS_STATUS_SUCCESS) {
-      b->h = nullptr;
-      return nullptr;
-    }
-    cublasSetMathMode(b->h, CUBLAS_DEFAULT_MATH);  // float32 stays float32 (no TF32)
-  }
-  return b;
-}
-
+// ---- fp32 products -----------------------------------------------------------
 // row-major C[M][N] (ldc) = op(A) op(B); op(A) is M x K (A stored K x M when ta),
-// op(B) is K x N (B stored N x K when tb); operands of type tab, C of type tc
-bool gemm_rm(cublasHandle_t h, bool ta, bool tb, int M, int N, int K, const void* A, int lda,
-             const void* B, int ldb, void* C, int ldc, cudaDataType tab, cudaDataType tc) {
-  const float one = 1.f, zero = 0.f;
-  // column-major view: C^T = op(B)^T op(A)^T, with the same transpose flags
-  return cublasGemmEx(h, tb ? CUBLAS_OP_T : CUBLAS_OP_N, ta ? CUBLAS_OP_T : CUBLAS_OP_N, N, M, K,
-                      &one, B, tab, ldb, A, tab, lda, &zero, C, tc, ldc, CUBLAS_COMPUTE_32F,
-                      CUBLAS_GEMM_DEFAULT) == CUBLAS_STATUS_SUCCESS;
+// op(B) is K x N (B stored N x K when tb), on the FP32 FMA product: plain fp32
+// arithmetic.  (The three-term TF32 split of the tensor-core product, about
+// 1e-6 relative per product, was measured against the fp64 oracle on a float32
+// layer: the attention's backward amplified the output projection's error and
+// dX = dQKV W_qkv^T cancels, so dX and dW_qkv missed the fp32 tolerance by 5x.)
+cudaError_t gemm_f32(bool ta, bool tb, int M, int N, int K, const void* A, int lda, const void* B,
+                     int ldb, void* C, int ldc, cudaStream_t st) {
+  return run_gemm2(ta, tb, false, 1, M, N, (const float*)A, lda, 0, (const float*)B, ldb, 0, K,
+                   nullptr, 0, 0, nullptr, 0, 0, 0, (float*)C, ldc, 0, nullptr, 0, 0, 1.f, 0.f, st);
 }
 
 // ---- sizes ------------------------------------------------------------------
 struct BlockLayout {
   // ctx: attention ctx, then the saved q, k (untied), v, and Ot [B*N][H*d]
   size_t c_attn, c_q, c_k, c_v, c_ot, c_total, attn_ctx;
-  // forward ws: f32 scratch, O, saved tensors when there is no ctx, attention ws, cuBLAS
-  size_t f_s32, f_o, f_lite, f_attn, f_blas, f_total;
-  // backward ws: f32 scratch, dO, dq, dk, dv, dqkv, column-sum partials, attention ws, cuBLAS
-  size_t b_s32, b_do, b_dq, b_dk, b_dv, b_dqkv, b_part, b_attn, b_blas, b_total;
+  // forward ws: f32 scratch, O, saved tensors when there is no ctx, attention ws
+  size_t f_s32, f_o, f_lite, f_attn, f_total;
+  // backward ws: f32 scratch, dO, dq, dk, dv, dqkv, column-sum partials, weight-gradient
+  // partials (bf16), attention ws
+  size_t b_s32, b_do, b_dq, b_dk, b_dv, b_dqkv, b_part, b_gpart, b_attn, b_total;
   size_t attn_ws;
 };
 
@@ -355,7 +333,6 @@ BlockLayout block_layout(int B, int N, int C, int H, int d, int m, int iters, in
   L.f_o = o; o = align256(o + head);
   L.f_lite = o; o = align256(o + saved);
   L.f_attn = o; o = align256(o + L.attn_ws);
-  L.f_blas = o; o = align256(o + kBlasWs + 256);
   L.f_total = o;
 
   o = 0;
@@ -366,24 +343,19 @@ BlockLayout block_layout(int B, int N, int C, int H, int d, int m, int iters, in
   L.b_dv = o; o = align256(o + head);
   L.b_dqkv = o; o = align256(o + rows * S * HD * es);
   L.b_part = o; o = align256(o + (size_t)row_ctas((int)rows, kRowsWide) * wide * 4);
+  const GemmDims g = {B, N, C, H, d, (int)S};
+  L.b_gpart = o; o = align256(o + (dtype == LAPNYS_BF16 ? gemm_wgrad_floats(g) * 4 : 0));
   L.b_attn = o; o = align256(o + L.attn_ws);
-  L.b_blas = o; o = align256(o + kBlasWs + 256);
   L.b_total = o;
   return L;
 }
 
 bool a16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
-// cuBLAS wants its workspace 256-byte aligned; the slice has 256 bytes of slack
-void* blas_ws(char* p) { return (void*)(((uintptr_t)p + 255) & ~(uintptr_t)255); }
 bool a16_or_null(const void* p) { return p == nullptr || a16(p); }
 
 #define CKB(x)                                   \
   do {                                           \
     if ((x) != cudaSuccess) return LAPNYS_ECUDA; \
-  } while (0)
-#define CKG(x)                    \
-  do {                            \
-    if (!(x)) return LAPNYS_ECUDA; \
   } while (0)
 
 }  // namespace
@@ -425,36 +397,61 @@ int lapnys_block_fwd(const void* x, const void* w_qkv, const void* b_qkv, const 
   const BlockLayout L = block_layout(B, N, C, H, d, m, iters, tied, dtype, flags);
   if (ws_bytes < L.f_total) return LAPNYS_ENOSPC;
   if (ctx != nullptr && ctx_bytes < L.c_total) return LAPNYS_ENOSPC;
-  Blas* bl = blas_for_current_device();
-  if (bl == nullptr) return LAPNYS_ECUDA;
 
   const int S = tied ? 2 : 3, HD = H * d;
   const int rows = B * N;
+  const GemmDims g = {B, N, C, H, d, S};
+  const bool bf = dtype == LAPNYS_BF16;
+  if (bf && !gemm_bf16_ok(g)) return LAPNYS_ENOTSUP;
+  const bool heads = bf && gemm_heads_ok(g);
   char* wb = (char*)ws;
   // saved tensors live in ctx for training, in ws for inference
   char* sb = ctx != nullptr ? (char*)ctx : wb + L.f_lite - L.c_q;
   void* q = sb + L.c_q;
   void* k = tied ? q : (void*)(sb + L.c_k);
   void* v = sb + L.c_v;
+  // the attention's output O as the output projection reads it: [B][H][N][d] in
+  // place (bf16 with per-head operands), else concatenated rows [B*N][H*d]
   void* ot = sb + L.c_ot;
   float* s32 = (float*)(wb + L.f_s32);
-  void* O = wb + L.f_o;
-  const cudaDataType tab = dtype == LAPNYS_BF16 ? CUDA_R_16BF : CUDA_R_32F;
+  void* O = heads ? ot : (void*)(wb + L.f_o);
 
-  std::lock_guard<std::mutex> lock(bl->mu);
-  CKG(cublasSetStream(bl->h, stream) == CUBLAS_STATUS_SUCCESS);
-  CKG(cublasSetWorkspace(bl->h, blas_ws(wb + L.f_blas), kBlasWs) == CUBLAS_STATUS_SUCCESS);
-  // [Q | K | V] = X W_qkv (+ b_qkv, in the head split)
-  CKG(gemm_rm(bl->h, false, false, rows, S * HD, C, x, C, w_qkv, S * HD, s32, S * HD, tab,
-              CUDA_R_32F));
-  CKB(DT_CALL(dtype, split_heads_t, s32, b_qkv, q, tied ? v : k, v, B, N, H, d, S, stream));
+  // [Q | K | V] = X W_qkv (+ b_qkv, split to heads)
+  const void* xs[1] = {x};
+  if (heads) {
+    void* dst[3] = {q, tied ? v : k, v};
+    CKB(run_gemm_rows("block_gemm_qkv", g, GOP_ROWS_K, xs, C, GOP_W_MN, w_qkv, S * HD, GEP_HEADS, dst, b_qkv,
+                      stream));
+  } else {
+    if (bf) {
+      void* dst[3] = {s32, nullptr, nullptr};
+      CKB(run_gemm_rows("block_gemm_qkv", g, GOP_ROWS_K, xs, C, GOP_W_MN, w_qkv, S * HD, GEP_F32, dst, nullptr,
+                        stream));
+    } else {
+      CKB(gemm_f32(false, false, rows, S * HD, C, x, C, w_qkv, S * HD, s32, S * HD, stream));
+    }
+    CKB(DT_CALL(dtype, split_heads_t, s32, b_qkv, q, tied ? v : k, v, B, N, H, d, S, stream));
+  }
   rc = lapnys_fwd(q, tied ? nullptr : k, v, O, B, H, N, d, grid_h, grid_w, m, lambda, eps, iters,
                   tied, stream, dtype, flags, ctx != nullptr ? (char*)ctx + L.c_attn : nullptr,
                   L.attn_ctx, wb + L.f_attn, L.attn_ws);
   if (rc != LAPNYS_OK) return rc;
   // Y = concat_h(O_h) W_o + b_o
+  void* ys[3] = {y, nullptr, nullptr};
+  if (heads) {
+    const void* os[1] = {ot};
+    CKB(run_gemm_rows("block_gemm_out", g, GOP_HEADS_K, os, HD, GOP_W_MN, w_o, C, GEP_ROWS, ys, b_o,
+                      stream));
+    return LAPNYS_OK;
+  }
   CKB(DT_CALL(dtype, merge_heads_t, O, nullptr, nullptr, ot, nullptr, B, N, H, d, 1, stream));
-  CKG(gemm_rm(bl->h, false, false, rows, C, HD, ot, HD, w_o, C, s32, C, tab, CUDA_R_32F));
+  if (bf) {
+    const void* os[1] = {ot};
+    CKB(run_gemm_rows("block_gemm_out", g, GOP_ROWS_K, os, HD, GOP_W_MN, w_o, C, GEP_ROWS, ys, b_o,
+                      stream));
+    return LAPNYS_OK;
+  }
+  CKB(gemm_f32(false, false, rows, C, HD, ot, HD, w_o, C, s32, C, stream));
   CKB(DT_CALL(dtype, bias_rows_t, s32, b_o, y, rows, C, stream));
   return LAPNYS_OK;
 }
@@ -473,11 +470,13 @@ int lapnys_block_bwd(const void* x, const void* w_qkv, const void* w_o, const vo
     return LAPNYS_EINVAL;
   const BlockLayout L = block_layout(B, N, C, H, d, m, iters, tied, dtype, flags);
   if (ws_bytes < L.b_total) return LAPNYS_ENOSPC;
-  Blas* bl = blas_for_current_device();
-  if (bl == nullptr) return LAPNYS_ECUDA;
 
   const int S = tied ? 2 : 3, HD = H * d;
   const int rows = B * N;
+  const GemmDims g = {B, N, C, H, d, S};
+  const bool bf = dtype == LAPNYS_BF16;
+  if (bf && !gemm_bf16_ok(g)) return LAPNYS_ENOTSUP;
+  const bool heads = bf && gemm_heads_ok(g);
   const char* cb = (const char*)ctx;
   const void* q = cb + L.c_q;
   const void* k = tied ? q : (const void*)(cb + L.c_k);
@@ -491,28 +490,67 @@ int lapnys_block_bwd(const void* x, const void* w_qkv, const void* w_o, const vo
   void* dv = wb + L.b_dv;
   void* dqkv = wb + L.b_dqkv;
   float* part = (float*)(wb + L.b_part);
-  const cudaDataType tab = dtype == LAPNYS_BF16 ? CUDA_R_16BF : CUDA_R_32F;
+  float* gpart = (float*)(wb + L.b_gpart);
+  const void* dys[1] = {dy};
+  const void* xs[1] = {x};
 
-  std::lock_guard<std::mutex> lock(bl->mu);
-  CKG(cublasSetStream(bl->h, stream) == CUBLAS_STATUS_SUCCESS);
-  CKG(cublasSetWorkspace(bl->h, blas_ws(wb + L.b_blas), kBlasWs) == CUBLAS_STATUS_SUCCESS);
-  // output projection: dO = dY W_o^T (to heads), dW_o = Ot^T dY, db_o = column sums of dY
-  CKG(gemm_rm(bl->h, false, true, rows, HD, C, dy, C, w_o, C, s32, HD, tab, CUDA_R_32F));
-  CKB(DT_CALL(dtype, split_heads_t, s32, nullptr, dO, nullptr, nullptr, B, N, H, d, 1, stream));
-  CKG(gemm_rm(bl->h, true, false, HD, C, rows, ot, HD, dy, C, dw_o, C, tab, tab));
-  if (db_o != nullptr) CKB(DT_CALL(dtype, colsum_t, dy, part, db_o, rows, C, stream));
+  // output projection: dO = dY W_o^T (to heads), dW_o = concat(O)^T dY, db_o = 1^T dY
+  if (heads) {
+    void* dst[3] = {dO, nullptr, nullptr};
+    CKB(run_gemm_rows("block_gemm_do", g, GOP_ROWS_K, dys, C, GOP_W_K, w_o, HD, GEP_HEADS, dst,
+                      nullptr, stream));
+    const void* os[1] = {ot};
+    CKB(run_gemm_wgrad("block_gemm_dwo", g, GOP_HEADS_MN, os, HD, GOP_TOK_MN, dys, C, gpart, dw_o,
+                       db_o, stream));
+  } else if (bf) {
+    void* dst[3] = {s32, nullptr, nullptr};
+    CKB(run_gemm_rows("block_gemm_do", g, GOP_ROWS_K, dys, C, GOP_W_K, w_o, HD, GEP_F32, dst,
+                      nullptr, stream));
+    CKB(DT_CALL(dtype, split_heads_t, s32, nullptr, dO, nullptr, nullptr, B, N, H, d, 1, stream));
+    const void* os[1] = {ot};
+    CKB(run_gemm_wgrad("block_gemm_dwo", g, GOP_TOK_MN, os, HD, GOP_TOK_MN, dys, C, gpart, dw_o,
+                       db_o, stream));
+  } else {
+    CKB(gemm_f32(false, true, rows, HD, C, dy, C, w_o, C, s32, HD, stream));
+    CKB(DT_CALL(dtype, split_heads_t, s32, nullptr, dO, nullptr, nullptr, B, N, H, d, 1, stream));
+    CKB(gemm_f32(true, false, HD, C, rows, ot, HD, dy, C, dw_o, C, stream));
+    if (db_o != nullptr) CKB(DT_CALL(dtype, colsum_t, dy, part, db_o, rows, C, stream));
+  }
   // the attention
   rc = lapnys_bwd(q, tied ? nullptr : k, v, dO, (const char*)ctx + L.c_attn, dq, dk, dv, B, H, N,
                   d, grid_h, grid_w, m, lambda, eps, iters, tied, stream, dtype, flags,
                   wb + L.b_attn, L.attn_ws);
   if (rc != LAPNYS_OK) return rc;
   // QKV projection: dqkv = [dQ | dK | dV], dW_qkv = X^T dqkv, db_qkv, dX = dqkv W_qkv^T
+  void* dxs[3] = {dx, nullptr, nullptr};
+  if (heads) {
+    const void* gs[3] = {dq, tied ? dv : dk, dv};
+    CKB(run_gemm_wgrad("block_gemm_dwqkv", g, GOP_TOK_MN, xs, C, GOP_HEADS_MN, gs, S * HD, gpart,
+                       dw_qkv, db_qkv,
+                       stream));
+    CKB(run_gemm_rows("block_gemm_dx", g, GOP_HEADS_K, gs, S * HD, GOP_W_K, w_qkv, C, GEP_ROWS, dxs,
+                      nullptr,
+                      stream));
+    return LAPNYS_OK;
+  }
+  if (bf) {
+    CKB(DT_CALL(dtype, merge_heads_t, dq, tied ? dv : dk, dv, dqkv, nullptr, B, N, H, d, S,
+                stream));
+    const void* gs[1] = {dqkv};
+    CKB(run_gemm_wgrad("block_gemm_dwqkv", g, GOP_TOK_MN, xs, C, GOP_TOK_MN, gs, S * HD, gpart,
+                       dw_qkv, db_qkv,
+                       stream));
+    CKB(run_gemm_rows("block_gemm_dx", g, GOP_ROWS_K, gs, S * HD, GOP_W_K, w_qkv, C, GEP_ROWS, dxs,
+                      nullptr,
+                      stream));
+    return LAPNYS_OK;
+  }
   CKB(DT_CALL(dtype, merge_heads_t, dq, tied ? dv : dk, dv, dqkv,
               db_qkv != nullptr ? part : nullptr, B, N, H, d, S, stream));
-  CKG(gemm_rm(bl->h, true, false, C, S * HD, rows, x, C, dqkv, S * HD, dw_qkv, S * HD, tab, tab));
+  CKB(gemm_f32(true, false, C, S * HD, rows, x, C, dqkv, S * HD, dw_qkv, S * HD, stream));
   if (db_qkv != nullptr)
     CKB(DT_CALL(dtype, colsum_final_t, part, db_qkv, rows, S * HD, stream));
-  CKG(gemm_rm(bl->h, false, true, rows, C, S * HD, dqkv, S * HD, w_qkv, S * HD, dx, C, tab, tab));
+  CKB(gemm_f32(false, true, rows, C, S * HD, dqkv, S * HD, w_qkv, S * HD, dx, C, stream));
   return LAPNYS_OK;
 }
 

@@ -64,6 +64,14 @@ CASES = [
     Case("bf16_tc", 2, 16, 16, 256, 4, 64, 128, dtype="bf16", iters=10),
     Case("bf16_tc_gauss_tied", 1, 16, 16, 64, 2, 32, 100, dtype="bf16", tied=True, kernel="gauss"),
     Case("f32_d128", 1, 8, 8, 128, 1, 128, 64, iters=6),
+    # bf16, per-head operands read in place: ragged token tiles (120 tokens), C = 72
+    # (a ragged K step, N tile and weight-gradient M tile)
+    Case("bf16_heads_ragged", 2, 10, 12, 72, 2, 64, 9, dtype="bf16"),
+    # bf16 with H d = 48 (not a multiple of 64): concatenated heads through the
+    # layout kernels and the same product on row-major operands
+    Case("bf16_rows_h3d16", 2, 8, 8, 48, 3, 16, 16, dtype="bf16", iters=6),
+    # bf16 with d = 128 (a 64-wide K step is half a head), no bias
+    Case("bf16_d128_nobias", 1, 8, 8, 128, 1, 128, 16, dtype="bf16", iters=6, bias=False),
 ]
 
 
