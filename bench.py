@@ -96,16 +96,17 @@ def algorithmic_ops(w):
     query passes 3 (distance 2, contraction 1), each backward side 7 (kernel
     value 2, dot 1, contraction 1, sign term 3); Newton-Schulz 2 m^3 per forward
     step and 6 m^3 per reverse step (all products of a step); norm statistics
-    2 per element.  The work is fixed by the method, not by where it runs:
-    contractions on the tensor cores and kernel values read back from the
-    forward still count."""
+    2 per element.  With Q = K the query pass's kernel values are the key
+    pass's (P = C^T), so its distances are not counted again (contraction 1).
+    The work is fixed by the method, not by where it runs: contractions on the
+    tensor cores and kernel values read back from the forward still count."""
     BH, N, m, d, T = w.B * w.H, w.N, w.m, w.d, w.iters
     nmd = BH * N * m * d
     # Gaussian kernel: the gradient term is two FMAs (sum g l, sum g x), not the 3-op sign term
     side = 6 if w.kernel == "gauss" else 7
     return {
         "key_fwd": 3 * nmd,
-        "query_fwd": 3 * nmd,
+        "query_fwd": (1 if w.tied else 3) * nmd,
         "qstats": 2 * nmd if w.norm else 0,
         "bwd_query": side * nmd,
         "bwd_key": side * nmd,
@@ -125,7 +126,8 @@ def fp32_pipe_ops(w):
     nmd = BH * N * m * d
     tc = w.dtype == "bf16"
     grad = 2 if w.kernel == "gauss" else 4   # Gaussian term: two FMAs; sign term: indicator + two FMAs
-    return {"key_fwd": (2 if tc else 3) * nmd, "query_fwd": (2 if tc else 3) * nmd,
+    shared = w.tied and tc and not w.norm and w.d in (32, 64)   # O = C W-hat on the tensor cores
+    return {"key_fwd": (2 if tc else 3) * nmd, "query_fwd": 0 if shared else (2 if tc else 3) * nmd,
             "bwd_query": (grad if tc else grad + 2) * nmd, "bwd_key": (grad if tc else grad + 2) * nmd}
 
 
@@ -463,6 +465,7 @@ def run_ours(args, rank, world, local_rank):
     achieved = per_launch_ops[dom] / (dom_ms / 1e3) / 1e12
     achieved_alone = per_launch_ops[dom] / (dom_ms_alone / 1e3) / 1e12
     total_ops = sum(ops.values())
+    fwd_ops = ops["key_fwd"] + ops["query_fwd"] + ops["qstats"] + ops["ns_cluster"]
     pipe = fp32_pipe_ops(w)
     traffic = measured_traffic(w.name, w.kernel, dom)
     roofline = {
@@ -477,6 +480,7 @@ def run_ours(args, rank, world, local_rank):
         "ms_per_launch": dom_ms, "ms_per_launch_alone": dom_ms_alone,
         "achieved_alone": achieved_alone, "frac_alone": achieved_alone / peak,
         "step_frac": total_ops / (ms / 1e3) / 1e12 / peak,
+        "fwd_frac": fwd_ops / (ms_fwd / 1e3) / 1e12 / peak,
         "fp32_pipe_frac": pipe[dom] / (dom_ms / 1e3) / 1e12 / peak,
         "fp32_pipe_frac_alone": pipe[dom] / (dom_ms_alone / 1e3) / 1e12 / peak,
     }

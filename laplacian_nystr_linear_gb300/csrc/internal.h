@@ -169,7 +169,10 @@ cudaError_t run_gemm_wgrad(const char* name, const GemmDims& g, int a_kind,
 // dV = C dW for bf16 tokens (d = 32 / 64) from the kept kernel values C
 // [BH][N][mp] and dW [BH][m][d]; writes dv [BH][N][d] in bf16
 bool dv_tc_ok(const Prob& p);
-cudaError_t run_dv(const Prob& p, const float* C, const float* dW, void* dv, cudaStream_t st);
+// out[BH][N][d] (bf16) = C[BH][N][mp] (fp32, token-major) R[BH][m][d] (fp32): dV = C dW,
+// or the forward's O = C W-hat when Q = K (P = C^T)
+cudaError_t run_dv(const Prob& p, const float* C, const float* R, void* out, const char* name,
+                   cudaStream_t st);
 // FP32 FMA-rate probe: a grid of 8 CTAs of 256 threads per SM, each thread
 // `iters` x 8 independent FMAs (paired: fma.rn.f32x2, two lane-ops each);
 // *lane_ops = the FP32 lane-ops the launch executes

@@ -3,7 +3,10 @@
 //                                  S-hat = P^T A^+ P read with C = k(L, K))
 // with the kernel values C the forward kept (token-major [BH][N][mp], fp32) and
 // dW = X_T^T dW-hat ([BH][m][d], fp32).  The product streams C once from HBM,
-// so it is bound by that read (4 mp bytes per token).
+// so it is bound by that read (4 mp bytes per token).  The same product is the
+// forward's query pass when Q = K and no feature map applies: P = k(Q, L) is
+// then C^T, stored token-major exactly like P, and O = P W-hat = C W-hat (the
+// symmetric kernel of the "SOFT" review, S-hat = P^T A^+ P).
 //
 // Persistent CTAs, one per SM, walk (slice, 128-token tile) items.  Per item
 // the 64-landmark chunks of its C rows arrive by TMA (four stages, so three
@@ -245,7 +248,8 @@ bool dv_tc_ok(const Prob& p) {
 }
 
 template <int D>
-static cudaError_t dv_t(const Prob& p, const float* C, const float* dW, void* dv, cudaStream_t st) {
+static cudaError_t dv_t(const Prob& p, const float* C, const float* dW, void* dv, const char* name,
+                        cudaStream_t st) {
   using S = DvSmem<D>;
   const size_t smem = S::total(p.mp);
   cudaError_t e = allow_smem(k_dv<D>, smem);
@@ -266,13 +270,14 @@ static cudaError_t dv_t(const Prob& p, const float* C, const float* dW, void* dv
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const long long items = (long long)a.BH * a.ntile;
   const int grid = (int)(items < sms ? items : sms);
-  return launch("dv", k_dv<D>, dim3(grid), dim3(NTH), smem, st, map, a);
+  return launch(name, k_dv<D>, dim3(grid), dim3(NTH), smem, st, map, a);
 }
 
-cudaError_t run_dv(const Prob& p, const float* C, const float* dW, void* dv, cudaStream_t st) {
+cudaError_t run_dv(const Prob& p, const float* C, const float* dW, void* dv, const char* name,
+                   cudaStream_t st) {
   if (!dv_tc_ok(p)) return cudaErrorInvalidValue;
-  if (p.d == 64) return dv_t<64>(p, C, dW, dv, st);
-  return dv_t<32>(p, C, dW, dv, st);
+  if (p.d == 64) return dv_t<64>(p, C, dW, dv, name, st);
+  return dv_t<32>(p, C, dW, dv, name, st);
 }
 
 }  // namespace lapnys

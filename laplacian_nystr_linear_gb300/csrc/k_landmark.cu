@@ -13,20 +13,25 @@
 namespace lapnys {
 
 // ---------------------------------------------------------------------------
-// pooling: one CTA per (row of landmark windows, slice); thread = (landmark
-// column wj = g, g + groups, ..; 4-wide feature chunk) sums its window's tokens
-// in row-major order and writes the mean (no cross-thread reduction).
-// Landmark a = wi * mw + wj averages token rows [wi gh / mh, (wi + 1) gh / mh)
-// and columns [wj gw / mw, (wj + 1) gw / mw) (floors): equal windows when the
-// grid divides, otherwise windows of the floor and ceil sizes.
+// pooling: one CTA per (landmark window, slice).  Thread (part p, 4-wide feature
+// chunk) sums the window's tokens p, p + P, .. (row-major order inside the
+// window), so each token row is read by d / 4 consecutive threads in one
+// coalesced piece; the P partial sums of a chunk are then combined in the
+// order p = 0, 1, .. by one thread.  Landmark a = wi * mw + wj averages token
+// rows [wi gh / mh, (wi + 1) gh / mh) and columns [wj gw / mw, (wj + 1) gw / mw)
+// (floors): equal windows when the grid divides, otherwise windows of the
+// floor and ceil sizes.
 //
-// The window sum is kept error-free as a pair s + e (each addition's rounding
-// error, by TwoSum, goes into e), and the mean is written as hi = the fp32
-// value nearest to (s + e) / n and lo = the rest, (s + e - n hi) / n (n hi is
-// subtracted exactly by an FMA).  The sign of x - l in the backward is then
-// decided by hi where x != hi and by -sgn(lo) where x == hi, i.e. against the
-// exact mean of the window.
+// Every sum is kept error-free as a pair s + e (each addition's rounding error,
+// by TwoSum, goes into e; two pairs combine by a TwoSum of their s and the sum
+// of their e), and the mean is written as hi = the fp32 value nearest to
+// (s + e) / n and lo = the rest, (s + e - n hi) / n (n hi is subtracted exactly
+// by an FMA).  The sign of x - l in the backward is then decided by hi where
+// x != hi and by -sgn(lo) where x == hi, i.e. against the exact mean of the
+// window.
 // ---------------------------------------------------------------------------
+constexpr int kPoolThreads = 128;
+
 __device__ __forceinline__ void two_sum_acc(float& s, float& e, float v) {
   const float t = s + v;
   const float bp = t - s;
@@ -44,111 +49,131 @@ __device__ __forceinline__ void mean_hi_lo(float s, float e, float n, float& hi,
 }
 
 template <typename T>
-__global__ void __launch_bounds__(kThreads) k_pool(const T* __restrict__ K, float* __restrict__ L,
-                                                   float* __restrict__ Llo,
-                                                   int32_t* __restrict__ idx, int N, int d, int gh,
-                                                   int gw, int mh, int mw, int m) {
-  const int wi = blockIdx.x, bh = blockIdx.y;
-  const int C4 = d / 4, groups = kThreads / C4;
-  const int chunk = threadIdx.x % C4, g = threadIdx.x / C4;
+__global__ void __launch_bounds__(kPoolThreads) k_pool(const T* __restrict__ K,
+                                                       float* __restrict__ L,
+                                                       float* __restrict__ Llo,
+                                                       int32_t* __restrict__ idx, int N, int d,
+                                                       int gh, int gw, int mh, int mw, int m) {
+  __shared__ float4 ps[kPoolThreads], pe[kPoolThreads];
+  const int a = blockIdx.x, bh = blockIdx.y;
+  const int wi = a / mw, wj = a - wi * mw;
+  const int C4 = d / 4, P = kPoolThreads / C4;
+  const int chunk = threadIdx.x % C4, part = threadIdx.x / C4;
   const int y0 = wi * gh / mh, y1 = (wi + 1) * gh / mh;
+  const int x0 = wj * gw / mw, x1 = (wj + 1) * gw / mw;
+  const int ww = x1 - x0, nwin = (y1 - y0) * ww;
   const T* Kb = K + (size_t)bh * N * d + chunk * 4;
-  for (int wj = g; wj < mw; wj += groups) {
-    const int x0 = wj * gw / mw, x1 = (wj + 1) * gw / mw;
-    float4 s = make_float4(0.f, 0.f, 0.f, 0.f), e = s;
-    for (int y = y0; y < y1; ++y) {
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f), e = s;
+  if (part < P) {
 #pragma unroll 4
-      for (int x = x0; x < x1; ++x) {
-        const float4 v = ld4(Kb + ((size_t)y * gw + x) * d);
-        two_sum_acc(s.x, e.x, v.x);
-        two_sum_acc(s.y, e.y, v.y);
-        two_sum_acc(s.z, e.z, v.z);
-        two_sum_acc(s.w, e.w, v.w);
-      }
+    for (int t = part; t < nwin; t += P) {
+      const int y = y0 + t / ww, x = x0 + t % ww;
+      const float4 v = ld4(Kb + ((size_t)y * gw + x) * d);
+      two_sum_acc(s.x, e.x, v.x);
+      two_sum_acc(s.y, e.y, v.y);
+      two_sum_acc(s.z, e.z, v.z);
+      two_sum_acc(s.w, e.w, v.w);
     }
-    const int a = wi * mw + wj;
-    const float n = (float)((y1 - y0) * (x1 - x0));
-    float4 hi, lo;
-    mean_hi_lo(s.x, e.x, n, hi.x, lo.x);
-    mean_hi_lo(s.y, e.y, n, hi.y, lo.y);
-    mean_hi_lo(s.z, e.z, n, hi.z, lo.z);
-    mean_hi_lo(s.w, e.w, n, hi.w, lo.w);
-    st4(L + ((size_t)bh * m + a) * d + chunk * 4, hi);
-    if (Llo != nullptr) st4(Llo + ((size_t)bh * m + a) * d + chunk * 4, lo);
-    if (idx != nullptr && bh == 0 && chunk == 0)
-      for (int y = y0; y < y1; ++y)
-        for (int x = x0; x < x1; ++x) idx[y * gw + x] = a;
+    ps[threadIdx.x] = s;
+    pe[threadIdx.x] = e;
   }
+  if (idx != nullptr && bh == 0 && chunk == 0 && part < P)
+    for (int t = part; t < nwin; t += P) idx[(y0 + t / ww) * gw + x0 + t % ww] = a;
+  __syncthreads();
+  if (part != 0) return;
+  for (int q = 1; q < P; ++q) {
+    const float4 s2 = ps[q * C4 + chunk], e2 = pe[q * C4 + chunk];
+    two_sum_acc(s.x, e.x, s2.x); e.x += e2.x;
+    two_sum_acc(s.y, e.y, s2.y); e.y += e2.y;
+    two_sum_acc(s.z, e.z, s2.z); e.z += e2.z;
+    two_sum_acc(s.w, e.w, s2.w); e.w += e2.w;
+  }
+  const float n = (float)nwin;
+  float4 hi, lo;
+  mean_hi_lo(s.x, e.x, n, hi.x, lo.x);
+  mean_hi_lo(s.y, e.y, n, hi.y, lo.y);
+  mean_hi_lo(s.z, e.z, n, hi.z, lo.z);
+  mean_hi_lo(s.w, e.w, n, hi.w, lo.w);
+  st4(L + ((size_t)bh * m + a) * d + chunk * 4, hi);
+  if (Llo != nullptr) st4(Llo + ((size_t)bh * m + a) * d + chunk * 4, lo);
 }
 
 cudaError_t run_pool(const Prob& p, const void* k, float* L, float* Llo, int32_t* idx,
                      cudaStream_t st) {
-  dim3 grid(p.mh, p.BH);
+  dim3 grid(p.m, p.BH);
   if (p.dtype == 1)
-    return launch("pool", k_pool<__nv_bfloat16>, grid, dim3(kThreads), 0, st,
+    return launch("pool", k_pool<__nv_bfloat16>, grid, dim3(kPoolThreads), 0, st,
                   (const __nv_bfloat16*)k, L, Llo, idx, p.N, p.d, p.gh, p.gw, p.mh, p.mw, p.m);
-  return launch("pool", k_pool<float>, grid, dim3(kThreads), 0, st, (const float*)k, L, Llo, idx,
-                p.N, p.d, p.gh, p.gw, p.mh, p.mw, p.m);
+  return launch("pool", k_pool<float>, grid, dim3(kPoolThreads), 0, st, (const float*)k, L, Llo,
+                idx, p.N, p.d, p.gh, p.gw, p.mh, p.mw, p.m);
 }
 
 // ---------------------------------------------------------------------------
-// 64 x 64 shared-memory matrix products for the on-chip solver.
-// Thread (ty, tx) owns rows i = 4 ty + r and columns j = col(s):
-//   TB == false: j = 4 tx + s   (B read as [k][j])
-//   TB == true : j = tx + 16 s  (B read as [j][k], interleaved to avoid bank conflicts)
-// op(A) is A[i][k] (TA == false) or A[k][i] (TA == true).  Stride 68 floats.
+// 64 x 64 shared-memory matrix products for the on-chip solver (row-major
+// tiles of stride 68 floats; op(A) is A[i][k] or, with TA, A[k][i]; op(B) is
+// B[k][j] or, with TB, B[j][k]).
 // ---------------------------------------------------------------------------
 constexpr int kMS = 68;
 
-template <bool TB>
-__device__ __forceinline__ int mcol(int s) {
-  const int tx = threadIdx.x & 15;
-  return TB ? tx + 16 * s : 4 * tx + s;
+// The products run on the tensor cores (mma.sync m16n8k8, TF32) at
+// fp32-level accuracy: every operand element is split x = hi + lo (hi = x
+// rounded to TF32, lo = x - hi) and the product accumulated in fp32 as
+// hi*hi + hi*lo + lo*hi (the missing lo*lo term and lo's own TF32 truncation
+// are O(2^-21) relative).  Warp w computes rows 16 (w / 2) .. + 15 and columns
+// 32 (w % 2) .. + 31 (four 16 x 8 tiles); tile n's fragment element c lands at
+//     row 16 (w / 2) + g + 8 (c / 2),  column 32 (w % 2) + 8 n + 2 t + c % 2
+// with g = lane / 4, t = lane % 4 (emit below walks them).  K is padded to a
+// multiple of 8 with the tiles' zero padding.
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
+  lo = __float_as_uint(x - __uint_as_float(hi));
+}
+
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
 template <bool TA, bool TB>
-__device__ __forceinline__ void mm64(const float* __restrict__ A, const float* __restrict__ B, int K,
-                                     float acc[4][4]) {
-  const int ty = threadIdx.x >> 4, tx = threadIdx.x & 15;
+__device__ __forceinline__ void mm64tc(const float* __restrict__ A, const float* __restrict__ B,
+                                       int K, float (&acc)[4][4]) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int i0 = 16 * (warp >> 1), j0 = 32 * (warp & 1);
 #pragma unroll
-  for (int r = 0; r < 4; ++r)
+  for (int n = 0; n < 4; ++n)
 #pragma unroll
-    for (int s = 0; s < 4; ++s) acc[r][s] = 0.f;
-  for (int k = 0; k < K; k += 4) {
-    float a[4][4], b[4][4];  // a[r][kk], b[kk][s]
-    if (!TA) {
+    for (int c = 0; c < 4; ++c) acc[n][c] = 0.f;
+  auto opa = [&](int i, int k) { return TA ? A[k * kMS + i] : A[i * kMS + k]; };
+  auto opb = [&](int k, int j) { return TB ? B[j * kMS + k] : B[k * kMS + j]; };
+  const int K8 = (K + 7) & ~7;
+  for (int k0 = 0; k0 < K8; k0 += 8) {
+    uint32_t ah[4], al[4];
+    split_tf32(opa(i0 + g, k0 + t), ah[0], al[0]);
+    split_tf32(opa(i0 + g + 8, k0 + t), ah[1], al[1]);
+    split_tf32(opa(i0 + g, k0 + t + 4), ah[2], al[2]);
+    split_tf32(opa(i0 + g + 8, k0 + t + 4), ah[3], al[3]);
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const float4 v = lds4(A + (4 * ty + r) * kMS + k);
-        a[r][0] = v.x; a[r][1] = v.y; a[r][2] = v.z; a[r][3] = v.w;
-      }
-    } else {
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const float4 v = lds4(A + (k + kk) * kMS + 4 * ty);
-        a[0][kk] = v.x; a[1][kk] = v.y; a[2][kk] = v.z; a[3][kk] = v.w;
-      }
+    for (int n = 0; n < 4; ++n) {
+      uint32_t bh0, bl0, bh1, bl1;
+      split_tf32(opb(k0 + t, j0 + 8 * n + g), bh0, bl0);
+      split_tf32(opb(k0 + t + 4, j0 + 8 * n + g), bh1, bl1);
+      mma_tf32(acc[n], ah, bh0, bh1);
+      mma_tf32(acc[n], ah, bl0, bl1);
+      mma_tf32(acc[n], al, bh0, bh1);
     }
-    if (!TB) {
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const float4 v = lds4(B + (k + kk) * kMS + 4 * tx);
-        b[kk][0] = v.x; b[kk][1] = v.y; b[kk][2] = v.z; b[kk][3] = v.w;
-      }
-    } else {
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        const float4 v = lds4(B + (tx + 16 * s) * kMS + k);
-        b[0][s] = v.x; b[1][s] = v.y; b[2][s] = v.z; b[3][s] = v.w;
-      }
-    }
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int s = 0; s < 4; ++s) acc[r][s] = fmaf(a[r][kk], b[kk][s], acc[r][s]);
   }
+}
+
+// smem offset (row-major, stride kMS) of fragment element c of tile n
+__device__ __forceinline__ int tc_off(int n, int c) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  return (16 * (warp >> 1) + g + 8 * (c >> 1)) * kMS + 32 * (warp & 1) + 8 * n + 2 * t + (c & 1);
 }
 
 // load an m x m row-major global matrix into a zero-padded 64 x 68 tile
@@ -242,20 +267,20 @@ __global__ void __launch_bounds__(kThreads) k_ns_small(const float* __restrict__
   const int K = (m + 3) & ~3;
   for (int t = 0; t < iters; ++t) {
     float acc[4][4];
-    mm64<false, false>(As, Xa, K, acc);  // Y_t = A X_t
+    mm64tc<false, false>(As, Xa, K, acc);  // Y_t = A X_t
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+    for (int n = 0; n < 4; ++n)
 #pragma unroll
-      for (int s = 0; s < 4; ++s) Ys[(4 * ty + r) * kMS + mcol<false>(s)] = acc[r][s];
+      for (int c = 0; c < 4; ++c) Ys[tc_off(n, c)] = acc[n][c];
     __syncthreads();
     store_mat(Y + ((size_t)bh * ny + t % ny) * mm, Ys, m);
-    mm64<false, false>(Xa, Ys, K, acc);  // X_{t+1} = 2 X_t - X_t Y_t
+    mm64tc<false, false>(Xa, Ys, K, acc);  // X_{t+1} = 2 X_t - X_t Y_t
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+    for (int n = 0; n < 4; ++n)
 #pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        const int o = (4 * ty + r) * kMS + mcol<false>(s);
-        Xb[o] = 2.f * Xa[o] - acc[r][s];
+      for (int c = 0; c < 4; ++c) {
+        const int o = tc_off(n, c);
+        Xb[o] = 2.f * Xa[o] - acc[n][c];
       }
     __syncthreads();
     store_mat(X + ((size_t)bh * nx + (t + 1) % nx) * mm, Xb, m);
@@ -536,7 +561,6 @@ __global__ void __launch_bounds__(kThreads) k_ns_bwd_small(const float* __restri
   float* Tm = dAs + 64 * kMS;
   __shared__ float red[kThreads];
   const int bh = blockIdx.x;
-  const int ty = threadIdx.x >> 4;
   const size_t mm = (size_t)m * m;
   const int K = (m + 3) & ~3;
 
@@ -548,33 +572,33 @@ __global__ void __launch_bounds__(kThreads) k_ns_bwd_small(const float* __restri
     load_mat(Xt, X + ((size_t)bh * nx + t % nx) * mm, m);
     load_mat(Yt, Y + ((size_t)bh * ny + t % ny) * mm, m);
     __syncthreads();
-    mm64<true, false>(Xt, G, K, acc);  // XG = X_t^T G
+    mm64tc<true, false>(Xt, G, K, acc);  // XG = X_t^T G
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+    for (int n = 0; n < 4; ++n)
 #pragma unroll
-      for (int s = 0; s < 4; ++s) XG[(4 * ty + r) * kMS + mcol<false>(s)] = acc[r][s];
+      for (int c = 0; c < 4; ++c) XG[tc_off(n, c)] = acc[n][c];
     __syncthreads();
-    mm64<false, true>(XG, Xt, K, acc);  // dA -= XG X_t^T
+    mm64tc<false, true>(XG, Xt, K, acc);  // dA -= XG X_t^T
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+    for (int n = 0; n < 4; ++n)
 #pragma unroll
-      for (int s = 0; s < 4; ++s) dAs[(4 * ty + r) * kMS + mcol<true>(s)] -= acc[r][s];
-    mm64<false, true>(G, Yt, K, acc);  // Tm = 2 G - G Y_t^T
+      for (int c = 0; c < 4; ++c) dAs[tc_off(n, c)] -= acc[n][c];
+    mm64tc<false, true>(G, Yt, K, acc);  // Tm = 2 G - G Y_t^T
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+    for (int n = 0; n < 4; ++n)
 #pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        const int o = (4 * ty + r) * kMS + mcol<true>(s);
-        Tm[o] = 2.f * G[o] - acc[r][s];
+      for (int c = 0; c < 4; ++c) {
+        const int o = tc_off(n, c);
+        Tm[o] = 2.f * G[o] - acc[n][c];
       }
     __syncthreads();
-    mm64<true, false>(As, XG, K, acc);  // G = Tm - A^T XG
+    mm64tc<true, false>(As, XG, K, acc);  // G = Tm - A^T XG
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+    for (int n = 0; n < 4; ++n)
 #pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        const int o = (4 * ty + r) * kMS + mcol<false>(s);
-        G[o] = Tm[o] - acc[r][s];
+      for (int c = 0; c < 4; ++c) {
+        const int o = tc_off(n, c);
+        G[o] = Tm[o] - acc[n][c];
       }
     __syncthreads();
   }

@@ -485,6 +485,15 @@ int lapnys_fwd(const void* q, const void* k, const void* v, void* out, int B, in
   // W-hat = X_T W
   CK(ns_mm(p, false, false, m, d, m, XT, m, c.nx * mm, W, d, (long)m * d, What, d, (long)m * d,
            nullptr, d, 0, 1.f, 0.f, stream));
+  // Q = K: P = k(Q, L) is C^T, and the key pass has just stored C token-major
+  // (the layout of P).  Without a feature map the query pass is then the product
+  // O = C W-hat, read once from ctx instead of recomputing the distances; the
+  // backward reads C as P (a tied forward stores no separate P).
+  if (full && tied_qk && !p.norm() && dv_tc_ok(p)) {
+    CK(run_dv(p, (const float*)(cb + c.C), What, out, "query_shared", stream));
+    return LAPNYS_OK;
+  }
+  float* Pout = full && !tied_qk ? (float*)(cb + c.P) : nullptr;
   if (p.norm()) {
     float* spart = (float*)(wb + w.spart);
     CK(run_qstats(p, q, L, spart, stream));
@@ -495,13 +504,13 @@ int lapnys_fwd(const void* q, const void* k, const void* v, void* out, int B, in
     if (p.gauss()) {
       float* packW = fpack + (size_t)p.BH * p.nt * (64 * d + 64);
       CK(run_pack_qg(p, L, What, fpack, packW, stream));
-      CK(run_query_gtc(p, q, fpack, packW, stats, out, full ? (float*)(cb + c.P) : nullptr, stream));
+      CK(run_query_gtc(p, q, fpack, packW, stats, out, Pout, stream));
     } else {
       CK(run_pack_q(p, L, What, fpack, stream));
-      CK(run_query_tc(p, q, fpack, stats, out, full ? (float*)(cb + c.P) : nullptr, stream));
+      CK(run_query_tc(p, q, fpack, stats, out, Pout, stream));
     }
   } else {
-    CK(run_query_fwd(p, q, L, What, stats, out, full ? (float*)(cb + c.P) : nullptr, stream));
+    CK(run_query_fwd(p, q, L, What, stats, out, Pout, stream));
   }
   return LAPNYS_OK;
 }
@@ -639,6 +648,9 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
   const long mm = (long)m * m;
   const long md = (long)m * d;
 
+  // the query side's kernel values P: a tied forward stores none, C^T is P then
+  const float* Pm = (const float*)(cb + (tied_qk ? c.C : c.P));
+
   // which 32-token blocks need the exact sign path (a value tied with a
   // landmark value, or out of the fast path's range)
   uint32_t* ties_q = (uint32_t*)(wb + w.ties);
@@ -661,7 +673,7 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
   memset(&qa, 0, sizeof(qa));
   qa.X = q; qa.U = dout; qa.L = L; qa.Llo = Llo; qa.R = What; qa.stats = stats; qa.mdz = mdz;
   qa.tok_part = dQp; qa.lm_part = dLqp; qa.lm_part2 = dWhp; qa.ns_part = nsp; qa.ties = ties_q;
-  qa.kv = (const float*)(cb + c.P);
+  qa.kv = Pm;
   if (p.norm()) {
     CK(run_bwd_tile(p, 0, qa, stream));
     CK(run_mdz(p, nsp, mdz, stream));
@@ -671,7 +683,7 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
     BwdTcArgs qt;
     memset(&qt, 0, sizeof(qt));
     qt.X = q; qt.U = dout; qt.L = L; qt.Llo = Llo; qt.R = What; qt.stats = stats; qt.mdz = mdz;
-    qt.kv = (const float*)(cb + c.P); qt.ties = ties_q; qt.out = dq_direct ? dq : nullptr;
+    qt.kv = Pm; qt.ties = ties_q; qt.out = dq_direct ? dq : nullptr;
     qt.tok_part = dQp; qt.lm_part = dLqp; qt.lm_part2 = dWhp; qt.S = p.Stc;
     CK(run_bwd_tc(p, 1, qt, stream));
     if (!p.norm()) CK(run_reduce_parts(p.BH, p.Stc, m, p.mp, d, dWhp, dWh, stream));
@@ -745,7 +757,7 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
     // bf16 directly when the streaming kernel applies, else through fp32 partials
     const float* Cm = (const float*)(cb + c.C);
     if (dv_tc_ok(p))
-      CK(run_dv(p, Cm, dW, dv, stream));
+      CK(run_dv(p, Cm, dW, dv, "dv", stream));
     else
       CK(ns_mm(p, false, false, N, d, m, Cm, p.mp, (long)N * p.mp, dW, d, md, dVp, d, (long)N * d,
                nullptr, d, 0, 1.f, 0.f, stream));

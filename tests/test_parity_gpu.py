@@ -110,8 +110,13 @@ def test_tensor_core_forward_intermediates(w):
     for (b, h), s in o["saved"].items():
         c = g["ctx"]
         assert rel(c["W"][b, h], s["W"]) < 1e-5          # C V with C as three bf16 planes
-        assert rel(c["P"][b, h], s["P"]) < 1e-6          # kernel values stored as computed
-        assert rel(c["C"][b, h], s["C"].T) < 1e-6
+        assert rel(c["C"][b, h], s["C"].T) < 1e-6        # kernel values stored as computed
+        if w.tied:
+            # Q = K: the forward keeps C alone, which is P's transpose (the query
+            # pass and the backward read it as P)
+            assert rel(c["C"][b, h], s["P"]) < 1e-6
+        else:
+            assert rel(c["P"][b, h], s["P"]) < 1e-6
 
 
 def test_norm_statistics():
@@ -473,7 +478,8 @@ def test_gaussian_backward_small_cases(w):
     for (b, h), s in o["saved"].items():
         c = g["ctx"]
         assert rel(c["A"][b, h], s["A"]) < 1e-6            # Gaussian landmark matrix
-        assert rel(c["P"][b, h], s["P"]) < (1e-4 if tc else 1e-5)
+        Pg = c["C"] if w.tied else c["P"]                    # Q = K: C is P's transpose
+        assert rel(Pg[b, h], s["P"]) < (1e-4 if tc else 1e-5)
         assert rel(c["C"][b, h], s["C"].T) < (1e-4 if tc else 1e-5)
 
 
