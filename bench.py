@@ -475,7 +475,8 @@ def run_ours(args, rank, world, local_rank):
         "peak_source": (f"{sms} SMs x {FP32_LANES_PER_SM} FP32 lanes x {mhz:.0f} MHz (SM count "
                         "from the device, maximum SM clock from nvidia-smi); measured by the "
                         f"library's FMA probe: {probe['scalar']:.1f} (scalar FFMA) and "
-                        f"{probe['paired']:.1f} (paired f32x2) Tlane-op/s"),
+                        f"{probe['paired']:.1f} (paired f32x2) Tlane-op/s "
+                        "(profiles/fma_probe_gb300.md)"),
         "peak_measured": probe,
         "ms_per_launch": dom_ms, "ms_per_launch_alone": dom_ms_alone,
         "achieved_alone": achieved_alone, "frac_alone": achieved_alone / peak,

@@ -114,16 +114,18 @@ cudaError_t run_pool(const Prob& p, const void* k, float* L, float* Llo, int32_t
 // B[k][j] or, with TB, B[j][k]).
 // ---------------------------------------------------------------------------
 constexpr int kMS = 68;
+constexpr int kNsThreads = 512;  // 16 warps: two 16 x 8 output tiles each
 
 // The products run on the tensor cores (mma.sync m16n8k8, TF32) at
 // fp32-level accuracy: every operand element is split x = hi + lo (hi = x
 // rounded to TF32, lo = x - hi) and the product accumulated in fp32 as
 // hi*hi + hi*lo + lo*hi (the missing lo*lo term and lo's own TF32 truncation
-// are O(2^-21) relative).  Warp w computes rows 16 (w / 2) .. + 15 and columns
-// 32 (w % 2) .. + 31 (four 16 x 8 tiles); tile n's fragment element c lands at
-//     row 16 (w / 2) + g + 8 (c / 2),  column 32 (w % 2) + 8 n + 2 t + c % 2
-// with g = lane / 4, t = lane % 4 (emit below walks them).  K is padded to a
-// multiple of 8 with the tiles' zero padding.
+// are O(2^-21) relative).  Of the 16 warps, warp w computes rows 16 (w / 4) ..
+// + 15 and columns 16 (w % 4) .. + 15 (two 16 x 8 tiles); tile n's fragment
+// element c lands at
+//     row 16 (w / 4) + g + 8 (c / 2),  column 16 (w % 4) + 8 n + 2 t + c % 2
+// with g = lane / 4, t = lane % 4 (tc_off below).  K is padded to a multiple
+// of 8 with the tiles' zero padding.
 __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
   lo = __float_as_uint(x - __uint_as_float(hi));
@@ -140,12 +142,12 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
 
 template <bool TA, bool TB>
 __device__ __forceinline__ void mm64tc(const float* __restrict__ A, const float* __restrict__ B,
-                                       int K, float (&acc)[4][4]) {
+                                       int K, float (&acc)[2][4]) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int i0 = 16 * (warp >> 1), j0 = 32 * (warp & 1);
+  const int i0 = 16 * (warp >> 2), j0 = 16 * (warp & 3);
 #pragma unroll
-  for (int n = 0; n < 4; ++n)
+  for (int n = 0; n < 2; ++n)
 #pragma unroll
     for (int c = 0; c < 4; ++c) acc[n][c] = 0.f;
   auto opa = [&](int i, int k) { return TA ? A[k * kMS + i] : A[i * kMS + k]; };
@@ -158,7 +160,7 @@ __device__ __forceinline__ void mm64tc(const float* __restrict__ A, const float*
     split_tf32(opa(i0 + g, k0 + t + 4), ah[2], al[2]);
     split_tf32(opa(i0 + g + 8, k0 + t + 4), ah[3], al[3]);
 #pragma unroll
-    for (int n = 0; n < 4; ++n) {
+    for (int n = 0; n < 2; ++n) {
       uint32_t bh0, bl0, bh1, bl1;
       split_tf32(opb(k0 + t, j0 + 8 * n + g), bh0, bl0);
       split_tf32(opb(k0 + t + 4, j0 + 8 * n + g), bh1, bl1);
@@ -173,18 +175,30 @@ __device__ __forceinline__ void mm64tc(const float* __restrict__ A, const float*
 __device__ __forceinline__ int tc_off(int n, int c) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  return (16 * (warp >> 1) + g + 8 * (c >> 1)) * kMS + 32 * (warp & 1) + 8 * n + 2 * t + (c & 1);
+  return (16 * (warp >> 2) + g + 8 * (c >> 1)) * kMS + 16 * (warp & 3) + 8 * n + 2 * t + (c & 1);
 }
 
 // load an m x m row-major global matrix into a zero-padded 64 x 68 tile
+// (thread: column j = tid % 64, rows tid / 64, + 8, ..)
 __device__ __forceinline__ void load_mat(float* s, const float* g, int m) {
-  for (int e = threadIdx.x; e < 64 * 64; e += kThreads) {
-    const int i = e >> 6, j = e & 63;
+  const int j = threadIdx.x & 63;
+  for (int i = threadIdx.x >> 6; i < 64; i += kNsThreads / 64)
     s[i * kMS + j] = (i < m && j < m) ? g[i * m + j] : 0.f;
+}
+// the same as an asynchronous copy (4-byte cp.async, zero fill past m)
+__device__ __forceinline__ void load_mat_async(float* s, const float* g, int m) {
+  const int j = threadIdx.x & 63;
+  for (int i = threadIdx.x >> 6; i < 64; i += kNsThreads / 64) {
+    const bool ok = i < m && j < m;
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_addr(s + i * kMS + j)),
+                 "l"(ok ? g + i * m + j : g), "r"(ok ? 4 : 0)
+                 : "memory");
   }
 }
 __device__ __forceinline__ void store_mat(float* g, const float* s, int m) {
-  for (int e = threadIdx.x; e < m * m; e += kThreads) g[e] = s[(e / m) * kMS + e % m];
+  const int j = threadIdx.x & 63;
+  if (j >= m) return;
+  for (int i = threadIdx.x >> 6; i < m; i += kNsThreads / 64) g[i * m + j] = s[i * kMS + j];
 }
 
 // alpha = 1 / (|A|_1 |A|_inf) of the m x m tile in shared memory; writes the
@@ -223,7 +237,7 @@ __device__ void alpha_of_tile(const float* As, int m, float* info_g, float* alph
 // gram + alpha + Newton-Schulz for m <= 64: one CTA per slice
 // ---------------------------------------------------------------------------
 template <int D, bool GAUSS>
-__global__ void __launch_bounds__(kThreads) k_ns_small(const float* __restrict__ L, float* __restrict__ A,
+__global__ void __launch_bounds__(kNsThreads) k_ns_small(const float* __restrict__ L, float* __restrict__ A,
                                                        float* __restrict__ alpha, float* __restrict__ X,
                                                        float* __restrict__ Y, int m, int iters, int nx,
                                                        int ny, float ns, float eps) {
@@ -238,9 +252,9 @@ __global__ void __launch_bounds__(kThreads) k_ns_small(const float* __restrict__
   const int ty = threadIdx.x >> 4;
   const size_t mm = (size_t)m * m;
 
-  load_tile<D>(Ls, L + (size_t)bh * m * D, 0, m);
+  if (threadIdx.x < kThreads) load_tile<D>(Ls, L + (size_t)bh * m * D, 0, m);
   __syncthreads();
-  {
+  if (threadIdx.x < kThreads) {  // the 16 x 16 thread grid of the distance tile
     float dist[4][4];
     dist_tile<D, GAUSS>(Ls, Ls, dist);
     const int tx = threadIdx.x & 15;
@@ -258,7 +272,7 @@ __global__ void __launch_bounds__(kThreads) k_ns_small(const float* __restrict__
   store_mat(A + bh * mm, As, m);
   alpha_of_tile(As, m, alpha + (size_t)bh * 4, &al_s);
   const float al = al_s;
-  for (int e = threadIdx.x; e < 64 * 64; e += kThreads) {
+  for (int e = threadIdx.x; e < 64 * 64; e += kNsThreads) {
     const int i = e >> 6, j = e & 63;
     Xa[i * kMS + j] = al * As[i * kMS + j];
   }
@@ -266,17 +280,17 @@ __global__ void __launch_bounds__(kThreads) k_ns_small(const float* __restrict__
   store_mat(X + (size_t)bh * nx * mm, Xa, m);
   const int K = (m + 3) & ~3;
   for (int t = 0; t < iters; ++t) {
-    float acc[4][4];
+    float acc[2][4];
     mm64tc<false, false>(As, Xa, K, acc);  // Y_t = A X_t
 #pragma unroll
-    for (int n = 0; n < 4; ++n)
+    for (int n = 0; n < 2; ++n)
 #pragma unroll
       for (int c = 0; c < 4; ++c) Ys[tc_off(n, c)] = acc[n][c];
     __syncthreads();
     store_mat(Y + ((size_t)bh * ny + t % ny) * mm, Ys, m);
     mm64tc<false, false>(Xa, Ys, K, acc);  // X_{t+1} = 2 X_t - X_t Y_t
 #pragma unroll
-    for (int n = 0; n < 4; ++n)
+    for (int n = 0; n < 2; ++n)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int o = tc_off(n, c);
@@ -296,12 +310,12 @@ cudaError_t run_ns_small(const Prob& p, const float* L, float* A, float* alpha, 
     if (p.gauss()) {                                                                        \
       static bool once = (allow_smem(k_ns_small<DD, true>, smem), true);                    \
       (void)once;                                                                           \
-      return launch("ns_small", k_ns_small<DD, true>, dim3(p.BH), dim3(kThreads), smem, st, \
+      return launch("ns_small", k_ns_small<DD, true>, dim3(p.BH), dim3(kNsThreads), smem, st, \
                     L, A, alpha, X, Y, p.m, p.iters, nx, ny, p.ns, p.eps);                  \
     }                                                                                       \
     static bool once = (allow_smem(k_ns_small<DD, false>, smem), true);                     \
     (void)once;                                                                             \
-    return launch("ns_small", k_ns_small<DD, false>, dim3(p.BH), dim3(kThreads), smem, st,  \
+    return launch("ns_small", k_ns_small<DD, false>, dim3(p.BH), dim3(kNsThreads), smem, st,  \
                   L, A, alpha, X, Y, p.m, p.iters, nx, ny, p.ns, p.eps);                    \
   }
   switch (p.d) {
@@ -544,48 +558,57 @@ cudaError_t run_gram_bwd(const Prob& p, const float* L, const float* Llo, const 
 // dalpha = <G, A> spread over the maximising column (n1) and row (ninf).
 // GT holds dLoss/dX_T on entry.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) k_ns_bwd_small(const float* __restrict__ A,
-                                                           const float* __restrict__ info,
-                                                           const float* __restrict__ X,
-                                                           const float* __restrict__ Y,
-                                                           const float* __restrict__ GT,
-                                                           float* __restrict__ dA, int m, int iters,
-                                                           int nx, int ny) {
+__global__ void __launch_bounds__(kNsThreads) k_ns_bwd_small(const float* __restrict__ A,
+                                                             const float* __restrict__ info,
+                                                             const float* __restrict__ X,
+                                                             const float* __restrict__ Y,
+                                                             const float* __restrict__ GT,
+                                                             float* __restrict__ dA, int m,
+                                                             int iters, int nx, int ny) {
   extern __shared__ float4 sm4[];
   float* As = reinterpret_cast<float*>(sm4);
-  float* Xt = As + 64 * kMS;
-  float* Yt = Xt + 64 * kMS;
-  float* G = Yt + 64 * kMS;
+  float* Xt2 = As + 64 * kMS;         // X_t, two buffers: step t - 1's arrives during step t
+  float* Yt2 = Xt2 + 2 * 64 * kMS;    // Y_t, likewise
+  float* G = Yt2 + 2 * 64 * kMS;
   float* XG = G + 64 * kMS;
   float* dAs = XG + 64 * kMS;
   float* Tm = dAs + 64 * kMS;
-  __shared__ float red[kThreads];
+  __shared__ float red[kNsThreads];
   const int bh = blockIdx.x;
   const size_t mm = (size_t)m * m;
   const int K = (m + 3) & ~3;
+  auto fetch = [&](int t, int buf) {
+    load_mat_async(Xt2 + buf * 64 * kMS, X + ((size_t)bh * nx + t % nx) * mm, m);
+    load_mat_async(Yt2 + buf * 64 * kMS, Y + ((size_t)bh * ny + t % ny) * mm, m);
+    cp_commit();
+  };
 
+  if (iters > 0) fetch(iters - 1, 0);
   load_mat(As, A + bh * mm, m);
   load_mat(G, GT + bh * mm, m);
-  for (int e = threadIdx.x; e < 64 * kMS; e += kThreads) dAs[e] = 0.f;
-  float acc[4][4];
+  for (int e = threadIdx.x; e < 64 * kMS; e += kNsThreads) dAs[e] = 0.f;
+  float acc[2][4];
   for (int t = iters - 1; t >= 0; --t) {
-    load_mat(Xt, X + ((size_t)bh * nx + t % nx) * mm, m);
-    load_mat(Yt, Y + ((size_t)bh * ny + t % ny) * mm, m);
-    __syncthreads();
+    const int buf = (iters - 1 - t) & 1;
+    const float* Xt = Xt2 + buf * 64 * kMS;
+    const float* Yt = Yt2 + buf * 64 * kMS;
+    cp_wait_all();
+    __syncthreads();  // step t's X_t, Y_t landed; step t + 1 is done with the other buffers
+    if (t > 0) fetch(t - 1, buf ^ 1);
     mm64tc<true, false>(Xt, G, K, acc);  // XG = X_t^T G
 #pragma unroll
-    for (int n = 0; n < 4; ++n)
+    for (int n = 0; n < 2; ++n)
 #pragma unroll
       for (int c = 0; c < 4; ++c) XG[tc_off(n, c)] = acc[n][c];
     __syncthreads();
     mm64tc<false, true>(XG, Xt, K, acc);  // dA -= XG X_t^T
 #pragma unroll
-    for (int n = 0; n < 4; ++n)
+    for (int n = 0; n < 2; ++n)
 #pragma unroll
       for (int c = 0; c < 4; ++c) dAs[tc_off(n, c)] -= acc[n][c];
     mm64tc<false, true>(G, Yt, K, acc);  // Tm = 2 G - G Y_t^T
 #pragma unroll
-    for (int n = 0; n < 4; ++n)
+    for (int n = 0; n < 2; ++n)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int o = tc_off(n, c);
@@ -594,32 +617,33 @@ __global__ void __launch_bounds__(kThreads) k_ns_bwd_small(const float* __restri
     __syncthreads();
     mm64tc<true, false>(As, XG, K, acc);  // G = Tm - A^T XG
 #pragma unroll
-    for (int n = 0; n < 4; ++n)
+    for (int n = 0; n < 2; ++n)
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int o = tc_off(n, c);
         G[o] = Tm[o] - acc[n][c];
       }
-    __syncthreads();
   }
+  cp_wait_all();
+  __syncthreads();
   // X_0 = alpha A
   const float* in = info + (size_t)bh * 4;
   const float al = in[0], n1 = in[1], ninf = in[2];
   const int code = __float_as_int(in[3]);
   const int jc = code & 0xffff, ir = code >> 16;
   float part = 0.f;
-  for (int e = threadIdx.x; e < 64 * 64; e += kThreads) {
+  for (int e = threadIdx.x; e < 64 * 64; e += kNsThreads) {
     const int o = (e >> 6) * kMS + (e & 63);
     part += G[o] * As[o];
   }
   red[threadIdx.x] = part;
   __syncthreads();
-  for (int w = kThreads / 2; w > 0; w >>= 1) {
+  for (int w = kNsThreads / 2; w > 0; w >>= 1) {
     if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
     __syncthreads();
   }
   const float dal = red[0];
-  for (int e = threadIdx.x; e < 64 * 64; e += kThreads) {
+  for (int e = threadIdx.x; e < 64 * 64; e += kNsThreads) {
     const int i = e >> 6, j = e & 63;
     const int o = i * kMS + j;
     float v = dAs[o] + al * G[o];
@@ -633,11 +657,11 @@ __global__ void __launch_bounds__(kThreads) k_ns_bwd_small(const float* __restri
 
 cudaError_t run_ns_bwd_small(const Prob& p, const float* A, const float* alpha, const float* X,
                              const float* Y, const float* GT, float* dA, cudaStream_t st) {
-  const size_t smem = 7 * 64 * kMS * sizeof(float);
+  const size_t smem = 9 * 64 * kMS * sizeof(float);
   static bool once = (allow_smem(k_ns_bwd_small, smem), true);
   (void)once;
-  return launch("ns_bwd_small", k_ns_bwd_small, dim3(p.BH), dim3(kThreads), smem, st, A, alpha, X,
-                Y, GT, dA, p.m, p.iters, p.iters + 1, p.iters);
+  return launch("ns_bwd_small", k_ns_bwd_small, dim3(p.BH), dim3(kNsThreads), smem, st, A, alpha,
+                X, Y, GT, dA, p.m, p.iters, p.iters + 1, p.iters);
 }
 
 // ---------------------------------------------------------------------------

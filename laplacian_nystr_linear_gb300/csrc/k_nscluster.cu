@@ -20,9 +20,11 @@
 // 168 registers):
 //   warp 9, one lane  copies each K-stage (16) of both operands into a 4-stage
 //           raw ring in shared memory with TMA (cp.async.bulk.tensor).  An
-//           operand whose rows hold K contiguously goes through a 4-D tensor
-//           map {4 k, rows, k / 4, matrix} whose box lands in K-major 16-byte
-//           pieces; one stored [k][row] through a 3-D map {row, k, matrix}.
+//           operand whose rows hold K contiguously goes through a 3-D tensor
+//           map {k, rows, matrix} in boxes of 16 k (one 64-byte row per copy
+//           request, 64-byte swizzle so that the splitters' row-wise reads are
+//           free of bank conflicts); one stored [k][row] through a 3-D map
+//           {row, k, matrix}.
 //   warps 0-7  per stage: split op(A) (lane = row 32 (w % 4) + lane, k-step
 //           w / 4) into TF32 hi / lo and write them into TMEM (tcgen05.st),
 //           where the MMA reads op(A); split op(B) and store hi / lo into a
@@ -85,7 +87,10 @@ constexpr uint32_t kEpiPitch = 36 * 4;               // staged row: 32 floats + 
 constexpr uint32_t kEpiWarp = 32 * kEpiPitch;
 static_assert(NTH / 32 * kEpiWarp <= 2 * kStage, "epilogue staging fits in two split stages");
 static_assert(kAcol + NSPL * 32 <= kTmemCols, "op(A) stages fit in TMEM");
-constexpr size_t kSmem = (size_t)NSPL * kStage + (size_t)NRAW * kRawStage + 128;
+// the raw ring starts 1024-byte aligned (the 64-byte swizzle of its K-contiguous
+// boxes is a function of the shared-memory address bits)
+constexpr size_t kRawOff = ((size_t)NSPL * kStage + 1023) / 1024 * 1024;
+constexpr size_t kSmem = kRawOff + (size_t)NRAW * kRawStage + 1024;
 constexpr int kWaitLimit = 1 << 22;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -152,14 +157,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity) {
   }
   return false;
 }
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
-                                            int c2, int c3, uint32_t mbar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(mbar)
-      : "memory");
-}
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
                                             int c2, uint32_t mbar) {
   asm volatile(
@@ -199,7 +196,7 @@ __device__ __forceinline__ float4 ldcg4(const float* p) {
 
 // Tensor maps of every operand use in the programs (encoded on the host per
 // launch).  A-role maps have 128-row boxes, B-role maps 256-row boxes; "kc":
-// rows hold K contiguously (4-D map), "mn": stored [k][row] (3-D map).  The
+// rows hold K contiguously (swizzled 64-byte rows), "mn": stored [k][row].  The
 // last dimension enumerates the m x m matrices of the buffer.
 struct NsMaps {
   CUtensorMap a_kc, a_mn;          // landmark matrix A [BH]: A X (fwd), A^T XG (rev)
@@ -226,7 +223,7 @@ namespace {
 struct Prod {
   const CUtensorMap* ma;  // op(A) rows: map and matrix index
   int za;
-  bool ka;                // rows of op(A) hold K contiguously (4-D map)
+  bool ka;                // rows of op(A) hold K contiguously
   const CUtensorMap* mb;  // op(B)^T rows (result columns)
   int zb;
   bool kb;
@@ -279,24 +276,25 @@ __device__ __forceinline__ Prod prod_of(const NsMaps& mp, const NsArgs& a, int s
 __device__ __forceinline__ void issue_stage(uint8_t* raw, const Prod& p, int i0, int c,
                                             uint32_t bar) {
   mbar_expect_tx(bar, kRawStage);
-  if (p.ka) tma_load_4d(smem_u32(raw), p.ma, 0, i0, c * (TK / 4), p.za, bar);
+  if (p.ka) tma_load_3d(smem_u32(raw), p.ma, c * TK, i0, p.za, bar);
   else tma_load_3d(smem_u32(raw), p.ma, i0, c * TK, p.za, bar);
-  if (p.kb) tma_load_4d(smem_u32(raw + kRawA), p.mb, 0, 0, c * (TK / 4), p.zb, bar);
+  if (p.kb) tma_load_3d(smem_u32(raw + kRawA), p.mb, c * TK, 0, p.zb, bar);
   else tma_load_3d(smem_u32(raw + kRawA), p.mb, 0, c * TK, p.zb, bar);
 }
 
 // op(A) of one stage for splitter lane `row` (0..127 of the panel), k-step ah
 // (k = 8 ah .. 8 ah + 7): split and written to TMEM columns colh, coll (+0..7)
-// of this warp's lane quarter (warp-collective).  Raw layout: 4-D box (kc):
-// piece (row, k4) at 16 (128 k4 + row); 3-D box (mn): value (k, row) at
-// 4 (128 k + row).
+// of this warp's lane quarter (warp-collective).  Raw layout: kc box: row r's
+// 16 k values in 64 bytes at 64 r, its 16-byte piece k4 swizzled to slot
+// k4 ^ ((r / 2) % 4) (the 64-byte swizzle: lanes reading one piece of 32 rows
+// then hit every bank once per 8 lanes); mn box: value (k, row) at 4 (128 k + row).
 __device__ __forceinline__ void split_a(const uint8_t* ra, bool kc, int row, int ah, uint32_t colh,
                                         uint32_t coll) {
   float v[8];
   if (kc) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      const float4 x = *reinterpret_cast<const float4*>(ra + 16 * (TM * (2 * ah + j) + row));
+      const float4 x = *reinterpret_cast<const float4*>(ra + 64 * row + 16 * ((2 * ah + j) ^ ((row >> 1) & 3)));
       v[4 * j] = x.x; v[4 * j + 1] = x.y; v[4 * j + 2] = x.z; v[4 * j + 3] = x.w;
     }
   } else {
@@ -324,8 +322,8 @@ __device__ __forceinline__ void store_transposed(uint8_t* hi, uint8_t* lo, uint3
 }
 
 // op(B)^T of one stage (256 rows x 16 k), thread ts of the 256 splitters.
-// Raw 4-D box (kc): piece (row, k4) at 16 (256 k4 + row); thread ts takes row
-// ts, pieces k4 = 0..3.  Raw 3-D box (mn): [16 k][256 rows]; thread ts takes
+// Raw kc box: piece (row, k4) of 16 bytes at 64 row + 16 (k4 ^ ((row / 2) % 4));
+// thread ts takes row ts, pieces k4 = 0..3.  Raw 3-D box (mn): [16 k][256 rows]; thread ts takes
 // the 4-row block rb = ts % 64 at k4 = ts / 64 (four pieces along the rows,
 // transposed).  Consecutive lanes read consecutive 16-byte words.
 __device__ __forceinline__ void split_b(const uint8_t* rbase, bool kc, uint8_t* sp, int ts) {
@@ -334,7 +332,7 @@ __device__ __forceinline__ void split_b(const uint8_t* rbase, bool kc, uint8_t* 
   if (kc) {
 #pragma unroll
     for (int k4 = 0; k4 < 4; ++k4) {
-      const float4 x = *reinterpret_cast<const float4*>(rbase + 16 * (TNMAX * k4 + ts));
+      const float4 x = *reinterpret_cast<const float4*>(rbase + 64 * ts + 16 * (k4 ^ ((ts >> 1) & 3)));
       store_split(bhi, blo, kmaj_off(ts, k4, kLboB), x);
     }
   } else {
@@ -360,9 +358,9 @@ __global__ void __launch_bounds__(NTH, 1)
   const int bh = blockIdx.y, i0 = TM * blockIdx.x;
   const int m = a.m;
   const int np = (m + 15) & ~15;  // MMA N
-  uint8_t* tsm = tsm_raw + ((128u - (smem_u32(tsm_raw) & 127u)) & 127u);
+  uint8_t* tsm = tsm_raw + ((1024u - (smem_u32(tsm_raw) & 1023u)) & 1023u);
   uint8_t* stage_base = tsm;
-  uint8_t* raw_base = tsm + NSPL * kStage;
+  uint8_t* raw_base = tsm + kRawOff;
   uint8_t* epi_base = stage_base;  // split stages 0-1 (see the header)
   const int nchunks = (m + TK - 1) / TK;
   const int nprod = a.reverse ? 4 * a.iters : 2 * a.iters;
@@ -632,16 +630,16 @@ EncodeTiled encoder() {
   return fn;
 }
 
-// nmat row-major m x m matrices at p, rows holding K contiguously: 4-D view
-// {4, m rows, m / 4 k-groups, nmat} read in {4, rows, 4, 1} boxes (K-major
-// 16-byte pieces, piece (row, k4) at 16 (rows k4 + row))
+// nmat row-major m x m matrices at p, rows holding K contiguously: 3-D view
+// {m k, m rows, nmat} read in {16, rows, 1} boxes, one 64-byte row per request,
+// with the 64-byte swizzle (piece k4 of row r lands in slot k4 ^ ((r / 2) % 4))
 bool map_kc(CUtensorMap* t, const float* p, int m, int nmat, int rows) {
-  const cuuint64_t dim[4] = {4, (cuuint64_t)m, (cuuint64_t)(m / 4), (cuuint64_t)nmat};
-  const cuuint64_t stride[3] = {(cuuint64_t)m * 4, 16, (cuuint64_t)m * m * 4};
-  const cuuint32_t box[4] = {4, (cuuint32_t)rows, TK / 4, 1};
-  const cuuint32_t es[4] = {1, 1, 1, 1};
-  return encoder()(t, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float*>(p), dim, stride, box,
-                   es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+  const cuuint64_t dim[3] = {(cuuint64_t)m, (cuuint64_t)m, (cuuint64_t)nmat};
+  const cuuint64_t stride[2] = {(cuuint64_t)m * 4, (cuuint64_t)m * m * 4};
+  const cuuint32_t box[3] = {TK, (cuuint32_t)rows, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return encoder()(t, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(p), dim, stride, box,
+                   es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
