@@ -672,13 +672,26 @@ bool bwd_tc_shape(int dtype, int d) { return dtype == 1 && d == D; }
 int bwd_tc_groups(int m) { return (m + 255) / 256; }
 
 int bwd_tc_splits(int BH, int m, int N) {
-  // about eight waves of one CTA per SM of a 152-SM part, from the dimensions
-  // alone (the landmark-side summation order does not depend on the device)
+  // Token splits per (slice, landmark group), from the dimensions alone (the
+  // landmark-side summation order does not depend on the device): the count
+  // that minimises rounds x (1 + blocks per CTA) on a 152-SM part, one CTA per
+  // SM at a time, where a CTA's fixed cost (R planes, tensor memory, the
+  // landmark-side epilogue) is about one 16-token block (measured on the PVT
+  // stages: 1216 CTAs of 2-3 blocks and 160 CTAs of 13 blocks were both slower
+  // than the minimum of this model); ties go to fewer splits.
   const int ng = bwd_tc_groups(m), nblk16 = (N + TJ - 1) / TJ;
-  int s = (8 * 152 + BH * ng / 2) / (BH * ng);
-  if (s < 1) s = 1;
-  if (s > nblk16) s = nblk16;
-  return s;
+  const long long units = (long long)BH * ng;
+  int best = 1;
+  long long best_cost = -1;
+  for (int s = 1; s <= nblk16 && s <= 4096; ++s) {
+    const long long rounds = (units * s + 151) / 152;
+    const long long cost = rounds * (1 + (nblk16 + s - 1) / s);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
 }
 
 template <int MODE, int MC, bool NORM, bool GAUSS>
