@@ -239,17 +239,22 @@ cudaError_t run_ns_bwd_small(const Prob& p, const float* A, const float* alpha, 
                              const float* Y, const float* GT, float* dA, cudaStream_t st);
 cudaError_t run_alpha_bwd(const Prob& p, const float* A, const float* alpha, const float* G,
                           float* dA, cudaStream_t st);
-// dL = sum over S splits of dLq and of dLc, plus dLA ([BH][S][mp][d] partials)
+// dLs = (sum over S splits of dLq and of dLc, plus dLA) / the landmark's window
+// size ([BH][S][mp][d] partials): each token's share of its landmark's gradient
 cudaError_t run_reduce_dl(const Prob& p, int S, const float* dLq, const float* dLc, const float* dLA,
-                          float* dL, cudaStream_t st);
+                          float* dLs, cudaStream_t st);
 cudaError_t run_zero(float* x, size_t n, cudaStream_t st);
+// token gradients: the token-side partials plus dLs[idx[n]] (idx: the pool's
+// token -> landmark map), converted to the tensor type
 cudaError_t run_finalize(const Prob& p, const float* dQp, const float* dKp, const float* dVp,
-                         const float* dL, void* dq, void* dk, void* dv, cudaStream_t st);
-// token gradients after the tensor-core backward: nq planes of dQ partials (0:
-// dq was written already), nk planes of dK partials, one plane of dV (fp32)
+                         const float* dLs, const int32_t* idx, void* dq, void* dk, void* dv,
+                         cudaStream_t st);
+// the same after the tensor-core backward: nq planes of dQ partials (0: dq was
+// written already), nk planes of dK partials, one plane of dV (fp32; null: dv
+// was written already)
 cudaError_t run_finalize_tc(const Prob& p, int nq, const float* dQp, int nk, const float* dKp,
-                            const float* dVp, const float* dL, void* dq, void* dk, void* dv,
-                            cudaStream_t st);
+                            const float* dVp, const float* dLs, const int32_t* idx, void* dq,
+                            void* dk, void* dv, cudaStream_t st);
 
 // tensor-core backward tile kernel (bf16 tokens, d = 64): one CTA per token
 // range and group of up to 256 landmarks; grid (S, bwd_tc_groups(m), BH)

@@ -907,9 +907,12 @@ cudaError_t run_mdz(const Prob& p, const float* ns_part, float* mdz, cudaStream_
 }
 
 // dL[bh][a][c] = sum_s dLq + sum_s dLc + dLA (fixed order)
+// dL of every landmark (split partials of both sides in order, plus the gram
+// path), divided by its window's token count: the share the pool backward
+// gives each token of the window
 __global__ void k_reduce_dl(const float* __restrict__ dLq, const float* __restrict__ dLc,
-                            const float* __restrict__ dLA, float* __restrict__ dL, int BH, int S,
-                            int m, int mp, int d) {
+                            const float* __restrict__ dLA, float* __restrict__ dLs, int BH, int S,
+                            int m, int mp, int d, int gh, int gw, int mh, int mw) {
   const size_t total = (size_t)BH * m * d;
   for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < total;
        e += (size_t)gridDim.x * blockDim.x) {
@@ -918,24 +921,27 @@ __global__ void k_reduce_dl(const float* __restrict__ dLq, const float* __restri
     float s = 0.f;
     for (int q = 0; q < S; ++q) s += dLq[base + (size_t)q * mp * d];
     for (int q = 0; q < S; ++q) s += dLc[base + (size_t)q * mp * d];
-    dL[e] = s + dLA[e];
+    const int a = (int)(ac / d), wi = a / mw, wj = a - wi * mw;
+    const float inv = 1.0f / (float)(((wi + 1) * gh / mh - wi * gh / mh) *
+                                     ((wj + 1) * gw / mw - wj * gw / mw));
+    dLs[e] = (s + dLA[e]) * inv;
   }
 }
 
 cudaError_t run_reduce_dl(const Prob& p, int S, const float* dLq, const float* dLc, const float* dLA,
-                          float* dL, cudaStream_t st) {
+                          float* dLs, cudaStream_t st) {
   const size_t n = (size_t)p.BH * p.m * p.d;
-  return launch("reduce_dl", k_reduce_dl, dim3(grid_for(n)), dim3(kThreads), 0, st, dLq, dLc, dLA, dL,
-                p.BH, S, p.m, p.mp, p.d);
+  return launch("reduce_dl", k_reduce_dl, dim3(grid_for(n)), dim3(kThreads), 0, st, dLq, dLc, dLA,
+                dLs, p.BH, S, p.m, p.mp, p.d, p.gh, p.gw, p.mh, p.mw);
 }
 
 // token gradients: sum the per-landmark-tile partials in tile order, add the
-// pooling path dL[a(n)] / window size to dK, convert to the tensor type.
+// pooling path dLs[a(n)] (dL / window size) to dK, convert to the tensor type.
 template <typename T>
 __global__ void k_finalize(const float* __restrict__ dQp, const float* __restrict__ dKp,
-                           const float* __restrict__ dVp, const float* __restrict__ dL,
-                           T* __restrict__ dq, T* __restrict__ dk, T* __restrict__ dv, int BH, int N,
-                           int d, int nt, int m, int gh, int gw, int mh, int mw, int tied) {
+                           const float* __restrict__ dVp, const float* __restrict__ dLs,
+                           const int32_t* __restrict__ idx, T* __restrict__ dq, T* __restrict__ dk,
+                           T* __restrict__ dv, int BH, int N, int d, int nt, int m, int tied) {
   const size_t total4 = (size_t)BH * N * d / 4;
   const size_t plane = (size_t)BH * N * d;
   for (size_t e4 = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e4 < total4;
@@ -954,14 +960,10 @@ __global__ void k_finalize(const float* __restrict__ dQp, const float* __restric
       k4.x += b.x; k4.y += b.y; k4.z += b.z; k4.w += b.w;
       v4.x += v.x; v4.y += v.y; v4.z += v.z; v4.w += v.w;
     }
-    // the token's pooling window (rows [wi gh / mh, (wi + 1) gh / mh), floors) and its size
-    const int y = n / gw, x = n % gw;
-    const int wi = ((y + 1) * mh - 1) / gh, wj = ((x + 1) * mw - 1) / gw;
-    const int a = wi * mw + wj;
-    const float inv = 1.0f / (float)(((wi + 1) * gh / mh - wi * gh / mh) *
-                                     ((wj + 1) * gw / mw - wj * gw / mw));
-    const float4 l4 = *reinterpret_cast<const float4*>(dL + (bh * m + a) * d + c);
-    k4.x += l4.x * inv; k4.y += l4.y * inv; k4.z += l4.z * inv; k4.w += l4.w * inv;
+    // the token's pooling window: its landmark's dL, already divided by the
+    // window's size
+    const float4 l4 = __ldg(reinterpret_cast<const float4*>(dLs + (bh * m + __ldg(idx + n)) * d + c));
+    k4.x += l4.x; k4.y += l4.y; k4.z += l4.z; k4.w += l4.w;
     if (tied) {
       q4.x += k4.x; q4.y += k4.y; q4.z += k4.z; q4.w += k4.w;
       st4(dq + e, q4);
@@ -979,70 +981,73 @@ __global__ void k_finalize(const float* __restrict__ dQp, const float* __restric
 // one fp32 plane (null: dv was written already); tied: dq = dQ + dK; all
 // converted to the tensor type.
 template <typename T>
-__global__ void k_finalize_tc(const float* __restrict__ dQp, const float* __restrict__ dKp,
-                              const float* __restrict__ dVp, const float* __restrict__ dL,
-                              T* __restrict__ dq, T* __restrict__ dk, T* __restrict__ dv, int BH,
-                              int N, int d, int nq, int nk, int m, int gh, int gw, int mh, int mw,
-                              int tied) {
-  const size_t total4 = (size_t)BH * N * d / 4;
+__global__ void __launch_bounds__(kThreads) k_finalize_tc(
+    const float* __restrict__ dQp, const float* __restrict__ dKp, const float* __restrict__ dVp,
+    const float* __restrict__ dLs, const int32_t* __restrict__ idx, T* __restrict__ dq,
+    T* __restrict__ dk, T* __restrict__ dv, int BH, int N, int d, int c4shift, int nq, int nk,
+    int m, int tied) {
+  // thread = (token n, 4-wide feature piece), 32-bit index arithmetic; the
+  // token's landmark from the pool's index map, its share of dL pre-divided
+  const int C4 = d >> 2;
+  const int per = N * C4;
   const size_t plane = (size_t)BH * N * d;
-  for (size_t e4 = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e4 < total4;
-       e4 += (size_t)gridDim.x * blockDim.x) {
-    const size_t e = e4 * 4;
-    const size_t row = e / d;
-    const int c = (int)(e % d);
-    const int n = (int)(row % N);
-    const size_t bh = row / N;
-    float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f), k4 = q4;
-    for (int t = 0; t < nq; ++t) {
-      const float4 a = *reinterpret_cast<const float4*>(dQp + t * plane + e);
-      q4.x += a.x; q4.y += a.y; q4.z += a.z; q4.w += a.w;
+  for (int bh = blockIdx.y; bh < BH; bh += gridDim.y) {
+    for (int id = blockIdx.x * blockDim.x + threadIdx.x; id < per; id += gridDim.x * blockDim.x) {
+      const int n = id >> c4shift, c = (id & (C4 - 1)) * 4;
+      const size_t e = ((size_t)bh * N + n) * d + c;
+      const int a = __ldg(idx + n);
+      float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f), k4 = q4;
+      for (int t = 0; t < nq; ++t) {
+        const float4 u = __ldcs(reinterpret_cast<const float4*>(dQp + t * plane + e));
+        q4.x += u.x; q4.y += u.y; q4.z += u.z; q4.w += u.w;
+      }
+      for (int t = 0; t < nk; ++t) {
+        const float4 u = __ldcs(reinterpret_cast<const float4*>(dKp + t * plane + e));
+        k4.x += u.x; k4.y += u.y; k4.z += u.z; k4.w += u.w;
+      }
+      const float4 l4 = __ldg(reinterpret_cast<const float4*>(dLs + ((size_t)bh * m + a) * d + c));
+      k4.x += l4.x; k4.y += l4.y; k4.z += l4.z; k4.w += l4.w;
+      if (tied) {
+        q4.x += k4.x; q4.y += k4.y; q4.z += k4.z; q4.w += k4.w;
+        st4(dq + e, q4);
+      } else {
+        if (nq > 0) st4(dq + e, q4);
+        st4(dk + e, k4);
+      }
+      if (dVp != nullptr) st4(dv + e, __ldcs(reinterpret_cast<const float4*>(dVp + e)));
     }
-    for (int t = 0; t < nk; ++t) {
-      const float4 b = *reinterpret_cast<const float4*>(dKp + t * plane + e);
-      k4.x += b.x; k4.y += b.y; k4.z += b.z; k4.w += b.w;
-    }
-    const int y = n / gw, x = n % gw;
-    const int wi = ((y + 1) * mh - 1) / gh, wj = ((x + 1) * mw - 1) / gw;
-    const int a = wi * mw + wj;
-    const float inv = 1.0f / (float)(((wi + 1) * gh / mh - wi * gh / mh) *
-                                     ((wj + 1) * gw / mw - wj * gw / mw));
-    const float4 l4 = *reinterpret_cast<const float4*>(dL + (bh * m + a) * d + c);
-    k4.x += l4.x * inv; k4.y += l4.y * inv; k4.z += l4.z * inv; k4.w += l4.w * inv;
-    if (tied) {
-      q4.x += k4.x; q4.y += k4.y; q4.z += k4.z; q4.w += k4.w;
-      st4(dq + e, q4);
-    } else {
-      if (nq > 0) st4(dq + e, q4);
-      st4(dk + e, k4);
-    }
-    if (dVp != nullptr) st4(dv + e, *reinterpret_cast<const float4*>(dVp + e));
   }
 }
 
 cudaError_t run_finalize_tc(const Prob& p, int nq, const float* dQp, int nk, const float* dKp,
-                            const float* dVp, const float* dL, void* dq, void* dk, void* dv,
-                            cudaStream_t st) {
-  const size_t n4 = (size_t)p.BH * p.N * p.d / 4;
+                            const float* dVp, const float* dLs, const int32_t* idx, void* dq,
+                            void* dk, void* dv, cudaStream_t st) {
+  const int C4 = p.d / 4;
+  int c4shift = 0;
+  while ((1 << c4shift) < C4) ++c4shift;
+  const long long per = (long long)p.N * C4;
+  const int bx = (int)((per + kThreads - 1) / kThreads);
+  dim3 grid(bx < 1024 ? bx : 1024, p.BH < 65535 ? p.BH : 65535);
   if (p.dtype == 1)
-    return launch("finalize", k_finalize_tc<__nv_bfloat16>, dim3(grid_for(n4)), dim3(kThreads), 0,
-                  st, dQp, dKp, dVp, dL, (__nv_bfloat16*)dq, (__nv_bfloat16*)dk, (__nv_bfloat16*)dv,
-                  p.BH, p.N, p.d, nq, nk, p.m, p.gh, p.gw, p.mh, p.mw, p.tied);
-  return launch("finalize", k_finalize_tc<float>, dim3(grid_for(n4)), dim3(kThreads), 0, st, dQp,
-                dKp, dVp, dL, (float*)dq, (float*)dk, (float*)dv, p.BH, p.N, p.d, nq, nk, p.m, p.gh,
-                p.gw, p.mh, p.mw, p.tied);
+    return launch("finalize", k_finalize_tc<__nv_bfloat16>, grid, dim3(kThreads), 0, st, dQp, dKp,
+                  dVp, dLs, idx, (__nv_bfloat16*)dq, (__nv_bfloat16*)dk, (__nv_bfloat16*)dv, p.BH,
+                  p.N, p.d, c4shift, nq, nk, p.m, p.tied);
+  return launch("finalize", k_finalize_tc<float>, grid, dim3(kThreads), 0, st, dQp, dKp, dVp, dLs,
+                idx, (float*)dq, (float*)dk, (float*)dv, p.BH, p.N, p.d, c4shift, nq, nk, p.m,
+                p.tied);
 }
 
 cudaError_t run_finalize(const Prob& p, const float* dQp, const float* dKp, const float* dVp,
-                         const float* dL, void* dq, void* dk, void* dv, cudaStream_t st) {
+                         const float* dLs, const int32_t* idx, void* dq, void* dk, void* dv,
+                         cudaStream_t st) {
   const size_t n4 = (size_t)p.BH * p.N * p.d / 4;
   if (p.dtype == 1)
     return launch("finalize", k_finalize<__nv_bfloat16>, dim3(grid_for(n4)), dim3(kThreads), 0, st,
-                  dQp, dKp, dVp, dL, (__nv_bfloat16*)dq, (__nv_bfloat16*)dk, (__nv_bfloat16*)dv,
-                  p.BH, p.N, p.d, p.nt, p.m, p.gh, p.gw, p.mh, p.mw, p.tied);
+                  dQp, dKp, dVp, dLs, idx, (__nv_bfloat16*)dq, (__nv_bfloat16*)dk,
+                  (__nv_bfloat16*)dv, p.BH, p.N, p.d, p.nt, p.m, p.tied);
   return launch("finalize", k_finalize<float>, dim3(grid_for(n4)), dim3(kThreads), 0, st, dQp, dKp,
-                dVp, dL, (float*)dq, (float*)dk, (float*)dv, p.BH, p.N, p.d, p.nt, p.m, p.gh, p.gw,
-                p.mh, p.mw, p.tied);
+                dVp, dLs, idx, (float*)dq, (float*)dk, (float*)dv, p.BH, p.N, p.d, p.nt, p.m,
+                p.tied);
 }
 
 // zero-fill (used when the Newton-Schulz backward has no step to initialise dA)

@@ -629,6 +629,7 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
   const float* W = (const float*)(cb + c.W);
   const float* What = (const float*)(cb + c.What);
   const float* stats = (const float*)(cb + c.stats);
+  const int32_t* idx = (const int32_t*)(cb + c.idx);
   float* dWhp = (float*)(wb + w.dWhp);
   float* dLqp = (float*)(wb + w.dLqp);
   float* dLcp = (float*)(wb + w.dLcp);
@@ -772,10 +773,10 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
   if (sd) CK(join(stream, ss, sd->ev[1]));
   CK(run_reduce_dl(p, Sl, dLqp, dLcp, dLA, dL, stream));
   if (tcb)
-    CK(run_finalize_tc(p, dq_direct ? 0 : ng, dQp, ng, dKp, dv_tc_ok(p) ? nullptr : dVp, dL, dq, dk,
-                       dv, stream));
+    CK(run_finalize_tc(p, dq_direct ? 0 : ng, dQp, ng, dKp, dv_tc_ok(p) ? nullptr : dVp, dL, idx,
+                       dq, dk, dv, stream));
   else
-    CK(run_finalize(p, dQp, dKp, dVp, dL, dq, dk, dv, stream));
+    CK(run_finalize(p, dQp, dKp, dVp, dL, idx, dq, dk, dv, stream));
   return LAPNYS_OK;
 }
 
