@@ -257,11 +257,17 @@ __global__ void __launch_bounds__(NTH, 1) k_query_tc(QArgs a) {
         for (int c = 0; c < D; ++c) {
           const float4 x0 = lds4(xp + c * QM), l = lds4(lp + c * TL);
           const float x[4] = {x0.x, x0.y, x0.z, x0.w};
-          const float lv[4] = {l.x, l.y, l.z, l.w};
+          if (GAUSS) {
+            const float lv[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
-          for (int r = 0; r < 4; ++r)
+            for (int r = 0; r < 4; ++r)
 #pragma unroll
-            for (int s = 0; s < 4; ++s) acc[r][s] = dist_add<GAUSS>(acc[r][s], x[r] - lv[s]);
+              for (int s = 0; s < 4; ++s) acc[r][s] = dist_add<GAUSS>(acc[r][s], x[r] - lv[s]);
+          } else {
+            const f32x2 la = pack2(l.x, l.y), lb = pack2(l.z, l.w);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) l1_row4(acc[r], x[r], la, lb);
+          }
         }
       }
       // the A buffer of this tile was read by MMA g - 2
@@ -476,11 +482,18 @@ __global__ void __launch_bounds__(NTH, 1) k_key_tc(KArgs a) {
       for (int c = 0; c < D; ++c) {
         const float4 l0 = lds4(lp + c * QM), x = lds4(xp + c * TL);
         const float lv[4] = {l0.x, l0.y, l0.z, l0.w};
-        const float xv[4] = {x.x, x.y, x.z, x.w};
+        if (GAUSS) {
+          const float xv[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
+          for (int r = 0; r < 4; ++r)
 #pragma unroll
-          for (int s = 0; s < 4; ++s) acc[r][s] = dist_add<GAUSS>(acc[r][s], xv[s] - lv[r]);
+            for (int s = 0; s < 4; ++s) acc[r][s] = dist_add<GAUSS>(acc[r][s], xv[s] - lv[r]);
+        } else {
+          // |x_s - l_r| = |l_r - x_s|: the pairs run over the keys
+          const f32x2 xa = pack2(x.x, x.y), xb = pack2(x.z, x.w);
+#pragma unroll
+          for (int r = 0; r < 4; ++r) l1_row4(acc[r], lv[r], xa, xb);
+        }
       }
     }
     {

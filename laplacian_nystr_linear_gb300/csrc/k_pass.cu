@@ -668,12 +668,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
       for (int r = 0; r < 4; ++r)
 #pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          dist[r][s] = dist_add<GAUSS>(dist[r][s], x[r].x - l[s].x);
-          dist[r][s] = dist_add<GAUSS>(dist[r][s], x[r].y - l[s].y);
-          dist[r][s] = dist_add<GAUSS>(dist[r][s], x[r].z - l[s].z);
-          dist[r][s] = dist_add<GAUSS>(dist[r][s], x[r].w - l[s].w);
-        }
+        for (int s = 0; s < 4; ++s) dist4_add<GAUSS>(dist[r][s], x[r], l[s]);
 #pragma unroll
       for (int r = 0; r < 4; ++r) x[r] = lds4(Us + (4 * ty + r) * row_stride(D) + c);
 #pragma unroll
