@@ -975,41 +975,59 @@ __global__ void k_finalize(const float* __restrict__ dQp, const float* __restric
 // dQ the sum of its nq planes (nq = 0: dq was written by the tile kernel); dV
 // one fp32 plane (null: dv was written already); tied: dq = dQ + dK; all
 // converted to the tensor type.
+// 8 consecutive values of T from two float4 (one 16-byte store for bf16)
+__device__ __forceinline__ void st8(float* p, float4 a, float4 b) {
+  st4(p, a);
+  st4(p + 4, b);
+}
+__device__ __forceinline__ void st8(__nv_bfloat16* p, float4 a, float4 b) {
+  const __nv_bfloat162 h0 = __floats2bfloat162_rn(a.x, a.y), h1 = __floats2bfloat162_rn(a.z, a.w);
+  const __nv_bfloat162 h2 = __floats2bfloat162_rn(b.x, b.y), h3 = __floats2bfloat162_rn(b.z, b.w);
+  *reinterpret_cast<uint4*>(p) =
+      make_uint4(*reinterpret_cast<const uint32_t*>(&h0), *reinterpret_cast<const uint32_t*>(&h1),
+                 *reinterpret_cast<const uint32_t*>(&h2), *reinterpret_cast<const uint32_t*>(&h3));
+}
+__device__ __forceinline__ float4 add4(float4 a, float4 b) {
+  return make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads) k_finalize_tc(
     const float* __restrict__ dQp, const float* __restrict__ dKp, const float* __restrict__ dVp,
     const float* __restrict__ dLs, const int32_t* __restrict__ idx, T* __restrict__ dq,
-    T* __restrict__ dk, T* __restrict__ dv, int BH, int N, int d, int c4shift, int nq, int nk,
+    T* __restrict__ dk, T* __restrict__ dv, int BH, int N, int d, int c8shift, int nq, int nk,
     int m, int tied) {
-  // thread = (token n, 4-wide feature piece), 32-bit index arithmetic; the
+  // thread = (token n, 8 consecutive features), 32-bit index arithmetic; the
   // token's landmark from the pool's index map, its share of dL pre-divided
-  const int C4 = d >> 2;
-  const int per = N * C4;
+  const int C8 = d >> 3;
+  const int per = N * C8;
   const size_t plane = (size_t)BH * N * d;
   for (int bh = blockIdx.y; bh < BH; bh += gridDim.y) {
     for (int id = blockIdx.x * blockDim.x + threadIdx.x; id < per; id += gridDim.x * blockDim.x) {
-      const int n = id >> c4shift, c = (id & (C4 - 1)) * 4;
+      const int n = id >> c8shift, c = (id & (C8 - 1)) * 8;
       const size_t e = ((size_t)bh * N + n) * d + c;
       const int a = __ldg(idx + n);
-      float4 q4 = make_float4(0.f, 0.f, 0.f, 0.f), k4 = q4;
-      for (int t = 0; t < nq; ++t) {
-        const float4 u = __ldcs(reinterpret_cast<const float4*>(dQp + t * plane + e));
-        q4.x += u.x; q4.y += u.y; q4.z += u.z; q4.w += u.w;
-      }
+      const float* lp = dLs + ((size_t)bh * m + a) * d + c;
+      float4 q0 = make_float4(0.f, 0.f, 0.f, 0.f), q1 = q0;
+      float4 k0 = __ldg(reinterpret_cast<const float4*>(lp));
+      float4 k1 = __ldg(reinterpret_cast<const float4*>(lp + 4));
       for (int t = 0; t < nk; ++t) {
-        const float4 u = __ldcs(reinterpret_cast<const float4*>(dKp + t * plane + e));
-        k4.x += u.x; k4.y += u.y; k4.z += u.z; k4.w += u.w;
+        k0 = add4(k0, __ldcs(reinterpret_cast<const float4*>(dKp + t * plane + e)));
+        k1 = add4(k1, __ldcs(reinterpret_cast<const float4*>(dKp + t * plane + e + 4)));
       }
-      const float4 l4 = __ldg(reinterpret_cast<const float4*>(dLs + ((size_t)bh * m + a) * d + c));
-      k4.x += l4.x; k4.y += l4.y; k4.z += l4.z; k4.w += l4.w;
+      for (int t = 0; t < nq; ++t) {
+        q0 = add4(q0, __ldcs(reinterpret_cast<const float4*>(dQp + t * plane + e)));
+        q1 = add4(q1, __ldcs(reinterpret_cast<const float4*>(dQp + t * plane + e + 4)));
+      }
       if (tied) {
-        q4.x += k4.x; q4.y += k4.y; q4.z += k4.z; q4.w += k4.w;
-        st4(dq + e, q4);
+        st8(dq + e, add4(q0, k0), add4(q1, k1));
       } else {
-        if (nq > 0) st4(dq + e, q4);
-        st4(dk + e, k4);
+        if (nq > 0) st8(dq + e, q0, q1);
+        st8(dk + e, k0, k1);
       }
-      if (dVp != nullptr) st4(dv + e, __ldcs(reinterpret_cast<const float4*>(dVp + e)));
+      if (dVp != nullptr)
+        st8(dv + e, __ldcs(reinterpret_cast<const float4*>(dVp + e)),
+            __ldcs(reinterpret_cast<const float4*>(dVp + e + 4)));
     }
   }
 }
@@ -1017,18 +1035,18 @@ __global__ void __launch_bounds__(kThreads) k_finalize_tc(
 cudaError_t run_finalize_tc(const Prob& p, int nq, const float* dQp, int nk, const float* dKp,
                             const float* dVp, const float* dLs, const int32_t* idx, void* dq,
                             void* dk, void* dv, cudaStream_t st) {
-  const int C4 = p.d / 4;
-  int c4shift = 0;
-  while ((1 << c4shift) < C4) ++c4shift;
-  const long long per = (long long)p.N * C4;
+  const int C8 = p.d / 8;
+  int c8shift = 0;
+  while ((1 << c8shift) < C8) ++c8shift;
+  const long long per = (long long)p.N * C8;
   const int bx = (int)((per + kThreads - 1) / kThreads);
   dim3 grid(bx < 1024 ? bx : 1024, p.BH < 65535 ? p.BH : 65535);
   if (p.dtype == 1)
     return launch("finalize", k_finalize_tc<__nv_bfloat16>, grid, dim3(kThreads), 0, st, dQp, dKp,
                   dVp, dLs, idx, (__nv_bfloat16*)dq, (__nv_bfloat16*)dk, (__nv_bfloat16*)dv, p.BH,
-                  p.N, p.d, c4shift, nq, nk, p.m, p.tied);
+                  p.N, p.d, c8shift, nq, nk, p.m, p.tied);
   return launch("finalize", k_finalize_tc<float>, grid, dim3(kThreads), 0, st, dQp, dKp, dVp, dLs,
-                idx, (float*)dq, (float*)dk, (float*)dv, p.BH, p.N, p.d, c4shift, nq, nk, p.m,
+                idx, (float*)dq, (float*)dk, (float*)dv, p.BH, p.N, p.d, c8shift, nq, nk, p.m,
                 p.tied);
 }
 
