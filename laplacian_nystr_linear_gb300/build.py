@@ -19,8 +19,9 @@ SOURCES = ["lapnys.cu", "k_landmark.cu", "k_gemm.cu", "k_pass.cu", "k_bwd.cu", "
 HEADERS = [os.path.join(CSRC, h) for h in ("common.cuh", "internal.h", "tc.cuh")] + [
     os.path.join(ROOT, "include", "lapnys.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-# no library beyond the CUDA runtime: every product is this library's own kernel
-LINK: list = []
+# no library beyond the CUDA runtime (every product is this library's own
+# kernel); the header-only NVTX ranges load their tool library through dlopen
+LINK = ["-ldl"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "-I" + os.path.join(ROOT, "include")]
 

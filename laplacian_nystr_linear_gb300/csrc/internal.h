@@ -4,6 +4,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -35,16 +36,28 @@ int prof_begin(const char* name, cudaStream_t s);
 void prof_end(int slot, cudaStream_t s);
 void count_launch();
 
+// Every launch is also an NVTX range named like its profiling record (a no-op
+// unless a tool such as Nsight Systems is attached).
 template <typename Kern, typename... Args>
 inline cudaError_t launch(const char* name, Kern kern, dim3 grid, dim3 block, size_t smem,
                           cudaStream_t st, Args... args) {
+  nvtxRangePushA(name);
   const int slot = prof_begin(name, st);
   kern<<<grid, block, smem, st>>>(args...);
   cudaError_t e = cudaGetLastError();
   prof_end(slot, st);
   count_launch();
+  nvtxRangePop();
   return e;
 }
+
+// an NVTX range over a scope (the library's entry points)
+struct NvtxScope {
+  explicit NvtxScope(const char* name) { nvtxRangePushA(name); }
+  ~NvtxScope() { nvtxRangePop(); }
+  NvtxScope(const NvtxScope&) = delete;
+  NvtxScope& operator=(const NvtxScope&) = delete;
+};
 
 // opt a kernel into more than 48 KB of dynamic shared memory (once per kernel)
 template <typename Kern>

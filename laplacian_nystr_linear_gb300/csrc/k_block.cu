@@ -387,6 +387,7 @@ int lapnys_block_fwd(const void* x, const void* w_qkv, const void* b_qkv, const 
                      int grid_w, int m, float lambda, float eps, int iters, int tied,
                      cudaStream_t stream, int dtype, unsigned flags, void* ctx, size_t ctx_bytes,
                      void* ws, size_t ws_bytes) {
+  NvtxScope nvtx_scope("lapnys_block_fwd");
   if (!block_dims_ok(B, N, C, H, d) || (tied != 0 && tied != 1)) return LAPNYS_EINVAL;
   int rc = check_attention(B, H, N, d, grid_h, grid_w, m, lambda, eps, iters, dtype, flags);
   if (rc != LAPNYS_OK) return rc;
@@ -461,6 +462,7 @@ int lapnys_block_bwd(const void* x, const void* w_qkv, const void* w_o, const vo
                      int B, int N, int C, int H, int d, int grid_h, int grid_w, int m, float lambda,
                      float eps, int iters, int tied, cudaStream_t stream, int dtype,
                      unsigned flags, void* ws, size_t ws_bytes) {
+  NvtxScope nvtx_scope("lapnys_block_bwd");
   if (!block_dims_ok(B, N, C, H, d) || (tied != 0 && tied != 1)) return LAPNYS_EINVAL;
   int rc = check_attention(B, H, N, d, grid_h, grid_w, m, lambda, eps, iters, dtype, flags);
   if (rc != LAPNYS_OK) return rc;

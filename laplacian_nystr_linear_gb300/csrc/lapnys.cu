@@ -407,6 +407,7 @@ int lapnys_ctx_offsets(int B, int H, int N, int d, int m, int iters, unsigned fl
 
 int lapnys_pool(const void* k, float* L, int32_t* idx, int B, int H, int N, int d, int grid_h,
                 int grid_w, int m, int dtype, cudaStream_t stream) {
+  NvtxScope nvtx_scope("lapnys_pool");
   int rc = check_common(B, H, N, d, grid_h, grid_w, m, 1.f, 0.f, 0, dtype, 0);
   if (rc != LAPNYS_OK) return rc;
   if (k == nullptr || L == nullptr || !aligned16(k) || !aligned16(L)) return LAPNYS_EINVAL;
@@ -419,6 +420,7 @@ int lapnys_fwd(const void* q, const void* k, const void* v, void* out, int B, in
                int grid_h, int grid_w, int m, float lambda, float eps, int iters, int tied_qk,
                cudaStream_t stream, int dtype, unsigned flags, void* ctx, size_t ctx_bytes,
                void* ws, size_t ws_bytes) {
+  NvtxScope nvtx_scope("lapnys_fwd");
   int rc = check_common(B, H, N, d, grid_h, grid_w, m, lambda, eps, iters, dtype, flags);
   if (rc != LAPNYS_OK) return rc;
   if (tied_qk != 0 && tied_qk != 1) return LAPNYS_EINVAL;
@@ -599,6 +601,7 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
                void* dq, void* dk, void* dv, int B, int H, int N, int d, int grid_h, int grid_w,
                int m, float lambda, float eps, int iters, int tied_qk, cudaStream_t stream,
                int dtype, unsigned flags, void* ws, size_t ws_bytes) {
+  NvtxScope nvtx_scope("lapnys_bwd");
   int rc = check_common(B, H, N, d, grid_h, grid_w, m, lambda, eps, iters, dtype, flags);
   if (rc != LAPNYS_OK) return rc;
   if (tied_qk != 0 && tied_qk != 1) return LAPNYS_EINVAL;
