@@ -205,10 +205,12 @@ __device__ __forceinline__ void dist_tile(const float* __restrict__ Xs, const fl
 //   A (16 x 8, row-major): a0 (g, t), a1 (g + 8, t), a2 (g, t + 4), a3 (g + 8, t + 4)
 //   B (8 x 8):             b0 (t, g), b1 (t + 4, g)
 //   C (16 x 8):            c0 (g, 2t), c1 (g, 2t + 1), c2 (g + 8, 2t), c3 (g + 8, 2t + 1)
+// x rounded to the nearest TF32 value, halfway cases away from zero: add half
+// a TF32 ulp to the magnitude bits and clear the 13 low bits (a carry into the
+// exponent is the correct rounding).  Two integer ops on the full-rate pipe.
+// Finite x.
 __device__ __forceinline__ uint32_t to_tf32(float x) {
-  uint32_t r;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-  return r;
+  return (__float_as_uint(x) + 0x1000u) & 0xffffe000u;
 }
 __device__ __forceinline__ void mma_16x8x8(float (&d)[4], const uint32_t (&a)[4],
                                            const uint32_t (&b)[2]) {

@@ -109,25 +109,25 @@ cudaError_t run_pool(const Prob& p, const void* k, float* L, float* Llo, int32_t
 }
 
 // ---------------------------------------------------------------------------
-// 64 x 64 shared-memory matrix products for the on-chip solver (row-major
-// tiles of stride 68 floats; op(A) is A[i][k] or, with TA, A[k][i]; op(B) is
-// B[k][j] or, with TB, B[j][k]).
+// Shared-memory matrix products for the on-chip solver (m <= 64): row-major
+// tiles of 64 x 68 floats, zero past m; op(A) is A[i][k] or, with TA, A[k][i];
+// op(B) is B[k][j] or, with TB, B[j][k].
 // ---------------------------------------------------------------------------
 constexpr int kMS = 68;
-constexpr int kNsThreads = 512;  // 16 warps: two 16 x 8 output tiles each
+constexpr int kNsThreads = 512;  // 16 warps
 
 // The products run on the tensor cores (mma.sync m16n8k8, TF32) at
 // fp32-level accuracy: every operand element is split x = hi + lo (hi = x
 // rounded to TF32, lo = x - hi) and the product accumulated in fp32 as
-// hi*hi + hi*lo + lo*hi (the missing lo*lo term and lo's own TF32 truncation
-// are O(2^-21) relative).  Of the 16 warps, warp w computes rows 16 (w / 4) ..
-// + 15 and columns 16 (w % 4) .. + 15 (two 16 x 8 tiles); tile n's fragment
-// element c lands at
-//     row 16 (w / 4) + g + 8 (c / 2),  column 16 (w % 4) + 8 n + 2 t + c % 2
-// with g = lane / 4, t = lane % 4 (tc_off below).  K is padded to a multiple
-// of 8 with the tiles' zero padding.
+// hi*hi + (hi*lo + lo*hi) (the missing lo*lo term and lo's own TF32
+// truncation are O(2^-21) relative).  The three terms go to separate
+// accumulators, so each k step issues six independent MMAs per warp.
+//
+// TF32 rounding: nearest, halfway cases away from zero (add half a TF32 ulp to
+// the magnitude bits, clear the 13 low bits; a carry into the exponent is the
+// correct rounding).  Finite x.
 __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
+  hi = (__float_as_uint(x) + 0x1000u) & 0xffffe000u;
   lo = __float_as_uint(x - __uint_as_float(hi));
 }
 
@@ -140,42 +140,64 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// One 16 x 16 block (rows r0 .., columns c0 ..) of op(A) op(B), summed over the
+// k steps k0 = 8 kq, 8 (kq + s), .. below K8 (a share of K when s warps split
+// it).  Element c of acc[n] sits at row r0 + g + 8 (c / 2), column
+// c0 + 8 n + 2 t + c % 2 (g = lane / 4, t = lane % 4).
 template <bool TA, bool TB>
-__device__ __forceinline__ void mm64tc(const float* __restrict__ A, const float* __restrict__ B,
-                                       int K, float (&acc)[2][4]) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+__device__ __forceinline__ void unit_mm(const float* __restrict__ A, const float* __restrict__ B,
+                                        int r0, int c0, int K8, int kq, int s,
+                                        float (&acc)[2][4]) {
+  const int lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int i0 = 16 * (warp >> 2), j0 = 16 * (warp & 3);
+  float hh[2][4], hl[2][4], lh[2][4];
 #pragma unroll
   for (int n = 0; n < 2; ++n)
 #pragma unroll
-    for (int c = 0; c < 4; ++c) acc[n][c] = 0.f;
+    for (int c = 0; c < 4; ++c) hh[n][c] = hl[n][c] = lh[n][c] = 0.f;
   auto opa = [&](int i, int k) { return TA ? A[k * kMS + i] : A[i * kMS + k]; };
   auto opb = [&](int k, int j) { return TB ? B[j * kMS + k] : B[k * kMS + j]; };
-  const int K8 = (K + 7) & ~7;
-  for (int k0 = 0; k0 < K8; k0 += 8) {
-    uint32_t ah[4], al[4];
-    split_tf32(opa(i0 + g, k0 + t), ah[0], al[0]);
-    split_tf32(opa(i0 + g + 8, k0 + t), ah[1], al[1]);
-    split_tf32(opa(i0 + g, k0 + t + 4), ah[2], al[2]);
-    split_tf32(opa(i0 + g + 8, k0 + t + 4), ah[3], al[3]);
 #pragma unroll
-    for (int n = 0; n < 2; ++n) {
-      uint32_t bh0, bl0, bh1, bl1;
-      split_tf32(opb(k0 + t, j0 + 8 * n + g), bh0, bl0);
-      split_tf32(opb(k0 + t + 4, j0 + 8 * n + g), bh1, bl1);
-      mma_tf32(acc[n], ah, bh0, bh1);
-      mma_tf32(acc[n], ah, bl0, bl1);
-      mma_tf32(acc[n], al, bh0, bh1);
+  for (int u = 0; u < 8; ++u) {
+    const int k0 = 8 * (kq + u * s);
+    if (k0 < K8) {
+      uint32_t ah[4], al[4];
+      split_tf32(opa(r0 + g, k0 + t), ah[0], al[0]);
+      split_tf32(opa(r0 + g + 8, k0 + t), ah[1], al[1]);
+      split_tf32(opa(r0 + g, k0 + t + 4), ah[2], al[2]);
+      split_tf32(opa(r0 + g + 8, k0 + t + 4), ah[3], al[3]);
+#pragma unroll
+      for (int n = 0; n < 2; ++n) {
+        uint32_t bh0, bl0, bh1, bl1;
+        split_tf32(opb(k0 + t, c0 + 8 * n + g), bh0, bl0);
+        split_tf32(opb(k0 + t + 4, c0 + 8 * n + g), bh1, bl1);
+        mma_tf32(hh[n], ah, bh0, bh1);
+        mma_tf32(hl[n], ah, bl0, bl1);
+        mma_tf32(lh[n], al, bh0, bh1);
+      }
     }
   }
+#pragma unroll
+  for (int n = 0; n < 2; ++n)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[n][c] = hh[n][c] + (hl[n][c] + lh[n][c]);
 }
 
-// smem offset (row-major, stride kMS) of fragment element c of tile n
-__device__ __forceinline__ int tc_off(int n, int c) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, t = lane & 3;
-  return (16 * (warp >> 2) + g + 8 * (c >> 1)) * kMS + 16 * (warp & 3) + 8 * n + 2 * t + (c & 1);
+// the 16 x 16 output blocks of an m x m product (R x R of them, R = ceil(m / 16))
+struct UnitSet {
+  int R, n, K8;
+  __device__ explicit UnitSet(int m) : R((m + 15) >> 4), K8((m + 7) & ~7) { n = R * R; }
+  __device__ void at(int i, int& r0, int& c0) const {
+    r0 = 16 * (i / R);
+    c0 = 16 * (i % R);
+  }
+};
+
+// element c of acc[n] of the block at (r0, c0): its (row, column)
+__device__ __forceinline__ void unit_pos(int r0, int c0, int n, int c, int& r, int& j) {
+  const int lane = threadIdx.x & 31;
+  r = r0 + (lane >> 2) + 8 * (c >> 1);
+  j = c0 + 8 * n + 2 * (lane & 3) + (c & 1);
 }
 
 // load an m x m row-major global matrix into a zero-padded 64 x 68 tile
@@ -202,7 +224,7 @@ __device__ __forceinline__ void store_mat(float* g, const float* s, int m) {
 }
 
 // alpha = 1 / (|A|_1 |A|_inf) of the m x m tile in shared memory; writes the
-// info record {alpha, |A|_1, |A|_inf, argmax column (int bits)}.
+// info record {alpha, |A|_1, |A|_inf, argmax column (int bits)} unless info_g is null.
 __device__ void alpha_of_tile(const float* As, int m, float* info_g, float* alpha_s) {
   __shared__ float csum[64], rsum[64];
   if (threadIdx.x < 64) {
@@ -225,16 +247,20 @@ __device__ void alpha_of_tile(const float* As, int m, float* info_g, float* alph
     const float n1 = csum[jc], ninf = rsum[ir];
     const float al = 1.0f / (n1 * ninf);
     *alpha_s = al;
-    info_g[0] = al;
-    info_g[1] = n1;
-    info_g[2] = ninf;
-    info_g[3] = __int_as_float(jc | (ir << 16));
+    if (info_g) {
+      info_g[0] = al;
+      info_g[1] = n1;
+      info_g[2] = ninf;
+      info_g[3] = __int_as_float(jc | (ir << 16));
+    }
   }
   __syncthreads();
 }
 
+
 // ---------------------------------------------------------------------------
-// gram + alpha + Newton-Schulz for m <= 64: one CTA per slice
+// gram + alpha + Newton-Schulz for m <= 64: one CTA per slice, everything on
+// chip; each of the 16 warps takes one 16 x 16 block of each product.
 // ---------------------------------------------------------------------------
 template <int D, bool GAUSS>
 __global__ void __launch_bounds__(kNsThreads) k_ns_small(const float* __restrict__ L, float* __restrict__ A,
@@ -261,10 +287,10 @@ __global__ void __launch_bounds__(kNsThreads) k_ns_small(const float* __restrict
 #pragma unroll
     for (int r = 0; r < 4; ++r)
 #pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        const int i = 4 * ty + r, j = tx + 16 * s;
+      for (int q = 0; q < 4; ++q) {
+        const int i = 4 * ty + r, j = tx + 16 * q;
         float v = 0.f;
-        if (i < m && j < m) v = exp2f(dist[r][s] * ns) + (i == j ? eps : 0.f);
+        if (i < m && j < m) v = exp2f(dist[r][q] * ns) + (i == j ? eps : 0.f);
         As[i * kMS + j] = v;
       }
   }
@@ -278,24 +304,39 @@ __global__ void __launch_bounds__(kNsThreads) k_ns_small(const float* __restrict
   }
   __syncthreads();
   store_mat(X + (size_t)bh * nx * mm, Xa, m);
-  const int K = (m + 3) & ~3;
+  const UnitSet us(m);
+  const int warp = threadIdx.x >> 5;
   for (int t = 0; t < iters; ++t) {
-    float acc[2][4];
-    mm64tc<false, false>(As, Xa, K, acc);  // Y_t = A X_t
+    for (int i = warp; i < us.n; i += kNsThreads / 32) {  // Y_t = A X_t
+      int r0, c0;
+      us.at(i, r0, c0);
+      float acc[2][4];
+      unit_mm<false, false>(As, Xa, r0, c0, us.K8, 0, 1, acc);
 #pragma unroll
-    for (int n = 0; n < 2; ++n)
+      for (int n = 0; n < 2; ++n)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) Ys[tc_off(n, c)] = acc[n][c];
+        for (int c = 0; c < 4; ++c) {
+          int r, j;
+          unit_pos(r0, c0, n, c, r, j);
+          Ys[r * kMS + j] = acc[n][c];
+        }
+    }
     __syncthreads();
     store_mat(Y + ((size_t)bh * ny + t % ny) * mm, Ys, m);
-    mm64tc<false, false>(Xa, Ys, K, acc);  // X_{t+1} = 2 X_t - X_t Y_t
+    for (int i = warp; i < us.n; i += kNsThreads / 32) {  // X_{t+1} = 2 X_t - X_t Y_t
+      int r0, c0;
+      us.at(i, r0, c0);
+      float acc[2][4];
+      unit_mm<false, false>(Xa, Ys, r0, c0, us.K8, 0, 1, acc);
 #pragma unroll
-    for (int n = 0; n < 2; ++n)
+      for (int n = 0; n < 2; ++n)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int o = tc_off(n, c);
-        Xb[o] = 2.f * Xa[o] - acc[n][c];
-      }
+        for (int c = 0; c < 4; ++c) {
+          int r, j;
+          unit_pos(r0, c0, n, c, r, j);
+          Xb[r * kMS + j] = 2.f * Xa[r * kMS + j] - acc[n][c];
+        }
+    }
     __syncthreads();
     store_mat(X + ((size_t)bh * nx + (t + 1) % nx) * mm, Xb, m);
     float* tmp = Xa; Xa = Xb; Xb = tmp;
@@ -551,12 +592,14 @@ cudaError_t run_gram_bwd(const Prob& p, const float* L, const float* Llo, const 
 
 // ---------------------------------------------------------------------------
 // Newton-Schulz backward for m <= 64, one CTA per slice, all on chip.
-// Reverse of X_{t+1} = 2 X_t - X_t A X_t with upstream G = dLoss/dX_{t+1}:
-//   dA  -= X_t^T G X_t^T
-//   G    = 2 G - G Y_t^T - A^T (X_t^T G)          (Y_t = A X_t)
+// Reverse of X_{t+1} = 2 X_t - X_t A X_t with upstream G = dLoss/dX_{t+1},
+// the exact adjoint of the forward's own products:
+//   XG  = X_t^T G,   Tm = 2 G - G Y_t^T              (phase 1, independent)
+//   dA -= XG X_t^T,  G  = Tm - A^T XG                 (phase 2, independent)
 // then X_0 = alpha A contributes alpha G and, through alpha = 1/(n1 ninf),
 // dalpha = <G, A> spread over the maximising column (n1) and row (ninf).
-// GT holds dLoss/dX_T on entry.
+// GT holds dLoss/dX_T on entry.  The 16 warps take two 16 x 16 blocks of a
+// phase's two products each; X_t and Y_t arrive one step ahead (cp.async).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kNsThreads) k_ns_bwd_small(const float* __restrict__ A,
                                                              const float* __restrict__ info,
@@ -571,12 +614,14 @@ __global__ void __launch_bounds__(kNsThreads) k_ns_bwd_small(const float* __rest
   float* Yt2 = Xt2 + 2 * 64 * kMS;    // Y_t, likewise
   float* G = Yt2 + 2 * 64 * kMS;
   float* XG = G + 64 * kMS;
-  float* dAs = XG + 64 * kMS;
-  float* Tm = dAs + 64 * kMS;
+  float* Tm = XG + 64 * kMS;
+  float* dAs = Tm + 64 * kMS;
   __shared__ float red[kNsThreads];
   const int bh = blockIdx.x;
   const size_t mm = (size_t)m * m;
-  const int K = (m + 3) & ~3;
+  const UnitSet us(m);
+  const int warp = threadIdx.x >> 5;
+  constexpr int kW = kNsThreads / 32;
   auto fetch = [&](int t, int buf) {
     load_mat_async(Xt2 + buf * 64 * kMS, X + ((size_t)bh * nx + t % nx) * mm, m);
     load_mat_async(Yt2 + buf * 64 * kMS, Y + ((size_t)bh * ny + t % ny) * mm, m);
@@ -587,42 +632,58 @@ __global__ void __launch_bounds__(kNsThreads) k_ns_bwd_small(const float* __rest
   load_mat(As, A + bh * mm, m);
   load_mat(G, GT + bh * mm, m);
   for (int e = threadIdx.x; e < 64 * kMS; e += kNsThreads) dAs[e] = 0.f;
-  float acc[2][4];
   for (int t = iters - 1; t >= 0; --t) {
     const int buf = (iters - 1 - t) & 1;
     const float* Xt = Xt2 + buf * 64 * kMS;
     const float* Yt = Yt2 + buf * 64 * kMS;
     cp_wait_all();
-    __syncthreads();  // step t's X_t, Y_t landed; step t + 1 is done with the other buffers
+    __syncthreads();  // step t's X_t, Y_t and G landed; step t + 1 is done with the other buffers
     if (t > 0) fetch(t - 1, buf ^ 1);
-    mm64tc<true, false>(Xt, G, K, acc);  // XG = X_t^T G
+    for (int i = warp; i < 2 * us.n; i += kW) {
+      const bool second = i >= us.n;
+      int r0, c0;
+      us.at(second ? i - us.n : i, r0, c0);
+      float acc[2][4];
+      if (second)
+        unit_mm<false, true>(G, Yt, r0, c0, us.K8, 0, 1, acc);  // G Y_t^T
+      else
+        unit_mm<true, false>(Xt, G, r0, c0, us.K8, 0, 1, acc);  // XG = X_t^T G
 #pragma unroll
-    for (int n = 0; n < 2; ++n)
+      for (int n = 0; n < 2; ++n)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) XG[tc_off(n, c)] = acc[n][c];
+        for (int c = 0; c < 4; ++c) {
+          int r, j;
+          unit_pos(r0, c0, n, c, r, j);
+          const int o = r * kMS + j;
+          if (second)
+            Tm[o] = 2.f * G[o] - acc[n][c];
+          else
+            XG[o] = acc[n][c];
+        }
+    }
     __syncthreads();
-    mm64tc<false, true>(XG, Xt, K, acc);  // dA -= XG X_t^T
+    for (int i = warp; i < 2 * us.n; i += kW) {
+      const bool second = i >= us.n;
+      int r0, c0;
+      us.at(second ? i - us.n : i, r0, c0);
+      float acc[2][4];
+      if (second)
+        unit_mm<true, false>(As, XG, r0, c0, us.K8, 0, 1, acc);  // A^T XG
+      else
+        unit_mm<false, true>(XG, Xt, r0, c0, us.K8, 0, 1, acc);  // XG X_t^T
 #pragma unroll
-    for (int n = 0; n < 2; ++n)
+      for (int n = 0; n < 2; ++n)
 #pragma unroll
-      for (int c = 0; c < 4; ++c) dAs[tc_off(n, c)] -= acc[n][c];
-    mm64tc<false, true>(G, Yt, K, acc);  // Tm = 2 G - G Y_t^T
-#pragma unroll
-    for (int n = 0; n < 2; ++n)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int o = tc_off(n, c);
-        Tm[o] = 2.f * G[o] - acc[n][c];
-      }
-    __syncthreads();
-    mm64tc<true, false>(As, XG, K, acc);  // G = Tm - A^T XG
-#pragma unroll
-    for (int n = 0; n < 2; ++n)
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int o = tc_off(n, c);
-        G[o] = Tm[o] - acc[n][c];
-      }
+        for (int c = 0; c < 4; ++c) {
+          int r, j;
+          unit_pos(r0, c0, n, c, r, j);
+          const int o = r * kMS + j;
+          if (second)
+            G[o] = Tm[o] - acc[n][c];
+          else
+            dAs[o] -= acc[n][c];
+        }
+    }
   }
   cp_wait_all();
   __syncthreads();

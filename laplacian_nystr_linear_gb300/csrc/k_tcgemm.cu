@@ -72,10 +72,10 @@ __device__ __forceinline__ uint32_t kmaj_off(int row, int k, uint32_t lbo) {
          (uint32_t)(k & 3) * 4u;
 }
 
+// x = hi + lo with hi rounded to the nearest TF32 value (halfway cases away
+// from zero: half an ulp added to the magnitude bits, 13 low bits cleared)
 __device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
-  uint32_t h;
-  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(h) : "f"(x));
-  hi = __uint_as_float(h);
+  hi = __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
   lo = x - hi;
 }
 
