@@ -139,6 +139,9 @@ void* tensor_map_encoder();
 bool encode_tiled_f32(CUtensorMap* t, int rank, const void* p, const cuuint64_t* dim,
                       const cuuint64_t* stride, const cuuint32_t* box);
 // a tiled bf16 map with the 128-byte swizzle (box rows of 64 elements)
+// the same with 128-byte swizzle (the inner box must be 32 floats = 128 bytes)
+bool encode_tiled_f32_sw128(CUtensorMap* t, int rank, const void* p, const cuuint64_t* dim,
+                            const cuuint64_t* stride, const cuuint32_t* box);
 bool encode_tiled_bf16_sw128(CUtensorMap* t, int rank, const void* p, const cuuint64_t* dim,
                              const cuuint64_t* stride, const cuuint32_t* box);
 
@@ -183,9 +186,11 @@ cudaError_t run_gemm_wgrad(const char* name, const GemmDims& g, int a_kind,
 // [BH][N][mp] and dW [BH][m][d]; writes dv [BH][N][d] in bf16
 bool dv_tc_ok(const Prob& p);
 // out[BH][N][d] (bf16) = C[BH][N][mp] (fp32, token-major) R[BH][m][d] (fp32): dV = C dW,
-// or the forward's O = C W-hat when Q = K (P = C^T)
-cudaError_t run_dv(const Prob& p, const float* C, const float* R, void* out, const char* name,
-                   cudaStream_t st);
+// or the forward's O = C W-hat when Q = K (P = C^T).  img: dv_image_floats(p)
+// floats of scratch for R^T as the product's operand image.
+size_t dv_image_floats(const Prob& p);
+cudaError_t run_dv(const Prob& p, const float* C, const float* R, float* img, void* out,
+                   const char* name, cudaStream_t st);
 // FP32 FMA-rate probe: a grid of 8 CTAs of 256 threads per SM, each thread
 // `iters` x 8 independent FMAs (paired: fma.rn.f32x2, two lane-ops each);
 // *lane_ops = the FP32 lane-ops the launch executes

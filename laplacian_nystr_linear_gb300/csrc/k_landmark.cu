@@ -729,42 +729,48 @@ cudaError_t run_ns_bwd_small(const Prob& p, const float* A, const float* alpha, 
 // alpha part of the Newton-Schulz backward for any m: one CTA per slice.
 //   dA += alpha G;  dalpha = <G, A>;  dA[:, j*] += dalpha (-alpha / n1);
 //   dA[i*, :] += dalpha (-alpha / ninf)
+// The slice's m^2 elements are streamed twice (the sum, then the update) by
+// 1024 threads, eight independent loads in flight per thread.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads) k_alpha_bwd(const float* __restrict__ A,
-                                                        const float* __restrict__ info,
-                                                        const float* __restrict__ G,
-                                                        float* __restrict__ dA, int m) {
-  __shared__ float red[kThreads];
+constexpr int kAlphaThreads = 1024;
+__global__ void __launch_bounds__(kAlphaThreads) k_alpha_bwd(const float* __restrict__ A,
+                                                             const float* __restrict__ info,
+                                                             const float* __restrict__ G,
+                                                             float* __restrict__ dA, int m) {
+  __shared__ float red[kAlphaThreads / 32];
   const int bh = blockIdx.x;
   const size_t mm = (size_t)m * m;
   const float* Ab = A + bh * mm;
   const float* Gb = G + bh * mm;
   float* dAb = dA + bh * mm;
   float part = 0.f;
-  for (size_t e = threadIdx.x; e < mm; e += kThreads) part += Gb[e] * Ab[e];
-  red[threadIdx.x] = part;
+#pragma unroll 8
+  for (size_t e = threadIdx.x; e < mm; e += kAlphaThreads) part += __ldg(Gb + e) * __ldg(Ab + e);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = part;
   __syncthreads();
-  for (int w = kThreads / 2; w > 0; w >>= 1) {
-    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
-    __syncthreads();
-  }
-  const float dal = red[0];
+  float dal = 0.f;
+  for (int w = 0; w < kAlphaThreads / 32; ++w) dal += red[w];  // fixed order: deterministic
   const float* in = info + (size_t)bh * 4;
   const float al = in[0], n1 = in[1], ninf = in[2];
   const int code = __float_as_int(in[3]);
   const int jc = code & 0xffff, ir = code >> 16;
-  for (size_t e = threadIdx.x; e < mm; e += kThreads) {
-    const int i = (int)(e / m), j = (int)(e % m);
-    float v = dAb[e] + al * Gb[e];
-    if (j == jc) v += dal * (-al / n1);
-    if (i == ir) v += dal * (-al / ninf);
+  const float cj = dal * (-al / n1), ci = dal * (-al / ninf);
+#pragma unroll 8
+  for (size_t e = threadIdx.x; e < mm; e += kAlphaThreads) {
+    const int i = (int)(e / m), j = (int)(e - (size_t)i * m);
+    float v = dAb[e] + al * __ldg(Gb + e);
+    if (j == jc) v += cj;
+    if (i == ir) v += ci;
     dAb[e] = v;
   }
 }
 
 cudaError_t run_alpha_bwd(const Prob& p, const float* A, const float* alpha, const float* G,
                           float* dA, cudaStream_t st) {
-  return launch("alpha_bwd", k_alpha_bwd, dim3(p.BH), dim3(kThreads), 0, st, A, alpha, G, dA, p.m);
+  return launch("alpha_bwd", k_alpha_bwd, dim3(p.BH), dim3(kAlphaThreads), 0, st, A, alpha, G, dA,
+                p.m);
 }
 
 }  // namespace lapnys

@@ -669,6 +669,16 @@ bool encode_tiled_f32(CUtensorMap* t, int rank, const void* p, const cuuint64_t*
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_tiled_f32_sw128(CUtensorMap* t, int rank, const void* p, const cuuint64_t* dim,
+                            const cuuint64_t* stride, const cuuint32_t* box) {
+  EncodeTiled fn = encoder();
+  if (fn == nullptr || rank < 1 || rank > 5) return false;
+  const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return fn(t, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)rank, const_cast<void*>(p), dim, stride,
+            box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_tiled_bf16_sw128(CUtensorMap* t, int rank, const void* p, const cuuint64_t* dim,
                              const cuuint64_t* stride, const cuuint32_t* box) {
   EncodeTiled fn = encoder();

@@ -172,6 +172,7 @@ struct WsLayout {
   size_t dQp, dKp, dVp;                        // backward token-side partials
   size_t dWh, dW, dLA, dL, G, XG, Tm, dA;      // backward landmark-side results
   size_t ties, tie_scratch;                    // tie records (query, key) and their scratch
+  size_t dvimg;                                // R^T operand image of the streaming C R product
   size_t total;
 };
 
@@ -204,6 +205,8 @@ static WsLayout ws_layout(const Prob& p) {
   w.dA = o; o = align256(o + BH * m * m * f);
   w.ties = o; o = align256(o + 2 * BH * (size_t)((p.N + 31) / 32) * kTieRec * 4);
   w.tie_scratch = o; o = align256(o + ties_scratch_bytes(p.BH, p.m, p.d));
+  // sized from the shape alone (the size queries know no element type)
+  w.dvimg = o; o = align256(o + (d == 32 || d == 64 ? dv_image_floats(p) * f : 0));
   w.total = o;
   return w;
 }
@@ -492,7 +495,8 @@ int lapnys_fwd(const void* q, const void* k, const void* v, void* out, int B, in
   // O = C W-hat, read once from ctx instead of recomputing the distances; the
   // backward reads C as P (a tied forward stores no separate P).
   if (full && tied_qk && !p.norm() && dv_tc_ok(p)) {
-    CK(run_dv(p, (const float*)(cb + c.C), What, out, "query_shared", stream));
+    CK(run_dv(p, (const float*)(cb + c.C), What, (float*)(wb + w.dvimg), out, "query_shared",
+              stream));
     return LAPNYS_OK;
   }
   float* Pout = full && !tied_qk ? (float*)(cb + c.P) : nullptr;
@@ -763,7 +767,7 @@ int lapnys_bwd(const void* q, const void* k, const void* v, const void* dout, co
     // hires16k step than the other order)
     const float* Cm = (const float*)(cb + c.C);
     if (dv_tc_ok(p))
-      CK(run_dv(p, Cm, dW, dv, "dv", stream));
+      CK(run_dv(p, Cm, dW, (float*)(wb + w.dvimg), dv, "dv", stream));
     else
       CK(ns_mm(p, false, false, N, d, m, Cm, p.mp, (long)N * p.mp, dW, d, md, dVp, d, (long)N * d,
                nullptr, d, 0, 1.f, 0.f, stream));
