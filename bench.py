@@ -133,23 +133,26 @@ def fp32_pipe_ops(w):
 
 def measured_traffic(workload: str, method_kernel: str, kernel: str):
     """DRAM bytes per launch of `kernel` from the ncu capture recorded in
-    profiles/traffic_<workload>.json, or None when there is no record for it
-    (this GPU kernel, this attention kernel) or its source file has changed
-    since the counters were taken."""
+    profiles/traffic_<workload>.json ("bytes_per_launch": {kernel: bytes}), or
+    None when there is no record for it (this GPU kernel, this attention kernel)
+    or its source file has changed since the counters were taken."""
     import hashlib
     path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles",
                         f"traffic_{workload}.json")
     try:
         with open(path) as f:
             rec = json.load(f)
-        if rec.get("kernel") != kernel or rec.get("method_kernel", "laplace") != method_kernel:
+        if rec.get("method_kernel", "laplace") != method_kernel:
+            return None
+        per = rec["bytes_per_launch"]
+        if kernel not in per:
             return None
         src = os.path.join(os.path.dirname(os.path.abspath(__file__)), rec["source"])
         with open(src, "rb") as f:
             if hashlib.sha256(f.read()).hexdigest() != rec["source_sha256"]:
                 return None
-        return float(rec["bytes_per_launch"])
-    except (OSError, KeyError, ValueError):
+        return float(per[kernel])
+    except (OSError, KeyError, ValueError, TypeError):
         return None
 
 

@@ -214,6 +214,26 @@ SMALL = [
 ]
 
 
+# Many slices of one or two 128-token tiles: the streaming C R product (dV, and
+# the tied forward's O = C W-hat) then walks several slices per CTA, reusing its
+# two operand-image buffers, with ragged last tiles.
+MANY_SLICES = [
+    _small("many_slices", dtype="bf16", B=40, H=16, d=64, m=16, iters=6),
+    _small("many_slices_tied", dtype="bf16", B=40, H=16, d=64, m=16, iters=6, tied=True),
+    _small("many_slices_d32_ragged", dtype="bf16", B=20, H=8, grid_h=12, grid_w=12, d=32, m=36,
+           iters=6),
+]
+
+
+@pytest.mark.parametrize("w", MANY_SLICES, ids=lambda w: w.name)
+def test_streaming_product_many_slices(w):
+    inp = random_inputs(61 + w.m, w.B, w.H, w.N, w.d, w.dtype, tied=w.tied)
+    g = gpu_run(w, inp, backward=True)
+    slices = [(b, h) for b in range(0, w.B, 7) for h in range(0, w.H, 5)] + [(w.B - 1, w.H - 1)]
+    o = oracle_run(w, inp, slices=slices, backward=True)
+    print(w.name, len(slices), compare(w, g, o, backward=True))
+
+
 @pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
 def test_backward_small_cases(w):
     inp = random_inputs(7 + w.m + w.d, w.B, w.H, w.N, w.d, w.dtype, tied=w.tied)
