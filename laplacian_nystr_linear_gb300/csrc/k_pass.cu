@@ -428,6 +428,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int gq = lane >> 2, tg = lane & 3;
   const int wj = (warp & 3) * 16, wc = (warp >> 2) * (D / 2);  // tensor-core fragment origin
   const T* Qb = Q + (size_t)bh * N * D;
+  // O null: only the kernel values P go out (to kvout), no contraction
+  const bool ponly = O == nullptr;
   load_tile<D>(Xs, Qb, b * kTile, N);
   float o[4][CPT];
 #pragma unroll
@@ -444,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     float* Lsb = LW + (lt & 1) * 2 * tile_floats(D);
     float* Wsb = Lsb + tile_floats(D);
     const int a0 = lt * kTile;
-    for (int id = threadIdx.x; id < 2 * kTile * (D / 4); id += kThreads) {
+    for (int id = threadIdx.x; id < (ponly ? 1 : 2) * kTile * (D / 4); id += kThreads) {
       const int which = id / (kTile * (D / 4)), rem = id % (kTile * (D / 4));
       const int r = rem / (D / 4), c4 = rem % (D / 4);
       const bool ok = a0 + r < m;
@@ -479,12 +481,14 @@ __global__ void __launch_bounds__(kThreads, 2)
         // keep the kernel value (before normalisation) for the backward
         const int j = b * kTile + 4 * ty + r;
         if (kvout && j < N) kvout[((size_t)bh * N + j) * (nt * kTile) + a0 + a] = pv;
+        if (ponly) continue;
         if (NORM && a0 + a < m) pv = (pv - mu_s[a]) * rs_s[a];
         if (kTC)
           Pt[(4 * ty + r) * 68 + a] = pv;
         else
           Pt[a * 68 + 4 * ty + r] = pv;
       }
+    if (ponly) continue;  // uniform over the CTA
     __syncthreads();
     if constexpr (kTC) {
       // O += Z W-hat on the tensor cores with both factors split into TF32 hi + lo
@@ -529,6 +533,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
   }
+  if (ponly) return;
   if constexpr (kTC) {
     const int j1 = b * kTile + wj + gq, j2 = j1 + 8;
 #pragma unroll
@@ -561,8 +566,8 @@ static cudaError_t query_fwd_t(const Prob& p, const void* q, const float* L, con
   do {                                                                                         \
     static bool once = (allow_smem(k_query_fwd<D, T, NN, GG>, smem), true);                    \
     (void)once;                                                                                \
-    return launch("query_fwd", k_query_fwd<D, T, NN, GG>, grid, dim3(kThreads), smem, st,      \
-                  (const T*)q, L, What, stats, (T*)out, kvout, p.N, p.m, p.nt, p.ns);          \
+    return launch(out ? "query_fwd" : "query_p", k_query_fwd<D, T, NN, GG>, grid, dim3(kThreads), \
+                  smem, st, (const T*)q, L, What, stats, (T*)out, kvout, p.N, p.m, p.nt, p.ns); \
   } while (0)
   if (p.norm()) {
     if (p.gauss()) QF_LAUNCH(true, true);

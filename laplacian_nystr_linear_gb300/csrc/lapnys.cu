@@ -485,11 +485,22 @@ int lapnys_fwd(const void* q, const void* k, const void* v, void* out, int B, in
     CK(run_key_fwd(p, k, v, L, kpart, full ? (float*)(cb + c.C) : nullptr, stream));
     CK(run_reduce_parts(p.BH, p.Sk, m, p.mp, d, kpart, W, stream));
   }
+  // With a ctx kept and no feature map, the query pass's kernel values P = k(Q, L)
+  // (which the ctx keeps for the backward) do not depend on the solver: on the
+  // FMA path they are formed here, beside it, and O = P W-hat is the streaming
+  // product once W-hat exists.
+  const bool split_q = full && !tied_qk && !p.norm() && !tc && dv_tc_ok(p);
+  if (split_q) CK(run_query_fwd(p, q, L, nullptr, stats, nullptr, (float*)(cb + c.P), stream));
   if (sd) CK(join(stream, ss, sd->ev[1]));
   const float* XT = X + (long)(iters % c.nx) * mm;
   // W-hat = X_T W
   CK(ns_mm(p, false, false, m, d, m, XT, m, c.nx * mm, W, d, (long)m * d, What, d, (long)m * d,
            nullptr, d, 0, 1.f, 0.f, stream));
+  if (split_q) {
+    CK(run_dv(p, (const float*)(cb + c.P), What, (float*)(wb + w.dvimg), out, "query_product",
+              stream));
+    return LAPNYS_OK;
+  }
   // Q = K: P = k(Q, L) is C^T, and the key pass has just stored C token-major
   // (the layout of P).  Without a feature map the query pass is then the product
   // O = C W-hat, read once from ctx instead of recomputing the distances; the
