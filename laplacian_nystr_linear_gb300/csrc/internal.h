@@ -210,6 +210,10 @@ cudaError_t run_reduce_parts(int BH, int S, int m, int mp, int d, const float* p
                              cudaStream_t st);
 cudaError_t run_qstats(const Prob& p, const void* q, const float* L, float* spart, cudaStream_t st);
 cudaError_t run_stats_final(const Prob& p, const float* spart, float* stats, cudaStream_t st);
+// the statistics partials of k_qstats from kernel values P already in memory
+cudaError_t run_pstats(const Prob& p, const float* P, float* spart, cudaStream_t st);
+// Z = (P - mu) * rsqrt(var + eta), 0 past m, from P and the statistics
+cudaError_t run_zmap(const Prob& p, const float* P, const float* stats, float* Z, cudaStream_t st);
 cudaError_t run_query_fwd(const Prob& p, const void* q, const float* L, const float* What,
                           const float* stats, void* out, float* kvout, cudaStream_t st);
 

@@ -330,6 +330,79 @@ cudaError_t run_qstats(const Prob& p, const void* q, const float* L, float* spar
   DISPATCH_DT(qstats_t, p, q, L, spart, st);
 }
 
+// The same partial triples from kernel values P already in memory ([BH][N][mp],
+// as the query pass stores them for the backward): per 64-token block, the
+// block's 64 x 64 tile is staged in shared memory and reduced exactly as above,
+// so the partials are bit-identical to the pass that forms P itself.
+// grid (landmark tile, split, slice)
+__global__ void __launch_bounds__(kThreads) k_pstats(const float* __restrict__ P,
+                                                     float* __restrict__ spart, int N, int mp,
+                                                     int S, int nblk) {
+  __shared__ float Ps[kTile * 68];
+  const int lt = blockIdx.x, sp = blockIdx.y, bh = blockIdx.z;
+  const int a0 = lt * kTile;
+  const float* Pb = P + (size_t)bh * N * mp + a0;
+  float n = 0.f, mean = 0.f, M2 = 0.f;
+  int b0, b1;
+  split_range(nblk, S, sp, b0, b1);
+  for (int b = b0; b < b1; ++b) {
+    const int nb = min(kTile, N - b * kTile);
+    __syncthreads();
+    for (int id = threadIdx.x; id < nb * (kTile / 4); id += kThreads) {
+      const int j = id / (kTile / 4), c4 = id % (kTile / 4);
+      st4(Ps + j * 68 + 4 * c4, ld4(Pb + (size_t)(b * kTile + j) * mp + 4 * c4));
+    }
+    __syncthreads();
+    if (threadIdx.x < kTile) {
+      float sum = 0.f;
+      for (int j = 0; j < nb; ++j) sum += Ps[j * 68 + threadIdx.x];
+      const float mb = sum / (float)nb;
+      float m2b = 0.f;
+      for (int j = 0; j < nb; ++j) {
+        const float dv = Ps[j * 68 + threadIdx.x] - mb;
+        m2b = fmaf(dv, dv, m2b);
+      }
+      chan_merge(n, mean, M2, (float)nb, mb, m2b);
+    }
+  }
+  if (threadIdx.x < kTile) {
+    float* o = spart + ((size_t)bh * S + sp) * 3 * mp + a0 + threadIdx.x;
+    o[0] = n;
+    o[mp] = mean;
+    o[2 * mp] = M2;
+  }
+}
+
+cudaError_t run_pstats(const Prob& p, const float* P, float* spart, cudaStream_t st) {
+  return launch("pstats", k_pstats, dim3(p.nt, p.Sq, p.BH), dim3(kThreads), 0, st, P, spart, p.N,
+                p.mp, p.Sq, p.nblk);
+}
+
+// Z = (P - mu) / sqrt(var + eta) per landmark column (the normalised feature map),
+// 0 past m; P and Z [BH][N][mp], stats [BH][3][m].  Four columns a thread.
+__global__ void k_zmap(const float* __restrict__ P, const float* __restrict__ stats,
+                       float* __restrict__ Z, int N, int m, int mp, long long n4) {
+  const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= n4) return;
+  const int per = mp / 4;
+  const long long row = e / per;
+  const int a = 4 * (int)(e - row * per);
+  const int bh = (int)(row / N);
+  const float* sb = stats + (size_t)bh * 3 * m;
+  const float4 pv = ld4(P + 4 * e);
+  const float in[4] = {pv.x, pv.y, pv.z, pv.w};
+  float out[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) out[q] = a + q < m ? (in[q] - sb[a + q]) * sb[2 * m + a + q] : 0.f;
+  st4(Z + 4 * e, make_float4(out[0], out[1], out[2], out[3]));
+}
+
+cudaError_t run_zmap(const Prob& p, const float* P, const float* stats, float* Z, cudaStream_t st) {
+  const long long n4 = (long long)p.BH * p.N * p.mp / 4;
+  return launch("zmap", k_zmap, dim3((unsigned)((n4 + 255) / 256)), dim3(256), 0, st, P, stats, Z,
+                p.N, p.m, p.mp, n4);
+}
+
 // Statistics are taken per slice, or (batch-pooled) over the B slices of a
 // head: group g < H, member r < B is slice r H + g.
 //

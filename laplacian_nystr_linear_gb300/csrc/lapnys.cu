@@ -173,6 +173,7 @@ struct WsLayout {
   size_t dWh, dW, dLA, dL, G, XG, Tm, dA;      // backward landmark-side results
   size_t ties, tie_scratch;                    // tie records (query, key) and their scratch
   size_t dvimg;                                // R^T operand image of the streaming C R product
+  size_t zmap;                                 // normalised feature map Z (m <= 64, ctx kept)
   size_t total;
 };
 
@@ -207,6 +208,8 @@ static WsLayout ws_layout(const Prob& p) {
   w.tie_scratch = o; o = align256(o + ties_scratch_bytes(p.BH, p.m, p.d));
   // sized from the shape alone (the size queries know no element type)
   w.dvimg = o; o = align256(o + (d == 32 || d == 64 ? dv_image_floats(p) * f : 0));
+  w.zmap = o;
+  o = align256(o + ((d == 32 || d == 64) && p.norm() && m <= kTile ? BH * p.N * mp * f : 0));
   w.total = o;
   return w;
 }
@@ -485,20 +488,31 @@ int lapnys_fwd(const void* q, const void* k, const void* v, void* out, int B, in
     CK(run_key_fwd(p, k, v, L, kpart, full ? (float*)(cb + c.C) : nullptr, stream));
     CK(run_reduce_parts(p.BH, p.Sk, m, p.mp, d, kpart, W, stream));
   }
-  // With a ctx kept and no feature map, the query pass's kernel values P = k(Q, L)
-  // (which the ctx keeps for the backward) do not depend on the solver: on the
-  // FMA path they are formed here, beside it, and O = P W-hat is the streaming
-  // product once W-hat exists.
-  const bool split_q = full && !tied_qk && !p.norm() && !tc && dv_tc_ok(p);
-  if (split_q) CK(run_query_fwd(p, q, L, nullptr, stats, nullptr, (float*)(cb + c.P), stream));
+  // With a ctx kept, the query pass's kernel values P = k(Q, L) (which the ctx
+  // keeps for the backward) and the feature map's statistics do not depend on
+  // the solver: on the FMA path they are formed here, beside it (the statistics
+  // from the stored P, Z = (P - mu) / sqrt(var + eta) into the workspace), and
+  // O = Z W-hat is the streaming product once W-hat exists.
+  const bool split_q = full && !tied_qk && !tc && dv_tc_ok(p);
+  const float* Zq = (const float*)(cb + c.P);
+  if (split_q) {
+    CK(run_query_fwd(p, q, L, nullptr, stats, nullptr, (float*)(cb + c.P), stream));
+    if (p.norm()) {
+      float* spart = (float*)(wb + w.spart);
+      float* Z = (float*)(wb + w.zmap);
+      CK(run_pstats(p, (const float*)(cb + c.P), spart, stream));
+      CK(run_stats_final(p, spart, stats, stream));
+      CK(run_zmap(p, (const float*)(cb + c.P), stats, Z, stream));
+      Zq = Z;
+    }
+  }
   if (sd) CK(join(stream, ss, sd->ev[1]));
   const float* XT = X + (long)(iters % c.nx) * mm;
   // W-hat = X_T W
   CK(ns_mm(p, false, false, m, d, m, XT, m, c.nx * mm, W, d, (long)m * d, What, d, (long)m * d,
            nullptr, d, 0, 1.f, 0.f, stream));
   if (split_q) {
-    CK(run_dv(p, (const float*)(cb + c.P), What, (float*)(wb + w.dvimg), out, "query_product",
-              stream));
+    CK(run_dv(p, Zq, What, (float*)(wb + w.dvimg), out, "query_product", stream));
     return LAPNYS_OK;
   }
   // Q = K: P = k(Q, L) is C^T, and the key pass has just stored C token-major
