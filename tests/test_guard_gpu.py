@@ -80,6 +80,10 @@ ATTN = [
     ("bf16_tc_m256_d64", api.Params(1, 2, 32, 32, 64, 256, 64.0, 1e-3, 10)),
     ("bf16_tc_gauss_m100_d32", api.Params(1, 1, 18, 22, 32, 100, 32.0, 1e-3, 8, False, False, "gauss")),
     ("bf16_d128_m64", api.Params(1, 1, 16, 16, 128, 64, 128.0, 1e-3, 6)),
+    # m <= 64, Q != K with a ctx: kernel values beside the solver, the streaming
+    # product (and, with the feature map, statistics from the stored values, Z)
+    ("bf16_split_norm_m49_d64", api.Params(2, 2, 14, 14, 64, 49, 64.0, 1e-3, 8, False, True)),
+    ("bf16_split_ragged_m16_d32", api.Params(1, 3, 10, 12, 32, 16, 32.0, 1e-3, 6)),
 ]
 
 
@@ -94,9 +98,10 @@ def test_attention_buffers_guarded(name, p):
     dout = to_dev(inp["dout"], dtype)
     shape = tuple(q.shape)
 
-    # plain buffers
+    # plain buffers (the forward with and without a ctx may take different paths)
     out0, ctx0 = api.fwd(q, k, v, p, need_ctx=True)
     dq0, dk0, dv0 = api.bwd(q, k, v, dout, ctx0, p)
+    out0n, _ = api.fwd(q, k, v, p, need_ctx=False)
 
     # guarded buffers
     g_out, out = _guarded_tensor(shape, tdt)
@@ -123,7 +128,7 @@ def test_attention_buffers_guarded(name, p):
     torch.cuda.synchronize()
     assert g_out2.intact() and g_ws3.intact()
 
-    for got, ref in ((out, out0), (out2, out0), (dq, dq0), (dv, dv0), (dk, dk0)):
+    for got, ref in ((out, out0), (out2, out0n), (dq, dq0), (dv, dv0), (dk, dk0)):
         if ref is None:
             continue
         assert not torch.isnan(got.float()).any(), "an output element was not written"
