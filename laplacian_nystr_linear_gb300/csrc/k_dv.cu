@@ -87,10 +87,17 @@ __global__ void __launch_bounds__(256) k_dv_pack(const float* __restrict__ R, fl
   const int kb = blockIdx.x, bh = blockIdx.y;
   const float* Rb = R + (size_t)bh * m * D;
   uint8_t* blk = reinterpret_cast<uint8_t*>(img + ((size_t)bh * mp + 32 * kb) * D);
-  for (int e = threadIdx.x; e < 32 * D; e += 256) {
-    const int k = e / D, n = e - k * D, a = 32 * kb + k;
-    const float v = a < m ? __ldg(Rb + (size_t)a * D + n) : 0.f;
-    const float t = __uint_as_float((__float_as_uint(v) + 0x1000u) & 0xffffe000u);  // nearest TF32
+  constexpr int kPer = 32 * D / 256;  // elements a thread: all loads first, then the stores
+  float v[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = threadIdx.x + 256 * i, k = e / D, n = e - k * D, a = 32 * kb + k;
+    v[i] = a < m ? __ldg(Rb + (size_t)a * D + n) : 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = threadIdx.x + 256 * i, k = e / D, n = e - k * D;
+    const float t = __uint_as_float((__float_as_uint(v[i]) + 0x1000u) & 0xffffe000u);  // nearest TF32
     const uint32_t off = (uint32_t)n * 128u + ((uint32_t)((k >> 2) ^ (n & 7)) << 4) + (uint32_t)(k & 3) * 4u;
     *reinterpret_cast<float*>(blk + off) = t;
   }
