@@ -492,76 +492,127 @@ def run_ours(args, rank, world, local_rank):
     # end to end through the public API: pinned host inputs in, results back to host
     e2e = None
     if not args.no_e2e and args.block:
-        # per step: x and dy in; y and dx out (weights and their gradients stay resident)
+        # per step: x and dy in, y and dx out (the weights and their gradients stay
+        # resident), overlapped across steps as in the attention's end-to-end loop below:
+        # step i + 1's x and dy come in and step i's dx goes out while step i + 1
+        # computes, y goes out during its own backward
         pin = {n: host[n].pin_memory() for n in host}
         back = {n: torch.empty(x.shape, dtype=tdt).pin_memory() for n in ("y", "dx")}
         ne = max(3, min(args.steps, 10))
+        dbuf = [{n: torch.empty_like(x) for n in ("x", "dy")} for _ in range(2)]
+        obuf = [{n: torch.empty_like(x) for n in ("y", "dx")} for _ in range(2)]
+        cin, cout = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev_in, ev_fwd, ev_bwd, ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(4))
 
-        cs = torch.cuda.Stream(dev)
-        dy_dev = torch.empty_like(x)
-        ev = [torch.cuda.Event() for _ in range(3)]
+        def copy_in(b):
+            for n in ("x", "dy"):
+                dbuf[b][n].copy_(pin[n], non_blocking=True)
+            ev_in[b].record(cin)
 
-        def step_e2e():
-            # dy comes in while the forward runs, y goes out while the backward runs
-            xd = pin["x"].to(dev, non_blocking=True)
-            cs.wait_stream(stream)
-            with torch.cuda.stream(cs):
-                dy_dev.copy_(pin["dy"], non_blocking=True)
-                ev[0].record(cs)
-            yo, c = api.block_fwd(xd, wq, bq, wo, bo, bp, y=y, ctx=ctx, ws=ws)
-            ev[1].record(stream)
-            with torch.cuda.stream(cs):
-                cs.wait_event(ev[1])
-                back["y"].copy_(yo, non_blocking=True)
-                ev[2].record(cs)
-            stream.wait_event(ev[0])
-            g = api.block_bwd(xd, wq, wo, dy_dev, c, bp, dx=dx, dw_qkv=gw_q, db_qkv=gb_q,
-                              dw_o=gw_o, db_o=gb_o, ws=ws)
-            back["dx"].copy_(g[0], non_blocking=True)
-            stream.wait_event(ev[2])
+        def run_e2e(n):
+            with torch.cuda.stream(cin):
+                cin.wait_stream(stream)
+                copy_in(0)
+            for i in range(n):
+                b = i % 2
+                if i + 1 < n:
+                    with torch.cuda.stream(cin):
+                        if i >= 1:
+                            cin.wait_event(ev_bwd[1 - b])
+                        copy_in(1 - b)
+                stream.wait_event(ev_in[b])
+                if i >= 2:
+                    stream.wait_event(ev_out[b])
+                d, o_ = dbuf[b], obuf[b]
+                yo, c = api.block_fwd(d["x"], wq, bq, wo, bo, bp, y=o_["y"], ctx=ctx, ws=ws)
+                ev_fwd[b].record(stream)
+                with torch.cuda.stream(cout):
+                    cout.wait_event(ev_fwd[b])
+                    back["y"].copy_(yo, non_blocking=True)
+                g = api.block_bwd(d["x"], wq, wo, d["dy"], c, bp, dx=o_["dx"], dw_qkv=gw_q,
+                                  db_qkv=gb_q, dw_o=gw_o, db_o=gb_o, ws=ws)
+                ev_bwd[b].record(stream)
+                with torch.cuda.stream(cout):
+                    cout.wait_event(ev_bwd[b])
+                    back["dx"].copy_(g[0], non_blocking=True)
+                    ev_out[b].record(cout)
+            stream.wait_stream(cout)
 
-        step_e2e()
+        run_e2e(3)
         barrier()
-        ms_e2e = max_over_ranks(timed(step_e2e, ne), world, dev)
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea.record(stream)
+        run_e2e(ne)
+        eb.record(stream)
+        barrier()
+        ms_e2e = max_over_ranks(ea.elapsed_time(eb) / ne, world, dev)
         nbytes = x.numel() * x.element_size()
         e2e = {"value": world * w.tokens / (ms_e2e / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": 2 * nbytes, "d2h_bytes_per_step": 2 * nbytes,
                "ms_per_step": ms_e2e}
     elif not args.no_e2e:
+        # Every step copies its inputs (Q, K, V, dO) in from pinned host memory and its
+        # results (O, dQ, dK, dV) back, through the public API, as a training loop that
+        # overlaps its transfers would: two copy streams beside the compute stream and
+        # two device buffer sets, so that step i + 1's inputs come in and step i's
+        # gradients go out while step i + 1 computes; O goes out during its own
+        # backward.  The first step's inputs and the last step's gradients are not
+        # overlapped; the timed region holds every copy of every step.
         pin = {n: host[n].pin_memory() for n in host}
         back = {n: torch.empty(q.shape, dtype=tdt).pin_memory() for n in ("out", "dq", "dk", "dv")}
         ne = max(3, min(args.steps, 10))
+        names_in = ["q", "v", "dout"] + ([] if w.tied else ["k"])
+        dbuf = [{n: torch.empty_like(q) for n in names_in} for _ in range(2)]
+        obuf = [{n: torch.empty_like(q) for n in ("out", "dq", "dk", "dv")} for _ in range(2)]
+        cin, cout = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev_in, ev_fwd, ev_bwd, ev_out = ([torch.cuda.Event() for _ in range(2)] for _ in range(4))
 
-        cs = torch.cuda.Stream(dev)
-        dd = torch.empty_like(q)
-        ev = [torch.cuda.Event() for _ in range(3)]
+        def copy_in(b):
+            for n in names_in:
+                dbuf[b][n].copy_(pin[n], non_blocking=True)
+            ev_in[b].record(cin)
 
-        def step_e2e():
-            # dO comes in while the forward runs, out goes back while the backward runs
-            qd = pin["q"].to(dev, non_blocking=True)
-            kd = qd if w.tied else pin["k"].to(dev, non_blocking=True)
-            vd = pin["v"].to(dev, non_blocking=True)
-            cs.wait_stream(stream)
-            with torch.cuda.stream(cs):
-                dd.copy_(pin["dout"], non_blocking=True)
-                ev[0].record(cs)
-            o, c = api.fwd(qd, kd, vd, p, out=out, ctx=ctx, ws=ws)
-            ev[1].record(stream)
-            with torch.cuda.stream(cs):
-                cs.wait_event(ev[1])
-                back["out"].copy_(o, non_blocking=True)
-                ev[2].record(cs)
-            stream.wait_event(ev[0])
-            gq, gk, gv = api.bwd(qd, kd, vd, dd, c, p, dq=dq, dk=dk, dv=dv, ws=ws)
-            back["dq"].copy_(gq, non_blocking=True)
-            if gk is not None:
-                back["dk"].copy_(gk, non_blocking=True)
-            back["dv"].copy_(gv, non_blocking=True)
-            stream.wait_event(ev[2])
+        def run_e2e(n):
+            with torch.cuda.stream(cin):
+                cin.wait_stream(stream)
+                copy_in(0)
+            for i in range(n):
+                b = i % 2
+                if i + 1 < n:  # the next step's inputs, into the buffer step i - 1 used
+                    with torch.cuda.stream(cin):
+                        if i >= 1:
+                            cin.wait_event(ev_bwd[1 - b])
+                        copy_in(1 - b)
+                stream.wait_event(ev_in[b])
+                if i >= 2:
+                    stream.wait_event(ev_out[b])  # step i - 2's results are on the host
+                d, o_ = dbuf[b], obuf[b]
+                kd = d["q"] if w.tied else d["k"]
+                o, c = api.fwd(d["q"], kd, d["v"], p, out=o_["out"], ctx=ctx, ws=ws)
+                ev_fwd[b].record(stream)
+                with torch.cuda.stream(cout):
+                    cout.wait_event(ev_fwd[b])
+                    back["out"].copy_(o, non_blocking=True)
+                gq, gk, gv = api.bwd(d["q"], kd, d["v"], d["dout"], c, p, dq=o_["dq"],
+                                     dk=None if w.tied else o_["dk"], dv=o_["dv"], ws=ws)
+                ev_bwd[b].record(stream)
+                with torch.cuda.stream(cout):
+                    cout.wait_event(ev_bwd[b])
+                    back["dq"].copy_(gq, non_blocking=True)
+                    if gk is not None:
+                        back["dk"].copy_(gk, non_blocking=True)
+                    back["dv"].copy_(gv, non_blocking=True)
+                    ev_out[b].record(cout)
+            stream.wait_stream(cout)  # the last step's results are on the host
 
-        step_e2e()
+        run_e2e(3)
         barrier()
-        ms_e2e = max_over_ranks(timed(step_e2e, ne), world, dev)
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea.record(stream)
+        run_e2e(ne)
+        eb.record(stream)
+        barrier()
+        ms_e2e = max_over_ranks(ea.elapsed_time(eb) / ne, world, dev)
         nbytes = q.numel() * q.element_size()
         n_in = 3 if w.tied else 4
         n_out = 3 if w.tied else 4
