@@ -211,6 +211,11 @@ SMALL = [
     # one landmark per token with Q = K: every token ties with its own landmark
     _small("bf16_tied_mN", dtype="bf16", d=64, grid_h=4, grid_w=4, m=16, iters=6, tied=True),
     _small("bf16_mN", dtype="bf16", d=32, grid_h=8, grid_w=8, m=64, iters=6),
+    # bf16, m <= 64 with the feature map and a ctx: kernel values beside the solver,
+    # statistics from the stored values, Z, then the streaming product
+    _small("bf16_norm_ragged", dtype="bf16", d=64, grid_h=10, grid_w=12, m=9, iters=6, norm=True),
+    _small("bf16_norm_d32", dtype="bf16", d=32, grid_h=12, grid_w=12, m=36, iters=8, norm=True,
+           B=2, H=2),
 ]
 
 
@@ -480,7 +485,7 @@ def test_batch_pooled_statistics_pvt2_full_batch():
 # Gaussian-kernel variant (LAPNYS_GAUSS): k(x, y) = exp(-|x - y|_2^2 / lambda)
 # ---------------------------------------------------------------------------
 GAUSS_NAMES = ("f32", "f32_norm", "f32_tied", "bf16", "ragged", "ragged_large_m", "m1", "iters0",
-               "d128", "m81", "batch", "bf16_mN")
+               "d128", "m81", "batch", "bf16_mN", "bf16_norm_ragged")
 GAUSS_SMALL = ([dataclasses.replace(w, name="gauss_" + w.name, kernel="gauss")
                 for w in SMALL if w.name in GAUSS_NAMES]
                + [dataclasses.replace(w, name="gauss_" + w.name, kernel="gauss") for w in TC_FWD])
