@@ -283,14 +283,13 @@ __device__ __forceinline__ void issue_stage(uint8_t* raw, const Prod& p, int i0,
 }
 
 // op(A) of one stage for splitter lane `row` (0..127 of the panel), k-step ah
-// (k = 8 ah .. 8 ah + 7): split and written to TMEM columns colh, coll (+0..7)
-// of this warp's lane quarter (warp-collective).  Raw layout: kc box: row r's
-// 16 k values in 64 bytes at 64 r, its 16-byte piece k4 swizzled to slot
-// k4 ^ ((r / 2) % 4) (the 64-byte swizzle: lanes reading one piece of 32 rows
-// then hit every bank once per 8 lanes); mn box: value (k, row) at 4 (128 k + row).
-__device__ __forceinline__ void split_a(const uint8_t* ra, bool kc, int row, int ah, uint32_t colh,
-                                        uint32_t coll) {
-  float v[8];
+// (k = 8 ah .. 8 ah + 7): read from the raw slot (load_a), then split and
+// written to TMEM columns colh, coll (+0..7) of this warp's lane quarter
+// (store_a, warp-collective).  Raw layout: kc box: row r's 16 k values in 64
+// bytes at 64 r, its 16-byte piece k4 swizzled to slot k4 ^ ((r / 2) % 4) (the
+// 64-byte swizzle: lanes reading one piece of 32 rows then hit every bank once
+// per 8 lanes); mn box: value (k, row) at 4 (128 k + row).
+__device__ __forceinline__ void load_a(const uint8_t* ra, bool kc, int row, int ah, float (&v)[8]) {
   if (kc) {
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
@@ -302,6 +301,8 @@ __device__ __forceinline__ void split_a(const uint8_t* ra, bool kc, int row, int
 #pragma unroll
     for (int j = 0; j < 8; ++j) v[j] = r[TM * (8 * ah + j) + row];
   }
+}
+__device__ __forceinline__ void store_a(const float (&v)[8], uint32_t colh, uint32_t coll) {
   uint32_t hi[8], lo[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
@@ -321,27 +322,34 @@ __device__ __forceinline__ void store_transposed(uint8_t* hi, uint8_t* lo, uint3
   store_split(hi, lo, kmaj_off(4 * rb + 3, k4, lbo), make_float4(x[0].w, x[1].w, x[2].w, x[3].w));
 }
 
-// op(B)^T of one stage (256 rows x 16 k), thread ts of the 256 splitters.
-// Raw kc box: piece (row, k4) of 16 bytes at 64 row + 16 (k4 ^ ((row / 2) % 4));
-// thread ts takes row ts, pieces k4 = 0..3.  Raw 3-D box (mn): [16 k][256 rows]; thread ts takes
-// the 4-row block rb = ts % 64 at k4 = ts / 64 (four pieces along the rows,
-// transposed).  Consecutive lanes read consecutive 16-byte words.
-__device__ __forceinline__ void split_b(const uint8_t* rbase, bool kc, uint8_t* sp, int ts) {
+// op(B)^T of one stage (256 rows x 16 k), thread ts of the 256 splitters: four
+// 16-byte pieces read from the raw slot (load_b), then split and stored in the
+// K-major layout (store_b).  Raw kc box: piece (row, k4) of 16 bytes at
+// 64 row + 16 (k4 ^ ((row / 2) % 4)); thread ts takes row ts, pieces k4 = 0..3.
+// Raw 3-D box (mn): [16 k][256 rows]; thread ts takes the 4-row block
+// rb = ts % 64 at k4 = ts / 64 (four pieces along the rows, transposed).
+// Consecutive lanes read consecutive 16-byte words.
+__device__ __forceinline__ void load_b(const uint8_t* rbase, bool kc, int ts, float4 (&x)[4]) {
+  if (kc) {
+#pragma unroll
+    for (int k4 = 0; k4 < 4; ++k4)
+      x[k4] = *reinterpret_cast<const float4*>(rbase + 64 * ts + 16 * (k4 ^ ((ts >> 1) & 3)));
+  } else {
+    const int rb = ts % (TNMAX / 4), k4 = ts / (TNMAX / 4);
+    const float* r = reinterpret_cast<const float*>(rbase);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      x[j] = *reinterpret_cast<const float4*>(r + TNMAX * (4 * k4 + j) + 4 * rb);
+  }
+}
+__device__ __forceinline__ void store_b(const float4 (&x)[4], bool kc, uint8_t* sp, int ts) {
   uint8_t* bhi = sp;
   uint8_t* blo = sp + kTileB;
   if (kc) {
 #pragma unroll
-    for (int k4 = 0; k4 < 4; ++k4) {
-      const float4 x = *reinterpret_cast<const float4*>(rbase + 64 * ts + 16 * (k4 ^ ((ts >> 1) & 3)));
-      store_split(bhi, blo, kmaj_off(ts, k4, kLboB), x);
-    }
+    for (int k4 = 0; k4 < 4; ++k4) store_split(bhi, blo, kmaj_off(ts, k4, kLboB), x[k4]);
   } else {
     const int rb = ts % (TNMAX / 4), k4 = ts / (TNMAX / 4);
-    const float* r = reinterpret_cast<const float*>(rbase);
-    float4 x[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      x[j] = *reinterpret_cast<const float4*>(r + TNMAX * (4 * k4 + j) + 4 * rb);
     store_transposed(bhi, blo, kLboB, rb, k4, x);
   }
 }
@@ -410,31 +418,45 @@ __global__ void __launch_bounds__(NTH, 1)
       const int ts = tid;
       const int aq = warp & 3, ah = warp >> 2;  // TMEM lane quarter, op(A) k-step
       const uint32_t alane = (uint32_t)(32 * aq) << 16;
-      for (int c = 0; c < nchunks; ++c) {
+      // Software-pipelined: stage c + 1's raw values are read (and its raw slot
+      // released) while stage c's split stores drain, before stage c is
+      // published; the waits for stage c + 1 need only earlier stages' MMAs and
+      // copies, never stage c's.
+      float va[8];
+      float4 xb[4];
+      auto fetch = [&](int c) -> bool {  // wait for stage c and read it (all lanes)
         const int qq = q + c, u = qq % NSPL, r = qq % NRAW;
-        if (__any_sync(kFull, abort_s)) break;
+        if (__any_sync(kFull, abort_s)) return false;
         const bool ok =
             (qq < NSPL || mbar_wait(smem_u32(&spl_free[u]), (uint32_t)((qq / NSPL - 1) & 1))) &&
             mbar_wait(smem_u32(&raw_full[r]), (uint32_t)((qq / NRAW) & 1));
         if (!__all_sync(kFull, ok)) {
           fail();
-          break;
+          return false;
         }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint8_t* raw = raw_base + r * kRawStage;
+        load_a(raw, p.ka, 32 * aq + lane, ah, va);
+        load_b(raw + kRawA, p.kb, ts, xb);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&raw_free[r]));  // this warp has read the raw slot
+        return true;
+      };
+      bool ok = nchunks > 0 && fetch(0);
+      for (int c = 0; ok && c < nchunks; ++c) {
+        const int qq = q + c, u = qq % NSPL;
         const uint32_t col = tmem + alane + kAcol + 32u * u + 8u * ah;
-        split_a(raw, p.ka, 32 * aq + lane, ah, col, col + 16u);
-        split_b(raw + kRawA, p.kb, stage_base + u * kStage, ts);
+        store_a(va, col, col + 16u);
+        store_b(xb, p.kb, stage_base + u * kStage, ts);
+        const bool more = c + 1 < nchunks;
+        if (more) ok = fetch(c + 1);
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         // generic-proxy stores visible to the tensor core's async proxy; TMEM
         // stores ordered before the MMA warp's thread sync
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(smem_u32(&raw_free[r]));  // this warp has read the raw slot
-          mbar_arrive(smem_u32(&spl_full[u]));
-        }
+        if (lane == 0) mbar_arrive(smem_u32(&spl_full[u]));
       }
     } else if (warp == kTmaWarp) {
       // ---- TMA producer (one lane) ----
