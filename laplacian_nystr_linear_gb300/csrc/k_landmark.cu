@@ -514,13 +514,13 @@ cudaError_t run_alpha(const Prob& p, const float* A, float* alpha, float* X0, lo
 // ---------------------------------------------------------------------------
 constexpr int kGB = 16;  // landmarks per CTA
 
-template <int D>
+template <int D, bool GAUSS>
 __global__ void __launch_bounds__(kThreads) k_gram_bwd(const float* __restrict__ L,
                                                        const float* __restrict__ Llo,
                                                        const float* __restrict__ A,
                                                        const float* __restrict__ dA,
                                                        float* __restrict__ dLA, int m,
-                                                       float inv_lam, int gauss) {
+                                                       float inv_lam) {
   constexpr int LPT = D / 16;           // landmarks per thread: kGB / (kThreads / D)
   constexpr int NG = kThreads / D;      // landmark groups
   extern __shared__ float4 sm4[];
@@ -557,10 +557,16 @@ __global__ void __launch_bounds__(kThreads) k_gram_bwd(const float* __restrict__
     for (int k = 0; k < LPT; ++k) {
       const float wv = w[(ag + NG * k) * m + b];
       float t = la[k] - lb;
-      if (t == 0.f && !gauss && Llo != nullptr && a0 + ag + NG * k < m)
-        t = __ldg(Llo + ((size_t)bh * m + a0 + ag + NG * k) * D + c) -
-            __ldg(Llo + ((size_t)bh * m + b) * D + c);
-      acc[k] += gauss ? 2.f * t * wv : sgn_times(t, wv);
+      if constexpr (GAUSS) {
+        acc[k] = fmaf(2.f * t, wv, acc[k]);
+      } else {
+        if (t == 0.f && Llo != nullptr && a0 + ag + NG * k < m)
+          t = __ldg(Llo + ((size_t)bh * m + a0 + ag + NG * k) * D + c) -
+              __ldg(Llo + ((size_t)bh * m + b) * D + c);
+        // sgn(t) w: w with t's sign bit folded in, 0 where t is 0
+        const float sw = __int_as_float(__float_as_int(wv) ^ (__float_as_int(t) & 0x80000000));
+        acc[k] += t == 0.f ? 0.f : sw;
+      }
     }
   }
 #pragma unroll
@@ -570,14 +576,21 @@ __global__ void __launch_bounds__(kThreads) k_gram_bwd(const float* __restrict__
   }
 }
 
+template <int D, bool GAUSS>
+static cudaError_t gram_bwd_g(const Prob& p, const float* L, const float* Llo, const float* A,
+                              const float* dA, float* dLA, cudaStream_t st) {
+  const size_t smem = (size_t)kGB * p.m * sizeof(float);
+  static bool once = (allow_smem(k_gram_bwd<D, GAUSS>, (size_t)kGB * 1024 * sizeof(float)), true);
+  (void)once;
+  return launch("gram_bwd", k_gram_bwd<D, GAUSS>, dim3((p.m + kGB - 1) / kGB, p.BH),
+                dim3(kThreads), smem, st, L, Llo, A, dA, dLA, p.m, p.inv_lam);
+}
+
 template <int D>
 static cudaError_t gram_bwd_t(const Prob& p, const float* L, const float* Llo, const float* A,
                               const float* dA, float* dLA, cudaStream_t st) {
-  const size_t smem = (size_t)kGB * p.m * sizeof(float);
-  static bool once = (allow_smem(k_gram_bwd<D>, (size_t)kGB * 1024 * sizeof(float)), true);
-  (void)once;
-  return launch("gram_bwd", k_gram_bwd<D>, dim3((p.m + kGB - 1) / kGB, p.BH), dim3(kThreads), smem,
-                st, L, Llo, A, dA, dLA, p.m, p.inv_lam, p.gauss() ? 1 : 0);
+  return p.gauss() ? gram_bwd_g<D, true>(p, L, Llo, A, dA, dLA, st)
+                   : gram_bwd_g<D, false>(p, L, Llo, A, dA, dLA, st);
 }
 
 cudaError_t run_gram_bwd(const Prob& p, const float* L, const float* Llo, const float* A,
