@@ -31,6 +31,16 @@ namespace lapnys {
 // window.
 // ---------------------------------------------------------------------------
 constexpr int kPoolThreads = 128;
+constexpr int kPoolStage = 16 * 1024;  // a window of at most this many bytes is staged first
+
+// 4 consecutive elements from shared memory (a plain load: the read-only
+// global path of ld4 does not address shared memory)
+__device__ __forceinline__ float4 sm_ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 sm_ld4(const __nv_bfloat16* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                     __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+}
 
 __device__ __forceinline__ void two_sum_acc(float& s, float& e, float v) {
   const float t = s + v;
@@ -55,6 +65,7 @@ __global__ void __launch_bounds__(kPoolThreads) k_pool(const T* __restrict__ K,
                                                        int32_t* __restrict__ idx, int N, int d,
                                                        int gh, int gw, int mh, int mw, int m) {
   __shared__ float4 ps[kPoolThreads], pe[kPoolThreads];
+  extern __shared__ float4 wsm4[];  // the window's rows (kPoolStage bytes)
   const int a = blockIdx.x, bh = blockIdx.y;
   const int wi = a / mw, wj = a - wi * mw;
   const int C4 = d / 4, P = kPoolThreads / C4;
@@ -64,7 +75,36 @@ __global__ void __launch_bounds__(kPoolThreads) k_pool(const T* __restrict__ K,
   const int ww = x1 - x0, nwin = (y1 - y0) * ww;
   const T* Kb = K + (size_t)bh * N * d + chunk * 4;
   float4 s = make_float4(0.f, 0.f, 0.f, 0.f), e = s;
-  if (part < P) {
+  // A window that fits is copied in first (every 16-byte piece of its rows in
+  // flight at once), then summed from shared memory in the same order.
+  const int rowb = ww * d * (int)sizeof(T);  // bytes of one window row: a multiple of 16
+  const bool staged = (y1 - y0) * rowb <= kPoolStage;  // uniform over the CTA
+  if (staged) {
+    const int per = rowb / 16, total = (y1 - y0) * per;
+    const uint8_t* src0 = reinterpret_cast<const uint8_t*>(K + ((size_t)bh * N + (size_t)y0 * gw + x0) * d);
+    uint8_t* wsm = reinterpret_cast<uint8_t*>(wsm4);
+    for (int id = threadIdx.x; id < total; id += kPoolThreads) {
+      const int r = id / per, o = id - r * per;
+      cp_async16(smem_addr(wsm + r * rowb + 16 * o), src0 + (size_t)r * gw * d * sizeof(T) + 16 * o,
+                 true);
+    }
+    cp_commit();
+    cp_wait_all();
+    __syncthreads();
+    if (part < P) {
+      const T* wb = reinterpret_cast<const T*>(wsm4) + chunk * 4;
+#pragma unroll 4
+      for (int t = part; t < nwin; t += P) {
+        const float4 v = sm_ld4(wb + (size_t)t * d);  // rows of ww tokens, back to back
+        two_sum_acc(s.x, e.x, v.x);
+        two_sum_acc(s.y, e.y, v.y);
+        two_sum_acc(s.z, e.z, v.z);
+        two_sum_acc(s.w, e.w, v.w);
+      }
+      ps[threadIdx.x] = s;
+      pe[threadIdx.x] = e;
+    }
+  } else if (part < P) {
 #pragma unroll 4
     for (int t = part; t < nwin; t += P) {
       const int y = y0 + t / ww, x = x0 + t % ww;
@@ -102,10 +142,10 @@ cudaError_t run_pool(const Prob& p, const void* k, float* L, float* Llo, int32_t
                      cudaStream_t st) {
   dim3 grid(p.m, p.BH);
   if (p.dtype == 1)
-    return launch("pool", k_pool<__nv_bfloat16>, grid, dim3(kPoolThreads), 0, st,
+    return launch("pool", k_pool<__nv_bfloat16>, grid, dim3(kPoolThreads), kPoolStage, st,
                   (const __nv_bfloat16*)k, L, Llo, idx, p.N, p.d, p.gh, p.gw, p.mh, p.mw, p.m);
-  return launch("pool", k_pool<float>, grid, dim3(kPoolThreads), 0, st, (const float*)k, L, Llo,
-                idx, p.N, p.d, p.gh, p.gw, p.mh, p.mw, p.m);
+  return launch("pool", k_pool<float>, grid, dim3(kPoolThreads), kPoolStage, st, (const float*)k, L,
+                Llo, idx, p.N, p.d, p.gh, p.gw, p.mh, p.mw, p.m);
 }
 
 // ---------------------------------------------------------------------------
