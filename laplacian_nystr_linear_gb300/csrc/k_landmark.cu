@@ -180,14 +180,80 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// One 16 x 16 block (rows r0 .., columns c0 ..) of op(A) op(B), summed over the
-// k steps k0 = 8 kq, 8 (kq + s), .. below K8 (a share of K when s warps split
-// it).  Element c of acc[n] sits at row r0 + g + 8 (c / 2), column
+// Operand planes: a 64 x 64 matrix (zero past m) kept as {hi, lo} pairs,
+// P[i * kMS + k] = split of element (i, k), split once when the element is
+// written rather than at every use.  With 68 pairs a row, the 64-bit loads of
+// an MMA fragment (4 rows x 4 columns per half-warp, either way round) fall in
+// distinct banks.
+__device__ __forceinline__ float2 split_pair(float x) {
+  uint32_t h, l;
+  split_tf32(x, h, l);
+  return make_float2(__uint_as_float(h), __uint_as_float(l));
+}
+
+// the three partial sums of one 16 x 16 block
+struct Acc3 {
+  float hh[2][4], hl[2][4], lh[2][4];
+  __device__ void zero() {
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) hh[n][c] = hl[n][c] = lh[n][c] = 0.f;
+  }
+  // hi*hi + (hi*lo + lo*hi)
+  __device__ void sum(float (&acc)[2][4]) const {
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[n][c] = hh[n][c] + (hl[n][c] + lh[n][c]);
+  }
+};
+
+// k step k0 .. k0 + 7 of the 16 x 16 block (rows r0 .., columns c0 ..) of
+// op(A) op(B).  Element c of acc[n] sits at row r0 + g + 8 (c / 2), column
 // c0 + 8 n + 2 t + c % 2 (g = lane / 4, t = lane % 4).
 template <bool TA, bool TB>
-__device__ __forceinline__ void unit_mm(const float* __restrict__ A, const float* __restrict__ B,
-                                        int r0, int c0, int K8, int kq, int s,
-                                        float (&acc)[2][4]) {
+__device__ __forceinline__ void unit_kstep(const float2* __restrict__ A, const float2* __restrict__ B,
+                                           int r0, int c0, int k0, Acc3& s) {
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  auto opa = [&](int i, int k) { return TA ? A[k * kMS + i] : A[i * kMS + k]; };
+  auto opb = [&](int k, int j) { return TB ? B[j * kMS + k] : B[k * kMS + j]; };
+  const float2 a0 = opa(r0 + g, k0 + t), a1 = opa(r0 + g + 8, k0 + t);
+  const float2 a2 = opa(r0 + g, k0 + t + 4), a3 = opa(r0 + g + 8, k0 + t + 4);
+  const uint32_t ah[4] = {__float_as_uint(a0.x), __float_as_uint(a1.x), __float_as_uint(a2.x),
+                          __float_as_uint(a3.x)};
+  const uint32_t al[4] = {__float_as_uint(a0.y), __float_as_uint(a1.y), __float_as_uint(a2.y),
+                          __float_as_uint(a3.y)};
+#pragma unroll
+  for (int n = 0; n < 2; ++n) {
+    const float2 b0 = opb(k0 + t, c0 + 8 * n + g), b1 = opb(k0 + t + 4, c0 + 8 * n + g);
+    mma_tf32(s.hh[n], ah, __float_as_uint(b0.x), __float_as_uint(b1.x));
+    mma_tf32(s.hl[n], ah, __float_as_uint(b0.y), __float_as_uint(b1.y));
+    mma_tf32(s.lh[n], al, __float_as_uint(b0.x), __float_as_uint(b1.x));
+  }
+}
+
+// one 16 x 16 block of op(A) op(B) over k < K8
+template <bool TA, bool TB>
+__device__ __forceinline__ void unit_mm(const float2* __restrict__ A, const float2* __restrict__ B,
+                                        int r0, int c0, int K8, float (&acc)[2][4]) {
+  Acc3 s;
+  s.zero();
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    if (8 * u < K8) unit_kstep<TA, TB>(A, B, r0, c0, 8 * u, s);
+  s.sum(acc);
+}
+
+// The same block from fp32 planes (64 x 68 floats, zero past m), each operand
+// element split as it is loaded: the forward solver's form.  It holds 64
+// registers a thread and 87 KB, so two CTAs share an SM when slices outnumber
+// SMs; with pair planes the forward was no faster (the tensor pipe and the
+// dependent MMA chains bound both).
+template <bool TA, bool TB>
+__device__ __forceinline__ void unit_mm_f(const float* __restrict__ A, const float* __restrict__ B,
+                                          int r0, int c0, int K8, float (&acc)[2][4]) {
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   float hh[2][4], hl[2][4], lh[2][4];
@@ -199,7 +265,7 @@ __device__ __forceinline__ void unit_mm(const float* __restrict__ A, const float
   auto opb = [&](int k, int j) { return TB ? B[j * kMS + k] : B[k * kMS + j]; };
 #pragma unroll
   for (int u = 0; u < 8; ++u) {
-    const int k0 = 8 * (kq + u * s);
+    const int k0 = 8 * u;
     if (k0 < K8) {
       uint32_t ah[4], al[4];
       split_tf32(opa(r0 + g, k0 + t), ah[0], al[0]);
@@ -240,22 +306,28 @@ __device__ __forceinline__ void unit_pos(int r0, int c0, int n, int c, int& r, i
   j = c0 + 8 * n + 2 * (lane & 3) + (c & 1);
 }
 
-// load an m x m row-major global matrix into a zero-padded 64 x 68 tile
-// (thread: column j = tid % 64, rows tid / 64, + 8, ..)
-__device__ __forceinline__ void load_mat(float* s, const float* g, int m) {
-  const int j = threadIdx.x & 63;
-  for (int i = threadIdx.x >> 6; i < 64; i += kNsThreads / 64)
-    s[i * kMS + j] = (i < m && j < m) ? g[i * m + j] : 0.f;
+// a block's values into a pair plane (two adjacent pairs, 16 bytes, a store)
+__device__ __forceinline__ void put_unit(float2* P, int r0, int c0, const float (&v)[2][4]) {
+#pragma unroll
+  for (int n = 0; n < 2; ++n)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      int r, j;
+      unit_pos(r0, c0, n, 2 * h, r, j);
+      const float2 p0 = split_pair(v[n][2 * h]), p1 = split_pair(v[n][2 * h + 1]);
+      *reinterpret_cast<float4*>(P + r * kMS + j) = make_float4(p0.x, p0.y, p1.x, p1.y);
+    }
 }
-// the same as an asynchronous copy (4-byte cp.async, zero fill past m)
-__device__ __forceinline__ void load_mat_async(float* s, const float* g, int m) {
-  const int j = threadIdx.x & 63;
-  for (int i = threadIdx.x >> 6; i < 64; i += kNsThreads / 64) {
-    const bool ok = i < m && j < m;
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_addr(s + i * kMS + j)),
-                 "l"(ok ? g + i * m + j : g), "r"(ok ? 4 : 0)
-                 : "memory");
-  }
+// a block's elements inside the m x m matrix to a row-major global matrix
+__device__ __forceinline__ void store_unit(float* g, int m, int r0, int c0, const float (&v)[2][4]) {
+#pragma unroll
+  for (int n = 0; n < 2; ++n)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      int r, j;
+      unit_pos(r0, c0, n, c, r, j);
+      if (r < m && j < m) g[r * m + j] = v[n][c];
+    }
 }
 __device__ __forceinline__ void store_mat(float* g, const float* s, int m) {
   const int j = threadIdx.x & 63;
@@ -351,7 +423,7 @@ __global__ void __launch_bounds__(kNsThreads) k_ns_small(const float* __restrict
       int r0, c0;
       us.at(i, r0, c0);
       float acc[2][4];
-      unit_mm<false, false>(As, Xa, r0, c0, us.K8, 0, 1, acc);
+      unit_mm_f<false, false>(As, Xa, r0, c0, us.K8, acc);
 #pragma unroll
       for (int n = 0; n < 2; ++n)
 #pragma unroll
@@ -367,7 +439,7 @@ __global__ void __launch_bounds__(kNsThreads) k_ns_small(const float* __restrict
       int r0, c0;
       us.at(i, r0, c0);
       float acc[2][4];
-      unit_mm<false, false>(Xa, Ys, r0, c0, us.K8, 0, 1, acc);
+      unit_mm_f<false, false>(Xa, Ys, r0, c0, us.K8, acc);
 #pragma unroll
       for (int n = 0; n < 2; ++n)
 #pragma unroll
@@ -651,8 +723,12 @@ cudaError_t run_gram_bwd(const Prob& p, const float* L, const float* Llo, const 
 //   dA -= XG X_t^T,  G  = Tm - A^T XG                 (phase 2, independent)
 // then X_0 = alpha A contributes alpha G and, through alpha = 1/(n1 ninf),
 // dalpha = <G, A> spread over the maximising column (n1) and row (ninf).
-// GT holds dLoss/dX_T on entry.  The 16 warps take two 16 x 16 blocks of a
-// phase's two products each; X_t and Y_t arrive one step ahead (cp.async).
+// GT holds dLoss/dX_T on entry.  Warp w owns the 16 x 16 block w of all four
+// products, so its blocks of G (Tm between the phases) and dA stay in fp32
+// registers; A, X_t, Y_t, G and XG sit in shared memory as pair planes.  Each
+// thread loads its share of X_t (into registers) and of Y_t (by asynchronous
+// copies into a staging buffer) one step ahead and splits it into the planes
+// at the top of the step.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(kNsThreads) k_ns_bwd_small(const float* __restrict__ A,
                                                              const float* __restrict__ info,
@@ -662,93 +738,121 @@ __global__ void __launch_bounds__(kNsThreads) k_ns_bwd_small(const float* __rest
                                                              float* __restrict__ dA, int m,
                                                              int iters, int nx, int ny) {
   extern __shared__ float4 sm4[];
-  float* As = reinterpret_cast<float*>(sm4);
-  float* Xt2 = As + 64 * kMS;         // X_t, two buffers: step t - 1's arrives during step t
-  float* Yt2 = Xt2 + 2 * 64 * kMS;    // Y_t, likewise
-  float* G = Yt2 + 2 * 64 * kMS;
-  float* XG = G + 64 * kMS;
-  float* Tm = XG + 64 * kMS;
-  float* dAs = Tm + 64 * kMS;
+  float2* Ap = reinterpret_cast<float2*>(sm4);
+  float2* Xp2 = Ap + 64 * kMS;      // X_t, two planes: step t - 1's is written during step t
+  float2* Yp = Xp2 + 2 * 64 * kMS;  // Y_t
+  float2* Gp = Yp + 64 * kMS;
+  float2* XGp = Gp + 64 * kMS;
+  float* Yr = reinterpret_cast<float*>(XGp + 64 * kMS);  // Y_t as copied: element e at Yr[e]
   __shared__ float red[kNsThreads];
+  constexpr int kPer = 64 * 64 / kNsThreads;  // elements of a matrix per thread
   const int bh = blockIdx.x;
   const size_t mm = (size_t)m * m;
   const UnitSet us(m);
   const int warp = threadIdx.x >> 5;
-  constexpr int kW = kNsThreads / 32;
-  auto fetch = [&](int t, int buf) {
-    load_mat_async(Xt2 + buf * 64 * kMS, X + ((size_t)bh * nx + t % nx) * mm, m);
-    load_mat_async(Yt2 + buf * 64 * kMS, Y + ((size_t)bh * ny + t % ny) * mm, m);
+  const bool owner = warp < us.n;
+  int r0 = 0, c0 = 0;
+  if (owner) us.at(warp, r0, c0);
+
+  float xr[kPer];  // this thread's elements e = tid + 512 q of X_t (those of Y_t go to Yr[e])
+  auto fetch = [&](int t) {
+    const float* Xg = X + ((size_t)bh * nx + t % nx) * mm;
+    const float* Yg = Y + ((size_t)bh * ny + t % ny) * mm;
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int e = threadIdx.x + q * kNsThreads, i = e >> 6, j = e & 63;
+      const bool ok = i < m && j < m;
+      xr[q] = ok ? Xg[i * m + j] : 0.f;
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_addr(Yr + e)),
+                   "l"(ok ? Yg + i * m + j : Yg), "r"(ok ? 4 : 0)
+                   : "memory");
+    }
     cp_commit();
   };
+  if (iters > 0) fetch(iters - 1);
 
-  if (iters > 0) fetch(iters - 1, 0);
-  load_mat(As, A + bh * mm, m);
-  load_mat(G, GT + bh * mm, m);
-  for (int e = threadIdx.x; e < 64 * kMS; e += kNsThreads) dAs[e] = 0.f;
-  for (int t = iters - 1; t >= 0; --t) {
-    const int buf = (iters - 1 - t) & 1;
-    const float* Xt = Xt2 + buf * 64 * kMS;
-    const float* Yt = Yt2 + buf * 64 * kMS;
-    cp_wait_all();
-    __syncthreads();  // step t's X_t, Y_t and G landed; step t + 1 is done with the other buffers
-    if (t > 0) fetch(t - 1, buf ^ 1);
-    for (int i = warp; i < 2 * us.n; i += kW) {
-      const bool second = i >= us.n;
-      int r0, c0;
-      us.at(second ? i - us.n : i, r0, c0);
-      float acc[2][4];
-      if (second)
-        unit_mm<false, true>(G, Yt, r0, c0, us.K8, 0, 1, acc);  // G Y_t^T
-      else
-        unit_mm<true, false>(Xt, G, r0, c0, us.K8, 0, 1, acc);  // XG = X_t^T G
+  const float* Ab = A + bh * mm;
+  const float* Gb = GT + bh * mm;
+  for (int e = threadIdx.x; e < 64 * 64; e += kNsThreads) {
+    const int i = e >> 6, j = e & 63, o = i * kMS + j;
+    const bool ok = i < m && j < m;
+    Ap[o] = split_pair(ok ? Ab[i * m + j] : 0.f);
+    Gp[o] = split_pair(ok ? Gb[i * m + j] : 0.f);
+  }
+  float gf[2][4], da[2][4];  // this warp's blocks of G and dA
 #pragma unroll
-      for (int n = 0; n < 2; ++n)
+  for (int n = 0; n < 2; ++n)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          int r, j;
-          unit_pos(r0, c0, n, c, r, j);
-          const int o = r * kMS + j;
-          if (second)
-            Tm[o] = 2.f * G[o] - acc[n][c];
-          else
-            XG[o] = acc[n][c];
-        }
+    for (int c = 0; c < 4; ++c) {
+      int r, j;
+      unit_pos(r0, c0, n, c, r, j);
+      gf[n][c] = (r < m && j < m) ? Gb[r * m + j] : 0.f;
+      da[n][c] = 0.f;
     }
-    __syncthreads();
-    for (int i = warp; i < 2 * us.n; i += kW) {
-      const bool second = i >= us.n;
-      int r0, c0;
-      us.at(second ? i - us.n : i, r0, c0);
-      float acc[2][4];
-      if (second)
-        unit_mm<true, false>(As, XG, r0, c0, us.K8, 0, 1, acc);  // A^T XG
-      else
-        unit_mm<false, true>(XG, Xt, r0, c0, us.K8, 0, 1, acc);  // XG X_t^T
+  for (int t = iters - 1; t >= 0; --t) {
+    float2* Xt = Xp2 + ((iters - 1 - t) & 1) * 64 * kMS;
+    cp_wait_all();  // this thread's own copies of Y_t landed
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int e = threadIdx.x + q * kNsThreads, o = (e >> 6) * kMS + (e & 63);
+      Xt[o] = split_pair(xr[q]);
+      Yp[o] = split_pair(Yr[e]);
+    }
+    __syncthreads();  // X_t, Y_t and G in place; step t + 1 is done with this X plane
+    if (t > 0) fetch(t - 1);
+    if (owner) {  // gf becomes Tm
+      float xg[2][4], gy[2][4];
+      unit_mm<true, false>(Xt, Gp, r0, c0, us.K8, xg);
+      unit_mm<false, true>(Gp, Yp, r0, c0, us.K8, gy);
+      put_unit(XGp, r0, c0, xg);
+#pragma unroll
+      for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) gf[n][c] = 2.f * gf[n][c] - gy[n][c];
+    }
+    __syncthreads();  // XG in place; phase 1 is done with G and Y_t
+    if (owner) {
+      float xgx[2][4], axg[2][4];
+      unit_mm<false, true>(XGp, Xt, r0, c0, us.K8, xgx);
+      unit_mm<true, false>(Ap, XGp, r0, c0, us.K8, axg);
 #pragma unroll
       for (int n = 0; n < 2; ++n)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          int r, j;
-          unit_pos(r0, c0, n, c, r, j);
-          const int o = r * kMS + j;
-          if (second)
-            G[o] = Tm[o] - acc[n][c];
-          else
-            dAs[o] -= acc[n][c];
+          da[n][c] -= xgx[n][c];
+          gf[n][c] -= axg[n][c];
         }
+      put_unit(Gp, r0, c0, gf);
     }
   }
-  cp_wait_all();
+  __syncthreads();  // the pair planes are free
+  // X_0 = alpha A, on fp32 planes in the X planes' space
+  float* Gs = reinterpret_cast<float*>(Xp2);
+  float* As = Gs + 64 * kMS;
+  float* dAs = As + 64 * kMS;
+  if (owner)
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        int r, j;
+        unit_pos(r0, c0, n, c, r, j);
+        Gs[r * kMS + j] = gf[n][c];
+        dAs[r * kMS + j] = da[n][c];
+      }
+  for (int e = threadIdx.x; e < 64 * 64; e += kNsThreads) {
+    const int i = e >> 6, j = e & 63;
+    if (i < m && j < m) As[i * kMS + j] = Ab[i * m + j];
+  }
   __syncthreads();
-  // X_0 = alpha A
   const float* in = info + (size_t)bh * 4;
   const float al = in[0], n1 = in[1], ninf = in[2];
   const int code = __float_as_int(in[3]);
   const int jc = code & 0xffff, ir = code >> 16;
   float part = 0.f;
   for (int e = threadIdx.x; e < 64 * 64; e += kNsThreads) {
-    const int o = (e >> 6) * kMS + (e & 63);
-    part += G[o] * As[o];
+    const int i = e >> 6, j = e & 63;
+    if (i < m && j < m) part += Gs[i * kMS + j] * As[i * kMS + j];
   }
   red[threadIdx.x] = part;
   __syncthreads();
@@ -759,19 +863,18 @@ __global__ void __launch_bounds__(kNsThreads) k_ns_bwd_small(const float* __rest
   const float dal = red[0];
   for (int e = threadIdx.x; e < 64 * 64; e += kNsThreads) {
     const int i = e >> 6, j = e & 63;
+    if (i >= m || j >= m) continue;
     const int o = i * kMS + j;
-    float v = dAs[o] + al * G[o];
+    float v = dAs[o] + al * Gs[o];
     if (j == jc) v += dal * (-al / n1);
     if (i == ir) v += dal * (-al / ninf);
-    dAs[o] = v;
+    dA[bh * mm + i * m + j] = v;
   }
-  __syncthreads();
-  store_mat(dA + bh * mm, dAs, m);
 }
 
 cudaError_t run_ns_bwd_small(const Prob& p, const float* A, const float* alpha, const float* X,
                              const float* Y, const float* GT, float* dA, cudaStream_t st) {
-  const size_t smem = 9 * 64 * kMS * sizeof(float);
+  const size_t smem = 6 * 64 * kMS * sizeof(float2) + 64 * 64 * sizeof(float);
   static bool once = (allow_smem(k_ns_bwd_small, smem), true);
   (void)once;
   return launch("ns_bwd_small", k_ns_bwd_small, dim3(p.BH), dim3(kNsThreads), smem, st, A, alpha,
