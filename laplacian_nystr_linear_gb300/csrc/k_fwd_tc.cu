@@ -389,7 +389,10 @@ __global__ void __launch_bounds__(NTH, 1) k_key_tc(KArgs a) {
   float* Lt = reinterpret_cast<float*>(sm + S::Lt);
   float* Kt = reinterpret_cast<float*>(sm + S::Kt);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int ty = tid >> 4, tx = tid & 15;  // landmarks 4 ty .. 4 ty + 3, tokens 4 tx .. 4 tx + 3
+  // landmarks 4 ty .. 4 ty + 3, tokens 4 tx .. 4 tx + 3; a warp takes 8 x 4 of these blocks
+  // (32 landmarks x 16 tokens), so that each of its kernel-value stores writes
+  // four whole 128-byte lines of token rows
+  const int ty = 8 * (warp & 3) + (lane & 7), tx = 4 * (warp >> 2) + (lane >> 3);
   const int lt = blockIdx.x, sp = blockIdx.y, bh = blockIdx.z;
   const int a0 = lt * QM;
   constexpr uint32_t kCols = tmem_cols(D);
@@ -433,6 +436,9 @@ __global__ void __launch_bounds__(NTH, 1) k_key_tc(KArgs a) {
   // flight are waited for (bounded) before the tensor memory is freed.
   bool bad = false, abort = false;
   int i = 0;
+  float* pend = nullptr;  // the previous block's kernel values, stored during this block's loop
+  int pn0 = 0;
+  float pv[4][4];
   for (int b = b0; b < b1; ++b, ++i) {
     const int buf = i & 1;
     cp_wait_all();
@@ -478,23 +484,36 @@ __global__ void __launch_bounds__(NTH, 1) k_key_tc(KArgs a) {
     {
       const float* lp = Lt + 4 * ty;
       const float* xp = Kt + 4 * tx;
+#pragma unroll
+      for (int c16 = 0; c16 < D; c16 += 16) {
+        if (pend != nullptr) {
+          const int s = c16 >> 4;
+          if (pn0 + s < a.N)
+            st4(pend + (size_t)s * a.mp, make_float4(pv[0][s], pv[1][s], pv[2][s], pv[3][s]));
+        }
 #pragma unroll 8
-      for (int c = 0; c < D; ++c) {
-        const float4 l0 = lds4(lp + c * QM), x = lds4(xp + c * TL);
-        const float lv[4] = {l0.x, l0.y, l0.z, l0.w};
-        if (GAUSS) {
-          const float xv[4] = {x.x, x.y, x.z, x.w};
+        for (int c = c16; c < c16 + 16; ++c) {
+          const float4 l0 = lds4(lp + c * QM), x = lds4(xp + c * TL);
+          const float lv[4] = {l0.x, l0.y, l0.z, l0.w};
+          if (GAUSS) {
+            const float xv[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-          for (int r = 0; r < 4; ++r)
+            for (int r = 0; r < 4; ++r)
 #pragma unroll
-            for (int s = 0; s < 4; ++s) acc[r][s] = dist_add<GAUSS>(acc[r][s], xv[s] - lv[r]);
-        } else {
-          // |x_s - l_r| = |l_r - x_s|: the pairs run over the keys
-          const f32x2 xa = pack2(x.x, x.y), xb = pack2(x.z, x.w);
+              for (int s = 0; s < 4; ++s) acc[r][s] = dist_add<GAUSS>(acc[r][s], xv[s] - lv[r]);
+          } else {
+            // |x_s - l_r| = |l_r - x_s|: the pairs run over the keys
+            const f32x2 xa = pack2(x.x, x.y), xb = pack2(x.z, x.w);
 #pragma unroll
-          for (int r = 0; r < 4; ++r) l1_row4(acc[r], lv[r], xa, xb);
+            for (int r = 0; r < 4; ++r) l1_row4(acc[r], lv[r], xa, xb);
+          }
         }
       }
+      if (pend != nullptr)  // D < 64: the rest of the previous block's values
+#pragma unroll
+        for (int s = D / 16; s < 4; ++s)
+          if (pn0 + s < a.N)
+            st4(pend + (size_t)s * a.mp, make_float4(pv[0][s], pv[1][s], pv[2][s], pv[3][s]));
     }
     {
       const int n0 = b * TL;
@@ -507,14 +526,14 @@ __global__ void __launch_bounds__(NTH, 1) k_key_tc(KArgs a) {
           cv[r][s] = ok ? exp2f(acc[r][s] * a.ns) : 0.f;
         }
       if (a.kvout != nullptr && a0 + 4 * ty < a.mp) {
-        // keep the kernel values for the backward: token-major rows
+        // kept for the backward (token-major rows), stored during the next
+        // block's distance loop, one token row every 16 features
+        pend = a.kvout + ((size_t)bh * a.N + n0 + 4 * tx) * a.mp + a0 + 4 * ty;
+        pn0 = n0 + 4 * tx;
 #pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          const int j = n0 + 4 * tx + s;
-          if (j < a.N)
-            st4(a.kvout + ((size_t)bh * a.N + j) * a.mp + a0 + 4 * ty,
-                make_float4(cv[0][s], cv[1][s], cv[2][s], cv[3][s]));
-        }
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int s = 0; s < 4; ++s) pv[r][s] = cv[r][s];
       }
       // C^T as three bf16 planes (row = landmark 4 ty + r, k = tokens 4 tx .. 4 tx + 3)
       uint8_t* ca = sm + S::Ca + buf * 3 * kPlaneC + (tx >> 1) * kLboC + (ty >> 1) * kSbo +
@@ -563,6 +582,11 @@ __global__ void __launch_bounds__(NTH, 1) k_key_tc(KArgs a) {
       tc::commit(tc::smem_u32(&mdone[buf]));
     }
   }
+  if (pend != nullptr && !abort)
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+      if (pn0 + s < a.N)
+        st4(pend + (size_t)s * a.mp, make_float4(pv[0][s], pv[1][s], pv[2][s], pv[3][s]));
   cp_wait_all();  // the next block's rows, when the loop stopped early
   // partial W of this range: lane quarter w % 4 holds landmarks 32 (w % 4) .., the
   // four warps w, w + 4, w + 8, w + 12 split the columns (MMAs of blocks < i)
