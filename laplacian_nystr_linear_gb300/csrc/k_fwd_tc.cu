@@ -69,10 +69,10 @@ constexpr uint32_t kPlaneC = (TL / 8) * kLboC;
 template <int D>
 struct KSmem {
   static constexpr uint32_t Lt = 0;                            // [D][QM] f32, feature-major landmarks
-  static constexpr uint32_t Kt = Lt + D * QM * 4;              // [D][TL] f32, feature-major keys
+  static constexpr uint32_t Kt = Lt + D * QM * 4;              // 2 x [D][TL] f32, feature-major keys
   static constexpr uint32_t kLboB = (D / 8) * kSboVB;          // B (V^T, bf16): 8-token K groups
   static constexpr uint32_t kTileB = (TL / 8) * kLboB;
-  static constexpr uint32_t Vb = Kt + D * TL * 4;              // 2 x B tiles (V^T)
+  static constexpr uint32_t Vb = Kt + 2 * D * TL * 4;          // 2 x B tiles (V^T)
   static constexpr uint32_t Ca = Vb + 2 * kTileB;              // 2 x 3 A planes (C^T, bf16)
   static constexpr uint32_t kRow = D * 2 + 16;                 // padded raw row
   static constexpr uint32_t Raw = Ca + 6 * kPlaneC;            // 2 x (64 key rows, 64 value rows)
@@ -416,21 +416,74 @@ __global__ void __launch_bounds__(NTH, 1) k_key_tc(KArgs a) {
   const uint32_t tmem = tmem_s;
 
   const int b0 = (int)((long long)a.nblk * sp / a.S), b1 = (int)((long long)a.nblk * (sp + 1) / a.S);
-  // raw key and value rows of block b into raw buffer `buf` (zero past N)
-  auto prefetch = [&](int b, int buf) {
-    if (b >= b1) return;
-    const int n0 = b * TL;
-    constexpr int CH = D / 8;
-    uint8_t* rb = sm + S::Raw + buf * S::kRawBuf;
-    for (int e = tid; e < 2 * TL * CH; e += NTH) {
-      const int which = e / (TL * CH), rem = e % (TL * CH), j = rem % TL, ch = rem / TL;
-      const bool ok = n0 + j < a.N;
-      const __nv_bfloat16* src = (which ? Vb : Kb) + (size_t)(ok ? n0 + j : 0) * D + 8 * ch;
-      cp_async16(smem_addr(rb + (which * TL + j) * S::kRow + 16 * ch), src, ok);
+  constexpr int CH = D / 8;
+  constexpr int NV = (TL / 2) * CH;  // value tasks (a token pair, 8 features): threads 0 ..
+  constexpr int NK = TL * CH;        // key pieces (a token, 8 features): threads NTH / 2 .., in turn
+  // Raw key and value rows of block b into raw buffer rbuf (zero past N), one
+  // commit group per block (empty past the range).  Each thread copies the
+  // pieces it converts afterwards, so its own wait on its copies is all that
+  // the conversion needs: no barrier between the copies and the conversion.
+  auto prefetch = [&](int b, int rbuf) {
+    if (b < b1) {
+      const int n0 = b * TL;
+      uint8_t* rb = sm + S::Raw + rbuf * S::kRawBuf;
+      if (tid < NTH / 2) {
+        if (tid < NV) {
+          const int ch = tid % CH, j = 2 * (tid / CH);
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const bool ok = n0 + j + u < a.N;
+            cp_async16(smem_addr(rb + (TL + j + u) * S::kRow + 16 * ch),
+                       Vb + (size_t)(ok ? n0 + j + u : 0) * D + 8 * ch, ok);
+          }
+        }
+      } else {
+        for (int kp = tid - NTH / 2; kp < NK; kp += NTH / 2) {
+          const int j = kp % TL, ch = kp / TL;
+          const bool ok = n0 + j < a.N;
+          cp_async16(smem_addr(rb + j * S::kRow + 16 * ch), Kb + (size_t)(ok ? n0 + j : 0) * D + 8 * ch, ok);
+        }
+      }
     }
     cp_commit();
   };
+  // the block in raw buffer rbuf -> keys feature-major f32 (Kt buffer kb; lanes
+  // take consecutive tokens) and values the bf16 B operand (V^T buffer kb; row =
+  // feature, k = token; a task is a token pair and 8 features)
+  auto convert = [&](int rbuf, int kb) {
+    const uint8_t* rb = sm + S::Raw + rbuf * S::kRawBuf;
+    if (tid < NTH / 2) {
+      if (tid < NV) {
+        const int ch = tid % CH, j = 2 * (tid / CH);
+        const uint4 u0 = *reinterpret_cast<const uint4*>(rb + (TL + j) * S::kRow + 16 * ch);
+        const uint4 u1 = *reinterpret_cast<const uint4*>(rb + (TL + j + 1) * S::kRow + 16 * ch);
+        const uint32_t w0[4] = {u0.x, u0.y, u0.z, u0.w}, w1[4] = {u1.x, u1.y, u1.z, u1.w};
+        uint8_t* dst = sm + S::Vb + kb * S::kTileB + (j >> 3) * S::kLboB + ch * kSboVB + (j & 7) * 2;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          // features 8 ch + 2 q (low halves) and 8 ch + 2 q + 1 (high halves)
+          *reinterpret_cast<uint32_t*>(dst + (2 * q) * 16) = (w0[q] & 0xffffu) | (w1[q] << 16);
+          *reinterpret_cast<uint32_t*>(dst + (2 * q + 1) * 16) = (w0[q] >> 16) | (w1[q] & 0xffff0000u);
+        }
+      }
+    } else {
+      float* kt = Kt + kb * D * TL;
+      for (int kp = tid - NTH / 2; kp < NK; kp += NTH / 2) {
+        const int j = kp % TL, ch = kp / TL;
+        float f[8];
+        bf16x8(*reinterpret_cast<const uint4*>(rb + j * S::kRow + 16 * ch), f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) kt[(8 * ch + q) * TL + j] = f[q];
+      }
+    }
+  };
+  // One barrier a block: block b + 1's operands are converted at the end of
+  // block b, before the barrier that precedes block b's MMAs.
   prefetch(b0, 0);
+  prefetch(b0 + 1, 1);
+  asm volatile("cp.async.wait_group 1;" ::: "memory");  // this thread's pieces of block b0
+  convert(0, 0);
+  __syncthreads();
   // An expired wait (bad) stops the CTA before its next MMAs, decided by all
   // threads alike (__syncthreads_or); the MMAs already issued and the copies in
   // flight are waited for (bounded) before the tensor memory is freed.
@@ -441,40 +494,7 @@ __global__ void __launch_bounds__(NTH, 1) k_key_tc(KArgs a) {
   float pv[4][4];
   for (int b = b0; b < b1; ++b, ++i) {
     const int buf = i & 1;
-    cp_wait_all();
-    __syncthreads();  // block b's rows landed; the previous block's distances are done
-    // the V^T and C^T buffers of this block were read by MMA i - 2
-    if (i >= 2) bad |= !wait_or_flag(a.err, tc::smem_u32(&mdone[buf]), ((i - 2) >> 1) & 1);
-    {
-      const uint8_t* rb = sm + S::Raw + buf * S::kRawBuf;
-      constexpr int CH = D / 8;
-      // keys -> feature-major f32 (lanes take consecutive tokens)
-      for (int e = tid; e < TL * CH; e += NTH) {
-        const int j = e % TL, ch = e / TL;
-        float f[8];
-        bf16x8(*reinterpret_cast<const uint4*>(rb + j * S::kRow + 16 * ch), f);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) Kt[(8 * ch + q) * TL + j] = f[q];
-      }
-      // values -> bf16 B operand (row = feature, k = token); a thread takes a
-      // token pair and 8 features, lanes: 8 feature groups x 4 token pairs
-      uint8_t* vb = sm + S::Vb + buf * S::kTileB;
-      for (int e = tid; e < (TL / 2) * CH; e += NTH) {
-        const int ch = e % CH, j = 2 * (e / CH);
-        const uint4 u0 = *reinterpret_cast<const uint4*>(rb + (TL + j) * S::kRow + 16 * ch);
-        const uint4 u1 = *reinterpret_cast<const uint4*>(rb + (TL + j + 1) * S::kRow + 16 * ch);
-        const uint32_t w0[4] = {u0.x, u0.y, u0.z, u0.w}, w1[4] = {u1.x, u1.y, u1.z, u1.w};
-        uint8_t* dst = vb + (j >> 3) * S::kLboB + ch * kSboVB + (j & 7) * 2;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          // features 8 ch + 2 q (low halves) and 8 ch + 2 q + 1 (high halves)
-          *reinterpret_cast<uint32_t*>(dst + (2 * q) * 16) = (w0[q] & 0xffffu) | (w1[q] << 16);
-          *reinterpret_cast<uint32_t*>(dst + (2 * q + 1) * 16) = (w0[q] >> 16) | (w1[q] & 0xffff0000u);
-        }
-      }
-    }
-    __syncthreads();
-    prefetch(b + 1, buf ^ 1);
+    prefetch(b + 2, buf);  // raw buffer buf held block b, converted before the last barrier
 
     float acc[4][4];
 #pragma unroll
@@ -483,7 +503,7 @@ __global__ void __launch_bounds__(NTH, 1) k_key_tc(KArgs a) {
       for (int s = 0; s < 4; ++s) acc[r][s] = 0.f;
     {
       const float* lp = Lt + 4 * ty;
-      const float* xp = Kt + 4 * tx;
+      const float* xp = Kt + buf * D * TL + 4 * tx;
 #pragma unroll
       for (int c16 = 0; c16 < D; c16 += 16) {
         if (pend != nullptr) {
@@ -535,6 +555,8 @@ __global__ void __launch_bounds__(NTH, 1) k_key_tc(KArgs a) {
 #pragma unroll
           for (int s = 0; s < 4; ++s) pv[r][s] = cv[r][s];
       }
+      // the C^T buffer of this block was read by MMA i - 2
+      if (i >= 2) bad |= !wait_or_flag(a.err, tc::smem_u32(&mdone[buf]), ((i - 2) >> 1) & 1);
       // C^T as three bf16 planes (row = landmark 4 ty + r, k = tokens 4 tx .. 4 tx + 3)
       uint8_t* ca = sm + S::Ca + buf * 3 * kPlaneC + (tx >> 1) * kLboC + (ty >> 1) * kSbo +
                     (ty & 1) * 64 + (tx & 1) * 8;
@@ -561,6 +583,12 @@ __global__ void __launch_bounds__(NTH, 1) k_key_tc(KArgs a) {
         for (int p = 0; p < 3; ++p)
           *reinterpret_cast<uint2*>(ca + p * kPlaneC + r * 16) = make_uint2(pl[p][0], pl[p][1]);
       }
+    }
+    if (b + 1 < b1) {
+      // block b + 1's V^T buffer was read by MMA i - 1
+      if (i >= 1) bad |= !wait_or_flag(a.err, tc::smem_u32(&mdone[buf ^ 1]), ((i - 1) >> 1) & 1);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");  // this thread's pieces of block b + 1
+      convert(buf ^ 1, buf ^ 1);
     }
     tc::fence_async_smem();
     tc::fence_before();
