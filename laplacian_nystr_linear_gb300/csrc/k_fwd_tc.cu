@@ -64,7 +64,11 @@ struct QSmem {
 // V exact and C as three bf16 planes c1 + c2 + c3 (24 significant bits): W
 // enters W-hat = X_T W, whose unconverged directions amplify a single rounding
 // of C (TF32: ~2e-4 in W) about a hundredfold.
-constexpr uint32_t kLboC = (QM / 8) * kSbo + 16;  // A (C^T planes): 8-token K groups, 2064 bytes apart
+// A (C^T planes): 8-landmark row groups 144 bytes apart, 8-token K groups 2304
+// bytes apart.  A warp's 8-byte plane stores (its 8 x 4 blocks of 4 landmarks x
+// 4 tokens) then fall on 16 distinct 8-byte bank slots, two lanes each.
+constexpr uint32_t kSboC = 144;
+constexpr uint32_t kLboC = (QM / 8) * kSboC;
 constexpr uint32_t kPlaneC = (TL / 8) * kLboC;
 template <int D>
 struct KSmem {
@@ -558,7 +562,7 @@ __global__ void __launch_bounds__(NTH, 1) k_key_tc(KArgs a) {
       // the C^T buffer of this block was read by MMA i - 2
       if (i >= 2) bad |= !wait_or_flag(a.err, tc::smem_u32(&mdone[buf]), ((i - 2) >> 1) & 1);
       // C^T as three bf16 planes (row = landmark 4 ty + r, k = tokens 4 tx .. 4 tx + 3)
-      uint8_t* ca = sm + S::Ca + buf * 3 * kPlaneC + (tx >> 1) * kLboC + (ty >> 1) * kSbo +
+      uint8_t* ca = sm + S::Ca + buf * 3 * kPlaneC + (tx >> 1) * kLboC + (ty >> 1) * kSboC +
                     (ty & 1) * 64 + (tx & 1) * 8;
 #pragma unroll
       for (int r = 0; r < 4; ++r) {
@@ -604,7 +608,7 @@ __global__ void __launch_bounds__(NTH, 1) k_key_tc(KArgs a) {
       for (int p = 0; p < 3; ++p)
 #pragma unroll
         for (int k16 = 0; k16 < TL / 16; ++k16)
-          tc::mma_bf16(tmem, tc::desc(ca + p * kPlaneC + k16 * 2 * kLboC, kLboC, kSbo),
+          tc::mma_bf16(tmem, tc::desc(ca + p * kPlaneC + k16 * 2 * kLboC, kLboC, kSboC),
                        tc::desc(vbs + k16 * 2 * S::kLboB, S::kLboB, kSboVB), id,
                        (i > 0 || p > 0 || k16 > 0) ? 1u : 0u);
       tc::commit(tc::smem_u32(&mdone[buf]));
