@@ -213,12 +213,10 @@ __global__ void __launch_bounds__(NTH, 1) k_query_tc(QArgs a) {
   prefetch_q(blockIdx.x);
   for (int item = blockIdx.x; item < a.items; item += gridDim.x) {
     const int bh = item / a.nb, j0 = (item % a.nb) * QM;
+    // this thread's pieces of the item's rows landed (each thread converts the
+    // pieces it copied); the previous item's distances ended before its last
+    // tile's barrier, so the query tile is free
     cp_wait_all();
-    // this item's rows landed; the previous item's distances are done
-    if (__syncthreads_or(bad)) {
-      abort = true;
-      break;
-    }
     {
       // raw rows -> feature-major f32 (lanes take consecutive queries)
       constexpr int CH = D / 8;
@@ -230,7 +228,10 @@ __global__ void __launch_bounds__(NTH, 1) k_query_tc(QArgs a) {
         for (int i = 0; i < 8; ++i) Xt[(8 * ch + i) * QM + j] = f[i];
       }
     }
-    __syncthreads();
+    if (__syncthreads_or(bad)) {
+      abort = true;
+      break;
+    }
     prefetch_q(item + gridDim.x);
 
     for (int t = 0; t < a.nt; ++t, ++g) {
