@@ -423,7 +423,8 @@ __global__ void __launch_bounds__(NTH, 1) k_key_tc(KArgs a) {
   const int b0 = (int)((long long)a.nblk * sp / a.S), b1 = (int)((long long)a.nblk * (sp + 1) / a.S);
   constexpr int CH = D / 8;
   constexpr int NV = (TL / 2) * CH;  // value tasks (a token pair, 8 features): threads 0 ..
-  constexpr int NK = TL * CH;        // key pieces (a token, 8 features): threads NTH / 2 .., in turn
+  constexpr int NK = TL * CH;        // key pieces (a token, 8 features): threads NTH / 2 .., two each
+  static_assert(NV <= NTH / 2 && NK / 2 <= NTH / 2, "one value task or key-piece pair per thread");
   // Raw key and value rows of block b into raw buffer rbuf (zero past N), one
   // commit group per block (empty past the range).  Each thread copies the
   // pieces it converts afterwards, so its own wait on its copies is all that
@@ -442,11 +443,13 @@ __global__ void __launch_bounds__(NTH, 1) k_key_tc(KArgs a) {
                        Vb + (size_t)(ok ? n0 + j + u : 0) * D + 8 * ch, ok);
           }
         }
-      } else {
-        for (int kp = tid - NTH / 2; kp < NK; kp += NTH / 2) {
-          const int j = kp % TL, ch = kp / TL;
-          const bool ok = n0 + j < a.N;
-          cp_async16(smem_addr(rb + j * S::kRow + 16 * ch), Kb + (size_t)(ok ? n0 + j : 0) * D + 8 * ch, ok);
+      } else if (tid - NTH / 2 < NK / 2) {
+        const int kp = tid - NTH / 2, j = 2 * (kp % (TL / 2)), ch = kp / (TL / 2);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const bool ok = n0 + j + u < a.N;
+          cp_async16(smem_addr(rb + (j + u) * S::kRow + 16 * ch),
+                     Kb + (size_t)(ok ? n0 + j + u : 0) * D + 8 * ch, ok);
         }
       }
     }
@@ -471,15 +474,15 @@ __global__ void __launch_bounds__(NTH, 1) k_key_tc(KArgs a) {
           *reinterpret_cast<uint32_t*>(dst + (2 * q + 1) * 16) = (w0[q] >> 16) | (w1[q] & 0xffff0000u);
         }
       }
-    } else {
-      float* kt = Kt + kb * D * TL;
-      for (int kp = tid - NTH / 2; kp < NK; kp += NTH / 2) {
-        const int j = kp % TL, ch = kp / TL;
-        float f[8];
-        bf16x8(*reinterpret_cast<const uint4*>(rb + j * S::kRow + 16 * ch), f);
+    } else if (tid - NTH / 2 < NK / 2) {
+      // a token pair: one 8-byte store per feature
+      const int kp = tid - NTH / 2, j = 2 * (kp % (TL / 2)), ch = kp / (TL / 2);
+      float f0[8], f1[8];
+      bf16x8(*reinterpret_cast<const uint4*>(rb + j * S::kRow + 16 * ch), f0);
+      bf16x8(*reinterpret_cast<const uint4*>(rb + (j + 1) * S::kRow + 16 * ch), f1);
+      float* kt = Kt + kb * D * TL + j;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) kt[(8 * ch + q) * TL + j] = f[q];
-      }
+      for (int q = 0; q < 8; ++q) *reinterpret_cast<float2*>(kt + (8 * ch + q) * TL) = make_float2(f0[q], f1[q]);
     }
   };
   // One barrier a block: block b + 1's operands are converted at the end of
@@ -570,19 +573,16 @@ __global__ void __launch_bounds__(NTH, 1) k_key_tc(KArgs a) {
         uint32_t pl[3][2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          uint32_t b[3][2];
+          // two tokens at a time: one packed rounding per plane, the remainders exact
+          float v0 = cv[r][2 * h], v1 = cv[r][2 * h + 1];
 #pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            float v = cv[r][2 * h + t];
-#pragma unroll
-            for (int p = 0; p < 3; ++p) {
-              const __nv_bfloat16 hb = __float2bfloat16_rn(v);
-              b[p][t] = *reinterpret_cast<const uint16_t*>(&hb);
-              v -= __bfloat162float(hb);
-            }
+          for (int p = 0; p < 3; ++p) {
+            const __nv_bfloat162 hb = __floats2bfloat162_rn(v0, v1);
+            const uint32_t u = *reinterpret_cast<const uint32_t*>(&hb);
+            pl[p][h] = u;
+            v0 -= __uint_as_float(u << 16);
+            v1 -= __uint_as_float(u & 0xffff0000u);
           }
-#pragma unroll
-          for (int p = 0; p < 3; ++p) pl[p][h] = b[p][0] | (b[p][1] << 16);
         }
 #pragma unroll
         for (int p = 0; p < 3; ++p)
