@@ -40,6 +40,21 @@ __device__ __forceinline__ void st4(__nv_bfloat16* p, float4 v) {
 
 __device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
+// Two fp32 values as three bf16 planes each, v = p0 + p1 + p2 (+ a remainder
+// below 2^-24 |v|): plane p is the bf16 rounding (nearest, ties to even) of what
+// the earlier planes leave, the subtractions exact.  Word w[p] packs plane p of
+// v0 (low half) and v1 (high half); one packed conversion per plane.
+__device__ __forceinline__ void split3_bf16x2(float v0, float v1, uint32_t (&w)[3]) {
+#pragma unroll
+  for (int p = 0; p < 3; ++p) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
+    const uint32_t u = *reinterpret_cast<const uint32_t*>(&h);
+    w[p] = u;
+    v0 -= __uint_as_float(u << 16);
+    v1 -= __uint_as_float(u & 0xffff0000u);
+  }
+}
+
 // Packed pairs of fp32 values (one 64-bit register, .x in the low half) and the
 // paired FMA of the sm_100-family FP32 pipe: one issue slot for two lanes'
 // worth of FMAs.

@@ -392,15 +392,10 @@ __global__ void __launch_bounds__(NTH, 1) k_bwd_tc(BtcArgs a) {
         uint32_t w[3][TPT / 2];
 #pragma unroll
         for (int t = 0; t < TPT; t += 2) {
-          const uint16_t a0 = bf16_bits(z[t]), a1 = bf16_bits(z[t + 1]);
-          const float r0 = z[t] - __uint_as_float((uint32_t)a0 << 16);
-          const float r1 = z[t + 1] - __uint_as_float((uint32_t)a1 << 16);
-          const uint16_t b0h = bf16_bits(r0), b1h = bf16_bits(r1);
-          const uint16_t c0 = bf16_bits(r0 - __uint_as_float((uint32_t)b0h << 16));
-          const uint16_t c1 = bf16_bits(r1 - __uint_as_float((uint32_t)b1h << 16));
-          w[0][t / 2] = (uint32_t)a0 | ((uint32_t)a1 << 16);
-          w[1][t / 2] = (uint32_t)b0h | ((uint32_t)b1h << 16);
-          w[2][t / 2] = (uint32_t)c0 | ((uint32_t)c1 << 16);
+          uint32_t u[3];
+          split3_bf16x2(z[t], z[t + 1], u);
+#pragma unroll
+          for (int p = 0; p < 3; ++p) w[p][t / 2] = u[p];
         }
         const uint32_t off = (tok0 >> 3) * LBO_Z + (r >> 3) * SBO + (r & 7) * 16 + (tok0 & 7) * 2;
 #pragma unroll

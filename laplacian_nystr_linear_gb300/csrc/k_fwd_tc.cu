@@ -573,16 +573,10 @@ __global__ void __launch_bounds__(NTH, 1) k_key_tc(KArgs a) {
         uint32_t pl[3][2];
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          // two tokens at a time: one packed rounding per plane, the remainders exact
-          float v0 = cv[r][2 * h], v1 = cv[r][2 * h + 1];
+          uint32_t w[3];  // two tokens at a time
+          split3_bf16x2(cv[r][2 * h], cv[r][2 * h + 1], w);
 #pragma unroll
-          for (int p = 0; p < 3; ++p) {
-            const __nv_bfloat162 hb = __floats2bfloat162_rn(v0, v1);
-            const uint32_t u = *reinterpret_cast<const uint32_t*>(&hb);
-            pl[p][h] = u;
-            v0 -= __uint_as_float(u << 16);
-            v1 -= __uint_as_float(u & 0xffff0000u);
-          }
+          for (int p = 0; p < 3; ++p) pl[p][h] = w[p];
         }
 #pragma unroll
         for (int p = 0; p < 3; ++p)

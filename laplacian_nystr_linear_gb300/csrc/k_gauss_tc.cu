@@ -553,19 +553,10 @@ __global__ void __launch_bounds__(NTH, 1) k_key_gtc(GKArgs a) {
       uint32_t pl[3][8];
 #pragma unroll
       for (int q = 0; q < 16; q += 2) {
-        uint32_t b[3][2];
+        uint32_t w[3];
+        split3_bf16x2(c[q], c[q + 1], w);
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          float v = c[q + t];
-#pragma unroll
-          for (int p = 0; p < 3; ++p) {
-            const __nv_bfloat16 hb = __float2bfloat16_rn(v);
-            b[p][t] = *reinterpret_cast<const uint16_t*>(&hb);
-            v -= __bfloat162float(hb);
-          }
-        }
-#pragma unroll
-        for (int p = 0; p < 3; ++p) pl[p][q / 2] = b[p][0] | (b[p][1] << 16);
+        for (int p = 0; p < 3; ++p) pl[p][q / 2] = w[p];
       }
 #pragma unroll
       for (int p = 0; p < 3; ++p)
