@@ -40,6 +40,17 @@ __device__ __forceinline__ void st4(__nv_bfloat16* p, float4 v) {
 
 __device__ __forceinline__ float4 lds4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
+// 2^x for the kernel values: the PTX base-2 exponential (ex2.approx) with
+// results below 2^-126 flushed to zero (a kernel value that small is taken as
+// 0, an absolute difference under 1.2e-38).  Fewer instructions than exp2f,
+// which also returns the subnormal results; on the hires16k inputs every kernel
+// value came out bit-identical to exp2f's.
+__device__ __forceinline__ float exp2_ftz(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Two fp32 values as three bf16 planes each, v = p0 + p1 + p2 (+ a remainder
 // below 2^-24 |v|): plane p is the bf16 rounding (nearest, ties to even) of what
 // the earlier planes leave, the subtractions exact.  Word w[p] packs plane p of

@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(NTH, 1) k_query_tc(QArgs a) {
 #pragma unroll
           for (int s = 0; s < 4; ++s) {
             const bool ok = ab + s < a.m;
-            pv[s] = ok ? exp2f(acc[r][s] * a.ns) : 0.f;
+            pv[s] = ok ? exp2_ftz(acc[r][s] * a.ns) : 0.f;
             z[s] = NORM ? (ok ? (pv[s] - mu[s]) * rs[s] : 0.f) : pv[s];
           }
           // keep the kernel value (before normalisation) for the backward
@@ -551,7 +551,7 @@ __global__ void __launch_bounds__(NTH, 1) k_key_tc(KArgs a) {
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
           const bool ok = (a0 + 4 * ty + r < a.m) && (n0 + 4 * tx + s < a.N);
-          cv[r][s] = ok ? exp2f(acc[r][s] * a.ns) : 0.f;
+          cv[r][s] = ok ? exp2_ftz(acc[r][s] * a.ns) : 0.f;
         }
       if (a.kvout != nullptr && a0 + 4 * ty < a.mp) {
         // kept for the backward (token-major rows), stored during the next

@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(NTH, 1) k_query_gtc(GQArgs a) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const float dist = fmaxf(fmaf(-2.f, __uint_as_float(v[i]), xn + ln[al0 + i]), 0.f);
-          p[i] = ab + i < a.m ? exp2f(dist * a.ns) : 0.f;
+          p[i] = ab + i < a.m ? exp2_ftz(dist * a.ns) : 0.f;
         }
         if (a.kvout != nullptr && j < a.N) {
           float* o = a.kvout + ((size_t)bh * a.N + j) * a.mp + ab;
@@ -537,7 +537,7 @@ __global__ void __launch_bounds__(NTH, 1) k_key_gtc(GKArgs a) {
 #pragma unroll
       for (int q = 0; q < 16; ++q) {
         const float dist = fmaxf(fmaf(-2.f, __uint_as_float(v[q]), lnv + kn[jl0 + q]), 0.f);
-        c[q] = (aa < a.m && n0 + jl0 + q < a.N) ? exp2f(dist * a.ns) : 0.f;
+        c[q] = (aa < a.m && n0 + jl0 + q < a.N) ? exp2_ftz(dist * a.ns) : 0.f;
       }
       if (a.kvout != nullptr && aa < a.mp) {
         // keep the kernel values for the backward: lanes write consecutive landmarks of a key row

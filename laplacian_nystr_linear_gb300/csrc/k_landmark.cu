@@ -402,7 +402,7 @@ __global__ void __launch_bounds__(kNsThreads) k_ns_small(const float* __restrict
       for (int q = 0; q < 4; ++q) {
         const int i = 4 * ty + r, j = tx + 16 * q;
         float v = 0.f;
-        if (i < m && j < m) v = exp2f(dist[r][q] * ns) + (i == j ? eps : 0.f);
+        if (i < m && j < m) v = exp2_ftz(dist[r][q] * ns) + (i == j ? eps : 0.f);
         As[i * kMS + j] = v;
       }
   }
@@ -505,7 +505,7 @@ __global__ void __launch_bounds__(kThreads) k_gram(const float* __restrict__ L, 
     for (int s = 0; s < 4; ++s) {
       const int i = it * 64 + 4 * ty + r, j = jt * 64 + tx + 16 * s;
       if (i < m && j < m)
-        A[((size_t)bh * m + i) * m + j] = exp2f(dist[r][s] * ns) + (i == j ? eps : 0.f);
+        A[((size_t)bh * m + i) * m + j] = exp2_ftz(dist[r][s] * ns) + (i == j ? eps : 0.f);
     }
 }
 

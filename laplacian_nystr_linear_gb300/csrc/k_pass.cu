@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
         const int j = b * kTile + 4 * ty + r, a = a0 + tx + 16 * s;
-        Cs[(4 * ty + r) * 68 + tx + 16 * s] = (j < N && a < m) ? exp2f(dist[r][s] * ns) : 0.f;
+        Cs[(4 * ty + r) * 68 + tx + 16 * s] = (j < N && a < m) ? exp2_ftz(dist[r][s] * ns) : 0.f;
       }
     __syncthreads();
     if (kvout) {
@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
     for (int r = 0; r < 4; ++r)
 #pragma unroll
-      for (int s = 0; s < 4; ++s) Ps[(4 * ty + r) * 68 + tx + 16 * s] = exp2f(dist[r][s] * ns);
+      for (int s = 0; s < 4; ++s) Ps[(4 * ty + r) * 68 + tx + 16 * s] = exp2_ftz(dist[r][s] * ns);
     __syncthreads();
     if (threadIdx.x < kTile) {
       const int nb = min(kTile, N - b * kTile);
@@ -550,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int s = 0; s < 4; ++s) {
         const int a = tx + 16 * s;
         float pv = 0.f;
-        if (a0 + a < m) pv = exp2f(dist[r][s] * ns);
+        if (a0 + a < m) pv = exp2_ftz(dist[r][s] * ns);
         // keep the kernel value (before normalisation) for the backward
         const int j = b * kTile + 4 * ty + r;
         if (kvout && j < N) kvout[((size_t)bh * N + j) * (nt * kTile) + a0 + a] = pv;
@@ -767,7 +767,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int s = 0; s < 4; ++s) {
         const int jl = 4 * ty + r, al = tx + 16 * s;
         const bool valid = (b * kTile + jl < N) && (a0 + al < m);
-        const float kv = exp2f(dist[r][s] * ns);
+        const float kv = exp2_ftz(dist[r][s] * ns);
         float g = 0.f, zc = 0.f;
         if (MODE == 2) {
           g = dot[r][s] * kv * inv_lam;
