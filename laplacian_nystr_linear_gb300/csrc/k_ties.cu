@@ -215,10 +215,10 @@ __global__ void __launch_bounds__(kThreads, 4) k_ties(const T* __restrict__ X,
       }
       if (bad_x) atomicOr(&oor[k >> 5], 1u << (k & 31));
     };
-    // four pieces in flight per thread (the thread's columns stay c0 ..)
+    // four pieces a round per thread (the thread's columns stay c0 ..), the
+    // next round's loads issued before this round is scanned
     constexpr int kIn = 4;
-    for (int e0 = tid; e0 < total; e0 += kIn * kThreads) {
-      uint4 u[kIn];
+    auto load = [&](int e0, uint4 (&u)[kIn]) {
 #pragma unroll
       for (int i = 0; i < kIn; ++i) {
         const int e = e0 + i * kThreads;
@@ -227,9 +227,16 @@ __global__ void __launch_bounds__(kThreads, 4) k_ties(const T* __restrict__ X,
           u[i] = __ldg(reinterpret_cast<const uint4*>(Xb + (size_t)n * D + c0));
         }
       }
+    };
+    uint4 u[kIn], un[kIn];
+    load(tid, u);
+    for (int e0 = tid; e0 < total; e0 += kIn * kThreads) {
+      load(e0 + kIn * kThreads, un);
 #pragma unroll
       for (int i = 0; i < kIn; ++i)
         if (e0 + i * kThreads < total) scan(e0 + i * kThreads, u[i]);
+#pragma unroll
+      for (int i = 0; i < kIn; ++i) u[i] = un[i];
     }
   }
   __syncthreads();
